@@ -1,0 +1,314 @@
+"""CPU oracle for the binarized linear / conv2d forward.
+
+TEST INFRASTRUCTURE ONLY. Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The library under
+``xnor_popcount_gemm_gb300`` never imports it, and this package imports
+nothing from there: the two share no code.
+
+The nested loops live in ``bt_oracle.c`` (plain C, compiled here with gcc);
+this module binarizes and contracts through them and does the epilogue with
+plain numpy / PyTorch CPU ops. Every function cites the passage it follows:
+
+* bitorch-engine ``BinaryConv2dCutlass.set_activation``: the activation shift
+  ``x + bias_a`` before binarizing ("learnable shift input").
+* bitorch-engine ``BinaryConv2dForward.forward``: the native forward is given
+  ``scale_a.item() * scale_w.item()`` and its result is cast back with
+  ``out.to(x.dtype)``.
+* bitorch-engine ``BinaryLinearForward.forward``: "the result of the binary
+  linear operation scaled by the activation and weight scaling factors".
+* banghao.live/blog/9, section 2 (``MyConv2d.forward``): the output-size
+  formula and the unfold + mm lowering of a convolution.
+* torch/ao/quantization/experimental/linear.py, ``LinearAPoT.matmul``: the
+  plain i-j-k triple loop of a matrix product.
+
+Readings where the pages leave a step open (each also listed in the design
+notes of the repository):
+
+1. The binarization threshold: ``x + bias >= 0`` gives +1, anything else
+   (negative, NaN) gives -1; -0.0 gives +1. Weights are binarized with the
+   same rule and no shift. The sum is taken in double, so its sign is the
+   sign of the exact sum.
+2. A positive ``scale_a`` does not change a sign, so the division by
+   ``scale_a`` of "integrated scaling and value range conversion" is not
+   applied before the threshold.
+3. The native call receives one float ``alpha = fp32(scale_a * scale_w)``
+   (the double product of two floats, rounded once to float); the native
+   result is ``fp32(dot * alpha)`` (one rounding) and ``.to(x.dtype)`` then
+   rounds to nearest-even.
+4. A convolution tap in the zero padding contributes 0 to the dot product,
+   as in the unfold + mm lowering.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bt_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``bt_oracle.c`` into ``_build/liboracle.so`` (gcc, OpenMP)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if fresh and not force:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.orc_binarize.argtypes = [p, i64, p, i64, i64, p]
+        lib.orc_linear_dot.argtypes = [p, p, i64, i64, i64, p]
+        lib.orc_linear_dot_at.argtypes = [p, p, i64, p, p, i64, p]
+        lib.orc_conv2d_dot.argtypes = [p, p] + [i64] * 9 + [p]
+        lib.orc_conv2d_dot_at.argtypes = [p, p] + [i64] * 9 + [p, i64, p]
+        lib.orc_conv2d_out_size.argtypes = [i64] * 5
+        lib.orc_conv2d_out_size.restype = i64
+        for f in ("orc_binarize", "orc_linear_dot", "orc_linear_dot_at", "orc_conv2d_dot",
+                  "orc_conv2d_dot_at"):
+            getattr(lib, f).restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _as_f32(x) -> np.ndarray:
+    """Exact conversion of an fp32 / bf16 / fp16 tensor or array to fp32 numpy."""
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu()
+        if x.dtype not in (torch.float32, torch.bfloat16, torch.float16):
+            raise TypeError(f"unsupported dtype {x.dtype}")
+        return np.ascontiguousarray(x.to(torch.float32).numpy())
+    x = np.asarray(x)
+    if x.dtype not in (np.float32, np.float16):
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    return np.ascontiguousarray(x.astype(np.float32))
+
+
+# ----------------------------------------------------------------------------
+# Binarization (set_activation's shift, then the sign threshold)
+# ----------------------------------------------------------------------------
+
+def binarize(x, bias=None, channel_axis: int | None = None) -> np.ndarray:
+    """+1/-1 int8 array: ``+1`` where ``x + bias >= 0`` (sum in double), else -1.
+
+    ``bias`` is None (no shift), a scalar, or a 1-D array along
+    ``channel_axis`` (the per-channel ``bias_a.view(1,-1,1,1)`` of
+    ``BinaryConv2dCutlass.set_activation`` uses ``channel_axis=1``; the
+    layer-wise bias of ``BinaryLinearCuda`` is a scalar).
+    """
+    xf = _as_f32(x)
+    out = np.empty(xf.shape, dtype=np.int8)
+    if bias is None:
+        b = np.zeros(1, np.float32)
+        blen, inner = 0, 1
+    else:
+        b = np.ascontiguousarray(_as_f32(bias).reshape(-1))
+        if b.size == 1:
+            blen, inner = 1, 1
+        else:
+            if channel_axis is None:
+                raise ValueError("a vector bias needs channel_axis")
+            ax = channel_axis % xf.ndim
+            if xf.shape[ax] != b.size:
+                raise ValueError("bias length does not match the channel axis")
+            blen = b.size
+            inner = int(np.prod(xf.shape[ax + 1:], dtype=np.int64))
+    _load().orc_binarize(_ptr(xf), xf.size, _ptr(b), blen, inner, _ptr(out))
+    return out
+
+
+def binarize_weight(w) -> np.ndarray:
+    """Weights: +1 where ``w >= 0``, else -1 (no shift)."""
+    return binarize(w)
+
+
+# ----------------------------------------------------------------------------
+# Contractions (nested loops in C)
+# ----------------------------------------------------------------------------
+
+def linear_dot(sa: np.ndarray, sw: np.ndarray) -> np.ndarray:
+    """``dot[m,n] = sum_k sa[m,k] sw[n,k]`` as int32 (the i-j-k loop)."""
+    sa = np.ascontiguousarray(sa, dtype=np.int8)
+    sw = np.ascontiguousarray(sw, dtype=np.int8)
+    M, K = sa.shape
+    N, K2 = sw.shape
+    if K != K2:
+        raise ValueError("K mismatch")
+    dot = np.empty((M, N), dtype=np.int32)
+    _load().orc_linear_dot(_ptr(sa), _ptr(sw), M, N, K, _ptr(dot))
+    return dot
+
+
+def linear_dot_at(sa: np.ndarray, sw: np.ndarray, rows, cols) -> np.ndarray:
+    """The same sums for the listed (row, col) pairs only."""
+    sa = np.ascontiguousarray(sa, dtype=np.int8)
+    sw = np.ascontiguousarray(sw, dtype=np.int8)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if sa.shape[1] != sw.shape[1] or rows.shape != cols.shape:
+        raise ValueError("shape mismatch")
+    out = np.empty(rows.shape, dtype=np.int32)
+    _load().orc_linear_dot_at(_ptr(sa), _ptr(sw), sa.shape[1], _ptr(rows), _ptr(cols),
+                              rows.size, _ptr(out))
+    return out
+
+
+def conv2d_out_size(h: int, k: int, s: int, p: int, d: int) -> int:
+    """``floor((h + 2p - d(k-1) - 1)/s + 1)`` (banghao.live/blog/9, section 2);
+    0 when the window does not fit."""
+    return int(_load().orc_conv2d_out_size(h, k, s, p, d))
+
+
+def conv2d_dot(sa: np.ndarray, sw: np.ndarray, stride: int, padding: int, dilation: int) -> np.ndarray:
+    """Direct 7-loop convolution of +1/-1 NCHW ``sa`` with OIHW ``sw``; padded taps add 0."""
+    sa = np.ascontiguousarray(sa, dtype=np.int8)
+    sw = np.ascontiguousarray(sw, dtype=np.int8)
+    B, C, H, W = sa.shape
+    O, C2, k, k2 = sw.shape
+    if C != C2 or k != k2:
+        raise ValueError("shape mismatch")
+    Ho = conv2d_out_size(H, k, stride, padding, dilation)
+    Wo = conv2d_out_size(W, k, stride, padding, dilation)
+    dot = np.empty((B, O, Ho, Wo), dtype=np.int32)
+    if dot.size:
+        _load().orc_conv2d_dot(_ptr(sa), _ptr(sw), B, C, H, W, O, k, stride, padding, dilation,
+                               _ptr(dot))
+    return dot
+
+
+def conv2d_dot_at(sa: np.ndarray, sw: np.ndarray, stride: int, padding: int, dilation: int,
+                  flat_index) -> np.ndarray:
+    """The same sums at the listed flat indices of the NCHW output only."""
+    sa = np.ascontiguousarray(sa, dtype=np.int8)
+    sw = np.ascontiguousarray(sw, dtype=np.int8)
+    B, C, H, W = sa.shape
+    O, _, k, _ = sw.shape
+    idx = np.ascontiguousarray(flat_index, dtype=np.int64)
+    out = np.empty(idx.shape, dtype=np.int32)
+    _load().orc_conv2d_dot_at(_ptr(sa), _ptr(sw), B, C, H, W, O, k, stride, padding, dilation,
+                              _ptr(idx), idx.size, _ptr(out))
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Epilogue: alpha = scale_a * scale_w, fp32 result, cast to the output dtype
+# ----------------------------------------------------------------------------
+
+_TORCH_OUT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "i32": torch.int32}
+
+
+def alpha(scale_a: float, scale_w: float) -> np.float32:
+    """``fp32(scale_a * scale_w)``: the double product of the two float scales
+    (``scale_a.item()*scale_w.item()``) rounded once to float."""
+    a = np.float64(np.float32(scale_a))
+    w = np.float64(np.float32(scale_w))
+    return np.float32(a * w)
+
+
+def epilogue(dot: np.ndarray, scale_a: float, scale_w: float, out_dtype: str) -> torch.Tensor:
+    """``fp32(dot * alpha)`` (exact product in double, one rounding to float),
+    then ``.to(out_dtype)`` (round to nearest even). ``i32`` returns ``dot``."""
+    dot = np.asarray(dot, dtype=np.int32)
+    if out_dtype == "i32":
+        return torch.from_numpy(dot.copy())
+    al = np.float64(alpha(scale_a, scale_w))
+    y64 = dot.astype(np.float64) * al          # exact: 24-bit integer times 24-bit float
+    y32 = torch.from_numpy(y64.astype(np.float32))
+    return y32.to(_TORCH_OUT[out_dtype])
+
+
+def binary_linear(x, w, scale_a: float, scale_w: float, bias_a=None, out_dtype: str = "f32"):
+    """Whole linear forward: shift + sign, sign of W, contraction, epilogue."""
+    sa = binarize(x, bias_a, channel_axis=-1)
+    sw = binarize_weight(w)
+    return epilogue(linear_dot(sa, sw), scale_a, scale_w, out_dtype)
+
+
+def binary_conv2d(x, w, scale_a: float, scale_w: float, stride: int, padding: int, dilation: int,
+                  bias_a=None, out_dtype: str = "f32"):
+    """Whole conv2d forward (NCHW in, OIHW weights, NCHW out)."""
+    sa = binarize(x, bias_a, channel_axis=1)
+    sw = binarize_weight(w)
+    return epilogue(conv2d_dot(sa, sw, stride, padding, dilation), scale_a, scale_w, out_dtype)
+
+
+# ----------------------------------------------------------------------------
+# The packed operand formats the library documents, written out plainly so the
+# packing kernels can be checked bit for bit.
+# ----------------------------------------------------------------------------
+
+CODE_BITS, CODE_E4M3, CODE_E2M1 = 0, 1, 2
+
+
+def packed_row_bytes(k: int, code: int) -> int:
+    """Bytes per packed row of ``k`` elements: rounded up to 16 bytes."""
+    if code == CODE_BITS:
+        nbytes = ((k + 31) // 32) * 4
+    elif code == CODE_E4M3:
+        nbytes = k
+    elif code == CODE_E2M1:
+        nbytes = (k + 1) // 2
+    else:
+        raise ValueError(code)
+    return (nbytes + 15) // 16 * 16
+
+
+def pack_rows(s: np.ndarray, code: int) -> np.ndarray:
+    """Pack the last axis of a +1/-1 array into the documented format.
+
+    BITS: uint32 words, bit j of word w holds element 32w + j, 1 for +1.
+    E4M3: one byte per element, 0x38 (+1.0) or 0xB8 (-1.0).
+    E2M1: two elements per byte, element 2i in the low nibble; 0x2 (+1.0) or
+    0xA (-1.0). Every position past the last element, up to the padded row
+    length, is 0. Returns uint8 [..., packed_row_bytes].
+    """
+    s = np.asarray(s, dtype=np.int8)
+    lead, k = s.shape[:-1], s.shape[-1]
+    rows = s.reshape(-1, k)
+    nb = packed_row_bytes(k, code)
+    out = np.zeros((rows.shape[0], nb), dtype=np.uint8)
+    if code == CODE_BITS:
+        words = out.view(np.uint32)
+        for kk in range(k):
+            bit = (rows[:, kk] > 0).astype(np.uint32) << np.uint32(kk % 32)
+            words[:, kk // 32] |= bit
+    elif code == CODE_E4M3:
+        out[:, :k] = np.where(rows > 0, 0x38, 0xB8).astype(np.uint8)
+    else:
+        nib = np.where(rows > 0, 0x2, 0xA).astype(np.uint8)
+        for kk in range(k):
+            shift = 4 * (kk % 2)
+            out[:, kk // 2] |= (nib[:, kk] << shift).astype(np.uint8)
+    return out.reshape(*lead, nb)
+
+
+def pack_nchw_to_nhwc(s: np.ndarray, code: int) -> np.ndarray:
+    """Channel-packed NHWC: [B,C,H,W] +1/-1 -> uint8 [B,H,W,packed_row_bytes(C)].
+
+    Also the conv weight format: OIHW [O,C,k,k] -> [O,k,k,packed_row_bytes(C)].
+    """
+    s = np.asarray(s, dtype=np.int8)
+    return pack_rows(np.ascontiguousarray(np.transpose(s, (0, 2, 3, 1))), code)

@@ -1,0 +1,404 @@
+"""Pins for the CPU oracle, checked against things other than itself.
+
+Each pin comes from the pages or from mathematics: hand-worked examples
+(tests/golden/hand_examples.json), brute force with Python integers on tiny
+inputs, the invariants of a +1/-1 dot product (|dot| <= K, dot = K (mod 2),
+dot = K - 2*hamming), torch's own conv2d and the unfold + mm lowering of
+banghao.live/blog/9 section 2, the output-size formula of that section, and
+exact IEEE rounding cases worked out by hand. The last tests plant plausible
+mistakes in copies of the oracle's arithmetic and check that these pins
+catch them.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")
+
+
+def _rand_pm1(rng, shape):
+    return np.where(rng.random(shape) < 0.5, 1, -1).astype(np.int8)
+
+
+# ---------------------------------------------------------------------------
+# Hand-worked examples
+# ---------------------------------------------------------------------------
+
+def test_golden_linear():
+    for ex in json.load(open(GOLDEN))["linear"]:
+        x = torch.tensor(ex["x"], dtype=torch.float32)
+        w = torch.tensor(ex["w"], dtype=torch.float32)
+        bias = torch.tensor(ex["bias"]) if "bias" in ex else None
+        sa = oracle.binarize(x, bias, channel_axis=-1)
+        sw = oracle.binarize_weight(w)
+        np.testing.assert_array_equal(oracle.linear_dot(sa, sw), np.array(ex["dot"]), ex["why"])
+
+
+def test_golden_conv():
+    for ex in json.load(open(GOLDEN))["conv"]:
+        sa = oracle.binarize(torch.tensor(ex["x"]))
+        sw = oracle.binarize_weight(torch.tensor(ex["w"]))
+        got = oracle.conv2d_dot(sa, sw, ex["stride"], ex["padding"], ex["dilation"])
+        np.testing.assert_array_equal(got, np.array(ex["dot"]), ex["why"])
+
+
+def test_golden_pack():
+    g = json.load(open(GOLDEN))
+    for ex in g["pack_bits"]:
+        if "signs" in ex:
+            s = np.array([ex["signs"]], np.int8)
+        elif "signs_all_plus" in ex:
+            s = np.ones((1, ex["signs_all_plus"]), np.int8)
+        else:
+            s = np.array([[-1] * ex["signs_neg_then_plus"] + [1]], np.int8)
+        words = oracle.pack_rows(s, oracle.CODE_BITS).view(np.uint32)[0]
+        np.testing.assert_array_equal(words, np.array(ex["words"], np.uint32), ex["why"])
+    for ex in g["pack_codes"]:
+        code = {"e4m3": oracle.CODE_E4M3, "e2m1": oracle.CODE_E2M1}[ex["code"]]
+        got = oracle.pack_rows(np.array([ex["signs"]], np.int8), code)[0]
+        n = len(ex["bytes"])
+        assert got.size == 16
+        np.testing.assert_array_equal(got[:n], np.array(ex["bytes"], np.uint8), ex["why"])
+        assert not got[n:].any()
+
+
+def test_code_values_decode_to_plus_minus_one():
+    # E4M3 through torch's own float8 type.
+    b = torch.tensor([0x38, 0xB8, 0x00], dtype=torch.uint8)
+    np.testing.assert_array_equal(b.view(torch.float8_e4m3fn).float().numpy(), [1.0, -1.0, 0.0])
+
+    # E2M1 by its definition: sign bit 3, exponent bits 2..1 with bias 1, mantissa bit 0.
+    def e2m1(n):
+        sign = -1.0 if n & 0x8 else 1.0
+        e, m = (n >> 1) & 0x3, n & 0x1
+        return sign * (m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1 + 0.5 * m))
+
+    assert (e2m1(0x2), e2m1(0xA), e2m1(0x0)) == (1.0, -1.0, 0.0)
+
+
+# ---------------------------------------------------------------------------
+# Binarization rule
+# ---------------------------------------------------------------------------
+
+def test_binarize_special_values():
+    tiny = np.float32(1e-45)          # smallest positive subnormal
+    cases = [
+        (0.0, None, 1), (-0.0, None, 1), (tiny, None, 1), (-tiny, None, -1),
+        (np.nan, None, -1), (np.inf, None, 1), (-np.inf, None, -1),
+        (0.5, -0.5, 1),                                   # x == -bias exactly: sum is 0
+        (0.5, -np.nextafter(np.float32(0.5), np.float32(1)), -1),  # sum is -2^-24
+        (-1e-40, 0.0, -1), (1e-40, -1e-40, 1),            # subnormals, no flush to zero
+        (3.0, -np.inf, -1), (np.inf, -np.inf, -1),        # inf - inf is NaN -> -1
+        (1.0e30, -1.0e30, 1), (-3.0, 2.5, -1),
+    ]
+    for x, b, want in cases:
+        bias = None if b is None else np.array([b], np.float32)
+        got = oracle.binarize(np.array([x], np.float32), bias)[0]
+        assert got == want, (x, b)
+
+
+def test_binarize_bf16_and_f16_inputs_are_exact():
+    v = torch.tensor([-1.0e-38, 1.0e-38, -0.0, 3.5, -3.5])
+    for dt in (torch.bfloat16, torch.float16):
+        got = oracle.binarize(v.to(dt))
+        want = [(-1 if float(t) < 0 else 1) for t in v.to(dt).float()]
+        np.testing.assert_array_equal(got, want)
+
+
+def test_binarize_per_channel_bias_uses_channel_axis():
+    x = torch.zeros(2, 3, 2, 2)
+    bias = torch.tensor([-1.0, 0.0, 1.0])
+    s = oracle.binarize(x, bias, channel_axis=1)
+    assert (s[:, 0] == -1).all() and (s[:, 1] == 1).all() and (s[:, 2] == 1).all()
+    x2 = torch.full((2, 3), 0.5)
+    s2 = oracle.binarize(x2, torch.tensor([-1.0, -0.5, 0.0]), channel_axis=-1)
+    np.testing.assert_array_equal(s2, [[-1, 1, 1], [-1, 1, 1]])
+
+
+# ---------------------------------------------------------------------------
+# Linear: brute force, invariants, special cases
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("K", [1, 31, 32, 33, 63, 64, 65, 127, 4100])
+def test_linear_brute_force(K):
+    rng = np.random.default_rng(K)
+    M, N = (3, 4) if K > 1000 else (5, 7)
+    sa, sw = _rand_pm1(rng, (M, K)), _rand_pm1(rng, (N, K))
+    got = oracle.linear_dot(sa, sw)
+    a, w = sa.tolist(), sw.tolist()
+    for m in range(M):
+        for n in range(N):
+            assert got[m, n] == sum(a[m][k] * w[n][k] for k in range(K))
+
+
+@pytest.mark.parametrize("K", [7, 64, 300, 1031])
+def test_linear_invariants(K):
+    rng = np.random.default_rng(100 + K)
+    sa, sw = _rand_pm1(rng, (9, K)), _rand_pm1(rng, (11, K))
+    dot = oracle.linear_dot(sa, sw).astype(np.int64)
+    ham = np.array([[np.count_nonzero((sa[m] > 0) != (sw[n] > 0)) for n in range(11)]
+                    for m in range(9)])
+    np.testing.assert_array_equal(dot, K - 2 * ham)
+    assert (np.abs(dot) <= K).all()
+    assert ((dot - K) % 2 == 0).all()
+
+
+def test_linear_special_cases():
+    rng = np.random.default_rng(7)
+    K = 257
+    w = _rand_pm1(rng, (6, K))
+    np.testing.assert_array_equal(np.diag(oracle.linear_dot(w, w)), [K] * 6)
+    np.testing.assert_array_equal(np.diag(oracle.linear_dot(-w, w)), [-K] * 6)
+    ones = np.ones((1, K), np.int8)
+    np.testing.assert_array_equal(oracle.linear_dot(ones, w)[0], w.astype(np.int64).sum(1))
+
+
+def test_linear_matches_float64_matmul_of_signs():
+    rng = np.random.default_rng(3)
+    x = torch.from_numpy(rng.standard_normal((33, 517)).astype(np.float32))
+    w = torch.from_numpy(rng.standard_normal((19, 517)).astype(np.float32))
+    sx = torch.where(x >= 0, 1.0, -1.0).double()
+    sw = torch.where(w >= 0, 1.0, -1.0).double()
+    want = (sx @ sw.T).numpy()
+    got = oracle.linear_dot(oracle.binarize(x), oracle.binarize_weight(w))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_linear_dot_at_agrees_with_full():
+    rng = np.random.default_rng(11)
+    sa, sw = _rand_pm1(rng, (40, 77)), _rand_pm1(rng, (30, 77))
+    full = oracle.linear_dot(sa, sw)
+    rows, cols = rng.integers(0, 40, 50), rng.integers(0, 30, 50)
+    np.testing.assert_array_equal(oracle.linear_dot_at(sa, sw, rows, cols), full[rows, cols])
+
+
+# ---------------------------------------------------------------------------
+# Conv: output size, torch conv2d, unfold + mm, brute force, invariants
+# ---------------------------------------------------------------------------
+
+CONV_GRID = [
+    # (B, C, H, W, O, k, s, p, d)
+    (1, 1, 5, 5, 1, 3, 1, 1, 1), (2, 3, 7, 6, 4, 3, 2, 1, 1), (1, 31, 6, 6, 3, 1, 1, 0, 1),
+    (2, 33, 5, 7, 2, 3, 1, 2, 2), (1, 64, 9, 9, 5, 5, 3, 3, 1), (1, 4, 1, 1, 2, 3, 1, 1, 1),
+    (1, 2, 8, 8, 3, 3, 2, 2, 2), (3, 5, 4, 9, 2, 5, 1, 2, 1), (1, 3, 11, 11, 2, 3, 3, 0, 2),
+]
+
+
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", CONV_GRID)
+def test_conv_matches_torch_conv2d(B, C, H, W, O, k, s, p, d):
+    rng = np.random.default_rng(B * 1000 + C * 10 + k)
+    sa, sw = _rand_pm1(rng, (B, C, H, W)), _rand_pm1(rng, (O, C, k, k))
+    want = F.conv2d(torch.from_numpy(sa).double(), torch.from_numpy(sw).double(),
+                    stride=s, padding=p, dilation=d)
+    got = oracle.conv2d_dot(sa, sw, s, p, d)
+    assert got.shape == tuple(want.shape)
+    np.testing.assert_array_equal(got, want.numpy())
+
+
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", CONV_GRID)
+def test_conv_matches_unfold_mm(B, C, H, W, O, k, s, p, d):
+    # banghao.live/blog/9 section 2: unfold -> [bs*L, C*k*k] -> mm(W.view(O,-1).T)
+    # -> reshape to [bs, O, h_out, w_out]; dilation is passed to unfold here.
+    rng = np.random.default_rng(7 + C + H)
+    sa, sw = _rand_pm1(rng, (B, C, H, W)), _rand_pm1(rng, (O, C, k, k))
+    ho = (H + 2 * p - d * (k - 1) - 1) // s + 1
+    wo = (W + 2 * p - d * (k - 1) - 1) // s + 1
+    cols = F.unfold(torch.from_numpy(sa).double(), kernel_size=k, padding=p, stride=s, dilation=d)
+    L = cols.shape[2]
+    cols = cols.transpose(1, 2).reshape(-1, C * k * k)
+    out = torch.mm(cols, torch.from_numpy(sw).double().view(O, -1).t())
+    out = out.reshape(B, L, O).transpose(1, 2).reshape(B, O, ho, wo)
+    np.testing.assert_array_equal(oracle.conv2d_dot(sa, sw, s, p, d), out.numpy())
+
+
+def test_conv_output_size_formula():
+    for h, k, s, p, d in itertools.product([1, 5, 14, 28], [1, 3, 5], [1, 2, 3], [0, 1, 2], [1, 2]):
+        num = h + 2 * p - d * (k - 1) - 1
+        got = oracle.conv2d_out_size(h, k, s, p, d)
+        if num < 0:
+            assert got == 0
+            continue
+        ref = F.conv2d(torch.zeros(1, 1, h, h), torch.zeros(1, 1, k, k), stride=s, padding=p,
+                       dilation=d).shape[-1]
+        assert got == ref
+
+
+def test_conv_brute_force_python_loops():
+    rng = np.random.default_rng(5)
+    B, C, H, W, O, k, s, p, d = 2, 2, 4, 5, 2, 3, 2, 2, 2
+    sa, sw = _rand_pm1(rng, (B, C, H, W)), _rand_pm1(rng, (O, C, k, k))
+    got = oracle.conv2d_dot(sa, sw, s, p, d)
+    ho, wo = got.shape[2:]
+    for b, o, i, j in itertools.product(range(B), range(O), range(ho), range(wo)):
+        acc = 0
+        for c, kh, kw in itertools.product(range(C), range(k), range(k)):
+            y, x = i * s - p + kh * d, j * s - p + kw * d
+            if 0 <= y < H and 0 <= x < W:
+                acc += int(sa[b, c, y, x]) * int(sw[o, c, kh, kw])
+        assert got[b, o, i, j] == acc
+
+
+def test_conv_invariants_with_valid_tap_count():
+    rng = np.random.default_rng(9)
+    B, C, H, W, O, k, s, p, d = 2, 5, 6, 6, 3, 3, 1, 2, 1
+    sa, sw = _rand_pm1(rng, (B, C, H, W)), _rand_pm1(rng, (O, C, k, k))
+    dot = oracle.conv2d_dot(sa, sw, s, p, d).astype(np.int64)
+    ho, wo = dot.shape[2:]
+    for i, j in itertools.product(range(ho), range(wo)):
+        nv = sum(1 for kh in range(k) for kw in range(k)
+                 if 0 <= i * s - p + kh * d < H and 0 <= j * s - p + kw * d < W)
+        assert (np.abs(dot[:, :, i, j]) <= C * nv).all()
+        assert ((dot[:, :, i, j] - C * nv) % 2 == 0).all()
+
+
+def test_conv_dot_at_agrees_with_full():
+    rng = np.random.default_rng(21)
+    sa, sw = _rand_pm1(rng, (2, 6, 7, 7)), _rand_pm1(rng, (4, 6, 3, 3))
+    full = oracle.conv2d_dot(sa, sw, 2, 1, 1)
+    idx = rng.integers(0, full.size, 64)
+    np.testing.assert_array_equal(oracle.conv2d_dot_at(sa, sw, 2, 1, 1, idx), full.reshape(-1)[idx])
+
+
+def test_pack_nhwc_is_channel_rows():
+    rng = np.random.default_rng(4)
+    s = _rand_pm1(rng, (2, 37, 3, 4))
+    for code in (oracle.CODE_BITS, oracle.CODE_E4M3, oracle.CODE_E2M1):
+        p = oracle.pack_nchw_to_nhwc(s, code)
+        assert p.shape == (2, 3, 4, oracle.packed_row_bytes(37, code))
+        np.testing.assert_array_equal(p[1, 2, 3], oracle.pack_rows(s[1, :, 2, 3][None], code)[0])
+
+
+# ---------------------------------------------------------------------------
+# Epilogue: exact rounding cases worked by hand
+# ---------------------------------------------------------------------------
+
+def test_alpha_rounds_the_exact_product_once_to_float():
+    # (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24: the 2^-24 term is half an ulp of 1.0
+    # in fp32, a tie, rounded to the even neighbour 1 + 2^-11.
+    a = 1.0 + 2.0 ** -12
+    assert oracle.alpha(a, a) == np.float32(1.0 + 2.0 ** -11)
+    # (1 + 2^-12)(1 + 2^-11) = 1 + 3*2^-12 + 2^-23: exactly representable.
+    assert oracle.alpha(a, 1.0 + 2.0 ** -11) == np.float32(1.0 + 3 * 2.0 ** -12 + 2.0 ** -23)
+
+
+def test_epilogue_bf16_round_half_even():
+    dot = np.array([1, 1, -1, 2], np.int32)
+    # 1 + 2^-8 sits halfway between bf16 neighbours 1 and 1 + 2^-7 -> even (1.0)
+    y = oracle.epilogue(dot[:1], 1.0 + 2.0 ** -8, 1.0, "bf16")
+    assert y.dtype == torch.bfloat16 and float(y[0]) == 1.0
+    # 1 + 3*2^-8 sits halfway between 1 + 2^-7 and 1 + 2^-6 -> even (1 + 2^-6)
+    y = oracle.epilogue(dot, 1.0 + 3 * 2.0 ** -8, 1.0, "bf16")
+    assert [float(v) for v in y] == [1.015625, 1.015625, -1.015625, 2.03125]
+    # just above the tie rounds up
+    y = oracle.epilogue(dot[:1], 1.0 + 2.0 ** -8 + 2.0 ** -20, 1.0, "bf16")
+    assert float(y[0]) == 1.0 + 2.0 ** -7
+
+
+def test_epilogue_f32_and_i32():
+    dot = np.array([0, 3, -11008, 4096], np.int32)
+    a = 1.0 + 2.0 ** -12
+    y = oracle.epilogue(dot, a, a, "f32")
+    al = 1.0 + 2.0 ** -11
+    assert y.dtype == torch.float32
+    assert [float(v) for v in y] == [0.0, 3 * al, -11008 * al, 4096 * al]
+    np.testing.assert_array_equal(oracle.epilogue(dot, a, a, "i32").numpy(), dot)
+
+
+def test_epilogue_f32_single_rounding_of_product():
+    # dot = 3, alpha = 1 + 2^-23 (one ulp above 1): 3 + 3*2^-23 = 3 + 1.5 ulp
+    # (the ulp in [2,4) is 2^-22), a tie between 3 + 2^-22 (odd last bit) and
+    # 3 + 2^-21 (even) -> 3 + 2^-21. dot = 5: the ulp in [4,8) is 2^-21, so
+    # 5 + 5*2^-23 = 5 + 1.25 ulp -> 5 + 2^-21.
+    y = oracle.epilogue(np.array([3, 5], np.int32), 1.0 + 2.0 ** -23, 1.0, "f32")
+    assert float(y[0]) == 3.0 + 2.0 ** -21
+    assert float(y[1]) == 5.0 + 2.0 ** -21
+
+
+# ---------------------------------------------------------------------------
+# Whole forward composed from the parts, and the workload recipe
+# ---------------------------------------------------------------------------
+
+def test_binary_linear_composition():
+    wl = workloads.tiny_linear()
+    y = oracle.binary_linear(wl.x, wl.w, wl.scale_a, wl.scale_w, wl.bias, wl.out_dtype)
+    sx = torch.where(wl.x >= 0, 1.0, -1.0).double()
+    sw = torch.where(wl.w >= 0, 1.0, -1.0).double()
+    ref = (sx @ sw.T) * float(np.float32(np.float64(wl.scale_a) * np.float64(wl.scale_w)))
+    assert y.shape == (64, 256) and y.dtype == torch.float32
+    torch.testing.assert_close(y.double(), ref, rtol=1e-7, atol=0)
+
+
+def test_workload_recipe():
+    wl = workloads.tiny_linear()
+    assert tuple(wl.x.shape) == (64, 512) and tuple(wl.w.shape) == (256, 512)
+    assert wl.bias is None and wl.out_dtype == "f32"
+    assert wl.scale_a == pytest.approx(float(wl.x.abs().double().mean()), rel=1e-7)
+    again = workloads.tiny_linear()
+    assert torch.equal(wl.x, again.x) and torch.equal(wl.w, again.w)
+    assert wl.gemm_shape() == (64, 256, 512)
+    c = workloads.conv("c", 2, 3, 14, 14, 4, 3, 2, 1, 1)
+    assert c.gemm_shape() == (2 * 7 * 7, 4, 27)
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: plausible errors in copies of the oracle's arithmetic
+# must fail the pins above.
+# ---------------------------------------------------------------------------
+
+def _conv_mutant(sa, sw, s, p, d, mistake):
+    B, C, H, W = sa.shape
+    O, _, k, _ = sw.shape
+    ho, wo = (H + 2 * p - d * (k - 1) - 1) // s + 1, (W + 2 * p - d * (k - 1) - 1) // s + 1
+    out = np.zeros((B, O, ho, wo), np.int64)
+    for b, o, i, j in itertools.product(range(B), range(O), range(ho), range(wo)):
+        for c, kh, kw in itertools.product(range(C), range(k), range(k)):
+            y, x = i * s - p + kh * d, j * s - p + kw * d
+            if mistake == "flipped_kernel":
+                wv = sw[o, c, k - 1 - kh, k - 1 - kw]
+            elif mistake == "swapped_taps":
+                wv = sw[o, c, kw, kh]
+            else:
+                wv = sw[o, c, kh, kw]
+            if mistake == "no_dilation":
+                y, x = i * s - p + kh, j * s - p + kw
+            if 0 <= y < H and 0 <= x < W:
+                out[b, o, i, j] += int(sa[b, c, y, x]) * int(wv)
+            elif mistake == "pad_as_plus_one":
+                out[b, o, i, j] += int(wv)
+    return out
+
+
+@pytest.mark.parametrize("mistake", ["flipped_kernel", "swapped_taps", "no_dilation",
+                                     "pad_as_plus_one"])
+def test_planted_conv_mistakes_are_caught(mistake):
+    rng = np.random.default_rng(31)
+    sa, sw = _rand_pm1(rng, (1, 3, 6, 6)), _rand_pm1(rng, (2, 3, 3, 3))
+    want = F.conv2d(torch.from_numpy(sa).double(), torch.from_numpy(sw).double(),
+                    stride=1, padding=2, dilation=2).numpy()
+    assert np.array_equal(_conv_mutant(sa, sw, 1, 2, 2, None), want)
+    assert not np.array_equal(_conv_mutant(sa, sw, 1, 2, 2, mistake), want)
+
+
+def test_planted_linear_mistakes_are_caught():
+    rng = np.random.default_rng(32)
+    K = 33
+    sa, sw = _rand_pm1(rng, (4, K)), _rand_pm1(rng, (5, K))
+    ham = np.array([[np.count_nonzero((sa[m] > 0) != (sw[n] > 0)) for n in range(5)]
+                    for m in range(4)])
+    good = sa.astype(np.int64) @ sw.T.astype(np.int64)
+    assert np.array_equal(good, K - 2 * ham)
+    dropped_last = sa[:, :-1].astype(np.int64) @ sw[:, :-1].T.astype(np.int64)
+    assert not np.array_equal(dropped_last, K - 2 * ham)
+    wrong_sign = -good
+    assert not np.array_equal(wrong_sign, K - 2 * ham)
+    # a threshold of > 0 instead of >= 0 changes the sign of exact zeros
+    x = np.array([[0.0, 1.0, -1.0]], np.float32)
+    assert oracle.binarize(x)[0, 0] == 1 and np.where(x > 0, 1, -1)[0, 0] == -1
