@@ -1,0 +1,429 @@
+"""Benchmark of the binarized linear / conv2d forward on GB300.
+
+One step = one forward over one batch of synthetic input: shift + sign +
+pack of the activations, the packed contraction and the fused scale + cast
+epilogue. Weights are packed once, before timing (the pages' weights are
+packed offline by w_pack). Default workload: the 4096 x 4096 x 4096 bf16
+linear layer with a scalar activation bias.
+
+Prints ONE JSON line on rank 0. Under torchrun every rank runs its own
+replica of the workload (its shard of a batch N times larger; no collective
+on the data path) and the max-over-ranks time gives the whole-job value.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+import workloads
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llm_linear", choices=sorted(workloads.NAMED))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "popc", "e4m3", "e2m1"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks only)
+# ---------------------------------------------------------------------------
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# peaks
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p)), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+# nominal dense tensor rates (PFLOP/s) for the ratio to the measured bf16 peak
+NOMINAL_PF = {"bf16": 2.25, "e4m3": 4.5, "e2m1": 13.5}
+POPC_PER_CLK_PER_SM = 16        # 32-bit population counts per clock per SM
+SM_COUNT_GB300 = 152
+
+
+def roofline_peak(algo: str, peaks: dict, sms: int):
+    if algo == "popc":
+        # each 32-bit popcount of a XOR retires 32 multiply-adds = 64 binary ops
+        tops = sms * POPC_PER_CLK_PER_SM * 64 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        return "alu", tops, "TOP/s", f"{sms} SMs x {POPC_PER_CLK_PER_SM} POPC/clk x 64 ops x max SM clock"
+    tflops = peaks["bf16_tflops"] * NOMINAL_PF[algo] / NOMINAL_PF["bf16"]
+    return "tensor", tflops, "TFLOP/s", f"measured bf16 x nominal {algo}/bf16 ratio"
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+ALGO_NAME = {0: "popc", 1: "e4m3", 2: "e2m1"}
+
+
+def run_ours(args, rank, world):
+    import xnor_popcount_gemm_gb300 as bt
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    wl = workloads.NAMED[args.workload]()
+    M, N, K = wl.gemm_shape()
+    ops = wl.binary_ops()
+    op = bt.BT_OP_LINEAR if wl.kind == "linear" else bt.BT_OP_CONV2D
+    if args.algo == "auto":
+        code, algo = bt.bt_plan(op, M, N, K)
+    else:
+        code = {"popc": bt.BT_CODE_BITS, "e4m3": bt.BT_CODE_E4M3, "e2m1": bt.BT_CODE_E2M1}[args.algo]
+        algo = bt.BT_ALGO_AUTO
+    algo_name = ALGO_NAME[code]
+    out_t = {"f32": torch.float32, "bf16": torch.bfloat16}[wl.out_dtype]
+    stream = torch.cuda.current_stream()
+
+    # weights: packed once, outside timing
+    if wl.kind == "linear":
+        wp = bt.bt_pack_sign(wl.w.to(dev), code)
+    else:
+        wp = bt.bt_pack_sign(wl.w.to(dev), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    bias = None if wl.bias is None else wl.bias.to(dev)
+
+    # rotate over enough input/output buffers that one pass exceeds L2
+    x_bytes = wl.x.numel() * wl.x.element_size()
+    out_elems = M * N
+    out_bytes = out_elems * torch.tensor([], dtype=out_t).element_size()
+    nbuf = max(1, -(-2 * L2_BYTES // (x_bytes + out_bytes)))
+    xs = [wl.x.to(dev) for _ in range(nbuf)]
+    if wl.kind == "linear":
+        outs = [torch.empty((M, N), dtype=out_t, device=dev) for _ in range(nbuf)]
+        ws = torch.empty(bt.bt_binary_linear_workspace(M, K, bt.BT_BF16, code), dtype=torch.uint8, device=dev)
+        xp_shape = (M, bt.bt_packed_row_bytes(K, code))
+    else:
+        B, C, H, W = wl.x.shape
+        k = wl.w.shape[2]
+        Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
+        Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
+        outs = [torch.empty((B, N, Ho, Wo), dtype=out_t, device=dev) for _ in range(nbuf)]
+        ws = torch.empty(bt.bt_binary_conv2d_workspace(B, C, H, W, bt.BT_BF16, code), dtype=torch.uint8, device=dev)
+        xp_shape = (B, H, W, bt.bt_packed_row_bytes(C, code))
+    xp = ws[: int(np.prod(xp_shape))].view(*xp_shape)
+
+    def step(i, ev=None):
+        x, out = xs[i % nbuf], outs[i % nbuf]
+        # pack (a1/a3) then contraction + epilogue (a5/a6 + a7): two public calls
+        if ev is not None:
+            ev[0].record(stream)
+        if wl.kind == "linear":
+            bt.bt_pack_sign(x, code, bt.BT_LAYOUT_ROWS, bias, out=xp)
+        else:
+            bt.bt_pack_sign(x, code, bt.BT_LAYOUT_NCHW_TO_NHWC, bias, out=xp)
+        if ev is not None:
+            ev[1].record(stream)
+        if wl.kind == "linear":
+            bt.bt_binary_linear(xp, wp, code, K, wl.scale_a, wl.scale_w, out=out, out_dtype=out_t,
+                                algo=algo, x_packed=True)
+        else:
+            C, k = wl.x.shape[1], wl.w.shape[2]
+            bt.bt_binary_conv2d(xp, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
+                                wl.scale_w, out=out, out_dtype=out_t, algo=algo, x_packed=True)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert bt.bt_device_status() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    status = bt.bt_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {bt.bt_status_string(status)}")
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world)
+    ms_step = ms_total / args.steps
+    pack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    gemm_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    value = ops * world * args.steps / (ms_total / 1e3) / 1e9
+
+    # end to end through the public API from pinned host buffers
+    x_host = wl.x.pin_memory()
+    y_host = torch.empty(outs[0].shape, dtype=out_t).pin_memory()
+    xdev = xs[0]
+
+    def e2e_step():
+        xdev.copy_(x_host, non_blocking=True)
+        if wl.kind == "linear":
+            bt.bt_binary_linear(xdev, wp, code, K, wl.scale_a, wl.scale_w, bias, out=outs[0],
+                                out_dtype=out_t, algo=algo, workspace=ws)
+        else:
+            C, k = wl.x.shape[1], wl.w.shape[2]
+            bt.bt_binary_conv2d(xdev, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
+                                wl.scale_w, bias, out=outs[0], out_dtype=out_t, algo=algo, workspace=ws)
+        y_host.copy_(outs[0], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(5, args.steps // 2)
+    barrier(world)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), world) / e2e_steps
+    e2e_value = ops * world / (e2e_ms / 1e3) / 1e9
+
+    peaks, peak_src = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    bound, peak, unit, peak_how = roofline_peak(algo_name, peaks, sms)
+    achieved = ops / (gemm_ms / 1e3) / 1e12
+    traffic = load_traffic(wl.name, algo_name)
+    line = {
+        "metric": "binary GOPS (2*M*N*K/s)",
+        "value": round(value, 1),
+        "unit": "GOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {"popc": "b1 (xor+popc, int32 acc)", "e4m3": "fp8 e4m3 +-1 (fp32 acc, exact)",
+                  "e2m1": "fp4 e2m1 +-1 (fp32 acc, exact)"}[algo_name],
+        "data": "synthetic (seeded, shapes of the pages' layers)",
+        "config": {"workload": wl.name, "M": M, "N": N, "K": K, "x_dtype": wl.x_dtype,
+                   "out_dtype": wl.out_dtype, "code": algo_name, "weights": "pre-packed outside timing",
+                   "l2": f"inputs+outputs rotate over {nbuf} buffers ({nbuf * (x_bytes + out_bytes) / 1e6:.0f} MB > L2)",
+                   "parallelism": f"replicas x{world}"},
+        "kernel_ms": {"pack": round(pack_ms, 5), "contraction": round(gemm_ms, 5)},
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src}: {peak_how}", "kernel": "contraction"},
+        "pack_roofline": {"bound": "hbm", "achieved": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9, 1),
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GOPS",
+                "h2d_bytes_per_step": int(x_bytes), "d2h_bytes_per_step": int(out_bytes),
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    return line
+
+
+def pack_bytes(wl, code, bt):
+    """Algorithmic bytes of the activation pack: read x once, write it packed."""
+    if wl.kind == "linear":
+        M, K = wl.x.shape
+        return wl.x.numel() * wl.x.element_size() + M * bt.bt_packed_row_bytes(K, code)
+    B, C, H, W = wl.x.shape
+    return wl.x.numel() * wl.x.element_size() + B * H * W * bt.bt_packed_row_bytes(C, code)
+
+
+def load_traffic(workload: str, algo: str):
+    """DRAM bytes per contraction launch from a committed ncu summary, if one
+    exists for this exact kernel build and workload."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        return json.load(open(p)).get(f"{workload}/{algo}")
+    except (ValueError, OSError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_forward(wl, rows: int):
+    import oracle
+    if wl.kind == "linear":
+        return oracle.binary_linear(wl.x[:rows], wl.w, wl.scale_a, wl.scale_w, wl.bias, wl.out_dtype)
+    return oracle.binary_conv2d(wl.x[:rows], wl.w, wl.scale_a, wl.scale_w, wl.stride, wl.padding,
+                                wl.dilation, wl.bias, wl.out_dtype)
+
+
+def sample_rows(wl, budget_ops: float) -> int:
+    """Rows (linear) or images (conv) of the workload whose forward is about
+    `budget_ops` binary ops."""
+    total = wl.x.shape[0]
+    per = wl.binary_ops() / total
+    return int(max(1, min(total, budget_ops // per)))
+
+
+def cpu_baseline(wl, budget_ops: float = 1.5e11):
+    rows = sample_rows(wl, budget_ops)
+    ops = wl.binary_ops() * rows / wl.x.shape[0]
+    t = time.perf_counter()
+    oracle_forward(wl, rows)
+    dt = time.perf_counter() - t
+    return {"value": round(ops / dt / 1e9, 3), "unit": "GOPS", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"first {rows} of {wl.x.shape[0]} {'rows' if wl.kind == 'linear' else 'images'} "
+                      f"of {wl.name} (binarize + nested-loop dot + epilogue)"}
+
+
+def run_reference(args, rank, world):
+    wl = workloads.NAMED[args.workload]()
+    rows = sample_rows(wl, 2.0e10)
+    ops = wl.binary_ops() * rows / wl.x.shape[0]
+    for _ in range(args.warmup):
+        oracle_forward(wl, rows)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_forward(wl, rows)
+    dt = (time.perf_counter() - t) / args.steps
+    value = ops / dt / 1e9
+    cores = len(os.sched_getaffinity(0))
+    sample = f"first {rows} of {wl.x.shape[0]} rows/images of {wl.name} per step"
+    return {"impl": "reference", "metric": "binary GOPS (2*M*N*K/s)", "value": round(value, 3), "unit": "GOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 +-1 (int32 acc)",
+            "data": "synthetic (seeded, shapes of the pages' layers)",
+            "config": {"workload": wl.name, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GOPS", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # rank 0 alone times the oracle on the host cores; other ranks exit
+        rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    rank, world = dist_init(args)
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

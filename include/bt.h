@@ -1,0 +1,222 @@
+/*
+ * bt.h -- C ABI of libbt: the binarized linear and conv2d forward on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (bitorch-engine: BinaryConv2dCutlass / BinaryConv2dForward,
+ * BinaryLinearCuda / BinaryLinearForward):
+ *   1. shift      a = x + bias_a            (set_activation, "learnable shift input")
+ *   2. binarize   sa = +1 if a >= 0 else -1, sw = +1 if W >= 0 else -1
+ *   3. contract   dot = sum_k sa*sw = K - 2*popcount(bits(sa) XOR bits(sw))
+ *                 (a convolution through an implicit im2col)
+ *   4. scale      y = fp32(dot * alpha), alpha = fp32(scale_a * scale_w)
+ *                 (the native forward receives scale_a.item()*scale_w.item())
+ *   5. cast       out = y.to(x.dtype)        (BinaryConv2dForward.forward)
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device (or managed) memory; all work is
+ *     enqueued asynchronously on `stream` (NULL = the legacy default stream).
+ *     The caller owns every buffer; the library allocates nothing and keeps no
+ *     pointer after a call returns.
+ *   - Tensors are dense and contiguous (row-major / NCHW as stated). Device
+ *     pointers must be 16-byte aligned; the workspace 256-byte aligned.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns an error status and launches nothing.
+ *   - A launch failure returns BT_ERR_CUDA. Kernels never trap: a bounded
+ *     wait that runs out records BT_ERR_TIMEOUT in a device error word and the
+ *     kernel returns; bt_device_status() reports it.
+ *   - No call aborts the process.
+ *
+ * Binarization rule: +1 where x + bias >= 0 (the sum in IEEE fp32 without
+ * flushing subnormals, whose sign is the sign of the exact sum), else -1;
+ * -0.0 gives +1 and NaN gives -1. Weights use the same rule without a shift.
+ * The pages' spec writes the shift as x - bias_a; the pages' code adds
+ * it (x + bias_a.view(1,-1,1,1)); this library adds it, so pass -b for the
+ * other convention.
+ */
+#ifndef BT_H
+#define BT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *bt_stream;
+
+typedef enum {
+    BT_OK = 0,
+    BT_ERR_INVALID_ARG = -1,   /* null pointer, bad size, bad scale, bad enum value */
+    BT_ERR_UNSUPPORTED = -2,   /* valid request this build cannot serve (e.g. algo vs code) */
+    BT_ERR_ALIGNMENT = -3,     /* a pointer misses its required alignment */
+    BT_ERR_WORKSPACE = -4,     /* workspace missing or smaller than the query says */
+    BT_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
+    BT_ERR_TIMEOUT = -6        /* a kernel's bounded wait ran out (device error word) */
+} bt_status;
+
+/* Element types. BT_PACKED is an input already packed in the weight's code. */
+typedef enum {
+    BT_F32 = 0,
+    BT_BF16 = 1,
+    BT_F16 = 2,
+    BT_I32 = 3,     /* output only: the raw integer dot products */
+    BT_PACKED = 4   /* input only */
+} bt_dtype;
+
+/*
+ * Packed operand encodings ("bit-packing" of bitorch-engine's w_pack /
+ * generate_quantized_weight, there with 8-bit words; here with a 16-byte row
+ * pitch). A packed row of k elements occupies bt_packed_row_bytes(k, code)
+ * bytes; every position after the last element is 0.
+ *
+ *   BT_CODE_BITS  1 bit per element in little-endian uint32 words: bit j of
+ *                 word w holds element 32*w + j; 1 means +1, 0 means -1.
+ *                 Contracted by XOR + popcount: dot = k - 2*popc(a ^ w).
+ *   BT_CODE_E4M3  1 byte per element, the FP8 E4M3 value +1.0 (0x38) or
+ *                 -1.0 (0xB8); padding is 0x00 (0.0).
+ *   BT_CODE_E2M1  4 bits per element, the FP4 E2M1 value +1.0 (0x2) or -1.0
+ *                 (0xA), element 2i in the low nibble of byte i; padding 0.
+ *
+ * The E4M3 / E2M1 encodings feed the tcgen05 tensor cores; products of +1/-1
+ * codes are +1/-1 and the sums are integers, so dot is the same integer as
+ * with BITS. A padded or zero-filled position contributes 0.
+ */
+typedef enum {
+    BT_CODE_BITS = 0,
+    BT_CODE_E4M3 = 1,
+    BT_CODE_E2M1 = 2
+} bt_code;
+
+typedef enum {
+    BT_LAYOUT_ROWS = 0,          /* [R, K] row-major -> [R, row_bytes(K)] */
+    BT_LAYOUT_NCHW_TO_NHWC = 1   /* [B, C, H, W] -> [B, H, W, row_bytes(C)] (channel-packed) */
+} bt_layout;
+
+/*
+ * Contraction kernels (the BMM type of BinaryLinearCuda, whose default
+ * BMM.ADAPTIVE picks one; here BT_ALGO_AUTO does).
+ */
+typedef enum {
+    BT_ALGO_AUTO = 0,        /* the kernel for the weight's code chosen by bt_plan() */
+    BT_ALGO_POPC = 1,        /* CUDA cores: XOR + popcount, code BITS */
+    BT_ALGO_TC_E4M3 = 2,     /* tcgen05 kind::f8f6f4 on +1/-1 E4M3, code E4M3 */
+    BT_ALGO_TC_E2M1 = 3      /* tcgen05 kind::mxf4 on +1/-1 E2M1 (unit block scales), code E2M1 */
+} bt_algo;
+
+typedef enum { BT_OP_LINEAR = 0, BT_OP_CONV2D = 1 } bt_op;
+
+/* Library version as 10000*major + 100*minor + patch. */
+int bt_version(void);
+
+/* Static text for a status code; never NULL. */
+const char *bt_status_string(bt_status status);
+
+/* Bytes of one packed row of k elements in `code` (rounded up to 16 bytes);
+ * -1 for k < 0 or an unknown code. */
+int64_t bt_packed_row_bytes(int64_t k, bt_code code);
+
+/*
+ * bt_pack_sign -- fused shift + sign + pack (BinaryConv2dCutlass.set_activation
+ * followed by the native binarization; w_pack for weights).
+ *
+ *   x        device, x_dtype in {BT_F32, BT_BF16, BT_F16}, dense:
+ *              ROWS:          [d0=R, d1=K]            (d2, d3 ignored)
+ *              NCHW_TO_NHWC:  [d0=B, d1=C, d2=H, d3=W] (OIHW weights: B=O, H=W=k)
+ *   bias     device fp32 or NULL; bias_len 0 (none), 1 (one scalar) or d1
+ *            (one per column of ROWS / per channel of NCHW).
+ *   out      device, ROWS: [R, bt_packed_row_bytes(K, code)] bytes;
+ *            NCHW_TO_NHWC: [B, H, W, bt_packed_row_bytes(C, code)] bytes.
+ * Errors: BT_ERR_INVALID_ARG for null x/out, d0..d3 < 1 (d0 = 0 rows is
+ * allowed and does nothing), a bad bias_len or enum; BT_ERR_ALIGNMENT when x or
+ * out is not 16-byte aligned.
+ */
+bt_status bt_pack_sign(const void *x, bt_dtype x_dtype, bt_layout layout,
+                       int64_t d0, int64_t d1, int64_t d2, int64_t d3,
+                       const float *bias, int64_t bias_len,
+                       bt_code code, void *out, bt_stream stream);
+
+/* Workspace bytes bt_binary_linear needs (0 when x is BT_PACKED). */
+size_t bt_binary_linear_workspace(int64_t M, int64_t K, bt_dtype x_dtype, bt_code code);
+
+/*
+ * bt_binary_linear -- out = cast(fp32(dot * fp32(scale_a*scale_w))),
+ * dot[m,n] = sum_k sign(x[m,k] + bias) * sign(W[n,k])
+ * (BinaryLinearForward.forward(input, weight, bmm_type, scale_a, scale_w)).
+ *
+ *   x          device [M, K] in x_dtype (BT_F32/BF16/F16), or BT_PACKED:
+ *              [M, bt_packed_row_bytes(K, w_code)] already in w_code.
+ *   weight     device [N, bt_packed_row_bytes(K, w_code)], packed by
+ *              bt_pack_sign (layout ROWS) from W [N, K].
+ *   scale_a, scale_w  finite and > 0 (a positive scale_a leaves every sign
+ *              unchanged, so it only scales the result).
+ *   bias_a     device fp32 or NULL; bias_len 0, 1 or K. Ignored for BT_PACKED.
+ *   out        device [M, N] in out_dtype (BT_F32, BT_BF16, BT_F16, or BT_I32
+ *              for the raw dot products).
+ *   algo       BT_ALGO_AUTO or the kernel matching w_code.
+ *   workspace  device, >= bt_binary_linear_workspace(M, K, x_dtype, w_code)
+ *              bytes, 256-byte aligned; holds the packed activations.
+ * M = 0 or N = 0 is a no-op. K must be >= 1.
+ */
+bt_status bt_binary_linear(const void *x, bt_dtype x_dtype,
+                           const void *weight, bt_code w_code,
+                           int64_t M, int64_t N, int64_t K,
+                           float scale_a, float scale_w,
+                           const float *bias_a, int64_t bias_len,
+                           void *out, bt_dtype out_dtype, bt_algo algo,
+                           void *workspace, size_t workspace_bytes, bt_stream stream);
+
+/* Workspace bytes bt_binary_conv2d needs (0 when x is BT_PACKED). */
+size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W,
+                                  bt_dtype x_dtype, bt_code code);
+
+/*
+ * bt_binary_conv2d -- BinaryConv2dForward.forward(x, weight, scale_a, scale_w,
+ * is_train=False, kernel_size, stride, padding, dilation) as an implicit-im2col
+ * contraction over channel-packed NHWC activations.
+ *
+ *   x          device NCHW [B, C, H, W] in x_dtype, or BT_PACKED:
+ *              [B, H, W, bt_packed_row_bytes(C, w_code)].
+ *   weight     device [O, k, k, bt_packed_row_bytes(C, w_code)]: OIHW weights
+ *              packed by bt_pack_sign with layout NCHW_TO_NHWC.
+ *   Output size Ho = floor((H + 2p - d(k-1) - 1)/s + 1), same for Wo
+ *   (banghao.live/blog/9, section 2); both must be >= 1.
+ *   A tap that falls in the zero padding contributes 0 to dot (the unfold +
+ *   mm lowering of that page).
+ *   bias_a     device fp32 or NULL; bias_len 0, 1 or C (per input channel,
+ *              bias_a.view(1,-1,1,1)). Ignored for BT_PACKED.
+ *   out        device NCHW [B, O, Ho, Wo] in out_dtype.
+ *   kernel_size >= 1, stride >= 1, padding >= 0, dilation >= 1.
+ */
+bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype,
+                           const void *weight, bt_code w_code,
+                           int64_t B, int64_t C, int64_t H, int64_t W, int64_t O,
+                           int kernel_size, int stride, int padding, int dilation,
+                           float scale_a, float scale_w,
+                           const float *bias_a, int64_t bias_len,
+                           void *out, bt_dtype out_dtype, bt_algo algo,
+                           void *workspace, size_t workspace_bytes, bt_stream stream);
+
+/*
+ * bt_plan -- the "ADAPTIVE" choice: the code (weight format) and kernel this
+ * build runs fastest for a problem of this size, from measurements on GB300.
+ * For BT_OP_LINEAR pass (M, N, K); for BT_OP_CONV2D pass M = B*Ho*Wo, N = O,
+ * K = C*k*k. Returns BT_ERR_INVALID_ARG for null outputs or sizes < 1.
+ * The environment variable BT_FORCE_ALGO=popc|e4m3|e2m1 overrides it.
+ */
+bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo);
+
+/*
+ * bt_device_status -- synchronizes `stream`, then reads and clears the
+ * device error word of the current device: BT_ERR_TIMEOUT if a kernel's
+ * bounded wait ran out since the last call, BT_ERR_CUDA if the stream holds a
+ * CUDA error, else BT_OK.
+ */
+bt_status bt_device_status(bt_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BT_H */

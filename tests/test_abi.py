@@ -1,0 +1,158 @@
+"""CPU checks of the C ABI: the library builds and loads, exports every
+function include/bt.h declares, and validates arguments on the host before
+it launches anything (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from xnor_popcount_gemm_gb300 import build as bt_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+bt_build.build()
+import xnor_popcount_gemm_gb300 as bt  # noqa: E402
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "bt.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bt_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(bt.lib_path)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(bt.EXPORTED) == names
+
+
+def test_version_and_status_strings():
+    assert bt.bt_version() >= 100
+    for st in range(-6, 1):
+        s = bt.bt_status_string(st)
+        assert s.startswith("BT_")
+    assert "unknown" in bt.bt_status_string(42)
+
+
+@pytest.mark.parametrize("k,code,want", [
+    (1, 0, 16), (32, 0, 16), (128, 0, 16), (129, 0, 32), (4096, 0, 512), (4100, 0, 528),
+    (1, 1, 16), (16, 1, 16), (17, 1, 32), (4100, 1, 4112),
+    (1, 2, 16), (32, 2, 16), (33, 2, 32), (4100, 2, 2064), (11008, 2, 5504),
+])
+def test_packed_row_bytes(k, code, want):
+    assert bt.bt_packed_row_bytes(k, code) == want
+
+
+def test_packed_row_bytes_rejects_bad_input():
+    assert bt.bt_packed_row_bytes(-1, 0) == -1
+    assert bt.bt_packed_row_bytes(5, 7) == -1
+
+
+def test_workspace_queries():
+    assert bt.bt_binary_linear_workspace(4096, 4096, bt.BT_BF16, bt.BT_CODE_BITS) == 4096 * 512
+    assert bt.bt_binary_linear_workspace(3, 33, bt.BT_F32, bt.BT_CODE_BITS) == 256
+    assert bt.bt_binary_linear_workspace(10, 10, bt.BT_PACKED, bt.BT_CODE_BITS) == 0
+    assert bt.bt_binary_conv2d_workspace(2, 256, 14, 14, bt.BT_F32, bt.BT_CODE_E2M1) == \
+        2 * 14 * 14 * 128
+    assert bt.bt_binary_conv2d_workspace(1, 1, 1, 1, bt.BT_F32, bt.BT_CODE_BITS) == 256
+
+
+# Host validation. Pointers below are never dereferenced: every call fails
+# its checks before anything is enqueued.
+L = bt._c_lin
+C = bt._c_conv
+P = bt._c_pack
+
+
+def lin(**kw):
+    a = dict(x=256, xt=bt.BT_F32, w=512, code=0, M=4, N=4, K=8, sa=1.0, sw=1.0, bias=None, blen=0,
+             out=768, ot=bt.BT_F32, algo=0, ws=None, wsb=0, s=None)
+    a.update(kw)
+    return L(*a.values())
+
+
+def test_linear_validation():
+    assert lin(K=0) == bt.BT_ERR_INVALID_ARG
+    assert lin(M=-1) == bt.BT_ERR_INVALID_ARG
+    assert lin(sa=0.0) == bt.BT_ERR_INVALID_ARG
+    assert lin(sw=float("nan")) == bt.BT_ERR_INVALID_ARG
+    assert lin(sa=float("inf")) == bt.BT_ERR_INVALID_ARG
+    assert lin(sa=-1.0) == bt.BT_ERR_INVALID_ARG
+    assert lin(blen=3) == bt.BT_ERR_INVALID_ARG
+    assert lin(blen=1, bias=None) == bt.BT_ERR_INVALID_ARG
+    assert lin(code=9) == bt.BT_ERR_INVALID_ARG
+    assert lin(ot=bt.BT_PACKED) == bt.BT_ERR_INVALID_ARG
+    assert lin(xt=bt.BT_I32) == bt.BT_ERR_INVALID_ARG
+    assert lin(algo=bt.BT_ALGO_TC_E2M1) == bt.BT_ERR_UNSUPPORTED   # algo does not match BITS
+    assert lin(algo=17) == bt.BT_ERR_INVALID_ARG
+    assert lin(x=None) == bt.BT_ERR_INVALID_ARG
+    assert lin(x=257) == bt.BT_ERR_ALIGNMENT
+    assert lin(out=770) == bt.BT_ERR_ALIGNMENT
+    assert lin(ws=None) == bt.BT_ERR_WORKSPACE                      # float x needs a workspace
+    assert lin(ws=4096, wsb=8) == bt.BT_ERR_WORKSPACE
+    assert lin(ws=4096 + 16, wsb=1 << 20) == bt.BT_ERR_ALIGNMENT
+    assert lin(K=(1 << 24) + 1) == bt.BT_ERR_UNSUPPORTED
+    assert lin(M=0) == bt.BT_OK                                      # empty: nothing to do
+    assert lin(N=0, x=None) == bt.BT_OK
+
+
+def conv(**kw):
+    a = dict(x=256, xt=bt.BT_F32, w=512, code=0, B=1, C=3, H=5, W=5, O=2, k=3, s=1, p=1, d=1,
+             sa=1.0, sw=1.0, bias=None, blen=0, out=768, ot=bt.BT_F32, algo=0, ws=None, wsb=0,
+             st=None)
+    a.update(kw)
+    return C(*a.values())
+
+
+def test_conv_validation():
+    assert conv(k=0) == bt.BT_ERR_INVALID_ARG
+    assert conv(s=0) == bt.BT_ERR_INVALID_ARG
+    assert conv(p=-1) == bt.BT_ERR_INVALID_ARG
+    assert conv(d=0) == bt.BT_ERR_INVALID_ARG
+    assert conv(H=2, p=0) == bt.BT_ERR_INVALID_ARG        # window larger than the image
+    assert conv(blen=2) == bt.BT_ERR_INVALID_ARG
+    assert conv(C=0) == bt.BT_ERR_INVALID_ARG
+    assert conv(sa=0.0) == bt.BT_ERR_INVALID_ARG
+    assert conv(x=264 + 1) == bt.BT_ERR_ALIGNMENT
+    assert conv(ws=None) == bt.BT_ERR_WORKSPACE
+    assert conv(B=0) == bt.BT_OK
+    assert conv(O=0, x=None) == bt.BT_OK
+
+
+def test_pack_validation():
+    s = None
+    assert P(256, bt.BT_F32, 0, 4, 0, 1, 1, None, 0, 0, 512, s) == bt.BT_ERR_INVALID_ARG   # K = 0
+    assert P(256, bt.BT_I32, 0, 4, 8, 1, 1, None, 0, 0, 512, s) == bt.BT_ERR_INVALID_ARG
+    assert P(256, bt.BT_F32, 5, 4, 8, 1, 1, None, 0, 0, 512, s) == bt.BT_ERR_INVALID_ARG
+    assert P(256, bt.BT_F32, 0, 4, 8, 1, 1, None, 3, 0, 512, s) == bt.BT_ERR_INVALID_ARG
+    assert P(256, bt.BT_F32, 0, 4, 8, 1, 1, None, 1, 0, 512, s) == bt.BT_ERR_INVALID_ARG
+    assert P(None, bt.BT_F32, 0, 4, 8, 1, 1, None, 0, 0, 512, s) == bt.BT_ERR_INVALID_ARG
+    assert P(258, bt.BT_F32, 0, 4, 8, 1, 1, None, 0, 0, 512, s) == bt.BT_ERR_ALIGNMENT
+    assert P(256, bt.BT_F32, 1, 4, 8, 0, 1, None, 0, 0, 512, s) == bt.BT_ERR_INVALID_ARG
+    assert P(None, bt.BT_F32, 0, 0, 8, 1, 1, None, 0, 0, None, s) == bt.BT_OK             # 0 rows
+
+
+def test_plan():
+    code, algo = bt.bt_plan(bt.BT_OP_LINEAR, 4096, 4096, 4096)
+    assert code in (0, 1, 2) and algo == {0: bt.BT_ALGO_POPC, 1: bt.BT_ALGO_TC_E4M3,
+                                          2: bt.BT_ALGO_TC_E2M1}[code]
+    code, algo = bt.bt_plan(bt.BT_OP_LINEAR, 16, 16, 1 << 20)      # K beyond the tensor-core bound
+    assert code == bt.BT_CODE_BITS and algo == bt.BT_ALGO_POPC
+    with pytest.raises(bt.BtError):
+        bt.bt_plan(bt.BT_OP_LINEAR, 0, 1, 1)
+
+
+def test_plan_override(monkeypatch):
+    monkeypatch.setenv("BT_FORCE_ALGO", "popc")
+    assert bt.bt_plan(bt.BT_OP_CONV2D, 4096, 256, 2304) == (bt.BT_CODE_BITS, bt.BT_ALGO_POPC)
+    monkeypatch.setenv("BT_FORCE_ALGO", "e4m3")
+    assert bt.bt_plan(bt.BT_OP_LINEAR, 64, 64, 64) == (bt.BT_CODE_E4M3, bt.BT_ALGO_TC_E4M3)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_device_status_without_device():
+    assert bt._c_status(None) == bt.BT_ERR_CUDA

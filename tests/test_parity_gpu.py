@@ -1,0 +1,255 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer results (packed operands, raw dot products) must match bit for bit;
+scaled float outputs within 1e-6 relative (the epilogue is one fp32 multiply
+and one round-to-nearest-even cast on both sides, so they match exactly in
+practice). Sizes span several 128 x 128 tiles with ragged tails; the full
+workloads are checked on sampled outputs the oracle computes one by one, and
+through invariants over every output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from xnor_popcount_gemm_gb300 import build as bt_build
+
+bt_build.build()
+import xnor_popcount_gemm_gb300 as bt  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+REL_TOL = 1e-6
+OUT_T = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "i32": torch.int32}
+CODES = [bt.BT_CODE_BITS, bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
+CODE_IDS = ["bits", "e4m3", "e2m1"]
+
+
+@pytest.fixture(autouse=True)
+def _device_clean():
+    yield
+    assert bt.bt_device_status() == 0
+
+
+def assert_close_rel(got: torch.Tensor, want: torch.Tensor):
+    assert got.shape == want.shape and got.dtype == want.dtype
+    if got.dtype == torch.int32:
+        assert torch.equal(got, want)
+        return
+    g, w = got.double(), want.double()
+    err = (g - w).abs()
+    bad = err > REL_TOL * w.abs()
+    assert not bad.any(), f"{int(bad.sum())} mismatches, first at {bad.nonzero()[0].tolist()}"
+
+
+def _gen(seed, shape, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g).to(dtype)
+
+
+# ---------------------------------------------------------------------------
+# Packing
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("K", [1, 7, 31, 32, 33, 100, 255, 256, 257, 1000, 4100])
+def test_pack_rows(code, dtype, K):
+    x = _gen(K, (37, K), dtype)
+    x[0, : min(K, 6)] = torch.tensor([0.0, -0.0, float("nan"), float("inf"), -float("inf"), -1e-30])[: min(K, 6)].to(dtype)
+    for bias in (None, torch.tensor([0.05]), torch.linspace(-0.2, 0.2, K)):
+        got = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_ROWS,
+                              None if bias is None else bias.to(DEV)).cpu().numpy()
+        want = oracle.pack_rows(oracle.binarize(x, bias, channel_axis=-1), code)
+        np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(2, 3, 5, 5), (3, 37, 4, 4), (2, 64, 14, 14), (1, 130, 7, 9),
+                                   (4, 256, 3, 3)])
+def test_pack_nchw_to_nhwc(code, dtype, shape):
+    x = _gen(sum(shape), shape, dtype)
+    for bias in (None, torch.tensor([-0.1]), torch.linspace(-0.3, 0.3, shape[1])):
+        got = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC,
+                              None if bias is None else bias.to(DEV)).cpu().numpy()
+        want = oracle.pack_nchw_to_nhwc(oracle.binarize(x, bias, channel_axis=1), code)
+        np.testing.assert_array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# Linear
+# ---------------------------------------------------------------------------
+
+def gpu_linear(x, w, code, scale_a, scale_w, bias, out_dtype, algo=bt.BT_ALGO_AUTO):
+    wp = bt.bt_pack_sign(w.to(DEV), code)
+    y = bt.bt_binary_linear(x.to(DEV), wp, code, x.shape[1], scale_a, scale_w,
+                            None if bias is None else bias.to(DEV), out_dtype=OUT_T[out_dtype],
+                            algo=algo)
+    return y.cpu()
+
+
+LIN_SHAPES = [(1, 1, 1), (5, 7, 33), (130, 129, 257), (256, 384, 4100), (300, 200, 1000),
+              (129, 257, 96), (64, 256, 512), (17, 600, 2049)]
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("M,N,K", LIN_SHAPES)
+def test_linear_matches_oracle(code, M, N, K):
+    x = _gen(M + N + K, (M, K), torch.bfloat16)
+    w = _gen(M * N + K, (N, K), torch.bfloat16) * 0.02
+    bias = torch.tensor([0.03])
+    sa, sw = workloads.mean_abs(x), workloads.mean_abs(w)
+    for od in ("i32", "f32", "bf16", "f16"):
+        got = gpu_linear(x, w, code, sa, sw, bias, od)
+        want = oracle.binary_linear(x, w, sa, sw, bias, od)
+        assert_close_rel(got, want)
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+def test_linear_f32_input_per_column_bias(code):
+    M, N, K = 150, 140, 333
+    x = _gen(1, (M, K))
+    w = _gen(2, (N, K))
+    bias = torch.linspace(-0.5, 0.5, K)
+    got = gpu_linear(x, w, code, 0.75, 1.25, bias, "f32")
+    assert_close_rel(got, oracle.binary_linear(x, w, 0.75, 1.25, bias, "f32"))
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("K", [4096, 11008, 16384])
+def test_linear_extreme_sums_are_exact(code, K):
+    # rows equal to (or the negation of) weight rows drive every partial sum to
+    # its largest magnitude; dot must still be exactly +-K.
+    if code != bt.BT_CODE_BITS and K > 16384:
+        pytest.skip("beyond the tensor-core bound")
+    w = _gen(K, (128, K))
+    x = torch.cat([w[:64], -w[64:]])
+    x = torch.where(x == 0, torch.ones_like(x), x)
+    w = torch.where(w == 0, torch.ones_like(w), w)
+    got = gpu_linear(x, w, code, 1.0, 1.0, None, "i32")
+    want = oracle.linear_dot(oracle.binarize(x), oracle.binarize_weight(w))
+    assert torch.equal(got, torch.from_numpy(want))
+    d = got.diagonal()
+    assert (d[:64] == K).all() and (d[64:] == -K).all()
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+def test_linear_prepacked_input(code):
+    M, N, K = 200, 136, 700
+    x, w = _gen(3, (M, K)), _gen(4, (N, K))
+    xp = bt.bt_pack_sign(x.to(DEV), code)
+    wp = bt.bt_pack_sign(w.to(DEV), code)
+    y = bt.bt_binary_linear(xp, wp, code, K, 1.0, 1.0, out_dtype=torch.int32, x_packed=True).cpu()
+    want = oracle.linear_dot(oracle.binarize(x), oracle.binarize_weight(w))
+    assert torch.equal(y, torch.from_numpy(want))
+
+
+def test_linear_empty_and_errors():
+    w = bt.bt_pack_sign(torch.randn(8, 64, device=DEV), bt.BT_CODE_BITS)
+    y = bt.bt_binary_linear(torch.randn(0, 64, device=DEV), w, bt.BT_CODE_BITS, 64, 1.0, 1.0)
+    assert y.shape == (0, 8)
+    with pytest.raises(bt.BtError):
+        bt.bt_binary_linear(torch.randn(4, 64, device=DEV), w, bt.BT_CODE_BITS, 64, 0.0, 1.0)
+    with pytest.raises(bt.BtError):
+        bt.bt_binary_linear(torch.randn(4, 64, device=DEV), w, bt.BT_CODE_BITS, 64, 1.0, 1.0,
+                            algo=bt.BT_ALGO_TC_E2M1)
+
+
+# ---------------------------------------------------------------------------
+# Conv
+# ---------------------------------------------------------------------------
+
+def gpu_conv(x, w, code, s, p, d, scale_a, scale_w, bias, out_dtype):
+    wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    y = bt.bt_binary_conv2d(x.to(DEV), wp, code, x.shape[1], w.shape[2], s, p, d, scale_a, scale_w,
+                            None if bias is None else bias.to(DEV), out_dtype=OUT_T[out_dtype])
+    return y.cpu()
+
+
+CONV_SHAPES = [
+    # B, C, H, W, O, k, s, p, d
+    (2, 3, 5, 5, 4, 3, 1, 1, 1), (2, 70, 13, 13, 130, 3, 2, 1, 2), (1, 33, 9, 7, 5, 5, 3, 3, 1),
+    (3, 64, 14, 14, 129, 3, 1, 1, 1), (1, 256, 6, 6, 64, 3, 1, 1, 1), (2, 128, 11, 11, 40, 3, 2, 2, 2),
+    (1, 5, 1, 1, 3, 3, 1, 1, 1), (2, 31, 8, 8, 7, 1, 1, 0, 1), (1, 40, 12, 10, 33, 3, 2, 0, 1),
+]
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", CONV_SHAPES)
+def test_conv_matches_oracle(code, B, C, H, W, O, k, s, p, d):
+    x = _gen(B + C + H, (B, C, H, W), torch.bfloat16)
+    w = _gen(O + k, (O, C, k, k), torch.bfloat16)
+    bias = torch.linspace(-0.1, 0.1, C)
+    sa, sw = workloads.mean_abs(x), workloads.mean_abs(w)
+    for od in ("i32", "f32", "bf16"):
+        got = gpu_conv(x, w, code, s, p, d, sa, sw, bias, od)
+        want = oracle.binary_conv2d(x, w, sa, sw, s, p, d, bias, od)
+        assert_close_rel(got, want)
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+def test_conv_f32_scalar_bias(code):
+    x, w = _gen(5, (2, 48, 10, 10)), _gen(6, (24, 48, 3, 3))
+    bias = torch.tensor([0.2])
+    got = gpu_conv(x, w, code, 1, 1, 1, 0.5, 2.0, bias, "f32")
+    assert_close_rel(got, oracle.binary_conv2d(x, w, 0.5, 2.0, 1, 1, 1, bias, "f32"))
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times:
+# sampled outputs against the oracle, invariants over every output.
+# ---------------------------------------------------------------------------
+
+def _samples(rng, shape, n=1500):
+    idx = [rng.integers(0, s, n) for s in shape]
+    corners = np.array(np.meshgrid(*[[0, s - 1] for s in shape], indexing="ij")).reshape(len(shape), -1)
+    return [np.concatenate([i, c]) for i, c in zip(idx, corners)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("name", ["llm_linear", "large_linear", "ragged_linear", "tiny_linear"])
+def test_full_linear_workloads(code, name):
+    wl = workloads.NAMED[name]()
+    M, N, K = wl.gemm_shape()
+    wp = bt.bt_pack_sign(wl.w.to(DEV), code)
+    xd = wl.x.to(DEV)
+    bias = None if wl.bias is None else wl.bias.to(DEV)
+    dot = bt.bt_binary_linear(xd, wp, code, K, wl.scale_a, wl.scale_w, bias, out_dtype=torch.int32).cpu()
+    y = bt.bt_binary_linear(xd, wp, code, K, wl.scale_a, wl.scale_w, bias,
+                            out_dtype=OUT_T[wl.out_dtype]).cpu()
+    # invariants over every output
+    assert (dot.abs() <= K).all() and ((dot - K) % 2 == 0).all()
+    # sampled outputs against the oracle
+    sa = oracle.binarize(wl.x, wl.bias, channel_axis=-1)
+    sw = oracle.binarize_weight(wl.w)
+    rows, cols = _samples(np.random.default_rng(1), (M, N))
+    want = oracle.linear_dot_at(sa, sw, rows, cols)
+    np.testing.assert_array_equal(dot.numpy()[rows, cols], want)
+    assert_close_rel(y[rows, cols], oracle.epilogue(want, wl.scale_a, wl.scale_w, wl.out_dtype))
+    # the scaled output is the epilogue of the integer output everywhere
+    assert_close_rel(y, oracle.epilogue(dot.numpy(), wl.scale_a, wl.scale_w, wl.out_dtype))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("name", ["resnet_conv", "downsample_conv", "downsample_conv_d2"])
+def test_full_conv_workloads(code, name):
+    wl = workloads.NAMED[name]()
+    B, C, H, W = wl.x.shape
+    O, _, k, _ = wl.w.shape
+    wp = bt.bt_pack_sign(wl.w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    xd = wl.x.to(DEV)
+    args = (code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a, wl.scale_w, None)
+    dot = bt.bt_binary_conv2d(xd, wp, *args, out_dtype=torch.int32).cpu()
+    y = bt.bt_binary_conv2d(xd, wp, *args, out_dtype=OUT_T[wl.out_dtype]).cpu()
+    assert (dot.abs() <= C * k * k).all()
+    sa = oracle.binarize(wl.x)
+    sw = oracle.binarize_weight(wl.w)
+    b, o, i, j = _samples(np.random.default_rng(2), tuple(dot.shape))
+    flat = ((b * O + o) * dot.shape[2] + i) * dot.shape[3] + j
+    want = oracle.conv2d_dot_at(sa, sw, wl.stride, wl.padding, wl.dilation, flat)
+    np.testing.assert_array_equal(dot.numpy().reshape(-1)[flat], want)
+    assert_close_rel(y, oracle.epilogue(dot.numpy(), wl.scale_a, wl.scale_w, wl.out_dtype))

@@ -1,0 +1,216 @@
+"""Python binding of libbt, the binarized linear / conv2d forward for GB300.
+
+Argument marshalling only: every step of the forward runs in the CUDA
+kernels of ``_build/libbt.so`` (built from ``csrc/`` by ``build.py``). The
+functions keep the C names of ``include/bt.h`` and take torch CUDA tensors;
+torch supplies device memory and the current stream. A non-OK status raises
+``BtError``. If the library has not been built, importing this package raises:
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "BtError", "lib_path", "BT_F32", "BT_BF16", "BT_F16", "BT_I32", "BT_PACKED",
+    "BT_CODE_BITS", "BT_CODE_E4M3", "BT_CODE_E2M1", "BT_LAYOUT_ROWS", "BT_LAYOUT_NCHW_TO_NHWC",
+    "BT_ALGO_AUTO", "BT_ALGO_POPC", "BT_ALGO_TC_E4M3", "BT_ALGO_TC_E2M1", "BT_OP_LINEAR",
+    "BT_OP_CONV2D", "bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
+    "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
+    "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size",
+]
+
+BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_ALIGNMENT = 0, -1, -2, -3
+BT_ERR_WORKSPACE, BT_ERR_CUDA, BT_ERR_TIMEOUT = -4, -5, -6
+BT_F32, BT_BF16, BT_F16, BT_I32, BT_PACKED = 0, 1, 2, 3, 4
+BT_CODE_BITS, BT_CODE_E4M3, BT_CODE_E2M1 = 0, 1, 2
+BT_LAYOUT_ROWS, BT_LAYOUT_NCHW_TO_NHWC = 0, 1
+BT_ALGO_AUTO, BT_ALGO_POPC, BT_ALGO_TC_E4M3, BT_ALGO_TC_E2M1 = 0, 1, 2, 3
+BT_OP_LINEAR, BT_OP_CONV2D = 0, 1
+
+_DT = {torch.float32: BT_F32, torch.bfloat16: BT_BF16, torch.float16: BT_F16, torch.int32: BT_I32}
+_TORCH = {BT_F32: torch.float32, BT_BF16: torch.bfloat16, BT_F16: torch.float16, BT_I32: torch.int32}
+
+lib_path = _build.LIB
+if not os.path.exists(lib_path):
+    raise ImportError(f"libbt.so is not built ({lib_path}); run xnor_popcount_gemm_gb300.build.build()")
+
+_lib = ctypes.CDLL(lib_path)
+_i64, _p, _f, _i, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+
+
+def _sig(name, res, args):
+    fn = getattr(_lib, name)
+    fn.restype = res
+    fn.argtypes = args
+    return fn
+
+
+_c_version = _sig("bt_version", _i, [])
+_c_status_string = _sig("bt_status_string", ctypes.c_char_p, [_i])
+_c_row_bytes = _sig("bt_packed_row_bytes", _i64, [_i64, _i])
+_c_pack = _sig("bt_pack_sign", _i, [_p, _i, _i, _i64, _i64, _i64, _i64, _p, _i64, _i, _p, _p])
+_c_lin_ws = _sig("bt_binary_linear_workspace", _sz, [_i64, _i64, _i, _i])
+_c_lin = _sig("bt_binary_linear", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _i64, _p, _i, _i,
+                                       _p, _sz, _p])
+_c_conv_ws = _sig("bt_binary_conv2d_workspace", _sz, [_i64, _i64, _i64, _i64, _i, _i])
+_c_conv = _sig("bt_binary_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
+                                        _f, _f, _p, _i64, _p, _i, _i, _p, _sz, _p])
+_c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
+_c_status = _sig("bt_device_status", _i, [_p])
+
+#: every symbol include/bt.h declares
+EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
+            "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
+            "bt_binary_conv2d", "bt_plan", "bt_device_status"]
+
+
+class BtError(RuntimeError):
+    def __init__(self, status: int):
+        super().__init__(bt_status_string(status))
+        self.status = status
+
+
+def _check(st: int) -> None:
+    if st != BT_OK:
+        raise BtError(st)
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def bt_version() -> int:
+    return int(_c_version())
+
+
+def bt_status_string(status: int) -> str:
+    return _c_status_string(status).decode()
+
+
+def bt_packed_row_bytes(k: int, code: int) -> int:
+    return int(_c_row_bytes(k, code))
+
+
+def conv2d_out_size(h: int, k: int, s: int, p: int, d: int) -> int:
+    return (h + 2 * p - d * (k - 1) - 1) // s + 1
+
+
+def _contig(t: torch.Tensor, name: str) -> None:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def bt_pack_sign(x: torch.Tensor, code: int, layout: int = BT_LAYOUT_ROWS, bias=None,
+                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Shift + sign + pack. ROWS: x [R, K] -> uint8 [R, row_bytes(K)];
+    NCHW_TO_NHWC: x [B, C, H, W] -> uint8 [B, H, W, row_bytes(C)]."""
+    _contig(x, "x")
+    if layout == BT_LAYOUT_ROWS:
+        if x.dim() != 2:
+            raise ValueError("ROWS layout wants a 2-D x")
+        d = (x.shape[0], x.shape[1], 1, 1)
+        shape = (x.shape[0], bt_packed_row_bytes(x.shape[1], code))
+    else:
+        if x.dim() != 4:
+            raise ValueError("NCHW_TO_NHWC layout wants a 4-D x")
+        d = tuple(x.shape)
+        shape = (x.shape[0], x.shape[2], x.shape[3], bt_packed_row_bytes(x.shape[1], code))
+    if out is None:
+        out = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    blen = 0 if bias is None else bias.numel()
+    _check(_c_pack(_ptr(x), _DT[x.dtype], layout, *d, _ptr(bias), blen, code, _ptr(out), _stream(stream)))
+    return out
+
+
+def bt_binary_linear_workspace(M: int, K: int, x_dtype: int, code: int) -> int:
+    return int(_c_lin_ws(M, K, x_dtype, code))
+
+
+def bt_binary_conv2d_workspace(B: int, C: int, H: int, W: int, x_dtype: int, code: int) -> int:
+    return int(_c_conv_ws(B, C, H, W, x_dtype, code))
+
+
+def _workspace(nbytes: int, device, ws):
+    if nbytes == 0:
+        return None
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws
+
+
+def bt_binary_linear(x: torch.Tensor, weight: torch.Tensor, w_code: int, K: int, scale_a: float,
+                     scale_w: float, bias_a=None, out_dtype=None, algo: int = BT_ALGO_AUTO,
+                     x_packed: bool = False, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = cast(fp32(dot * fp32(scale_a*scale_w))) for x [M, K] (or packed rows)
+    and a packed weight [N, row_bytes(K)]."""
+    _contig(x, "x")
+    _contig(weight, "weight")
+    M, N = x.shape[0], weight.shape[0]
+    xt = BT_PACKED if x_packed else _DT[x.dtype]
+    if out_dtype is None:
+        out_dtype = x.dtype if not x_packed else torch.float32
+    ot = _DT[out_dtype]
+    if out is None:
+        out = torch.empty((M, N), dtype=_TORCH[ot], device=x.device)
+    ws = _workspace(bt_binary_linear_workspace(M, K, xt, w_code), x.device, workspace)
+    blen = 0 if bias_a is None else bias_a.numel()
+    _check(_c_lin(_ptr(x), xt, _ptr(weight), w_code, M, N, K, scale_a, scale_w, _ptr(bias_a), blen,
+                  _ptr(out), ot, algo, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def bt_binary_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int, kernel_size: int,
+                     stride: int, padding: int, dilation: int, scale_a: float, scale_w: float,
+                     bias_a=None, out_dtype=None, algo: int = BT_ALGO_AUTO, x_packed: bool = False,
+                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """NCHW x [B, C, H, W] (or packed NHWC [B, H, W, row_bytes(C)]) with a
+    packed weight [O, k, k, row_bytes(C)] -> NCHW [B, O, Ho, Wo]."""
+    _contig(x, "x")
+    _contig(weight, "weight")
+    if x_packed:
+        B, H, W = x.shape[0], x.shape[1], x.shape[2]
+    else:
+        B, C2, H, W = x.shape
+        if C2 != C:
+            raise ValueError("C does not match x")
+    O = weight.shape[0]
+    xt = BT_PACKED if x_packed else _DT[x.dtype]
+    if out_dtype is None:
+        out_dtype = x.dtype if not x_packed else torch.float32
+    ot = _DT[out_dtype]
+    Ho = conv2d_out_size(H, kernel_size, stride, padding, dilation)
+    Wo = conv2d_out_size(W, kernel_size, stride, padding, dilation)
+    if out is None:
+        out = torch.empty((B, O, max(Ho, 0), max(Wo, 0)), dtype=_TORCH[ot], device=x.device)
+    ws = _workspace(bt_binary_conv2d_workspace(B, C, H, W, xt, w_code), x.device, workspace)
+    blen = 0 if bias_a is None else bias_a.numel()
+    _check(_c_conv(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding,
+                   dilation, scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),
+                   0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def bt_plan(op: int, M: int, N: int, K: int) -> tuple[int, int]:
+    """The (code, algo) the library runs fastest for this problem size."""
+    code, algo = _i(0), _i(0)
+    _check(_c_plan(op, M, N, K, ctypes.byref(code), ctypes.byref(algo)))
+    return code.value, algo.value
+
+
+def bt_device_status(stream=None) -> int:
+    """Synchronize the stream; return (and clear) the device error status."""
+    return int(_c_status(_stream(stream)))

@@ -1,0 +1,240 @@
+// The C ABI of libbt (declared in include/bt.h): argument validation, the
+// pack -> contract dispatch, the "ADAPTIVE" planner and the device error word.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "bt_device.cuh"
+#include "bt_internal.h"
+
+namespace bt {
+
+__device__ unsigned int g_error_word;
+
+unsigned int *device_error_word() {
+    static std::mutex mu;
+    static unsigned int *ptrs[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned int *>(p);
+    }
+    return ptrs[dev];
+}
+
+namespace {
+
+bool valid_code(int c) { return c == BT_CODE_BITS || c == BT_CODE_E4M3 || c == BT_CODE_E2M1; }
+bool float_in(int t) { return t == BT_F32 || t == BT_BF16 || t == BT_F16; }
+bool valid_out(int t) { return t == BT_F32 || t == BT_BF16 || t == BT_F16 || t == BT_I32; }
+bool valid_scale(float v) { return std::isfinite(v) && v > 0.0f; }
+
+bt_algo algo_for_code(bt_code c) {
+    switch (c) {
+        case BT_CODE_BITS: return BT_ALGO_POPC;
+        case BT_CODE_E4M3: return BT_ALGO_TC_E4M3;
+        default: return BT_ALGO_TC_E2M1;
+    }
+}
+
+// alpha = fp32(scale_a * scale_w): the product of two floats is exact in
+// double; one rounding to float.
+float alpha_of(float sa, float sw) {
+    return static_cast<float>(static_cast<double>(sa) * static_cast<double>(sw));
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bt_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BT_OK : BT_ERR_CUDA; }
+
+int64_t conv_out(int64_t h, int64_t k, int64_t s, int64_t p, int64_t d) {
+    const int64_t num = h + 2 * p - d * (k - 1) - 1;
+    return num < 0 ? 0 : num / s + 1;
+}
+
+// Largest reduction length whose dot fits exactly in an fp32 (|dot| <= 2^24).
+constexpr int64_t kMaxK = int64_t(1) << 24;
+
+}  // namespace
+}  // namespace bt
+
+using namespace bt;
+
+extern "C" {
+
+int bt_version(void) { return 100; }
+
+const char *bt_status_string(bt_status s) {
+    switch (s) {
+        case BT_OK: return "BT_OK";
+        case BT_ERR_INVALID_ARG: return "BT_ERR_INVALID_ARG: invalid argument";
+        case BT_ERR_UNSUPPORTED: return "BT_ERR_UNSUPPORTED: unsupported combination";
+        case BT_ERR_ALIGNMENT: return "BT_ERR_ALIGNMENT: pointer not aligned (16 B; workspace 256 B)";
+        case BT_ERR_WORKSPACE: return "BT_ERR_WORKSPACE: workspace missing or too small";
+        case BT_ERR_CUDA: return "BT_ERR_CUDA: CUDA error";
+        case BT_ERR_TIMEOUT: return "BT_ERR_TIMEOUT: a kernel's bounded wait ran out";
+        default: return "unknown bt_status";
+    }
+}
+
+int64_t bt_packed_row_bytes(int64_t k, bt_code code) {
+    if (k < 0 || !valid_code(code)) return -1;
+    return row_bytes(k, code);
+}
+
+bt_status bt_pack_sign(const void *x, bt_dtype x_dtype, bt_layout layout, int64_t d0, int64_t d1,
+                       int64_t d2, int64_t d3, const float *bias, int64_t bias_len, bt_code code,
+                       void *out, bt_stream stream) {
+    if (!valid_code(code) || !float_in(x_dtype)) return BT_ERR_INVALID_ARG;
+    if (layout != BT_LAYOUT_ROWS && layout != BT_LAYOUT_NCHW_TO_NHWC) return BT_ERR_INVALID_ARG;
+    if (d0 < 0 || d1 < 1) return BT_ERR_INVALID_ARG;
+    if (layout == BT_LAYOUT_NCHW_TO_NHWC && (d2 < 1 || d3 < 1)) return BT_ERR_INVALID_ARG;
+    if (!(bias_len == 0 || bias_len == 1 || bias_len == d1)) return BT_ERR_INVALID_ARG;
+    if (bias_len > 0 && bias == nullptr) return BT_ERR_INVALID_ARG;
+    if (d0 == 0) return BT_OK;
+    if (x == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4))) return BT_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (layout == BT_LAYOUT_ROWS)
+        return from_cuda(launch_pack_rows(x, x_dtype, d0, d1, bias, bias_len, code, out, s));
+    return from_cuda(launch_pack_nhwc(x, x_dtype, d0, d1, d2 * d3, bias, bias_len, code, out, s));
+}
+
+size_t bt_binary_linear_workspace(int64_t M, int64_t K, bt_dtype x_dtype, bt_code code) {
+    if (M < 0 || K < 1 || !valid_code(code) || x_dtype == BT_PACKED) return 0;
+    return round_up(static_cast<size_t>(M) * static_cast<size_t>(row_bytes(K, code)), 256);
+}
+
+bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                           int64_t M, int64_t N, int64_t K, float scale_a, float scale_w,
+                           const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
+                           bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+    if (!valid_code(w_code) || !valid_out(out_dtype)) return BT_ERR_INVALID_ARG;
+    if (!(float_in(x_dtype) || x_dtype == BT_PACKED)) return BT_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 1) return BT_ERR_INVALID_ARG;
+    if (!valid_scale(scale_a) || !valid_scale(scale_w)) return BT_ERR_INVALID_ARG;
+    if (!(bias_len == 0 || bias_len == 1 || bias_len == K)) return BT_ERR_INVALID_ARG;
+    if (bias_len > 0 && bias_a == nullptr && x_dtype != BT_PACKED) return BT_ERR_INVALID_ARG;
+    if (algo != BT_ALGO_AUTO && algo != algo_for_code(w_code)) {
+        if (algo < BT_ALGO_AUTO || algo > BT_ALGO_TC_E2M1) return BT_ERR_INVALID_ARG;
+        return BT_ERR_UNSUPPORTED;
+    }
+    if (K > kMaxK) return BT_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return BT_OK;
+    if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16)) return BT_ERR_ALIGNMENT;
+    if ((M + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
+    const bt_algo run = algo_for_code(w_code);
+    if (run != BT_ALGO_POPC && K > kTcMaxK) return BT_ERR_UNSUPPORTED;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const void *xp = x;
+    if (x_dtype != BT_PACKED) {
+        const size_t need = bt_binary_linear_workspace(M, K, x_dtype, w_code);
+        if (workspace == nullptr || workspace_bytes < need) return BT_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
+        cudaError_t e = launch_pack_rows(x, x_dtype, M, K, bias_a, bias_len, w_code, workspace, s);
+        if (e != cudaSuccess) return BT_ERR_CUDA;
+        xp = workspace;
+    }
+    const float alpha = alpha_of(scale_a, scale_w);
+    if (run == BT_ALGO_POPC)
+        return from_cuda(launch_popc_linear(static_cast<const uint32_t *>(xp),
+                                            static_cast<const uint32_t *>(weight), M, N, K, alpha, out,
+                                            out_dtype, s));
+    unsigned int *err = device_error_word();
+    if (err == nullptr) return BT_ERR_CUDA;
+    return from_cuda(launch_tc_linear(static_cast<const uint8_t *>(xp), static_cast<const uint8_t *>(weight),
+                                      w_code, M, N, K, alpha, out, out_dtype, err, s));
+}
+
+size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, bt_dtype x_dtype,
+                                  bt_code code) {
+    if (B < 0 || C < 1 || H < 1 || W < 1 || !valid_code(code) || x_dtype == BT_PACKED) return 0;
+    return round_up(static_cast<size_t>(B) * H * W * static_cast<size_t>(row_bytes(C, code)), 256);
+}
+
+bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                           int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,
+                           int stride, int padding, int dilation, float scale_a, float scale_w,
+                           const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
+                           bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+    if (!valid_code(w_code) || !valid_out(out_dtype)) return BT_ERR_INVALID_ARG;
+    if (!(float_in(x_dtype) || x_dtype == BT_PACKED)) return BT_ERR_INVALID_ARG;
+    if (B < 0 || C < 1 || H < 1 || W < 1 || O < 0) return BT_ERR_INVALID_ARG;
+    if (kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return BT_ERR_INVALID_ARG;
+    if (!valid_scale(scale_a) || !valid_scale(scale_w)) return BT_ERR_INVALID_ARG;
+    if (!(bias_len == 0 || bias_len == 1 || bias_len == C)) return BT_ERR_INVALID_ARG;
+    if (bias_len > 0 && bias_a == nullptr && x_dtype != BT_PACKED) return BT_ERR_INVALID_ARG;
+    if (algo != BT_ALGO_AUTO && algo != algo_for_code(w_code)) {
+        if (algo < BT_ALGO_AUTO || algo > BT_ALGO_TC_E2M1) return BT_ERR_INVALID_ARG;
+        return BT_ERR_UNSUPPORTED;
+    }
+    ConvGeom g{B, C, H, W, O, 0, 0, kernel_size, stride, padding, dilation};
+    g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
+    g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
+    if (g.Ho < 1 || g.Wo < 1) return BT_ERR_INVALID_ARG;
+    const int64_t kk = static_cast<int64_t>(kernel_size) * kernel_size;
+    if (C * kk > kMaxK || H > (1 << 20) || W > (1 << 20) || kernel_size > 64 || padding > (1 << 20) ||
+        stride > (1 << 20) || dilation > (1 << 10))
+        return BT_ERR_UNSUPPORTED;
+    if (B == 0 || O == 0) return BT_OK;
+    if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16)) return BT_ERR_ALIGNMENT;
+    const int64_t M = B * g.Ho * g.Wo;
+    if ((M + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
+    const bt_algo run = algo_for_code(w_code);
+    if (run != BT_ALGO_POPC && C * kk > kTcMaxK) return BT_ERR_UNSUPPORTED;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const void *xp = x;
+    if (x_dtype != BT_PACKED) {
+        const size_t need = bt_binary_conv2d_workspace(B, C, H, W, x_dtype, w_code);
+        if (workspace == nullptr || workspace_bytes < need) return BT_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
+        cudaError_t e = launch_pack_nhwc(x, x_dtype, B, C, H * W, bias_a, bias_len, w_code, workspace, s);
+        if (e != cudaSuccess) return BT_ERR_CUDA;
+        xp = workspace;
+    }
+    const float alpha = alpha_of(scale_a, scale_w);
+    if (run == BT_ALGO_POPC)
+        return from_cuda(launch_popc_conv(static_cast<const uint32_t *>(xp), static_cast<const uint32_t *>(weight),
+                                          g, alpha, out, out_dtype, s));
+    unsigned int *err = device_error_word();
+    if (err == nullptr) return BT_ERR_CUDA;
+    return from_cuda(launch_tc_conv(static_cast<const uint8_t *>(xp), static_cast<const uint8_t *>(weight), w_code,
+                                    g, alpha, out, out_dtype, err, s));
+}
+
+bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo) {
+    if (code == nullptr || algo == nullptr || M < 1 || N < 1 || K < 1) return BT_ERR_INVALID_ARG;
+    if (op != BT_OP_LINEAR && op != BT_OP_CONV2D) return BT_ERR_INVALID_ARG;
+    bt_code c = BT_CODE_BITS;
+    const char *force = std::getenv("BT_FORCE_ALGO");
+    if (force != nullptr && std::strcmp(force, "popc") == 0) c = BT_CODE_BITS;
+    else if (force != nullptr && std::strcmp(force, "e4m3") == 0) c = BT_CODE_E4M3;
+    else if (force != nullptr && std::strcmp(force, "e2m1") == 0) c = BT_CODE_E2M1;
+    else c = (K <= kTcMaxK && tc_available()) ? BT_CODE_E2M1 : BT_CODE_BITS;
+    *code = c;
+    *algo = algo_for_code(c);
+    return BT_OK;
+}
+
+bt_status bt_device_status(bt_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BT_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return BT_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return BT_ERR_CUDA;
+        return BT_ERR_TIMEOUT;
+    }
+    return BT_OK;
+}
+
+}  // extern "C"

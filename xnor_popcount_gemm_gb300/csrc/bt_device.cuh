@@ -1,0 +1,130 @@
+// Device-side helpers shared by the kernels of libbt.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "bt.h"
+
+namespace bt {
+
+// Error-word bits. A kernel ORs one in and returns; it never traps.
+constexpr unsigned int kErrTimeout = 1u;
+
+// ---------------------------------------------------------------------------
+// Binarization: +1 where x + bias >= 0. The fp32 sum is exact in sign (without
+// flushing subnormals, the exact sum of two floats never rounds to zero), so
+// this is the sign of the exact sum; -0.0 gives +1, NaN gives -1.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t sign_bit(float v, float b) {
+    return __fadd_rn(v, b) >= 0.0f ? 1u : 0u;
+}
+
+// Codes of +1 / -1.
+constexpr uint32_t kE4M3Plus = 0x38u, kE4M3Minus = 0xB8u;
+constexpr uint32_t kE2M1Plus = 0x2u, kE2M1Minus = 0xAu;
+
+__device__ __forceinline__ uint32_t e4m3_code(uint32_t bit) { return bit ? kE4M3Plus : kE4M3Minus; }
+__device__ __forceinline__ uint32_t e2m1_code(uint32_t bit) { return bit ? kE2M1Plus : kE2M1Minus; }
+
+// Element loads converted exactly to fp32.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kPerVec = 4;
+    __device__ __forceinline__ static float to_f32(float v) { return v; }
+    __device__ __forceinline__ static void unpack(const uint4 &q, float *f) {
+        f[0] = __uint_as_float(q.x); f[1] = __uint_as_float(q.y);
+        f[2] = __uint_as_float(q.z); f[3] = __uint_as_float(q.w);
+    }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kPerVec = 8;
+    __device__ __forceinline__ static float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ __forceinline__ static void unpack(const uint4 &q, float *f) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+};
+template <> struct Elem<__half> {
+    static constexpr int kPerVec = 8;
+    __device__ __forceinline__ static float to_f32(__half v) { return __half2float(v); }
+    __device__ __forceinline__ static void unpack(const uint4 &q, float *f) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 t = __half22float2(h);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+};
+
+// Streaming 16-byte load (read once, do not keep in L1).
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue: y = fp32(dot * alpha) (one rounding), cast to the output type.
+// ---------------------------------------------------------------------------
+template <int OUT> struct OutT;
+template <> struct OutT<BT_F32> {
+    using type = float;
+    __device__ __forceinline__ static float cvt(int dot, float alpha) {
+        return __fmul_rn(static_cast<float>(dot), alpha);
+    }
+};
+template <> struct OutT<BT_BF16> {
+    using type = __nv_bfloat16;
+    __device__ __forceinline__ static __nv_bfloat16 cvt(int dot, float alpha) {
+        return __float2bfloat16_rn(__fmul_rn(static_cast<float>(dot), alpha));
+    }
+};
+template <> struct OutT<BT_F16> {
+    using type = __half;
+    __device__ __forceinline__ static __half cvt(int dot, float alpha) {
+        return __float2half_rn(__fmul_rn(static_cast<float>(dot), alpha));
+    }
+};
+template <> struct OutT<BT_I32> {
+    using type = int;
+    __device__ __forceinline__ static int cvt(int dot, float) { return dot; }
+};
+
+// ---------------------------------------------------------------------------
+// Bounded waiting. Every spin in these kernels gives up after kWaitNs of
+// %globaltimer time, records kErrTimeout and lets the kernel return.
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// cp.async (16 bytes, zero-filled when src_bytes == 0)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem_dst)),
+                 "l"(gmem_src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+}  // namespace bt

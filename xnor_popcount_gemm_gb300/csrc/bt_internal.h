@@ -1,0 +1,70 @@
+// Host-side declarations shared by the translation units of libbt.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "bt.h"
+
+namespace bt {
+
+// Element and code helpers --------------------------------------------------
+inline int dtype_bytes(bt_dtype t) {
+    switch (t) {
+        case BT_F32: case BT_I32: return 4;
+        case BT_BF16: case BT_F16: return 2;
+        default: return 0;
+    }
+}
+
+inline int64_t row_bytes(int64_t k, bt_code code) {
+    int64_t nb;
+    switch (code) {
+        case BT_CODE_BITS: nb = ((k + 31) / 32) * 4; break;
+        case BT_CODE_E4M3: nb = k; break;
+        case BT_CODE_E2M1: nb = (k + 1) / 2; break;
+        default: return -1;
+    }
+    return (nb + 15) / 16 * 16;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device error word of the current device (a static __device__ variable,
+// address looked up once per device). Returns nullptr on a CUDA error.
+unsigned int *device_error_word();
+
+// Launchers (enqueue only; the caller has validated every argument) ---------
+cudaError_t launch_pack_rows(const void *x, bt_dtype xt, int64_t R, int64_t K, const float *bias,
+                             int64_t bias_len, bt_code code, void *out, cudaStream_t s);
+cudaError_t launch_pack_nhwc(const void *x, bt_dtype xt, int64_t B, int64_t C, int64_t HW,
+                             const float *bias, int64_t bias_len, bt_code code, void *out,
+                             cudaStream_t s);
+
+struct ConvGeom {
+    int64_t B, C, H, W, O, Ho, Wo;
+    int k, s, p, d;
+};
+
+cudaError_t launch_popc_linear(const uint32_t *xp, const uint32_t *wp, int64_t M, int64_t N,
+                               int64_t K, float alpha, void *out, bt_dtype out_t, cudaStream_t s);
+cudaError_t launch_popc_conv(const uint32_t *xp, const uint32_t *wp, const ConvGeom &g, float alpha,
+                             void *out, bt_dtype out_t, cudaStream_t s);
+
+cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M,
+                             int64_t N, int64_t K, float alpha, void *out, bt_dtype out_t,
+                             unsigned int *err, cudaStream_t s);
+cudaError_t launch_tc_conv(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g,
+                           float alpha, void *out, bt_dtype out_t, unsigned int *err,
+                           cudaStream_t s);
+
+// True when this build carries the tensor-core kernels.
+bool tc_available();
+
+// Largest K (elements) for which the tensor-core kernels are used: a bound on
+// the magnitude of the fp32 partial sums they accumulate.
+constexpr int64_t kTcMaxK = 16384;
+
+}  // namespace bt
