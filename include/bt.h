@@ -67,9 +67,10 @@ typedef enum {
 
 /*
  * Packed operand encodings ("bit-packing" of bitorch-engine's w_pack /
- * generate_quantized_weight, there with 8-bit words; here with a 16-byte row
- * pitch). A packed row of k elements occupies bt_packed_row_bytes(k, code)
- * bytes; every position after the last element is 0.
+ * generate_quantized_weight, there with 8-bit words). A packed row of k
+ * elements occupies bt_packed_row_bytes(k, code) bytes (BITS: rounded up to
+ * 16 bytes; E4M3 / E2M1: rounded up to 64 bytes); every position after the
+ * last element is 0.
  *
  *   BT_CODE_BITS  1 bit per element in little-endian uint32 words: bit j of
  *                 word w holds element 32*w + j; 1 means +1, 0 means -1.
@@ -113,8 +114,8 @@ int bt_version(void);
 /* Static text for a status code; never NULL. */
 const char *bt_status_string(bt_status status);
 
-/* Bytes of one packed row of k elements in `code` (rounded up to 16 bytes);
- * -1 for k < 0 or an unknown code. */
+/* Bytes of one packed row of k elements in `code` (BITS: a multiple of 16;
+ * E4M3 / E2M1: a multiple of 64); -1 for k < 0 or an unknown code. */
 int64_t bt_packed_row_bytes(int64_t k, bt_code code);
 
 /*

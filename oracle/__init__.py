@@ -264,16 +264,15 @@ CODE_BITS, CODE_E4M3, CODE_E2M1 = 0, 1, 2
 
 
 def packed_row_bytes(k: int, code: int) -> int:
-    """Bytes per packed row of ``k`` elements: rounded up to 16 bytes."""
+    """Bytes per packed row of ``k`` elements: BITS rows rounded up to 16
+    bytes, E4M3 / E2M1 rows to 64 bytes."""
     if code == CODE_BITS:
-        nbytes = ((k + 31) // 32) * 4
-    elif code == CODE_E4M3:
-        nbytes = k
-    elif code == CODE_E2M1:
-        nbytes = (k + 1) // 2
-    else:
-        raise ValueError(code)
-    return (nbytes + 15) // 16 * 16
+        return (((k + 31) // 32) * 4 + 15) // 16 * 16
+    if code == CODE_E4M3:
+        return (k + 63) // 64 * 64
+    if code == CODE_E2M1:
+        return ((k + 1) // 2 + 63) // 64 * 64
+    raise ValueError(code)
 
 
 def pack_rows(s: np.ndarray, code: int) -> np.ndarray:

@@ -9,3 +9,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: full-size workloads")
+    # build the CUDA library (nvcc cross-compiles without a GPU) and the C
+    # oracle before any test module imports them
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    import oracle
+    oracle.build()

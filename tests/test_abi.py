@@ -8,11 +8,9 @@ import re
 import pytest
 import torch
 
-from xnor_popcount_gemm_gb300 import build as bt_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-bt_build.build()
-import xnor_popcount_gemm_gb300 as bt  # noqa: E402
+import xnor_popcount_gemm_gb300 as bt
 
 
 def declared_functions():
@@ -40,8 +38,8 @@ def test_version_and_status_strings():
 
 @pytest.mark.parametrize("k,code,want", [
     (1, 0, 16), (32, 0, 16), (128, 0, 16), (129, 0, 32), (4096, 0, 512), (4100, 0, 528),
-    (1, 1, 16), (16, 1, 16), (17, 1, 32), (4100, 1, 4112),
-    (1, 2, 16), (32, 2, 16), (33, 2, 32), (4100, 2, 2064), (11008, 2, 5504),
+    (1, 1, 64), (64, 1, 64), (65, 1, 128), (4100, 1, 4160),
+    (1, 2, 64), (128, 2, 64), (129, 2, 128), (4100, 2, 2112), (11008, 2, 5504), (256, 2, 128),
 ])
 def test_packed_row_bytes(k, code, want):
     assert bt.bt_packed_row_bytes(k, code) == want
@@ -58,6 +56,8 @@ def test_workspace_queries():
     assert bt.bt_binary_linear_workspace(10, 10, bt.BT_PACKED, bt.BT_CODE_BITS) == 0
     assert bt.bt_binary_conv2d_workspace(2, 256, 14, 14, bt.BT_F32, bt.BT_CODE_E2M1) == \
         2 * 14 * 14 * 128
+    assert bt.bt_binary_conv2d_workspace(2, 128, 14, 14, bt.BT_F32, bt.BT_CODE_E2M1) == \
+        2 * 14 * 14 * 64
     assert bt.bt_binary_conv2d_workspace(1, 1, 1, 1, bt.BT_F32, bt.BT_CODE_BITS) == 256
 
 

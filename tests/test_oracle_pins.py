@@ -65,7 +65,7 @@ def test_golden_pack():
         code = {"e4m3": oracle.CODE_E4M3, "e2m1": oracle.CODE_E2M1}[ex["code"]]
         got = oracle.pack_rows(np.array([ex["signs"]], np.int8), code)[0]
         n = len(ex["bytes"])
-        assert got.size == 16
+        assert got.size == 64
         np.testing.assert_array_equal(got[:n], np.array(ex["bytes"], np.uint8), ex["why"])
         assert not got[n:].any()
 

@@ -13,10 +13,8 @@ import torch
 
 import oracle
 import workloads
-from xnor_popcount_gemm_gb300 import build as bt_build
 
-bt_build.build()
-import xnor_popcount_gemm_gb300 as bt  # noqa: E402
+import xnor_popcount_gemm_gb300 as bt
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"

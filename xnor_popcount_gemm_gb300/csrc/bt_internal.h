@@ -19,15 +19,15 @@ inline int dtype_bytes(bt_dtype t) {
     }
 }
 
+// Bytes of one packed row: BITS rows round up to 16 bytes; E4M3 / E2M1 rows
+// to 64 bytes, so that a row splits into whole 64- or 128-byte swizzle rows.
 inline int64_t row_bytes(int64_t k, bt_code code) {
-    int64_t nb;
     switch (code) {
-        case BT_CODE_BITS: nb = ((k + 31) / 32) * 4; break;
-        case BT_CODE_E4M3: nb = k; break;
-        case BT_CODE_E2M1: nb = (k + 1) / 2; break;
+        case BT_CODE_BITS: return (((k + 31) / 32) * 4 + 15) / 16 * 16;
+        case BT_CODE_E4M3: return (k + 63) / 64 * 64;
+        case BT_CODE_E2M1: return ((k + 1) / 2 + 63) / 64 * 64;
         default: return -1;
     }
-    return (nb + 15) / 16 * 16;
 }
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
