@@ -200,6 +200,37 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype,
                            void *workspace, size_t workspace_bytes, bt_stream stream);
 
 /*
+ * bt_binary_linear_noalloc -- bt_binary_linear for callers that cannot
+ * allocate device memory. The pages have no counterpart: it exists because
+ * some callers run inside a host framework that owns every device
+ * allocation (a plugin's enqueue callback, say) or under a fixed memory
+ * budget, where the workspace bt_binary_linear needs cannot be obtained.
+ *
+ * Same arguments and result as bt_binary_linear without the workspace: the
+ * packed activations go to a scratch array of
+ * bt_binary_linear_noalloc_max_bytes() bytes (16 MiB) compiled into the
+ * library, held in device memory of every GPU that loads it until the
+ * process exits. Calls allocate nothing (no cudaMalloc / cudaFree).
+ *   - A problem whose bt_binary_linear_workspace(M, K, x_dtype, w_code)
+ *     exceeds that size returns BT_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls whose kernels overlap on the
+ *     GPU race on it. Each call rewrites all of the scratch it reads, so
+ *     nothing carries over from the previous call.
+ */
+bt_status bt_binary_linear_noalloc(const void *x, bt_dtype x_dtype,
+                                   const void *weight, bt_code w_code,
+                                   int64_t M, int64_t N, int64_t K,
+                                   float scale_a, float scale_w,
+                                   const float *bias_a, int64_t bias_len,
+                                   void *out, bt_dtype out_dtype, bt_algo algo,
+                                   bt_stream stream);
+
+/* Size in bytes of the scratch array bt_binary_linear_noalloc uses. */
+size_t bt_binary_linear_noalloc_max_bytes(void);
+
+/*
  * bt_plan -- the "ADAPTIVE" choice: the code (weight format) and kernel this
  * build runs fastest for a problem of this size, from measurements on GB300.
  * For BT_OP_LINEAR pass (M, N, K); for BT_OP_CONV2D pass M = B*Ho*Wo, N = O,

@@ -22,7 +22,8 @@ __all__ = [
     "BT_ALGO_AUTO", "BT_ALGO_POPC", "BT_ALGO_TC_E4M3", "BT_ALGO_TC_E2M1", "BT_OP_LINEAR",
     "BT_OP_CONV2D", "bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
-    "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size",
+    "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
+    "bt_binary_linear_noalloc_max_bytes",
 ]
 
 BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_ALIGNMENT = 0, -1, -2, -3
@@ -61,13 +62,17 @@ _c_lin = _sig("bt_binary_linear", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f,
 _c_conv_ws = _sig("bt_binary_conv2d_workspace", _sz, [_i64, _i64, _i64, _i64, _i, _i])
 _c_conv = _sig("bt_binary_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
                                         _f, _f, _p, _i64, _p, _i, _i, _p, _sz, _p])
+_c_lin_noalloc = _sig("bt_binary_linear_noalloc", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _i64,
+                                                      _p, _i, _i, _p])
+_c_noalloc_max = _sig("bt_binary_linear_noalloc_max_bytes", _sz, [])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
 _c_status = _sig("bt_device_status", _i, [_p])
 
 #: every symbol include/bt.h declares
 EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
             "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
-            "bt_binary_conv2d", "bt_plan", "bt_device_status"]
+            "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
+            "bt_binary_linear_noalloc_max_bytes"]
 
 
 class BtError(RuntimeError):
@@ -201,6 +206,32 @@ def bt_binary_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int,
     _check(_c_conv(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding,
                    dilation, scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),
                    0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def bt_binary_linear_noalloc_max_bytes() -> int:
+    return int(_c_noalloc_max())
+
+
+def bt_binary_linear_noalloc(x: torch.Tensor, weight: torch.Tensor, w_code: int, K: int, scale_a: float,
+                             scale_w: float, bias_a=None, out_dtype=None, algo: int = BT_ALGO_AUTO,
+                             x_packed: bool = False, out: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """bt_binary_linear without a workspace: for callers that cannot allocate
+    device memory (the packed activations go to the library's fixed scratch
+    array). Only `out`, if not given, is allocated here, by torch."""
+    _contig(x, "x")
+    _contig(weight, "weight")
+    M, N = x.shape[0], weight.shape[0]
+    xt = BT_PACKED if x_packed else _DT[x.dtype]
+    if out_dtype is None:
+        out_dtype = x.dtype if not x_packed else torch.float32
+    ot = _DT[out_dtype]
+    if out is None:
+        out = torch.empty((M, N), dtype=_TORCH[ot], device=x.device)
+    blen = 0 if bias_a is None else bias_a.numel()
+    _check(_c_lin_noalloc(_ptr(x), xt, _ptr(weight), w_code, M, N, K, scale_a, scale_w, _ptr(bias_a), blen,
+                          _ptr(out), ot, algo, _stream(stream)))
     return out
 
 
