@@ -251,3 +251,40 @@ def test_full_conv_workloads(code, name):
     want = oracle.conv2d_dot_at(sa, sw, wl.stride, wl.padding, wl.dilation, flat)
     np.testing.assert_array_equal(dot.numpy().reshape(-1)[flat], want)
     assert_close_rel(y, oracle.epilogue(dot.numpy(), wl.scale_a, wl.scale_w, wl.out_dtype))
+
+
+# ---------------------------------------------------------------------------
+# Every tile / cluster configuration of the tensor-core kernel (the planner
+# picks one per shape; BT_TC_CONFIG="cm,cn,bn" forces it): cm CTAs share each
+# B slice, cn CTAs share each A slice (TMA multicast inside a cluster).
+# ---------------------------------------------------------------------------
+
+TC_CONFIGS = ["1,1,64", "2,1,64", "1,2,64", "2,2,64", "2,2,160", "2,1,224", "1,2,96"]
+TC_CODES = [bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
+
+
+@pytest.mark.parametrize("cfg", TC_CONFIGS)
+@pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
+def test_linear_tc_configs(cfg, code, monkeypatch):
+    monkeypatch.setenv("BT_TC_CONFIG", cfg)
+    for (M, N, K) in ((700, 600, 1000), (1100, 330, 4100)):
+        x = _gen(M + K, (M, K), torch.bfloat16)
+        w = _gen(N + K, (N, K), torch.bfloat16)
+        sa, sw = workloads.mean_abs(x), workloads.mean_abs(w)
+        want_dot = oracle.linear_dot(oracle.binarize(x), oracle.binarize_weight(w))
+        got = gpu_linear(x, w, code, sa, sw, None, "i32")
+        assert torch.equal(got, torch.from_numpy(want_dot)), (cfg, M, N, K)
+        got = gpu_linear(x, w, code, sa, sw, None, "bf16")
+        assert_close_rel(got, oracle.epilogue(want_dot, sa, sw, "bf16"))
+
+
+@pytest.mark.parametrize("cfg", TC_CONFIGS)
+@pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
+def test_conv_tc_configs(cfg, code, monkeypatch):
+    monkeypatch.setenv("BT_TC_CONFIG", cfg)
+    for (B, C, H, W, O, k, s, p, d) in ((3, 128, 14, 14, 200, 3, 1, 1, 1), (4, 64, 15, 13, 70, 3, 2, 2, 2)):
+        x = _gen(B + C, (B, C, H, W), torch.bfloat16)
+        w = _gen(O + C, (O, C, k, k), torch.bfloat16)
+        want = oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d)
+        got = gpu_conv(x, w, code, s, p, d, 1.0, 1.0, None, "i32")
+        assert torch.equal(got, torch.from_numpy(want)), (cfg, B, C, H, W, O)

@@ -95,6 +95,9 @@ bt_status bt_pack_sign(const void *x, bt_dtype x_dtype, bt_layout layout, int64_
     if (layout == BT_LAYOUT_NCHW_TO_NHWC && (d2 < 1 || d3 < 1)) return BT_ERR_INVALID_ARG;
     if (!(bias_len == 0 || bias_len == 1 || bias_len == d1)) return BT_ERR_INVALID_ARG;
     if (bias_len > 0 && bias == nullptr) return BT_ERR_INVALID_ARG;
+    if (d1 > (int64_t(1) << 30) || (layout == BT_LAYOUT_NCHW_TO_NHWC && (d2 * d3 > (int64_t(1) << 30) ||
+                                                                        d0 > (int64_t(1) << 30))))
+        return BT_ERR_UNSUPPORTED;
     if (d0 == 0) return BT_OK;
     if (x == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4))) return BT_ERR_ALIGNMENT;

@@ -22,6 +22,10 @@ constexpr unsigned int kErrTimeout = 1u;
 __device__ __forceinline__ uint32_t sign_bit(float v, float b) {
     return __fadd_rn(v, b) >= 0.0f ? 1u : 0u;
 }
+// The complement: 1 where the value binarizes to -1.
+__device__ __forceinline__ uint32_t is_negative(float v, float b) {
+    return __fadd_rn(v, b) >= 0.0f ? 0u : 1u;
+}
 
 // Codes of +1 / -1.
 constexpr uint32_t kE4M3Plus = 0x38u, kE4M3Minus = 0xB8u;
@@ -98,6 +102,31 @@ template <> struct OutT<BT_I32> {
     using type = int;
     __device__ __forceinline__ static int cvt(int dot, float) { return dot; }
 };
+
+// The same from a tensor-core accumulator: the fp32 accumulator already holds
+// the exact integer dot (|dot| < 2^24), so fp32(dot * alpha) is one multiply
+// of it -- no integer round trip.
+template <int OUT> struct FromAcc;
+template <> struct FromAcc<BT_F32> {
+    __device__ __forceinline__ static uint32_t bits(float acc, float alpha) {
+        return __float_as_uint(__fmul_rn(acc, alpha));
+    }
+};
+template <> struct FromAcc<BT_I32> {
+    __device__ __forceinline__ static uint32_t bits(float acc, float) {
+        return static_cast<uint32_t>(__float2int_rn(acc));
+    }
+};
+// Two 16-bit outputs packed in one word (first in the low half).
+template <int OUT> __device__ __forceinline__ uint32_t pack2_from_acc(float a0, float a1, float alpha);
+template <> __device__ __forceinline__ uint32_t pack2_from_acc<BT_BF16>(float a0, float a1, float alpha) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(__fmul_rn(a0, alpha), __fmul_rn(a1, alpha));
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2_from_acc<BT_F16>(float a0, float a1, float alpha) {
+    const __half2 v = __floats2half2_rn(__fmul_rn(a0, alpha), __fmul_rn(a1, alpha));
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
 
 // ---------------------------------------------------------------------------
 // Bounded waiting. Every spin in these kernels gives up after kWaitNs of

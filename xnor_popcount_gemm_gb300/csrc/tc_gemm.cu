@@ -11,20 +11,34 @@
 // outside the tensor, and taps that fall in a convolution's zero padding)
 // contribute 0, which is the unfold + mm reading of padding.
 //
-// One CTA computes a 128 x 256 output tile with one tcgen05.mma chain
-// (M=128, N=256, accumulator in 256 TMEM columns):
+// Persistent, warp-specialised: one CTA per SM walks output tiles of
+// 128 x BN (BN a multiple of 32, chosen per problem so the tiles spread evenly
+// over the SMs). The fp32 accumulator is double-buffered in TMEM (2 x 224
+// columns plus 32 of unit block scales for E2M1, 2 x 256 for E4M3), so a
+// tile's epilogue -- and its output stores -- overlap the next tile's MMAs.
 //   warp 0 lane 0   TMA producer: a ring of smem stages, each one 128- or
-//                   64-byte-wide K slice of A (128 rows) and B (256 rows),
-//                   written by TMA with the matching swizzle;
-//   warp 1 lane 0   MMA issuer: 4 (or 2) MMAs of K = 32 bytes per stage,
-//                   tcgen05.commit frees the stage;
-//   warps 0..3      epilogue: tcgen05.ld of the warp's 32 TMEM lanes (rows),
-//                   scale, cast, store.
+//                   64-byte-wide K slice of A (128 rows) and B (BN rows),
+//                   written with the matching swizzle; it runs ahead across
+//                   tile boundaries.
+//   warp 1 lane 0   MMA issuer: per 32 bytes of a stage, one tcgen05.mma
+//                   (M=128, N=BN) into the tile's accumulator buffer;
+//                   tcgen05.commit frees the stage, and, after a tile's last
+//                   stage, hands the buffer to the epilogue.
+//   warps 2..5      epilogue: each drains its 32 TMEM lanes (rows), the next
+//                   32-column box in flight while the current
+//                   one is scaled and cast. A linear output goes through a
+//                   swizzled 32 x 32 smem box so that whole row segments leave in
+//                   16-byte stores; a convolution's NCHW output is stored
+//                   straight from registers (consecutive lanes, consecutive
+//                   pixels). Once drained, the buffer goes back to the MMA
+//                   warp.
 // A convolution reads A through TMA im2col mode: for filter tap (kh, kw) the
-// box is the 128 output pixels of the tile, each shifted by (kh*d, kw*d), the
+// box is 128 consecutive output pixels, each shifted by (kh*d, kw*d), the
 // traversal stepping by the stride inside the padded bounding box.
 #include <cudaTypedefs.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "bt_device.cuh"
@@ -34,37 +48,49 @@
 namespace bt {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kThreads = 128;
+constexpr int kBM = 128, kMaxBN = 256;           // tile rows (= MMA M), widest tile
+constexpr int kThreads = 192;                    // producer, MMA, 4 epilogue warps
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = 256;         // 32 columns of unit block scales (E2M1)
-constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;   // UE8M0 127 = 2^0 in every byte
-constexpr int kSmemBudget = 200 * 1024;
+constexpr uint32_t kSfCol = 448;                 // 32 columns of unit block scales (E2M1)
+constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;    // UE8M0 127 = 2^0 in every byte
+constexpr int kSmemMax = 232448;                 // 227 KB opt-in per CTA
+constexpr int kBoxBytes = 32 * 128;              // one epilogue staging box: 32 rows x 128 B
+constexpr int kStagingBytes = 4 * kBoxBytes;     // one box per epilogue warp
+constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
 
 struct TcArgs {
     int64_t M, N;
-    int nk;                    // K steps (smem stages to consume)
+    int nk;                    // K steps per tile (smem stages to consume)
+    int num_n, num_tiles, bn;  // tile grid; BN (multiple of 32, <= 256)
+    int cm, cn;                // cluster shape: CTAs sharing B (along M) x sharing A (along N)
+    int num_sn, num_super;     // super-tiles (cm x cn tiles, one per cluster at a time)
+    uint32_t idesc;            // instruction descriptor for M=128, N=BN
     float alpha;
     void *out;
     unsigned int *err;
+    int vec_store;             // 1: output rows 16-byte aligned (16-byte stores)
     // conv
     int Ho, Wo, s, p, d, k, cpt, rbc;
 };
 
-template <int ROWB> __host__ __device__ constexpr int stages_for() {
-    return kSmemBudget / ((kBM + kBN) * ROWB) > 8 ? 8 : kSmemBudget / ((kBM + kBN) * ROWB);
+template <int ROWB, bool CONV> __host__ __device__ constexpr int stage_bytes() { return (kBM + kMaxBN) * ROWB; }
+template <int ROWB, bool CONV> __host__ __device__ constexpr int num_stages() {
+    return (kSmemMax - kReserve - (CONV ? 0 : kStagingBytes)) / stage_bytes<ROWB, CONV>() > 8
+               ? 8
+               : (kSmemMax - kReserve - (CONV ? 0 : kStagingBytes)) / stage_bytes<ROWB, CONV>();
 }
-template <int ROWB> __host__ __device__ constexpr int smem_bytes() {
-    return stages_for<ROWB>() * (kBM + kBN) * ROWB + 1024 /*align*/ + 256 /*barriers*/;
+template <int ROWB, bool CONV> __host__ __device__ constexpr int smem_bytes() {
+    return num_stages<ROWB, CONV>() * stage_bytes<ROWB, CONV>() + (CONV ? 0 : kStagingBytes) + kReserve;
 }
 
-template <int CODE, int ROWB>
-__device__ __forceinline__ constexpr uint32_t instr_desc() {
-    // D = F32, K-major A and B, N = 256, M = 128.
-    return CODE == BT_CODE_E4M3
-               ? ((1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t(kBN) >> 3) << 17) | ((uint32_t(kBM) >> 4) << 24))
-               // block-scaled: A/B = E2M1, scale type UE8M0, scale-factor ids 0
-               : ((1u << 7) | (1u << 10) | ((uint32_t(kBN) >> 3) << 17) | (1u << 23) |
-                  ((uint32_t(kBM) >> 4) << 24));
+// TMEM column of the second accumulator buffer; also the largest BN.
+template <int CODE> __host__ __device__ constexpr uint32_t acc_stride() { return CODE == BT_CODE_E2M1 ? 224u : 256u; }
+
+// Instruction descriptor: D = F32, K-major A and B, M = 128, N = bn.
+uint32_t make_idesc(bt_code code, int bn) {
+    const uint32_t mn = ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(kBM) >> 4) << 24);
+    if (code == BT_CODE_E4M3) return (1u << 4) | (0u << 7) | (0u << 10) | mn;       // E4M3 x E4M3
+    return (1u << 7) | (1u << 10) | (1u << 23) | mn;   // block-scaled E2M1 x E2M1, UE8M0 scales, ids 0
 }
 
 template <int ROWB>
@@ -78,54 +104,79 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t saddr) {
     return d;
 }
 
-template <int OUT>
-__device__ __forceinline__ void store_row_linear(typename OutT<OUT>::type *out, int64_t N, int64_t m, int64_t n,
-                                                 const uint32_t (&r)[32], float alpha, bool vec_ok) {
-    using T = typename OutT<OUT>::type;
-    T v[32];
+// 16 bytes of converted outputs from accumulators r[j0 .. j0 + 16/elem).
+template <int OUT, int ELEM>
+__device__ __forceinline__ uint4 chunk16(const uint32_t (&r)[32], int j0, float alpha) {
+    uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = OutT<OUT>::cvt(__float2int_rn(__uint_as_float(r[j])), alpha);
-    T *dst = out + m * N + n;
-    if (vec_ok && n + 32 <= N) {
-        constexpr int PER = 16 / sizeof(T);
-#pragma unroll
-        for (int q = 0; q < 32 / PER; ++q) *reinterpret_cast<uint4 *>(dst + q * PER) = *reinterpret_cast<const uint4 *>(&v[q * PER]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (n + j < N) dst[j] = v[j];
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (ELEM == 4) {
+            w[i] = FromAcc<OUT>::bits(__uint_as_float(r[j0 + i]), alpha);
+        } else {
+            w[i] = pack2_from_acc<OUT>(__uint_as_float(r[j0 + 2 * i]), __uint_as_float(r[j0 + 2 * i + 1]), alpha);
+        }
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One output value (conv epilogue) from its accumulator.
+template <int OUT>
+__device__ __forceinline__ typename OutT<OUT>::type from_acc(float acc, float alpha) {
+    if constexpr (OUT == BT_F32) return __fmul_rn(acc, alpha);
+    else if constexpr (OUT == BT_BF16) return __float2bfloat16_rn(__fmul_rn(acc, alpha));
+    else if constexpr (OUT == BT_F16) return __float2half_rn(__fmul_rn(acc, alpha));
+    else return __float2int_rn(acc);
+}
+
+// Position of 16-byte chunk q of staging-box row `row`: the 128-byte swizzle
+// (q ^ row % 8) for 4-byte outputs (128-byte rows), the 64-byte swizzle
+// (q ^ (row / 2) % 4) for 2-byte outputs (64-byte rows) -- the layouts TMA
+// expects for CU_TENSOR_MAP_SWIZZLE_128B / _64B.
+template <int ELEM>
+__device__ __forceinline__ uint32_t box_chunk(int q, int row) {
+    return ELEM == 4 ? static_cast<uint32_t>(q ^ (row & 7)) : static_cast<uint32_t>(q ^ ((row >> 1) & 3));
 }
 
 template <int CODE, int ROWB, bool CONV, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
-    constexpr int S = stages_for<ROWB>();
-    constexpr uint32_t kABytes = kBM * ROWB, kBBytes = kBN * ROWB;
+tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+          const TcArgs a) {
+    constexpr int S = num_stages<ROWB, CONV>();
+    constexpr uint32_t kABytes = kBM * ROWB, kBBytes = kMaxBN * ROWB;
     constexpr int kMmaPerStage = ROWB / 32;        // K = 32 bytes per MMA
+    using T = typename OutT<OUT>::type;
+    constexpr int kElem = sizeof(T);
+    constexpr int kBoxInner = 32 * kElem;          // bytes of one staging-box row: 32 output columns
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base, sB = base + S * kABytes;
-    const uint32_t bars = sB + S * kBBytes;               // full[S], empty[S], accum
+    const uint32_t sStage = sB + S * kBBytes;                        // epilogue staging (linear)
+    const uint32_t bars = sStage + (CONV ? 0 : kStagingBytes);      // full[S], empty[S], tfull[2], tempty[2], drain
     uint8_t *gbars = smem_raw + (bars - raw);
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbars + 8 * (2 * S + 1));
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbars + 8 * (2 * S + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (S + s); };
-    const uint32_t accum = bars + 8u * (2 * S);
+    auto tfull = [&](int b) { return bars + 8u * (2 * S + b); };          // accumulator buffer b written
+    auto tempty = [&](int b) { return bars + 8u * (2 * S + 2 + b); };     // accumulator buffer b drained
+    const uint32_t drain = bars + 8u * (2 * S + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kBM;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(full(s), 1);
-            tc::mbar_init(empty(s), 1);
+            // released by every CTA this one's copies land in (itself, its A
+            // sharers and its B sharers)
+            tc::mbar_init(empty(s), static_cast<uint32_t>(a.cm + a.cn - 1));
         }
-        tc::mbar_init(accum, 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(tfull(b), 1);
+            tc::mbar_init(tempty(b), 4);   // one arrival per epilogue warp
+        }
+        tc::mbar_init(drain, 1);
         *abort_flag = 0u;
         tc::fence_mbar_init();
         tc::prefetch_map(&tmA);
@@ -138,58 +189,89 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    const bool clustered = a.cm * a.cn > 1;
+    if (clustered) tc::cluster_sync();        // peers' barriers exist before any multicast lands
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // position in the cluster: rm along M (B sharers), rn along N (A sharers)
+    const int crank = clustered ? static_cast<int>(tc::cluster_ctarank()) : 0;
+    const int rm = crank % a.cm, rn = crank / a.cm;
+    const int cluster = clustered ? static_cast<int>(tc::cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int nclusters = clustered ? static_cast<int>(tc::num_clusters_x()) : static_cast<int>(gridDim.x);
+    uint16_t maskA = 0, maskB = 0;
+    for (int j = 0; j < a.cn; ++j) maskA |= static_cast<uint16_t>(1u << (rm + a.cm * j));
+    for (int j = 0; j < a.cm; ++j) maskB |= static_cast<uint16_t>(1u << (j + a.cm * rn));
+    const uint16_t mask_release = maskA | maskB;
+    const int a_rows = kBM / a.cn;            // rows of the A tile this CTA loads
+    const int b_rows = a.bn / a.cm;           // rows of the B tile this CTA loads
+    const int quarter = warp & 3;                                   // TMEM lanes this warp may touch
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
 
     if (CODE == BT_CODE_E2M1) {
-        // unit block scales for A and B: every byte of columns [256, 288)
-        tc::tmem_st16_fill(tmem + lane_base + kSfCol, kUnitScales);
-        tc::tmem_st16_fill(tmem + lane_base + kSfCol + 16, kUnitScales);
-        tc::tmem_st_wait();
+        if (warp >= 2) {
+            // unit block scales for A and B: every byte of columns [256, 288)
+            tc::tmem_st16_fill(tmem + lane_base + kSfCol, kUnitScales);
+            tc::tmem_st16_fill(tmem + lane_base + kSfCol + 16, kUnitScales);
+            tc::tmem_st_wait();
+        }
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
     }
 
-    // conv: base coordinates of the tile's first output pixel
-    int cb = 0, ch = 0, cw = 0;
-    if (CONV) {
-        const int64_t hw = static_cast<int64_t>(a.Ho) * a.Wo;
-        cb = static_cast<int>(m0 / hw);
-        const int r = static_cast<int>(m0 - static_cast<int64_t>(cb) * hw);
-        ch = (r / a.Wo) * a.s - a.p;
-        cw = (r % a.Wo) * a.s - a.p;
-    }
+    const int bn = a.bn;
+    const uint32_t tx_bytes = static_cast<uint32_t>((kBM + bn) * ROWB);
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
+            uint32_t it = 0;
             int last_issue[8];
 #pragma unroll
             for (int s = 0; s < 8; ++s) last_issue[s] = -1;
             bool ok = true;
-            for (int kb = 0; kb < a.nk && ok; ++kb) {
-                const int s = kb % S;
-                const uint32_t ph = static_cast<uint32_t>(kb / S) & 1u;
-                if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-                tc::mbar_arrive_expect_tx(full(s), kABytes + kBBytes);
+            for (int st = cluster; st < a.num_super && ok; st += nclusters) {
+                const int mt = (st / a.num_sn) * a.cm + rm, nt = (st % a.num_sn) * a.cn + rn;
+                // this CTA's share of the A tile starts a_rows * rn rows in
+                const int64_t am0 = static_cast<int64_t>(mt) * kBM + static_cast<int64_t>(a_rows) * rn;
+                const int bn0 = nt * bn + b_rows * rm;                       // and of the B tile
+                int cb = 0, ch = 0, cw = 0;
                 if (CONV) {
-                    const int tap = kb / a.cpt, chunk = kb - tap * a.cpt;
-                    const int kh = tap / a.k, kw = tap - kh * a.k;
-                    tc::tma_load_im2col_4d(sA + s * kABytes, &tmA, chunk * ROWB, cw, ch, cb,
-                                           static_cast<uint16_t>(kw * a.d), static_cast<uint16_t>(kh * a.d), full(s));
-                    tc::tma_load_2d(sB + s * kBBytes, &tmB, tap * a.rbc + chunk * ROWB, static_cast<int>(n0), full(s));
-                } else {
-                    tc::tma_load_2d(sA + s * kABytes, &tmA, kb * ROWB, static_cast<int>(m0), full(s));
-                    tc::tma_load_2d(sB + s * kBBytes, &tmB, kb * ROWB, static_cast<int>(n0), full(s));
+                    const int64_t hw = static_cast<int64_t>(a.Ho) * a.Wo;
+                    cb = static_cast<int>(am0 / hw);
+                    const int r = static_cast<int>(am0 - static_cast<int64_t>(cb) * hw);
+                    ch = (r / a.Wo) * a.s - a.p;
+                    cw = (r % a.Wo) * a.s - a.p;
                 }
-                last_issue[s < 8 ? s : 0] = kb;
+                const uint32_t a_off = static_cast<uint32_t>(a_rows * rn * ROWB);
+                const uint32_t b_off = static_cast<uint32_t>(b_rows * rm * ROWB);
+                for (int kb = 0; kb < a.nk; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S);
+                    const uint32_t ph = (it / S) & 1u;
+                    if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+                    tc::mbar_arrive_expect_tx(full(s), tx_bytes);
+                    const uint32_t adst = sA + s * kABytes + a_off, bdst = sB + s * kBBytes + b_off;
+                    int bcol = kb * ROWB;
+                    if (CONV) {
+                        const int tap = kb / a.cpt, chunk = kb - tap * a.cpt;
+                        const int kh = tap / a.k, kw = tap - kh * a.k;
+                        const uint16_t ow = static_cast<uint16_t>(kw * a.d), oh = static_cast<uint16_t>(kh * a.d);
+                        if (a.cn > 1) tc::tma_load_im2col_4d_mc(adst, &tmA, chunk * ROWB, cw, ch, cb, ow, oh, full(s), maskA);
+                        else tc::tma_load_im2col_4d(adst, &tmA, chunk * ROWB, cw, ch, cb, ow, oh, full(s));
+                        bcol = tap * a.rbc + chunk * ROWB;
+                    } else {
+                        if (a.cn > 1) tc::tma_load_2d_mc(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s), maskA);
+                        else tc::tma_load_2d(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s));
+                    }
+                    if (a.cm > 1) tc::tma_load_2d_mc(bdst, &tmB, bcol, bn0, full(s), maskB);
+                    else tc::tma_load_2d(bdst, &tmB, bcol, bn0, full(s));
+                    last_issue[s] = static_cast<int>(it);
+                }
             }
             if (!ok) {
-                // drain: let every issued copy land before the CTA can exit
-                for (int s = 0; s < S && s < 8; ++s) {
+                // let every issued copy land before the CTA can exit
+                for (int s = 0; s < S; ++s) {
                     if (last_issue[s] >= 0) {
-                        const uint32_t ph = static_cast<uint32_t>(last_issue[s] / S) & 1u;
+                        const uint32_t ph = (static_cast<uint32_t>(last_issue[s]) / S) & 1u;
                         const unsigned long long t0 = globaltimer_ns();
                         while (!tc::mbar_try_wait(full(s), ph) && globaltimer_ns() - t0 < kWaitNs) {}
                     }
@@ -200,67 +282,173 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = instr_desc<CODE, ROWB>();
-            bool issued = false;
-            for (int kb = 0; kb < a.nk; ++kb) {
-                const int s = kb % S;
-                const uint32_t ph = static_cast<uint32_t>(kb / S) & 1u;
-                if (!tc::wait_bounded(full(s), ph, abort_flag, a.err)) break;
-                tc::fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < kMmaPerStage; ++kk) {
-                    const uint64_t ad = operand_desc<ROWB>(sA + s * kABytes + kk * 32);
-                    const uint64_t bd = operand_desc<ROWB>(sB + s * kBBytes + kk * 32);
-                    const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-                    if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(tmem, ad, bd, idesc, acc);
-                    else tc::mma_mxf4(tmem, ad, bd, idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true;
+            for (int st = cluster; st < a.num_super && ok; st += nclusters, ++local) {
+                const int buf = local & 1;
+                if (local >= 2) {
+                    // the epilogue has drained this buffer (two tiles ago)
+                    if (!tc::wait_bounded(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err))
+                        break;
+                    tc::fence_after_sync();
                 }
-                issued = true;
-                tc::mma_commit(empty(s));
+                const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * acc_stride<CODE>();
+                for (int kb = 0; kb < a.nk; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S);
+                    const uint32_t ph = (it / S) & 1u;
+                    if (!tc::wait_bounded(full(s), ph, abort_flag, a.err)) { ok = false; break; }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kMmaPerStage; ++kk) {
+                        const uint64_t bd = operand_desc<ROWB>(sB + s * kBBytes + kk * 32);
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        const uint64_t ad = operand_desc<ROWB>(sA + s * kABytes + kk * 32);
+                        if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, ad, bd, a.idesc, acc);
+                        else tc::mma_mxf4(dacc, ad, bd, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+                    }
+                    if (clustered) tc::mma_commit_mc(empty(s), mask_release);
+                    else tc::mma_commit(empty(s));
+                }
+                if (ok) tc::mma_commit(tfull(buf));
             }
-            // signals the epilogue (also when nothing was issued, so nobody waits in vain)
-            (void)issued;
-            tc::mma_commit(accum);
+            // every MMA issued must finish before the accumulator is freed
+            tc::mma_commit(drain);
+            const unsigned long long t0 = globaltimer_ns();
+            while (!tc::mbar_try_wait(drain, 0u) && globaltimer_ns() - t0 < kWaitNs) {}
         }
         __syncwarp();
-    }
-
-    // ---------------- epilogue (all 4 warps) ----------------
-    const bool have = tc::wait_bounded(accum, 0u, abort_flag, a.err);
-    tc::fence_after_sync();
-    if (have && *abort_flag == 0u) {
-        using T = typename OutT<OUT>::type;
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
         T *out = static_cast<T *>(a.out);
-        const int64_t m = m0 + warp * 32 + lane;
-        const bool row_ok = m < a.M;
-        const bool vec_ok = ((a.N * static_cast<int64_t>(sizeof(T))) % 16) == 0;
-        int64_t ob = 0, pix = 0, hw = 0;
-        if (CONV) {
-            hw = static_cast<int64_t>(a.Ho) * a.Wo;
-            ob = row_ok ? m / hw : 0;
-            pix = m - ob * hw;
-        }
-#pragma unroll 1
-        for (int c = 0; c < kBN; c += 32) {
-            if (n0 + c >= a.N) break;                    // warp-uniform
-            uint32_t r[32];
-            tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(c), r);
-            tc::tmem_ld_wait();
-            if (!row_ok) continue;
-            if (CONV) {
+        const uint32_t my_stage = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // one box per warp
+        int local = 0;
+        for (int st = cluster; st < a.num_super; st += nclusters, ++local) {
+            const int mt = (st / a.num_sn) * a.cm + rm, nt = (st % a.num_sn) * a.cn + rn;
+            const int64_t m0 = static_cast<int64_t>(mt) * kBM;
+            const int n0 = nt * bn;
+            const int buf = local & 1;
+            if (!tc::wait_bounded(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err)) break;
+            tc::fence_after_sync();
+            bool released = false;
+            auto release = [&]() {
+                // every TMEM read of this tile is complete: hand the accumulators back
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tempty(buf));
+                released = true;
+            };
+            if constexpr (!CONV) {
+                // Boxes of 32 rows x 32 columns (64 or 128 bytes, matching swizzle)
+                // through the warp's staging box. The TMEM read of the next box is
+                // in flight while the current one is converted.
+                const int64_t ncols = a.N - n0 < bn ? a.N - n0 : bn;
+                const int nbox = ncols > 0 ? static_cast<int>((ncols + 31) / 32) : 0;
+                const int64_t mrow0 = m0 + quarter * 32;                     // this warp's first row
+                const int total = mrow0 < a.M ? nbox : 0;
+                const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
+                auto tcol_of = [&](int b) { return tbase + static_cast<uint32_t>(32 * b); };
+                auto emit = [&](const uint32_t (&r)[32], int b) {
+                    const int c0 = 32 * b;
+                    const uint32_t buf = my_stage;
+                    __syncwarp();                                             // previous box fully read back
+                    constexpr int kChunks = kBoxInner / 16;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int64_t o = n0 + c + j;
-                    if (o < a.N)
-                        out[(ob * a.N + o) * hw + pix] = OutT<OUT>::cvt(__float2int_rn(__uint_as_float(r[j])), a.alpha);
+                    for (int q = 0; q < kChunks; ++q) {
+                        const uint32_t addr = buf + static_cast<uint32_t>(lane * kBoxInner) + (box_chunk<kElem>(q, lane) << 4);
+                        const uint4 w = chunk16<OUT, kElem>(r, q * (16 / kElem), a.alpha);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w.x), "r"(w.y),
+                                     "r"(w.z), "r"(w.w)
+                                     : "memory");
+                    }
+                    __syncwarp();
+                    if (a.vec_store) {
+                        // aligned rows: read the box back as 16-byte chunks, kChunks lanes
+                        // per row, 32/kChunks rows per instruction, and store them whole
+                        constexpr int kRowsPer = 32 / kChunks;
+                        const int q = lane % kChunks;
+                        const int64_t col = n0 + c0 + q * (16 / kElem);
+#pragma unroll
+                        for (int rr0 = 0; rr0 < 32; rr0 += kRowsPer) {
+                            const int rr = rr0 + lane / kChunks;
+                            const uint32_t addr = buf + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(q, rr) << 4);
+                            uint4 v;
+                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                         : "r"(addr));
+                            const int64_t row = mrow0 + rr;
+                            if (row < a.M && col < a.N)
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out) +
+                                                           (row * a.N + col) * kElem) = v;
+                        }
+                    } else {
+                        // ragged N: read the box back one row at a time, lanes along
+                        // the columns, so every store is 32 consecutive elements
+                        const int64_t col = n0 + c0 + lane;
+                        constexpr int kPer = 16 / kElem;
+                        const uint32_t off = static_cast<uint32_t>((lane % kPer) * kElem);
+#pragma unroll 4
+                        for (int rr = 0; rr < 32; ++rr) {
+                            const uint32_t addr =
+                                buf + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(lane / kPer, rr) << 4) + off;
+                            uint32_t v;
+                            if (kElem == 4) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+                            else asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+                            const int64_t row = mrow0 + rr;
+                            if (row < a.M && col < a.N) {
+                                if (kElem == 4) reinterpret_cast<uint32_t *>(out)[row * a.N + col] = v;
+                                else reinterpret_cast<uint16_t *>(out)[row * a.N + col] = static_cast<uint16_t>(v);
+                            }
+                        }
+                    }
+                };
+                uint32_t r0[32], r1[32];
+                if (total > 0) tc::tmem_ld32(tcol_of(0), r0);
+#pragma unroll 1
+                for (int b = 0; b < total; b += 2) {
+                    tc::tmem_ld_wait();
+                    if (b + 1 < total) tc::tmem_ld32(tcol_of(b + 1), r1);
+                    else release();
+                    emit(r0, b);
+                    if (b + 1 < total) {
+                        tc::tmem_ld_wait();
+                        if (b + 2 < total) tc::tmem_ld32(tcol_of(b + 2), r0);
+                        else release();
+                        emit(r1, b + 1);
+                    }
                 }
             } else {
-                store_row_linear<OUT>(out, a.N, m, n0 + c, r, a.alpha, vec_ok);
+                {
+                    const int64_t mrow0 = m0 + quarter * 32;                     // this warp's first row
+                    const int64_t m = mrow0 + lane;
+                    const bool row_ok = m < a.M;
+                    const uint32_t tcol = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
+                    const int64_t hw = static_cast<int64_t>(a.Ho) * a.Wo;
+                    const int64_t ob = row_ok ? m / hw : 0;
+                    const int64_t pix = m - ob * hw;
+#pragma unroll 1
+                    for (int c = 0; c < bn; c += 32) {
+                        if (n0 + c >= a.N) break;                            // warp-uniform
+                        uint32_t r[32];
+                        tc::tmem_ld32(tcol + static_cast<uint32_t>(c), r);
+                        tc::tmem_ld_wait();
+                        if (!row_ok) continue;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int64_t o = n0 + c + j;
+                            if (o < a.N) out[(ob * a.N + o) * hw + pix] = from_acc<OUT>(__uint_as_float(r[j]), a.alpha);
+                        }
+                    }
+                }
             }
+            if (!released) release();
         }
     }
+
     tc::fence_before_sync();
     __syncthreads();
+    // no CTA leaves while a peer may still multicast into it or release its stages
+    if (clustered) tc::cluster_sync();
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
@@ -297,6 +485,18 @@ PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col() {
     return fn;
 }
 
+int sm_count() {
+    static int n[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (n[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
 // 2-D byte matrix [rows, row_bytes] with row pitch `pitch`; box = box_inner bytes x box_rows.
 bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t pitch, uint64_t rows, uint32_t box_inner,
             uint32_t box_rows) {
@@ -312,21 +512,92 @@ bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t pitch,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tile configuration: BN (a multiple of 32 -- the epilogue's box width -- up
+// to 224 for E2M1 / 256 for E4M3) and the cluster shape CM x CN. The cost
+// model: a problem takes `rounds` waves of super-tiles over the clusters;
+// each K stage costs the larger of its MMA time (one M=128, N=BN MMA per 32
+// bytes, about 125 clocks at N=256 on GB300) and the time for the whole stage
+// to land in this SM's shared memory (about 80 bytes per clock per SM
+// measured for TMA into the ring; multicast inside a cluster lowers L2 reads
+// but not the bytes each SM receives, so clusters only change the wave
+// count); with the accumulator double-buffered only the last tile's epilogue
+// (about 8 clocks per output column) is exposed.
+// BT_TC_CONFIG="cm,cn,bn" overrides the choice.
+struct TileCfg {
+    int cm, cn, bn;
+};
+
+TileCfg choose_cfg(int64_t M, int64_t N, int nk, int rowb, int sms, int max_bn) {
+    TileCfg best{1, 1, max_bn};
+    if (const char *env = std::getenv("BT_TC_CONFIG")) {
+        int cm = 0, cn = 0, bn = 0;
+        if (std::sscanf(env, "%d,%d,%d", &cm, &cn, &bn) == 3 && (cm == 1 || cm == 2) && (cn == 1 || cn == 2) &&
+            bn >= 32 && bn <= max_bn && bn % 32 == 0)
+            return TileCfg{cm, cn, bn};
+    }
+    const int64_t num_m = (M + kBM - 1) / kBM;
+    double best_cost = -1.0;
+    for (int cm = 1; cm <= 2; ++cm) {
+        for (int cn = 1; cn <= 2; ++cn) {
+            const int64_t clusters = sms / (cm * cn);
+            for (int bn = max_bn; bn >= 32; bn -= 32) {
+                const int64_t num_n = (N + bn - 1) / bn;
+                const int64_t super = ((num_m + cm - 1) / cm) * ((num_n + cn - 1) / cn);
+                const int64_t rounds = (super + clusters - 1) / clusters;
+                const double mma = (rowb / 32) * 125.0 * bn / 256.0;
+                const double bytes = static_cast<double>(kBM + bn) * rowb;
+                const double stage = mma > bytes / 80.0 ? mma : bytes / 80.0;
+                const double cost = static_cast<double>(rounds) * nk * stage + 8.0 * bn + 600.0;
+                if (best_cost < 0.0 || cost < best_cost * 0.999) {
+                    best_cost = cost;
+                    best = TileCfg{cm, cn, bn};
+                }
+            }
+        }
+    }
+    return best;
+}
+
 template <int CODE, int ROWB, bool CONV, int OUT>
-cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a, cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
+                     cudaStream_t s) {
     auto kern = tc_kernel<CODE, ROWB, CONV, OUT>;
-    constexpr int smem = smem_bytes<ROWB>();
+    constexpr int smem = smem_bytes<ROWB, CONV>();
+    static_assert(smem <= kSmemMax, "shared memory budget");
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] { attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 grid(static_cast<unsigned>((a.N + kBN - 1) / kBN), static_cast<unsigned>((a.M + kBM - 1) / kBM));
-    kern<<<grid, kThreads, smem, s>>>(ma, mb, a);
+    const int csize = a.cm * a.cn;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many clusters as fit at once on the device, at most one per super-tile
+    int clusters = sm_count() / csize;
+    if (csize > 1) {
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * csize), 1, 1);
+        int fit = 0;
+        if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < clusters) clusters = fit;
+    }
+    if (clusters > a.num_super) clusters = a.num_super;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * csize), 1, 1);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int CODE, int ROWB, bool CONV>
-cudaError_t launch_out(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a, bt_dtype out_t, cudaStream_t s) {
+cudaError_t launch_out(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
+                       bt_dtype out_t, cudaStream_t s) {
     switch (out_t) {
         case BT_F32: return launch_t<CODE, ROWB, CONV, BT_F32>(ma, mb, a, s);
         case BT_BF16: return launch_t<CODE, ROWB, CONV, BT_BF16>(ma, mb, a, s);
@@ -345,6 +616,24 @@ cudaError_t launch_code(bt_code code, int rowb, const CUtensorMap &ma, const CUt
                        : launch_out<BT_CODE_E2M1, 64, CONV>(ma, mb, a, out_t, s);
 }
 
+int out_elem_bytes(bt_dtype t) { return t == BT_BF16 || t == BT_F16 ? 2 : 4; }
+
+// Fill the tile-grid fields of `a` for configuration `c`.
+bool set_grid(TcArgs &a, const TileCfg &c, int64_t M, int64_t N) {
+    a.cm = c.cm;
+    a.cn = c.cn;
+    a.bn = c.bn;
+    const int64_t num_m = (M + kBM - 1) / kBM, num_n = (N + c.bn - 1) / c.bn;
+    const int64_t num_sn = (num_n + c.cn - 1) / c.cn;
+    const int64_t num_super = ((num_m + c.cm - 1) / c.cm) * num_sn;
+    if (num_super > (int64_t(1) << 30)) return false;
+    a.num_n = static_cast<int>(num_n);
+    a.num_tiles = static_cast<int>(num_m * num_n);
+    a.num_sn = static_cast<int>(num_sn);
+    a.num_super = static_cast<int>(num_super);
+    return true;
+}
+
 }  // namespace
 
 bool tc_available() { return encode_tiled() != nullptr && encode_im2col() != nullptr; }
@@ -352,10 +641,17 @@ bool tc_available() { return encode_tiled() != nullptr && encode_im2col() != nul
 cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M, int64_t N, int64_t K,
                              float alpha, void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
     const int64_t rb = row_bytes(K, code);
-    CUtensorMap ma, mb;
-    if (!map_2d(&ma, xp, rb, rb, M, 128, kBM) || !map_2d(&mb, wp, rb, rb, N, 128, kBN)) return cudaErrorInvalidValue;
     TcArgs a{};
     a.M = M; a.N = N; a.nk = static_cast<int>((rb + 127) / 128); a.alpha = alpha; a.out = out; a.err = err;
+    const int64_t ob = out_elem_bytes(out_t);
+    a.vec_store = ((N * ob) % 16 == 0) && aligned(out, 16) ? 1 : 0;
+    const TileCfg c = choose_cfg(M, N, a.nk, 128, sm_count(), code == BT_CODE_E2M1 ? 224 : 256);
+    if (!set_grid(a, c, M, N)) return cudaErrorInvalidValue;
+    a.idesc = make_idesc(code, a.bn);
+    CUtensorMap ma, mb;
+    if (!map_2d(&ma, xp, rb, rb, M, 128, static_cast<uint32_t>(kBM / a.cn)) ||
+        !map_2d(&mb, wp, rb, rb, N, 128, static_cast<uint32_t>(a.bn / a.cm)))
+        return cudaErrorInvalidValue;
     return launch_code<false>(code, 128, ma, mb, a, out_t, s);
 }
 
@@ -365,6 +661,16 @@ cudaError_t launch_tc_conv(const uint8_t *xp, const uint8_t *wp, bt_code code, c
     const int rowb = (rbc % 128 == 0) ? 128 : 64;
     auto fn = encode_im2col();
     if (fn == nullptr || rbc % 64 != 0) return cudaErrorInvalidValue;
+    TcArgs a{};
+    a.M = g.B * g.Ho * g.Wo; a.N = g.O; a.alpha = alpha; a.out = out; a.err = err;
+    a.Ho = static_cast<int>(g.Ho); a.Wo = static_cast<int>(g.Wo);
+    a.s = g.s; a.p = g.p; a.d = g.d; a.k = g.k;
+    a.cpt = static_cast<int>(rbc / rowb); a.rbc = static_cast<int>(rbc);
+    a.nk = g.k * g.k * a.cpt;
+    const TileCfg c = choose_cfg(a.M, a.N, a.nk, rowb, sm_count(), code == BT_CODE_E2M1 ? 224 : 256);
+    if (!set_grid(a, c, a.M, a.N)) return cudaErrorInvalidValue;
+    a.idesc = make_idesc(code, a.bn);
+    a.vec_store = 0;
     CUtensorMap ma, mb;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(rbc), static_cast<cuuint64_t>(g.W), static_cast<cuuint64_t>(g.H),
                           static_cast<cuuint64_t>(g.B)};
@@ -375,17 +681,13 @@ cudaError_t launch_tc_conv(const uint8_t *xp, const uint8_t *wp, bt_code code, c
     cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(g.s), static_cast<cuuint32_t>(g.s), 1};
     const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (fn(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(xp), dims, strides, lower, upper,
-           static_cast<cuuint32_t>(rowb), kBM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           static_cast<cuuint32_t>(rowb), static_cast<cuuint32_t>(kBM / a.cn), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int64_t krow = static_cast<int64_t>(g.k) * g.k * rbc;
-    if (!map_2d(&mb, wp, krow, krow, g.O, static_cast<uint32_t>(rowb), kBN)) return cudaErrorInvalidValue;
-    TcArgs a{};
-    a.M = g.B * g.Ho * g.Wo; a.N = g.O; a.alpha = alpha; a.out = out; a.err = err;
-    a.Ho = static_cast<int>(g.Ho); a.Wo = static_cast<int>(g.Wo);
-    a.s = g.s; a.p = g.p; a.d = g.d; a.k = g.k;
-    a.cpt = static_cast<int>(rbc / rowb); a.rbc = static_cast<int>(rbc);
-    a.nk = g.k * g.k * a.cpt;
+    if (!map_2d(&mb, wp, krow, krow, g.O, static_cast<uint32_t>(rowb), static_cast<uint32_t>(a.bn / a.cm)))
+        return cudaErrorInvalidValue;
     return launch_code<true>(code, rowb, ma, mb, a, out_t, s);
 }
 
