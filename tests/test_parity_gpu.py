@@ -259,7 +259,7 @@ def test_full_conv_workloads(code, name):
 # B slice, cn CTAs share each A slice (TMA multicast inside a cluster).
 # ---------------------------------------------------------------------------
 
-TC_CONFIGS = ["1,1,64", "2,1,64", "1,2,64", "2,2,64", "2,2,160", "2,1,224", "1,2,96"]
+TC_CONFIGS = ["1,1,64", "2,1,64", "1,2,64", "2,2,64", "2,2,160", "2,1,224", "1,2,96", "1,1,240", "1,1,208", "1,2,48"]
 TC_CODES = [bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
 
 

@@ -141,6 +141,24 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. launch_dependents lets the next kernel in the
+// stream be scheduled once every CTA of this grid has started; wait blocks
+// until the previous grid in the stream has completed and its memory is
+// visible (a no-op when this grid was launched without the attribute). Every
+// kernel calls wait before its first global-memory access.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Streaming (evict-first) 16-byte global store.
+__device__ __forceinline__ void st_stream_v4(void *p, const uint4 &v) {
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // cp.async (16 bytes, zero-filled when src_bytes == 0)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

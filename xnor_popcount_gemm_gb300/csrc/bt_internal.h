@@ -63,6 +63,15 @@ cudaError_t launch_tc_conv(const uint8_t *xp, const uint8_t *wp, bt_code code, c
 // True when this build carries the tensor-core kernels.
 bool tc_available();
 
+// Launch attribute list allowing programmatic dependent launch (the kernel
+// overlaps its prologue with the previous kernel in the stream).
+inline cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 // Largest K (elements) for which the tensor-core kernels are used: a bound on
 // the magnitude of the fp32 partial sums they accumulate.
 constexpr int64_t kTcMaxK = 16384;

@@ -94,6 +94,8 @@ __global__ void __launch_bounds__(kRowThreads)
 pack_rows_kernel(const T *__restrict__ x, int64_t R, int K, const float *__restrict__ bias, int bias_len,
                  uint8_t *__restrict__ out, int rb, int G) {
     constexpr int OB = GroupOut<CODE>::kBytes;
+    pdl_launch_dependents();
+    pdl_wait();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
     for (int64_t row = blockIdx.y; row < R; row += gridDim.y) {
         const T *xr = x + row * K;
@@ -171,7 +173,9 @@ pack_rows_staged_kernel(const T *__restrict__ x, int64_t R, int K, const float *
         *flag = 0u;
         tc::fence_mbar_init();
     }
+    pdl_launch_dependents();
     __syncthreads();
+    pdl_wait();
 
     auto issue = [&](int64_t unit, int s) {
         const int64_t row = unit / upr;
@@ -179,7 +183,7 @@ pack_rows_staged_kernel(const T *__restrict__ x, int64_t R, int K, const float *
         const int len = K - k0 < seg ? K - k0 : seg;
         const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
         tc::mbar_arrive_expect_tx(bars + 8u * s, bytes);
-        tc::bulk_load(sbase + s * kSegBytes, x + row * K + k0, bytes, bars + 8u * s);
+        tc::bulk_load_once(sbase + s * kSegBytes, x + row * K + k0, bytes, bars + 8u * s);
     };
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -272,6 +276,8 @@ pack_nhwc_kernel(const T *__restrict__ x, int B, int C, int HW, const float *__r
     const uint32_t npg = static_cast<uint32_t>((HW + E - 1) / E);
     const uint32_t ncg = static_cast<uint32_t>(padded_elems<CODE>(rb) / 8);
     const uint64_t total = static_cast<uint64_t>(B) * ncg * npg;
+    pdl_launch_dependents();
+    pdl_wait();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
 
     for (uint64_t t = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
@@ -350,10 +356,16 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
         const int64_t units = R * upr;
         const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * 3;
         const int grid = static_cast<int>(units < cap ? units : cap);
-        kern<<<grid, kStagedThreads, kStagedSmem, s>>>(x, R, static_cast<int>(K), bias, static_cast<int>(bias_len), out,
-                                                       static_cast<int>(rb), static_cast<int>(G), seg,
-                                                       static_cast<int>(upr), err);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute pdl = pdl_attribute();
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kStagedThreads);
+        cfg.dynamicSmemBytes = kStagedSmem;
+        cfg.stream = s;
+        cfg.attrs = &pdl;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, x, R, static_cast<int>(K), bias, static_cast<int>(bias_len), out,
+                                  static_cast<int>(rb), static_cast<int>(G), seg, static_cast<int>(upr), err);
     }
     if (vec)
         pack_rows_kernel<T, CODE, true><<<grid, kRowThreads, 0, s>>>(x, R, static_cast<int>(K), bias,

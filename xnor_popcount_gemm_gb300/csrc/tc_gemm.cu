@@ -13,7 +13,7 @@
 //
 // Persistent, warp-specialised: one CTA per SM walks output tiles of
 // 128 x BN (BN a multiple of 32, chosen per problem so the tiles spread evenly
-// over the SMs). The fp32 accumulator is double-buffered in TMEM (2 x 224
+// over the SMs). The fp32 accumulator is double-buffered in TMEM (2 x 240
 // columns plus 32 of unit block scales for E2M1, 2 x 256 for E4M3), so a
 // tile's epilogue -- and its output stores -- overlap the next tile's MMAs.
 //   warp 0 lane 0   TMA producer: a ring of smem stages, each one 128- or
@@ -51,7 +51,7 @@ namespace {
 constexpr int kBM = 128, kMaxBN = 256;           // tile rows (= MMA M), widest tile
 constexpr int kThreads = 192;                    // producer, MMA, 4 epilogue warps
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = 448;                 // 32 columns of unit block scales (E2M1)
+constexpr uint32_t kSfCol = 480;                 // 32 columns of unit block scales (E2M1)
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;    // UE8M0 127 = 2^0 in every byte
 constexpr int kSmemMax = 232448;                 // 227 KB opt-in per CTA
 constexpr int kBoxBytes = 32 * 128;              // one epilogue staging box: 32 rows x 128 B
@@ -84,7 +84,7 @@ template <int ROWB, bool CONV> __host__ __device__ constexpr int smem_bytes() {
 }
 
 // TMEM column of the second accumulator buffer; also the largest BN.
-template <int CODE> __host__ __device__ constexpr uint32_t acc_stride() { return CODE == BT_CODE_E2M1 ? 224u : 256u; }
+template <int CODE> __host__ __device__ constexpr uint32_t acc_stride() { return CODE == BT_CODE_E2M1 ? 240u : 256u; }
 
 // Instruction descriptor: D = F32, K-major A and B, M = 128, N = bn.
 uint32_t make_idesc(bt_code code, int bn) {
@@ -165,6 +165,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    if (threadIdx.x == 0) pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(full(s), 1);
@@ -224,6 +225,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
+            pdl_wait();                                   // operands come from the previous kernel
             uint32_t it = 0;
             int last_issue[8];
 #pragma unroll
@@ -320,6 +322,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         __syncwarp();
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
+        pdl_wait();                                       // the previous kernel may still use `out`
         T *out = static_cast<T *>(a.out);
         const uint32_t my_stage = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // one box per warp
         int local = 0;
@@ -343,6 +346,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // through the warp's staging box. The TMEM read of the next box is
                 // in flight while the current one is converted.
                 const int64_t ncols = a.N - n0 < bn ? a.N - n0 : bn;
+                const int64_t ncol_end = n0 + ncols;                         // this tile's columns end here
                 const int nbox = ncols > 0 ? static_cast<int>((ncols + 31) / 32) : 0;
                 const int64_t mrow0 = m0 + quarter * 32;                     // this warp's first row
                 const int total = mrow0 < a.M ? nbox : 0;
@@ -377,9 +381,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                                          : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                                          : "r"(addr));
                             const int64_t row = mrow0 + rr;
-                            if (row < a.M && col < a.N)
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(out) +
-                                                           (row * a.N + col) * kElem) = v;
+                            if (row < a.M && col < ncol_end)
+                                st_stream_v4(reinterpret_cast<uint8_t *>(out) + (row * a.N + col) * kElem, v);
                         }
                     } else {
                         // ragged N: read the box back one row at a time, lanes along
@@ -395,7 +398,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                             if (kElem == 4) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
                             else asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
                             const int64_t row = mrow0 + rr;
-                            if (row < a.M && col < a.N) {
+                            if (row < a.M && col < ncol_end) {
                                 if (kElem == 4) reinterpret_cast<uint32_t *>(out)[row * a.N + col] = v;
                                 else reinterpret_cast<uint16_t *>(out)[row * a.N + col] = static_cast<uint16_t>(v);
                             }
@@ -436,7 +439,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const int64_t o = n0 + c + j;
-                            if (o < a.N) out[(ob * a.N + o) * hw + pix] = from_acc<OUT>(__uint_as_float(r[j]), a.alpha);
+                            if (o < a.N && c + j < bn)
+                                out[(ob * a.N + o) * hw + pix] = from_acc<OUT>(__uint_as_float(r[j]), a.alpha);
                         }
                     }
                 }
@@ -512,16 +516,18 @@ bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t pitch,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tile configuration: BN (a multiple of 32 -- the epilogue's box width -- up
-// to 224 for E2M1 / 256 for E4M3) and the cluster shape CM x CN. The cost
+// Tile configuration: BN (a multiple of 16 up to 240 for E2M1 / 256 for E4M3;
+// the epilogue masks the part of its last 32-column box past the tile) and the
+// cluster shape CM x CN. The cost
 // model: a problem takes `rounds` waves of super-tiles over the clusters;
-// each K stage costs the larger of its MMA time (one M=128, N=BN MMA per 32
-// bytes, about 125 clocks at N=256 on GB300) and the time for the whole stage
-// to land in this SM's shared memory (about 80 bytes per clock per SM
-// measured for TMA into the ring; multicast inside a cluster lowers L2 reads
-// but not the bytes each SM receives, so clusters only change the wave
-// count); with the accumulator double-buffered only the last tile's epilogue
-// (about 8 clocks per output column) is exposed.
+// each K stage costs the largest of its MMA time (one M=128 MMA per 32 bytes,
+// about 116 clocks on GB300 whatever N up to 256), the time for the whole
+// stage to land in this SM's shared memory (about 95 bytes per clock per SM
+// for TMA into the ring; multicast inside a cluster lowers L2 reads but not
+// the bytes each SM receives, so clusters only change the wave count), and
+// the measured pipelined stage time of about 640 clocks per 128-byte stage;
+// with the accumulator double-buffered only the last tile's epilogue (about 8
+// clocks per output column) is exposed.
 // BT_TC_CONFIG="cm,cn,bn" overrides the choice.
 struct TileCfg {
     int cm, cn, bn;
@@ -532,7 +538,7 @@ TileCfg choose_cfg(int64_t M, int64_t N, int nk, int rowb, int sms, int max_bn) 
     if (const char *env = std::getenv("BT_TC_CONFIG")) {
         int cm = 0, cn = 0, bn = 0;
         if (std::sscanf(env, "%d,%d,%d", &cm, &cn, &bn) == 3 && (cm == 1 || cm == 2) && (cn == 1 || cn == 2) &&
-            bn >= 32 && bn <= max_bn && bn % 32 == 0)
+            bn >= 32 && bn <= max_bn && bn % 16 == 0 && (bn / cm) % 16 == 0)
             return TileCfg{cm, cn, bn};
     }
     const int64_t num_m = (M + kBM - 1) / kBM;
@@ -540,13 +546,16 @@ TileCfg choose_cfg(int64_t M, int64_t N, int nk, int rowb, int sms, int max_bn) 
     for (int cm = 1; cm <= 2; ++cm) {
         for (int cn = 1; cn <= 2; ++cn) {
             const int64_t clusters = sms / (cm * cn);
-            for (int bn = max_bn; bn >= 32; bn -= 32) {
+            for (int bn = max_bn; bn >= 32; bn -= 16) {
+                if ((bn / cm) % 16 != 0) continue;           // B slice rows: whole 16-row groups
                 const int64_t num_n = (N + bn - 1) / bn;
                 const int64_t super = ((num_m + cm - 1) / cm) * ((num_n + cn - 1) / cn);
                 const int64_t rounds = (super + clusters - 1) / clusters;
-                const double mma = (rowb / 32) * 125.0 * bn / 256.0;
-                const double bytes = static_cast<double>(kBM + bn) * rowb;
-                const double stage = mma > bytes / 80.0 ? mma : bytes / 80.0;
+                const double mma = (rowb / 32) * 116.0;
+                const double land = static_cast<double>(kBM + bn) * rowb / 95.0;
+                const double piped = 640.0 * rowb / 128.0;
+                double stage = mma > land ? mma : land;
+                if (piped > stage) stage = piped;
                 const double cost = static_cast<double>(rounds) * nk * stage + 8.0 * bn + 600.0;
                 if (best_cost < 0.0 || cost < best_cost * 0.999) {
                     best_cost = cost;
@@ -570,7 +579,7 @@ cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs 
     if (attr_err != cudaSuccess) return attr_err;
     const int csize = a.cm * a.cn;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -578,8 +587,9 @@ cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs 
     attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     // as many clusters as fit at once on the device, at most one per super-tile
     int clusters = sm_count() / csize;
     if (csize > 1) {
@@ -645,7 +655,7 @@ cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code,
     a.M = M; a.N = N; a.nk = static_cast<int>((rb + 127) / 128); a.alpha = alpha; a.out = out; a.err = err;
     const int64_t ob = out_elem_bytes(out_t);
     a.vec_store = ((N * ob) % 16 == 0) && aligned(out, 16) ? 1 : 0;
-    const TileCfg c = choose_cfg(M, N, a.nk, 128, sm_count(), code == BT_CODE_E2M1 ? 224 : 256);
+    const TileCfg c = choose_cfg(M, N, a.nk, 128, sm_count(), code == BT_CODE_E2M1 ? 240 : 256);
     if (!set_grid(a, c, M, N)) return cudaErrorInvalidValue;
     a.idesc = make_idesc(code, a.bn);
     CUtensorMap ma, mb;
@@ -667,7 +677,7 @@ cudaError_t launch_tc_conv(const uint8_t *xp, const uint8_t *wp, bt_code code, c
     a.s = g.s; a.p = g.p; a.d = g.d; a.k = g.k;
     a.cpt = static_cast<int>(rbc / rowb); a.rbc = static_cast<int>(rbc);
     a.nk = g.k * g.k * a.cpt;
-    const TileCfg c = choose_cfg(a.M, a.N, a.nk, rowb, sm_count(), code == BT_CODE_E2M1 ? 224 : 256);
+    const TileCfg c = choose_cfg(a.M, a.N, a.nk, rowb, sm_count(), code == BT_CODE_E2M1 ? 240 : 256);
     if (!set_grid(a, c, a.M, a.N)) return cudaErrorInvalidValue;
     a.idesc = make_idesc(code, a.bn);
     a.vec_store = 0;

@@ -116,11 +116,16 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
     return r;
 }
 
-// Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
+// Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of
+// 16) of data read once: L2 evict-first.
+__device__ __forceinline__ void bulk_load_once(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "{\n"
+        ".reg .b64 pol;\n"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n"
+        "}\n" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
 // im2col mode over an NHWC tensor: coordinates {c, w, h, n} of the window's
