@@ -2,8 +2,8 @@
 
 One step = one forward over one batch of synthetic input: shift + sign +
 pack of the activations, the packed contraction and the fused scale + cast
-epilogue. Weights are packed once, before timing (the pages' weights are
-packed offline by w_pack). Default workload: the 4096 x 4096 x 4096 bf16
+epilogue. Weights are packed once, before timing (bitorch-engine packs
+weights offline, in generate_quantized_weight / w_pack). Default workload: the 4096 x 4096 x 4096 bf16
 linear layer with a scalar activation bias.
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own
@@ -349,7 +349,7 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": {"popc": "b1 (xor+popc, int32 acc)", "e4m3": "fp8 e4m3 +-1 (fp32 acc, exact)",
                   "e2m1": "fp4 e2m1 +-1 (fp32 acc, exact)"}[algo_name],
-        "data": "synthetic (seeded, shapes of the pages' layers)",
+        "data": "synthetic (seeded; shapes of binarized LLM linear and ResNet conv layers)",
         "config": {"workload": wl.name, "M": M, "N": N, "K": K, "x_dtype": wl.x_dtype,
                    "out_dtype": wl.out_dtype, "code": algo_name, "weights": "pre-packed outside timing",
                    "l2": f"inputs+outputs rotate over {nbuf} buffers ({nbuf * (x_bytes + out_bytes) / 1e6:.0f} MB > L2)",
@@ -441,7 +441,7 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": "binary GOPS (2*M*N*K/s)", "value": round(value, 3), "unit": "GOPS",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 +-1 (int32 acc)",
-            "data": "synthetic (seeded, shapes of the pages' layers)",
+            "data": "synthetic (seeded; shapes of binarized LLM linear and ResNet conv layers)",
             "config": {"workload": wl.name, "sample_rows": rows},
             "cpu_baseline": {"value": round(value, 3), "unit": "GOPS", "cores": cores, "kind": "oracle",
                              "sample": sample},

@@ -29,9 +29,8 @@
  * Binarization rule: +1 where x + bias >= 0 (the sum in IEEE fp32 without
  * flushing subnormals, whose sign is the sign of the exact sum), else -1;
  * -0.0 gives +1 and NaN gives -1. Weights use the same rule without a shift.
- * The pages' spec writes the shift as x - bias_a; the pages' code adds
- * it (x + bias_a.view(1,-1,1,1)); this library adds it, so pass -b for the
- * other convention.
+ * The shift is added, as BinaryConv2dCutlass.set_activation does
+ * (x + bias_a.view(1,-1,1,1)); for a subtracted shift (x - b), pass -b.
  */
 #ifndef BT_H
 #define BT_H

@@ -21,8 +21,7 @@ plain numpy / PyTorch CPU ops. Every function cites the passage it follows:
 * torch/ao/quantization/experimental/linear.py, ``LinearAPoT.matmul``: the
   plain i-j-k triple loop of a matrix product.
 
-Readings where the pages leave a step open (each also listed in the design
-notes of the repository):
+Readings where the sources leave a step open:
 
 1. The binarization threshold: ``x + bias >= 0`` gives +1, anything else
    (negative, NaN) gives -1; -0.0 gives +1. Weights are binarized with the

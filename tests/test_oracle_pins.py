@@ -1,6 +1,7 @@
 """Pins for the CPU oracle, checked against things other than itself.
 
-Each pin comes from the pages or from mathematics: hand-worked examples
+Each pin comes from the sources (bitorch-engine's binary layers, the
+im2col+gemm write-up) or from mathematics: hand-worked examples
 (tests/golden/hand_examples.json), brute force with Python integers on tiny
 inputs, the invariants of a +1/-1 dot product (|dot| <= K, dot = K (mod 2),
 dot = K - 2*hamming), torch's own conv2d and the unfold + mm lowering of

@@ -10,7 +10,8 @@ where the workload is bf16. Scales are ``mean|.|`` of the cast tensor,
 reduced in float64 and rounded once to fp32. A scalar activation bias, where
 one is used, is drawn from U(-0.1, 0.1) in fp32.
 
-The shapes are those of the layers the pages talk about: a small linear, an
+The shapes are those of the binarized layers bitorch-engine and the
+im2col+gemm write-up deal with: a small linear, an
 LLM projection (4096 x 4096), ResNet-style 3x3 convolutions (stride 1; stride
 2 with dilation 1 and 2), and a large linear plus one with ragged M, N, K.
 """
