@@ -250,9 +250,17 @@ def run_ours(args, rank, world):
         Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
         Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
         outs = [torch.empty((B, N, Ho, Wo), dtype=out_t, device=dev) for _ in range(nbuf)]
-        ws = torch.empty(bt.bt_binary_conv2d_workspace(B, C, H, W, bt.BT_BF16, code), dtype=torch.uint8, device=dev)
+        geom = (B, C, H, W, k, wl.stride, wl.padding, wl.dilation)
+        ws = torch.empty(bt.bt_binary_conv2d_workspace(*geom, bt.BT_BF16, code), dtype=torch.uint8, device=dev)
         xp_shape = (B, H, W, bt.bt_packed_row_bytes(C, code))
-    xp = ws[: int(np.prod(xp_shape))].view(*xp_shape)
+        # the contraction's own workspace (im2col rows) when it takes packed pixels
+        ws_packed = bt.bt_binary_conv2d_workspace(*geom, bt.BT_PACKED, code)
+        ws_rows = torch.empty(ws_packed, dtype=torch.uint8, device=dev) if ws_packed else None
+    xp = torch.empty(xp_shape, dtype=torch.uint8, device=dev)
+
+    # kernels per step: the pack, then the contraction (a tensor-core convolution
+    # first unfolds the packed pixels into im2col rows: one more kernel)
+    launches_per_step = 3 if (wl.kind == "conv" and code != bt.BT_CODE_BITS) else 2
 
     def step(i, ev=None):
         x, out = xs[i % nbuf], outs[i % nbuf]
@@ -271,7 +279,8 @@ def run_ours(args, rank, world):
         else:
             C, k = wl.x.shape[1], wl.w.shape[2]
             bt.bt_binary_conv2d(xp, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
-                                wl.scale_w, out=out, out_dtype=out_t, algo=algo, x_packed=True)
+                                wl.scale_w, out=out, out_dtype=out_t, algo=algo, x_packed=True,
+                                workspace=ws_rows)
         if ev is not None:
             ev[2].record(stream)
 
@@ -364,7 +373,7 @@ def run_ours(args, rank, world):
         "e2e": {"value": round(e2e_value, 1), "unit": "GOPS",
                 "h2d_bytes_per_step": int(x_bytes), "d2h_bytes_per_step": int(out_bytes),
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -167,14 +167,25 @@ bt_status bt_binary_linear(const void *x, bt_dtype x_dtype,
                            void *out, bt_dtype out_dtype, bt_algo algo,
                            void *workspace, size_t workspace_bytes, bt_stream stream);
 
-/* Workspace bytes bt_binary_conv2d needs (0 when x is BT_PACKED). */
+/*
+ * Workspace bytes bt_binary_conv2d needs for this geometry: the packed NHWC
+ * activations (unless x is BT_PACKED), then, for the tensor-core codes
+ * (E4M3 / E2M1), the im2col rows [B*Ho*Wo, k*k*bt_packed_row_bytes(C, code)]
+ * the contraction reads, each part rounded up to 256 bytes. 0 when nothing is
+ * needed (BITS with BT_PACKED x), for invalid arguments, and beyond the sizes
+ * bt_binary_conv2d serves.
+ */
 size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W,
+                                  int kernel_size, int stride, int padding, int dilation,
                                   bt_dtype x_dtype, bt_code code);
 
 /*
  * bt_binary_conv2d -- BinaryConv2dForward.forward(x, weight, scale_a, scale_w,
- * is_train=False, kernel_size, stride, padding, dilation) as an implicit-im2col
- * contraction over channel-packed NHWC activations.
+ * is_train=False, kernel_size, stride, padding, dilation) as an im2col
+ * contraction over channel-packed NHWC activations: BITS contracts the
+ * packed pixels in place (the im2col is implicit, in shared memory); E4M3 /
+ * E2M1 first unfold them into im2col rows in the workspace, then run the
+ * tensor-core contraction on those rows.
  *
  *   x          device NCHW [B, C, H, W] in x_dtype, or BT_PACKED:
  *              [B, H, W, bt_packed_row_bytes(C, w_code)].
@@ -188,6 +199,12 @@ size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W,
  *              bias_a.view(1,-1,1,1)). Ignored for BT_PACKED.
  *   out        device NCHW [B, O, Ho, Wo] in out_dtype.
  *   kernel_size >= 1, stride >= 1, padding >= 0, dilation >= 1.
+ *   workspace  device, >= bt_binary_conv2d_workspace(B, C, H, W, kernel_size,
+ *              stride, padding, dilation, x_dtype, w_code) bytes, 256-byte
+ *              aligned (may be NULL when that is 0).
+ * Errors: BT_ERR_WORKSPACE when the workspace is missing or too small;
+ * BT_ERR_UNSUPPORTED beyond the sizes served (C*k*k > 16384 for E4M3/E2M1,
+ * more than 65535*128 output pixels, H or W > 2^20).
  */
 bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype,
                            const void *weight, bt_code w_code,

@@ -54,11 +54,25 @@ def test_workspace_queries():
     assert bt.bt_binary_linear_workspace(4096, 4096, bt.BT_BF16, bt.BT_CODE_BITS) == 4096 * 512
     assert bt.bt_binary_linear_workspace(3, 33, bt.BT_F32, bt.BT_CODE_BITS) == 256
     assert bt.bt_binary_linear_workspace(10, 10, bt.BT_PACKED, bt.BT_CODE_BITS) == 0
-    assert bt.bt_binary_conv2d_workspace(2, 256, 14, 14, bt.BT_F32, bt.BT_CODE_E2M1) == \
-        2 * 14 * 14 * 128
-    assert bt.bt_binary_conv2d_workspace(2, 128, 14, 14, bt.BT_F32, bt.BT_CODE_E2M1) == \
-        2 * 14 * 14 * 64
-    assert bt.bt_binary_conv2d_workspace(1, 1, 1, 1, bt.BT_F32, bt.BT_CODE_BITS) == 256
+    ws = bt.bt_binary_conv2d_workspace
+    # BITS: the packed NHWC pixels only
+    assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_BITS) == 2 * 14 * 14 * 32
+    assert ws(1, 1, 1, 1, 1, 1, 0, 1, bt.BT_F32, bt.BT_CODE_BITS) == 256
+    assert ws(1, 1, 1, 1, 1, 1, 0, 1, bt.BT_PACKED, bt.BT_CODE_BITS) == 0
+    # E2M1: packed pixels, then the im2col rows [B*Ho*Wo, k*k*row_bytes(C)]
+    assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) == \
+        2 * 14 * 14 * 128 + 2 * 14 * 14 * 9 * 128
+    assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_PACKED, bt.BT_CODE_E2M1) == 2 * 14 * 14 * 9 * 128
+    # stride 2, padding 1 on 28 x 28 -> 14 x 14 outputs; 128 channels -> 64-byte pixels
+    assert ws(2, 128, 28, 28, 3, 2, 1, 1, bt.BT_BF16, bt.BT_CODE_E2M1) == \
+        2 * 28 * 28 * 64 + 2 * 14 * 14 * 9 * 64
+    # E4M3: one byte per channel; each part rounded up to 256 bytes
+    # (25 pixels x 64 B = 1600 -> 1792; 3 x 3 outputs x 9 taps x 64 B = 5184 -> 5376)
+    assert ws(1, 3, 5, 5, 3, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E4M3) == 1792 + 5376
+    # invalid geometry or arguments
+    assert ws(1, 8, 4, 4, 0, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
+    assert ws(1, 8, 4, 4, 3, 0, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
+    assert ws(1, 8, 4, 4, 3, 1, 0, 1, bt.BT_F32, 7) == 0
 
 
 # Host validation. Pointers below are never dereferenced: every call fails
@@ -119,6 +133,10 @@ def test_conv_validation():
     assert conv(sa=0.0) == bt.BT_ERR_INVALID_ARG
     assert conv(x=264 + 1) == bt.BT_ERR_ALIGNMENT
     assert conv(ws=None) == bt.BT_ERR_WORKSPACE
+    # the tensor-core codes need the im2col rows even for packed pixels
+    assert conv(xt=bt.BT_PACKED, code=bt.BT_CODE_E2M1, ws=None) == bt.BT_ERR_WORKSPACE
+    assert conv(xt=bt.BT_PACKED, code=bt.BT_CODE_E4M3, ws=4096, wsb=1024) == bt.BT_ERR_WORKSPACE
+    assert conv(xt=bt.BT_PACKED, code=bt.BT_CODE_E2M1, ws=4096 + 16, wsb=1 << 20) == bt.BT_ERR_ALIGNMENT
     assert conv(B=0) == bt.BT_OK
     assert conv(O=0, x=None) == bt.BT_OK
 

@@ -63,10 +63,73 @@ def test_pack_rows(code, dtype, K):
         np.testing.assert_array_equal(got, want)
 
 
+# Shifts around which the sign decision is delicate: values of -b that the
+# input type cannot represent (the comparison must round them the right way),
+# ones it can (x = -b gives +1), signed zeros, a subnormal, values past the
+# fp16 range, the fp32 extremes, and non-finite shifts.
+EDGE_SHIFTS = [0.05, -0.1, 0.125, -0.0, 0.0, 1e-40, -1e-40, 65504.0, 70000.0, -70000.0, 1.0000001,
+               3.0e38, -3.0e38, float("inf"), -float("inf"), float("nan")]
+
+
+def _all_16bit(dtype):
+    """Every bit pattern of a 2-byte float type, as a [64, 1024] tensor."""
+    bits = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16)
+    return bits.view(dtype).reshape(64, 1024)
+
+
+def _near_f32(values):
+    """fp32 values next to each of `values` (4 steps either way) and the specials."""
+    out = [0.0, -0.0, float("inf"), -float("inf"), float("nan"), 1e-45, -1e-45, 3.4e38, -3.4e38]
+    for v in values:
+        t = torch.tensor([v], dtype=torch.float32)
+        for direction in (float("inf"), -float("inf")):
+            u = t.clone()
+            for _ in range(4):
+                u = torch.nextafter(u, torch.tensor([direction]))
+                out.append(float(u))
+        out.append(float(t))
+    x = torch.tensor(out, dtype=torch.float32)
+    pad = (-x.numel()) % 64
+    return torch.cat([x, torch.zeros(pad)]).reshape(-1, 64)
+
+
 @pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+def test_pack_rows_sign_decision_edges(code, dtype):
+    # 2-byte inputs: every bit pattern against every edge shift; fp32: the
+    # neighbours of -b. Scalar shifts use the threshold comparison (finite) or
+    # the fp32 sum (non-finite); both must equal the oracle's sign of x + b.
+    for b in EDGE_SHIFTS:
+        x = _all_16bit(dtype) if dtype != torch.float32 else _near_f32([-b] + [-v for v in EDGE_SHIFTS])
+        bias = torch.tensor([b], dtype=torch.float32)
+        got = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_ROWS, bias.to(DEV)).cpu().numpy()
+        want = oracle.pack_rows(oracle.binarize(x, bias, channel_axis=-1), code)
+        np.testing.assert_array_equal(got, want, err_msg=f"shift {b}")
+    # a per-column shift holding all of them at once
+    x = _all_16bit(dtype) if dtype != torch.float32 else _near_f32([-v for v in EDGE_SHIFTS])
+    cols = torch.tensor(EDGE_SHIFTS, dtype=torch.float32).repeat(x.shape[1] // len(EDGE_SHIFTS) + 1)[: x.shape[1]]
+    got = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_ROWS, cols.to(DEV)).cpu().numpy()
+    want = oracle.pack_rows(oracle.binarize(x, cols, channel_axis=-1), code)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_pack_nhwc_sign_decision_edges(code, dtype):
+    # every bit pattern as NCHW [4, 16, 32, 32], against each edge shift as a
+    # scalar and against all of them as the 16 per-channel shifts
+    x = _all_16bit(dtype).reshape(4, 16, 32, 32)
+    for bias in [torch.tensor([b], dtype=torch.float32) for b in EDGE_SHIFTS] + \
+            [torch.tensor(EDGE_SHIFTS, dtype=torch.float32)]:
+        got = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC, bias.to(DEV)).cpu().numpy()
+        want = oracle.pack_nchw_to_nhwc(oracle.binarize(x, bias, channel_axis=1), code)
+        np.testing.assert_array_equal(got, want, err_msg=f"shift {bias.tolist()}")
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("shape", [(2, 3, 5, 5), (3, 37, 4, 4), (2, 64, 14, 14), (1, 130, 7, 9),
-                                   (4, 256, 3, 3)])
+                                   (4, 256, 3, 3), (2, 128, 28, 28), (1, 700, 10, 10), (1, 6200, 3, 3)])
 def test_pack_nchw_to_nhwc(code, dtype, shape):
     x = _gen(sum(shape), shape, dtype)
     for bias in (None, torch.tensor([-0.1]), torch.linspace(-0.3, 0.3, shape[1])):
@@ -193,6 +256,23 @@ def test_conv_f32_scalar_bias(code):
     bias = torch.tensor([0.2])
     got = gpu_conv(x, w, code, 1, 1, 1, 0.5, 2.0, bias, "f32")
     assert_close_rel(got, oracle.binary_conv2d(x, w, 0.5, 2.0, 1, 1, 1, bias, "f32"))
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+def test_conv_prepacked_input(code):
+    # packed NHWC pixels in, through a caller workspace sized by the query
+    B, C, H, W, O, k, s, p, d = 2, 96, 9, 11, 50, 3, 2, 1, 1
+    x = _gen(11, (B, C, H, W), torch.bfloat16)
+    w = _gen(12, (O, C, k, k), torch.bfloat16)
+    xp = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    nbytes = bt.bt_binary_conv2d_workspace(B, C, H, W, k, s, p, d, bt.BT_PACKED, code)
+    assert (nbytes == 0) == (code == bt.BT_CODE_BITS)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=DEV) if nbytes else None
+    got = bt.bt_binary_conv2d(xp, wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32, x_packed=True,
+                              workspace=ws).cpu()
+    want = oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d)
+    assert torch.equal(got, torch.from_numpy(want))
 
 
 # ---------------------------------------------------------------------------

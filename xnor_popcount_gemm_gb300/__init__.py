@@ -59,7 +59,7 @@ _c_pack = _sig("bt_pack_sign", _i, [_p, _i, _i, _i64, _i64, _i64, _i64, _p, _i64
 _c_lin_ws = _sig("bt_binary_linear_workspace", _sz, [_i64, _i64, _i, _i])
 _c_lin = _sig("bt_binary_linear", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _i64, _p, _i, _i,
                                        _p, _sz, _p])
-_c_conv_ws = _sig("bt_binary_conv2d_workspace", _sz, [_i64, _i64, _i64, _i64, _i, _i])
+_c_conv_ws = _sig("bt_binary_conv2d_workspace", _sz, [_i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _i])
 _c_conv = _sig("bt_binary_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
                                         _f, _f, _p, _i64, _p, _i, _i, _p, _sz, _p])
 _c_lin_noalloc = _sig("bt_binary_linear_noalloc", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _i64,
@@ -143,8 +143,9 @@ def bt_binary_linear_workspace(M: int, K: int, x_dtype: int, code: int) -> int:
     return int(_c_lin_ws(M, K, x_dtype, code))
 
 
-def bt_binary_conv2d_workspace(B: int, C: int, H: int, W: int, x_dtype: int, code: int) -> int:
-    return int(_c_conv_ws(B, C, H, W, x_dtype, code))
+def bt_binary_conv2d_workspace(B: int, C: int, H: int, W: int, kernel_size: int, stride: int,
+                               padding: int, dilation: int, x_dtype: int, code: int) -> int:
+    return int(_c_conv_ws(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype, code))
 
 
 def _workspace(nbytes: int, device, ws):
@@ -201,7 +202,8 @@ def bt_binary_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int,
     Wo = conv2d_out_size(W, kernel_size, stride, padding, dilation)
     if out is None:
         out = torch.empty((B, O, max(Ho, 0), max(Wo, 0)), dtype=_TORCH[ot], device=x.device)
-    ws = _workspace(bt_binary_conv2d_workspace(B, C, H, W, xt, w_code), x.device, workspace)
+    ws = _workspace(bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, xt, w_code),
+                    x.device, workspace)
     blen = 0 if bias_a is None else bias_a.numel()
     _check(_c_conv(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding,
                    dilation, scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),

@@ -155,10 +155,26 @@ bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, 
                                       w_code, M, N, K, alpha, out, out_dtype, err, s));
 }
 
-size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, bt_dtype x_dtype,
-                                  bt_code code) {
-    if (B < 0 || C < 1 || H < 1 || W < 1 || !valid_code(code) || x_dtype == BT_PACKED) return 0;
-    return round_up(static_cast<size_t>(B) * H * W * static_cast<size_t>(row_bytes(C, code)), 256);
+size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride,
+                                  int padding, int dilation, bt_dtype x_dtype, bt_code code) {
+    if (B < 0 || C < 1 || H < 1 || W < 1 || !valid_code(code)) return 0;
+    if (kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return 0;
+    if (B > (int64_t(1) << 30) || C > kMaxK || H > (1 << 20) || W > (1 << 20) || kernel_size > 64 ||
+        padding > (1 << 20) || stride > (1 << 20) || dilation > (1 << 10))
+        return 0;
+    const int64_t rbc = row_bytes(C, code);
+    const double approx = static_cast<double>(B) * H * W * rbc +
+                          static_cast<double>(B) * H * W * kernel_size * kernel_size * rbc;
+    if (approx > 4.0e18) return 0;
+    size_t n = 0;
+    if (x_dtype != BT_PACKED) n += round_up(static_cast<size_t>(B * H * W * rbc), 256);   // packed NHWC pixels
+    if (code != BT_CODE_BITS) {                                                            // im2col rows
+        ConvGeom g{B, C, H, W, 0, 0, 0, kernel_size, stride, padding, dilation};
+        g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
+        g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
+        n += round_up(static_cast<size_t>(im2col_bytes(g, rbc)), 256);
+    }
+    return n;
 }
 
 bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
@@ -194,14 +210,20 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
     if (run != BT_ALGO_POPC && C * kk > kTcMaxK) return BT_ERR_UNSUPPORTED;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t need = bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype,
+                                                   w_code);
+    const bool needs_ws = x_dtype != BT_PACKED || run != BT_ALGO_POPC;
+    if (needs_ws && need == 0) return BT_ERR_UNSUPPORTED;      // beyond the sizes the query serves
+    if (needs_ws && (workspace == nullptr || workspace_bytes < need)) return BT_ERR_WORKSPACE;
+    if (needs_ws && !aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t rbc = row_bytes(C, w_code);
     const void *xp = x;
     if (x_dtype != BT_PACKED) {
-        const size_t need = bt_binary_conv2d_workspace(B, C, H, W, x_dtype, w_code);
-        if (workspace == nullptr || workspace_bytes < need) return BT_ERR_WORKSPACE;
-        if (!aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
-        cudaError_t e = launch_pack_nhwc(x, x_dtype, B, C, H * W, bias_a, bias_len, w_code, workspace, s);
+        cudaError_t e = launch_pack_nhwc(x, x_dtype, B, C, H * W, bias_a, bias_len, w_code, ws, s);
         if (e != cudaSuccess) return BT_ERR_CUDA;
-        xp = workspace;
+        xp = ws;
+        ws += round_up(static_cast<size_t>(B * H * W * rbc), 256);
     }
     const float alpha = alpha_of(scale_a, scale_w);
     if (run == BT_ALGO_POPC)
@@ -209,8 +231,10 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
                                           g, alpha, out, out_dtype, s));
     unsigned int *err = device_error_word();
     if (err == nullptr) return BT_ERR_CUDA;
-    return from_cuda(launch_tc_conv(static_cast<const uint8_t *>(xp), static_cast<const uint8_t *>(weight), w_code,
-                                    g, alpha, out, out_dtype, err, s));
+    cudaError_t e = launch_im2col_rows(static_cast<const uint8_t *>(xp), g, rbc, ws, s);
+    if (e != cudaSuccess) return BT_ERR_CUDA;
+    return from_cuda(launch_tc_conv(ws, static_cast<const uint8_t *>(weight), w_code, g, alpha, out, out_dtype, err,
+                                    s));
 }
 
 bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo) {

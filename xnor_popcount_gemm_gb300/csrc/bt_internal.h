@@ -48,6 +48,15 @@ struct ConvGeom {
     int k, s, p, d;
 };
 
+// im2col rows: channel-packed pixels [B, H, W, row_bytes(C)] -> [B*Ho*Wo,
+// k*k*row_bytes(C)], row (b, ho, wo) holding the packed pixel of every filter
+// tap (kh, kw) in turn, zeros for a tap in the padding. Row bytes a multiple
+// of 16.
+cudaError_t launch_im2col_rows(const uint8_t *xp, const ConvGeom &g, int64_t rbc, uint8_t *rows,
+                               cudaStream_t s);
+// Bytes of that matrix.
+inline int64_t im2col_bytes(const ConvGeom &g, int64_t rbc) { return g.B * g.Ho * g.Wo * g.k * g.k * rbc; }
+
 cudaError_t launch_popc_linear(const uint32_t *xp, const uint32_t *wp, int64_t M, int64_t N,
                                int64_t K, float alpha, void *out, bt_dtype out_t, cudaStream_t s);
 cudaError_t launch_popc_conv(const uint32_t *xp, const uint32_t *wp, const ConvGeom &g, float alpha,
@@ -56,7 +65,8 @@ cudaError_t launch_popc_conv(const uint32_t *xp, const uint32_t *wp, const ConvG
 cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M,
                              int64_t N, int64_t K, float alpha, void *out, bt_dtype out_t,
                              unsigned int *err, cudaStream_t s);
-cudaError_t launch_tc_conv(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g,
+// rows: the im2col rows of the packed input (launch_im2col_rows); output NCHW.
+cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code, const ConvGeom &g,
                            float alpha, void *out, bt_dtype out_t, unsigned int *err,
                            cudaStream_t s);
 

@@ -85,6 +85,162 @@ __device__ __forceinline__ void store_group(uint8_t *dst, uint32_t neg, uint32_t
     }
 }
 
+// ---------------------------------------------------------------------------
+// Sign masks. For a finite shift b, x + b >= 0 (the fp32 sum, exact in sign)
+// holds exactly when x >= -b, and for x of a 2-byte type exactly when x >= t
+// with t = -b rounded up to that type (the smallest value of the type that is
+// >= -b; +inf past its range). So 2-byte inputs are compared two at a time
+// against t, without widening. A non-finite b takes the fp32 sum itself.
+// The masks come out as two words P0 (values 0..3) and P1 (values 4..7), byte
+// e 0xFF where value e binarizes to +1, else 0.
+// ---------------------------------------------------------------------------
+template <typename T> struct Thresh;
+template <> struct Thresh<__nv_bfloat16> {
+    using type = __nv_bfloat162;
+    __device__ __forceinline__ static type of(float neg_b) {
+        const __nv_bfloat16 t = __float2bfloat16_ru(neg_b);
+        return __halves2bfloat162(t, t);
+    }
+    __device__ __forceinline__ static uint32_t ge(uint32_t w, type t) {
+        return __hge2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w), t);
+    }
+};
+template <> struct Thresh<__half> {
+    using type = __half2;
+    __device__ __forceinline__ static type of(float neg_b) {
+        const __half t = __float2half_ru(neg_b);
+        return __halves2half2(t, t);
+    }
+    __device__ __forceinline__ static uint32_t ge(uint32_t w, type t) {
+        return __hge2_mask(*reinterpret_cast<const __half2 *>(&w), t);
+    }
+};
+
+// Masks of one group from its 16-byte (2-byte types) or 2 x 16-byte (fp32)
+// loads against a threshold (finite shift).
+template <typename T>
+__device__ __forceinline__ void masks_ge(const Group<T> &g, float neg_b, uint32_t &P0, uint32_t &P1) {
+    if constexpr (sizeof(T) == 2) {
+        const typename Thresh<T>::type t = Thresh<T>::of(neg_b);
+        const uint32_t m0 = Thresh<T>::ge(g.q[0].x, t), m1 = Thresh<T>::ge(g.q[0].y, t);
+        const uint32_t m2 = Thresh<T>::ge(g.q[0].z, t), m3 = Thresh<T>::ge(g.q[0].w, t);
+        P0 = __byte_perm(m0, m1, 0x6420);
+        P1 = __byte_perm(m2, m3, 0x6420);
+    } else {
+        uint32_t s[8];
+        const uint32_t w[8] = {g.q[0].x, g.q[0].y, g.q[0].z, g.q[0].w, g.q[1].x, g.q[1].y, g.q[1].z, g.q[1].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[e] = __uint_as_float(w[e]) >= neg_b ? 0xFFFFFFFFu : 0u;
+        P0 = __byte_perm(__byte_perm(s[0], s[1], 0x0040), __byte_perm(s[2], s[3], 0x0040), 0x5410);
+        P1 = __byte_perm(__byte_perm(s[4], s[5], 0x0040), __byte_perm(s[6], s[7], 0x0040), 0x5410);
+    }
+}
+
+// The same from the fp32 sums x + b (any shift, one per value).
+__device__ __forceinline__ void masks_add(const float (&f)[8], const float (&b)[8], uint32_t &P0, uint32_t &P1) {
+    uint32_t s[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] = is_negative(f[e], b[e]) ? 0u : 0xFFFFFFFFu;
+    P0 = __byte_perm(__byte_perm(s[0], s[1], 0x0040), __byte_perm(s[2], s[3], 0x0040), 0x5410);
+    P1 = __byte_perm(__byte_perm(s[4], s[5], 0x0040), __byte_perm(s[6], s[7], 0x0040), 0x5410);
+}
+
+// One byte, bit e set where value e binarizes to +1: one bit gathered from
+// each mask byte with a multiply (the four partial products land on distinct
+// bits, so nothing carries).
+__device__ __forceinline__ uint32_t mask_byte(uint32_t P0, uint32_t P1) {
+    const uint32_t lo = ((P0 & 0x08040201u) * 0x01010101u) >> 24;
+    const uint32_t hi = ((P1 & 0x08040201u) * 0x01010101u) >> 24;
+    return lo | (hi << 4);
+}
+
+// Codes of a full group of 8 from its masks.
+template <int CODE>
+__device__ __forceinline__ void store_masks(uint8_t *dst, uint32_t P0, uint32_t P1) {
+    if (CODE == BT_CODE_BITS) {
+        *dst = static_cast<uint8_t>(mask_byte(P0, P1));
+    } else if (CODE == BT_CODE_E4M3) {
+        // +1 = 0x38, -1 = 0xB8
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(0x38383838u | (~P0 & 0x80808080u), 0x38383838u | (~P1 & 0x80808080u));
+    } else {
+        // +1 = 0x2, -1 = 0xA; value 2i in the low nibble of byte i
+        const uint32_t even = __byte_perm(P0, P1, 0x6420), odd = __byte_perm(P0, P1, 0x7531);
+        *reinterpret_cast<uint32_t *>(dst) = 0x22222222u | (~even & 0x08080808u) | (~odd & 0x80808080u);
+    }
+}
+
+// Division by a divisor fixed per launch, for n < 2^31: q = (hi32(m*n) + n) >> l
+// with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994).
+struct FastDiv {
+    uint32_t d, m, l;
+};
+FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) { return (__umulhi(f.m, n) + n) >> f.l; }
+
+// rows, flat: every output group of every row, numbered g = row * G + j over
+// the whole [R, G] output, kFlatUnroll per thread in flight; group j < Gd
+// holds elements 8j..8j+7 of the row (K a multiple of 8, rows 16-byte
+// aligned), the rest of the row is zero padding. Consecutive threads take
+// consecutive groups: contiguous loads and contiguous stores.
+constexpr int kFlatUnroll = 4;
+
+template <typename T, int CODE, bool COLBIAS>
+__global__ void __launch_bounds__(kPackThreads)
+pack_rows_flat_kernel(const T *__restrict__ x, uint32_t total, FastDiv divG, uint32_t Gd, int K,
+                      const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out) {
+    constexpr int OB = GroupOut<CODE>::kBytes;
+    pdl_launch_dependents();
+    pdl_wait();
+    const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
+    const bool finite = isfinite(bs);
+    const uint32_t stride = gridDim.x * (kPackThreads * kFlatUnroll);
+    for (uint32_t g0 = blockIdx.x * (kPackThreads * kFlatUnroll) + threadIdx.x; g0 < total; g0 += stride) {
+        Group<T> grp[kFlatUnroll];
+        uint32_t col[kFlatUnroll];
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            const uint32_t g = g0 + u * kPackThreads;
+            const uint32_t row = fdiv(g, divG);
+            col[u] = g - row * divG.d;
+            if (g < total && col[u] < Gd) grp[u].load(x + static_cast<int64_t>(row) * K + 8 * col[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            const uint32_t g = g0 + u * kPackThreads;
+            if (g >= total) break;
+            uint8_t *dst = out + static_cast<int64_t>(g) * OB;
+            if (col[u] >= Gd) {
+                store_group<CODE>(dst, 0u, 0u);                 // row padding
+                continue;
+            }
+            uint32_t P0, P1;
+            if (!COLBIAS && finite) {
+                masks_ge<T>(grp[u], -bs, P0, P1);
+            } else {
+                float f[8], b[8];
+                grp[u].unpack(f);
+                if (COLBIAS) {
+                    const float4 b0 = __ldg(reinterpret_cast<const float4 *>(bias + 8 * col[u]));
+                    const float4 b1 = __ldg(reinterpret_cast<const float4 *>(bias + 8 * col[u] + 4));
+                    b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+                    b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) b[e] = bs;
+                }
+                masks_add(f, b, P0, P1);
+            }
+            store_masks<CODE>(dst, P0, P1);
+        }
+    }
+}
+
 // rows: one thread per group of 8 consecutive elements of a row, kGroupsPerThread
 // groups (kRowThreads apart) per thread; blockIdx.y walks the rows. A group
 // wholly inside the row is one or two 16-byte loads (VEC); the row's last,
@@ -324,6 +480,157 @@ pack_nhwc_kernel(const T *__restrict__ x, int B, int C, int HW, const float *__r
     }
 }
 
+// Transpose of an 8 x 8 bit matrix held as 8 bytes (byte i = row i, bit j =
+// column j) into byte j = column j, bit i = row i: three rounds of swapping
+// blocks across the diagonal (the transpose8 method of Warren, Hacker's
+// Delight, section 7-3).
+__device__ __forceinline__ uint64_t transpose8x8(uint64_t v) {
+    uint64_t t = (v ^ (v >> 7)) & 0x00AA00AA00AA00AAull;
+    v = v ^ t ^ (t << 7);
+    t = (v ^ (v >> 14)) & 0x0000CCCC0000CCCCull;
+    v = v ^ t ^ (t << 14);
+    t = (v ^ (v >> 28)) & 0x00000000F0F0F0F0ull;
+    return v ^ t ^ (t << 28);
+}
+
+// nhwc, transposed through shared memory. A unit is (image b, a run of
+// kNhwcPixels pixels, every channel). Phase 1 reads each channel plane's run
+// with 16-byte loads (consecutive threads, consecutive 8-pixel groups of a
+// plane) and keeps one byte of sign bits per (pixel group, channel). Phase 2
+// turns each 8 pixel x 8 channel block around with a bit-matrix transpose and
+// writes the codes of whole pixel rows: consecutive threads take consecutive
+// channel groups of a row, so every store instruction covers whole rows.
+constexpr int kNhwcPixels = 64;
+constexpr int kNhwcGroups = kNhwcPixels / 8;
+constexpr int kNhwcUnroll = 4;
+constexpr int kNhwcMaxSmem = 48 * 1024;
+
+// Bytes of one pixel group's row of channel bytes in shared memory: the
+// channels rounded up to 8, plus 8 so that consecutive rows start in
+// different banks.
+__host__ __device__ __forceinline__ int nhwc_cstride(int C) { return (C + 7) / 8 * 8 + 8; }
+
+template <typename T, int CODE, bool VEC>
+__global__ void __launch_bounds__(kPackThreads)
+pack_nhwc_tr_kernel(const T *__restrict__ x, int C, int HW, int upi, uint32_t units, const float *__restrict__ bias,
+                    int bias_len, uint8_t *__restrict__ out, int rb, FastDiv divG) {
+    constexpr int OB = GroupOut<CODE>::kBytes;
+    extern __shared__ __align__(16) uint8_t sbits[];      // [kNhwcGroups][cstride]
+    const int cstride = nhwc_cstride(C);
+    const int G = static_cast<int>(divG.d);
+    const int tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();
+    const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
+    const int items1 = C * kNhwcGroups;
+
+    for (uint32_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int64_t b = unit / static_cast<uint32_t>(upi);
+        const int p0 = static_cast<int>(unit - static_cast<uint32_t>(b) * upi) * kNhwcPixels;
+        const int npx = HW - p0 < kNhwcPixels ? HW - p0 : kNhwcPixels;
+        const T *xb = x + b * C * static_cast<int64_t>(HW) + p0;
+
+        // phase 1: item it = (channel it / 8, pixel group it % 8)
+        for (int base = 0; base < items1; base += kPackThreads * kNhwcUnroll) {
+            Group<T> grp[kNhwcUnroll];
+#pragma unroll
+            for (int u = 0; u < kNhwcUnroll; ++u) {
+                const int it = base + u * kPackThreads + tid;
+                const int c = it >> 3, px = (it & 7) * 8;
+                if (VEC && it < items1 && px + 8 <= npx) grp[u].load(xb + static_cast<int64_t>(c) * HW + px);
+            }
+#pragma unroll
+            for (int u = 0; u < kNhwcUnroll; ++u) {
+                const int it = base + u * kPackThreads + tid;
+                if (it >= items1) break;
+                const int c = it >> 3, pg = it & 7, px = pg * 8;
+                if (px >= npx) continue;
+                const float bc = bias_len > 1 ? __ldg(bias + c) : bs;
+                const bool full = VEC && px + 8 <= npx;
+                uint32_t P0, P1;
+                if (full && isfinite(bc)) {
+                    masks_ge<T>(grp[u], -bc, P0, P1);
+                } else {
+                    float f[8], bb[8];
+                    if (full) {
+                        grp[u].unpack(f);
+                    } else {
+                        const T *src = xb + static_cast<int64_t>(c) * HW + px;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = px + e < npx ? Elem<T>::to_f32(src[e]) : 0.0f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) bb[e] = bc;
+                    masks_add(f, bb, P0, P1);
+                }
+                sbits[pg * cstride + c] = static_cast<uint8_t>(mask_byte(P0, P1));
+            }
+        }
+        __syncthreads();
+
+        // phase 2: item it = (pixel group it / G, channel group it % G)
+        const int npg = (npx + 7) >> 3;
+        for (int it = tid; it < npg * G; it += kPackThreads) {
+            const int pg = static_cast<int>(fdiv(static_cast<uint32_t>(it), divG));
+            const int cg = it - pg * G;
+            const int c0 = cg * 8;
+            const int nj = npx - pg * 8 < 8 ? npx - pg * 8 : 8;
+            uint8_t *dst = out + (b * HW + p0 + pg * 8) * static_cast<int64_t>(rb) + cg * OB;
+            if (c0 >= C) {
+                for (int j = 0; j < nj; ++j) store_group<CODE>(dst + static_cast<int64_t>(j) * rb, 0u, 0u);
+                continue;
+            }
+            const uint32_t cvalid = C - c0 >= 8 ? 0xFFu : (1u << (C - c0)) - 1u;
+            const uint64_t v = transpose8x8(*reinterpret_cast<const uint64_t *>(sbits + pg * cstride + c0));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= nj) break;
+                const uint32_t pos = static_cast<uint32_t>(v >> (8 * j)) & 0xFFu;
+                store_group<CODE>(dst + static_cast<int64_t>(j) * rb, ~pos & cvalid, cvalid);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// im2col rows (the unfold of the im2col write-up, on packed pixels): one
+// thread per (output row m, 16-byte chunk c of a packed pixel) walks the k*k
+// taps, so consecutive threads write consecutive chunks of a tap's slot in the
+// row. The packed input is small and was just written (its reads hit L2); the
+// rows are stored with plain stores so that they stay in L2 for the
+// contraction that reads them next.
+template <typename Idx>
+__global__ void __launch_bounds__(kPackThreads)
+im2col_rows_kernel(const uint4 *__restrict__ xp, int H, int W, int Ho, int Wo, int k, int s, int p, int d,
+                   int cpp, Idx total, uint4 *__restrict__ rows) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t row_chunks = static_cast<int64_t>(k) * k * cpp;
+    for (Idx t = static_cast<Idx>(blockIdx.x) * kPackThreads + threadIdx.x; t < total;
+         t += static_cast<Idx>(gridDim.x) * kPackThreads) {
+        const Idx m = t / static_cast<Idx>(cpp);
+        const int c = static_cast<int>(t - m * static_cast<Idx>(cpp));
+        const Idx r = m / static_cast<Idx>(Wo);
+        const int wo = static_cast<int>(m - r * static_cast<Idx>(Wo));
+        const Idx b = r / static_cast<Idx>(Ho);
+        const int ho = static_cast<int>(r - b * static_cast<Idx>(Ho));
+        const int h0 = ho * s - p, w0 = wo * s - p;
+        const uint4 *src = xp + static_cast<int64_t>(b) * H * W * cpp + c;
+        uint4 *dst = rows + static_cast<int64_t>(m) * row_chunks + c;
+        for (int kh = 0; kh < k; ++kh) {
+            const int hi = h0 + kh * d;
+            const bool hin = hi >= 0 && hi < H;
+#pragma unroll 4
+            for (int kw = 0; kw < k; ++kw) {
+                const int wi = w0 + kw * d;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (hin && wi >= 0 && wi < W) v = __ldg(src + (static_cast<int64_t>(hi) * W + wi) * cpp);
+                dst[(kh * k + kw) * cpp] = v;
+            }
+        }
+    }
+}
+
 int grid_for(int64_t threads) {
     int64_t blocks = (threads + kPackThreads - 1) / kPackThreads;
     const int64_t cap = int64_t(1) << 30;
@@ -339,6 +646,30 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
     const int64_t per_block = kRowThreads * kGroupsPerThread;
     dim3 grid(static_cast<unsigned>((G + per_block - 1) / per_block), static_cast<unsigned>(R < 65535 ? R : 65535));
     const bool vec = ((K * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned(x, 16);
+    const int64_t total = R * G;
+    const bool colbias = bias_len > 1;
+    if (vec && K % 8 == 0 && total <= (int64_t(1) << 31) - (int64_t(1) << 21) && (!colbias || aligned(bias, 16))) {
+        int sms = 0, dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t per_block = kPackThreads * kFlatUnroll;
+        const int64_t need = (total + per_block - 1) / per_block;
+        const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * (2048 / kPackThreads);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute pdl = pdl_attribute();
+        cfg.gridDim = dim3(static_cast<unsigned>(need < cap ? need : cap));
+        cfg.blockDim = dim3(kPackThreads);
+        cfg.stream = s;
+        cfg.attrs = &pdl;
+        cfg.numAttrs = 1;
+        const FastDiv divG = make_fastdiv(static_cast<uint32_t>(G));
+        const uint32_t Gd = static_cast<uint32_t>(K / 8);
+        if (colbias)
+            return cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true>, x, static_cast<uint32_t>(total), divG,
+                                      Gd, static_cast<int>(K), bias, static_cast<int>(bias_len), out);
+        return cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false>, x, static_cast<uint32_t>(total), divG, Gd,
+                                  static_cast<int>(K), bias, static_cast<int>(bias_len), out);
+    }
     unsigned int *err = device_error_word();
     if (vec && err != nullptr) {
         auto kern = pack_rows_staged_kernel<T, CODE>;
@@ -382,9 +713,35 @@ template <typename T, int CODE>
 cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bias, int64_t bias_len,
                    uint8_t *out, int64_t rb, cudaStream_t s) {
     constexpr int E = Elem<T>::kPerVec;
+    const bool vec = ((HW * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned(x, 16);
+    const int smem = kNhwcGroups * nhwc_cstride(static_cast<int>(C));
+    const int64_t upi = (HW + kNhwcPixels - 1) / kNhwcPixels;
+    const int64_t G = padded_elems<CODE>(rb) / 8;
+    if (smem <= kNhwcMaxSmem && B * upi < (int64_t(1) << 31) && G * kNhwcGroups < (int64_t(1) << 31)) {
+        int sms = 0, dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t units = B * upi;
+        const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * (2048 / kPackThreads);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute pdl = pdl_attribute();
+        cfg.gridDim = dim3(static_cast<unsigned>(units < cap ? units : cap));
+        cfg.blockDim = dim3(kPackThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = s;
+        cfg.attrs = &pdl;
+        cfg.numAttrs = 1;
+        const FastDiv divG = make_fastdiv(static_cast<uint32_t>(G));
+        if (vec)
+            return cudaLaunchKernelEx(&cfg, pack_nhwc_tr_kernel<T, CODE, true>, x, static_cast<int>(C),
+                                      static_cast<int>(HW), static_cast<int>(upi), static_cast<uint32_t>(units), bias,
+                                      static_cast<int>(bias_len), out, static_cast<int>(rb), divG);
+        return cudaLaunchKernelEx(&cfg, pack_nhwc_tr_kernel<T, CODE, false>, x, static_cast<int>(C),
+                                  static_cast<int>(HW), static_cast<int>(upi), static_cast<uint32_t>(units), bias,
+                                  static_cast<int>(bias_len), out, static_cast<int>(rb), divG);
+    }
     const int64_t threads = B * (padded_elems<CODE>(rb) / 8) * ((HW + E - 1) / E);
     const int grid = grid_for(threads);
-    const bool vec = ((HW * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned(x, 16);
     if (vec)
         pack_nhwc_kernel<T, CODE, true><<<grid, kPackThreads, 0, s>>>(x, static_cast<int>(B), static_cast<int>(C),
                                                                       static_cast<int>(HW), bias,
@@ -432,6 +789,34 @@ cudaError_t launch_pack_rows(const void *x, bt_dtype xt, int64_t R, int64_t K, c
         case BT_BF16: return rows_code(static_cast<const __nv_bfloat16 *>(x), R, K, bias, bias_len, code, out, s);
         default: return rows_code(static_cast<const __half *>(x), R, K, bias, bias_len, code, out, s);
     }
+}
+
+cudaError_t launch_im2col_rows(const uint8_t *xp, const ConvGeom &g, int64_t rbc, uint8_t *rows, cudaStream_t s) {
+    const int64_t M = g.B * g.Ho * g.Wo;
+    if (M == 0) return cudaSuccess;
+    const int cpp = static_cast<int>(rbc / 16);
+    const int64_t total = M * cpp;
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;
+    const int64_t blocks = (total + kPackThreads - 1) / kPackThreads;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute pdl = pdl_attribute();
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks < cap ? blocks : cap));
+    cfg.blockDim = dim3(kPackThreads);
+    cfg.stream = s;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    const uint4 *src = reinterpret_cast<const uint4 *>(xp);
+    uint4 *dst = reinterpret_cast<uint4 *>(rows);
+    const int H = static_cast<int>(g.H), W = static_cast<int>(g.W), Ho = static_cast<int>(g.Ho),
+              Wo = static_cast<int>(g.Wo);
+    if (total < (int64_t(1) << 32) - kPackThreads * cap)
+        return cudaLaunchKernelEx(&cfg, im2col_rows_kernel<uint32_t>, src, H, W, Ho, Wo, g.k, g.s, g.p, g.d, cpp,
+                                  static_cast<uint32_t>(total), dst);
+    return cudaLaunchKernelEx(&cfg, im2col_rows_kernel<uint64_t>, src, H, W, Ho, Wo, g.k, g.s, g.p, g.d, cpp,
+                              static_cast<uint64_t>(total), dst);
 }
 
 cudaError_t launch_pack_nhwc(const void *x, bt_dtype xt, int64_t B, int64_t C, int64_t HW,

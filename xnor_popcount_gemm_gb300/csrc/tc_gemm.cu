@@ -1,5 +1,5 @@
 // Tensor-core contraction (tcgen05) over +1/-1 codes, for the linear layer
-// and for the implicit-im2col convolution.
+// and for the convolution lowered to im2col rows.
 //
 // The +1/-1 operands are stored as FP8 E4M3 or FP4 E2M1 codes (the pack
 // kernel writes them); every product is +1 or -1, every partial sum an integer
@@ -8,11 +8,12 @@
 // epilogue applies y = fp32(dot * alpha) and the cast (bitorch-engine
 // BinaryConv2dForward.forward: the native result scaled by
 // scale_a*scale_w, then .to(x.dtype)). Zero codes (row padding, TMA zero fill
-// outside the tensor, and taps that fall in a convolution's zero padding)
-// contribute 0, which is the unfold + mm reading of padding.
+// outside the tensor, and the zero taps the im2col rows hold for a
+// convolution's padding) contribute 0, which is the unfold + mm reading of
+// padding.
 //
 // Persistent, warp-specialised: one CTA per SM walks output tiles of
-// 128 x BN (BN a multiple of 32, chosen per problem so the tiles spread evenly
+// 128 x BN (BN a multiple of 16, chosen per problem so the tiles spread evenly
 // over the SMs). The fp32 accumulator is double-buffered in TMEM (2 x 240
 // columns plus 32 of unit block scales for E2M1, 2 x 256 for E4M3), so a
 // tile's epilogue -- and its output stores -- overlap the next tile's MMAs.
@@ -32,9 +33,9 @@
 //                   straight from registers (consecutive lanes, consecutive
 //                   pixels). Once drained, the buffer goes back to the MMA
 //                   warp.
-// A convolution reads A through TMA im2col mode: for filter tap (kh, kw) the
-// box is 128 consecutive output pixels, each shifted by (kh*d, kw*d), the
-// traversal stepping by the stride inside the padded bounding box.
+// For a convolution, A is the matrix of im2col rows (one per output pixel,
+// k*k packed input pixels long) and B the weights packed as [O, k, k, C], so
+// the producer is the same as for a linear layer.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -68,20 +69,21 @@ struct TcArgs {
     float alpha;
     void *out;
     unsigned int *err;
-    int vec_store;             // 1: output rows 16-byte aligned (16-byte stores)
-    // conv
-    int Ho, Wo, s, p, d, k, cpt, rbc;
+    int vec_store;             // linear: 1 when output rows are 16-byte aligned (16-byte stores)
+                               // conv: bytes each lane stores at once (a run of pixels of one channel)
+    int64_t hw;                // conv: output pixels per image (Ho * Wo)
+    int stages;                // smem ring depth
 };
 
-template <int ROWB, bool CONV> __host__ __device__ constexpr int stage_bytes() { return (kBM + kMaxBN) * ROWB; }
-template <int ROWB, bool CONV> __host__ __device__ constexpr int num_stages() {
-    return (kSmemMax - kReserve - (CONV ? 0 : kStagingBytes)) / stage_bytes<ROWB, CONV>() > 8
-               ? 8
-               : (kSmemMax - kReserve - (CONV ? 0 : kStagingBytes)) / stage_bytes<ROWB, CONV>();
+// Shared memory: S stages of A (128 rows) and B (BN rows) K slices of ROWB
+// bytes, the epilogue staging boxes, barriers. S is as many stages as fit (at
+// most 8): narrow tiles get a deeper ring.
+constexpr int kMaxStages = 8;
+int num_stages(int rowb, int bn) {
+    const int s = (kSmemMax - kReserve - kStagingBytes) / ((kBM + bn) * rowb);
+    return s > kMaxStages ? kMaxStages : s;
 }
-template <int ROWB, bool CONV> __host__ __device__ constexpr int smem_bytes() {
-    return num_stages<ROWB, CONV>() * stage_bytes<ROWB, CONV>() + (CONV ? 0 : kStagingBytes) + kReserve;
-}
+int smem_bytes(int rowb, int bn) { return num_stages(rowb, bn) * (kBM + bn) * rowb + kStagingBytes + kReserve; }
 
 // TMEM column of the second accumulator buffer; also the largest BN.
 template <int CODE> __host__ __device__ constexpr uint32_t acc_stride() { return CODE == BT_CODE_E2M1 ? 240u : 256u; }
@@ -128,6 +130,14 @@ __device__ __forceinline__ typename OutT<OUT>::type from_acc(float acc, float al
     else return __float2int_rn(acc);
 }
 
+// The bits of one output value (conv epilogue staging), in the low bits.
+template <int OUT>
+__device__ __forceinline__ uint32_t out_bits(float acc, float alpha) {
+    if constexpr (OUT == BT_F32 || OUT == BT_I32) return FromAcc<OUT>::bits(acc, alpha);
+    else if constexpr (OUT == BT_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(acc, alpha)));
+    else return __half_as_ushort(__float2half_rn(__fmul_rn(acc, alpha)));
+}
+
 // Position of 16-byte chunk q of staging-box row `row`: the 128-byte swizzle
 // (q ^ row % 8) for 4-byte outputs (128-byte rows), the 64-byte swizzle
 // (q ^ (row / 2) % 4) for 2-byte outputs (64-byte rows) -- the layouts TMA
@@ -141,8 +151,10 @@ template <int CODE, int ROWB, bool CONV, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const TcArgs a) {
-    constexpr int S = num_stages<ROWB, CONV>();
-    constexpr uint32_t kABytes = kBM * ROWB, kBBytes = kMaxBN * ROWB;
+    const int S = a.stages;
+    const int bn = a.bn;
+    constexpr uint32_t kABytes = kBM * ROWB;
+    const uint32_t kBBytes = static_cast<uint32_t>(bn * ROWB);
     constexpr int kMmaPerStage = ROWB / 32;        // K = 32 bytes per MMA
     using T = typename OutT<OUT>::type;
     constexpr int kElem = sizeof(T);
@@ -152,8 +164,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base, sB = base + S * kABytes;
-    const uint32_t sStage = sB + S * kBBytes;                        // epilogue staging (linear)
-    const uint32_t bars = sStage + (CONV ? 0 : kStagingBytes);      // full[S], empty[S], tfull[2], tempty[2], drain
+    const uint32_t sStage = sB + S * kBBytes;                        // epilogue staging boxes
+    const uint32_t bars = sStage + kStagingBytes;                    // full[S], empty[S], tfull[2], tempty[2], drain
     uint8_t *gbars = smem_raw + (bars - raw);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbars + 8 * (2 * S + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -219,63 +231,43 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         tc::fence_after_sync();
     }
 
-    const int bn = a.bn;
     const uint32_t tx_bytes = static_cast<uint32_t>((kBM + bn) * ROWB);
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
             pdl_wait();                                   // operands come from the previous kernel
-            uint32_t it = 0;
-            int last_issue[8];
+            int s = 0;                                    // ring slot and its phase
+            uint32_t ph = 0;
+            uint32_t last_phase[kMaxStages];              // phase of each slot's last copy; 2 = none
 #pragma unroll
-            for (int s = 0; s < 8; ++s) last_issue[s] = -1;
+            for (int i = 0; i < kMaxStages; ++i) last_phase[i] = 2u;
             bool ok = true;
             for (int st = cluster; st < a.num_super && ok; st += nclusters) {
                 const int mt = (st / a.num_sn) * a.cm + rm, nt = (st % a.num_sn) * a.cn + rn;
                 // this CTA's share of the A tile starts a_rows * rn rows in
                 const int64_t am0 = static_cast<int64_t>(mt) * kBM + static_cast<int64_t>(a_rows) * rn;
                 const int bn0 = nt * bn + b_rows * rm;                       // and of the B tile
-                int cb = 0, ch = 0, cw = 0;
-                if (CONV) {
-                    const int64_t hw = static_cast<int64_t>(a.Ho) * a.Wo;
-                    cb = static_cast<int>(am0 / hw);
-                    const int r = static_cast<int>(am0 - static_cast<int64_t>(cb) * hw);
-                    ch = (r / a.Wo) * a.s - a.p;
-                    cw = (r % a.Wo) * a.s - a.p;
-                }
                 const uint32_t a_off = static_cast<uint32_t>(a_rows * rn * ROWB);
                 const uint32_t b_off = static_cast<uint32_t>(b_rows * rm * ROWB);
-                for (int kb = 0; kb < a.nk; ++kb, ++it) {
-                    const int s = static_cast<int>(it % S);
-                    const uint32_t ph = (it / S) & 1u;
+                for (int kb = 0; kb < a.nk; ++kb) {
                     if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
                     tc::mbar_arrive_expect_tx(full(s), tx_bytes);
                     const uint32_t adst = sA + s * kABytes + a_off, bdst = sB + s * kBBytes + b_off;
-                    int bcol = kb * ROWB;
-                    if (CONV) {
-                        const int tap = kb / a.cpt, chunk = kb - tap * a.cpt;
-                        const int kh = tap / a.k, kw = tap - kh * a.k;
-                        const uint16_t ow = static_cast<uint16_t>(kw * a.d), oh = static_cast<uint16_t>(kh * a.d);
-                        if (a.cn > 1) tc::tma_load_im2col_4d_mc(adst, &tmA, chunk * ROWB, cw, ch, cb, ow, oh, full(s), maskA);
-                        else tc::tma_load_im2col_4d(adst, &tmA, chunk * ROWB, cw, ch, cb, ow, oh, full(s));
-                        bcol = tap * a.rbc + chunk * ROWB;
-                    } else {
-                        if (a.cn > 1) tc::tma_load_2d_mc(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s), maskA);
-                        else tc::tma_load_2d(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s));
-                    }
-                    if (a.cm > 1) tc::tma_load_2d_mc(bdst, &tmB, bcol, bn0, full(s), maskB);
-                    else tc::tma_load_2d(bdst, &tmB, bcol, bn0, full(s));
-                    last_issue[s] = static_cast<int>(it);
+                    if (a.cn > 1) tc::tma_load_2d_mc(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s), maskA);
+                    else tc::tma_load_2d(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s));
+                    if (a.cm > 1) tc::tma_load_2d_mc(bdst, &tmB, kb * ROWB, bn0, full(s), maskB);
+                    else tc::tma_load_2d(bdst, &tmB, kb * ROWB, bn0, full(s));
+                    last_phase[s] = ph;
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
                 // let every issued copy land before the CTA can exit
-                for (int s = 0; s < S; ++s) {
-                    if (last_issue[s] >= 0) {
-                        const uint32_t ph = (static_cast<uint32_t>(last_issue[s]) / S) & 1u;
+                for (int i = 0; i < S; ++i) {
+                    if (last_phase[i] < 2u) {
                         const unsigned long long t0 = globaltimer_ns();
-                        while (!tc::mbar_try_wait(full(s), ph) && globaltimer_ns() - t0 < kWaitNs) {}
+                        while (!tc::mbar_try_wait(full(i), last_phase[i]) && globaltimer_ns() - t0 < kWaitNs) {}
                     }
                 }
             }
@@ -284,7 +276,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            uint32_t it = 0;
+            int s = 0;
+            uint32_t ph = 0;
             int local = 0;
             bool ok = true;
             for (int st = cluster; st < a.num_super && ok; st += nclusters, ++local) {
@@ -296,9 +289,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     tc::fence_after_sync();
                 }
                 const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * acc_stride<CODE>();
-                for (int kb = 0; kb < a.nk; ++kb, ++it) {
-                    const int s = static_cast<int>(it % S);
-                    const uint32_t ph = (it / S) & 1u;
+                for (int kb = 0; kb < a.nk; ++kb) {
                     if (!tc::wait_bounded(full(s), ph, abort_flag, a.err)) { ok = false; break; }
                     tc::fence_after_sync();
 #pragma unroll
@@ -311,6 +302,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     }
                     if (clustered) tc::mma_commit_mc(empty(s), mask_release);
                     else tc::mma_commit(empty(s));
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
                 if (ok) tc::mma_commit(tfull(buf));
             }
@@ -341,25 +333,84 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 if (lane == 0) tc::mbar_arrive(tempty(buf));
                 released = true;
             };
-            if constexpr (!CONV) {
-                // Boxes of 32 rows x 32 columns (64 or 128 bytes, matching swizzle)
-                // through the warp's staging box. The TMEM read of the next box is
-                // in flight while the current one is converted.
-                const int64_t ncols = a.N - n0 < bn ? a.N - n0 : bn;
-                const int64_t ncol_end = n0 + ncols;                         // this tile's columns end here
-                const int nbox = ncols > 0 ? static_cast<int>((ncols + 31) / 32) : 0;
-                const int64_t mrow0 = m0 + quarter * 32;                     // this warp's first row
-                const int total = mrow0 < a.M ? nbox : 0;
-                const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
-                auto tcol_of = [&](int b) { return tbase + static_cast<uint32_t>(32 * b); };
-                auto emit = [&](const uint32_t (&r)[32], int b) {
-                    const int c0 = 32 * b;
-                    const uint32_t buf = my_stage;
+            // Boxes of 32 rows x 32 columns; the TMEM read of the next box is in
+            // flight while the current one is converted and stored.
+            const int64_t ncols = a.N - n0 < bn ? a.N - n0 : bn;
+            const int64_t ncol_end = n0 + ncols;                             // this tile's columns end here
+            const int nbox = ncols > 0 ? static_cast<int>((ncols + 31) / 32) : 0;
+            const int64_t mrow0 = m0 + quarter * 32;                         // this warp's first row
+            const int total = mrow0 < a.M ? nbox : 0;
+            const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
+            auto tcol_of = [&](int b) { return tbase + static_cast<uint32_t>(32 * b); };
+            // conv: the output run this lane stores. With vw > kElem, a run of
+            // vw / kElem pixels of one channel (vw bytes), starting at row
+            // m = mrow0 + q * (vw / kElem) of the warp's 32; runs never straddle two
+            // images (hw is a multiple of the run). Otherwise one pixel, m = mrow0 + lane.
+            const int vw = CONV ? a.vec_store : 0;
+            const bool runs = CONV && vw > kElem;
+            const int lpr = runs ? kBoxInner / vw : 32;                      // lanes per staged channel row
+            const int q = lane % lpr;
+            const int64_t m = mrow0 + (runs ? q * (vw / kElem) : lane);
+            const bool row_ok = m < a.M;
+            T *pix_out = out;
+            if constexpr (CONV) {
+                const int64_t ob = row_ok ? m / a.hw : 0;
+                pix_out = out + (ob * a.N + n0) * a.hw + (m - ob * a.hw);
+            }
+            auto emit = [&](const uint32_t (&r)[32], int b) {
+                const int c0 = 32 * b;
+                if constexpr (CONV) {
+                    if (!runs) {
+                        // NCHW: one store per channel, 32 consecutive pixels across the warp
+                        if (!row_ok) return;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j < ncols)
+                                pix_out[static_cast<int64_t>(c0 + j) * a.hw] = from_acc<OUT>(__uint_as_float(r[j]), a.alpha);
+                        return;
+                    }
+                    // NCHW through the staging box, transposed to [channel][pixel]
+                    // rows; then each lane stores its run of one channel, 32 / lpr
+                    // channels per instruction
+                    const uint32_t sbox = my_stage;
+                    __syncwarp();                                             // previous box fully read back
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const uint32_t addr = sbox + static_cast<uint32_t>(j * kBoxInner + lane * kElem);
+                        const uint32_t v = out_bits<OUT>(__uint_as_float(r[j]), a.alpha);
+                        if (kElem == 4) asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+                        else asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
+                    }
+                    __syncwarp();
+                    if (!row_ok) return;
+                    const int rows_per = 32 / lpr;
+                    for (int rr = lane / lpr; rr < 32; rr += rows_per) {
+                        if (c0 + rr >= ncols) break;
+                        const uint32_t addr = sbox + static_cast<uint32_t>(rr * kBoxInner + q * vw);
+                        uint8_t *dst = reinterpret_cast<uint8_t *>(pix_out + static_cast<int64_t>(c0 + rr) * a.hw);
+                        if (vw == 16) {
+                            uint4 v;
+                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+                            *reinterpret_cast<uint4 *>(dst) = v;
+                        } else if (vw == 8) {
+                            uint2 v;
+                            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+                            *reinterpret_cast<uint2 *>(dst) = v;
+                        } else {
+                            uint32_t v;
+                            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+                            *reinterpret_cast<uint32_t *>(dst) = v;
+                        }
+                    }
+                } else {
+                    // row-major [M, N] through the warp's swizzled staging box
+                    const uint32_t sbox = my_stage;
                     __syncwarp();                                             // previous box fully read back
                     constexpr int kChunks = kBoxInner / 16;
 #pragma unroll
                     for (int q = 0; q < kChunks; ++q) {
-                        const uint32_t addr = buf + static_cast<uint32_t>(lane * kBoxInner) + (box_chunk<kElem>(q, lane) << 4);
+                        const uint32_t addr = sbox + static_cast<uint32_t>(lane * kBoxInner) + (box_chunk<kElem>(q, lane) << 4);
                         const uint4 w = chunk16<OUT, kElem>(r, q * (16 / kElem), a.alpha);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w.x), "r"(w.y),
                                      "r"(w.z), "r"(w.w)
@@ -375,7 +426,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
                         for (int rr0 = 0; rr0 < 32; rr0 += kRowsPer) {
                             const int rr = rr0 + lane / kChunks;
-                            const uint32_t addr = buf + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(q, rr) << 4);
+                            const uint32_t addr = sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(q, rr) << 4);
                             uint4 v;
                             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                                          : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -393,7 +444,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll 4
                         for (int rr = 0; rr < 32; ++rr) {
                             const uint32_t addr =
-                                buf + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(lane / kPer, rr) << 4) + off;
+                                sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(lane / kPer, rr) << 4) + off;
                             uint32_t v;
                             if (kElem == 4) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
                             else asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -404,45 +455,21 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                             }
                         }
                     }
-                };
-                uint32_t r0[32], r1[32];
-                if (total > 0) tc::tmem_ld32(tcol_of(0), r0);
-#pragma unroll 1
-                for (int b = 0; b < total; b += 2) {
-                    tc::tmem_ld_wait();
-                    if (b + 1 < total) tc::tmem_ld32(tcol_of(b + 1), r1);
-                    else release();
-                    emit(r0, b);
-                    if (b + 1 < total) {
-                        tc::tmem_ld_wait();
-                        if (b + 2 < total) tc::tmem_ld32(tcol_of(b + 2), r0);
-                        else release();
-                        emit(r1, b + 1);
-                    }
                 }
-            } else {
-                {
-                    const int64_t mrow0 = m0 + quarter * 32;                     // this warp's first row
-                    const int64_t m = mrow0 + lane;
-                    const bool row_ok = m < a.M;
-                    const uint32_t tcol = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
-                    const int64_t hw = static_cast<int64_t>(a.Ho) * a.Wo;
-                    const int64_t ob = row_ok ? m / hw : 0;
-                    const int64_t pix = m - ob * hw;
+            };
+            uint32_t r0[32], r1[32];
+            if (total > 0) tc::tmem_ld32(tcol_of(0), r0);
 #pragma unroll 1
-                    for (int c = 0; c < bn; c += 32) {
-                        if (n0 + c >= a.N) break;                            // warp-uniform
-                        uint32_t r[32];
-                        tc::tmem_ld32(tcol + static_cast<uint32_t>(c), r);
-                        tc::tmem_ld_wait();
-                        if (!row_ok) continue;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int64_t o = n0 + c + j;
-                            if (o < a.N && c + j < bn)
-                                out[(ob * a.N + o) * hw + pix] = from_acc<OUT>(__uint_as_float(r[j]), a.alpha);
-                        }
-                    }
+            for (int b = 0; b < total; b += 2) {
+                tc::tmem_ld_wait();
+                if (b + 1 < total) tc::tmem_ld32(tcol_of(b + 1), r1);
+                else release();
+                emit(r0, b);
+                if (b + 1 < total) {
+                    tc::tmem_ld_wait();
+                    if (b + 2 < total) tc::tmem_ld32(tcol_of(b + 2), r0);
+                    else release();
+                    emit(r1, b + 1);
                 }
             }
             if (!released) release();
@@ -472,19 +499,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess && q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col() {
-    static PFN_cuTensorMapEncodeIm2col_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(p);
     });
     return fn;
 }
@@ -525,21 +539,24 @@ bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t pitch,
 // stage to land in this SM's shared memory (about 95 bytes per clock per SM
 // for TMA into the ring; multicast inside a cluster lowers L2 reads but not
 // the bytes each SM receives, so clusters only change the wave count), and
-// the measured pipelined stage time of about 640 clocks per 128-byte stage;
-// with the accumulator double-buffered only the last tile's epilogue (about 8
-// clocks per output column) is exposed.
+// the pipelined stage time measured in whole launches on GB300 (about 1230
+// clocks per 128-byte stage and 790 per 64-byte stage, so 64-byte stages only
+// pay off when they save a half-empty last stage of many); with the
+// accumulator double-buffered only the last tile's epilogue (about 8 clocks
+// per output column) is exposed.
 // BT_TC_CONFIG="cm,cn,bn" overrides the choice.
 struct TileCfg {
     int cm, cn, bn;
+    double cost;     // modelled clocks of the whole launch
 };
 
 TileCfg choose_cfg(int64_t M, int64_t N, int nk, int rowb, int sms, int max_bn) {
-    TileCfg best{1, 1, max_bn};
+    TileCfg best{1, 1, max_bn, 0.0};
     if (const char *env = std::getenv("BT_TC_CONFIG")) {
         int cm = 0, cn = 0, bn = 0;
         if (std::sscanf(env, "%d,%d,%d", &cm, &cn, &bn) == 3 && (cm == 1 || cm == 2) && (cn == 1 || cn == 2) &&
             bn >= 32 && bn <= max_bn && bn % 16 == 0 && (bn / cm) % 16 == 0)
-            return TileCfg{cm, cn, bn};
+            return TileCfg{cm, cn, bn, 0.0};
     }
     const int64_t num_m = (M + kBM - 1) / kBM;
     double best_cost = -1.0;
@@ -553,13 +570,13 @@ TileCfg choose_cfg(int64_t M, int64_t N, int nk, int rowb, int sms, int max_bn) 
                 const int64_t rounds = (super + clusters - 1) / clusters;
                 const double mma = (rowb / 32) * 116.0;
                 const double land = static_cast<double>(kBM + bn) * rowb / 95.0;
-                const double piped = 640.0 * rowb / 128.0;
+                const double piped = 350.0 + 880.0 * rowb / 128.0;
                 double stage = mma > land ? mma : land;
                 if (piped > stage) stage = piped;
                 const double cost = static_cast<double>(rounds) * nk * stage + 8.0 * bn + 600.0;
                 if (best_cost < 0.0 || cost < best_cost * 0.999) {
                     best_cost = cost;
-                    best = TileCfg{cm, cn, bn};
+                    best = TileCfg{cm, cn, bn, cost};
                 }
             }
         }
@@ -568,20 +585,20 @@ TileCfg choose_cfg(int64_t M, int64_t N, int nk, int rowb, int sms, int max_bn) 
 }
 
 template <int CODE, int ROWB, bool CONV, int OUT>
-cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
-                     cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, TcArgs a, cudaStream_t s) {
     auto kern = tc_kernel<CODE, ROWB, CONV, OUT>;
-    constexpr int smem = smem_bytes<ROWB, CONV>();
-    static_assert(smem <= kSmemMax, "shared memory budget");
+    a.stages = num_stages(ROWB, a.bn);
+    const int smem = smem_bytes(ROWB, a.bn);
+    if (a.stages < 2 || smem > kSmemMax) return cudaErrorInvalidValue;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] { attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
+    std::call_once(once, [&] { attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax); });
     if (attr_err != cudaSuccess) return attr_err;
     const int csize = a.cm * a.cn;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
@@ -646,7 +663,7 @@ bool set_grid(TcArgs &a, const TileCfg &c, int64_t M, int64_t N) {
 
 }  // namespace
 
-bool tc_available() { return encode_tiled() != nullptr && encode_im2col() != nullptr; }
+bool tc_available() { return encode_tiled() != nullptr; }
 
 cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M, int64_t N, int64_t K,
                              float alpha, void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
@@ -665,38 +682,38 @@ cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code,
     return launch_code<false>(code, 128, ma, mb, a, out_t, s);
 }
 
-cudaError_t launch_tc_conv(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
+cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
                            void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
-    const int64_t rbc = row_bytes(g.C, code);
-    const int rowb = (rbc % 128 == 0) ? 128 : 64;
-    auto fn = encode_im2col();
-    if (fn == nullptr || rbc % 64 != 0) return cudaErrorInvalidValue;
+    // A: the im2col rows [M, k*k*rbc]; B: the weights [O, k*k*rbc]. Rows are a
+    // multiple of 64 bytes: 128-byte stages (the last one half zero fill when
+    // the row is an odd number of 64-byte blocks) or 64-byte stages, whichever
+    // the cost model prefers.
+    const int64_t krow = static_cast<int64_t>(g.k) * g.k * row_bytes(g.C, code);
+    if (krow % 64 != 0) return cudaErrorInvalidValue;
     TcArgs a{};
     a.M = g.B * g.Ho * g.Wo; a.N = g.O; a.alpha = alpha; a.out = out; a.err = err;
-    a.Ho = static_cast<int>(g.Ho); a.Wo = static_cast<int>(g.Wo);
-    a.s = g.s; a.p = g.p; a.d = g.d; a.k = g.k;
-    a.cpt = static_cast<int>(rbc / rowb); a.rbc = static_cast<int>(rbc);
-    a.nk = g.k * g.k * a.cpt;
-    const TileCfg c = choose_cfg(a.M, a.N, a.nk, rowb, sm_count(), code == BT_CODE_E2M1 ? 240 : 256);
+    a.hw = g.Ho * g.Wo;
+    // widest store of a run of one channel's pixels that keeps every run inside
+    // one image and naturally aligned
+    const int eb = out_elem_bytes(out_t);
+    a.vec_store = eb;
+    for (int v = 16; v > eb; v /= 2) {
+        if ((a.hw * eb) % v == 0 && aligned(out, static_cast<size_t>(v))) { a.vec_store = v; break; }
+    }
+    const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;
+    const int nk128 = static_cast<int>((krow + 127) / 128), nk64 = static_cast<int>(krow / 64);
+    TileCfg c = choose_cfg(a.M, a.N, nk128, 128, sm_count(), max_bn);
+    int rowb = 128;
+    a.nk = nk128;
+    if (krow % 128 != 0) {
+        const TileCfg c64 = choose_cfg(a.M, a.N, nk64, 64, sm_count(), max_bn);
+        if (c64.cost < c.cost) { c = c64; rowb = 64; a.nk = nk64; }
+    }
     if (!set_grid(a, c, a.M, a.N)) return cudaErrorInvalidValue;
     a.idesc = make_idesc(code, a.bn);
-    a.vec_store = 0;
     CUtensorMap ma, mb;
-    cuuint64_t dims[4] = {static_cast<cuuint64_t>(rbc), static_cast<cuuint64_t>(g.W), static_cast<cuuint64_t>(g.H),
-                          static_cast<cuuint64_t>(g.B)};
-    cuuint64_t strides[3] = {static_cast<cuuint64_t>(rbc), static_cast<cuuint64_t>(rbc * g.W),
-                             static_cast<cuuint64_t>(rbc * g.W * g.H)};
-    const int lo = -g.p, hi = g.p - (g.k - 1) * g.d;
-    int lower[2] = {lo, lo}, upper[2] = {hi, hi};
-    cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(g.s), static_cast<cuuint32_t>(g.s), 1};
-    const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (fn(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(xp), dims, strides, lower, upper,
-           static_cast<cuuint32_t>(rowb), static_cast<cuuint32_t>(kBM / a.cn), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    const int64_t krow = static_cast<int64_t>(g.k) * g.k * rbc;
-    if (!map_2d(&mb, wp, krow, krow, g.O, static_cast<uint32_t>(rowb), static_cast<uint32_t>(a.bn / a.cm)))
+    if (!map_2d(&ma, rows, krow, krow, a.M, static_cast<uint32_t>(rowb), static_cast<uint32_t>(kBM / a.cn)) ||
+        !map_2d(&mb, wp, krow, krow, g.O, static_cast<uint32_t>(rowb), static_cast<uint32_t>(a.bn / a.cm)))
         return cudaErrorInvalidValue;
     return launch_code<true>(code, rowb, ma, mb, a, out_t, s);
 }

@@ -86,16 +86,6 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
         : "memory");
 }
-__device__ __forceinline__ void tma_load_im2col_4d_mc(uint32_t dst, const CUtensorMap *m, int c, int w, int h, int n,
-                                                      uint16_t off_w, uint16_t off_h, uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8}, %9;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar),
-          "h"(off_w), "h"(off_h), "h"(mask)
-        : "memory");
-}
-
 // Cluster-wide barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -125,18 +115,6 @@ __device__ __forceinline__ void bulk_load_once(uint32_t dst, const void *src, ui
         "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n"
         "}\n" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// im2col mode over an NHWC tensor: coordinates {c, w, h, n} of the window's
-// base pixel, offsets {kw*d, kh*d} of the filter tap.
-__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap *m, int c, int w, int h, int n,
-                                                   uint16_t off_w, uint16_t off_h, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar),
-          "h"(off_w), "h"(off_h)
         : "memory");
 }
 
