@@ -334,12 +334,15 @@ def test_full_conv_workloads(code, name):
 
 
 # ---------------------------------------------------------------------------
-# Every tile / cluster configuration of the tensor-core kernel (the planner
-# picks one per shape; BT_TC_CONFIG="cm,cn,bn" forces it): cm CTAs share each
-# B slice, cn CTAs share each A slice (TMA multicast inside a cluster).
+# Every tile configuration of the tensor-core kernel (the planner picks one
+# per shape; BT_TC_CONFIG="bn,d" or "pair,bn,d" forces it): BN columns per
+# tile, d 128-byte K slices per pipeline stage; "pair" runs 256-row tiles on
+# CTA pairs (cta_group::2). The shapes cover a whole number of slices, a half
+# last slice, and rows shorter than one slice.
 # ---------------------------------------------------------------------------
 
-TC_CONFIGS = ["1,1,64", "2,1,64", "1,2,64", "2,2,64", "2,2,160", "2,1,224", "1,2,96", "1,1,240", "1,1,208", "1,2,48"]
+TC_CONFIGS = ["240,1", "224,2", "128,4", "64,2", "32,1", "208,2", "96,4",
+              "pair,240,2", "pair,224,1", "pair,160,4", "pair,128,2", "pair,64,4", "pair,32,1", "pair,208,2"]
 TC_CODES = [bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
 
 
@@ -347,7 +350,7 @@ TC_CODES = [bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
 @pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
 def test_linear_tc_configs(cfg, code, monkeypatch):
     monkeypatch.setenv("BT_TC_CONFIG", cfg)
-    for (M, N, K) in ((700, 600, 1000), (1100, 330, 4100)):
+    for (M, N, K) in ((700, 600, 1000), (1100, 330, 4100), (300, 200, 100), (260, 520, 700)):
         x = _gen(M + K, (M, K), torch.bfloat16)
         w = _gen(N + K, (N, K), torch.bfloat16)
         sa, sw = workloads.mean_abs(x), workloads.mean_abs(w)

@@ -34,18 +34,39 @@ template <int CODE> __host__ __device__ __forceinline__ int64_t padded_elems(int
     return CODE == BT_CODE_BITS ? rb * 8 : (CODE == BT_CODE_E4M3 ? rb : rb * 2);
 }
 
-// Loads of one group of 8 elements: one 16-byte vector for 2-byte types,
-// two for fp32.
+// One group of 8 elements as 2 * sizeof(T) 32-bit words (value e of a 2-byte
+// type in half e % 2 of word e / 2), loaded with VB-byte vectors (16 or 8;
+// the group's address must be VB-aligned).
 template <typename T> struct Group {
-    static constexpr int kVecs = 8 / Elem<T>::kPerVec;
-    uint4 q[kVecs];
+    static constexpr int kWords = 2 * static_cast<int>(sizeof(T));
+    uint32_t w[kWords];
+    template <int VB = 16>
     __device__ __forceinline__ void load(const T *p) {
+        if constexpr (VB == 16) {
 #pragma unroll
-        for (int v = 0; v < kVecs; ++v) q[v] = ld_stream_v4(p + v * Elem<T>::kPerVec);
+            for (int i = 0; i < kWords / 4; ++i) {
+                const uint4 q = ld_stream_v4(p + i * (16 / sizeof(T)));
+                w[4 * i] = q.x; w[4 * i + 1] = q.y; w[4 * i + 2] = q.z; w[4 * i + 3] = q.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kWords / 2; ++i) {
+                const uint2 q = __ldcs(reinterpret_cast<const uint2 *>(p + i * (8 / sizeof(T))));
+                w[2 * i] = q.x; w[2 * i + 1] = q.y;
+            }
+        }
+    }
+    __device__ __forceinline__ void load_smem(const T *p) {     // 16-byte aligned shared memory
+#pragma unroll
+        for (int i = 0; i < kWords / 4; ++i) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(p + i * (16 / sizeof(T)));
+            w[4 * i] = q.x; w[4 * i + 1] = q.y; w[4 * i + 2] = q.z; w[4 * i + 3] = q.w;
+        }
     }
     __device__ __forceinline__ void unpack(float (&f)[8]) const {
 #pragma unroll
-        for (int v = 0; v < kVecs; ++v) Elem<T>::unpack(q[v], f + v * Elem<T>::kPerVec);
+        for (int i = 0; i < kWords / 4; ++i)
+            Elem<T>::unpack(make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]), f + i * Elem<T>::kPerVec);
     }
 };
 
@@ -122,15 +143,14 @@ template <typename T>
 __device__ __forceinline__ void masks_ge(const Group<T> &g, float neg_b, uint32_t &P0, uint32_t &P1) {
     if constexpr (sizeof(T) == 2) {
         const typename Thresh<T>::type t = Thresh<T>::of(neg_b);
-        const uint32_t m0 = Thresh<T>::ge(g.q[0].x, t), m1 = Thresh<T>::ge(g.q[0].y, t);
-        const uint32_t m2 = Thresh<T>::ge(g.q[0].z, t), m3 = Thresh<T>::ge(g.q[0].w, t);
+        const uint32_t m0 = Thresh<T>::ge(g.w[0], t), m1 = Thresh<T>::ge(g.w[1], t);
+        const uint32_t m2 = Thresh<T>::ge(g.w[2], t), m3 = Thresh<T>::ge(g.w[3], t);
         P0 = __byte_perm(m0, m1, 0x6420);
         P1 = __byte_perm(m2, m3, 0x6420);
     } else {
         uint32_t s[8];
-        const uint32_t w[8] = {g.q[0].x, g.q[0].y, g.q[0].z, g.q[0].w, g.q[1].x, g.q[1].y, g.q[1].z, g.q[1].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s[e] = __uint_as_float(w[e]) >= neg_b ? 0xFFFFFFFFu : 0u;
+        for (int e = 0; e < 8; ++e) s[e] = __uint_as_float(g.w[e]) >= neg_b ? 0xFFFFFFFFu : 0u;
         P0 = __byte_perm(__byte_perm(s[0], s[1], 0x0040), __byte_perm(s[2], s[3], 0x0040), 0x5410);
         P1 = __byte_perm(__byte_perm(s[4], s[5], 0x0040), __byte_perm(s[6], s[7], 0x0040), 0x5410);
     }
@@ -184,39 +204,52 @@ FastDiv make_fastdiv(uint32_t d) {
 __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) { return (__umulhi(f.m, n) + n) >> f.l; }
 
 // rows, flat: every output group of every row, numbered g = row * G + j over
-// the whole [R, G] output, kFlatUnroll per thread in flight; group j < Gd
-// holds elements 8j..8j+7 of the row (K a multiple of 8, rows 16-byte
-// aligned), the rest of the row is zero padding. Consecutive threads take
-// consecutive groups: contiguous loads and contiguous stores.
+// the whole [R, G] output, kFlatUnroll per thread in flight. Group j < Gf
+// holds elements 8j..8j+7 of the row and is read with VB-byte vectors (rows
+// VB-aligned); a last, partial group (K not a multiple of 8) is read element
+// by element; groups from Gd = ceil(K / 8) on are the row's zero padding.
+// Consecutive threads take consecutive groups: contiguous loads and stores.
 constexpr int kFlatUnroll = 4;
 
-template <typename T, int CODE, bool COLBIAS>
+template <typename T, int CODE, bool COLBIAS, int VB>
 __global__ void __launch_bounds__(kPackThreads)
-pack_rows_flat_kernel(const T *__restrict__ x, uint32_t total, FastDiv divG, uint32_t Gd, int K,
+pack_rows_flat_kernel(const T *__restrict__ x, uint32_t total, FastDiv divG, uint32_t Gf, int K,
                       const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out) {
     constexpr int OB = GroupOut<CODE>::kBytes;
     pdl_launch_dependents();
     pdl_wait();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
     const bool finite = isfinite(bs);
+    const uint32_t Gd = static_cast<uint32_t>((K + 7) / 8);
     const uint32_t stride = gridDim.x * (kPackThreads * kFlatUnroll);
     for (uint32_t g0 = blockIdx.x * (kPackThreads * kFlatUnroll) + threadIdx.x; g0 < total; g0 += stride) {
         Group<T> grp[kFlatUnroll];
-        uint32_t col[kFlatUnroll];
+        uint32_t col[kFlatUnroll], row[kFlatUnroll];
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
             const uint32_t g = g0 + u * kPackThreads;
-            const uint32_t row = fdiv(g, divG);
-            col[u] = g - row * divG.d;
-            if (g < total && col[u] < Gd) grp[u].load(x + static_cast<int64_t>(row) * K + 8 * col[u]);
+            row[u] = fdiv(g, divG);
+            col[u] = g - row[u] * divG.d;
+            if (g < total && col[u] < Gf) grp[u].template load<VB>(x + static_cast<int64_t>(row[u]) * K + 8 * col[u]);
         }
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
             const uint32_t g = g0 + u * kPackThreads;
             if (g >= total) break;
             uint8_t *dst = out + static_cast<int64_t>(g) * OB;
-            if (col[u] >= Gd) {
-                store_group<CODE>(dst, 0u, 0u);                 // row padding
+            if (col[u] >= Gf) {
+                uint32_t neg = 0, valid = 0;
+                if (col[u] < Gd) {
+                    // the row's last, partial group
+                    const int k0 = 8 * static_cast<int>(col[u]);
+                    const T *xr = x + static_cast<int64_t>(row[u]) * K;
+                    for (int e = 0; e < K - k0; ++e) {
+                        const float b = COLBIAS ? __ldg(bias + k0 + e) : bs;
+                        neg |= is_negative(Elem<T>::to_f32(xr[k0 + e]), b) << e;
+                        valid |= 1u << e;
+                    }
+                }
+                store_group<CODE>(dst, neg, valid);             // (or row padding: code 0)
                 continue;
             }
             uint32_t P0, P1;
@@ -369,9 +402,7 @@ pack_rows_staged_kernel(const T *__restrict__ x, int64_t R, int K, const float *
             uint32_t valid = 0xFFu;
             if (kl + 8 <= len) {
                 Group<T> grp;
-#pragma unroll
-                for (int v = 0; v < Group<T>::kVecs; ++v)
-                    grp.q[v] = *reinterpret_cast<const uint4 *>(sx + kl + v * Elem<T>::kPerVec);
+                grp.load_smem(sx + kl);
                 grp.unpack(f);
             } else {
                 valid = 0;
@@ -646,9 +677,10 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
     const int64_t per_block = kRowThreads * kGroupsPerThread;
     dim3 grid(static_cast<unsigned>((G + per_block - 1) / per_block), static_cast<unsigned>(R < 65535 ? R : 65535));
     const bool vec = ((K * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned(x, 16);
+    const bool vec8 = ((K * static_cast<int64_t>(sizeof(T))) % 8 == 0) && aligned(x, 8);
     const int64_t total = R * G;
     const bool colbias = bias_len > 1;
-    if (vec && K % 8 == 0 && total <= (int64_t(1) << 31) - (int64_t(1) << 21) && (!colbias || aligned(bias, 16))) {
+    if (vec8 && total <= (int64_t(1) << 31) - (int64_t(1) << 21) && (!colbias || aligned(bias, 16))) {
         int sms = 0, dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -663,12 +695,14 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
         cfg.attrs = &pdl;
         cfg.numAttrs = 1;
         const FastDiv divG = make_fastdiv(static_cast<uint32_t>(G));
-        const uint32_t Gd = static_cast<uint32_t>(K / 8);
-        if (colbias)
-            return cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true>, x, static_cast<uint32_t>(total), divG,
-                                      Gd, static_cast<int>(K), bias, static_cast<int>(bias_len), out);
-        return cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false>, x, static_cast<uint32_t>(total), divG, Gd,
-                                  static_cast<int>(K), bias, static_cast<int>(bias_len), out);
+        const uint32_t Gf = static_cast<uint32_t>(K / 8);
+        const uint32_t tot = static_cast<uint32_t>(total);
+        const int k = static_cast<int>(K), bl = static_cast<int>(bias_len);
+        if (vec)
+            return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 16>, x, tot, divG, Gf, k, bias, bl, out)
+                           : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 16>, x, tot, divG, Gf, k, bias, bl, out);
+        return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 8>, x, tot, divG, Gf, k, bias, bl, out)
+                       : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 8>, x, tot, divG, Gf, k, bias, bl, out);
     }
     unsigned int *err = device_error_word();
     if (vec && err != nullptr) {

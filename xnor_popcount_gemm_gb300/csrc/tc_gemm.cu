@@ -12,34 +12,48 @@
 // convolution's padding) contribute 0, which is the unfold + mm reading of
 // padding.
 //
-// Persistent, warp-specialised: one CTA per SM walks output tiles of
-// 128 x BN (BN a multiple of 16, chosen per problem so the tiles spread evenly
-// over the SMs). The fp32 accumulator is double-buffered in TMEM (2 x 240
-// columns plus 32 of unit block scales for E2M1, 2 x 256 for E4M3), so a
-// tile's epilogue -- and its output stores -- overlap the next tile's MMAs.
-//   warp 0 lane 0   TMA producer: a ring of smem stages, each one 128- or
-//                   64-byte-wide K slice of A (128 rows) and B (BN rows),
-//                   written with the matching swizzle; it runs ahead across
-//                   tile boundaries.
-//   warp 1 lane 0   MMA issuer: per 32 bytes of a stage, one tcgen05.mma
-//                   (M=128, N=BN) into the tile's accumulator buffer;
-//                   tcgen05.commit frees the stage, and, after a tile's last
+// D[r, c] = sum_k A[r, k] * B[c, k]: A and B are packed rows (K-major), read
+// in 128-byte K slices. A linear layer has A = activations, B = weights and a
+// row-major output [M, N]. A convolution has A = weights [O, k*k*C] and B =
+// im2col rows [B*Ho*Wo, k*k*C], so a tile's rows are output channels and its
+// columns output pixels: each TMEM lane holds a run of consecutive pixels of
+// one channel, which is what the NCHW output wants.
+//
+// Persistent and warp-specialised, one CTA per SM. Two shapes:
+//   single  a CTA computes 128 x BN tiles with cta_group::1 MMAs;
+//   pair    a cluster of 2 CTAs computes 256 x BN tiles with cta_group::2
+//           MMAs: each CTA loads its own 128 rows of A and half of the tile's
+//           B rows, the even CTA issues the MMAs, and each CTA's TMEM holds
+//           its 128 rows of the accumulator. Every SM receives 128 + BN/2
+//           rows per K slice instead of 128 + BN, for the same MMA work.
+// A smem stage holds D consecutive 128-byte K slices of A and of B, each
+// operand loaded with one TMA box over a 3-D view {128 B, rows, slices} of
+// its rows: on GB300 a TMA box costs a roughly fixed ~470 clocks of the SM's
+// copy engine whatever its size, so two slices per box halve the cost per
+// byte. A stage that reaches the row's last, partial slice is loaded slice by
+// slice from the 2-D view instead, whose zero fill covers the half slice.
+// The fp32 accumulator is double-buffered in TMEM (2 x 240 columns plus 32 of
+// unit block scales for E2M1, 2 x 256 for E4M3), so a tile's epilogue -- and
+// its output stores -- overlap the next tile's MMAs.
+//   warp 0 lane 0   TMA producer: a ring of smem stages (128-byte swizzle),
+//                   running ahead across tile boundaries.
+//   warp 1 lane 0   MMA issuer (the even CTA of a pair): per 32 bytes of K
+//                   one tcgen05.mma into the tile's accumulator buffer;
+//                   tcgen05.commit frees the stage and, after a tile's last
 //                   stage, hands the buffer to the epilogue.
 //   warps 2..5      epilogue: each drains its 32 TMEM lanes (rows), the next
-//                   32-column box in flight while the current
-//                   one is scaled and cast. A linear output goes through a
-//                   swizzled 32 x 32 smem box so that whole row segments leave in
-//                   16-byte stores; a convolution's NCHW output is stored
-//                   straight from registers (consecutive lanes, consecutive
-//                   pixels). Once drained, the buffer goes back to the MMA
-//                   warp.
-// For a convolution, A is the matrix of im2col rows (one per output pixel,
-// k*k packed input pixels long) and B the weights packed as [O, k, k, C], so
-// the producer is the same as for a linear layer.
+//                   32-column box in flight while the current one is scaled,
+//                   cast, and written to a swizzled 32 x 32 smem box, from
+//                   which whole row segments leave in 16-byte stores (or, for
+//                   NCHW, runs of pixels in the widest aligned stores). Once
+//                   drained, the buffer goes back to the MMA warp.
+// Every wait is bounded (kWaitNs): a wait that runs out records BT_ERR_TIMEOUT
+// in the device error word and the kernel winds down without trapping.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "bt_device.cuh"
@@ -49,7 +63,8 @@
 namespace bt {
 namespace {
 
-constexpr int kBM = 128, kMaxBN = 256;           // tile rows (= MMA M), widest tile
+constexpr int kBM = 128;                         // rows of A per CTA (= MMA M per CTA)
+constexpr int kRowB = 128;                       // bytes of a K slice
 constexpr int kThreads = 192;                    // producer, MMA, 4 epilogue warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 480;                 // 32 columns of unit block scales (E2M1)
@@ -58,52 +73,49 @@ constexpr int kSmemMax = 232448;                 // 227 KB opt-in per CTA
 constexpr int kBoxBytes = 32 * 128;              // one epilogue staging box: 32 rows x 128 B
 constexpr int kStagingBytes = 4 * kBoxBytes;     // one box per epilogue warp
 constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
+constexpr int kMaxStages = 8;
+
+enum Layout { kRowsOut = 0, kNchwOut = 1 };
 
 struct TcArgs {
-    int64_t M, N;
-    int nk;                    // K steps per tile (smem stages to consume)
-    int num_n, num_tiles, bn;  // tile grid; BN (multiple of 32, <= 256)
-    int cm, cn;                // cluster shape: CTAs sharing B (along M) x sharing A (along N)
-    int num_sn, num_super;     // super-tiles (cm x cn tiles, one per cluster at a time)
-    uint32_t idesc;            // instruction descriptor for M=128, N=BN
+    int64_t M, N;              // D is M x N
+    int slices;                // 128-byte K slices per row (the last may be half zero fill)
+    int full_slices;           // whole slices: those the 3-D view covers
+    int d;                     // K slices per smem stage
+    int nk;                    // stages per tile
+    int num_n, bn;             // column tiles; tile width BN (multiple of 16)
+    int num_super;             // tiles (pairs: 256-row tiles)
+    uint32_t idesc;            // instruction descriptor
     float alpha;
     void *out;
     unsigned int *err;
-    int vec_store;             // linear: 1 when output rows are 16-byte aligned (16-byte stores)
-                               // conv: bytes each lane stores at once (a run of pixels of one channel)
-    int64_t hw;                // conv: output pixels per image (Ho * Wo)
+    int vec;                   // rows: 1 when output rows are 16-byte aligned (16-byte stores)
+                               // NCHW: bytes each lane stores at once (a run of one channel's pixels)
+    int64_t hw;                // NCHW: output pixels per image (Ho * Wo)
     int stages;                // smem ring depth
 };
 
-// Shared memory: S stages of A (128 rows) and B (BN rows) K slices of ROWB
-// bytes, the epilogue staging boxes, barriers. S is as many stages as fit (at
-// most 8): narrow tiles get a deeper ring.
-constexpr int kMaxStages = 8;
-int num_stages(int rowb, int bn) {
-    const int s = (kSmemMax - kReserve - kStagingBytes) / ((kBM + bn) * rowb);
+// B rows one CTA holds per slice.
+__host__ __device__ __forceinline__ int b_slot_rows(int bn, bool pair) { return pair ? bn / 2 : bn; }
+
+// Shared memory: S stages of D slices of A (128 rows) and B, the epilogue
+// staging boxes, barriers. S is as many stages as fit (at most 8).
+int stage_bytes(int bn, bool pair, int d) { return (kBM + b_slot_rows(bn, pair)) * kRowB * d; }
+int num_stages(int bn, bool pair, int d) {
+    const int s = (kSmemMax - kReserve - kStagingBytes) / stage_bytes(bn, pair, d);
     return s > kMaxStages ? kMaxStages : s;
 }
-int smem_bytes(int rowb, int bn) { return num_stages(rowb, bn) * (kBM + bn) * rowb + kStagingBytes + kReserve; }
+int smem_bytes(int bn, bool pair, int d) { return num_stages(bn, pair, d) * stage_bytes(bn, pair, d) + kStagingBytes + kReserve; }
 
 // TMEM column of the second accumulator buffer; also the largest BN.
 template <int CODE> __host__ __device__ constexpr uint32_t acc_stride() { return CODE == BT_CODE_E2M1 ? 240u : 256u; }
 
-// Instruction descriptor: D = F32, K-major A and B, M = 128, N = bn.
-uint32_t make_idesc(bt_code code, int bn) {
-    const uint32_t mn = ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(kBM) >> 4) << 24);
+// Instruction descriptor: D = F32, K-major A and B, M rows (128, or 256 for a
+// pair), N = bn.
+uint32_t make_idesc(bt_code code, int m, int bn) {
+    const uint32_t mn = ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(m) >> 4) << 24);
     if (code == BT_CODE_E4M3) return (1u << 4) | (0u << 7) | (0u << 10) | mn;       // E4M3 x E4M3
     return (1u << 7) | (1u << 10) | (1u << 23) | mn;   // block-scaled E2M1 x E2M1, UE8M0 scales, ids 0
-}
-
-template <int ROWB>
-__device__ __forceinline__ uint64_t operand_desc(uint32_t saddr) {
-    uint64_t d = tc::sw128_kmajor_desc(saddr);
-    if (ROWB == 64) {
-        // 64-byte swizzle: 8-row groups 512 bytes apart
-        d &= ~((static_cast<uint64_t>(0x3FFF) << 32) | (static_cast<uint64_t>(7) << 61));
-        d |= (static_cast<uint64_t>(512u >> 4) << 32) | (static_cast<uint64_t>(4u) << 61);
-    }
-    return d;
 }
 
 // 16 bytes of converted outputs from accumulators r[j0 .. j0 + 16/elem).
@@ -121,149 +133,214 @@ __device__ __forceinline__ uint4 chunk16(const uint32_t (&r)[32], int j0, float 
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One output value (conv epilogue) from its accumulator.
-template <int OUT>
-__device__ __forceinline__ typename OutT<OUT>::type from_acc(float acc, float alpha) {
-    if constexpr (OUT == BT_F32) return __fmul_rn(acc, alpha);
-    else if constexpr (OUT == BT_BF16) return __float2bfloat16_rn(__fmul_rn(acc, alpha));
-    else if constexpr (OUT == BT_F16) return __float2half_rn(__fmul_rn(acc, alpha));
-    else return __float2int_rn(acc);
-}
-
-// The bits of one output value (conv epilogue staging), in the low bits.
-template <int OUT>
-__device__ __forceinline__ uint32_t out_bits(float acc, float alpha) {
-    if constexpr (OUT == BT_F32 || OUT == BT_I32) return FromAcc<OUT>::bits(acc, alpha);
-    else if constexpr (OUT == BT_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(acc, alpha)));
-    else return __half_as_ushort(__float2half_rn(__fmul_rn(acc, alpha)));
-}
-
 // Position of 16-byte chunk q of staging-box row `row`: the 128-byte swizzle
 // (q ^ row % 8) for 4-byte outputs (128-byte rows), the 64-byte swizzle
-// (q ^ (row / 2) % 4) for 2-byte outputs (64-byte rows) -- the layouts TMA
-// expects for CU_TENSOR_MAP_SWIZZLE_128B / _64B.
+// (q ^ (row / 2) % 4) for 2-byte outputs (64-byte rows), so that 32 lanes
+// writing their rows' chunk q hit different banks.
 template <int ELEM>
 __device__ __forceinline__ uint32_t box_chunk(int q, int row) {
     return ELEM == 4 ? static_cast<uint32_t>(q ^ (row & 7)) : static_cast<uint32_t>(q ^ ((row >> 1) & 3));
 }
 
-template <int CODE, int ROWB, bool CONV, int OUT>
+// Global stores of 16, 8, 4 or 2 bytes (explicitly global; the low words of v).
+template <int V> __device__ __forceinline__ void st_global(uint8_t *p, const uint4 &v) {
+    if constexpr (V == 16)
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+    else if constexpr (V == 8)
+        asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+    else if constexpr (V == 4)
+        asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(v.x) : "memory");
+    else
+        asm volatile("st.global.b16 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(v.x)) : "memory");
+}
+template <int V> __device__ __forceinline__ uint4 ld_shared(uint32_t a) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (V == 16)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    else if constexpr (V == 8)
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    else if constexpr (V == 4)
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v.x) : "r"(a));
+    else {
+        uint16_t h;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+        v.x = h;
+    }
+    return v;
+}
+
+// NCHW read-back of one staged 32 x 32 box (rows = channels, columns =
+// pixels): each lane takes a run of V bytes (V / ELEM consecutive pixels,
+// inside one image and V-aligned) of one channel row; 32 / LPR rows per
+// instruction, so each store instruction covers whole runs of several rows.
+// `col` is the box's first column (pixel), `row0` its first row.
+template <int V, int ELEM>
+__device__ __forceinline__ void nchw_box(uint8_t *out, uint32_t sbox, int lane, uint32_t col, uint32_t ncol_end,
+                                         int64_t row0, int64_t M, uint32_t hw) {
+    constexpr int kBoxRow = 32 * ELEM;
+    constexpr int kLpr = kBoxRow / V;                    // lanes per row
+    constexpr int kRowsPer = 32 / kLpr;
+    const int q = lane % kLpr;
+    const uint32_t c = col + static_cast<uint32_t>(q * (V / ELEM));
+    if (c >= ncol_end) return;
+    const uint32_t ob = c / hw, pix = c - ob * hw;
+    uint8_t *base = out + (static_cast<int64_t>(ob) * M * hw + pix) * ELEM;
+    const uint32_t qb = static_cast<uint32_t>(q * V);
+#pragma unroll
+    for (int i = 0; i < 32 / kRowsPer; ++i) {
+        const int rr = lane / kLpr + i * kRowsPer;
+        const int64_t row = row0 + rr;
+        if (row >= M) break;
+        const uint32_t src = sbox + static_cast<uint32_t>(rr * kBoxRow) + (box_chunk<ELEM>(static_cast<int>(qb >> 4), rr) << 4) +
+                             (qb & 15u);
+        st_global<V>(base + row * hw * ELEM, ld_shared<V>(src));
+    }
+}
+
+template <int CODE, int LAYOUT, int OUT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-          const TcArgs a) {
-    const int S = a.stages;
-    const int bn = a.bn;
-    constexpr uint32_t kABytes = kBM * ROWB;
-    const uint32_t kBBytes = static_cast<uint32_t>(bn * ROWB);
-    constexpr int kMmaPerStage = ROWB / 32;        // K = 32 bytes per MMA
+tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUtensorMap tmB3,
+          const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, const TcArgs a) {
+    constexpr uint32_t kASlice = kBM * kRowB;      // A bytes per K slice (128 rows)
+    constexpr int kMmaPerSlice = kRowB / 32;       // K = 32 bytes per MMA
     using T = typename OutT<OUT>::type;
     constexpr int kElem = sizeof(T);
     constexpr int kBoxInner = 32 * kElem;          // bytes of one staging-box row: 32 output columns
+    constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
+    const int S = a.stages;
+    const int bn = a.bn;
+    const int D = a.d;
+    const uint32_t kBSlice = static_cast<uint32_t>(b_slot_rows(bn, PAIR) * kRowB);   // B bytes per K slice
+    const uint32_t kAStage = kASlice * D, kBStage = kBSlice * D;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sA = base, sB = base + S * kABytes;
-    const uint32_t sStage = sB + S * kBBytes;                        // epilogue staging boxes
+    const uint32_t sA = base, sB = base + S * kAStage;
+    const uint32_t sStage = sB + S * kBStage;                        // epilogue staging boxes
     const uint32_t bars = sStage + kStagingBytes;                    // full[S], empty[S], tfull[2], tempty[2], drain
     uint8_t *gbars = smem_raw + (bars - raw);
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbars + 8 * (2 * S + 5));
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbars + 8 * (2 * kMaxStages + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
     auto full = [&](int s) { return bars + 8u * s; };
-    auto empty = [&](int s) { return bars + 8u * (S + s); };
-    auto tfull = [&](int b) { return bars + 8u * (2 * S + b); };          // accumulator buffer b written
-    auto tempty = [&](int b) { return bars + 8u * (2 * S + 2 + b); };     // accumulator buffer b drained
-    const uint32_t drain = bars + 8u * (2 * S + 4);
+    auto empty = [&](int s) { return bars + 8u * (kMaxStages + s); };
+    auto tfull = [&](int b) { return bars + 8u * (2 * kMaxStages + b); };      // accumulator buffer b written
+    auto tempty = [&](int b) { return bars + 8u * (2 * kMaxStages + 2 + b); }; // accumulator buffer b drained
+    const uint32_t drain = bars + 8u * (2 * kMaxStages + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = PAIR ? tc::cluster_ctarank() : 0u;
+    const bool leader = !PAIR || crank == 0;                         // issues the MMAs
 
     if (threadIdx.x == 0) pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(full(s), 1);
-            // released by every CTA this one's copies land in (itself, its A
-            // sharers and its B sharers)
-            tc::mbar_init(empty(s), static_cast<uint32_t>(a.cm + a.cn - 1));
+            tc::mbar_init(empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(tfull(b), 1);
-            tc::mbar_init(tempty(b), 4);   // one arrival per epilogue warp
+            tc::mbar_init(tempty(b), PAIR ? 8u : 4u);   // one arrival per epilogue warp (of both CTAs of a pair)
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0u;
         tc::fence_mbar_init();
-        tc::prefetch_map(&tmA);
-        tc::prefetch_map(&tmB);
+        tc::prefetch_map(&tmA3);
+        tc::prefetch_map(&tmB3);
+        tc::prefetch_map(&tmA2);
+        tc::prefetch_map(&tmB2);
     }
     if (warp == 1) {
-        tc::tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
-        tc::tmem_relinquish();
+        if (PAIR) {
+            tc::tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+            tc::tmem_relinquish();
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const bool clustered = a.cm * a.cn > 1;
-    if (clustered) tc::cluster_sync();        // peers' barriers exist before any multicast lands
     const uint32_t tmem = *tmem_slot;
-    // position in the cluster: rm along M (B sharers), rn along N (A sharers)
-    const int crank = clustered ? static_cast<int>(tc::cluster_ctarank()) : 0;
-    const int rm = crank % a.cm, rn = crank / a.cm;
-    const int cluster = clustered ? static_cast<int>(tc::cluster_id_x()) : static_cast<int>(blockIdx.x);
-    const int nclusters = clustered ? static_cast<int>(tc::num_clusters_x()) : static_cast<int>(gridDim.x);
-    uint16_t maskA = 0, maskB = 0;
-    for (int j = 0; j < a.cn; ++j) maskA |= static_cast<uint16_t>(1u << (rm + a.cm * j));
-    for (int j = 0; j < a.cm; ++j) maskB |= static_cast<uint16_t>(1u << (j + a.cm * rn));
-    const uint16_t mask_release = maskA | maskB;
-    const int a_rows = kBM / a.cn;            // rows of the A tile this CTA loads
-    const int b_rows = a.bn / a.cm;           // rows of the B tile this CTA loads
     const int quarter = warp & 3;                                   // TMEM lanes this warp may touch
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-
-    if (CODE == BT_CODE_E2M1) {
-        if (warp >= 2) {
-            // unit block scales for A and B: every byte of columns [256, 288)
-            tc::tmem_st16_fill(tmem + lane_base + kSfCol, kUnitScales);
-            tc::tmem_st16_fill(tmem + lane_base + kSfCol + 16, kUnitScales);
-            tc::tmem_st_wait();
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
+    if (CODE == BT_CODE_E2M1 && warp >= 2) {
+        // unit block scales for A and B: every byte of the last 32 columns
+        tc::tmem_st16_fill(tmem + lane_base + kSfCol, kUnitScales);
+        tc::tmem_st16_fill(tmem + lane_base + kSfCol + 16, kUnitScales);
+        tc::tmem_st_wait();
     }
+    tc::fence_before_sync();
+    __syncthreads();
+    // the peer's barriers and block scales exist before any copy, commit or MMA reaches them
+    if (PAIR) tc::cluster_sync();
+    tc::fence_after_sync();
 
-    const uint32_t tx_bytes = static_cast<uint32_t>((kBM + bn) * ROWB);
+    const int unit = PAIR ? static_cast<int>(tc::cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int nunits = PAIR ? static_cast<int>(tc::num_clusters_x()) : static_cast<int>(gridDim.x);
+    // rows of the A tile and of the B tile this CTA loads
+    const int a_first = PAIR ? static_cast<int>(crank) * kBM : 0;
+    const int b_rows = b_slot_rows(bn, PAIR);
+    const int b_first = PAIR ? static_cast<int>(crank) * b_rows : 0;
+    // slices of stage kb of a tile: [kb * D, kb * D + count)
+    auto slice_count = [&](int kb) { return a.slices - kb * D < D ? a.slices - kb * D : D; };
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
             pdl_wait();                                   // operands come from the previous kernel
+            // a pair's copies complete on the even CTA's full barriers, which
+            // expect the bytes of both CTAs
+            const uint32_t slice_bytes = static_cast<uint32_t>((PAIR ? 2 : 1) * (kBM + b_rows) * kRowB);
             int s = 0;                                    // ring slot and its phase
             uint32_t ph = 0;
             uint32_t last_phase[kMaxStages];              // phase of each slot's last copy; 2 = none
 #pragma unroll
             for (int i = 0; i < kMaxStages; ++i) last_phase[i] = 2u;
             bool ok = true;
-            for (int st = cluster; st < a.num_super && ok; st += nclusters) {
-                const int mt = (st / a.num_sn) * a.cm + rm, nt = (st % a.num_sn) * a.cn + rn;
-                // this CTA's share of the A tile starts a_rows * rn rows in
-                const int64_t am0 = static_cast<int64_t>(mt) * kBM + static_cast<int64_t>(a_rows) * rn;
-                const int bn0 = nt * bn + b_rows * rm;                       // and of the B tile
-                const uint32_t a_off = static_cast<uint32_t>(a_rows * rn * ROWB);
-                const uint32_t b_off = static_cast<uint32_t>(b_rows * rm * ROWB);
+            for (int st = unit; st < a.num_super && ok; st += nunits) {
+                const int mt = st / a.num_n, nt = st % a.num_n;
+                const int am0 = mt * kTileRows + a_first;
+                const int bn0 = nt * bn + b_first;
                 for (int kb = 0; kb < a.nk; ++kb) {
                     if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
-                    tc::mbar_arrive_expect_tx(full(s), tx_bytes);
-                    const uint32_t adst = sA + s * kABytes + a_off, bdst = sB + s * kBBytes + b_off;
-                    if (a.cn > 1) tc::tma_load_2d_mc(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s), maskA);
-                    else tc::tma_load_2d(adst, &tmA, kb * ROWB, static_cast<int>(am0), full(s));
-                    if (a.cm > 1) tc::tma_load_2d_mc(bdst, &tmB, kb * ROWB, bn0, full(s), maskB);
-                    else tc::tma_load_2d(bdst, &tmB, kb * ROWB, bn0, full(s));
+                    const uint32_t adst = sA + s * kAStage, bdst = sB + s * kBStage;
+                    const uint32_t fbar = PAIR ? tc::mapa(full(s), 0u) : full(s);
+                    const int k0 = kb * D;
+                    const bool whole = k0 + D <= a.full_slices;
+                    if (whole) {
+                        // D whole slices: one box per operand
+                        if (leader) tc::mbar_arrive_expect_tx(full(s), slice_bytes * D);
+                        if (PAIR) {
+                            tc::tma_load_3d_pair(adst, &tmA3, 0, am0, k0, fbar);
+                            tc::tma_load_3d_pair(bdst, &tmB3, 0, bn0, k0, fbar);
+                        } else {
+                            tc::tma_load_3d(adst, &tmA3, 0, am0, k0, fbar);
+                            tc::tma_load_3d(bdst, &tmB3, 0, bn0, k0, fbar);
+                        }
+                    } else {
+                        // the row's last stage: slice by slice from the 2-D view
+                        const int cnt = slice_count(kb);
+                        if (leader) tc::mbar_arrive_expect_tx(full(s), slice_bytes * cnt);
+                        for (int i = 0; i < cnt; ++i) {
+                            const uint32_t ad = adst + i * kASlice, bd = bdst + i * kBSlice;
+                            if (PAIR) {
+                                tc::tma_load_2d_pair(ad, &tmA2, (k0 + i) * kRowB, am0, fbar);
+                                tc::tma_load_2d_pair(bd, &tmB2, (k0 + i) * kRowB, bn0, fbar);
+                            } else {
+                                tc::tma_load_2d(ad, &tmA2, (k0 + i) * kRowB, am0, fbar);
+                                tc::tma_load_2d(bd, &tmB2, (k0 + i) * kRowB, bn0, fbar);
+                            }
+                        }
+                    }
                     last_phase[s] = ph;
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
-            if (!ok) {
-                // let every issued copy land before the CTA can exit
+            if (!ok && leader) {
+                // let every issued copy land before the CTA can exit (a pair's
+                // copies all complete on the even CTA's barriers)
                 for (int i = 0; i < S; ++i) {
                     if (last_phase[i] < 2u) {
                         const unsigned long long t0 = globaltimer_ns();
@@ -274,16 +351,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ---------------- MMA issuer ----------------
             int s = 0;
             uint32_t ph = 0;
             int local = 0;
             bool ok = true;
-            for (int st = cluster; st < a.num_super && ok; st += nclusters, ++local) {
+            for (int st = unit; st < a.num_super && ok; st += nunits, ++local) {
                 const int buf = local & 1;
                 if (local >= 2) {
-                    // the epilogue has drained this buffer (two tiles ago)
+                    // the epilogue (of both CTAs of a pair) has drained this buffer
                     if (!tc::wait_bounded(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err))
                         break;
                     tc::fence_after_sync();
@@ -292,22 +369,34 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 for (int kb = 0; kb < a.nk; ++kb) {
                     if (!tc::wait_bounded(full(s), ph, abort_flag, a.err)) { ok = false; break; }
                     tc::fence_after_sync();
+                    const int cnt = slice_count(kb);
+                    for (int i = 0; i < cnt; ++i) {
 #pragma unroll
-                    for (int kk = 0; kk < kMmaPerStage; ++kk) {
-                        const uint64_t bd = operand_desc<ROWB>(sB + s * kBBytes + kk * 32);
-                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-                        const uint64_t ad = operand_desc<ROWB>(sA + s * kABytes + kk * 32);
-                        if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, ad, bd, a.idesc, acc);
-                        else tc::mma_mxf4(dacc, ad, bd, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+                        for (int kk = 0; kk < kMmaPerSlice; ++kk) {
+                            const uint64_t ad = tc::sw128_kmajor_desc(sA + s * kAStage + i * kASlice + kk * 32);
+                            const uint64_t bd = tc::sw128_kmajor_desc(sB + s * kBStage + i * kBSlice + kk * 32);
+                            const uint32_t acc = (kb | i | kk) != 0 ? 1u : 0u;
+                            if (PAIR) {
+                                if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4_pair(dacc, ad, bd, a.idesc, acc);
+                                else tc::mma_mxf4_pair(dacc, ad, bd, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+                            } else {
+                                if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, ad, bd, a.idesc, acc);
+                                else tc::mma_mxf4(dacc, ad, bd, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+                            }
+                        }
                     }
-                    if (clustered) tc::mma_commit_mc(empty(s), mask_release);
+                    if (PAIR) tc::mma_commit_pair(empty(s), 0x3);
                     else tc::mma_commit(empty(s));
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
-                if (ok) tc::mma_commit(tfull(buf));
+                if (ok) {
+                    if (PAIR) tc::mma_commit_pair(tfull(buf), 0x3);
+                    else tc::mma_commit(tfull(buf));
+                }
             }
             // every MMA issued must finish before the accumulator is freed
-            tc::mma_commit(drain);
+            if (PAIR) tc::mma_commit_pair(drain, 0x1);
+            else tc::mma_commit(drain);
             const unsigned long long t0 = globaltimer_ns();
             while (!tc::mbar_try_wait(drain, 0u) && globaltimer_ns() - t0 < kWaitNs) {}
         }
@@ -316,11 +405,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // ---------------- epilogue (warps 2..5) ----------------
         pdl_wait();                                       // the previous kernel may still use `out`
         T *out = static_cast<T *>(a.out);
-        const uint32_t my_stage = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // one box per warp
+        const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // this warp's staging box
         int local = 0;
-        for (int st = cluster; st < a.num_super; st += nclusters, ++local) {
-            const int mt = (st / a.num_sn) * a.cm + rm, nt = (st % a.num_sn) * a.cn + rn;
-            const int64_t m0 = static_cast<int64_t>(mt) * kBM;
+        for (int st = unit; st < a.num_super; st += nunits, ++local) {
+            const int mt = st / a.num_n, nt = st % a.num_n;
+            const int64_t m0 = static_cast<int64_t>(mt) * kTileRows + (PAIR ? static_cast<int64_t>(crank) * kBM : 0);
             const int n0 = nt * bn;
             const int buf = local & 1;
             if (!tc::wait_bounded(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err)) break;
@@ -330,11 +419,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 // every TMEM read of this tile is complete: hand the accumulators back
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tempty(buf));
+                if (lane == 0) {
+                    if (PAIR && crank != 0) tc::mbar_arrive_cluster(tc::mapa(tempty(buf), 0u));
+                    else tc::mbar_arrive(tempty(buf));
+                }
                 released = true;
             };
-            // Boxes of 32 rows x 32 columns; the TMEM read of the next box is in
-            // flight while the current one is converted and stored.
             const int64_t ncols = a.N - n0 < bn ? a.N - n0 : bn;
             const int64_t ncol_end = n0 + ncols;                             // this tile's columns end here
             const int nbox = ncols > 0 ? static_cast<int>((ncols + 31) / 32) : 0;
@@ -342,117 +432,63 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const int total = mrow0 < a.M ? nbox : 0;
             const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
             auto tcol_of = [&](int b) { return tbase + static_cast<uint32_t>(32 * b); };
-            // conv: the output run this lane stores. With vw > kElem, a run of
-            // vw / kElem pixels of one channel (vw bytes), starting at row
-            // m = mrow0 + q * (vw / kElem) of the warp's 32; runs never straddle two
-            // images (hw is a multiple of the run). Otherwise one pixel, m = mrow0 + lane.
-            const int vw = CONV ? a.vec_store : 0;
-            const bool runs = CONV && vw > kElem;
-            const int lpr = runs ? kBoxInner / vw : 32;                      // lanes per staged channel row
-            const int q = lane % lpr;
-            const int64_t m = mrow0 + (runs ? q * (vw / kElem) : lane);
-            const bool row_ok = m < a.M;
-            T *pix_out = out;
-            if constexpr (CONV) {
-                const int64_t ob = row_ok ? m / a.hw : 0;
-                pix_out = out + (ob * a.N + n0) * a.hw + (m - ob * a.hw);
-            }
             auto emit = [&](const uint32_t (&r)[32], int b) {
                 const int c0 = 32 * b;
-                if constexpr (CONV) {
-                    if (!runs) {
-                        // NCHW: one store per channel, 32 consecutive pixels across the warp
-                        if (!row_ok) return;
+                // stage the box: row = this lane's TMEM lane, 32 columns, swizzled;
+                // reading it back across rows lets every store instruction cover
+                // whole row segments
+                __syncwarp();                                                 // previous box fully read back
+                constexpr int kChunks = kBoxInner / 16;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (c0 + j < ncols)
-                                pix_out[static_cast<int64_t>(c0 + j) * a.hw] = from_acc<OUT>(__uint_as_float(r[j]), a.alpha);
-                        return;
-                    }
-                    // NCHW through the staging box, transposed to [channel][pixel]
-                    // rows; then each lane stores its run of one channel, 32 / lpr
-                    // channels per instruction
-                    const uint32_t sbox = my_stage;
-                    __syncwarp();                                             // previous box fully read back
+                for (int q = 0; q < kChunks; ++q) {
+                    const uint32_t addr = sbox + static_cast<uint32_t>(lane * kBoxInner) + (box_chunk<kElem>(q, lane) << 4);
+                    const uint4 w = chunk16<OUT, kElem>(r, q * (16 / kElem), a.alpha);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w.x), "r"(w.y), "r"(w.z),
+                                 "r"(w.w)
+                                 : "memory");
+                }
+                __syncwarp();
+                if constexpr (LAYOUT == kNchwOut) {
+                    uint8_t *ob = reinterpret_cast<uint8_t *>(out);
+                    const uint32_t col = static_cast<uint32_t>(n0 + c0), cend = static_cast<uint32_t>(ncol_end);
+                    const uint32_t hw = static_cast<uint32_t>(a.hw);
+                    if (a.vec == 16) nchw_box<16, kElem>(ob, sbox, lane, col, cend, mrow0, a.M, hw);
+                    else if (a.vec == 8) nchw_box<8, kElem>(ob, sbox, lane, col, cend, mrow0, a.M, hw);
+                    else if constexpr (kElem == 4) nchw_box<4, kElem>(ob, sbox, lane, col, cend, mrow0, a.M, hw);
+                    else if (a.vec == 4) nchw_box<4, kElem>(ob, sbox, lane, col, cend, mrow0, a.M, hw);
+                    else nchw_box<2, kElem>(ob, sbox, lane, col, cend, mrow0, a.M, hw);
+                } else if (a.vec) {
+                    // aligned rows: read the box back as 16-byte chunks, kChunks lanes
+                    // per row, 32/kChunks rows per instruction, and store them whole
+                    constexpr int kRowsPer = 32 / kChunks;
+                    const int q = lane % kChunks;
+                    const int64_t col = n0 + c0 + q * (16 / kElem);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const uint32_t addr = sbox + static_cast<uint32_t>(j * kBoxInner + lane * kElem);
-                        const uint32_t v = out_bits<OUT>(__uint_as_float(r[j]), a.alpha);
-                        if (kElem == 4) asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-                        else asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
-                    }
-                    __syncwarp();
-                    if (!row_ok) return;
-                    const int rows_per = 32 / lpr;
-                    for (int rr = lane / lpr; rr < 32; rr += rows_per) {
-                        if (c0 + rr >= ncols) break;
-                        const uint32_t addr = sbox + static_cast<uint32_t>(rr * kBoxInner + q * vw);
-                        uint8_t *dst = reinterpret_cast<uint8_t *>(pix_out + static_cast<int64_t>(c0 + rr) * a.hw);
-                        if (vw == 16) {
-                            uint4 v;
-                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-                            *reinterpret_cast<uint4 *>(dst) = v;
-                        } else if (vw == 8) {
-                            uint2 v;
-                            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-                            *reinterpret_cast<uint2 *>(dst) = v;
-                        } else {
-                            uint32_t v;
-                            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-                            *reinterpret_cast<uint32_t *>(dst) = v;
-                        }
+                    for (int rr0 = 0; rr0 < 32; rr0 += kRowsPer) {
+                        const int rr = rr0 + lane / kChunks;
+                        const uint32_t addr = sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(q, rr) << 4);
+                        const uint4 v = ld_shared<16>(addr);
+                        const int64_t row = mrow0 + rr;
+                        if (row < a.M && col < ncol_end)
+                            st_stream_v4(reinterpret_cast<uint8_t *>(out) + (row * a.N + col) * kElem, v);
                     }
                 } else {
-                    // row-major [M, N] through the warp's swizzled staging box
-                    const uint32_t sbox = my_stage;
-                    __syncwarp();                                             // previous box fully read back
-                    constexpr int kChunks = kBoxInner / 16;
-#pragma unroll
-                    for (int q = 0; q < kChunks; ++q) {
-                        const uint32_t addr = sbox + static_cast<uint32_t>(lane * kBoxInner) + (box_chunk<kElem>(q, lane) << 4);
-                        const uint4 w = chunk16<OUT, kElem>(r, q * (16 / kElem), a.alpha);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w.x), "r"(w.y),
-                                     "r"(w.z), "r"(w.w)
-                                     : "memory");
-                    }
-                    __syncwarp();
-                    if (a.vec_store) {
-                        // aligned rows: read the box back as 16-byte chunks, kChunks lanes
-                        // per row, 32/kChunks rows per instruction, and store them whole
-                        constexpr int kRowsPer = 32 / kChunks;
-                        const int q = lane % kChunks;
-                        const int64_t col = n0 + c0 + q * (16 / kElem);
-#pragma unroll
-                        for (int rr0 = 0; rr0 < 32; rr0 += kRowsPer) {
-                            const int rr = rr0 + lane / kChunks;
-                            const uint32_t addr = sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(q, rr) << 4);
-                            uint4 v;
-                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                         : "r"(addr));
-                            const int64_t row = mrow0 + rr;
-                            if (row < a.M && col < ncol_end)
-                                st_stream_v4(reinterpret_cast<uint8_t *>(out) + (row * a.N + col) * kElem, v);
-                        }
-                    } else {
-                        // ragged N: read the box back one row at a time, lanes along
-                        // the columns, so every store is 32 consecutive elements
-                        const int64_t col = n0 + c0 + lane;
-                        constexpr int kPer = 16 / kElem;
-                        const uint32_t off = static_cast<uint32_t>((lane % kPer) * kElem);
+                    // ragged N: read the box back one row at a time, lanes along
+                    // the columns, so every store is 32 consecutive elements
+                    const int64_t col = n0 + c0 + lane;
+                    constexpr int kPer = 16 / kElem;
+                    const uint32_t off = static_cast<uint32_t>((lane % kPer) * kElem);
 #pragma unroll 4
-                        for (int rr = 0; rr < 32; ++rr) {
-                            const uint32_t addr =
-                                sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(lane / kPer, rr) << 4) + off;
-                            uint32_t v;
-                            if (kElem == 4) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-                            else asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
-                            const int64_t row = mrow0 + rr;
-                            if (row < a.M && col < ncol_end) {
-                                if (kElem == 4) reinterpret_cast<uint32_t *>(out)[row * a.N + col] = v;
-                                else reinterpret_cast<uint16_t *>(out)[row * a.N + col] = static_cast<uint16_t>(v);
-                            }
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const uint32_t addr =
+                            sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(lane / kPer, rr) << 4) + off;
+                        uint32_t v;
+                        if (kElem == 4) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+                        else asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+                        const int64_t row = mrow0 + rr;
+                        if (row < a.M && col < ncol_end) {
+                            if (kElem == 4) reinterpret_cast<uint32_t *>(out)[row * a.N + col] = v;
+                            else reinterpret_cast<uint16_t *>(out)[row * a.N + col] = static_cast<uint16_t>(v);
                         }
                     }
                 }
@@ -478,11 +514,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     tc::fence_before_sync();
     __syncthreads();
-    // no CTA leaves while a peer may still multicast into it or release its stages
-    if (clustered) tc::cluster_sync();
+    // no CTA of a pair leaves while its peer may still signal its barriers or
+    // run MMAs on its shared memory and TMEM
+    if (PAIR) tc::cluster_sync();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        if (PAIR) tc::tmem_dealloc_pair(tmem, kTmemCols);
+        else tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -515,150 +553,179 @@ int sm_count() {
     return n[dev];
 }
 
-// 2-D byte matrix [rows, row_bytes] with row pitch `pitch`; box = box_inner bytes x box_rows.
-bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t pitch, uint64_t rows, uint32_t box_inner,
-            uint32_t box_rows) {
+// Views of a byte matrix [rows, row_bytes] (row pitch = row_bytes), 128-byte
+// swizzle, zero fill outside:
+//   2-D {row_bytes, rows}, box 128 bytes x box_rows;
+//   3-D {128, rows, full slices} (strides row_bytes, 128), box 128 x box_rows
+//   x d: d consecutive whole K slices in one copy, landing slice after slice.
+bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
     auto fn = encode_tiled();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {row_bytes, rows};
-    cuuint64_t strides[1] = {pitch};
-    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kRowB), box_rows};
     cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapSwizzle sw = box_inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool map_3d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint64_t full_slices,
+            uint32_t box_rows, uint32_t d) {
+    auto fn = encode_tiled();
+    if (fn == nullptr) return false;
+    // rows without a whole slice never use this view: encode a one-row stand-in
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kRowB), full_slices > 0 ? rows : 1, full_slices > 0 ? full_slices : 1};
+    cuuint64_t strides[2] = {full_slices > 0 ? row_bytes : static_cast<cuuint64_t>(kRowB), static_cast<cuuint64_t>(kRowB)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowB), box_rows, d};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tile configuration: BN (a multiple of 16 up to 240 for E2M1 / 256 for E4M3;
-// the epilogue masks the part of its last 32-column box past the tile) and the
-// cluster shape CM x CN. The cost
-// model: a problem takes `rounds` waves of super-tiles over the clusters;
-// each K stage costs the largest of its MMA time (one M=128 MMA per 32 bytes,
-// about 116 clocks on GB300 whatever N up to 256), the time for the whole
-// stage to land in this SM's shared memory (about 95 bytes per clock per SM
-// for TMA into the ring; multicast inside a cluster lowers L2 reads but not
-// the bytes each SM receives, so clusters only change the wave count), and
-// the pipelined stage time measured in whole launches on GB300 (about 1230
-// clocks per 128-byte stage and 790 per 64-byte stage, so 64-byte stages only
-// pay off when they save a half-empty last stage of many); with the
-// accumulator double-buffered only the last tile's epilogue (about 8 clocks
-// per output column) is exposed.
-// BT_TC_CONFIG="cm,cn,bn" overrides the choice.
+// Tile configuration: the shape (single CTAs or CTA pairs), BN (a multiple of
+// 16 up to 240 for E2M1 / 256 for E4M3; the epilogue masks the part of its
+// last 32-column box past the tile) and D, the K slices per stage.
+// The cost model, from measurements on GB300 (2070 MHz): a problem takes
+// `rounds` waves of tiles over the SMs (pairs: SMs / 2 at a time); a stage
+// costs the larger of its MMA time (an M=128 MMA of 32 bytes of K per row
+// takes N / 2 clocks per SM, pair or not) and its copy time (about 480 clocks
+// per TMA box of up to two slices, the same for any box size; a box of four
+// slices is costed 560), plus a tile's epilogue where it is longer than the
+// tile's MMAs (about 20 clocks per output column with the accumulator
+// double-buffered); the last tile's epilogue is always exposed.
+// BT_TC_CONFIG="bn,d" (single) or "pair,bn,d" overrides the choice.
 struct TileCfg {
-    int cm, cn, bn;
+    bool pair;
+    int bn, d;
     double cost;     // modelled clocks of the whole launch
 };
 
-TileCfg choose_cfg(int64_t M, int64_t N, int nk, int rowb, int sms, int max_bn) {
-    TileCfg best{1, 1, max_bn, 0.0};
+double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int sms) {
+    const int rows = pair ? 2 * kBM : kBM;
+    const int64_t num_m = (M + rows - 1) / rows, num_n = (N + bn - 1) / bn;
+    const int64_t units = pair ? sms / 2 : sms;
+    const int64_t tiles = num_m * num_n;
+    const int64_t rounds = (tiles + units - 1) / units;
+    const int nk = (slices + d - 1) / d;
+    const double mma = static_cast<double>(d) * (kRowB / 32) * (bn / 2.0);
+    const double copy = 2.0 * (d <= 2 ? 480.0 : 560.0);
+    const double stage = mma > copy ? mma : copy;
+    double tile = nk * stage;
+    const double epi = 20.0 * bn;
+    if (epi > tile) tile = epi;
+    return static_cast<double>(rounds) * tile + epi + 600.0;
+}
+
+TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn) {
     if (const char *env = std::getenv("BT_TC_CONFIG")) {
-        int cm = 0, cn = 0, bn = 0;
-        if (std::sscanf(env, "%d,%d,%d", &cm, &cn, &bn) == 3 && (cm == 1 || cm == 2) && (cn == 1 || cn == 2) &&
-            bn >= 32 && bn <= max_bn && bn % 16 == 0 && (bn / cm) % 16 == 0)
-            return TileCfg{cm, cn, bn, 0.0};
+        int bn = 0, d = 0;
+        const bool pair = std::strncmp(env, "pair,", 5) == 0;
+        if (std::sscanf(pair ? env + 5 : env, "%d,%d", &bn, &d) == 2 && bn >= 32 && bn <= max_bn && bn % 16 == 0 &&
+            (d == 1 || d == 2 || d == 4) && num_stages(bn, pair, d) >= 2)
+            return TileCfg{pair, bn, d, 0.0};
     }
-    const int64_t num_m = (M + kBM - 1) / kBM;
-    double best_cost = -1.0;
-    for (int cm = 1; cm <= 2; ++cm) {
-        for (int cn = 1; cn <= 2; ++cn) {
-            const int64_t clusters = sms / (cm * cn);
+    TileCfg best{false, max_bn, 1, -1.0};
+    for (int p = 1; p >= 0; --p)
+        for (int d = 4; d >= 1; d /= 2)
             for (int bn = max_bn; bn >= 32; bn -= 16) {
-                if ((bn / cm) % 16 != 0) continue;           // B slice rows: whole 16-row groups
-                const int64_t num_n = (N + bn - 1) / bn;
-                const int64_t super = ((num_m + cm - 1) / cm) * ((num_n + cn - 1) / cn);
-                const int64_t rounds = (super + clusters - 1) / clusters;
-                const double mma = (rowb / 32) * 116.0;
-                const double land = static_cast<double>(kBM + bn) * rowb / 95.0;
-                const double piped = 350.0 + 880.0 * rowb / 128.0;
-                double stage = mma > land ? mma : land;
-                if (piped > stage) stage = piped;
-                const double cost = static_cast<double>(rounds) * nk * stage + 8.0 * bn + 600.0;
-                if (best_cost < 0.0 || cost < best_cost * 0.999) {
-                    best_cost = cost;
-                    best = TileCfg{cm, cn, bn, cost};
-                }
+                if (num_stages(bn, p == 1, d) < 2) continue;
+                const double c = tile_cost(p == 1, bn, d, M, N, slices, sms);
+                if (best.cost < 0.0 || c < best.cost * 0.999) best = TileCfg{p == 1, bn, d, c};
             }
-        }
-    }
     return best;
 }
 
-template <int CODE, int ROWB, bool CONV, int OUT>
-cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, TcArgs a, cudaStream_t s) {
-    auto kern = tc_kernel<CODE, ROWB, CONV, OUT>;
-    a.stages = num_stages(ROWB, a.bn);
-    const int smem = smem_bytes(ROWB, a.bn);
+struct Maps {
+    CUtensorMap a3, b3, a2, b2;
+};
+
+template <int CODE, int LAYOUT, int OUT, bool PAIR>
+cudaError_t launch_t(const Maps &mp, TcArgs a, cudaStream_t s) {
+    auto kern = tc_kernel<CODE, LAYOUT, OUT, PAIR>;
+    a.stages = num_stages(a.bn, PAIR, a.d);
+    const int smem = smem_bytes(a.bn, PAIR, a.d);
     if (a.stages < 2 || smem > kSmemMax) return cudaErrorInvalidValue;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] { attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax); });
     if (attr_err != cudaSuccess) return attr_err;
-    const int csize = a.cm * a.cn;
+    const int csize = PAIR ? 2 : 1;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1] = pdl_attribute();
+    attr[0] = pdl_attribute();
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(csize);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    // as many clusters as fit at once on the device, at most one per super-tile
-    int clusters = sm_count() / csize;
-    if (csize > 1) {
-        cfg.gridDim = dim3(static_cast<unsigned>(clusters * csize), 1, 1);
+    cfg.numAttrs = PAIR ? 2 : 1;
+    // as many units (CTAs, or pairs) as fit at once on the device, at most one per tile
+    int units = sm_count() / csize;
+    if (PAIR) {
+        cfg.gridDim = dim3(static_cast<unsigned>(units * csize), 1, 1);
         int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < clusters) clusters = fit;
+        if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < units) units = fit;
     }
-    if (clusters > a.num_super) clusters = a.num_super;
-    if (clusters < 1) clusters = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * csize), 1, 1);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
+    if (units > a.num_super) units = a.num_super;
+    if (units < 1) units = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(units * csize), 1, 1);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.a3, mp.b3, mp.a2, mp.b2, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int CODE, int ROWB, bool CONV>
-cudaError_t launch_out(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
-                       bt_dtype out_t, cudaStream_t s) {
+template <int CODE, int LAYOUT, bool PAIR>
+cudaError_t launch_out(const Maps &mp, const TcArgs &a, bt_dtype out_t, cudaStream_t s) {
     switch (out_t) {
-        case BT_F32: return launch_t<CODE, ROWB, CONV, BT_F32>(ma, mb, a, s);
-        case BT_BF16: return launch_t<CODE, ROWB, CONV, BT_BF16>(ma, mb, a, s);
-        case BT_F16: return launch_t<CODE, ROWB, CONV, BT_F16>(ma, mb, a, s);
-        default: return launch_t<CODE, ROWB, CONV, BT_I32>(ma, mb, a, s);
+        case BT_F32: return launch_t<CODE, LAYOUT, BT_F32, PAIR>(mp, a, s);
+        case BT_BF16: return launch_t<CODE, LAYOUT, BT_BF16, PAIR>(mp, a, s);
+        case BT_F16: return launch_t<CODE, LAYOUT, BT_F16, PAIR>(mp, a, s);
+        default: return launch_t<CODE, LAYOUT, BT_I32, PAIR>(mp, a, s);
     }
 }
 
-template <bool CONV>
-cudaError_t launch_code(bt_code code, int rowb, const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
-                        bt_dtype out_t, cudaStream_t s) {
+template <int LAYOUT>
+cudaError_t launch_code(bt_code code, bool pair, const Maps &mp, const TcArgs &a, bt_dtype out_t, cudaStream_t s) {
     if (code == BT_CODE_E4M3)
-        return rowb == 128 ? launch_out<BT_CODE_E4M3, 128, CONV>(ma, mb, a, out_t, s)
-                           : launch_out<BT_CODE_E4M3, 64, CONV>(ma, mb, a, out_t, s);
-    return rowb == 128 ? launch_out<BT_CODE_E2M1, 128, CONV>(ma, mb, a, out_t, s)
-                       : launch_out<BT_CODE_E2M1, 64, CONV>(ma, mb, a, out_t, s);
+        return pair ? launch_out<BT_CODE_E4M3, LAYOUT, true>(mp, a, out_t, s)
+                    : launch_out<BT_CODE_E4M3, LAYOUT, false>(mp, a, out_t, s);
+    return pair ? launch_out<BT_CODE_E2M1, LAYOUT, true>(mp, a, out_t, s)
+                : launch_out<BT_CODE_E2M1, LAYOUT, false>(mp, a, out_t, s);
 }
 
 int out_elem_bytes(bt_dtype t) { return t == BT_BF16 || t == BT_F16 ? 2 : 4; }
 
-// Fill the tile-grid fields of `a` for configuration `c`.
-bool set_grid(TcArgs &a, const TileCfg &c, int64_t M, int64_t N) {
-    a.cm = c.cm;
-    a.cn = c.cn;
+// Plan the tiles of an M x N contraction over rows of rb bytes (a multiple of
+// 64) and encode the maps.
+bool plan(TcArgs &a, Maps &mp, TileCfg &c, bt_code code, const uint8_t *ap, const uint8_t *bp, int64_t M, int64_t N,
+          int64_t rb) {
+    if (rb % 64 != 0 || M > (int64_t(1) << 31) - 512 || N > (int64_t(1) << 31) - 512) return false;
+    a.M = M;
+    a.N = N;
+    a.slices = static_cast<int>((rb + kRowB - 1) / kRowB);
+    a.full_slices = static_cast<int>(rb / kRowB);
+    const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;
+    c = choose_cfg(M, N, a.slices, sm_count(), max_bn);
     a.bn = c.bn;
-    const int64_t num_m = (M + kBM - 1) / kBM, num_n = (N + c.bn - 1) / c.bn;
-    const int64_t num_sn = (num_n + c.cn - 1) / c.cn;
-    const int64_t num_super = ((num_m + c.cm - 1) / c.cm) * num_sn;
-    if (num_super > (int64_t(1) << 30)) return false;
+    a.d = c.d;
+    a.nk = (a.slices + a.d - 1) / a.d;
+    const int rows = c.pair ? 2 * kBM : kBM;
+    const int64_t num_m = (M + rows - 1) / rows, num_n = (N + c.bn - 1) / c.bn;
+    if (num_m * num_n > (int64_t(1) << 30)) return false;
     a.num_n = static_cast<int>(num_n);
-    a.num_tiles = static_cast<int>(num_m * num_n);
-    a.num_sn = static_cast<int>(num_sn);
-    a.num_super = static_cast<int>(num_super);
-    return true;
+    a.num_super = static_cast<int>(num_m * num_n);
+    a.idesc = make_idesc(code, rows, a.bn);
+    const uint32_t b_box = static_cast<uint32_t>(b_slot_rows(a.bn, c.pair));
+    return map_3d(&mp.a3, ap, static_cast<uint64_t>(rb), static_cast<uint64_t>(M), static_cast<uint64_t>(a.full_slices),
+                  kBM, static_cast<uint32_t>(a.d)) &&
+           map_3d(&mp.b3, bp, static_cast<uint64_t>(rb), static_cast<uint64_t>(N), static_cast<uint64_t>(a.full_slices),
+                  b_box, static_cast<uint32_t>(a.d)) &&
+           map_2d(&mp.a2, ap, static_cast<uint64_t>(rb), static_cast<uint64_t>(M), kBM) &&
+           map_2d(&mp.b2, bp, static_cast<uint64_t>(rb), static_cast<uint64_t>(N), b_box);
 }
 
 }  // namespace
@@ -667,55 +734,38 @@ bool tc_available() { return encode_tiled() != nullptr; }
 
 cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M, int64_t N, int64_t K,
                              float alpha, void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
-    const int64_t rb = row_bytes(K, code);
     TcArgs a{};
-    a.M = M; a.N = N; a.nk = static_cast<int>((rb + 127) / 128); a.alpha = alpha; a.out = out; a.err = err;
+    Maps mp;
+    TileCfg c;
+    if (!plan(a, mp, c, code, xp, wp, M, N, row_bytes(K, code))) return cudaErrorInvalidValue;
+    a.alpha = alpha;
+    a.out = out;
+    a.err = err;
     const int64_t ob = out_elem_bytes(out_t);
-    a.vec_store = ((N * ob) % 16 == 0) && aligned(out, 16) ? 1 : 0;
-    const TileCfg c = choose_cfg(M, N, a.nk, 128, sm_count(), code == BT_CODE_E2M1 ? 240 : 256);
-    if (!set_grid(a, c, M, N)) return cudaErrorInvalidValue;
-    a.idesc = make_idesc(code, a.bn);
-    CUtensorMap ma, mb;
-    if (!map_2d(&ma, xp, rb, rb, M, 128, static_cast<uint32_t>(kBM / a.cn)) ||
-        !map_2d(&mb, wp, rb, rb, N, 128, static_cast<uint32_t>(a.bn / a.cm)))
-        return cudaErrorInvalidValue;
-    return launch_code<false>(code, 128, ma, mb, a, out_t, s);
+    a.vec = ((N * ob) % 16 == 0) && aligned(out, 16) ? 1 : 0;
+    return launch_code<kRowsOut>(code, c.pair, mp, a, out_t, s);
 }
 
 cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
                            void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
-    // A: the im2col rows [M, k*k*rbc]; B: the weights [O, k*k*rbc]. Rows are a
-    // multiple of 64 bytes: 128-byte stages (the last one half zero fill when
-    // the row is an odd number of 64-byte blocks) or 64-byte stages, whichever
-    // the cost model prefers.
+    // D = W x rows^T: rows of the tile are output channels, columns output pixels.
     const int64_t krow = static_cast<int64_t>(g.k) * g.k * row_bytes(g.C, code);
-    if (krow % 64 != 0) return cudaErrorInvalidValue;
     TcArgs a{};
-    a.M = g.B * g.Ho * g.Wo; a.N = g.O; a.alpha = alpha; a.out = out; a.err = err;
+    Maps mp;
+    TileCfg c;
+    if (!plan(a, mp, c, code, wp, rows, g.O, g.B * g.Ho * g.Wo, krow)) return cudaErrorInvalidValue;
+    a.alpha = alpha;
+    a.out = out;
+    a.err = err;
     a.hw = g.Ho * g.Wo;
     // widest store of a run of one channel's pixels that keeps every run inside
     // one image and naturally aligned
     const int eb = out_elem_bytes(out_t);
-    a.vec_store = eb;
+    a.vec = eb;
     for (int v = 16; v > eb; v /= 2) {
-        if ((a.hw * eb) % v == 0 && aligned(out, static_cast<size_t>(v))) { a.vec_store = v; break; }
+        if ((a.hw * eb) % v == 0 && aligned(out, static_cast<size_t>(v))) { a.vec = v; break; }
     }
-    const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;
-    const int nk128 = static_cast<int>((krow + 127) / 128), nk64 = static_cast<int>(krow / 64);
-    TileCfg c = choose_cfg(a.M, a.N, nk128, 128, sm_count(), max_bn);
-    int rowb = 128;
-    a.nk = nk128;
-    if (krow % 128 != 0) {
-        const TileCfg c64 = choose_cfg(a.M, a.N, nk64, 64, sm_count(), max_bn);
-        if (c64.cost < c.cost) { c = c64; rowb = 64; a.nk = nk64; }
-    }
-    if (!set_grid(a, c, a.M, a.N)) return cudaErrorInvalidValue;
-    a.idesc = make_idesc(code, a.bn);
-    CUtensorMap ma, mb;
-    if (!map_2d(&ma, rows, krow, krow, a.M, static_cast<uint32_t>(rowb), static_cast<uint32_t>(kBM / a.cn)) ||
-        !map_2d(&mb, wp, krow, krow, g.O, static_cast<uint32_t>(rowb), static_cast<uint32_t>(a.bn / a.cm)))
-        return cudaErrorInvalidValue;
-    return launch_code<true>(code, rowb, ma, mb, a, out_t, s);
+    return launch_code<kNchwOut>(code, c.pair, mp, a, out_t, s);
 }
 
 }  // namespace bt
