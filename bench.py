@@ -16,6 +16,7 @@ on the data path) and the max-over-ranks time gives the whole-job value.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -366,7 +367,10 @@ def run_ours(args, rank, world):
         "kernel_ms": {"pack": round(pack_ms, 5), "contraction": round(gemm_ms, 5)},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src}: {peak_how}", "kernel": "contraction"},
+                     "traffic_unit": "DRAM bytes per tc_kernel launch (ncu, this kernel source)",
+                     "peak_source": f"{peak_src}: {peak_how}",
+                     "kernel": "contraction" if wl.kind == "linear" or code == bt.BT_CODE_BITS
+                     else "contraction (im2col gather + tc_kernel)"},
         "pack_roofline": {"bound": "hbm", "achieved": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9, 1),
                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
@@ -390,16 +394,30 @@ def pack_bytes(wl, code, bt):
     return wl.x.numel() * wl.x.element_size() + B * H * W * bt.bt_packed_row_bytes(C, code)
 
 
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the sha256 of the contraction kernel's sources."""
+    h = hashlib.sha256()
+    for f in ("tc_gemm.cu", "tc_ptx.cuh"):
+        with open(os.path.join(ROOT, "xnor_popcount_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(workload: str, algo: str):
-    """DRAM bytes per contraction launch from a committed ncu summary, if one
-    exists for this exact kernel build and workload."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per contraction launch from the committed ncu summary, if one
+    exists for this workload and for the kernel source as it is now."""
+    p = os.path.join(ROOT, "profiles", "contraction_dram_traffic.txt")
     if not os.path.exists(p):
         return None
     try:
-        return json.load(open(p)).get(f"{workload}/{algo}")
+        src = kernel_source_hash()
+        for line in open(p):
+            parts = line.split()
+            if len(parts) == 3 and not line.startswith("#") and parts[0] == f"{workload}/{algo}" and parts[2] == src:
+                return int(parts[1])
     except (ValueError, OSError):
         return None
+    return None
 
 
 # ---------------------------------------------------------------------------

@@ -587,13 +587,19 @@ bool map_3d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, 
 // 16 up to 240 for E2M1 / 256 for E4M3; the epilogue masks the part of its
 // last 32-column box past the tile) and D, the K slices per stage.
 // The cost model, from measurements on GB300 (2070 MHz): a problem takes
-// `rounds` waves of tiles over the SMs (pairs: SMs / 2 at a time); a stage
-// costs the larger of its MMA time (an M=128 MMA of 32 bytes of K per row
-// takes N / 2 clocks per SM, pair or not) and its copy time (about 480 clocks
-// per TMA box of up to two slices, the same for any box size; a box of four
-// slices is costed 560), plus a tile's epilogue where it is longer than the
-// tile's MMAs (about 20 clocks per output column with the accumulator
-// double-buffered); the last tile's epilogue is always exposed.
+// `rounds` waves of tiles over the SMs (pairs: SMs / 2 at a time). A K slice
+// costs the largest of
+//   - its MMA time: an M=128 MMA of 32 bytes of K per row takes N / 2 clocks
+//     per SM, pair or not (4 MMAs per slice);
+//   - the shared-memory traffic it puts on one SM, at about 125 bytes per
+//     clock: the copies written (128 A rows and the B rows this SM loads)
+//     plus the operand reads of the MMAs (128 A rows, and BN B rows: a pair's
+//     B half is read by both SMs' tensor cores);
+//   - its share of the copy engine: about 480 clocks per TMA box of up to two
+//     slices, whatever its size (560 for four), two boxes per stage;
+// plus about 1000 clocks per tile. The epilogue (about 20 clocks per output
+// column of the CTA's 128 rows) overlaps the next tile's MMAs and shows only
+// where it is the longer of the two, and once for the last tile.
 // BT_TC_CONFIG="bn,d" (single) or "pair,bn,d" overrides the choice.
 struct TileCfg {
     bool pair;
@@ -607,11 +613,14 @@ double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int
     const int64_t units = pair ? sms / 2 : sms;
     const int64_t tiles = num_m * num_n;
     const int64_t rounds = (tiles + units - 1) / units;
-    const int nk = (slices + d - 1) / d;
-    const double mma = static_cast<double>(d) * (kRowB / 32) * (bn / 2.0);
-    const double copy = 2.0 * (d <= 2 ? 480.0 : 560.0);
-    const double stage = mma > copy ? mma : copy;
-    double tile = nk * stage;
+    const double mma = (kRowB / 32) * (bn / 2.0);
+    const double written = static_cast<double>(kBM + b_slot_rows(bn, pair)) * kRowB;
+    const double read = static_cast<double>(kBM + bn) * kRowB;
+    const double smem = (written + read) / 125.0;
+    const double copy = 2.0 * (d <= 2 ? 480.0 : 560.0) / d;
+    double slice = mma > smem ? mma : smem;
+    if (copy > slice) slice = copy;
+    double tile = slices * slice + 1000.0;
     const double epi = 20.0 * bn;
     if (epi > tile) tile = epi;
     return static_cast<double>(rounds) * tile + epi + 600.0;
