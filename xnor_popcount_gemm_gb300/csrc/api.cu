@@ -12,6 +12,18 @@ namespace bt {
 
 __device__ unsigned int g_error_word;
 
+int device_sm_count() {
+    static int n[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (n[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
 unsigned int *device_error_word() {
     static std::mutex mu;
     static unsigned int *ptrs[128] = {};

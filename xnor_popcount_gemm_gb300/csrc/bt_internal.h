@@ -32,6 +32,9 @@ inline int64_t row_bytes(int64_t k, bt_code code) {
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Streaming multiprocessors of the current device (looked up once per device).
+int device_sm_count();
+
 // Device error word of the current device (a static __device__ variable,
 // address looked up once per device). Returns nullptr on a CUDA error.
 unsigned int *device_error_word();

@@ -681,9 +681,7 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
     const int64_t total = R * G;
     const bool colbias = bias_len > 1;
     if (vec8 && total <= (int64_t(1) << 31) - (int64_t(1) << 21) && (!colbias || aligned(bias, 16))) {
-        int sms = 0, dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int sms = device_sm_count();
         const int64_t per_block = kPackThreads * kFlatUnroll;
         const int64_t need = (total + per_block - 1) / per_block;
         const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * (2048 / kPackThreads);
@@ -715,9 +713,7 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
         if (attr != cudaSuccess) return attr;
         const int seg = kSegBytes / static_cast<int>(sizeof(T));
         const int64_t upr = (K + seg - 1) / seg;
-        int sms = 0, dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int sms = device_sm_count();
         const int64_t units = R * upr;
         const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * 3;
         const int grid = static_cast<int>(units < cap ? units : cap);
@@ -752,9 +748,7 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
     const int64_t upi = (HW + kNhwcPixels - 1) / kNhwcPixels;
     const int64_t G = padded_elems<CODE>(rb) / 8;
     if (smem <= kNhwcMaxSmem && B * upi < (int64_t(1) << 31) && G * kNhwcGroups < (int64_t(1) << 31)) {
-        int sms = 0, dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int sms = device_sm_count();
         const int64_t units = B * upi;
         const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * (2048 / kPackThreads);
         cudaLaunchConfig_t cfg = {};
@@ -830,9 +824,7 @@ cudaError_t launch_im2col_rows(const uint8_t *xp, const ConvGeom &g, int64_t rbc
     if (M == 0) return cudaSuccess;
     const int cpp = static_cast<int>(rbc / 16);
     const int64_t total = M * cpp;
-    int sms = 0, dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = device_sm_count();
     const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;
     const int64_t blocks = (total + kPackThreads - 1) / kPackThreads;
     cudaLaunchConfig_t cfg = {};

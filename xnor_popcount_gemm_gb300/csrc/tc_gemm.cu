@@ -541,17 +541,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
     return fn;
 }
 
-int sm_count() {
-    static int n[128] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
-    if (n[dev] == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-        n[dev] = v;
-    }
-    return n[dev];
-}
+int sm_count() { return device_sm_count(); }
 
 // Views of a byte matrix [rows, row_bytes] (row pitch = row_bytes), 128-byte
 // swizzle, zero fill outside:
@@ -675,9 +665,24 @@ cudaError_t launch_t(const Maps &mp, TcArgs a, cudaStream_t s) {
     // as many units (CTAs, or pairs) as fit at once on the device, at most one per tile
     int units = sm_count() / csize;
     if (PAIR) {
-        cfg.gridDim = dim3(static_cast<unsigned>(units * csize), 1, 1);
+        // how many pairs fit at once: one query per device and shared-memory size
+        static std::mutex mu;
+        static int cached_smem[128] = {}, cached_fit[128] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) dev = 0;
         int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < units) units = fit;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (cached_smem[dev] == smem) {
+                fit = cached_fit[dev];
+            } else {
+                cfg.gridDim = dim3(static_cast<unsigned>(units * csize), 1, 1);
+                if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess) fit = 0;
+                cached_smem[dev] = smem;
+                cached_fit[dev] = fit;
+            }
+        }
+        if (fit > 0 && fit < units) units = fit;
     }
     if (units > a.num_super) units = a.num_super;
     if (units < 1) units = 1;
