@@ -65,13 +65,14 @@ namespace {
 
 constexpr int kBM = 128;                         // rows of A per CTA (= MMA M per CTA)
 constexpr int kRowB = 128;                       // bytes of a K slice
-constexpr int kThreads = 192;                    // producer, MMA, 4 epilogue warps
+constexpr int kEpiWarps = 8;                     // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer, MMA, epilogue warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 480;                 // 32 columns of unit block scales (E2M1)
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;    // UE8M0 127 = 2^0 in every byte
 constexpr int kSmemMax = 232448;                 // 227 KB opt-in per CTA
 constexpr int kBoxBytes = 32 * 128;              // one epilogue staging box: 32 rows x 128 B
-constexpr int kStagingBytes = 4 * kBoxBytes;     // one box per epilogue warp
+constexpr int kStagingBytes = kEpiWarps * kBoxBytes;   // one box per epilogue warp
 constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
 constexpr int kMaxStages = 8;
 
@@ -186,14 +187,22 @@ __device__ __forceinline__ void nchw_box(uint8_t *out, uint32_t sbox, int lane, 
     const uint32_t ob = c / hw, pix = c - ob * hw;
     uint8_t *base = out + (static_cast<int64_t>(ob) * M * hw + pix) * ELEM;
     const uint32_t qb = static_cast<uint32_t>(q * V);
+    // all shared-memory reads first, then all stores (the asm statements keep
+    // their order, so interleaving them would expose each read's latency)
+    constexpr int kIters = 32 / kRowsPer;
+    uint4 v[kIters];
 #pragma unroll
-    for (int i = 0; i < 32 / kRowsPer; ++i) {
+    for (int i = 0; i < kIters; ++i) {
         const int rr = lane / kLpr + i * kRowsPer;
-        const int64_t row = row0 + rr;
-        if (row >= M) break;
-        const uint32_t src = sbox + static_cast<uint32_t>(rr * kBoxRow) + (box_chunk<ELEM>(static_cast<int>(qb >> 4), rr) << 4) +
-                             (qb & 15u);
-        st_global<V>(base + row * hw * ELEM, ld_shared<V>(src));
+        v[i] = ld_shared<V>(sbox + static_cast<uint32_t>(rr * kBoxRow) +
+                            (box_chunk<ELEM>(static_cast<int>(qb >> 4), rr) << 4) + (qb & 15u));
+    }
+    const int64_t plane = static_cast<int64_t>(hw) * ELEM;
+    uint8_t *p = base + (row0 + lane / kLpr) * plane;
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+        if (row0 + lane / kLpr + i * kRowsPer >= M) break;
+        st_global<V>(p + static_cast<int64_t>(i * kRowsPer) * plane, v[i]);
     }
 }
 
@@ -240,7 +249,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(tfull(b), 1);
-            tc::mbar_init(tempty(b), PAIR ? 8u : 4u);   // one arrival per epilogue warp (of both CTAs of a pair)
+            // one arrival per epilogue warp (of both CTAs of a pair)
+            tc::mbar_init(tempty(b), static_cast<uint32_t>(PAIR ? 2 * kEpiWarps : kEpiWarps));
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0u;
@@ -265,7 +275,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
     const uint32_t tmem = *tmem_slot;
     const int quarter = warp & 3;                                   // TMEM lanes this warp may touch
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    if (CODE == BT_CODE_E2M1 && warp >= 2) {
+    if (CODE == BT_CODE_E2M1 && warp >= 2 && warp < 6) {
         // unit block scales for A and B: every byte of the last 32 columns
         tc::tmem_st16_fill(tmem + lane_base + kSfCol, kUnitScales);
         tc::tmem_st16_fill(tmem + lane_base + kSfCol + 16, kUnitScales);
@@ -429,11 +439,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
             const int64_t ncol_end = n0 + ncols;                             // this tile's columns end here
             const int nbox = ncols > 0 ? static_cast<int>((ncols + 31) / 32) : 0;
             const int64_t mrow0 = m0 + quarter * 32;                         // this warp's first row
-            const int total = mrow0 < a.M ? nbox : 0;
+            // the two warps of a lane quarter take alternate 32-column boxes
+            const int half = (warp - 2) / 4;
+            const int total = mrow0 < a.M && nbox > half ? (nbox - half + 1) / 2 : 0;   // this warp's boxes
             const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
-            auto tcol_of = [&](int b) { return tbase + static_cast<uint32_t>(32 * b); };
-            auto emit = [&](const uint32_t (&r)[32], int b) {
-                const int c0 = 32 * b;
+            auto tcol_of = [&](int j) { return tbase + static_cast<uint32_t>(32 * (2 * j + half)); };
+            auto emit = [&](const uint32_t (&r)[32], int j) {
+                const int c0 = 32 * (2 * j + half);
                 // stage the box: row = this lane's TMEM lane, 32 columns, swizzled;
                 // reading it back across rows lets every store instruction cover
                 // whole row segments
@@ -461,16 +473,23 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                     // aligned rows: read the box back as 16-byte chunks, kChunks lanes
                     // per row, 32/kChunks rows per instruction, and store them whole
                     constexpr int kRowsPer = 32 / kChunks;
+                    constexpr int kIters = 32 / kRowsPer;
                     const int q = lane % kChunks;
                     const int64_t col = n0 + c0 + q * (16 / kElem);
+                    // all shared-memory reads first, then all stores
+                    uint4 v[kIters];
 #pragma unroll
-                    for (int rr0 = 0; rr0 < 32; rr0 += kRowsPer) {
-                        const int rr = rr0 + lane / kChunks;
-                        const uint32_t addr = sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(q, rr) << 4);
-                        const uint4 v = ld_shared<16>(addr);
-                        const int64_t row = mrow0 + rr;
-                        if (row < a.M && col < ncol_end)
-                            st_stream_v4(reinterpret_cast<uint8_t *>(out) + (row * a.N + col) * kElem, v);
+                    for (int i = 0; i < kIters; ++i) {
+                        const int rr = i * kRowsPer + lane / kChunks;
+                        v[i] = ld_shared<16>(sbox + static_cast<uint32_t>(rr * kBoxInner) + (box_chunk<kElem>(q, rr) << 4));
+                    }
+                    if (col < ncol_end) {
+                        const int64_t row = mrow0 + lane / kChunks;
+                        uint8_t *p = reinterpret_cast<uint8_t *>(out) + (row * a.N + col) * kElem;
+#pragma unroll
+                        for (int i = 0; i < kIters; ++i)
+                            if (row + i * kRowsPer < a.M)
+                                st_stream_v4(p + static_cast<int64_t>(i * kRowsPer) * a.N * kElem, v[i]);
                     }
                 } else {
                     // ragged N: read the box back one row at a time, lanes along
