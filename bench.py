@@ -253,15 +253,23 @@ def run_ours(args, rank, world):
         outs = [torch.empty((B, N, Ho, Wo), dtype=out_t, device=dev) for _ in range(nbuf)]
         geom = (B, C, H, W, k, wl.stride, wl.padding, wl.dilation)
         ws = torch.empty(bt.bt_binary_conv2d_workspace(*geom, bt.BT_BF16, code), dtype=torch.uint8, device=dev)
-        xp_shape = (B, H, W, bt.bt_packed_row_bytes(C, code))
-        # the contraction's own workspace (im2col rows) when it takes packed pixels
-        ws_packed = bt.bt_binary_conv2d_workspace(*geom, bt.BT_PACKED, code)
-        ws_rows = torch.empty(ws_packed, dtype=torch.uint8, device=dev) if ws_packed else None
+        # the two public calls that split the library's own path for this shape
+        single_pass = bt.bt_conv2d_single_pass(*geom, {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16,
+                                                       torch.float16: bt.BT_F16}[wl.x.dtype], code)
+        if not single_pass:
+            # packed NHWC pixels; the contraction call unfolds them (tensor cores) or
+            # contracts them in place (popcount)
+            xp_shape = (B, H, W, bt.bt_packed_row_bytes(C, code))
+            ws_rows_bytes = bt.bt_binary_conv2d_workspace(*geom, bt.BT_PACKED, code)
+            ws_rows = torch.empty(ws_rows_bytes, dtype=torch.uint8, device=dev) if ws_rows_bytes else None
+        else:
+            # im2col rows of packed codes (one pass from x), contracted with the weights
+            xp_shape = (B * Ho * Wo, k * k * bt.bt_packed_row_bytes(C, code))
     xp = torch.empty(xp_shape, dtype=torch.uint8, device=dev)
 
-    # kernels per step: the pack, then the contraction (a tensor-core convolution
-    # first unfolds the packed pixels into im2col rows: one more kernel)
-    launches_per_step = 3 if (wl.kind == "conv" and code != bt.BT_CODE_BITS) else 2
+    # kernels per step: the pack, then the contraction; a tensor-core convolution
+    # that packs NHWC pixels unfolds them in one more kernel
+    launches_per_step = 3 if (wl.kind == "conv" and code != bt.BT_CODE_BITS and not single_pass) else 2
 
     def step(i, ev=None):
         x, out = xs[i % nbuf], outs[i % nbuf]
@@ -270,18 +278,22 @@ def run_ours(args, rank, world):
             ev[0].record(stream)
         if wl.kind == "linear":
             bt.bt_pack_sign(x, code, bt.BT_LAYOUT_ROWS, bias, out=xp)
-        else:
+        elif not single_pass:
             bt.bt_pack_sign(x, code, bt.BT_LAYOUT_NCHW_TO_NHWC, bias, out=xp)
+        else:
+            bt.bt_pack_im2col(x, code, k, wl.stride, wl.padding, wl.dilation, bias, out=xp)
         if ev is not None:
             ev[1].record(stream)
         if wl.kind == "linear":
             bt.bt_binary_linear(xp, wp, code, K, wl.scale_a, wl.scale_w, out=out, out_dtype=out_t,
                                 algo=algo, x_packed=True)
-        else:
-            C, k = wl.x.shape[1], wl.w.shape[2]
+        elif not single_pass:
             bt.bt_binary_conv2d(xp, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
                                 wl.scale_w, out=out, out_dtype=out_t, algo=algo, x_packed=True,
                                 workspace=ws_rows)
+        else:
+            bt.bt_binary_conv2d(xp, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
+                                wl.scale_w, out=out, out_dtype=out_t, algo=algo, x_im2col_hw=(B, H, W))
         if ev is not None:
             ev[2].record(stream)
 
@@ -369,8 +381,7 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "traffic_unit": "DRAM bytes per tc_kernel launch (ncu, this kernel source)",
                      "peak_source": f"{peak_src}: {peak_how}",
-                     "kernel": "contraction" if wl.kind == "linear" or code == bt.BT_CODE_BITS
-                     else "contraction (im2col gather + tc_kernel)"},
+                     "kernel": "contraction"},
         "pack_roofline": {"bound": "hbm", "achieved": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9, 1),
                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
@@ -386,12 +397,20 @@ def run_ours(args, rank, world):
 
 
 def pack_bytes(wl, code, bt):
-    """Algorithmic bytes of the activation pack: read x once, write it packed."""
+    """Algorithmic bytes of the activation pack: read x once, write it packed
+    (a tensor-core convolution's pack writes its im2col rows)."""
     if wl.kind == "linear":
         M, K = wl.x.shape
         return wl.x.numel() * wl.x.element_size() + M * bt.bt_packed_row_bytes(K, code)
     B, C, H, W = wl.x.shape
-    return wl.x.numel() * wl.x.element_size() + B * H * W * bt.bt_packed_row_bytes(C, code)
+    k = wl.w.shape[2]
+    dt = {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16, torch.float16: bt.BT_F16}[wl.x.dtype]
+    if not bt.bt_conv2d_single_pass(B, C, H, W, k, wl.stride, wl.padding, wl.dilation, dt, code):
+        return wl.x.numel() * wl.x.element_size() + B * H * W * bt.bt_packed_row_bytes(C, code)
+    # one pass: x read once, the im2col rows written
+    Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
+    Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
+    return wl.x.numel() * wl.x.element_size() + B * Ho * Wo * k * k * bt.bt_packed_row_bytes(C, code)
 
 
 def kernel_source_hash() -> str:

@@ -55,13 +55,15 @@ typedef enum {
     BT_ERR_TIMEOUT = -6        /* a kernel's bounded wait ran out (device error word) */
 } bt_status;
 
-/* Element types. BT_PACKED is an input already packed in the weight's code. */
+/* Element types. BT_PACKED is an input already packed in the weight's code;
+ * BT_PACKED_IM2COL a convolution input already unfolded by bt_pack_im2col. */
 typedef enum {
     BT_F32 = 0,
     BT_BF16 = 1,
     BT_F16 = 2,
-    BT_I32 = 3,     /* output only: the raw integer dot products */
-    BT_PACKED = 4   /* input only */
+    BT_I32 = 3,            /* output only: the raw integer dot products */
+    BT_PACKED = 4,         /* input only */
+    BT_PACKED_IM2COL = 5   /* input only (bt_binary_conv2d, codes E4M3 / E2M1) */
 } bt_dtype;
 
 /*
@@ -137,6 +139,40 @@ bt_status bt_pack_sign(const void *x, bt_dtype x_dtype, bt_layout layout,
                        const float *bias, int64_t bias_len,
                        bt_code code, void *out, bt_stream stream);
 
+/*
+ * bt_pack_im2col -- fused shift + sign + pack + unfold of a convolution's
+ * input (BinaryConv2dCutlass.set_activation and binarization, then the unfold
+ * of banghao.live/blog/9 section 2, MyConv2d.forward, on packed codes): the
+ * matrix a tensor-core bt_binary_conv2d contracts with the weights.
+ *
+ *   x        device NCHW [B, C, H, W] in x_dtype (BT_F32 / BF16 / F16).
+ *   bias     device fp32 or NULL; bias_len 0, 1 or C (per input channel).
+ *   code     BT_CODE_E4M3 or BT_CODE_E2M1.
+ *   out      device [B*Ho*Wo, k*k*bt_packed_row_bytes(C, code)] bytes, 16-byte
+ *            aligned; Ho, Wo as in bt_binary_conv2d. Row (b, ho, wo) holds, for
+ *            each tap (kh, kw) in turn, the packed input pixel
+ *            (ho*s - p + kh*d, wo*s - p + kw*d) of image b, all zero codes
+ *            where that pixel is in the padding.
+ * Errors: BT_ERR_INVALID_ARG for null pointers, bad sizes, a bad bias_len or
+ * code; BT_ERR_ALIGNMENT when x or out is not 16-byte aligned; BT_ERR_UNSUPPORTED
+ * beyond the sizes bt_binary_conv2d serves. B = 0 does nothing.
+ */
+bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, int64_t H, int64_t W,
+                         int kernel_size, int stride, int padding, int dilation,
+                         const float *bias, int64_t bias_len, bt_code code, void *out, bt_stream stream);
+
+/*
+ * bt_conv2d_single_pass -- 1 when bt_binary_conv2d, given a 16-byte aligned
+ * float x of this geometry and a tensor-core code, builds the im2col rows in
+ * one pass from x (the staged form of bt_pack_im2col); 0 when it packs the
+ * pixels to NHWC and unfolds them in a second kernel (or for BITS, or invalid
+ * arguments). Either way the result is the same; this tells a caller which two
+ * public calls split the same work (bt_pack_im2col + BT_PACKED_IM2COL, or
+ * bt_pack_sign NCHW_TO_NHWC + BT_PACKED).
+ */
+int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride,
+                          int padding, int dilation, bt_dtype x_dtype, bt_code code);
+
 /* Workspace bytes bt_binary_linear needs (0 when x is BT_PACKED). */
 size_t bt_binary_linear_workspace(int64_t M, int64_t K, bt_dtype x_dtype, bt_code code);
 
@@ -169,11 +205,11 @@ bt_status bt_binary_linear(const void *x, bt_dtype x_dtype,
 
 /*
  * Workspace bytes bt_binary_conv2d needs for this geometry: the packed NHWC
- * activations (unless x is BT_PACKED), then, for the tensor-core codes
+ * activations (unless x is packed), then, for the tensor-core codes
  * (E4M3 / E2M1), the im2col rows [B*Ho*Wo, k*k*bt_packed_row_bytes(C, code)]
  * the contraction reads, each part rounded up to 256 bytes. 0 when nothing is
- * needed (BITS with BT_PACKED x), for invalid arguments, and beyond the sizes
- * bt_binary_conv2d serves.
+ * needed (BITS with BT_PACKED x, or BT_PACKED_IM2COL x), for invalid
+ * arguments, and beyond the sizes bt_binary_conv2d serves.
  */
 size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W,
                                   int kernel_size, int stride, int padding, int dilation,
@@ -184,11 +220,13 @@ size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W,
  * is_train=False, kernel_size, stride, padding, dilation) as an im2col
  * contraction over channel-packed NHWC activations: BITS contracts the
  * packed pixels in place (the im2col is implicit, in shared memory); E4M3 /
- * E2M1 first unfold them into im2col rows in the workspace, then run the
- * tensor-core contraction on those rows.
+ * E2M1 contract the weights with the im2col rows of the input (built in the
+ * workspace by one fused pass over x, as bt_pack_im2col does, or unfolded
+ * from packed pixels), or take those rows as BT_PACKED_IM2COL.
  *
  *   x          device NCHW [B, C, H, W] in x_dtype, or BT_PACKED:
- *              [B, H, W, bt_packed_row_bytes(C, w_code)].
+ *              [B, H, W, bt_packed_row_bytes(C, w_code)], or BT_PACKED_IM2COL
+ *              (E4M3 / E2M1 only): the rows bt_pack_im2col writes.
  *   weight     device [O, k, k, bt_packed_row_bytes(C, w_code)]: OIHW weights
  *              packed by bt_pack_sign with layout NCHW_TO_NHWC.
  *   Output size Ho = floor((H + 2p - d(k-1) - 1)/s + 1), same for Wo

@@ -141,6 +141,44 @@ def test_conv_validation():
     assert conv(O=0, x=None) == bt.BT_OK
 
 
+def test_pack_im2col_validation():
+    f = bt._c_pack_im2col
+    s = None
+    def call(**kw):
+        a = dict(x=256, xt=bt.BT_F32, B=1, C=8, H=5, W=5, k=3, st=1, p=1, d=1, bias=None, blen=0,
+                 code=bt.BT_CODE_E2M1, out=512, stream=s)
+        a.update(kw)
+        return f(*a.values())
+    assert call(code=bt.BT_CODE_BITS) == bt.BT_ERR_INVALID_ARG      # codes for the tensor cores only
+    assert call(xt=bt.BT_PACKED) == bt.BT_ERR_INVALID_ARG
+    assert call(C=0) == bt.BT_ERR_INVALID_ARG
+    assert call(k=0) == bt.BT_ERR_INVALID_ARG
+    assert call(H=1, p=0) == bt.BT_ERR_INVALID_ARG                  # window larger than the image
+    assert call(blen=3) == bt.BT_ERR_INVALID_ARG
+    assert call(blen=1) == bt.BT_ERR_INVALID_ARG                    # bias length without a bias
+    assert call(C=2000) == bt.BT_ERR_UNSUPPORTED                    # C*k*k > 16384
+    assert call(x=None) == bt.BT_ERR_INVALID_ARG
+    assert call(x=256 + 8) == bt.BT_ERR_ALIGNMENT
+    assert call(out=512 + 4) == bt.BT_ERR_ALIGNMENT
+    assert call(B=0, x=None, out=None) == bt.BT_OK
+
+
+def test_conv_im2col_input_validation():
+    # pre-unfolded rows: tensor-core codes only, no workspace needed
+    assert conv(xt=bt.BT_PACKED_IM2COL, code=bt.BT_CODE_BITS) == bt.BT_ERR_INVALID_ARG
+    assert bt.bt_binary_conv2d_workspace(2, 64, 8, 8, 3, 1, 1, 1, bt.BT_PACKED_IM2COL, bt.BT_CODE_E2M1) == 0
+
+
+def test_conv2d_single_pass_query():
+    q = bt.bt_conv2d_single_pass
+    geom = (2, 64, 16, 16, 3, 1, 1, 1)
+    assert q(*geom, bt.BT_F32, bt.BT_CODE_BITS) is False            # popcount convs contract NHWC pixels
+    assert q(*geom, bt.BT_PACKED, bt.BT_CODE_E2M1) is False         # already packed
+    assert q(0, 64, 16, 16, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) is False
+    assert q(2, 64, 1, 1, 3, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) is False   # window larger than the image
+    assert q(2, 2000, 16, 16, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) is False  # K beyond the tensor-core limit
+
+
 def test_pack_validation():
     s = None
     assert P(256, bt.BT_F32, 0, 4, 0, 1, 1, None, 0, 0, 512, s) == bt.BT_ERR_INVALID_ARG   # K = 0

@@ -22,6 +22,7 @@ REL_TOL = 1e-6
 OUT_T = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "i32": torch.int32}
 CODES = [bt.BT_CODE_BITS, bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
 CODE_IDS = ["bits", "e4m3", "e2m1"]
+TC_CODES = [bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
 
 
 @pytest.fixture(autouse=True)
@@ -137,6 +138,62 @@ def test_pack_nchw_to_nhwc(code, dtype, shape):
                               None if bias is None else bias.to(DEV)).cpu().numpy()
         want = oracle.pack_nchw_to_nhwc(oracle.binarize(x, bias, channel_axis=1), code)
         np.testing.assert_array_equal(got, want)
+
+
+def _unfold_expected(x, bias, code, k, s, p, d):
+    """The im2col rows of the oracle's packed pixels: row (b, ho, wo), tap
+    (kh, kw) holds pixel (ho*s - p + kh*d, wo*s - p + kw*d), zeros in the padding."""
+    pix = oracle.pack_nchw_to_nhwc(oracle.binarize(x, bias, channel_axis=1), code)   # [B, H, W, rbc]
+    B, H, W, rbc = pix.shape
+    Ho, Wo = bt.conv2d_out_size(H, k, s, p, d), bt.conv2d_out_size(W, k, s, p, d)
+    rows = np.zeros((B, Ho, Wo, k, k, rbc), dtype=np.uint8)
+    for kh in range(k):
+        for kw in range(k):
+            for ho in range(Ho):
+                hi = ho * s - p + kh * d
+                if not 0 <= hi < H:
+                    continue
+                for wo in range(Wo):
+                    wi = wo * s - p + kw * d
+                    if 0 <= wi < W:
+                        rows[:, ho, wo, kh, kw] = pix[:, hi, wi]
+    return rows.reshape(B * Ho * Wo, k * k * rbc)
+
+
+IM2COL_SHAPES = [
+    # B, C, H, W, k, s, p, d, dtype
+    (2, 128, 28, 28, 3, 2, 1, 1, torch.bfloat16), (2, 128, 28, 28, 3, 2, 2, 2, torch.bfloat16),
+    (2, 256, 14, 14, 3, 1, 1, 1, torch.float32), (3, 64, 14, 14, 3, 1, 1, 1, torch.float16),
+    (2, 70, 13, 13, 3, 2, 1, 2, torch.bfloat16), (1, 33, 9, 7, 5, 3, 3, 1, torch.float32),
+    (2, 31, 8, 8, 1, 1, 0, 1, torch.bfloat16), (1, 40, 12, 10, 3, 2, 0, 1, torch.float32),
+    (2, 3, 5, 5, 3, 1, 1, 1, torch.bfloat16),       # planes not 16-byte aligned: direct kernel
+    (1, 700, 10, 10, 3, 1, 1, 1, torch.float32),    # band too wide for shared memory: direct kernel
+    (1, 16, 4, 4, 1, 1, 3, 1, torch.bfloat16),      # taps far into the padding
+]
+
+
+@pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
+@pytest.mark.parametrize("B,C,H,W,k,s,p,d,dtype", IM2COL_SHAPES)
+def test_pack_im2col(code, B, C, H, W, k, s, p, d, dtype):
+    x = _gen(B + C + H + k, (B, C, H, W), dtype)
+    x[0, 0, 0, : min(W, 3)] = torch.tensor([0.0, -0.0, float("nan")])[: min(W, 3)].to(dtype)
+    for bias in (None, torch.tensor([0.05]), torch.linspace(-0.2, 0.2, C)):
+        got = bt.bt_pack_im2col(x.to(DEV), code, k, s, p, d, None if bias is None else bias.to(DEV)).cpu().numpy()
+        np.testing.assert_array_equal(got, _unfold_expected(x, bias, code, k, s, p, d))
+
+
+@pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
+def test_conv_from_im2col_rows(code):
+    B, C, H, W, O, k, s, p, d = 3, 96, 15, 15, 70, 3, 2, 1, 1
+    x = _gen(21, (B, C, H, W), torch.bfloat16)
+    w = _gen(22, (O, C, k, k), torch.bfloat16)
+    rows = bt.bt_pack_im2col(x.to(DEV), code, k, s, p, d)
+    wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    assert bt.bt_binary_conv2d_workspace(B, C, H, W, k, s, p, d, bt.BT_PACKED_IM2COL, code) == 0
+    got = bt.bt_binary_conv2d(rows, wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32,
+                              x_im2col_hw=(B, H, W)).cpu()
+    want = oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d)
+    assert torch.equal(got, torch.from_numpy(want))
 
 
 # ---------------------------------------------------------------------------
@@ -343,7 +400,6 @@ def test_full_conv_workloads(code, name):
 
 TC_CONFIGS = ["240,1", "224,2", "128,4", "64,2", "32,1", "208,2", "96,4",
               "pair,240,2", "pair,224,1", "pair,160,4", "pair,128,2", "pair,64,4", "pair,32,1", "pair,208,2"]
-TC_CODES = [bt.BT_CODE_E4M3, bt.BT_CODE_E2M1]
 
 
 @pytest.mark.parametrize("cfg", TC_CONFIGS)

@@ -17,18 +17,18 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "BtError", "lib_path", "BT_F32", "BT_BF16", "BT_F16", "BT_I32", "BT_PACKED",
+    "BtError", "lib_path", "BT_F32", "BT_BF16", "BT_F16", "BT_I32", "BT_PACKED", "BT_PACKED_IM2COL",
     "BT_CODE_BITS", "BT_CODE_E4M3", "BT_CODE_E2M1", "BT_LAYOUT_ROWS", "BT_LAYOUT_NCHW_TO_NHWC",
     "BT_ALGO_AUTO", "BT_ALGO_POPC", "BT_ALGO_TC_E4M3", "BT_ALGO_TC_E2M1", "BT_OP_LINEAR",
     "BT_OP_CONV2D", "bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
     "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
-    "bt_binary_linear_noalloc_max_bytes",
+    "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
 ]
 
 BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_ALIGNMENT = 0, -1, -2, -3
 BT_ERR_WORKSPACE, BT_ERR_CUDA, BT_ERR_TIMEOUT = -4, -5, -6
-BT_F32, BT_BF16, BT_F16, BT_I32, BT_PACKED = 0, 1, 2, 3, 4
+BT_F32, BT_BF16, BT_F16, BT_I32, BT_PACKED, BT_PACKED_IM2COL = 0, 1, 2, 3, 4, 5
 BT_CODE_BITS, BT_CODE_E4M3, BT_CODE_E2M1 = 0, 1, 2
 BT_LAYOUT_ROWS, BT_LAYOUT_NCHW_TO_NHWC = 0, 1
 BT_ALGO_AUTO, BT_ALGO_POPC, BT_ALGO_TC_E4M3, BT_ALGO_TC_E2M1 = 0, 1, 2, 3
@@ -65,6 +65,8 @@ _c_conv = _sig("bt_binary_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, 
 _c_lin_noalloc = _sig("bt_binary_linear_noalloc", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _i64,
                                                       _p, _i, _i, _p])
 _c_noalloc_max = _sig("bt_binary_linear_noalloc_max_bytes", _sz, [])
+_c_pack_im2col = _sig("bt_pack_im2col", _i, [_p, _i, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _p, _i64, _i, _p, _p])
+_c_single_pass = _sig("bt_conv2d_single_pass", _i, [_i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _i])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
 _c_status = _sig("bt_device_status", _i, [_p])
 
@@ -72,7 +74,7 @@ _c_status = _sig("bt_device_status", _i, [_p])
 EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
             "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
-            "bt_binary_linear_noalloc_max_bytes"]
+            "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass"]
 
 
 class BtError(RuntimeError):
@@ -139,6 +141,31 @@ def bt_pack_sign(x: torch.Tensor, code: int, layout: int = BT_LAYOUT_ROWS, bias=
     return out
 
 
+def bt_pack_im2col(x: torch.Tensor, code: int, kernel_size: int, stride: int, padding: int, dilation: int,
+                   bias=None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Shift + sign + pack + unfold of NCHW x [B, C, H, W]: the im2col rows
+    uint8 [B*Ho*Wo, k*k*row_bytes(C)] a tensor-core conv contracts."""
+    _contig(x, "x")
+    if x.dim() != 4:
+        raise ValueError("bt_pack_im2col wants a 4-D x")
+    B, C, H, W = x.shape
+    Ho = conv2d_out_size(H, kernel_size, stride, padding, dilation)
+    Wo = conv2d_out_size(W, kernel_size, stride, padding, dilation)
+    if out is None:
+        out = torch.empty((B * max(Ho, 0) * max(Wo, 0), kernel_size * kernel_size * bt_packed_row_bytes(C, code)),
+                          dtype=torch.uint8, device=x.device)
+    blen = 0 if bias is None else bias.numel()
+    _check(_c_pack_im2col(_ptr(x), _DT[x.dtype], B, C, H, W, kernel_size, stride, padding, dilation, _ptr(bias),
+                          blen, code, _ptr(out), _stream(stream)))
+    return out
+
+
+def bt_conv2d_single_pass(B: int, C: int, H: int, W: int, kernel_size: int, stride: int, padding: int,
+                          dilation: int, x_dtype: int, code: int) -> bool:
+    """Whether bt_binary_conv2d unfolds x in one pass (as bt_pack_im2col)."""
+    return bool(_c_single_pass(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype, code))
+
+
 def bt_binary_linear_workspace(M: int, K: int, x_dtype: int, code: int) -> int:
     return int(_c_lin_ws(M, K, x_dtype, code))
 
@@ -182,21 +209,27 @@ def bt_binary_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int,
                      stride: int, padding: int, dilation: int, scale_a: float, scale_w: float,
                      bias_a=None, out_dtype=None, algo: int = BT_ALGO_AUTO, x_packed: bool = False,
                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                     stream=None) -> torch.Tensor:
+                     stream=None, x_im2col_hw: tuple | None = None) -> torch.Tensor:
     """NCHW x [B, C, H, W] (or packed NHWC [B, H, W, row_bytes(C)]) with a
-    packed weight [O, k, k, row_bytes(C)] -> NCHW [B, O, Ho, Wo]."""
+    packed weight [O, k, k, row_bytes(C)] -> NCHW [B, O, Ho, Wo]. With
+    x_im2col_hw = (B, H, W), x is the rows bt_pack_im2col wrote for an input
+    of that batch and size."""
     _contig(x, "x")
     _contig(weight, "weight")
-    if x_packed:
+    if x_im2col_hw is not None:
+        B, H, W = x_im2col_hw
+        xt = BT_PACKED_IM2COL
+    elif x_packed:
         B, H, W = x.shape[0], x.shape[1], x.shape[2]
+        xt = BT_PACKED
     else:
         B, C2, H, W = x.shape
         if C2 != C:
             raise ValueError("C does not match x")
+        xt = _DT[x.dtype]
     O = weight.shape[0]
-    xt = BT_PACKED if x_packed else _DT[x.dtype]
     if out_dtype is None:
-        out_dtype = x.dtype if not x_packed else torch.float32
+        out_dtype = x.dtype if xt not in (BT_PACKED, BT_PACKED_IM2COL) else torch.float32
     ot = _DT[out_dtype]
     Ho = conv2d_out_size(H, kernel_size, stride, padding, dilation)
     Wo = conv2d_out_size(W, kernel_size, stride, padding, dilation)

@@ -169,7 +169,7 @@ bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, 
 
 size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride,
                                   int padding, int dilation, bt_dtype x_dtype, bt_code code) {
-    if (B < 0 || C < 1 || H < 1 || W < 1 || !valid_code(code)) return 0;
+    if (B < 0 || C < 1 || H < 1 || W < 1 || !valid_code(code) || x_dtype == BT_PACKED_IM2COL) return 0;
     if (kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return 0;
     if (B > (int64_t(1) << 30) || C > kMaxK || H > (1 << 20) || W > (1 << 20) || kernel_size > 64 ||
         padding > (1 << 20) || stride > (1 << 20) || dilation > (1 << 10))
@@ -195,12 +195,13 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
                            const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
                            bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
     if (!valid_code(w_code) || !valid_out(out_dtype)) return BT_ERR_INVALID_ARG;
-    if (!(float_in(x_dtype) || x_dtype == BT_PACKED)) return BT_ERR_INVALID_ARG;
+    if (!(float_in(x_dtype) || x_dtype == BT_PACKED || x_dtype == BT_PACKED_IM2COL)) return BT_ERR_INVALID_ARG;
+    if (x_dtype == BT_PACKED_IM2COL && w_code == BT_CODE_BITS) return BT_ERR_INVALID_ARG;
     if (B < 0 || C < 1 || H < 1 || W < 1 || O < 0) return BT_ERR_INVALID_ARG;
     if (kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return BT_ERR_INVALID_ARG;
     if (!valid_scale(scale_a) || !valid_scale(scale_w)) return BT_ERR_INVALID_ARG;
     if (!(bias_len == 0 || bias_len == 1 || bias_len == C)) return BT_ERR_INVALID_ARG;
-    if (bias_len > 0 && bias_a == nullptr && x_dtype != BT_PACKED) return BT_ERR_INVALID_ARG;
+    if (bias_len > 0 && bias_a == nullptr && float_in(x_dtype)) return BT_ERR_INVALID_ARG;
     if (algo != BT_ALGO_AUTO && algo != algo_for_code(w_code)) {
         if (algo < BT_ALGO_AUTO || algo > BT_ALGO_TC_E2M1) return BT_ERR_INVALID_ARG;
         return BT_ERR_UNSUPPORTED;
@@ -224,29 +225,78 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype,
                                                    w_code);
-    const bool needs_ws = x_dtype != BT_PACKED || run != BT_ALGO_POPC;
+    const bool needs_ws = float_in(x_dtype) || (x_dtype == BT_PACKED && run != BT_ALGO_POPC);
     if (needs_ws && need == 0) return BT_ERR_UNSUPPORTED;      // beyond the sizes the query serves
     if (needs_ws && (workspace == nullptr || workspace_bytes < need)) return BT_ERR_WORKSPACE;
     if (needs_ws && !aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int64_t rbc = row_bytes(C, w_code);
+    const float alpha = alpha_of(scale_a, scale_w);
+    unsigned int *err = device_error_word();
+    if (err == nullptr) return BT_ERR_CUDA;
+    if (x_dtype == BT_PACKED_IM2COL)
+        return from_cuda(launch_tc_conv(static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(weight), w_code,
+                                        g, alpha, out, out_dtype, err, s));
+    uint8_t *rows = ws + (x_dtype == BT_PACKED ? 0 : round_up(static_cast<size_t>(B * H * W * rbc), 256));
+    if (run != BT_ALGO_POPC && x_dtype != BT_PACKED) {
+        // one pass from x to the im2col rows, where the staged unfold applies
+        const cudaError_t e = launch_pack_im2col(x, x_dtype, g, bias_a, bias_len, w_code, rows, false, s);
+        if (e == cudaSuccess)
+            return from_cuda(launch_tc_conv(rows, static_cast<const uint8_t *>(weight), w_code, g, alpha, out,
+                                            out_dtype, err, s));
+        if (e != cudaErrorNotSupported) return BT_ERR_CUDA;
+    }
     const void *xp = x;
     if (x_dtype != BT_PACKED) {
         cudaError_t e = launch_pack_nhwc(x, x_dtype, B, C, H * W, bias_a, bias_len, w_code, ws, s);
         if (e != cudaSuccess) return BT_ERR_CUDA;
         xp = ws;
-        ws += round_up(static_cast<size_t>(B * H * W * rbc), 256);
     }
-    const float alpha = alpha_of(scale_a, scale_w);
     if (run == BT_ALGO_POPC)
         return from_cuda(launch_popc_conv(static_cast<const uint32_t *>(xp), static_cast<const uint32_t *>(weight),
                                           g, alpha, out, out_dtype, s));
-    unsigned int *err = device_error_word();
-    if (err == nullptr) return BT_ERR_CUDA;
-    cudaError_t e = launch_im2col_rows(static_cast<const uint8_t *>(xp), g, rbc, ws, s);
+    cudaError_t e = launch_im2col_rows(static_cast<const uint8_t *>(xp), g, rbc, rows, s);
     if (e != cudaSuccess) return BT_ERR_CUDA;
-    return from_cuda(launch_tc_conv(ws, static_cast<const uint8_t *>(weight), w_code, g, alpha, out, out_dtype, err,
+    return from_cuda(launch_tc_conv(rows, static_cast<const uint8_t *>(weight), w_code, g, alpha, out, out_dtype, err,
                                     s));
+}
+
+int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride, int padding,
+                          int dilation, bt_dtype x_dtype, bt_code code) {
+    if (!float_in(x_dtype) || (code != BT_CODE_E4M3 && code != BT_CODE_E2M1)) return 0;
+    if (B < 1 || C < 1 || H < 1 || W < 1 || kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return 0;
+    if (H > (1 << 20) || W > (1 << 20) || kernel_size > 64 || padding > (1 << 20) || stride > (1 << 20) ||
+        dilation > (1 << 10) || C * kernel_size * kernel_size > kTcMaxK)
+        return 0;
+    ConvGeom g{B, C, H, W, 0, 0, 0, kernel_size, stride, padding, dilation};
+    g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
+    g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
+    if (g.Ho < 1 || g.Wo < 1) return 0;
+    return unfold_single_pass(g, x_dtype, code) ? 1 : 0;
+}
+
+bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, int64_t H, int64_t W,
+                         int kernel_size, int stride, int padding, int dilation, const float *bias,
+                         int64_t bias_len, bt_code code, void *out, bt_stream stream) {
+    if (!float_in(x_dtype) || (code != BT_CODE_E4M3 && code != BT_CODE_E2M1)) return BT_ERR_INVALID_ARG;
+    if (B < 0 || C < 1 || H < 1 || W < 1) return BT_ERR_INVALID_ARG;
+    if (kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return BT_ERR_INVALID_ARG;
+    if (!(bias_len == 0 || bias_len == 1 || bias_len == C)) return BT_ERR_INVALID_ARG;
+    if (bias_len > 0 && bias == nullptr) return BT_ERR_INVALID_ARG;
+    ConvGeom g{B, C, H, W, 0, 0, 0, kernel_size, stride, padding, dilation};
+    g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
+    g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
+    if (g.Ho < 1 || g.Wo < 1) return BT_ERR_INVALID_ARG;
+    const int64_t kk = static_cast<int64_t>(kernel_size) * kernel_size;
+    if (C * kk > kTcMaxK || H > (1 << 20) || W > (1 << 20) || kernel_size > 64 || padding > (1 << 20) ||
+        stride > (1 << 20) || dilation > (1 << 10))
+        return BT_ERR_UNSUPPORTED;
+    if (B == 0) return BT_OK;
+    if ((B * g.Ho * g.Wo + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
+    if (x == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4))) return BT_ERR_ALIGNMENT;
+    return from_cuda(launch_pack_im2col(x, x_dtype, g, bias, bias_len, code, static_cast<uint8_t *>(out), true,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo) {

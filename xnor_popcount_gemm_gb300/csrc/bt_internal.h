@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "bt.h"
 
@@ -75,6 +76,21 @@ cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code,
 
 // True when this build carries the tensor-core kernels.
 bool tc_available();
+
+// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// Fused shift + sign + pack + unfold for the tensor-core convolution: NCHW x
+// straight to the im2col rows launch_im2col_rows would build from the packed
+// pixels (codes E4M3 / E2M1). The staged kernel needs x's channel planes
+// 16-byte aligned and a band of input rows that fits shared memory; otherwise
+// a direct kernel runs when direct_ok, else cudaErrorNotSupported is returned
+// (the caller packs to NHWC and unfolds in two kernels).
+cudaError_t launch_pack_im2col(const void *x, bt_dtype xt, const ConvGeom &g, const float *bias, int64_t bias_len,
+                               bt_code code, uint8_t *rows, bool direct_ok, cudaStream_t s);
+// Whether the convolution builds its im2col rows in one pass from x (for a
+// 16-byte aligned x of type xt): the staged plan exists and pays.
+bool unfold_single_pass(const ConvGeom &g, bt_dtype xt, bt_code code);
 
 // Launch attribute list allowing programmatic dependent launch (the kernel
 // overlaps its prologue with the previous kernel in the stream).

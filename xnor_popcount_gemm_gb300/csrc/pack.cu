@@ -662,6 +662,233 @@ im2col_rows_kernel(const uint4 *__restrict__ xp, int H, int W, int Ho, int Wo, i
     }
 }
 
+// ---------------------------------------------------------------------------
+// Fused shift + sign + pack + unfold for the tensor-core convolution: NCHW x
+// straight to its im2col rows of packed codes. A unit is (image b, a band of
+// hb output rows). TMA boxes bring the band's input rows into shared memory
+// -- all channels; of each channel plane the band's pixels as one run from a
+// 16-byte aligned pixel xa, in boxes of bw pixels x cbox channels; sign bits
+// per (8-pixel group, channel) and the 8 x 8 bit transpose turn them into
+// packed pixel codes in shared memory; then each output pixel's k*k taps
+// leave as 16-byte stores of its im2col row, consecutive threads on
+// consecutive chunks (zeros for a tap in the padding). The next unit's boxes
+// are requested as soon as the band has been read.
+// ---------------------------------------------------------------------------
+constexpr int kUnfoldThreads = 256;
+
+struct UnfoldArgs {
+    int C, H, W, Ho, Wo, k, s, p, d;
+    int hb, nbands;            // output rows per band, bands per image
+    uint32_t units;            // B * nbands
+    int bw, nxb;               // pixels per box (multiple of 32), boxes along the run
+    int cbox, ncb;             // channels per box, boxes along the channels
+    int span;                  // pixels staged per unit (nxb * bw)
+    int cstride;               // bytes of a pixel group's row of sign bits
+    int rbc, krow;             // bytes per packed pixel, per im2col row
+    uint32_t box_bytes;        // bytes of one box
+    uint32_t band_bytes;       // bytes of all boxes of a unit
+    FastDiv div_nq;            // span / 32 pixel quads (32 pixels)
+    FastDiv div_qpb;           // quads per box (bw / 32)
+    FastDiv div_cbox;          // channels per box
+    FastDiv div_g;             // 8-channel groups per packed pixel
+    FastDiv div_rowc;          // 16-byte chunks per im2col row
+    FastDiv div_cpp;           // 16-byte chunks per packed pixel
+    FastDiv div_k, div_wo;
+};
+
+// Input rows [r_lo, r_hi] a band of output rows [ho0, ho1) reads, clipped to
+// the image, and the aligned first pixel xa of its run.
+__host__ __device__ __forceinline__ void unfold_band(const UnfoldArgs &u, int ho0, int ho1, int &r_lo, int &r_hi, int &xa) {
+    r_lo = ho0 * u.s - u.p;
+    r_hi = (ho1 - 1) * u.s - u.p + (u.k - 1) * u.d;
+    if (r_lo < 0) r_lo = 0;
+    if (r_lo > u.H - 1) r_lo = u.H - 1;
+    if (r_hi > u.H - 1) r_hi = u.H - 1;
+    xa = (r_lo * u.W) & ~7;
+}
+
+template <typename T, int CODE>
+__global__ void __launch_bounds__(kUnfoldThreads)
+pack_im2col_kernel(const __grid_constant__ CUtensorMap tmx, const UnfoldArgs u, const float *__restrict__ bias,
+                   int bias_len, uint8_t *__restrict__ rows, unsigned int *err) {
+    constexpr int OB = GroupOut<CODE>::kBytes;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *band = smem;
+    uint8_t *sbits = smem + u.band_bytes;
+    uint8_t *spix = sbits + (u.span / 8) * u.cstride;
+    const uint32_t bar = smem_u32(spix + u.span * u.rbc);
+    volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(spix + u.span * u.rbc + 8);
+    const int tid = threadIdx.x;
+    const int npg = u.span / 8;
+    const int G = static_cast<int>(u.div_g.d);
+    const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
+
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        *flag = 0u;
+        tc::fence_mbar_init();
+    }
+    pdl_launch_dependents();
+    __syncthreads();
+    pdl_wait();                                          // x may come from, and rows go to, the previous kernel
+
+    auto request = [&](uint32_t unit) {                  // thread 0: this unit's boxes
+        const int b = static_cast<int>(unit / static_cast<uint32_t>(u.nbands));
+        const int bnd = static_cast<int>(unit - static_cast<uint32_t>(b) * u.nbands);
+        const int ho0 = bnd * u.hb, ho1 = ho0 + u.hb < u.Ho ? ho0 + u.hb : u.Ho;
+        int r_lo, r_hi, xa;
+        unfold_band(u, ho0, ho1, r_lo, r_hi, xa);
+        tc::mbar_arrive_expect_tx(bar, u.band_bytes);
+        for (int cb = 0; cb < u.ncb; ++cb)
+            for (int xb = 0; xb < u.nxb; ++xb)
+                tc::tma_load_2d(smem_u32(band) + static_cast<uint32_t>(cb * u.nxb + xb) * u.box_bytes, &tmx,
+                                xa + xb * u.bw, b * u.C + cb * u.cbox, bar);
+    };
+    if (tid == 0 && blockIdx.x < u.units) request(blockIdx.x);
+
+    uint32_t it = 0;
+    for (uint32_t unit = blockIdx.x; unit < u.units; unit += gridDim.x, ++it) {
+        const int b = static_cast<int>(unit / static_cast<uint32_t>(u.nbands));
+        const int bnd = static_cast<int>(unit - static_cast<uint32_t>(b) * u.nbands);
+        const int ho0 = bnd * u.hb, ho1 = ho0 + u.hb < u.Ho ? ho0 + u.hb : u.Ho;
+        int r_lo, r_hi, xa;
+        unfold_band(u, ho0, ho1, r_lo, r_hi, xa);
+        if (tid == 0) (void)tc::wait_bounded(bar, it & 1u, flag, err);
+        __syncthreads();
+        if (*flag) break;
+        (void)tc::mbar_try_wait(bar, it & 1u);           // completed phase: acquire for this thread
+
+        // phase 1: sign bits, item (channel c, 32 pixels q4): four 8-pixel groups
+        const int nq = u.span / 32;
+        for (int i = tid; i < u.C * nq; i += kUnfoldThreads) {
+            const int c = static_cast<int>(fdiv(static_cast<uint32_t>(i), u.div_nq));
+            const int q4 = i - c * nq;
+            const int cb = u.ncb == 1 ? 0 : static_cast<int>(fdiv(static_cast<uint32_t>(c), u.div_cbox));
+            const int cl = c - cb * u.cbox;
+            const int xb = u.nxb == 1 ? 0 : static_cast<int>(fdiv(static_cast<uint32_t>(q4), u.div_qpb));
+            const int xl = 32 * q4 - xb * u.bw;
+            const T *src = reinterpret_cast<const T *>(band + static_cast<uint32_t>(cb * u.nxb + xb) * u.box_bytes) +
+                           cl * u.bw + xl;
+            const float bc = bias_len > 1 ? __ldg(bias + c) : bs;
+            const bool finite = isfinite(bc);
+            uint8_t *dst = sbits + (4 * q4) * u.cstride + c;
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) {
+                Group<T> grp;
+                grp.load_smem(src + 8 * g4);
+                uint32_t P0, P1;
+                if (finite) {
+                    masks_ge<T>(grp, -bc, P0, P1);
+                } else {
+                    float f[8], bb[8];
+                    grp.unpack(f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) bb[e] = bc;
+                    masks_add(f, bb, P0, P1);
+                }
+                dst[g4 * u.cstride] = static_cast<uint8_t>(mask_byte(P0, P1));
+            }
+        }
+        __syncthreads();
+        // the band has been read: request the next unit's boxes
+        if (tid == 0 && unit + gridDim.x < u.units) {
+            tc::fence_proxy_async_smem();
+            request(unit + gridDim.x);
+        }
+
+        // phase 2: packed pixel codes, item (pixel group pg, channel group cg)
+        for (int i = tid; i < npg * G; i += kUnfoldThreads) {
+            const int pg = static_cast<int>(fdiv(static_cast<uint32_t>(i), u.div_g));
+            const int cg = i - pg * G;
+            const int c0 = cg * 8;
+            uint8_t *dst = spix + (8 * pg) * u.rbc + cg * OB;
+            if (c0 >= u.C) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) store_group<CODE>(dst + j * u.rbc, 0u, 0u);
+                continue;
+            }
+            const uint32_t cvalid = u.C - c0 >= 8 ? 0xFFu : (1u << (u.C - c0)) - 1u;
+            const uint64_t v = transpose8x8(*reinterpret_cast<const uint64_t *>(sbits + pg * u.cstride + c0));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t pos = static_cast<uint32_t>(v >> (8 * j)) & 0xFFu;
+                store_group<CODE>(dst + j * u.rbc, ~pos & cvalid, cvalid);
+            }
+        }
+        __syncthreads();
+
+        // phase 3: im2col rows, item (output pixel, 16-byte chunk of its row)
+        const int rowc = static_cast<int>(u.div_rowc.d), cpp = static_cast<int>(u.div_cpp.d);
+        const int nopix = (ho1 - ho0) * u.Wo;
+        for (int i = tid; i < nopix * rowc; i += kUnfoldThreads) {
+            const int opix = static_cast<int>(fdiv(static_cast<uint32_t>(i), u.div_rowc));
+            const int rc = i - opix * rowc;
+            const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(rc), u.div_cpp));
+            const int chunk = rc - tap * cpp;
+            const int kh = static_cast<int>(fdiv(static_cast<uint32_t>(tap), u.div_k));
+            const int kw = tap - kh * u.k;
+            const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(opix), u.div_wo));
+            const int wo = opix - oh * u.Wo;
+            const int ho = ho0 + oh;
+            const int hi = ho * u.s - u.p + kh * u.d, wi = wo * u.s - u.p + kw * u.d;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (hi >= 0 && hi < u.H && wi >= 0 && wi < u.W) {
+                const int q = hi * u.W + wi - xa;
+                v = *reinterpret_cast<const uint4 *>(spix + q * u.rbc + chunk * 16);
+            }
+            *reinterpret_cast<uint4 *>(rows + ((static_cast<int64_t>(b) * u.Ho + ho) * u.Wo + wo) * u.krow +
+                                       rc * 16) = v;
+        }
+        __syncthreads();
+    }
+    if (tid == 0 && *flag) {
+        // aborted: let a copy still in flight land before the CTA exits
+        const unsigned long long t0 = globaltimer_ns();
+        while (!tc::mbar_try_wait(bar, it & 1u) && globaltimer_ns() - t0 < kWaitNs) {}
+    }
+}
+
+// The same result for any x layout (planes not 16-byte aligned): one thread
+// per (output pixel m, tap, 8-channel group) reads its 8 channels straight
+// from x and writes the group's code bytes; consecutive threads write
+// consecutive groups of a row.
+template <typename T, int CODE>
+__global__ void __launch_bounds__(kPackThreads)
+pack_im2col_direct_kernel(const T *__restrict__ x, int C, int H, int W, int Ho, int Wo, int k, int s, int p, int d,
+                          FastDiv div_g, FastDiv div_kk, int krow, int64_t total, const float *__restrict__ bias,
+                          int bias_len, uint8_t *__restrict__ rows) {
+    constexpr int OB = GroupOut<CODE>::kBytes;
+    pdl_launch_dependents();
+    pdl_wait();
+    const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
+    const int G = static_cast<int>(div_g.d), kk = static_cast<int>(div_kk.d);
+    const int64_t HW = static_cast<int64_t>(H) * W;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kPackThreads + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * kPackThreads) {
+        const int64_t mt = t / G;                          // (m, tap)
+        const int cg = static_cast<int>(t - mt * G);
+        const int64_t m = mt / kk;
+        const int tap = static_cast<int>(mt - m * kk);
+        const int wo = static_cast<int>(m % Wo);
+        const int64_t r = m / Wo;
+        const int ho = static_cast<int>(r % Ho);
+        const int64_t b = r / Ho;
+        const int kh = tap / k, kw = tap - kh * k;
+        const int hi = ho * s - p + kh * d, wi = wo * s - p + kw * d;
+        const int c0 = cg * 8;
+        uint32_t neg = 0, valid = 0;
+        if (hi >= 0 && hi < H && wi >= 0 && wi < W) {
+            const T *src = x + (b * C + c0) * HW + static_cast<int64_t>(hi) * W + wi;
+            for (int e = 0; e < 8 && c0 + e < C; ++e) {
+                const float bc = bias_len > 1 ? __ldg(bias + c0 + e) : bs;
+                neg |= is_negative(Elem<T>::to_f32(src[e * HW]), bc) << e;
+                valid |= 1u << e;
+            }
+        }
+        store_group<CODE>(rows + m * krow + tap * (G * OB) + cg * OB, neg, valid);
+    }
+}
+
 int grid_for(int64_t threads) {
     int64_t blocks = (threads + kPackThreads - 1) / kPackThreads;
     const int64_t cap = int64_t(1) << 30;
@@ -817,6 +1044,185 @@ cudaError_t launch_pack_rows(const void *x, bt_dtype xt, int64_t R, int64_t K, c
         case BT_BF16: return rows_code(static_cast<const __nv_bfloat16 *>(x), R, K, bias, bias_len, code, out, s);
         default: return rows_code(static_cast<const __half *>(x), R, K, bias, bias_len, code, out, s);
     }
+}
+
+namespace {
+
+constexpr int kUnfoldMaxSmem = 113 * 1024;              // two units' worth of CTAs per SM
+
+template <typename T> CUtensorMapDataType map_type();
+template <> CUtensorMapDataType map_type<float>() { return CU_TENSOR_MAP_DATA_TYPE_FLOAT32; }
+template <> CUtensorMapDataType map_type<__nv_bfloat16>() { return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; }
+template <> CUtensorMapDataType map_type<__half>() { return CU_TENSOR_MAP_DATA_TYPE_FLOAT16; }
+
+int unfold_smem(const UnfoldArgs &u) {
+    return static_cast<int>(u.band_bytes) + (u.span / 8) * u.cstride + u.span * u.rbc + 16;
+}
+
+// Plan the staged unfold of a problem: the band height and boxes (see
+// UnfoldArgs). False when x's planes are not 16-byte aligned or no band fits.
+// `efficient` tells whether the plan runs at least three CTAs per SM and
+// stages at most 1.3x the input (measured on GB300: then one pass beats
+// packing pixels and unfolding them in a second kernel).
+bool plan_unfold(const ConvGeom &g, int elem, bt_code code, UnfoldArgs &out, bool &efficient) {
+    const int64_t HW = g.H * g.W;
+    if ((HW * elem) % 16 != 0 || g.C > 16384 || g.B * g.C > (int64_t(1) << 31)) return false;
+    UnfoldArgs u{};
+    u.C = static_cast<int>(g.C); u.H = static_cast<int>(g.H); u.W = static_cast<int>(g.W);
+    u.Ho = static_cast<int>(g.Ho); u.Wo = static_cast<int>(g.Wo);
+    u.k = g.k; u.s = g.s; u.p = g.p; u.d = g.d;
+    u.rbc = static_cast<int>(row_bytes(g.C, code));
+    u.krow = g.k * g.k * u.rbc;
+    u.ncb = static_cast<int>((g.C + 255) / 256);
+    u.cbox = static_cast<int>((g.C + u.ncb - 1) / u.ncb);
+    u.cstride = static_cast<int>((g.C + 7) / 8 * 8 + 8);
+    const int sms = device_sm_count();
+    // the tallest band that leaves two units per SM within a staging budget,
+    // trying budgets of four, three and two CTAs per SM in turn (else the
+    // shortest band that fits the largest budget)
+    bool found = false;
+    UnfoldArgs best{};
+    int64_t best_rows_in = 0;
+    const int budgets[3] = {54 * 1024, 74 * 1024, kUnfoldMaxSmem};
+    for (int bi = 0; bi < 3 && !found; ++bi) {
+        for (int hb = u.Ho; hb >= 1; --hb) {
+            int64_t rows_in = static_cast<int64_t>(hb - 1) * g.s + static_cast<int64_t>(g.k - 1) * g.d + 1;
+            if (rows_in > g.H) rows_in = g.H;
+            const int64_t need = rows_in * g.W + 7;
+            const int64_t nxb = (need + 255) / 256;
+            const int64_t bw = ((need + nxb - 1) / nxb + 31) / 32 * 32;
+            if (bw > 256 || nxb > 16) continue;
+            UnfoldArgs c = u;
+            c.hb = hb;
+            c.nbands = (u.Ho + hb - 1) / hb;
+            c.nxb = static_cast<int>(nxb);
+            c.bw = static_cast<int>(bw);
+            c.span = static_cast<int>(nxb * bw);
+            c.box_bytes = static_cast<uint32_t>(c.cbox * c.bw * elem);
+            c.band_bytes = c.box_bytes * static_cast<uint32_t>(c.ncb * c.nxb);
+            if (unfold_smem(c) > budgets[bi]) continue;
+            const int64_t units = g.B * c.nbands;
+            if (units >= 2LL * sms) { best = c; best_rows_in = rows_in; found = true; break; }
+            if (bi == 2) { best = c; best_rows_in = rows_in; found = true; }   // keep shrinking: more units
+        }
+    }
+    if (!found || g.B * best.nbands > (int64_t(1) << 31) - 1) return false;
+    const int per_sm = (227 * 1024) / (unfold_smem(best) + 1024);
+    const double overread = static_cast<double>(best.nbands) * static_cast<double>(best_rows_in) / static_cast<double>(g.H);
+    efficient = per_sm >= 3 && overread <= 1.3;
+    out = best;
+    return true;
+}
+
+template <typename T, int CODE>
+cudaError_t im2col_t(const T *x, const ConvGeom &g, const float *bias, int64_t bias_len, uint8_t *rows,
+                     bool efficient_only, cudaStream_t s) {
+    constexpr int elem = static_cast<int>(sizeof(T));
+    const int64_t HW = g.H * g.W;
+    auto enc = tensor_map_encoder();
+    UnfoldArgs u{};
+    bool efficient = false;
+    if (enc == nullptr || !aligned(x, 16) || !plan_unfold(g, elem, static_cast<bt_code>(CODE), u, efficient) ||
+        (efficient_only && !efficient))
+        return cudaErrorNotSupported;
+    const int sms = device_sm_count();
+    u.units = static_cast<uint32_t>(g.B * u.nbands);
+    u.div_nq = make_fastdiv(static_cast<uint32_t>(u.span / 32));
+    u.div_qpb = make_fastdiv(static_cast<uint32_t>(u.bw / 32));
+    u.div_cbox = make_fastdiv(static_cast<uint32_t>(u.cbox));
+    u.div_g = make_fastdiv(static_cast<uint32_t>(u.rbc / GroupOut<CODE>::kBytes));
+    u.div_rowc = make_fastdiv(static_cast<uint32_t>(u.krow / 16));
+    u.div_cpp = make_fastdiv(static_cast<uint32_t>(u.rbc / 16));
+    u.div_k = make_fastdiv(static_cast<uint32_t>(g.k));
+    u.div_wo = make_fastdiv(static_cast<uint32_t>(g.Wo));
+
+    // x as a 2-D tensor [B*C planes, H*W pixels]; boxes of bw pixels x cbox channels, zero fill outside
+    CUtensorMap m;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(HW), static_cast<cuuint64_t>(g.B * g.C)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(HW * elem)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(u.bw), static_cast<cuuint32_t>(u.cbox)};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&m, map_type<T>(), 2, const_cast<T *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return cudaErrorNotSupported;
+
+    unsigned int *err = device_error_word();
+    if (err == nullptr) return cudaErrorUnknown;
+    auto kern = pack_im2col_kernel<T, CODE>;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kUnfoldMaxSmem); });
+    if (attr != cudaSuccess) return attr;
+    const int smem = unfold_smem(u);
+    int per_sm = (227 * 1024) / (smem + 1024);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute pdl = pdl_attribute();
+    cfg.gridDim = dim3(static_cast<unsigned>(u.units < cap ? u.units : cap));
+    cfg.blockDim = dim3(kUnfoldThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, m, u, bias, static_cast<int>(bias_len), rows, err);
+}
+
+template <typename T, int CODE>
+cudaError_t im2col_direct_t(const T *x, const ConvGeom &g, const float *bias, int64_t bias_len, uint8_t *rows,
+                            cudaStream_t s) {
+    const int64_t rbc = row_bytes(g.C, static_cast<bt_code>(CODE));
+    const int G = static_cast<int>(rbc / GroupOut<CODE>::kBytes), kk = g.k * g.k;
+    const int64_t total = g.B * g.Ho * g.Wo * kk * G;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * (2048 / kPackThreads);
+    const int64_t blocks = (total + kPackThreads - 1) / kPackThreads;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute pdl = pdl_attribute();
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks < cap ? blocks : cap));
+    cfg.blockDim = dim3(kPackThreads);
+    cfg.stream = s;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pack_im2col_direct_kernel<T, CODE>, x, static_cast<int>(g.C), static_cast<int>(g.H),
+                              static_cast<int>(g.W), static_cast<int>(g.Ho), static_cast<int>(g.Wo), g.k, g.s, g.p, g.d,
+                              make_fastdiv(static_cast<uint32_t>(G)), make_fastdiv(static_cast<uint32_t>(kk)),
+                              static_cast<int>(kk * rbc), total, bias, static_cast<int>(bias_len), rows);
+}
+
+template <typename T>
+cudaError_t im2col_code(const T *x, const ConvGeom &g, const float *bias, int64_t bias_len, bt_code code,
+                        uint8_t *rows, bool direct_ok, cudaStream_t s) {
+    // direct_ok: a public unfold call (any plan, else the direct kernel);
+    // otherwise the convolution asks for the one-pass unfold only where it pays
+    cudaError_t e = cudaErrorNotSupported;
+    if (code == BT_CODE_E4M3) e = im2col_t<T, BT_CODE_E4M3>(x, g, bias, bias_len, rows, !direct_ok, s);
+    else if (code == BT_CODE_E2M1) e = im2col_t<T, BT_CODE_E2M1>(x, g, bias, bias_len, rows, !direct_ok, s);
+    if (e != cudaErrorNotSupported || !direct_ok) return e;
+    if (code == BT_CODE_E4M3) return im2col_direct_t<T, BT_CODE_E4M3>(x, g, bias, bias_len, rows, s);
+    if (code == BT_CODE_E2M1) return im2col_direct_t<T, BT_CODE_E2M1>(x, g, bias, bias_len, rows, s);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_pack_im2col(const void *x, bt_dtype xt, const ConvGeom &g, const float *bias, int64_t bias_len,
+                               bt_code code, uint8_t *rows, bool direct_ok, cudaStream_t s) {
+    if (g.B == 0 || g.Ho * g.Wo == 0) return cudaSuccess;
+    switch (xt) {
+        case BT_F32: return im2col_code(static_cast<const float *>(x), g, bias, bias_len, code, rows, direct_ok, s);
+        case BT_BF16:
+            return im2col_code(static_cast<const __nv_bfloat16 *>(x), g, bias, bias_len, code, rows, direct_ok, s);
+        case BT_F16: return im2col_code(static_cast<const __half *>(x), g, bias, bias_len, code, rows, direct_ok, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+bool unfold_single_pass(const ConvGeom &g, bt_dtype xt, bt_code code) {
+    if ((code != BT_CODE_E4M3 && code != BT_CODE_E2M1) || tensor_map_encoder() == nullptr) return false;
+    UnfoldArgs u{};
+    bool efficient = false;
+    return plan_unfold(g, dtype_bytes(xt), code, u, efficient) && efficient;
 }
 
 cudaError_t launch_im2col_rows(const uint8_t *xp, const ConvGeom &g, int64_t rbc, uint8_t *rows, cudaStream_t s) {

@@ -765,6 +765,8 @@ bool plan(TcArgs &a, Maps &mp, TileCfg &c, bt_code code, const uint8_t *ap, cons
 
 bool tc_available() { return encode_tiled() != nullptr; }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encode_tiled(); }
+
 cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M, int64_t N, int64_t K,
                              float alpha, void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
     TcArgs a{};
