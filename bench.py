@@ -342,6 +342,15 @@ def run_ours(args, rank, world):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     bound, peak, unit, peak_how = roofline_peak(algo_name, peaks, sms)
     achieved = ops / (gemm_ms / 1e3) / 1e12
+    # the contraction call's least traffic; below the ridge point (peak ops per
+    # byte of HBM) it is bounded by HBM, not by its pipe
+    call_bytes = contraction_bytes(wl, code, bt, single_pass if wl.kind == "conv" else False)
+    intensity = ops / call_bytes
+    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity < ridge:
+        bound, unit = "hbm", "GB/s"
+        peak, peak_how = peaks["hbm_gbs"], f"measured copy bandwidth; {intensity:.0f} ops/B < ridge {ridge:.0f}"
+        achieved = call_bytes / (gemm_ms / 1e3) / 1e9
     traffic = load_traffic(wl.name, algo_name)
     line = {
         "metric": "binary GOPS (2*M*N*K/s)",
@@ -365,6 +374,7 @@ def run_ours(args, rank, world):
                       "how": "second pass of the same steps, CUDA events around each kernel on its stream"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": int(call_bytes), "ops_per_byte": round(intensity, 1),
                      "traffic_unit": "DRAM bytes per tc_kernel launch (ncu, this kernel source)",
                      "peak_source": f"{peak_src}: {peak_how}",
                      "kernel": "contraction"},
@@ -382,6 +392,25 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     return line
+
+
+def contraction_bytes(wl, code, bt, single_pass: bool) -> float:
+    """Least bytes the contraction call moves: its packed activations (packed
+    rows of a linear layer; im2col rows when the convolution was unfolded in
+    one pass; packed NHWC pixels otherwise), the packed weights, the output."""
+    out_b = 4 if wl.out_dtype == "f32" else 2
+    if wl.kind == "linear":
+        M, K = wl.x.shape
+        N = wl.w.shape[0]
+        rb = bt.bt_packed_row_bytes(K, code)
+        return (M + N) * rb + M * N * out_b
+    B, C, H, W = wl.x.shape
+    O, k = wl.w.shape[0], wl.w.shape[2]
+    Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
+    Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
+    rbc = bt.bt_packed_row_bytes(C, code)
+    x_b = B * Ho * Wo * k * k * rbc if single_pass else B * H * W * rbc
+    return x_b + O * k * k * rbc + B * O * Ho * Wo * out_b
 
 
 HOST_LLC_BYTES = 256 << 20     # rotate host buffers over more than this

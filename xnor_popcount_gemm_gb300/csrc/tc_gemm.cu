@@ -41,12 +41,13 @@
 //                   one tcgen05.mma into the tile's accumulator buffer;
 //                   tcgen05.commit frees the stage and, after a tile's last
 //                   stage, hands the buffer to the epilogue.
-//   warps 2..5      epilogue: each drains its 32 TMEM lanes (rows), the next
-//                   32-column box in flight while the current one is scaled,
-//                   cast, and written to a swizzled 32 x 32 smem box, from
-//                   which whole row segments leave in 16-byte stores (or, for
-//                   NCHW, runs of pixels in the widest aligned stores). Once
-//                   drained, the buffer goes back to the MMA warp.
+//   warps 2..9      epilogue, two warps per TMEM lane quarter (32 rows) taking
+//                   alternate 32-column boxes: the next box's TMEM load in
+//                   flight while the current one is scaled, cast, and written
+//                   to the warp's swizzled 32 x 32 smem box, from which whole
+//                   row segments leave in 16-byte stores (or, for NCHW, runs
+//                   of pixels in the widest aligned stores). Once both CTAs'
+//                   warps have drained it, the buffer goes back to the MMA warp.
 // Every wait is bounded (kWaitNs): a wait that runs out records BT_ERR_TIMEOUT
 // in the device error word and the kernel winds down without trapping.
 #include <cudaTypedefs.h>
@@ -412,7 +413,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
+        // ---------------- epilogue (warps 2..9) ----------------
         pdl_wait();                                       // the previous kernel may still use `out`
         T *out = static_cast<T *>(a.out);
         const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // this warp's staging box
@@ -607,8 +608,9 @@ bool map_3d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, 
 //   - its share of the copy engine: about 480 clocks per TMA box of up to two
 //     slices, whatever its size (560 for four), two boxes per stage;
 // plus about 1000 clocks per tile. The epilogue (about 20 clocks per output
-// column of the CTA's 128 rows) overlaps the next tile's MMAs and shows only
-// where it is the longer of the two, and once for the last tile.
+// column of the CTA's 128 rows; 30 for a pair, whose tcgen05.ld of one buffer
+// waits behind the pair MMAs writing the other) overlaps the next tile's MMAs
+// and shows only where it is the longer of the two, and once for the last tile.
 // BT_TC_CONFIG="bn,d" (single) or "pair,bn,d" overrides the choice.
 struct TileCfg {
     bool pair;
@@ -630,7 +632,7 @@ double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int
     double slice = mma > smem ? mma : smem;
     if (copy > slice) slice = copy;
     double tile = slices * slice + 1000.0;
-    const double epi = 20.0 * bn;
+    const double epi = (pair ? 30.0 : 20.0) * bn;
     if (epi > tile) tile = epi;
     return static_cast<double>(rounds) * tile + epi + 600.0;
 }
