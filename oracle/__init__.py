@@ -20,6 +20,14 @@ plain numpy / PyTorch CPU ops. Every function cites the passage it follows:
   formula and the unfold + mm lowering of a convolution.
 * torch/ao/quantization/experimental/linear.py, ``LinearAPoT.matmul``: the
   plain i-j-k triple loop of a matrix product.
+* bitorch-engine ``BinaryConv2dForward.backward`` (the straight-through
+  backward written out in code) and ``BinaryLinearForward.backward`` (the
+  same steps in prose for the linear layer): ``grad_input`` from the upstream
+  gradient and ``sign(w) * scale_w`` in the gradient's dtype, zeroed where
+  ``x / scale_a`` falls outside [-1, 1]; ``grad_scale_a`` as the sum of
+  ``grad_input * sign(x) / sqrt(numel)``; ``grad_weight`` from
+  ``sign(x) * scale_a`` and the upstream gradient. (The int8 quantization of
+  ``grad_weight`` that follows on the page is not part of this oracle.)
 
 Readings where the sources leave a step open:
 
@@ -36,6 +44,14 @@ Readings where the sources leave a step open:
    rounds to nearest-even.
 4. A convolution tap in the zero padding contributes 0 to the dot product,
    as in the unfold + mm lowering.
+5. Backward, linear layer: the page's conv steps with the convolution's
+   input and weight gradients replaced by the two matrix products
+   ``g @ wt`` and ``g^T @ xs``. Each product is formed exactly (double) and
+   rounded once to the gradient's dtype (bf16), as a matrix product in that
+   dtype returns it; ``x / scale_a`` is an fp32 division rounded to x's
+   dtype before the comparison with -1 and 1; ``grad_input`` is the
+   rounded product times the fp32 mask (so fp32, holding bf16 values); the
+   ``grad_scale_a`` terms are fp32 products and their sum is taken in double.
 """
 from __future__ import annotations
 
@@ -310,3 +326,74 @@ def pack_nchw_to_nhwc(s: np.ndarray, code: int) -> np.ndarray:
     """
     s = np.asarray(s, dtype=np.int8)
     return pack_rows(np.ascontiguousarray(np.transpose(s, (0, 2, 3, 1))), code)
+
+
+# ----------------------------------------------------------------------------
+# Backward (straight-through estimator) of the binary linear layer, following
+# bitorch-engine BinaryConv2dForward.backward step by step with the conv
+# gradients replaced by matrix products (BinaryLinearForward.backward states
+# the same steps for the linear layer).
+# ----------------------------------------------------------------------------
+
+_BF16_MAX = float.fromhex("0x1.fep127")
+
+
+def bf16_round(a) -> np.ndarray:
+    """Round to the nearest bfloat16 value, ties to even, from float64 (one
+    rounding); returns float32 holding bf16 values. NaN stays NaN, values
+    beyond the largest finite bf16 after rounding become +-inf."""
+    v = np.asarray(a, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.float64)
+    fin = np.isfinite(v)
+    out[~fin] = v[~fin]
+    vf = v[fin]
+    _, e = np.frexp(vf)                       # vf = m * 2**e, 0.5 <= |m| < 1
+    # 8 significant bits: the spacing is 2**(e-8); below the normal range
+    # (e - 1 < -126) the spacing stays 2**-133
+    step = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    r = np.rint(vf / step) * step             # rint rounds half to even
+    r[np.abs(r) > _BF16_MAX] = np.inf * np.sign(r[np.abs(r) > _BF16_MAX])
+    out[fin] = r
+    return out.astype(np.float32)
+
+
+def sign(a) -> np.ndarray:
+    """``torch.sign``: -1, 0 or +1 (NaN stays NaN)."""
+    return np.sign(np.asarray(a, dtype=np.float32))
+
+
+def linear_backward(x, w, g, scale_a: float, scale_w: float, x_dtype: str = "bf16") -> dict:
+    """The three gradients of the binary linear layer for upstream gradient
+    ``g`` [M, N] (bf16 values), input ``x`` [M, K], weight ``w`` [N, K].
+
+    Steps (BinaryConv2dForward.backward):
+      wt = (sign(w) in g's dtype) * scale_w        -> bf16(sign(w) * scale_w)
+      grad_input = g @ wt                          -> exact sum, rounded to bf16
+      q = x / scale_a (x's dtype); middle = 1 - [q < -1] - [q > 1]
+      grad_input = grad_input * middle             (fp32)
+      grad_scale_a = sum(grad_input * sign(x) * (1 / sqrt(numel(x))))
+      grad_weight = g^T @ (sign(x) * scale_a)      -> exact sum, rounded to bf16
+    Returns the rounded and the exact (float64) products as well."""
+    x32 = _as_f32(x)
+    w32 = _as_f32(w)
+    g64 = _as_f32(g).astype(np.float64)
+    M, K = x32.shape
+    sa32, sw32 = np.float32(scale_a), np.float32(scale_w)
+    wt = bf16_round(sign(w32) * sw32)                       # [N, K]
+    gi_exact = g64 @ wt.astype(np.float64)                  # [M, K]
+    gi = bf16_round(gi_exact)
+    q = x32 / sa32                                          # fp32 division
+    if x_dtype in ("bf16",):
+        q = bf16_round(q)
+    elif x_dtype == "f16":
+        q = torch.from_numpy(q).to(torch.float16).float().numpy()
+    middle = (1.0 - (q < -1).astype(np.float32) - (q > 1).astype(np.float32)).astype(np.float32)
+    grad_input = (gi * middle).astype(np.float32)
+    inv = np.float32(1.0 / np.sqrt(np.float64(M * K)))
+    terms = ((grad_input * sign(x32)).astype(np.float32) * inv).astype(np.float32)
+    grad_scale_a = float(terms.astype(np.float64).sum())
+    xs = bf16_round(sign(x32) * sa32)                       # [M, K]
+    gw_exact = g64.T @ xs.astype(np.float64)                # [N, K]
+    return {"grad_input": grad_input, "grad_input_exact": gi_exact, "middle": middle,
+            "grad_scale_a": grad_scale_a, "grad_scale_a_abs": float(np.abs(terms.astype(np.float64)).sum()),
+            "grad_weight": bf16_round(gw_exact), "grad_weight_exact": gw_exact}

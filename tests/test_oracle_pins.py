@@ -403,3 +403,115 @@ def test_planted_linear_mistakes_are_caught():
     # a threshold of > 0 instead of >= 0 changes the sign of exact zeros
     x = np.array([[0.0, 1.0, -1.0]], np.float32)
     assert oracle.binarize(x)[0, 0] == 1 and np.where(x > 0, 1, -1)[0, 0] == -1
+
+
+# ---------------------------------------------------------------------------
+# Backward of the binary linear layer (straight-through estimator)
+# ---------------------------------------------------------------------------
+
+def test_golden_linear_backward():
+    for ex in json.load(open(GOLDEN))["linear_backward"]:
+        got = oracle.linear_backward(np.array(ex["x"], np.float32), np.array(ex["w"], np.float32),
+                                     np.array(ex["g"], np.float32), ex["scale_a"], ex["scale_w"], ex["x_dtype"])
+        np.testing.assert_array_equal(got["grad_input"], np.array(ex["grad_input"], np.float32), ex["why"])
+        np.testing.assert_array_equal(got["grad_weight"], np.array(ex["grad_weight"], np.float32), ex["why"])
+        assert got["grad_scale_a"] == ex["grad_scale_a"], ex["why"]
+        if "grad_input_if_f32_x" in ex:
+            got32 = oracle.linear_backward(np.array(ex["x"], np.float32), np.array(ex["w"], np.float32),
+                                           np.array(ex["g"], np.float32), ex["scale_a"], ex["scale_w"], "f32")
+            np.testing.assert_array_equal(got32["grad_input"], np.array(ex["grad_input_if_f32_x"], np.float32))
+
+
+def test_bf16_round_matches_torch_cast():
+    rng = np.random.default_rng(41)
+    v = np.concatenate([rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 20000),
+                        np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 3.39e38, 3.4e38, 1e-39, -1e-41,
+                                  2.0 ** -133, 1.5 * 2.0 ** -133, 2.5 * 2.0 ** -133], np.float32)]).astype(np.float32)
+    # exact ties: 1 + (2j + 1) * 2^-8 sit halfway between bf16 neighbours
+    ties = (1.0 + (2 * np.arange(64) + 1) * 2.0 ** -8).astype(np.float32)
+    v = np.concatenate([v, ties, -ties])
+    want = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    got = oracle.bf16_round(v)
+    np.testing.assert_array_equal(got, want)
+    num = ~np.isnan(want)
+    assert np.array_equal(np.signbit(got[num]), np.signbit(want[num]))
+
+
+def _ste_autograd(x, w, g, scale_a, scale_w, x_dtype):
+    """The straight-through gradients by torch autograd in float64: the
+    activation passes through a clamp-like function whose derivative is 1
+    where |x / scale_a| < 1 and 0 outside; the weight enters as sign(w)
+    rounded to bf16 times scale_w, with an identity derivative for w."""
+    xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    wt = torch.tensor(w, dtype=torch.float64, requires_grad=True)
+    s_w = torch.from_numpy(oracle.bf16_round(np.sign(np.asarray(w, np.float32)) * np.float32(scale_w))).double()
+    s_x = torch.from_numpy(oracle.bf16_round(np.sign(np.asarray(x, np.float32)) * np.float32(scale_a))).double()
+    act = torch.nn.functional.hardtanh(xt / scale_a) * scale_a        # derivative: 1 strictly inside
+    wq = s_w + (wt - wt.detach())                                       # value s_w, derivative 1
+    y = act @ s_w.T + s_x @ wq.T - s_x @ s_w.T.detach()                 # splits the two paths
+    (y * torch.tensor(g, dtype=torch.float64)).sum().backward()
+    return xt.grad.numpy(), wt.grad.numpy()
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 4, 5), (8, 16, 7), (1, 33, 64)])
+def test_linear_backward_matches_autograd(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    scale_a, scale_w = 0.75, 0.3
+    x = torch.randn(M, K, generator=torch.Generator().manual_seed(K)).to(torch.bfloat16).float().numpy()
+    # keep |x / scale_a| away from 1, where bf16 rounding of the quotient decides the mask
+    r = np.abs(x / scale_a)
+    x[(r > 1 - 2.0 ** -6) & (r < 1 + 2.0 ** -6)] = 0.0
+    w = rng.standard_normal((N, K)).astype(np.float32)
+    w[0, 0] = 0.0                                                       # sign(0) = 0
+    g = torch.randn(M, N, generator=torch.Generator().manual_seed(N)).to(torch.bfloat16).float().numpy()
+    o = oracle.linear_backward(x, w, g, scale_a, scale_w, "bf16")
+    gx, gw = _ste_autograd(x, w, g, scale_a, scale_w, "bf16")
+    np.testing.assert_allclose(o["grad_input_exact"] * o["middle"], gx, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o["grad_weight_exact"], gw, rtol=0, atol=1e-12)
+
+
+def test_linear_backward_closed_forms():
+    rng = np.random.default_rng(43)
+    M, N, K = 5, 7, 9
+    scale_a, scale_w = 0.6, 0.45
+    x = (np.abs(torch.randn(M, K).to(torch.bfloat16).float().numpy()) * 0.5).astype(np.float32) + 0.01
+    g = torch.randn(M, N).to(torch.bfloat16).float().numpy()
+    w = np.abs(rng.standard_normal((N, K))).astype(np.float32) + 0.1   # every sign +1
+    o = oracle.linear_backward(x, w, g, scale_a, scale_w, "bf16")
+    bw = np.float64(oracle.bf16_round(np.float32(scale_w)))
+    ba = np.float64(oracle.bf16_round(np.float32(scale_a)))
+    # all weights +1: every grad_input column is bf16(scale_w) times the row sum of g
+    np.testing.assert_array_equal(o["grad_input_exact"], np.repeat(bw * g.astype(np.float64).sum(1, keepdims=True), K, 1))
+    # all activations positive: every grad_weight column is bf16(scale_a) times the column sum of g
+    np.testing.assert_array_equal(o["grad_weight_exact"], np.repeat(ba * g.astype(np.float64).sum(0)[:, None], K, 1))
+    # doubling g doubles every gradient exactly (power-of-two scaling commutes with rounding)
+    o2 = oracle.linear_backward(x, w, 2 * g, scale_a, scale_w, "bf16")
+    np.testing.assert_array_equal(o2["grad_input"], 2 * o["grad_input"])
+    np.testing.assert_array_equal(o2["grad_weight"], 2 * o["grad_weight"])
+    assert o2["grad_scale_a"] == 2 * o["grad_scale_a"]
+    # outside |x| <= scale_a the input gradient is zero
+    x[0, 0] = 3.0
+    o3 = oracle.linear_backward(x, w, g, scale_a, scale_w, "bf16")
+    assert o3["middle"][0, 0] == 0 and o3["grad_input"][0, 0] == 0
+
+
+def test_planted_backward_mistakes_are_caught():
+    rng = np.random.default_rng(44)
+    M, N, K = 4, 6, 5
+    x = torch.randn(M, K, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).float().numpy()
+    x[np.abs(np.abs(x / 0.8) - 1) < 2.0 ** -6] = 0.0
+    w = rng.standard_normal((N, K)).astype(np.float32)
+    g = torch.randn(M, N, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16).float().numpy()
+    gx, gw = _ste_autograd(x, w, g, 0.8, 0.3, "bf16")
+    o = oracle.linear_backward(x, w, g, 0.8, 0.3, "bf16")
+    assert np.allclose(o["grad_input_exact"] * o["middle"], gx) and np.allclose(o["grad_weight_exact"], gw)
+    wt = oracle.bf16_round(np.sign(w) * np.float32(0.3)).astype(np.float64)
+    xs = oracle.bf16_round(np.sign(x) * np.float32(0.8)).astype(np.float64)
+    assert not np.allclose(g.astype(np.float64) @ wt, gx)                          # mask dropped
+    assert not np.allclose((g.astype(np.float64) @ -wt) * o["middle"], gx)         # sign flipped
+    wt_a = oracle.bf16_round(np.sign(w) * np.float32(0.8)).astype(np.float64)
+    assert not np.allclose((g.astype(np.float64) @ wt_a) * o["middle"], gx)       # scales swapped
+    mid_x = ((x >= -1) & (x <= 1)).astype(np.float64)
+    assert not np.allclose((g.astype(np.float64) @ wt) * mid_x, gx)               # mask on x, not x / scale_a
+    assert not np.allclose(g.astype(np.float64).T @ np.sign(x).astype(np.float64), gw)   # scale_a dropped
+    assert not np.allclose(g.astype(np.float64).T @ oracle.bf16_round(np.sign(w[:M] if N >= M else w) * 0.8).astype(np.float64)[:, :K], gw)  # w for x
