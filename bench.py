@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", default="auto", choices=["auto", "popc", "e4m3", "e2m1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
+                    help="backward: the straight-through backward of a linear workload (all three gradients)")
     return ap.parse_args()
 
 
@@ -531,6 +533,100 @@ def load_traffic(workload: str, algo: str):
 
 
 # ---------------------------------------------------------------------------
+# backward pass (straight-through estimator) of a linear workload
+# ---------------------------------------------------------------------------
+
+def run_backward(args, rank, world):
+    """K steps of bt_binary_linear_backward (grad_input with the fused mask and
+    grad_scale_a, grad_weight) on the workload's x and W with a synthetic bf16
+    upstream gradient; sign(W)^T is prepared once outside timing, as the
+    forward's packed weight is."""
+    import xnor_popcount_gemm_gb300 as bt
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    wl = workloads.NAMED[args.workload]()
+    if wl.kind != "linear":
+        raise SystemExit("--pass backward covers the linear workloads")
+    M, K = wl.x.shape
+    N = wl.w.shape[0]
+    if N % 8 or K % 8:
+        raise SystemExit("--pass backward needs N and K multiples of 8")
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator().manual_seed(1000)
+    g_host = (torch.randn(M, N, generator=gen) * 0.01).to(torch.bfloat16)
+    x_host = wl.x if wl.x.dtype in (torch.bfloat16, torch.float32) else wl.x.float()
+    wst = bt.bt_sign_transpose(wl.w.to(dev))
+    per = x_host.numel() * x_host.element_size() + g_host.numel() * 2 + (M * K + N * K) * 2
+    nbuf = max(1, -(-2 * L2_BYTES // per))
+    xs = [x_host.to(dev) for _ in range(nbuf)]
+    gs = [g_host.to(dev) for _ in range(nbuf)]
+    gxs = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    gws = [torch.empty(N, K, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    gsa = torch.empty((), dtype=torch.float32, device=dev)
+    ws = torch.empty(bt.bt_binary_linear_backward_workspace(M, N, K, True), dtype=torch.uint8, device=dev)
+    flops = 2 * (2.0 * M * N * K)
+
+    def step(i, which="both"):
+        j = i % nbuf
+        bt.bt_binary_linear_backward(xs[j], wst, gs[j], wl.scale_a, wl.scale_w,
+                                     grad_input=which in ("both", "input"),
+                                     grad_weight_dtype=torch.bfloat16 if which in ("both", "weight") else None,
+                                     grad_x=gxs[j], grad_scale_a=gsa, grad_w=gws[j], workspace=ws)
+
+    def timed(which, n):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        a0.record(stream)
+        for i in range(n):
+            step(i, which)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a0.elapsed_time(a1), world) / n
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert bt.bt_device_status() == 0
+    with ClockSampler(dev.index) as clk:
+        ms = timed("both", args.steps)
+        ms_in = timed("input", args.steps)
+        ms_w = timed("weight", args.steps)
+    if bt.bt_device_status() != 0:
+        raise RuntimeError("device status")
+    peaks, peak_src = measured_peaks()
+    achieved = 2.0 * M * N * K / (ms_in / 1e3) / 1e12
+    line = {
+        "metric": "backward TFLOP/s (grad_input + grad_weight, 2 x 2*M*N*K / s)",
+        "value": round(flops * world / (ms / 1e3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 x bf16 (fp32 acc)",
+        "data": "synthetic (the workload's x and W; upstream gradient N(0, 0.01) in bf16)",
+        "config": {"workload": wl.name, "pass": "backward", "M": M, "N": N, "K": K,
+                   "x_dtype": str(x_host.dtype).replace("torch.", ""),
+                   "weights": "sign(W)^T prepared outside timing",
+                   "l2": f"inputs+outputs rotate over {nbuf} buffers", "parallelism": f"replicas x{world}"},
+        "kernel_ms": {"grad_input_call": round(ms_in, 5), "grad_weight_call": round(ms_w, 5),
+                      "how": "the same call asking for one gradient only, K steps each"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": f"{peak_src}: cuBLAS bf16 burst",
+                     "kernel": "grad_input contraction (tc_kernel bf16 with the fused mask), per call"},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
 
@@ -595,7 +691,7 @@ def main():
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return
     rank, world = dist_init(args)
-    line = run_ours(args, rank, world)
+    line = run_backward(args, rank, world) if args.pass_ == "backward" else run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -293,6 +293,69 @@ size_t bt_binary_linear_noalloc_max_bytes(void);
  */
 bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo);
 
+/* ------------------------------------------------------------------------
+ * Backward of the binary linear layer (straight-through estimator).
+ * bitorch-engine BinaryLinearForward.backward states the steps for the linear
+ * layer; BinaryConv2dForward.backward writes them out (for the convolution):
+ *   wt           = weight.type(grad.dtype).sign() * scale_w
+ *   grad_input   = (grad @ wt) in grad's dtype, then times
+ *                  middle = 1 - [x/scale_a < -1] - [x/scale_a > 1]
+ *   grad_scale_a = sum(grad_input * x.sign() * (1 / sqrt(x.numel())))
+ *   grad_weight  = (grad^T @ (x.sign() * scale_a)) in grad's dtype
+ * The int8 quantization of grad_weight that follows on the page is left to
+ * the caller. sign is torch.sign: (v > 0) - (v < 0), 0 for zeros and NaN.
+ * ------------------------------------------------------------------------ */
+
+/* Row pitch (elements) of the transposed weight signs bt_binary_linear_backward
+ * takes for an N-row weight: N rounded up to 64. -1 for N < 0. */
+int64_t bt_backward_weight_ld(int64_t N);
+
+/*
+ * bt_sign_transpose -- torch.sign of w, transposed, as bf16 (the
+ * `weight.type(grad.dtype).sign()` of BinaryConv2dForward.backward, laid out
+ * as the backward's contraction reads it). w [R, C] row-major (F32, BF16 or
+ * F16); out [C, ld] bf16 with out[c*ld + r] = sign(w[r, c]) for r < R and 0
+ * for R <= r < ld. Build it once per weight (like bt_pack_sign) with
+ * ld = bt_backward_weight_ld(R). ld >= R and a multiple of 8; w and out
+ * 16-byte aligned device memory owned by the caller.
+ * Errors: INVALID_ARG (dtype, sizes, null), ALIGNMENT, UNSUPPORTED
+ * (C or ld > 4,194,240), CUDA.
+ */
+bt_status bt_sign_transpose(const void *w, bt_dtype w_dtype, int64_t R, int64_t C, int64_t ld, void *out,
+                            bt_stream stream);
+
+/* Workspace bytes bt_binary_linear_backward needs: 0 without grad_weight;
+ * else 2 * (N + K) * roundup(M, 64) bytes (each part rounded up to 256 B). */
+size_t bt_binary_linear_backward_workspace(int64_t M, int64_t N, int64_t K, int want_grad_weight);
+
+/*
+ * bt_binary_linear_backward -- the gradients above for the layer
+ * y = binary_linear(x, W) with upstream gradient g:
+ *   x      [M, K] the forward's input, BF16 or F32 (q = x / scale_a is rounded
+ *          to x's dtype before it is compared with -1 and 1);
+ *   wst    [K, ldw] bf16, bt_sign_transpose(W) with ldw = bt_backward_weight_ld(N);
+ *          needed only for grad_x;
+ *   g      [M, N] bf16;
+ *   grad_x [M, K] bf16 out (the page's fp32 grad_input holds these same
+ *          values: bf16 products times 0 or 1), or NULL;
+ *   grad_scale_a  one device float, overwritten with the sum (fp32 terms,
+ *          summed in fp32 in no fixed order), or NULL; needs grad_x;
+ *   grad_w [N, K] out, BF16 (the page's value) or F32 (the fp32 sums before
+ *          the rounding to bf16), or NULL;
+ *   workspace  bt_binary_linear_backward_workspace(M, N, K, grad_w != NULL)
+ *          bytes, 256-byte aligned (the transposes of g and sign(x)).
+ * Both products run on the tensor cores (bf16 x bf16, fp32 accumulators):
+ * each output is the fp32 sum of exact products, scaled by bf16(scale) and
+ * rounded once to bf16. N and K multiples of 8; scale_a, scale_w finite > 0;
+ * pointers 16-byte aligned device memory owned by the caller; asynchronous on
+ * `stream`. Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED (N or K
+ * not a multiple of 8, no tensor-core support), CUDA.
+ */
+bt_status bt_binary_linear_backward(const void *x, bt_dtype x_dtype, const void *wst, int64_t ldw, const void *g,
+                                    int64_t M, int64_t N, int64_t K, float scale_a, float scale_w,
+                                    void *grad_x, float *grad_scale_a, void *grad_w, bt_dtype grad_w_dtype,
+                                    void *workspace, size_t workspace_bytes, bt_stream stream);
+
 /*
  * bt_device_status -- synchronizes `stream`, then reads and clears the
  * device error word of the current device: BT_ERR_TIMEOUT if a kernel's

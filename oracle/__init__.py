@@ -358,8 +358,10 @@ def bf16_round(a) -> np.ndarray:
 
 
 def sign(a) -> np.ndarray:
-    """``torch.sign``: -1, 0 or +1 (NaN stays NaN)."""
-    return np.sign(np.asarray(a, dtype=np.float32))
+    """``torch.sign``, which is ``(a > 0) - (a < 0)``: -1, 0 or +1, and 0 for
+    NaN and for -0.0."""
+    a = np.asarray(a, dtype=np.float32)
+    return ((a > 0).astype(np.float32) - (a < 0).astype(np.float32)).astype(np.float32)
 
 
 def linear_backward(x, w, g, scale_a: float, scale_w: float, x_dtype: str = "bf16") -> dict:

@@ -212,3 +212,33 @@ def test_plan_override(monkeypatch):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_device_status_without_device():
     assert bt._c_status(None) == bt.BT_ERR_CUDA
+
+
+def test_backward_abi_validation():
+    assert bt.bt_backward_weight_ld(4093) == 4096 and bt.bt_backward_weight_ld(64) == 64
+    assert bt.bt_backward_weight_ld(0) == 0 and bt.bt_backward_weight_ld(-1) == -1
+    assert bt.bt_binary_linear_backward_workspace(100, 16, 24, True) == 16 * 128 * 2 + 24 * 128 * 2
+    assert bt.bt_binary_linear_backward_workspace(100, 16, 24, False) == 0
+    st = bt._c_sign_t
+    assert st(256, bt.BT_I32, 4, 4, 8, 512, None) == bt.BT_ERR_INVALID_ARG       # dtype
+    assert st(256, bt.BT_F32, 10, 4, 8, 512, None) == bt.BT_ERR_INVALID_ARG      # ld < R
+    assert st(256, bt.BT_F32, 4, 4, 12, 512, None) == bt.BT_ERR_INVALID_ARG      # ld not a multiple of 8
+    assert st(None, bt.BT_F32, 0, 4, 8, None, None) == bt.BT_OK                  # empty
+    assert st(None, bt.BT_F32, 4, 4, 8, 512, None) == bt.BT_ERR_INVALID_ARG
+    assert st(256 + 4, bt.BT_F32, 4, 4, 8, 512, None) == bt.BT_ERR_ALIGNMENT
+    bw = bt._c_bwd
+
+    def call(**kw):
+        a = dict(x=256, xt=bt.BT_BF16, wst=512, ldw=64, g=768, M=16, N=64, K=64, sa=0.5, sw=0.5, gx=1024,
+                 gsa=2048, gw=4096, gwt=bt.BT_BF16, ws=8192, wsb=1 << 20, s=None)
+        a.update(kw)
+        return bw(*a.values())
+    assert call(xt=bt.BT_F16) == bt.BT_ERR_INVALID_ARG
+    assert call(gwt=bt.BT_I32) == bt.BT_ERR_INVALID_ARG
+    assert call(sa=0.0) == bt.BT_ERR_INVALID_ARG
+    assert call(sw=float("inf")) == bt.BT_ERR_INVALID_ARG
+    assert call(gx=None) == bt.BT_ERR_INVALID_ARG                                # grad_scale_a without grad_x
+    assert call(ldw=56) == bt.BT_ERR_INVALID_ARG                                 # ldw < N
+    assert call(wst=None) == bt.BT_ERR_INVALID_ARG
+    assert call(N=60, ldw=64) == bt.BT_ERR_UNSUPPORTED                           # N not a multiple of 8
+    assert call(K=20) == bt.BT_ERR_UNSUPPORTED

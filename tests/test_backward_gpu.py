@@ -1,0 +1,188 @@
+"""GPU parity of the straight-through backward of the binary linear layer
+(bt_sign_transpose + bt_binary_linear_backward, through the C ABI) against
+oracle.linear_backward.
+
+The tensor cores accumulate exact bf16 products in fp32, the oracle sums
+them exactly (float64); each side rounds its sum once to bf16. So an output
+may differ from the oracle's by the fp32 accumulation error, which can move
+the bf16 rounding by one step: every output must lie within
+max(one bf16 step of the oracle's value, n * 2^-23 * sum_j |terms_j|) of the
+oracle's, n the contraction length (the classical bound n*u*sum|terms| for a
+sum of n floats with unit roundoff u = 2^-24, doubled for the scale). The
+straight-through mask is an integer decision taken in x's dtype on both sides
+and must agree exactly; grad_scale_a (fp32 terms, summed in no fixed order
+on the GPU) must lie within 1e-5 of the sum of |terms| plus the terms of the
+outputs where the two grad_inputs differ.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import xnor_popcount_gemm_gb300 as bt
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def _device_clean():
+    yield
+    assert bt.bt_device_status() == 0
+
+
+def _inputs(M, N, K, x_dtype, seed):
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=gen).to(x_dtype)
+    w = (torch.randn(N, K, generator=gen) * 0.02).to(torch.bfloat16)
+    g = (torch.randn(M, N, generator=gen) * 0.01).to(torch.bfloat16)
+    x.view(-1)[:4] = torch.tensor([0.0, -0.0, 1e-30, -1e-30]).to(x_dtype)[: min(4, x.numel())]
+    w.view(-1)[0] = 0.0
+    scale_a = float(x.float().abs().mean())
+    scale_w = float(w.float().abs().mean())
+    return x, w, g, scale_a, scale_w
+
+
+def _bf16_step(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (2^(e-7) for |v| in [2^e, 2^(e+1)))."""
+    a = np.abs(v.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 7).astype(np.int64))
+
+
+def _check_sum(got, want, abs_terms, n, what):
+    got = got.astype(np.float64)
+    tol = np.maximum(_bf16_step(want), n * 2.0 ** -23 * abs_terms)
+    bad = np.abs(got - want.astype(np.float64)) > tol
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside tolerance, first {np.argwhere(bad)[0].tolist()}"
+
+
+def _run(M, N, K, x_dtype, gw_dtype, seed=0):
+    x, w, g, sa, sw = _inputs(M, N, K, x_dtype, seed)
+    wst = bt.bt_sign_transpose(w.to(DEV))
+    gx, gsa, gw = bt.bt_binary_linear_backward(x.to(DEV), wst, g.to(DEV), sa, sw, grad_weight_dtype=gw_dtype)
+    torch.cuda.synchronize()
+    return x, w, g, sa, sw, gx.cpu(), float(gsa.cpu()), gw.cpu()
+
+
+def _compare(x, w, g, sa, sw, gx, gsa, gw, x_dt):
+    o = oracle.linear_backward(x.float().numpy(), w.float().numpy(), g.float().numpy(), sa, sw, x_dt)
+    g64 = g.double().numpy()
+    bw = float(oracle.bf16_round(np.float32(sw)))
+    ba = float(oracle.bf16_round(np.float32(sa)))
+    M, K = x.shape
+    N = w.shape[0]
+    # grad_input: mask exactly, values within the bound
+    gxn = gx.float().numpy()
+    masked = o["middle"] == 0
+    assert np.all(gxn[masked] == 0), "mask disagrees"
+    abs_in = np.abs(g64).sum(1, keepdims=True) * bw * np.ones((1, K))
+    _check_sum(gxn, o["grad_input"], abs_in, N, "grad_input")
+    # grad_scale_a
+    differ = gxn != o["grad_input"]
+    extra = float(np.abs(o["grad_input"][differ]).sum()) / np.sqrt(M * K) * 2.0 ** -7
+    assert abs(gsa - o["grad_scale_a"]) <= 1e-5 * o["grad_scale_a_abs"] + extra + 1e-30, (gsa, o["grad_scale_a"])
+    # grad_weight
+    abs_w = np.abs(g64).sum(0)[:, None] * ba * np.ones((1, K))
+    if gw.dtype == torch.bfloat16:
+        _check_sum(gw.float().numpy(), o["grad_weight"], abs_w, M, "grad_weight")
+    else:
+        got = gw.double().numpy()
+        bad = np.abs(got - o["grad_weight_exact"]) > M * 2.0 ** -23 * abs_w + 1e-30
+        assert not bad.any(), f"grad_weight f32: {int(bad.sum())} outside the fp32 bound"
+    return o, differ
+
+
+SHAPES = [(64, 64, 64), (128, 8, 16), (200, 136, 264), (333, 520, 72), (1000, 264, 1040), (257, 1024, 512)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float32], ids=["x_bf16", "x_f32"])
+def test_linear_backward_matches_oracle(M, N, K, x_dtype):
+    x, w, g, sa, sw, gx, gsa, gw = _run(M, N, K, x_dtype, torch.bfloat16, seed=M + N + K)
+    _, differ = _compare(x, w, g, sa, sw, gx, gsa, gw, "bf16" if x_dtype == torch.bfloat16 else "f32")
+    assert differ.mean() < 0.01                  # almost every bf16 output is the exact one
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 264), (1000, 264, 1040)])
+def test_linear_backward_grad_weight_f32(M, N, K):
+    x, w, g, sa, sw, gx, gsa, gw = _run(M, N, K, torch.bfloat16, torch.float32, seed=7)
+    _compare(x, w, g, sa, sw, gx, gsa, gw, "bf16")
+
+
+def test_linear_backward_mask_decided_in_x_dtype():
+    # x / scale_a just above 1: masked for an f32 x, kept for a bf16 x (the
+    # quotient rounds to exactly 1.0 in bf16)
+    M, N, K = 128, 64, 64
+    sa = 0.998046875
+    x = torch.full((M, K), 1.0)
+    w = torch.ones(N, K, dtype=torch.bfloat16)
+    g = torch.ones(M, N, dtype=torch.bfloat16)
+    wst = bt.bt_sign_transpose(w.to(DEV))
+    gx16, _, _ = bt.bt_binary_linear_backward(x.to(torch.bfloat16).to(DEV), wst, g.to(DEV), sa, 1.0,
+                                             grad_weight_dtype=None)
+    gx32, _, _ = bt.bt_binary_linear_backward(x.to(DEV), wst, g.to(DEV), sa, 1.0, grad_weight_dtype=None)
+    assert torch.all(gx16.cpu().float() == float(N)) and torch.all(gx32.cpu().float() == 0.0)
+
+
+def test_linear_backward_sign_transpose():
+    w = torch.randn(300, 136).to(torch.bfloat16)
+    w[0, :3] = torch.tensor([0.0, -0.0, float("nan")]).to(torch.bfloat16)
+    got = bt.bt_sign_transpose(w.to(DEV)).cpu()
+    assert got.shape == (136, bt.bt_backward_weight_ld(300)) == (136, 320)
+    want = torch.zeros(136, 320, dtype=torch.bfloat16)
+    want[:, :300] = w.float().sign().t().to(torch.bfloat16)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    got32 = bt.bt_sign_transpose(w.float().to(DEV), ld=304).cpu()
+    assert torch.equal(got32[:, :300], want[:, :300]) and torch.all(got32[:, 300:] == 0)
+
+
+def test_linear_backward_partial_requests_and_empty():
+    x, w, g, sa, sw = _inputs(130, 64, 96, torch.bfloat16, 3)
+    wst = bt.bt_sign_transpose(w.to(DEV))
+    gx, gsa, gw = bt.bt_binary_linear_backward(x.to(DEV), wst, g.to(DEV), sa, sw, grad_weight_dtype=None)
+    assert gw is None and gx is not None
+    gx2, gsa2, gw2 = bt.bt_binary_linear_backward(x.to(DEV), None, g.to(DEV), sa, sw, grad_input=False)
+    assert gx2 is None and gsa2 is None and gw2 is not None
+    gx3, gsa3, gw3 = bt.bt_binary_linear_backward(x.to(DEV), wst, g.to(DEV), sa, sw)
+    assert torch.equal(gx3.cpu(), gx.cpu()) and torch.equal(gw3.cpu(), gw2.cpu())
+    e = torch.empty(0, 96, dtype=torch.bfloat16, device=DEV)
+    ge = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    gxe, gsae, gwe = bt.bt_binary_linear_backward(e, wst, ge, sa, sw)
+    assert gxe.numel() == 0 and float(gsae.cpu()) == 0.0 and torch.all(gwe.cpu() == 0)
+
+
+@pytest.mark.parametrize("cfg", ["pair,224,2", "pair,128,2", "224,2", "128,4", "64,1", "pair,256,1"])
+def test_linear_backward_tile_configs(cfg, monkeypatch):
+    monkeypatch.setenv("BT_TC_CONFIG", cfg)
+    x, w, g, sa, sw, gx, gsa, gw = _run(300, 264, 520, torch.bfloat16, torch.bfloat16, seed=11)
+    _compare(x, w, g, sa, sw, gx, gsa, gw, "bf16")
+
+
+@pytest.mark.slow
+def test_linear_backward_full_size_sampled():
+    # the 4096 x 4096 x 4096 bf16 layer: the oracle computes sampled rows of
+    # grad_input and sampled rows of grad_weight
+    M = N = K = 4096
+    x, w, g, sa, sw = _inputs(M, N, K, torch.bfloat16, 2)
+    wst = bt.bt_sign_transpose(w.to(DEV))
+    gx, gsa, gw = bt.bt_binary_linear_backward(x.to(DEV), wst, g.to(DEV), sa, sw)
+    torch.cuda.synchronize()
+    gx, gw = gx.cpu(), gw.cpu()
+    rows = np.array([0, 1, 127, 128, 2047, 4000, 4095])
+    o = oracle.linear_backward(x[rows].float().numpy(), w.float().numpy(), g[rows].float().numpy(), sa, sw, "bf16")
+    g64 = g.double().numpy()
+    bw = float(oracle.bf16_round(np.float32(sw)))
+    _check_sum(gx[rows].float().numpy(), o["grad_input"], np.abs(g64[rows]).sum(1, keepdims=True) * bw * np.ones((1, K)),
+               N, "grad_input rows")
+    assert np.all(gx[rows].float().numpy()[o["middle"] == 0] == 0)
+    cols = np.array([0, 5, 255, 256, 3071, 4095])
+    xs = oracle.bf16_round(oracle.sign(x.float().numpy()) * np.float32(sa)).astype(np.float64)
+    gw_exact = g64[:, cols].T @ xs
+    ba = float(oracle.bf16_round(np.float32(sa)))
+    _check_sum(gw[cols].float().numpy(), oracle.bf16_round(gw_exact), np.abs(g64[:, cols]).sum(0)[:, None] * ba * np.ones((1, K)),
+               M, "grad_weight rows")
+    # grad_scale_a over every output: recompute the terms from the GPU's own grad_input
+    xf = x.float().numpy()
+    terms = ((gx.float().numpy() * oracle.sign(xf)).astype(np.float32) * np.float32(1.0 / np.sqrt(M * K))).astype(np.float64)
+    assert abs(float(gsa.cpu()) - terms.sum()) <= 1e-5 * np.abs(terms).sum()

@@ -422,6 +422,14 @@ def test_golden_linear_backward():
             np.testing.assert_array_equal(got32["grad_input"], np.array(ex["grad_input_if_f32_x"], np.float32))
 
 
+def test_sign_matches_torch_sign():
+    v = np.array([-0.0, 0.0, np.nan, -np.nan, 2.0, -3.0, 1e-45, -1e-45, np.inf, -np.inf], np.float32)
+    want = torch.from_numpy(v).sign().numpy()
+    got = oracle.sign(v)
+    np.testing.assert_array_equal(got, want)
+    assert not np.signbit(got[0]) and not np.isnan(got[2])
+
+
 def test_bf16_round_matches_torch_cast():
     rng = np.random.default_rng(41)
     v = np.concatenate([rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 20000),
@@ -444,8 +452,8 @@ def _ste_autograd(x, w, g, scale_a, scale_w, x_dtype):
     rounded to bf16 times scale_w, with an identity derivative for w."""
     xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
     wt = torch.tensor(w, dtype=torch.float64, requires_grad=True)
-    s_w = torch.from_numpy(oracle.bf16_round(np.sign(np.asarray(w, np.float32)) * np.float32(scale_w))).double()
-    s_x = torch.from_numpy(oracle.bf16_round(np.sign(np.asarray(x, np.float32)) * np.float32(scale_a))).double()
+    s_w = torch.from_numpy(oracle.bf16_round(torch.from_numpy(np.asarray(w, np.float32)).sign().numpy() * np.float32(scale_w))).double()
+    s_x = torch.from_numpy(oracle.bf16_round(torch.from_numpy(np.asarray(x, np.float32)).sign().numpy() * np.float32(scale_a))).double()
     act = torch.nn.functional.hardtanh(xt / scale_a) * scale_a        # derivative: 1 strictly inside
     wq = s_w + (wt - wt.detach())                                       # value s_w, derivative 1
     y = act @ s_w.T + s_x @ wq.T - s_x @ s_w.T.detach()                 # splits the two paths

@@ -67,6 +67,11 @@ _c_lin_noalloc = _sig("bt_binary_linear_noalloc", _i, [_p, _i, _p, _i, _i64, _i6
 _c_noalloc_max = _sig("bt_binary_linear_noalloc_max_bytes", _sz, [])
 _c_pack_im2col = _sig("bt_pack_im2col", _i, [_p, _i, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _p, _i64, _i, _p, _p])
 _c_single_pass = _sig("bt_conv2d_single_pass", _i, [_i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _i])
+_c_bwd_ld = _sig("bt_backward_weight_ld", _i64, [_i64])
+_c_sign_t = _sig("bt_sign_transpose", _i, [_p, _i, _i64, _i64, _i64, _p, _p])
+_c_bwd_ws = _sig("bt_binary_linear_backward_workspace", _sz, [_i64, _i64, _i64, _i])
+_c_bwd = _sig("bt_binary_linear_backward", _i, [_p, _i, _p, _i64, _p, _i64, _i64, _i64, _f, _f, _p, _p, _p, _i,
+                                                _p, _sz, _p])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
 _c_status = _sig("bt_device_status", _i, [_p])
 
@@ -74,7 +79,9 @@ _c_status = _sig("bt_device_status", _i, [_p])
 EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
             "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
-            "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass"]
+            "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
+            "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
+            "bt_binary_linear_backward"]
 
 
 class BtError(RuntimeError):
@@ -164,6 +171,70 @@ def bt_conv2d_single_pass(B: int, C: int, H: int, W: int, kernel_size: int, stri
                           dilation: int, x_dtype: int, code: int) -> bool:
     """Whether bt_binary_conv2d unfolds x in one pass (as bt_pack_im2col)."""
     return bool(_c_single_pass(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype, code))
+
+
+def bt_backward_weight_ld(N: int) -> int:
+    return int(_c_bwd_ld(N))
+
+
+def bt_sign_transpose(w: torch.Tensor, ld: int | None = None, out: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """torch.sign of w [R, C], transposed to bf16 [C, ld] (zeros past R):
+    the weight operand of bt_binary_linear_backward (ld defaults to
+    bt_backward_weight_ld(R))."""
+    _contig(w, "w")
+    if w.dim() != 2:
+        raise ValueError("bt_sign_transpose wants a 2-D w")
+    R, C = w.shape
+    ld = bt_backward_weight_ld(R) if ld is None else ld
+    if out is None:
+        out = torch.empty((C, ld), dtype=torch.bfloat16, device=w.device)
+    _check(_c_sign_t(_ptr(w), _DT[w.dtype], R, C, ld, _ptr(out), _stream(stream)))
+    return out
+
+
+def bt_binary_linear_backward_workspace(M: int, N: int, K: int, want_grad_weight: bool = True) -> int:
+    return int(_c_bwd_ws(M, N, K, 1 if want_grad_weight else 0))
+
+
+def bt_binary_linear_backward(x: torch.Tensor, wst: torch.Tensor | None, g: torch.Tensor, scale_a: float,
+                              scale_w: float, grad_input: bool = True, grad_weight_dtype=torch.bfloat16,
+                              grad_x: torch.Tensor | None = None, grad_scale_a: torch.Tensor | None = None,
+                              grad_w: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                              stream=None):
+    """Straight-through backward of the binary linear layer for upstream
+    gradient g [M, N] (bf16) and forward input x [M, K] (bf16 or f32):
+    returns (grad_x [M, K] bf16, grad_scale_a (device float tensor),
+    grad_w [N, K]); grad_x / grad_scale_a are None unless grad_input,
+    grad_w is None when grad_weight_dtype is None. wst is
+    bt_sign_transpose(W)."""
+    _contig(x, "x")
+    _contig(g, "g")
+    M, K = x.shape
+    N = g.shape[1]
+    if g.shape[0] != M:
+        raise ValueError("g and x disagree on M")
+    if grad_input:
+        if wst is None:
+            raise ValueError("grad_input needs wst = bt_sign_transpose(W)")
+        _contig(wst, "wst")
+        if grad_x is None:
+            grad_x = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+        if grad_scale_a is None:
+            grad_scale_a = torch.empty((), dtype=torch.float32, device=x.device)
+    else:
+        grad_x = grad_scale_a = None
+    if grad_weight_dtype is not None and grad_w is None:
+        grad_w = torch.empty((N, K), dtype=grad_weight_dtype, device=x.device)
+    elif grad_weight_dtype is None:
+        grad_w = None
+    ws = _workspace(bt_binary_linear_backward_workspace(M, N, K, grad_w is not None), x.device, workspace)
+    ldw = wst.shape[1] if (grad_input and wst is not None) else 0
+    _check(_c_bwd(_ptr(x), _DT[x.dtype], _ptr(wst) if grad_input else None, ldw, _ptr(g), M, N, K, scale_a,
+                  scale_w, _ptr(grad_x), _ptr(grad_scale_a), _ptr(grad_w),
+                  _DT[grad_w.dtype] if grad_w is not None else BT_BF16, _ptr(ws),
+                  0 if ws is None else ws.numel(), _stream(stream)))
+    return grad_x, grad_scale_a, grad_w
 
 
 def bt_binary_linear_workspace(M: int, K: int, x_dtype: int, code: int) -> int:

@@ -1,0 +1,206 @@
+// Straight-through backward of the binary linear layer (bitorch-engine
+// BinaryLinearForward.backward, whose steps BinaryConv2dForward.backward
+// writes out for the convolution):
+//   grad_input  = bf16(g @ bf16(sign(w) * scale_w)), zeroed where x / scale_a
+//                 (in x's dtype) lies outside [-1, 1]
+//   grad_scale_a = sum(grad_input * sign(x) / sqrt(numel(x)))
+//   grad_weight = bf16(g^T @ bf16(sign(x) * scale_a))
+// Both products run on the tensor cores (tcgen05 kind::f16, bf16 operands,
+// fp32 accumulators) through the contraction kernel of tc_gemm.cu. Its
+// operands are K-major rows, so the products take:
+//   input gradient   A = g [M, N] as is, B = sign(w)^T [K, N] (built once
+//                    per weight by bt_sign_transpose); the scale, the rounding
+//                    to bf16, the mask and the grad_scale_a terms are fused
+//                    into the epilogue;
+//   weight gradient  A = g^T [N, M], B = sign(x)^T [K, M], both transposed
+//                    here into the workspace.
+// sign(v) is torch.sign: (v > 0) - (v < 0), so 0 for zeros and NaN. A +-1 or 0
+// operand times a bf16 scale is the page's bf16(sign * scale): the scale is
+// rounded to bf16 once on the host and applied to the fp32 sums.
+#include <cmath>
+#include <cstring>
+
+#include <cuda_bf16.h>
+
+#include "bt_device.cuh"
+#include "bt_internal.h"
+
+namespace bt {
+namespace {
+
+constexpr int kTile = 64;           // transpose tile: 64 x 64 elements
+constexpr int kTThreads = 256;
+
+__device__ float g_scale_sink;      // grad_scale_a terms when the caller does not want them
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+
+__device__ __forceinline__ uint16_t sign_bf16(float v) {
+    return v > 0.0f ? uint16_t(0x3F80) : (v < 0.0f ? uint16_t(0xBF80) : uint16_t(0));
+}
+
+// out[c * ldo + r] = f(in[r * C + c]) for a 64 x 64 tile, through shared
+// memory: reads run along c, writes along r, both coalesced. Rows r in
+// [R, ldo) are written as 0.
+template <typename T, bool SIGN>
+__global__ void __launch_bounds__(kTThreads) transpose_kernel(const T *__restrict__ in, int64_t R, int64_t C,
+                                                              int64_t ldo, uint16_t *__restrict__ out) {
+    __shared__ uint16_t tile[kTile][kTile + 2];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
+    for (int i = threadIdx.x; i < kTile * kTile; i += kTThreads) {
+        const int rr = i / kTile, cc = i % kTile;
+        const int64_t r = r0 + rr, c = c0 + cc;
+        uint16_t v = 0;
+        if (r < R && c < C) {
+            const T x = in[r * C + c];
+            if constexpr (SIGN) v = sign_bf16(to_f32<T>(x));
+            else v = *reinterpret_cast<const uint16_t *>(&x);
+        }
+        tile[rr][cc] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kTile * kTile; i += kTThreads) {
+        const int cc = i / kTile, rr = i % kTile;
+        const int64_t r = r0 + rr, c = c0 + cc;
+        if (c < C && r < ldo) out[c * ldo + r] = tile[rr][cc];
+    }
+}
+
+template <typename T, bool SIGN>
+cudaError_t transpose_t(const void *in, int64_t R, int64_t C, int64_t ldo, uint16_t *out, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute pdl = pdl_attribute();
+    cfg.gridDim = dim3(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((ldo + kTile - 1) / kTile));
+    cfg.blockDim = dim3(kTThreads);
+    cfg.stream = s;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, transpose_kernel<T, SIGN>, static_cast<const T *>(in), R, C, ldo, out);
+}
+
+// Round a float to the nearest bf16 value (ties to even) on the host.
+float bf16_round_host(float v) {
+    uint32_t u;
+    std::memcpy(&u, &v, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u) return v;                  // inf / NaN unchanged
+    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    float r;
+    std::memcpy(&r, &u, 4);
+    return r;
+}
+
+int64_t round_up64(int64_t v) { return (v + 63) / 64 * 64; }
+size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+cudaError_t launch_transpose_bf16(const void *in, bt_dtype in_t, int64_t R, int64_t C, int64_t ldo, bool sign,
+                                  uint16_t *out, cudaStream_t s) {
+    if (R == 0 || C == 0) return cudaSuccess;
+    if (C > (int64_t(65535) * kTile) || ldo > (int64_t(65535) * kTile)) return cudaErrorInvalidValue;
+    if (!sign) return transpose_t<__nv_bfloat16, false>(in, R, C, ldo, out, s);
+    switch (in_t) {
+        case BT_F32: return transpose_t<float, true>(in, R, C, ldo, out, s);
+        case BT_F16: return transpose_t<__half, true>(in, R, C, ldo, out, s);
+        default: return transpose_t<__nv_bfloat16, true>(in, R, C, ldo, out, s);
+    }
+}
+
+}  // namespace bt
+
+using namespace bt;
+
+namespace {
+bool finite_pos(float v) { return std::isfinite(v) && v > 0.0f; }
+bt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BT_OK : BT_ERR_CUDA; }
+}  // namespace
+
+extern "C" {
+
+int64_t bt_backward_weight_ld(int64_t N) { return N < 0 ? -1 : round_up64(N); }
+
+bt_status bt_sign_transpose(const void *w, bt_dtype w_dtype, int64_t R, int64_t C, int64_t ld, void *out,
+                            bt_stream stream) {
+    if (w_dtype != BT_F32 && w_dtype != BT_BF16 && w_dtype != BT_F16) return BT_ERR_INVALID_ARG;
+    if (R < 0 || C < 0 || ld < R || ld % 8 != 0) return BT_ERR_INVALID_ARG;
+    if (C > (int64_t(65535) * 64) || ld > (int64_t(65535) * 64)) return BT_ERR_UNSUPPORTED;
+    if (R == 0 || C == 0) return BT_OK;
+    if (w == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(out, 16)) return BT_ERR_ALIGNMENT;
+    return cuda_status(launch_transpose_bf16(w, w_dtype, R, C, ld, true, static_cast<uint16_t *>(out),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t bt_binary_linear_backward_workspace(int64_t M, int64_t N, int64_t K, int want_grad_weight) {
+    if (M < 0 || N < 0 || K < 0 || !want_grad_weight) return 0;
+    const int64_t ldm = round_up64(M);
+    return round_up256(static_cast<size_t>(N * ldm * 2)) + round_up256(static_cast<size_t>(K * ldm * 2));
+}
+
+bt_status bt_binary_linear_backward(const void *x, bt_dtype x_dtype, const void *wst, int64_t ldw, const void *g,
+                                    int64_t M, int64_t N, int64_t K, float scale_a, float scale_w, void *grad_x,
+                                    float *grad_scale_a, void *grad_w, bt_dtype grad_w_dtype, void *workspace,
+                                    size_t workspace_bytes, bt_stream stream) {
+    if (x_dtype != BT_BF16 && x_dtype != BT_F32) return BT_ERR_INVALID_ARG;
+    if (grad_w != nullptr && grad_w_dtype != BT_BF16 && grad_w_dtype != BT_F32) return BT_ERR_INVALID_ARG;
+    if (M < 0 || N < 1 || K < 1 || !finite_pos(scale_a) || !finite_pos(scale_w)) return BT_ERR_INVALID_ARG;
+    if (N % 8 != 0 || K % 8 != 0) return BT_ERR_UNSUPPORTED;
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return BT_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (M == 0) {
+        // empty batch (grad_x is empty too): the sum is zero, grad_w = 0
+        if (grad_scale_a != nullptr && cudaMemsetAsync(grad_scale_a, 0, sizeof(float), s) != cudaSuccess) return BT_ERR_CUDA;
+        if (grad_w != nullptr &&
+            cudaMemsetAsync(grad_w, 0, static_cast<size_t>(N * K) * (grad_w_dtype == BT_F32 ? 4 : 2), s) != cudaSuccess)
+            return BT_ERR_CUDA;
+        return BT_OK;
+    }
+    if (grad_scale_a != nullptr && grad_x == nullptr) return BT_ERR_INVALID_ARG;
+    if (grad_x != nullptr && (wst == nullptr || ldw < N || ldw % 8 != 0)) return BT_ERR_INVALID_ARG;
+    if (x == nullptr || g == nullptr) return BT_ERR_INVALID_ARG;
+    if (!tc_available()) return BT_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(g, 16) || (wst && !aligned(wst, 16)) || (grad_x && !aligned(grad_x, 16)) ||
+        (grad_w && !aligned(grad_w, 16)) || (grad_scale_a && !aligned(grad_scale_a, 4)))
+        return BT_ERR_ALIGNMENT;
+    const size_t need = bt_binary_linear_backward_workspace(M, N, K, grad_w != nullptr);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return BT_ERR_WORKSPACE;
+    if (need > 0 && !aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
+    unsigned int *err = device_error_word();
+    if (err == nullptr) return BT_ERR_CUDA;
+
+    if (grad_x != nullptr) {
+        float *sum = grad_scale_a;
+        if (sum == nullptr) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_scale_sink) != cudaSuccess) return BT_ERR_CUDA;
+            sum = static_cast<float *>(p);
+        }
+        if (cudaMemsetAsync(sum, 0, sizeof(float), s) != cudaSuccess) return BT_ERR_CUDA;
+        TcMask mk{x, x_dtype, scale_a, static_cast<float>(1.0 / std::sqrt(static_cast<double>(M) * static_cast<double>(K))),
+                  sum};
+        const cudaError_t e = launch_tc_bf16(static_cast<const uint16_t *>(g), N, static_cast<const uint16_t *>(wst), ldw,
+                                             M, K, N, bf16_round_host(scale_w), grad_x, BT_BF16, &mk, err, s);
+        if (e != cudaSuccess) return BT_ERR_CUDA;
+    }
+    if (grad_w != nullptr) {
+        const int64_t ldm = round_up64(M);
+        uint16_t *gt = static_cast<uint16_t *>(workspace);
+        uint16_t *xst = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(workspace) +
+                                                     round_up256(static_cast<size_t>(N * ldm * 2)));
+        if (launch_transpose_bf16(g, BT_BF16, M, N, ldm, false, gt, s) != cudaSuccess ||
+            launch_transpose_bf16(x, x_dtype, M, K, ldm, true, xst, s) != cudaSuccess)
+            return BT_ERR_CUDA;
+        // the contraction runs over the zero-padded length ldm: the pads add 0
+        const cudaError_t e = launch_tc_bf16(gt, ldm, xst, ldm, N, K, ldm, bf16_round_host(scale_a), grad_w,
+                                             grad_w_dtype, nullptr, err, s);
+        if (e != cudaSuccess) return BT_ERR_CUDA;
+    }
+    return BT_OK;
+}
+
+}  // extern "C"

@@ -74,6 +74,36 @@ cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code,
                            float alpha, void *out, bt_dtype out_t, unsigned int *err,
                            cudaStream_t s);
 
+// bf16 x bf16 contraction on the tensor cores (tcgen05 kind::f16, fp32
+// accumulators), for the backward's products: a code value beside bt_code's.
+constexpr int kCodeBF16 = 3;
+
+// Straight-through mask applied by the bf16 contraction's epilogue: the
+// output D [M, N] (bf16) is multiplied by middle = !(q < -1 || q > 1), q =
+// x / scale_a rounded to x's dtype, x [M, N] of type x_t (BF16 or F32, row
+// pitch N); and sum over D * sign(x) * norm is added to *sum (fp32 atomics).
+struct TcMask {
+    const void *x;
+    bt_dtype x_t;
+    float scale_a;
+    float norm;
+    float *sum;
+};
+
+// D[r, c] = alpha * sum_j A[r, j] * B[c, j] over bf16 rows: A [M, klen] with a
+// row pitch of lda elements, B [N, klen] with pitch ldb; D row-major [M, N]
+// (bf16 or f32; rounded to bf16 before any mask). klen, lda, ldb multiples
+// of 8; with a mask, N a multiple of 8 and out 16-byte aligned.
+cudaError_t launch_tc_bf16(const uint16_t *a, int64_t lda, const uint16_t *b, int64_t ldb, int64_t M, int64_t N,
+                           int64_t klen, float alpha, void *out, bt_dtype out_t, const TcMask *mask,
+                           unsigned int *err, cudaStream_t s);
+
+// out[c * ldo + r] = f(in[r * C + c]) as bf16 for r < R, c < C, and 0 for
+// R <= r < ldo: f = torch.sign (sign = true; in of type in_t) or the value
+// itself (sign = false; in bf16).
+cudaError_t launch_transpose_bf16(const void *in, bt_dtype in_t, int64_t R, int64_t C, int64_t ldo, bool sign,
+                                  uint16_t *out, cudaStream_t s);
+
 // True when this build carries the tensor-core kernels.
 bool tc_available();
 

@@ -77,7 +77,9 @@ constexpr int kStagingBytes = kEpiWarps * kBoxBytes;   // one box per epilogue w
 constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
 constexpr int kMaxStages = 8;
 
-enum Layout { kRowsOut = 0, kNchwOut = 1 };
+// Output layouts: row-major; NCHW (convolution); row-major times the
+// straight-through mask of x (bf16 or f32 x), for the backward's input gradient.
+enum Layout { kRowsOut = 0, kNchwOut = 1, kRowsMaskBf16 = 2, kRowsMaskF32 = 3 };
 
 struct TcArgs {
     int64_t M, N;              // D is M x N
@@ -95,6 +97,10 @@ struct TcArgs {
                                // NCHW: bytes each lane stores at once (a run of one channel's pixels)
     int64_t hw;                // NCHW: output pixels per image (Ho * Wo)
     int stages;                // smem ring depth
+    const void *aux;           // masked layouts: x [M, N]
+    float aux_scale;           // masked layouts: scale_a
+    float aux_norm;            // masked layouts: 1 / sqrt(numel(x)), fp32
+    float *aux_sum;            // masked layouts: sum(D * sign(x) * norm) accumulates here
 };
 
 // B rows one CTA holds per slice.
@@ -114,8 +120,9 @@ template <int CODE> __host__ __device__ constexpr uint32_t acc_stride() { return
 
 // Instruction descriptor: D = F32, K-major A and B, M rows (128, or 256 for a
 // pair), N = bn.
-uint32_t make_idesc(bt_code code, int m, int bn) {
+uint32_t make_idesc(int code, int m, int bn) {
     const uint32_t mn = ((static_cast<uint32_t>(bn) >> 3) << 17) | ((static_cast<uint32_t>(m) >> 4) << 24);
+    if (code == kCodeBF16) return (1u << 4) | (1u << 7) | (1u << 10) | mn;          // BF16 x BF16 -> F32
     if (code == BT_CODE_E4M3) return (1u << 4) | (0u << 7) | (0u << 10) | mn;       // E4M3 x E4M3
     return (1u << 7) | (1u << 10) | (1u << 23) | mn;   // block-scaled E2M1 x E2M1, UE8M0 scales, ids 0
 }
@@ -205,6 +212,40 @@ __device__ __forceinline__ void nchw_box(uint8_t *out, uint32_t sbox, int lane, 
         if (row0 + lane / kLpr + i * kRowsPer >= M) break;
         st_global<V>(p + static_cast<int64_t>(i * kRowsPer) * plane, v[i]);
     }
+}
+
+// One 16-byte chunk of eight bf16 outputs y at x[idx .. idx + 8): each
+// becomes y * middle, middle = !(q < -1 || q > 1) for q = x / scale_a in x's
+// dtype, and sum(y * middle * sign(x) * norm) (each product rounded to fp32)
+// is added to tsum. sign(x) = (x > 0) - (x < 0).
+template <int LAYOUT>
+__device__ __forceinline__ uint4 mask_chunk(const uint4 &v, const void *x, int64_t idx, float scale_a, float norm,
+                                            float &tsum) {
+    float xf[8];
+    if constexpr (LAYOUT == kRowsMaskBf16) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + idx));
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xf[e] = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+    } else {
+        const float4 x0 = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + idx));
+        const float4 x1 = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + idx + 4));
+        xf[0] = x0.x; xf[1] = x0.y; xf[2] = x0.z; xf[3] = x0.w;
+        xf[4] = x1.x; xf[5] = x1.y; xf[6] = x1.z; xf[7] = x1.w;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float y = __uint_as_float(((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+        float q = __fdiv_rn(xf[e], scale_a);
+        if constexpr (LAYOUT == kRowsMaskBf16) q = __bfloat162float(__float2bfloat16_rn(q));
+        const float ym = __fmul_rn(y, (q < -1.0f || q > 1.0f) ? 0.0f : 1.0f);
+        const float sg = (xf[e] > 0.0f ? 1.0f : 0.0f) - (xf[e] < 0.0f ? 1.0f : 0.0f);
+        tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(ym, sg), norm));
+        o[e >> 1] |= (__float_as_uint(ym) >> 16) << (16 * (e & 1));        // ym is y or +-0: exact in bf16
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <int CODE, int LAYOUT, int OUT, bool PAIR>
@@ -388,10 +429,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                             const uint64_t bd = tc::sw128_kmajor_desc(sB + s * kBStage + i * kBSlice + kk * 32);
                             const uint32_t acc = (kb | i | kk) != 0 ? 1u : 0u;
                             if (PAIR) {
-                                if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4_pair(dacc, ad, bd, a.idesc, acc);
+                                if (CODE == kCodeBF16) tc::mma_f16_pair(dacc, ad, bd, a.idesc, acc);
+                                else if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4_pair(dacc, ad, bd, a.idesc, acc);
                                 else tc::mma_mxf4_pair(dacc, ad, bd, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
                             } else {
-                                if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, ad, bd, a.idesc, acc);
+                                if (CODE == kCodeBF16) tc::mma_f16(dacc, ad, bd, a.idesc, acc);
+                                else if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, ad, bd, a.idesc, acc);
                                 else tc::mma_mxf4(dacc, ad, bd, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
                             }
                         }
@@ -417,6 +460,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
         pdl_wait();                                       // the previous kernel may still use `out`
         T *out = static_cast<T *>(a.out);
         const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // this warp's staging box
+        constexpr bool kMask = LAYOUT == kRowsMaskBf16 || LAYOUT == kRowsMaskF32;
+        float tsum = 0.0f;                                // masked layouts: this lane's grad_scale_a terms
         int local = 0;
         for (int st = unit; st < a.num_super; st += nunits, ++local) {
             const int mt = st / a.num_n, nt = st % a.num_n;
@@ -489,10 +534,14 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                         uint8_t *p = reinterpret_cast<uint8_t *>(out) + (row * a.N + col) * kElem;
 #pragma unroll
                         for (int i = 0; i < kIters; ++i)
-                            if (row + i * kRowsPer < a.M)
+                            if (row + i * kRowsPer < a.M) {
+                                if constexpr (kMask)
+                                    v[i] = mask_chunk<LAYOUT>(v[i], a.aux, (row + i * kRowsPer) * a.N + col, a.aux_scale,
+                                                              a.aux_norm, tsum);
                                 st_stream_v4(p + static_cast<int64_t>(i * kRowsPer) * a.N * kElem, v[i]);
+                            }
                     }
-                } else {
+                } else if constexpr (!kMask) {
                     // ragged N: read the box back one row at a time, lanes along
                     // the columns, so every store is 32 consecutive elements
                     const int64_t col = n0 + c0 + lane;
@@ -530,6 +579,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
             }
             if (!released) release();
         }
+        if constexpr (kMask) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xFFFFFFFFu, tsum, o);
+            if (lane == 0) atomicAdd(a.aux_sum, tsum);
+        }
     }
 
     tc::fence_before_sync();
@@ -563,29 +617,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 
 int sm_count() { return device_sm_count(); }
 
-// Views of a byte matrix [rows, row_bytes] (row pitch = row_bytes), 128-byte
-// swizzle, zero fill outside:
+// Views of a byte matrix [rows, row_bytes] (row pitch `pitch` >= row_bytes,
+// both multiples of 16), 128-byte swizzle, zero fill outside:
 //   2-D {row_bytes, rows}, box 128 bytes x box_rows;
-//   3-D {128, rows, full slices} (strides row_bytes, 128), box 128 x box_rows
-//   x d: d consecutive whole K slices in one copy, landing slice after slice.
-bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+//   3-D {128, rows, full slices} (strides pitch, 128), box 128 x box_rows x
+//   d: d consecutive whole K slices in one copy, landing slice after slice.
+bool map_2d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t pitch, uint64_t rows, uint32_t box_rows) {
     auto fn = encode_tiled();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {row_bytes, rows};
-    cuuint64_t strides[1] = {row_bytes};
+    cuuint64_t strides[1] = {pitch};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kRowB), box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-bool map_3d(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows, uint64_t full_slices,
+bool map_3d(CUtensorMap *m, const void *ptr, uint64_t pitch, uint64_t rows, uint64_t full_slices,
             uint32_t box_rows, uint32_t d) {
     auto fn = encode_tiled();
     if (fn == nullptr) return false;
     // rows without a whole slice never use this view: encode a one-row stand-in
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kRowB), full_slices > 0 ? rows : 1, full_slices > 0 ? full_slices : 1};
-    cuuint64_t strides[2] = {full_slices > 0 ? row_bytes : static_cast<cuuint64_t>(kRowB), static_cast<cuuint64_t>(kRowB)};
+    cuuint64_t strides[2] = {full_slices > 0 ? pitch : static_cast<cuuint64_t>(kRowB), static_cast<cuuint64_t>(kRowB)};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowB), box_rows, d};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
@@ -735,15 +789,17 @@ cudaError_t launch_code(bt_code code, bool pair, const Maps &mp, const TcArgs &a
 int out_elem_bytes(bt_dtype t) { return t == BT_BF16 || t == BT_F16 ? 2 : 4; }
 
 // Plan the tiles of an M x N contraction over rows of rb bytes (a multiple of
-// 64) and encode the maps.
-bool plan(TcArgs &a, Maps &mp, TileCfg &c, bt_code code, const uint8_t *ap, const uint8_t *bp, int64_t M, int64_t N,
-          int64_t rb) {
-    if (rb % 64 != 0 || M > (int64_t(1) << 31) - 512 || N > (int64_t(1) << 31) - 512) return false;
+// 16; A and B rows pitch_a and pitch_b bytes apart) and encode the maps.
+bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const uint8_t *bp, int64_t M, int64_t N,
+          int64_t rb, int64_t pitch_a, int64_t pitch_b) {
+    if (rb % 16 != 0 || pitch_a % 16 != 0 || pitch_b % 16 != 0 || pitch_a < rb || pitch_b < rb ||
+        M > (int64_t(1) << 31) - 512 || N > (int64_t(1) << 31) - 512)
+        return false;
     a.M = M;
     a.N = N;
     a.slices = static_cast<int>((rb + kRowB - 1) / kRowB);
     a.full_slices = static_cast<int>(rb / kRowB);
-    const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;
+    const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;       // E2M1 keeps 32 TMEM columns for block scales
     c = choose_cfg(M, N, a.slices, sm_count(), max_bn);
     a.bn = c.bn;
     a.d = c.d;
@@ -755,12 +811,12 @@ bool plan(TcArgs &a, Maps &mp, TileCfg &c, bt_code code, const uint8_t *ap, cons
     a.num_super = static_cast<int>(num_m * num_n);
     a.idesc = make_idesc(code, rows, a.bn);
     const uint32_t b_box = static_cast<uint32_t>(b_slot_rows(a.bn, c.pair));
-    return map_3d(&mp.a3, ap, static_cast<uint64_t>(rb), static_cast<uint64_t>(M), static_cast<uint64_t>(a.full_slices),
-                  kBM, static_cast<uint32_t>(a.d)) &&
-           map_3d(&mp.b3, bp, static_cast<uint64_t>(rb), static_cast<uint64_t>(N), static_cast<uint64_t>(a.full_slices),
-                  b_box, static_cast<uint32_t>(a.d)) &&
-           map_2d(&mp.a2, ap, static_cast<uint64_t>(rb), static_cast<uint64_t>(M), kBM) &&
-           map_2d(&mp.b2, bp, static_cast<uint64_t>(rb), static_cast<uint64_t>(N), b_box);
+    return map_3d(&mp.a3, ap, static_cast<uint64_t>(pitch_a), static_cast<uint64_t>(M),
+                  static_cast<uint64_t>(a.full_slices), kBM, static_cast<uint32_t>(a.d)) &&
+           map_3d(&mp.b3, bp, static_cast<uint64_t>(pitch_b), static_cast<uint64_t>(N),
+                  static_cast<uint64_t>(a.full_slices), b_box, static_cast<uint32_t>(a.d)) &&
+           map_2d(&mp.a2, ap, static_cast<uint64_t>(rb), static_cast<uint64_t>(pitch_a), static_cast<uint64_t>(M), kBM) &&
+           map_2d(&mp.b2, bp, static_cast<uint64_t>(rb), static_cast<uint64_t>(pitch_b), static_cast<uint64_t>(N), b_box);
 }
 
 }  // namespace
@@ -774,7 +830,8 @@ cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code,
     TcArgs a{};
     Maps mp;
     TileCfg c;
-    if (!plan(a, mp, c, code, xp, wp, M, N, row_bytes(K, code))) return cudaErrorInvalidValue;
+    const int64_t rb = row_bytes(K, code);
+    if (!plan(a, mp, c, code, xp, wp, M, N, rb, rb, rb)) return cudaErrorInvalidValue;
     a.alpha = alpha;
     a.out = out;
     a.err = err;
@@ -790,7 +847,7 @@ cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code,
     TcArgs a{};
     Maps mp;
     TileCfg c;
-    if (!plan(a, mp, c, code, wp, rows, g.O, g.B * g.Ho * g.Wo, krow)) return cudaErrorInvalidValue;
+    if (!plan(a, mp, c, code, wp, rows, g.O, g.B * g.Ho * g.Wo, krow, krow, krow)) return cudaErrorInvalidValue;
     a.alpha = alpha;
     a.out = out;
     a.err = err;
@@ -803,6 +860,40 @@ cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code,
         if ((a.hw * eb) % v == 0 && aligned(out, static_cast<size_t>(v))) { a.vec = v; break; }
     }
     return launch_code<kNchwOut>(code, c.pair, mp, a, out_t, s);
+}
+
+// bf16 contractions: row-major output (bf16 or f32), or bf16 times the mask.
+namespace {
+template <int LAYOUT, int OUT>
+cudaError_t launch_bf16_t(bool pair, const Maps &mp, const TcArgs &a, cudaStream_t s) {
+    return pair ? launch_t<kCodeBF16, LAYOUT, OUT, true>(mp, a, s) : launch_t<kCodeBF16, LAYOUT, OUT, false>(mp, a, s);
+}
+}  // namespace
+
+cudaError_t launch_tc_bf16(const uint16_t *a_ptr, int64_t lda, const uint16_t *b_ptr, int64_t ldb, int64_t M,
+                           int64_t N, int64_t klen, float alpha, void *out, bt_dtype out_t, const TcMask *mask,
+                           unsigned int *err, cudaStream_t s) {
+    TcArgs a{};
+    Maps mp;
+    TileCfg c;
+    if (!plan(a, mp, c, kCodeBF16, reinterpret_cast<const uint8_t *>(a_ptr), reinterpret_cast<const uint8_t *>(b_ptr),
+              M, N, klen * 2, lda * 2, ldb * 2))
+        return cudaErrorInvalidValue;
+    a.alpha = alpha;
+    a.out = out;
+    a.err = err;
+    a.vec = ((N * out_elem_bytes(out_t)) % 16 == 0) && aligned(out, 16) ? 1 : 0;
+    if (mask != nullptr) {
+        if (out_t != BT_BF16 || !a.vec || N % 8 != 0 || !aligned(mask->x, 16)) return cudaErrorInvalidValue;
+        a.aux = mask->x;
+        a.aux_scale = mask->scale_a;
+        a.aux_norm = mask->norm;
+        a.aux_sum = mask->sum;
+        return mask->x_t == BT_F32 ? launch_bf16_t<kRowsMaskF32, BT_BF16>(c.pair, mp, a, s)
+                                   : launch_bf16_t<kRowsMaskBf16, BT_BF16>(c.pair, mp, a, s);
+    }
+    return out_t == BT_F32 ? launch_bf16_t<kRowsOut, BT_F32>(c.pair, mp, a, s)
+                           : launch_bf16_t<kRowsOut, BT_BF16>(c.pair, mp, a, s);
 }
 
 }  // namespace bt
