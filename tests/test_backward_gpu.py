@@ -137,6 +137,19 @@ def test_linear_backward_sign_transpose():
     assert torch.equal(got32[:, :300], want[:, :300]) and torch.all(got32[:, 300:] == 0)
 
 
+@pytest.mark.parametrize("R,C,dtype", [(300, 136, torch.float16), (77, 13, torch.bfloat16), (1030, 72, torch.float32),
+                                       (9, 8, torch.float16), (513, 264, torch.bfloat16)])
+def test_sign_transpose_shapes_and_special_values(R, C, dtype):
+    w = torch.randn(R, C, generator=torch.Generator().manual_seed(R * C)).to(dtype)
+    specials = torch.tensor([0.0, -0.0, float("nan"), float("inf"), -float("inf"), -1e-3, 1e-3])
+    w.view(-1)[: specials.numel()] = specials.to(dtype)[: w.numel()]
+    ld = bt.bt_backward_weight_ld(R)
+    got = bt.bt_sign_transpose(w.to(DEV)).cpu()
+    want = torch.zeros(C, ld, dtype=torch.bfloat16)
+    want[:, :R] = torch.from_numpy(oracle.sign(w.float().numpy())).t().to(torch.bfloat16)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
 def test_linear_backward_partial_requests_and_empty():
     x, w, g, sa, sw = _inputs(130, 64, 96, torch.bfloat16, 3)
     wst = bt.bt_sign_transpose(w.to(DEV))

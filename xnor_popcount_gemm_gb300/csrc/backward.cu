@@ -19,6 +19,7 @@
 // rounded to bf16 once on the host and applied to the fp32 sums.
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -71,15 +72,111 @@ __global__ void __launch_bounds__(kTThreads) transpose_kernel(const T *__restric
     }
 }
 
+// torch.sign of two 16-bit values (bf16, or f16 when F16) packed in a word,
+// as bf16: 0x3F80 / 0xBF80, 0 for +-0 and NaN (magnitude bits above those of
+// infinity).
+template <bool F16>
+__device__ __forceinline__ uint32_t sign_pair_bf16(uint32_t w) {
+    constexpr uint32_t kInf = F16 ? 0x7C00u : 0x7F80u;
+    uint32_t r = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t v = (w >> (16 * h)) & 0xFFFFu, mag = v & 0x7FFFu;
+        const uint32_t sg = (mag == 0u || mag > kInf) ? 0u : (0x3F80u | (v & 0x8000u));
+        r |= sg << (16 * h);
+    }
+    return r;
+}
+
+// Wide form: each thread moves an 8 x 8 block (8 input rows of 16 bytes in,
+// 8 output rows of 16 bytes out); a warp covers 32 rows x 64 columns of the
+// input, a 256-thread block 256 x 64. Loads of one warp instruction cover
+// four whole 128-byte row segments. In registers, one pass of byte permutes
+// pairs rows 2i and 2i+1 column by column; output row 2w + p is then the
+// words (w, rows 0..7 in pairs) picked out of the 32 registers.
+// Needs C a multiple of 8 (bf16) or 4 (f32) and ldo a multiple of 8.
+template <typename T, bool SIGN>
+__global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restrict__ in, int64_t R, int64_t C,
+                                                               int64_t ldo, uint16_t *__restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tc = threadIdx.x & 7, tr = threadIdx.x >> 3;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64 + 8 * tc;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 256 + 8 * tr;
+    if (c0 >= C || r0 >= ldo) return;
+    const bool cfull = c0 + 8 <= C;
+    uint32_t W[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = r0 + i;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (r < R) {
+            if constexpr (sizeof(T) == 2) {
+                if (cfull) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(in + r * C + c0));
+                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                } else {
+                    const uint16_t *p = reinterpret_cast<const uint16_t *>(in + r * C);
+                    for (int e = 0; c0 + e < C; ++e) w[e >> 1] |= static_cast<uint32_t>(p[c0 + e]) << (16 * (e & 1));
+                }
+                if constexpr (SIGN) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) w[k] = sign_pair_bf16<std::is_same<T, __half>::value>(w[k]);
+                }
+            } else {
+                float f[8];
+                if (cfull) {
+                    const float4 a = __ldg(reinterpret_cast<const float4 *>(in + r * C + c0));
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(in + r * C + c0 + 4));
+                    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = c0 + e < C ? in[r * C + c0 + e] : 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e >> 1] |= static_cast<uint32_t>(sign_bf16(f[e])) << (16 * (e & 1));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) W[i][k] = w[k];
+    }
+    // rows 2i, 2i+1: X[2i][w] = (M[2i][2w], M[2i+1][2w]), X[2i+1][w] = (.., 2w+1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t a = W[2 * i][k], b = W[2 * i + 1][k];
+            W[2 * i][k] = __byte_perm(a, b, 0x5410);
+            W[2 * i + 1][k] = __byte_perm(a, b, 0x7632);
+        }
+    }
+    // output row c0 + 2w + p holds rows r0 .. r0 + 7: words X[2v + p][w], v = 0..3
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int64_t c = c0 + 2 * w + p;
+            if (c < C)
+                *reinterpret_cast<uint4 *>(out + c * ldo + r0) =
+                    make_uint4(W[p][w], W[2 + p][w], W[4 + p][w], W[6 + p][w]);
+        }
+    }
+}
+
 template <typename T, bool SIGN>
 cudaError_t transpose_t(const void *in, int64_t R, int64_t C, int64_t ldo, uint16_t *out, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute pdl = pdl_attribute();
-    cfg.gridDim = dim3(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((ldo + kTile - 1) / kTile));
     cfg.blockDim = dim3(kTThreads);
     cfg.stream = s;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
+    const bool wide = ldo % 8 == 0 && aligned(in, 16) && aligned(out, 16) && (C * static_cast<int64_t>(sizeof(T))) % 16 == 0;
+    if (wide && (ldo + 255) / 256 <= 65535) {
+        cfg.gridDim = dim3(static_cast<unsigned>((C + 63) / 64), static_cast<unsigned>((ldo + 255) / 256));
+        return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN>, static_cast<const T *>(in), R, C, ldo, out);
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((ldo + kTile - 1) / kTile));
     return cudaLaunchKernelEx(&cfg, transpose_kernel<T, SIGN>, static_cast<const T *>(in), R, C, ldo, out);
 }
 
