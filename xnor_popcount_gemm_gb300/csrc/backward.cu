@@ -88,57 +88,66 @@ __device__ __forceinline__ uint32_t sign_pair_bf16(uint32_t w) {
     return r;
 }
 
-// Wide form: each thread moves an 8 x 8 block (8 input rows of 16 bytes in,
-// 8 output rows of 16 bytes out); a warp covers 32 rows x 64 columns of the
-// input, a 256-thread block 256 x 64. Loads of one warp instruction cover
-// four whole 128-byte row segments. In registers, one pass of byte permutes
-// pairs rows 2i and 2i+1 column by column; output row 2w + p is then the
-// words (w, rows 0..7 in pairs) picked out of the 32 registers.
-// Needs C a multiple of 8 (bf16) or 4 (f32) and ldo a multiple of 8.
+// Eight consecutive elements of a row as eight bf16 values: torch.sign of
+// them (SIGN) or the bf16 values themselves.
+template <typename T, bool SIGN>
+__device__ __forceinline__ uint4 load8_bf16(const T *p) {
+    uint32_t w[4];
+    if constexpr (sizeof(T) == 2) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        if constexpr (SIGN) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = sign_pair_bf16<std::is_same<T, __half>::value>(w[k]);
+        }
+    } else {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(sign_bf16(f[2 * k])) | (static_cast<uint32_t>(sign_bf16(f[2 * k + 1])) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Wide form: a 256-thread block moves a 128 x 128 tile through 32 KB of shared
+// memory. Loads: every thread takes eight 16-byte chunks (8 elements of a
+// row), all in flight at once; 16 threads cover a 256-byte row segment. The
+// chunk (row, q) is stored at chunk q ^ (row / 8 mod 16) of its 256-byte
+// shared row, so that both the stores here and the 8-row reads below spread
+// over all banks. Transpose: each thread reads an 8 x 8 block (8 rows of one
+// chunk), pairs rows 2i and 2i+1 column by column with byte permutes, and
+// writes output row 2w + p as the words (w, rows 0..7 in pairs) -- 16 bytes
+// per output row; 16 threads cover a 256-byte output row segment.
+// Needs C a multiple of 8 and ldo a multiple of 8.
 template <typename T, bool SIGN>
 __global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restrict__ in, int64_t R, int64_t C,
                                                                int64_t ldo, uint16_t *__restrict__ out) {
+    __shared__ uint4 tile[128 * 16];
     pdl_launch_dependents();
     pdl_wait();
-    const int tc = threadIdx.x & 7, tr = threadIdx.x >> 3;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64 + 8 * tc;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 256 + 8 * tr;
-    if (c0 >= C || r0 >= ldo) return;
-    const bool cfull = c0 + 8 <= C;
+    const int t = threadIdx.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int k = i * kTThreads + t, rr = k >> 4, q = k & 15;
+        const int64_t r = r0 + rr, c = c0 + 8 * q;
+        v[i] = (r < R && c < C) ? load8_bf16<T, SIGN>(in + r * C + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int k = i * kTThreads + t, rr = k >> 4, q = k & 15;
+        tile[rr * 16 + (q ^ ((rr >> 3) & 15))] = v[i];
+    }
+    __syncthreads();
+    const int br = t & 15, bc = t >> 4;
     uint32_t W[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int64_t r = r0 + i;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (r < R) {
-            if constexpr (sizeof(T) == 2) {
-                if (cfull) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(in + r * C + c0));
-                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-                } else {
-                    const uint16_t *p = reinterpret_cast<const uint16_t *>(in + r * C);
-                    for (int e = 0; c0 + e < C; ++e) w[e >> 1] |= static_cast<uint32_t>(p[c0 + e]) << (16 * (e & 1));
-                }
-                if constexpr (SIGN) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) w[k] = sign_pair_bf16<std::is_same<T, __half>::value>(w[k]);
-                }
-            } else {
-                float f[8];
-                if (cfull) {
-                    const float4 a = __ldg(reinterpret_cast<const float4 *>(in + r * C + c0));
-                    const float4 b = __ldg(reinterpret_cast<const float4 *>(in + r * C + c0 + 4));
-                    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = c0 + e < C ? in[r * C + c0 + e] : 0.0f;
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) w[e >> 1] |= static_cast<uint32_t>(sign_bf16(f[e])) << (16 * (e & 1));
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) W[i][k] = w[k];
+        const uint4 x = tile[(8 * br + i) * 16 + (bc ^ br)];
+        W[i][0] = x.x; W[i][1] = x.y; W[i][2] = x.z; W[i][3] = x.w;
     }
     // rows 2i, 2i+1: X[2i][w] = (M[2i][2w], M[2i+1][2w]), X[2i+1][w] = (.., 2w+1)
 #pragma unroll
@@ -150,15 +159,15 @@ __global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restri
             W[2 * i + 1][k] = __byte_perm(a, b, 0x7632);
         }
     }
-    // output row c0 + 2w + p holds rows r0 .. r0 + 7: words X[2v + p][w], v = 0..3
+    const int64_t rs = r0 + 8 * br;
+    if (rs >= ldo) return;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-            const int64_t c = c0 + 2 * w + p;
+            const int64_t c = c0 + 8 * bc + 2 * w + p;
             if (c < C)
-                *reinterpret_cast<uint4 *>(out + c * ldo + r0) =
-                    make_uint4(W[p][w], W[2 + p][w], W[4 + p][w], W[6 + p][w]);
+                *reinterpret_cast<uint4 *>(out + c * ldo + rs) = make_uint4(W[p][w], W[2 + p][w], W[4 + p][w], W[6 + p][w]);
         }
     }
 }
@@ -171,9 +180,9 @@ cudaError_t transpose_t(const void *in, int64_t R, int64_t C, int64_t ldo, uint1
     cfg.stream = s;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    const bool wide = ldo % 8 == 0 && aligned(in, 16) && aligned(out, 16) && (C * static_cast<int64_t>(sizeof(T))) % 16 == 0;
-    if (wide && (ldo + 255) / 256 <= 65535) {
-        cfg.gridDim = dim3(static_cast<unsigned>((C + 63) / 64), static_cast<unsigned>((ldo + 255) / 256));
+    const bool wide = ldo % 8 == 0 && C % 8 == 0 && aligned(in, 16) && aligned(out, 16);
+    if (wide && (ldo + 127) / 128 <= 65535) {
+        cfg.gridDim = dim3(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>((ldo + 127) / 128));
         return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN>, static_cast<const T *>(in), R, C, ldo, out);
     }
     cfg.gridDim = dim3(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((ldo + kTile - 1) / kTile));

@@ -218,29 +218,59 @@ __device__ __forceinline__ void nchw_box(uint8_t *out, uint32_t sbox, int lane, 
 // becomes y * middle, middle = !(q < -1 || q > 1) for q = x / scale_a in x's
 // dtype, and sum(y * middle * sign(x) * norm) (each product rounded to fp32)
 // is added to tsum. sign(x) = (x > 0) - (x < 0).
+// Whether q = x / scale_a (fp32 division, then rounded to bf16 for a bf16 x)
+// lies outside [-1, 1]. x * (1 / scale_a) is within a few ulps of x / scale_a,
+// so it decides every x whose quotient is not near the boundary (1 for an
+// f32 x; 1 + 2^-8, the point where bf16 rounding leaves 1, for a bf16 x); the
+// rest take the division.
+template <bool BF16X>
+__device__ __forceinline__ bool outside_unit(float x, float scale_a, float inv_scale) {
+    constexpr float kEdge = BF16X ? 1.00390625f : 1.0f;
+    const float qa = fabsf(x * inv_scale);
+    if (qa < kEdge * 0.99999f) return false;
+    if (qa > kEdge * 1.00001f) return true;
+    float q = __fdiv_rn(x, scale_a);
+    if constexpr (BF16X) q = __bfloat162float(__float2bfloat16_rn(q));
+    return q < -1.0f || q > 1.0f;
+}
+
+// Eight consecutive elements of x (bf16 or f32), loaded ahead of their use.
+template <int LAYOUT> struct XChunk {
+    uint4 a, b;
+    __device__ __forceinline__ void load(const void *x, int64_t idx) {
+        if constexpr (LAYOUT == kRowsMaskBf16) {
+            a = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + idx));
+        } else {
+            a = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(x) + idx));
+            b = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(x) + idx + 4));
+        }
+    }
+    __device__ __forceinline__ void to_f32(float (&xf)[8]) const {
+        if constexpr (LAYOUT == kRowsMaskBf16) {
+            const uint32_t xw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xf[e] = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+        } else {
+            const uint32_t xw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xf[e] = __uint_as_float(xw[e]);
+        }
+    }
+};
+
 template <int LAYOUT>
-__device__ __forceinline__ uint4 mask_chunk(const uint4 &v, const void *x, int64_t idx, float scale_a, float norm,
+__device__ __forceinline__ uint4 mask_chunk(const uint4 &v, const XChunk<LAYOUT> &xc, float scale_a, float norm,
                                             float &tsum) {
     float xf[8];
-    if constexpr (LAYOUT == kRowsMaskBf16) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + idx));
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xf[e] = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
-    } else {
-        const float4 x0 = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + idx));
-        const float4 x1 = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + idx + 4));
-        xf[0] = x0.x; xf[1] = x0.y; xf[2] = x0.z; xf[3] = x0.w;
-        xf[4] = x1.x; xf[5] = x1.y; xf[6] = x1.z; xf[7] = x1.w;
-    }
+    xc.to_f32(xf);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const float inv_scale = 1.0f / scale_a;
     uint32_t o[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const float y = __uint_as_float(((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
-        float q = __fdiv_rn(xf[e], scale_a);
-        if constexpr (LAYOUT == kRowsMaskBf16) q = __bfloat162float(__float2bfloat16_rn(q));
-        const float ym = __fmul_rn(y, (q < -1.0f || q > 1.0f) ? 0.0f : 1.0f);
+        const bool out = outside_unit<LAYOUT == kRowsMaskBf16>(xf[e], scale_a, inv_scale);
+        const float ym = __fmul_rn(y, out ? 0.0f : 1.0f);
         const float sg = (xf[e] > 0.0f ? 1.0f : 0.0f) - (xf[e] < 0.0f ? 1.0f : 0.0f);
         tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(ym, sg), norm));
         o[e >> 1] |= (__float_as_uint(ym) >> 16) << (16 * (e & 1));        // ym is y or +-0: exact in bf16
@@ -492,6 +522,19 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
             auto tcol_of = [&](int j) { return tbase + static_cast<uint32_t>(32 * (2 * j + half)); };
             auto emit = [&](const uint32_t (&r)[32], int j) {
                 const int c0 = 32 * (2 * j + half);
+                // masked layouts: this lane's x chunks (the rows and columns of the
+                // 16-byte chunks it stores below) go in flight before the staging
+                XChunk<LAYOUT == kRowsMaskF32 ? kRowsMaskF32 : kRowsMaskBf16> xc[4];
+                if constexpr (kMask) {
+                    constexpr int kCh = kBoxInner / 16, kRp = 32 / kCh;
+                    static_assert(32 / kRp <= 4, "x chunks per lane");
+                    const int64_t xcol = n0 + c0 + (lane % kCh) * (16 / kElem), xrow = mrow0 + lane / kCh;
+                    if (xcol < ncol_end) {
+#pragma unroll
+                        for (int i = 0; i < 32 / kRp; ++i)
+                            if (xrow + i * kRp < a.M) xc[i].load(a.aux, (xrow + i * kRp) * a.N + xcol);
+                    }
+                }
                 // stage the box: row = this lane's TMEM lane, 32 columns, swizzled;
                 // reading it back across rows lets every store instruction cover
                 // whole row segments
@@ -532,14 +575,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                     if (col < ncol_end) {
                         const int64_t row = mrow0 + lane / kChunks;
                         uint8_t *p = reinterpret_cast<uint8_t *>(out) + (row * a.N + col) * kElem;
+                        if constexpr (kMask) {
+#pragma unroll
+                            for (int i = 0; i < kIters; ++i)
+                                if (row + i * kRowsPer < a.M)
+                                    v[i] = mask_chunk<LAYOUT>(v[i], xc[i], a.aux_scale, a.aux_norm, tsum);
+                        }
 #pragma unroll
                         for (int i = 0; i < kIters; ++i)
-                            if (row + i * kRowsPer < a.M) {
-                                if constexpr (kMask)
-                                    v[i] = mask_chunk<LAYOUT>(v[i], a.aux, (row + i * kRowsPer) * a.N + col, a.aux_scale,
-                                                              a.aux_norm, tsum);
+                            if (row + i * kRowsPer < a.M)
                                 st_stream_v4(p + static_cast<int64_t>(i * kRowsPer) * a.N * kElem, v[i]);
-                            }
                     }
                 } else if constexpr (!kMask) {
                     // ragged N: read the box back one row at a time, lanes along
