@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", default="auto", choices=["auto", "popc", "e4m3", "e2m1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the headline steps one call at a time instead of replaying them as a CUDA graph")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
                     help="backward: the straight-through backward of a linear workload (all three gradients)")
     return ap.parse_args()
@@ -309,6 +311,22 @@ def run_ours(args, rank, world):
     # stream); then the same K steps again with events around each kernel for
     # the split and the roofline (those events serialise the two kernels and
     # add each launch's latency to its kernel's time)
+    # The K headline steps are captured once into a CUDA graph (the same public
+    # calls, each kernel a node) and replayed, so the host's per-call overhead
+    # does not set the pace of small steps; --no-graph launches them one by one.
+    graph, graph_note = None, "off (--no-graph)"
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(args.steps):
+                    step(i)
+            graph.replay()
+            torch.cuda.synchronize()
+            graph_note = f"one CUDA graph of the {args.steps} steps, replayed"
+        except RuntimeError as e:                       # capture unsupported: launch eagerly
+            graph, graph_note = None, f"off (capture failed: {str(e).splitlines()[0][:80]})"
+            torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     with ClockSampler(dev.index) as clk:
         barrier(world)
@@ -316,8 +334,11 @@ def run_ours(args, rank, world):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for i in range(args.steps):
-            step(i)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                step(i)
         t1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -371,7 +392,7 @@ def run_ours(args, rank, world):
         "config": {"workload": wl.name, "M": M, "N": N, "K": K, "x_dtype": wl.x_dtype,
                    "out_dtype": wl.out_dtype, "code": algo_name, "weights": "pre-packed outside timing",
                    "l2": f"inputs+outputs rotate over {nbuf} buffers ({nbuf * (x_bytes + out_bytes) / 1e6:.0f} MB > L2)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "launch": graph_note},
         "kernel_ms": {"pack": round(pack_ms, 5), "contraction": round(gemm_ms, 5),
                       "how": "second pass of the same steps, CUDA events around each kernel on its stream"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
