@@ -44,7 +44,7 @@ Readings where the sources leave a step open:
    rounds to nearest-even.
 4. A convolution tap in the zero padding contributes 0 to the dot product,
    as in the unfold + mm lowering.
-5. Backward, linear layer: the page's conv steps with the convolution's
+5. Backward: the page's steps; for the linear layer with the convolution's
    input and weight gradients replaced by the two matrix products
    ``g @ wt`` and ``g^T @ xs``. Each product is formed exactly (double) and
    rounded once to the gradient's dtype (bf16), as a matrix product in that
@@ -399,3 +399,43 @@ def linear_backward(x, w, g, scale_a: float, scale_w: float, x_dtype: str = "bf1
     return {"grad_input": grad_input, "grad_input_exact": gi_exact, "middle": middle,
             "grad_scale_a": grad_scale_a, "grad_scale_a_abs": float(np.abs(terms.astype(np.float64)).sum()),
             "grad_weight": bf16_round(gw_exact), "grad_weight_exact": gw_exact}
+
+
+def conv2d_backward(x, w, g, scale_a: float, scale_w: float, stride: int, padding: int, dilation: int,
+                    x_dtype: str = "bf16") -> dict:
+    """The three gradients of the binary conv2d layer (BinaryConv2dForward.backward)
+    for upstream gradient ``g`` [B, O, Ho, Wo] (bf16 values), input ``x``
+    [B, C, H, W], weight ``w`` [O, C, k, k]:
+      wt = bf16(sign(w) * scale_w)
+      grad_input = conv2d_input(x.shape, wt, g)    -> exact, rounded to bf16
+      q = x / scale_a (x's dtype); grad_input *= 1 - [q < -1] - [q > 1]
+      grad_scale_a = sum(grad_input * sign(x) * (1 / sqrt(numel(x))))
+      grad_weight = conv2d_weight(bf16(sign(x) * scale_a), w.shape, g) -> exact, rounded to bf16
+    The two convolution gradients are torch.nn.grad's routines in float64
+    (the page calls the same two routines), exact for these operands."""
+    x32 = _as_f32(x)
+    w32 = _as_f32(w)
+    g64 = torch.from_numpy(_as_f32(g).astype(np.float64))
+    B, C, H, W = x32.shape
+    sa32, sw32 = np.float32(scale_a), np.float32(scale_w)
+    wt = torch.from_numpy(bf16_round(sign(w32) * sw32).astype(np.float64))
+    gi_exact = torch.nn.grad.conv2d_input((B, C, H, W), wt, g64, stride=stride, padding=padding,
+                                          dilation=dilation).numpy()
+    gi = bf16_round(gi_exact)
+    q = x32 / sa32
+    if x_dtype == "bf16":
+        q = bf16_round(q)
+    elif x_dtype == "f16":
+        q = torch.from_numpy(q).to(torch.float16).float().numpy()
+    middle = (1.0 - (q < -1).astype(np.float32) - (q > 1).astype(np.float32)).astype(np.float32)
+    grad_input = (gi * middle).astype(np.float32)
+    inv = np.float32(1.0 / np.sqrt(np.float64(x32.size)))
+    terms = ((grad_input * sign(x32)).astype(np.float32) * inv).astype(np.float32)
+    xs = torch.from_numpy(bf16_round(sign(x32) * sa32).astype(np.float64))
+    gw_exact = torch.nn.grad.conv2d_weight(xs, tuple(w32.shape), g64, stride=stride, padding=padding,
+                                           dilation=dilation).numpy()
+    return {"grad_input": grad_input, "grad_input_exact": gi_exact, "middle": middle,
+            "grad_scale_a": float(terms.astype(np.float64).sum()),
+            "grad_scale_a_abs": float(np.abs(terms.astype(np.float64)).sum()),
+            "grad_weight": bf16_round(gw_exact), "grad_weight_exact": gw_exact}
+

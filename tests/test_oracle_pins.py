@@ -523,3 +523,101 @@ def test_planted_backward_mistakes_are_caught():
     assert not np.allclose((g.astype(np.float64) @ wt) * mid_x, gx)               # mask on x, not x / scale_a
     assert not np.allclose(g.astype(np.float64).T @ np.sign(x).astype(np.float64), gw)   # scale_a dropped
     assert not np.allclose(g.astype(np.float64).T @ oracle.bf16_round(np.sign(w[:M] if N >= M else w) * 0.8).astype(np.float64)[:, :K], gw)  # w for x
+
+
+# ---------------------------------------------------------------------------
+# Backward of the binary conv2d layer
+# ---------------------------------------------------------------------------
+
+def test_golden_conv_backward():
+    for ex in json.load(open(GOLDEN))["conv_backward"]:
+        o = oracle.conv2d_backward(np.array(ex["x"], np.float32), np.array(ex["w"], np.float32),
+                                   np.array(ex["g"], np.float32), ex["scale_a"], ex["scale_w"], ex["stride"],
+                                   ex["padding"], ex["dilation"], ex["x_dtype"])
+        np.testing.assert_array_equal(o["grad_input"], np.array(ex["grad_input"], np.float32), ex["why"])
+        np.testing.assert_array_equal(o["grad_weight"], np.array(ex["grad_weight"], np.float32), ex["why"])
+        if "grad_scale_a" in ex:
+            assert o["grad_scale_a"] == ex["grad_scale_a"], ex["why"]
+        else:
+            assert abs(o["grad_scale_a"] - 20.0 / 3.0) < 1e-6
+
+
+def _conv_backward_scatter(x, w, g, scale_a, scale_w, s, p, d, mistake=None):
+    """grad_input and grad_weight (exact, before rounding) by the definition
+    of the convolution, summed output pixel by output pixel and tap by tap."""
+    B, C, H, W = x.shape
+    O, _, k, _ = w.shape
+    _, _, Ho, Wo = g.shape
+    wt = oracle.bf16_round(torch.from_numpy(w).sign().numpy() * np.float32(scale_w)).astype(np.float64)
+    xs = oracle.bf16_round(torch.from_numpy(x).sign().numpy() * np.float32(scale_a)).astype(np.float64)
+    gi = np.zeros((B, C, H, W))
+    gw = np.zeros((O, C, k, k))
+    for b, o, i, j in itertools.product(range(B), range(O), range(Ho), range(Wo)):
+        gv = float(g[b, o, i, j])
+        for c, kh, kw in itertools.product(range(C), range(k), range(k)):
+            dd = 1 if mistake == "no_dilation" else d
+            h, ww = i * s - p + kh * dd, j * s - p + kw * dd
+            if 0 <= h < H and 0 <= ww < W:
+                wv = wt[o, c, k - 1 - kh, k - 1 - kw] if mistake == "flipped_kernel" else wt[o, c, kh, kw]
+                gi[b, c, h, ww] += gv * wv
+                gw[o, c, kh, kw] += gv * xs[b, c, h, ww]
+    return gi, gw
+
+
+CONV_BWD_SHAPES = [(1, 2, 5, 5, 3, 3, 1, 1, 1), (2, 3, 6, 7, 2, 3, 2, 1, 1), (1, 2, 7, 6, 2, 3, 2, 2, 2),
+                   (2, 1, 4, 4, 3, 1, 1, 0, 1), (1, 3, 5, 5, 2, 2, 3, 2, 1)]
+
+
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", CONV_BWD_SHAPES)
+def test_conv_backward_matches_scatter_loops(B, C, H, W, O, k, s, p, d):
+    rng = np.random.default_rng(B * 1000 + C * 100 + H * 10 + k)
+    ho, wo = oracle.conv2d_out_size(H, k, s, p, d), oracle.conv2d_out_size(W, k, s, p, d)
+    x = torch.randn(B, C, H, W, generator=torch.Generator().manual_seed(H)).to(torch.bfloat16).float().numpy()
+    w = rng.standard_normal((O, C, k, k)).astype(np.float32)
+    g = torch.randn(B, O, ho, wo, generator=torch.Generator().manual_seed(W)).to(torch.bfloat16).float().numpy()
+    o = oracle.conv2d_backward(x, w, g, 0.7, 0.4, s, p, d, "bf16")
+    gi, gw = _conv_backward_scatter(x, w, g, 0.7, 0.4, s, p, d)
+    np.testing.assert_allclose(o["grad_input_exact"], gi, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o["grad_weight_exact"], gw, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", CONV_BWD_SHAPES)
+def test_conv_backward_matches_fold_unfold(B, C, H, W, O, k, s, p, d):
+    # the unfold + mm lowering of banghao.live/blog/9 section 2, run backwards:
+    # grad_input = fold(wt^T @ g), grad_weight = g @ unfold(xs)^T
+    ho, wo = oracle.conv2d_out_size(H, k, s, p, d), oracle.conv2d_out_size(W, k, s, p, d)
+    x = torch.randn(B, C, H, W, generator=torch.Generator().manual_seed(k)).to(torch.bfloat16).float().numpy()
+    w = torch.randn(O, C, k, k, generator=torch.Generator().manual_seed(C)).numpy()
+    g = torch.randn(B, O, ho, wo, generator=torch.Generator().manual_seed(O)).to(torch.bfloat16).float().numpy()
+    o = oracle.conv2d_backward(x, w, g, 0.6, 0.3, s, p, d, "bf16")
+    wt = torch.from_numpy(oracle.bf16_round(np.sign(w) * np.float32(0.3)).astype(np.float64)).reshape(O, -1)
+    xs = torch.from_numpy(oracle.bf16_round(torch.from_numpy(x).sign().numpy() * np.float32(0.6)).astype(np.float64))
+    gm = torch.from_numpy(g.astype(np.float64)).reshape(B, O, -1)
+    cols = wt.T @ gm                                               # [B, C*k*k, L]
+    gi = F.fold(cols, (H, W), k, dilation=d, padding=p, stride=s).numpy()
+    u = F.unfold(xs, k, dilation=d, padding=p, stride=s)           # [B, C*k*k, L]
+    gw = torch.einsum("bol,bcl->oc", gm, u).reshape(O, C, k, k).numpy()
+    np.testing.assert_allclose(o["grad_input_exact"], gi, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o["grad_weight_exact"], gw, rtol=0, atol=1e-12)
+
+
+def test_conv_backward_1x1_equals_linear_backward():
+    B, C, O = 6, 9, 5
+    x = torch.randn(B, C).to(torch.bfloat16).float().numpy()
+    w = torch.randn(O, C).numpy().astype(np.float32)
+    g = torch.randn(B, O).to(torch.bfloat16).float().numpy()
+    oc = oracle.conv2d_backward(x[:, :, None, None], w[:, :, None, None], g[:, :, None, None], 0.8, 0.2, 1, 0, 1, "bf16")
+    ol = oracle.linear_backward(x, w, g, 0.8, 0.2, "bf16")
+    np.testing.assert_array_equal(oc["grad_input"][:, :, 0, 0], ol["grad_input"])
+    np.testing.assert_array_equal(oc["grad_weight"][:, :, 0, 0], ol["grad_weight"])
+    assert oc["grad_scale_a"] == ol["grad_scale_a"]
+
+
+@pytest.mark.parametrize("mistake", ["flipped_kernel", "no_dilation"])
+def test_planted_conv_backward_mistakes_are_caught(mistake):
+    x = torch.randn(1, 2, 7, 7, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).float().numpy()
+    w = torch.randn(2, 2, 3, 3, generator=torch.Generator().manual_seed(6)).numpy()
+    g = torch.randn(1, 2, 3, 3, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).float().numpy()
+    o = oracle.conv2d_backward(x, w, g, 0.7, 0.4, 1, 0, 2, "bf16")
+    gi, gw = _conv_backward_scatter(x, w, g, 0.7, 0.4, 1, 0, 2, mistake)
+    assert not (np.allclose(o["grad_input_exact"], gi) and np.allclose(o["grad_weight_exact"], gw))
