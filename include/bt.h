@@ -356,6 +356,42 @@ bt_status bt_binary_linear_backward(const void *x, bt_dtype x_dtype, const void 
                                     void *grad_x, float *grad_scale_a, void *grad_w, bt_dtype grad_w_dtype,
                                     void *workspace, size_t workspace_bytes, bt_stream stream);
 
+/* Workspace bytes bt_binary_conv2d_backward needs for the gradients asked for
+ * (0 for invalid sizes). */
+size_t bt_binary_conv2d_backward_workspace(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,
+                                           int stride, int padding, int dilation, int want_grad_input,
+                                           int want_grad_weight);
+
+/*
+ * bt_binary_conv2d_backward -- the straight-through backward of the binary
+ * conv2d layer, BinaryConv2dForward.backward step by step:
+ *   wt           = bf16(sign(w) * scale_w)
+ *   grad_x       = bf16(conv2d_input(x.shape, wt, g)) * middle,
+ *                  middle = !(q < -1 || q > 1), q = x / scale_a in x's dtype
+ *   *grad_scale_a = sum(grad_x * sign(x) * fp32(1 / sqrt(B*C*H*W)))
+ *   grad_w       = bf16(conv2d_weight(bf16(sign(x) * scale_a), w.shape, g))
+ *   x      [B, C, H, W] NCHW, BF16 or F32;
+ *   wst    [C*k*k, ldw] bf16 = bt_sign_transpose(w viewed as [O, C*k*k]),
+ *          ldw = bt_backward_weight_ld(O); needed only for grad_x;
+ *   g      [B, O, Ho, Wo] bf16 (Ho, Wo as in the forward);
+ *   grad_x [B, C, H, W] bf16 out or NULL; grad_scale_a one device float
+ *          (overwritten) or NULL, needs grad_x; grad_w [O, C, k, k] BF16 or
+ *          F32 (the fp32 sums before the rounding) out, or NULL;
+ *   workspace  bt_binary_conv2d_backward_workspace(...) bytes, 256-byte aligned.
+ * The two convolution gradients run as tensor-core products (bf16 operands,
+ * fp32 accumulators) over the unfolded taps; the input gradient gathers its
+ * taps in fp32 and rounds once. O a multiple of 8, B <= 65535; scales finite
+ * > 0; pointers 16-byte aligned device memory owned by the caller;
+ * asynchronous on `stream`. Errors: INVALID_ARG, ALIGNMENT, WORKSPACE,
+ * UNSUPPORTED (O not a multiple of 8, sizes beyond the limits, no tensor
+ * cores), CUDA.
+ */
+bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void *wst, int64_t ldw, const void *g,
+                                    int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
+                                    int padding, int dilation, float scale_a, float scale_w, void *grad_x,
+                                    float *grad_scale_a, void *grad_w, bt_dtype grad_w_dtype, void *workspace,
+                                    size_t workspace_bytes, bt_stream stream);
+
 /*
  * bt_device_status -- synchronizes `stream`, then reads and clears the
  * device error word of the current device: BT_ERR_TIMEOUT if a kernel's

@@ -242,3 +242,25 @@ def test_backward_abi_validation():
     assert call(wst=None) == bt.BT_ERR_INVALID_ARG
     assert call(N=60, ldw=64) == bt.BT_ERR_UNSUPPORTED                           # N not a multiple of 8
     assert call(K=20) == bt.BT_ERR_UNSUPPORTED
+
+
+def test_conv_backward_abi_validation():
+    ws = bt.bt_binary_conv2d_backward_workspace
+    assert ws(2, 8, 6, 6, 16, 3, 1, 1, 1, True, True) > 0
+    assert ws(2, 8, 6, 6, 16, 3, 1, 1, 1, False, False) == 0
+    assert ws(2, 8, 1, 1, 16, 3, 1, 0, 1, True, True) == 0                       # window larger than the image
+    f = bt._c_cbwd
+
+    def call(**kw):
+        a = dict(x=256, xt=bt.BT_BF16, wst=512, ldw=64, g=768, B=2, C=8, H=6, W=6, O=16, k=3, st=1, p=1, d=1,
+                 sa=0.5, sw=0.5, gx=1024, gsa=2048, gw=4096, gwt=bt.BT_BF16, ws=8192, wsb=1 << 24, s=None)
+        a.update(kw)
+        return f(*a.values())
+    assert call(xt=bt.BT_F16) == bt.BT_ERR_INVALID_ARG
+    assert call(gwt=bt.BT_I32) == bt.BT_ERR_INVALID_ARG
+    assert call(sa=-1.0) == bt.BT_ERR_INVALID_ARG
+    assert call(k=0) == bt.BT_ERR_INVALID_ARG
+    assert call(H=1, p=0) == bt.BT_ERR_INVALID_ARG                              # empty output
+    assert call(O=12) == bt.BT_ERR_UNSUPPORTED                                  # O not a multiple of 8
+    assert call(gx=None) == bt.BT_ERR_INVALID_ARG                               # grad_scale_a without grad_x
+    assert call(ldw=8) == bt.BT_ERR_INVALID_ARG                                 # ldw < O

@@ -199,3 +199,85 @@ def test_linear_backward_full_size_sampled():
     xf = x.float().numpy()
     terms = ((gx.float().numpy() * oracle.sign(xf)).astype(np.float32) * np.float32(1.0 / np.sqrt(M * K))).astype(np.float64)
     assert abs(float(gsa.cpu()) - terms.sum()) <= 1e-5 * np.abs(terms).sum()
+
+
+# ---------------------------------------------------------------------------
+# conv2d
+# ---------------------------------------------------------------------------
+
+def _conv_inputs(B, C, H, W, O, k, s, p, d, x_dtype, seed):
+    gen = torch.Generator().manual_seed(seed)
+    Ho, Wo = oracle.conv2d_out_size(H, k, s, p, d), oracle.conv2d_out_size(W, k, s, p, d)
+    x = torch.randn(B, C, H, W, generator=gen).to(x_dtype)
+    w = (torch.randn(O, C, k, k, generator=gen) * 0.05).to(torch.bfloat16)
+    g = (torch.randn(B, O, Ho, Wo, generator=gen) * 0.01).to(torch.bfloat16)
+    x.view(-1)[:2] = torch.tensor([0.0, -0.0]).to(x_dtype)
+    w.view(-1)[0] = 0.0
+    return x, w, g, float(x.float().abs().mean()), float(w.float().abs().mean())
+
+
+def _conv_run_and_compare(B, C, H, W, O, k, s, p, d, x_dtype, gw_dtype, seed):
+    x, w, g, sa, sw = _conv_inputs(B, C, H, W, O, k, s, p, d, x_dtype, seed)
+    wst = bt.bt_sign_transpose(w.view(O, -1).to(DEV))
+    gx, gsa, gw = bt.bt_binary_conv2d_backward(x.to(DEV), wst, g.to(DEV), O, k, s, p, d, sa, sw,
+                                               grad_weight_dtype=gw_dtype)
+    torch.cuda.synchronize()
+    gx, gsa, gw = gx.cpu(), float(gsa.cpu()), gw.cpu()
+    x_dt = "bf16" if x_dtype == torch.bfloat16 else "f32"
+    o = oracle.conv2d_backward(x.float().numpy(), w.float().numpy(), g.float().numpy(), sa, sw, s, p, d, x_dt)
+    # per-output bounds from the same sums over absolute values
+    ag = g.double().abs()
+    bw = float(oracle.bf16_round(np.float32(sw)))
+    ba = float(oracle.bf16_round(np.float32(sa)))
+    abs_in = torch.nn.grad.conv2d_input(x.shape, torch.full(w.shape, bw, dtype=torch.float64), ag, stride=s,
+                                        padding=p, dilation=d).numpy()
+    abs_w = torch.nn.grad.conv2d_weight(torch.full(x.shape, ba, dtype=torch.float64), w.shape, ag, stride=s,
+                                        padding=p, dilation=d).numpy()
+    gxn = gx.float().numpy()
+    assert np.all(gxn[o["middle"] == 0] == 0), "mask disagrees"
+    _check_sum(gxn, o["grad_input"], abs_in, O * k * k, "conv grad_input")
+    differ = gxn != o["grad_input"]
+    extra = float(np.abs(o["grad_input"][differ]).sum()) / np.sqrt(x.numel()) * 2.0 ** -7
+    assert abs(gsa - o["grad_scale_a"]) <= 1e-5 * o["grad_scale_a_abs"] + extra + 1e-30, (gsa, o["grad_scale_a"])
+    P = B * g.shape[2] * g.shape[3]
+    if gw.dtype == torch.bfloat16:
+        _check_sum(gw.float().numpy(), o["grad_weight"], abs_w, P, "conv grad_weight")
+    else:
+        bad = np.abs(gw.double().numpy() - o["grad_weight_exact"]) > P * 2.0 ** -23 * abs_w + 1e-30
+        assert not bad.any(), f"conv grad_weight f32: {int(bad.sum())} outside the fp32 bound"
+    return differ
+
+
+CONV_BWD = [(2, 8, 9, 9, 16, 3, 1, 1, 1), (3, 5, 11, 10, 24, 3, 2, 1, 1), (2, 16, 12, 12, 32, 3, 2, 2, 2),
+            (1, 3, 7, 7, 8, 1, 1, 0, 1), (4, 32, 14, 14, 64, 3, 1, 1, 1), (2, 4, 6, 6, 8, 5, 1, 2, 1),
+            (2, 20, 15, 13, 40, 3, 3, 1, 1)]
+
+
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", CONV_BWD)
+@pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float32], ids=["x_bf16", "x_f32"])
+def test_conv_backward_matches_oracle(B, C, H, W, O, k, s, p, d, x_dtype):
+    differ = _conv_run_and_compare(B, C, H, W, O, k, s, p, d, x_dtype, torch.bfloat16, seed=B + C + H + k)
+    assert differ.mean() < 0.01
+
+
+def test_conv_backward_grad_weight_f32():
+    _conv_run_and_compare(2, 16, 12, 12, 32, 3, 2, 1, 1, torch.bfloat16, torch.float32, seed=9)
+
+
+def test_conv_backward_partial_and_empty():
+    x, w, g, sa, sw = _conv_inputs(2, 8, 9, 9, 16, 3, 1, 1, 1, torch.bfloat16, 4)
+    wst = bt.bt_sign_transpose(w.view(16, -1).to(DEV))
+    gx, gsa, gw = bt.bt_binary_conv2d_backward(x.to(DEV), wst, g.to(DEV), 16, 3, 1, 1, 1, sa, sw)
+    gx1, _, gw1 = bt.bt_binary_conv2d_backward(x.to(DEV), wst, g.to(DEV), 16, 3, 1, 1, 1, sa, sw, grad_weight_dtype=None)
+    _, _, gw2 = bt.bt_binary_conv2d_backward(x.to(DEV), None, g.to(DEV), 16, 3, 1, 1, 1, sa, sw, grad_input=False)
+    assert gw1 is None and torch.equal(gx1.cpu(), gx.cpu()) and torch.equal(gw2.cpu(), gw.cpu())
+    e = torch.empty(0, 8, 9, 9, dtype=torch.bfloat16, device=DEV)
+    ge = torch.empty(0, 16, 9, 9, dtype=torch.bfloat16, device=DEV)
+    gxe, gsae, gwe = bt.bt_binary_conv2d_backward(e, wst, ge, 16, 3, 1, 1, 1, sa, sw)
+    assert gxe.numel() == 0 and float(gsae.cpu()) == 0.0 and torch.all(gwe.cpu() == 0)
+
+
+@pytest.mark.slow
+def test_conv_backward_stride2_layer_slice():
+    # 16 images of the stride-2 downsampling layer [256,128,28,28] x [256,128,3,3]
+    _conv_run_and_compare(16, 128, 28, 28, 256, 3, 2, 1, 1, torch.bfloat16, torch.bfloat16, seed=21)

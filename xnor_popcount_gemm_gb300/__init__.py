@@ -72,6 +72,9 @@ _c_sign_t = _sig("bt_sign_transpose", _i, [_p, _i, _i64, _i64, _i64, _p, _p])
 _c_bwd_ws = _sig("bt_binary_linear_backward_workspace", _sz, [_i64, _i64, _i64, _i])
 _c_bwd = _sig("bt_binary_linear_backward", _i, [_p, _i, _p, _i64, _p, _i64, _i64, _i64, _f, _f, _p, _p, _p, _i,
                                                 _p, _sz, _p])
+_c_cbwd_ws = _sig("bt_binary_conv2d_backward_workspace", _sz, [_i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _i])
+_c_cbwd = _sig("bt_binary_conv2d_backward", _i, [_p, _i, _p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
+                                                 _f, _f, _p, _p, _p, _i, _p, _sz, _p])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
 _c_status = _sig("bt_device_status", _i, [_p])
 
@@ -81,7 +84,7 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
             "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
-            "bt_binary_linear_backward"]
+            "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_binary_conv2d_backward"]
 
 
 class BtError(RuntimeError):
@@ -234,6 +237,51 @@ def bt_binary_linear_backward(x: torch.Tensor, wst: torch.Tensor | None, g: torc
                   scale_w, _ptr(grad_x), _ptr(grad_scale_a), _ptr(grad_w),
                   _DT[grad_w.dtype] if grad_w is not None else BT_BF16, _ptr(ws),
                   0 if ws is None else ws.numel(), _stream(stream)))
+    return grad_x, grad_scale_a, grad_w
+
+
+def bt_binary_conv2d_backward_workspace(B: int, C: int, H: int, W: int, O: int, kernel_size: int, stride: int,
+                                        padding: int, dilation: int, want_grad_input: bool = True,
+                                        want_grad_weight: bool = True) -> int:
+    return int(_c_cbwd_ws(B, C, H, W, O, kernel_size, stride, padding, dilation, 1 if want_grad_input else 0,
+                          1 if want_grad_weight else 0))
+
+
+def bt_binary_conv2d_backward(x: torch.Tensor, wst: torch.Tensor | None, g: torch.Tensor, O: int, kernel_size: int,
+                              stride: int, padding: int, dilation: int, scale_a: float, scale_w: float,
+                              grad_input: bool = True, grad_weight_dtype=torch.bfloat16,
+                              grad_x: torch.Tensor | None = None, grad_scale_a: torch.Tensor | None = None,
+                              grad_w: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                              stream=None):
+    """Straight-through backward of the binary conv2d layer: x [B, C, H, W]
+    (bf16 or f32), g [B, O, Ho, Wo] bf16, wst = bt_sign_transpose(w.view(O,
+    -1)). Returns (grad_x [B, C, H, W] bf16, grad_scale_a (device float
+    tensor), grad_w [O, C, k, k]), as bt_binary_linear_backward does."""
+    _contig(x, "x")
+    _contig(g, "g")
+    B, C, H, W = x.shape
+    k = kernel_size
+    if grad_input:
+        if wst is None:
+            raise ValueError("grad_input needs wst = bt_sign_transpose(w.view(O, -1))")
+        _contig(wst, "wst")
+        if grad_x is None:
+            grad_x = torch.empty((B, C, H, W), dtype=torch.bfloat16, device=x.device)
+        if grad_scale_a is None:
+            grad_scale_a = torch.empty((), dtype=torch.float32, device=x.device)
+    else:
+        grad_x = grad_scale_a = None
+    if grad_weight_dtype is not None and grad_w is None:
+        grad_w = torch.empty((O, C, k, k), dtype=grad_weight_dtype, device=x.device)
+    elif grad_weight_dtype is None:
+        grad_w = None
+    ws = _workspace(bt_binary_conv2d_backward_workspace(B, C, H, W, O, k, stride, padding, dilation,
+                                                        grad_x is not None, grad_w is not None), x.device, workspace)
+    ldw = wst.shape[1] if (grad_input and wst is not None) else 0
+    _check(_c_cbwd(_ptr(x), _DT[x.dtype], _ptr(wst) if grad_input else None, ldw, _ptr(g), B, C, H, W, O, k, stride,
+                   padding, dilation, scale_a, scale_w, _ptr(grad_x), _ptr(grad_scale_a), _ptr(grad_w),
+                   _DT[grad_w.dtype] if grad_w is not None else BT_BF16, _ptr(ws), 0 if ws is None else ws.numel(),
+                   _stream(stream)))
     return grad_x, grad_scale_a, grad_w
 
 

@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(kTThreads) transpose_kernel(const T *__restric
     __shared__ uint16_t tile[kTile][kTile + 2];
     pdl_launch_dependents();
     pdl_wait();
+    in += static_cast<int64_t>(blockIdx.z) * R * C;             // batch of matrices
+    out += static_cast<int64_t>(blockIdx.z) * C * ldo;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
     for (int i = threadIdx.x; i < kTile * kTile; i += kTThreads) {
         const int rr = i / kTile, cc = i % kTile;
@@ -120,13 +122,17 @@ __device__ __forceinline__ uint4 load8_bf16(const T *p) {
 // chunk), pairs rows 2i and 2i+1 column by column with byte permutes, and
 // writes output row 2w + p as the words (w, rows 0..7 in pairs) -- 16 bytes
 // per output row; 16 threads cover a 256-byte output row segment.
-// Needs C a multiple of 8 and ldo a multiple of 8.
-template <typename T, bool SIGN>
+// Needs ldo a multiple of 8; rows whose length C is not a multiple of 8 are
+// read element by element (ALIGNED false). blockIdx.z walks a batch of
+// matrices stored one after the other.
+template <typename T, bool SIGN, bool ALIGNED>
 __global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restrict__ in, int64_t R, int64_t C,
                                                                int64_t ldo, uint16_t *__restrict__ out) {
     __shared__ uint4 tile[128 * 16];
     pdl_launch_dependents();
     pdl_wait();
+    in += static_cast<int64_t>(blockIdx.z) * R * C;
+    out += static_cast<int64_t>(blockIdx.z) * C * ldo;
     const int t = threadIdx.x;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128, c0 = static_cast<int64_t>(blockIdx.x) * 128;
     uint4 v[8];
@@ -134,7 +140,24 @@ __global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restri
     for (int i = 0; i < 8; ++i) {
         const int k = i * kTThreads + t, rr = k >> 4, q = k & 15;
         const int64_t r = r0 + rr, c = c0 + 8 * q;
-        v[i] = (r < R && c < C) ? load8_bf16<T, SIGN>(in + r * C + c) : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (ALIGNED) {
+            v[i] = (r < R && c < C) ? load8_bf16<T, SIGN>(in + r * C + c) : make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (r < R) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (c + e < C) {
+                        const T xv = in[r * C + c + e];
+                        uint16_t h;
+                        if constexpr (SIGN) h = sign_bf16(to_f32<T>(xv));
+                        else h = *reinterpret_cast<const uint16_t *>(&xv);
+                        w[e >> 1] |= static_cast<uint32_t>(h) << (16 * (e & 1));
+                    }
+                }
+            }
+            v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -173,19 +196,23 @@ __global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restri
 }
 
 template <typename T, bool SIGN>
-cudaError_t transpose_t(const void *in, int64_t R, int64_t C, int64_t ldo, uint16_t *out, cudaStream_t s) {
+cudaError_t transpose_t(const void *in, int64_t R, int64_t C, int64_t ldo, uint16_t *out, cudaStream_t s,
+                        int batch = 1) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute pdl = pdl_attribute();
     cfg.blockDim = dim3(kTThreads);
     cfg.stream = s;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    const bool wide = ldo % 8 == 0 && C % 8 == 0 && aligned(in, 16) && aligned(out, 16);
-    if (wide && (ldo + 127) / 128 <= 65535) {
-        cfg.gridDim = dim3(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>((ldo + 127) / 128));
-        return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN>, static_cast<const T *>(in), R, C, ldo, out);
+    if (ldo % 8 == 0 && aligned(out, 16) && (ldo + 127) / 128 <= 65535) {
+        cfg.gridDim = dim3(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>((ldo + 127) / 128),
+                           static_cast<unsigned>(batch));
+        if (C % 8 == 0 && aligned(in, 16))
+            return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN, true>, static_cast<const T *>(in), R, C, ldo, out);
+        return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN, false>, static_cast<const T *>(in), R, C, ldo, out);
     }
-    cfg.gridDim = dim3(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((ldo + kTile - 1) / kTile));
+    cfg.gridDim = dim3(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((ldo + kTile - 1) / kTile),
+                       static_cast<unsigned>(batch));
     return cudaLaunchKernelEx(&cfg, transpose_kernel<T, SIGN>, static_cast<const T *>(in), R, C, ldo, out);
 }
 
@@ -204,6 +231,19 @@ int64_t round_up64(int64_t v) { return (v + 63) / 64 * 64; }
 size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
+
+cudaError_t launch_transpose_bf16_batched(const void *in, bt_dtype in_t, int64_t R, int64_t C, int64_t ldo, bool sign,
+                                          uint16_t *out, int batch, cudaStream_t s) {
+    if (R == 0 || C == 0 || batch == 0) return cudaSuccess;
+    if (batch < 0 || batch > 65535 || C > (int64_t(65535) * kTile) || ldo > (int64_t(65535) * kTile))
+        return cudaErrorInvalidValue;
+    if (!sign) return transpose_t<__nv_bfloat16, false>(in, R, C, ldo, out, s, batch);
+    switch (in_t) {
+        case BT_F32: return transpose_t<float, true>(in, R, C, ldo, out, s, batch);
+        case BT_F16: return transpose_t<__half, true>(in, R, C, ldo, out, s, batch);
+        default: return transpose_t<__nv_bfloat16, true>(in, R, C, ldo, out, s, batch);
+    }
+}
 
 cudaError_t launch_transpose_bf16(const void *in, bt_dtype in_t, int64_t R, int64_t C, int64_t ldo, bool sign,
                                   uint16_t *out, cudaStream_t s) {

@@ -98,11 +98,23 @@ cudaError_t launch_tc_bf16(const uint16_t *a, int64_t lda, const uint16_t *b, in
                            int64_t klen, float alpha, void *out, bt_dtype out_t, const TcMask *mask,
                            unsigned int *err, cudaStream_t s);
 
+// The same contraction split along K into `splits` equal parts (klen a
+// multiple of 64 * splits), each part's fp32 partial sums (times alpha) in
+// out [splits, M, N]; the caller adds them up.
+cudaError_t launch_tc_bf16_splitk(const uint16_t *a, int64_t lda, const uint16_t *b, int64_t ldb, int64_t M,
+                                  int64_t N, int64_t klen, int splits, float alpha, float *out, unsigned int *err,
+                                  cudaStream_t s);
+
 // out[c * ldo + r] = f(in[r * C + c]) as bf16 for r < R, c < C, and 0 for
 // R <= r < ldo: f = torch.sign (sign = true; in of type in_t) or the value
 // itself (sign = false; in bf16).
 cudaError_t launch_transpose_bf16(const void *in, bt_dtype in_t, int64_t R, int64_t C, int64_t ldo, bool sign,
                                   uint16_t *out, cudaStream_t s);
+
+// The same for `batch` matrices stored one after the other (in: R*C
+// elements apart; out: C*ldo apart). batch <= 65535.
+cudaError_t launch_transpose_bf16_batched(const void *in, bt_dtype in_t, int64_t R, int64_t C, int64_t ldo, bool sign,
+                                          uint16_t *out, int batch, cudaStream_t s);
 
 // True when this build carries the tensor-core kernels.
 bool tc_available();

@@ -88,7 +88,9 @@ struct TcArgs {
     int d;                     // K slices per smem stage
     int nk;                    // stages per tile
     int num_n, bn;             // column tiles; tile width BN (multiple of 16)
-    int num_super;             // tiles (pairs: 256-row tiles)
+    int num_super;             // units of work: tiles (pairs: 256-row tiles) x K splits
+    int num_tiles;             // tiles of one K split
+    int64_t split_out;         // split-K: output elements between the splits' partial results
     uint32_t idesc;            // instruction descriptor
     float alpha;
     void *out;
@@ -382,15 +384,17 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
             for (int i = 0; i < kMaxStages; ++i) last_phase[i] = 2u;
             bool ok = true;
             for (int st = unit; st < a.num_super && ok; st += nunits) {
-                const int mt = st / a.num_n, nt = st % a.num_n;
+                // K split `sp` covers slices [sp * slices, (sp + 1) * slices) of the rows
+                const int sp = st / a.num_tiles, tl = st - sp * a.num_tiles;
+                const int mt = tl / a.num_n, nt = tl % a.num_n;
                 const int am0 = mt * kTileRows + a_first;
                 const int bn0 = nt * bn + b_first;
                 for (int kb = 0; kb < a.nk; ++kb) {
                     if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
                     const uint32_t adst = sA + s * kAStage, bdst = sB + s * kBStage;
                     const uint32_t fbar = PAIR ? tc::mapa(full(s), 0u) : full(s);
-                    const int k0 = kb * D;
-                    const bool whole = k0 + D <= a.full_slices;
+                    const int k0 = sp * a.slices + kb * D;
+                    const bool whole = kb * D + D <= a.slices && k0 + D <= a.full_slices;
                     if (whole) {
                         // D whole slices: one box per operand
                         if (leader) tc::mbar_arrive_expect_tx(full(s), slice_bytes * D);
@@ -488,13 +492,15 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
     } else {
         // ---------------- epilogue (warps 2..9) ----------------
         pdl_wait();                                       // the previous kernel may still use `out`
-        T *out = static_cast<T *>(a.out);
+        T *const out_base = static_cast<T *>(a.out);
         const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // this warp's staging box
         constexpr bool kMask = LAYOUT == kRowsMaskBf16 || LAYOUT == kRowsMaskF32;
         float tsum = 0.0f;                                // masked layouts: this lane's grad_scale_a terms
         int local = 0;
         for (int st = unit; st < a.num_super; st += nunits, ++local) {
-            const int mt = st / a.num_n, nt = st % a.num_n;
+            const int sp = st / a.num_tiles, tl = st - sp * a.num_tiles;
+            const int mt = tl / a.num_n, nt = tl % a.num_n;
+            T *const out = out_base + sp * a.split_out;           // split-K: this split's partial result
             const int64_t m0 = static_cast<int64_t>(mt) * kTileRows + (PAIR ? static_cast<int64_t>(crank) * kBM : 0);
             const int n0 = nt * bn;
             const int buf = local & 1;
@@ -834,16 +840,19 @@ cudaError_t launch_code(bt_code code, bool pair, const Maps &mp, const TcArgs &a
 int out_elem_bytes(bt_dtype t) { return t == BT_BF16 || t == BT_F16 ? 2 : 4; }
 
 // Plan the tiles of an M x N contraction over rows of rb bytes (a multiple of
-// 16; A and B rows pitch_a and pitch_b bytes apart) and encode the maps.
+// 16; A and B rows pitch_a and pitch_b bytes apart) and encode the maps. With
+// rb_split > 0 the contraction is split along K into parts of rb_split bytes
+// (a multiple of 128) that the caller runs as K splits.
 bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const uint8_t *bp, int64_t M, int64_t N,
-          int64_t rb, int64_t pitch_a, int64_t pitch_b) {
+          int64_t rb, int64_t pitch_a, int64_t pitch_b, int64_t rb_split = -1) {
     if (rb % 16 != 0 || pitch_a % 16 != 0 || pitch_b % 16 != 0 || pitch_a < rb || pitch_b < rb ||
         M > (int64_t(1) << 31) - 512 || N > (int64_t(1) << 31) - 512)
         return false;
     a.M = M;
     a.N = N;
-    a.slices = static_cast<int>((rb + kRowB - 1) / kRowB);
-    a.full_slices = static_cast<int>(rb / kRowB);
+    if (rb_split > 0 && (rb_split % kRowB != 0 || rb % rb_split != 0)) return false;
+    a.slices = static_cast<int>(((rb_split > 0 ? rb_split : rb) + kRowB - 1) / kRowB);   // per K split
+    a.full_slices = static_cast<int>(rb / kRowB);                                       // of the whole row
     const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;       // E2M1 keeps 32 TMEM columns for block scales
     c = choose_cfg(M, N, a.slices, sm_count(), max_bn);
     a.bn = c.bn;
@@ -854,6 +863,8 @@ bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const ui
     if (num_m * num_n > (int64_t(1) << 30)) return false;
     a.num_n = static_cast<int>(num_n);
     a.num_super = static_cast<int>(num_m * num_n);
+    a.num_tiles = a.num_super;
+    a.split_out = 0;
     a.idesc = make_idesc(code, rows, a.bn);
     const uint32_t b_box = static_cast<uint32_t>(b_slot_rows(a.bn, c.pair));
     return map_3d(&mp.a3, ap, static_cast<uint64_t>(pitch_a), static_cast<uint64_t>(M),
@@ -939,6 +950,28 @@ cudaError_t launch_tc_bf16(const uint16_t *a_ptr, int64_t lda, const uint16_t *b
     }
     return out_t == BT_F32 ? launch_bf16_t<kRowsOut, BT_F32>(c.pair, mp, a, s)
                            : launch_bf16_t<kRowsOut, BT_BF16>(c.pair, mp, a, s);
+}
+
+// Split-K: out [splits, M, N] fp32 holds each K split's partial sums (alpha
+// applied); klen a multiple of 64 * splits.
+cudaError_t launch_tc_bf16_splitk(const uint16_t *a_ptr, int64_t lda, const uint16_t *b_ptr, int64_t ldb, int64_t M,
+                                  int64_t N, int64_t klen, int splits, float alpha, float *out, unsigned int *err,
+                                  cudaStream_t s) {
+    if (splits < 1 || klen % (64 * splits) != 0) return cudaErrorInvalidValue;
+    TcArgs a{};
+    Maps mp;
+    TileCfg c;
+    if (!plan(a, mp, c, kCodeBF16, reinterpret_cast<const uint8_t *>(a_ptr), reinterpret_cast<const uint8_t *>(b_ptr),
+              M, N, klen * 2, lda * 2, ldb * 2, klen * 2 / splits))
+        return cudaErrorInvalidValue;
+    if (static_cast<int64_t>(a.num_tiles) * splits > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    a.num_super = a.num_tiles * splits;
+    a.split_out = M * N;
+    a.alpha = alpha;
+    a.out = out;
+    a.err = err;
+    a.vec = (N % 4 == 0) && aligned(out, 16) ? 1 : 0;
+    return launch_bf16_t<kRowsOut, BT_F32>(c.pair, mp, a, s);
 }
 
 }  // namespace bt
