@@ -558,42 +558,59 @@ def load_traffic(workload: str, algo: str):
 # ---------------------------------------------------------------------------
 
 def run_backward(args, rank, world):
-    """K steps of bt_binary_linear_backward (grad_input with the fused mask and
-    grad_scale_a, grad_weight) on the workload's x and W with a synthetic bf16
-    upstream gradient; sign(W)^T is prepared once outside timing, as the
-    forward's packed weight is."""
+    """K steps of the straight-through backward (the input gradient with its
+    fused mask and grad_scale_a, and the weight gradient) on the workload's x
+    and W with a synthetic bf16 upstream gradient; sign(W)^T is prepared once
+    outside timing, as the forward's packed weight is."""
     import xnor_popcount_gemm_gb300 as bt
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     wl = workloads.NAMED[args.workload]()
-    if wl.kind != "linear":
-        raise SystemExit("--pass backward covers the linear workloads")
-    M, K = wl.x.shape
-    N = wl.w.shape[0]
-    if N % 8 or K % 8:
-        raise SystemExit("--pass backward needs N and K multiples of 8")
+    M, N, K = wl.gemm_shape()
+    conv = wl.kind == "conv"
+    if conv:
+        B, C, H, W = wl.x.shape
+        O, k = wl.w.shape[0], wl.w.shape[2]
+        Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
+        Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
+        g_shape = (B, O, Ho, Wo)
+        if O % 8:
+            raise SystemExit("--pass backward needs O a multiple of 8")
+    else:
+        g_shape = (M, N)
+        if N % 8 or K % 8:
+            raise SystemExit("--pass backward needs N and K multiples of 8")
     stream = torch.cuda.current_stream()
     gen = torch.Generator().manual_seed(1000)
-    g_host = (torch.randn(M, N, generator=gen) * 0.01).to(torch.bfloat16)
+    g_host = (torch.randn(*g_shape, generator=gen) * 0.01).to(torch.bfloat16)
     x_host = wl.x if wl.x.dtype in (torch.bfloat16, torch.float32) else wl.x.float()
-    wst = bt.bt_sign_transpose(wl.w.to(dev))
-    per = x_host.numel() * x_host.element_size() + g_host.numel() * 2 + (M * K + N * K) * 2
+    wst = bt.bt_sign_transpose(wl.w.reshape(wl.w.shape[0], -1).to(dev))
+    gw_shape = tuple(wl.w.shape)
+    per = x_host.numel() * x_host.element_size() + g_host.numel() * 2 + (x_host.numel() + wl.w.numel()) * 2
     nbuf = max(1, -(-2 * L2_BYTES // per))
     xs = [x_host.to(dev) for _ in range(nbuf)]
     gs = [g_host.to(dev) for _ in range(nbuf)]
-    gxs = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
-    gws = [torch.empty(N, K, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    gxs = [torch.empty(x_host.shape, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
+    gws = [torch.empty(gw_shape, dtype=torch.bfloat16, device=dev) for _ in range(nbuf)]
     gsa = torch.empty((), dtype=torch.float32, device=dev)
-    ws = torch.empty(bt.bt_binary_linear_backward_workspace(M, N, K, True), dtype=torch.uint8, device=dev)
+    if conv:
+        ws = torch.empty(bt.bt_binary_conv2d_backward_workspace(B, C, H, W, O, k, wl.stride, wl.padding, wl.dilation),
+                         dtype=torch.uint8, device=dev)
+    else:
+        ws = torch.empty(bt.bt_binary_linear_backward_workspace(M, N, K, True), dtype=torch.uint8, device=dev)
     flops = 2 * (2.0 * M * N * K)
 
     def step(i, which="both"):
         j = i % nbuf
-        bt.bt_binary_linear_backward(xs[j], wst, gs[j], wl.scale_a, wl.scale_w,
-                                     grad_input=which in ("both", "input"),
-                                     grad_weight_dtype=torch.bfloat16 if which in ("both", "weight") else None,
-                                     grad_x=gxs[j], grad_scale_a=gsa, grad_w=gws[j], workspace=ws)
+        kw = dict(grad_input=which in ("both", "input"),
+                  grad_weight_dtype=torch.bfloat16 if which in ("both", "weight") else None,
+                  grad_x=gxs[j], grad_scale_a=gsa, grad_w=gws[j], workspace=ws)
+        if conv:
+            bt.bt_binary_conv2d_backward(xs[j], wst, gs[j], O, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
+                                         wl.scale_w, **kw)
+        else:
+            bt.bt_binary_linear_backward(xs[j], wst, gs[j], wl.scale_a, wl.scale_w, **kw)
 
     def timed(which, n):
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -618,6 +635,7 @@ def run_backward(args, rank, world):
         raise RuntimeError("device status")
     peaks, peak_src = measured_peaks()
     achieved = 2.0 * M * N * K / (ms_in / 1e3) / 1e12
+    launches = (6 if not conv else 7) * args.steps
     line = {
         "metric": "backward TFLOP/s (grad_input + grad_weight, 2 x 2*M*N*K / s)",
         "value": round(flops * world / (ms / 1e3) / 1e12, 2),
@@ -640,8 +658,8 @@ def run_backward(args, rank, world):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
                      "peak_source": f"{peak_src}: cuBLAS bf16 burst",
-                     "kernel": "grad_input contraction (tc_kernel bf16 with the fused mask), per call"},
-        "gpu_launches": 6 * args.steps,
+                     "kernel": "the input-gradient call (contraction + fused mask" + (", col2im" if conv else "") + ")"},
+        "gpu_launches": launches,
         "clocks": clk.summary(),
     }
     return line

@@ -47,91 +47,153 @@ template <> __device__ __forceinline__ float ld_f32<__nv_bfloat16>(const __nv_bf
     return __bfloat162float(p[i]);
 }
 
+// The kernels below map rows to blockIdx.y (looping when there are more
+// rows than grid rows) and the elements of a row to threads, so that every
+// index is a 32-bit quotient of a row position; sizes are validated to fit.
+
 // g [B, O, Ho*Wo] -> go [O, ldp]: row o holds g[b, o, :] for b = 0, 1, ...
 // one after the other; columns P .. ldp-1 are 0.
 __global__ void __launch_bounds__(kThreads) g_rows_kernel(const uint16_t *__restrict__ g, ConvBwdGeom q, int64_t ldp,
                                                           uint16_t *__restrict__ go) {
     pdl_launch_dependents();
     pdl_wait();
-    const int64_t hw = q.Ho * q.Wo, total = q.O * ldp;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t o = i / ldp, col = i - o * ldp;
+    const uint32_t hw = static_cast<uint32_t>(q.Ho * q.Wo);
+    const uint32_t col = blockIdx.x * kThreads + threadIdx.x;
+    if (col >= ldp) return;
+    const uint32_t b = col / hw, pix = col - b * hw;
+    for (int64_t o = blockIdx.y; o < q.O; o += gridDim.y) {
         uint16_t v = 0;
-        if (col < q.P) {
-            const int64_t b = col / hw, pix = col - b * hw;
-            v = g[(b * q.O + o) * hw + pix];
-        }
-        go[i] = v;
+        if (col < q.P) v = g[(static_cast<int64_t>(b) * q.O + o) * hw + pix];
+        go[o * ldp + col] = v;
     }
 }
 
 // im2col of sign(x), transposed: u[t, p] (row pitch ldp) = sign(x[b, c, ih, iw])
 // as bf16 for tap t = (c, kh, kw) of output pixel p = (b, i, j), ih = i*s - p
-// + kh*d, iw = j*s - p + kw*d; 0 in the padding and for p >= P.
+// + kh*d, iw = j*s - p + kw*d; 0 in the padding and for p >= P. A thread
+// keeps its pixel p and walks kTapRows consecutive taps, stepping (c, kh, kw)
+// without divisions.
+constexpr int kTapRows = 16;
 template <typename T>
 __global__ void __launch_bounds__(kThreads) sign_im2col_t_kernel(const T *__restrict__ x, ConvBwdGeom q, int64_t ldp,
                                                                  uint16_t *__restrict__ u) {
     pdl_launch_dependents();
     pdl_wait();
-    const int64_t total = q.T * ldp, hw = q.Ho * q.Wo, kk = static_cast<int64_t>(q.k) * q.k;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t t = i / ldp, col = i - t * ldp;
-        uint16_t v = 0;
-        if (col < q.P) {
-            const int64_t c = t / kk, tap = t - c * kk;
-            const int kh = static_cast<int>(tap / q.k), kw = static_cast<int>(tap - static_cast<int64_t>(kh) * q.k);
-            const int64_t b = col / hw, pix = col - b * hw;
-            const int64_t oi = pix / q.Wo, oj = pix - oi * q.Wo;
-            const int64_t ih = oi * q.s - q.p + static_cast<int64_t>(kh) * q.d;
-            const int64_t iw = oj * q.s - q.p + static_cast<int64_t>(kw) * q.d;
-            if (ih >= 0 && ih < q.H && iw >= 0 && iw < q.W) v = sign_bf16_f(ld_f32<T>(x, ((b * q.C + c) * q.H + ih) * q.W + iw));
+    const uint32_t col = blockIdx.x * kThreads + threadIdx.x;
+    if (col >= ldp) return;
+    const uint32_t hw = static_cast<uint32_t>(q.Ho * q.Wo), wo = static_cast<uint32_t>(q.Wo);
+    const bool live = col < q.P;
+    const uint32_t b = live ? col / hw : 0u, pix = col - b * hw, oi = pix / wo, oj = pix - oi * wo;
+    const int h0 = static_cast<int>(oi) * q.s - q.p, w0 = static_cast<int>(oj) * q.s - q.p;
+    const int64_t xb = static_cast<int64_t>(b) * q.C * q.H * q.W;
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.y) * kTapRows; t0 < q.T;
+         t0 += static_cast<int64_t>(gridDim.y) * kTapRows) {
+        const uint32_t kk = static_cast<uint32_t>(q.k * q.k);
+        uint32_t c = static_cast<uint32_t>(t0) / kk, tap = static_cast<uint32_t>(t0) - c * kk;
+        int kh = static_cast<int>(tap) / q.k, kw = static_cast<int>(tap) - kh * q.k;
+        const int64_t tend = t0 + kTapRows < q.T ? t0 + kTapRows : q.T;
+        for (int64_t t = t0; t < tend; ++t) {
+            uint16_t v = 0;
+            const int ih = h0 + kh * q.d, iw = w0 + kw * q.d;
+            if (live && ih >= 0 && ih < q.H && iw >= 0 && iw < q.W)
+                v = sign_bf16_f(ld_f32<T>(x, xb + (static_cast<int64_t>(c) * q.H + ih) * q.W + iw));
+            u[t * ldp + col] = v;
+            if (++kw == q.k) { kw = 0; if (++kh == q.k) { kh = 0; ++c; } }
         }
-        u[i] = v;
     }
 }
 
 // col2im of D [T, P] (fp32, row pitch P) into the input gradient, with the
 // straight-through mask and the grad_scale_a terms: one thread per input
-// element (b, c, h, w), w fastest. Taps are summed in (kh, kw) order.
-template <typename T>
+// element (b, c, h, w) of an image plane (b, c) (blockIdx.y), w fastest.
+// The taps that read (h, w) -- kh with h + p - kh*d = i*s, 0 <= i < Ho, and
+// the same for w -- are listed once per thread (S = the stride when it is 1
+// or 2, so the divisions become shifts; 0 for any stride); taps are summed
+// in (kh, kw) order.
+constexpr int kMaxTapList = 8;
+template <int S>
+__device__ __forceinline__ int tap_list(int pos, int pad, int k, int d, int s, int nout, int (&tk)[kMaxTapList],
+                                        int (&ti)[kMaxTapList]) {
+    int n = 0;
+    for (int kk = 0; kk < k; ++kk) {
+        const int r = pos + pad - kk * d;
+        if (r < 0) break;                                     // r falls as kk grows
+        int i;
+        if constexpr (S == 1) {
+            i = r;
+        } else if constexpr (S == 2) {
+            if (r & 1) continue;
+            i = r >> 1;
+        } else {
+            if (r % s != 0) continue;
+            i = r / s;
+        }
+        if (i < nout) { tk[n] = kk; ti[n] = i; ++n; }
+    }
+    return n;
+}
+
+constexpr int kCh = 8;                                        // channels per col2im thread
+template <typename T, int S>
 __global__ void __launch_bounds__(kThreads) col2im_mask_kernel(const float *__restrict__ dt, const T *__restrict__ x,
                                                                ConvBwdGeom q, float scale_a, float norm,
                                                                __nv_bfloat16 *__restrict__ gx, float *__restrict__ sum) {
     pdl_launch_dependents();
     pdl_wait();
-    const int64_t total = q.B * q.C * q.H * q.W;
+    const uint32_t pix = blockIdx.x * kThreads + threadIdx.x;
+    const uint32_t W = static_cast<uint32_t>(q.W), hwin = static_cast<uint32_t>(q.H * q.W);
+    const int64_t cgroups = (q.C + kCh - 1) / kCh;
     float tsum = 0.0f;
-    for (int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t w = e % q.W, r1 = e / q.W, h = r1 % q.H, r2 = r1 / q.H, c = r2 % q.C, b = r2 / q.C;
-        float acc = 0.0f;
-        for (int kh = 0; kh < q.k; ++kh) {
-            const int64_t hn = h + q.p - static_cast<int64_t>(kh) * q.d;
-            if (hn < 0 || hn % q.s != 0 || hn / q.s >= q.Ho) continue;
-            const int64_t i = hn / q.s;
-            for (int kw = 0; kw < q.k; ++kw) {
-                const int64_t wn = w + q.p - static_cast<int64_t>(kw) * q.d;
-                if (wn < 0 || wn % q.s != 0 || wn / q.s >= q.Wo) continue;
-                const int64_t j = wn / q.s;
-                const int64_t t = (c * q.k + kh) * q.k + kw;
-                acc = __fadd_rn(acc, __ldg(dt + t * q.P + (b * q.Ho + i) * q.Wo + j));
+    if (pix < hwin) {
+        const int h = static_cast<int>(pix / W), w = static_cast<int>(pix - (pix / W) * W);
+        int hk[kMaxTapList], hi[kMaxTapList], wk[kMaxTapList], wj[kMaxTapList];
+        const int nh = tap_list<S>(h, q.p, q.k, q.d, q.s, static_cast<int>(q.Ho), hk, hi);
+        const int nw = tap_list<S>(w, q.p, q.k, q.d, q.s, static_cast<int>(q.Wo), wk, wj);
+        const int64_t tstride = static_cast<int64_t>(q.k) * q.k * q.P;        // one channel further: k*k rows
+        for (int64_t unit = blockIdx.y; unit < q.B * cgroups; unit += gridDim.y) {
+            const int64_t b = unit / cgroups, c0 = (unit - b * cgroups) * kCh;
+            const int nc = q.C - c0 < kCh ? static_cast<int>(q.C - c0) : kCh;
+            const float *db = dt + b * q.Ho * q.Wo + c0 * tstride;
+            // kCh channels of this pixel: each tap's kCh loads are independent
+            float acc[kCh];
+#pragma unroll
+            for (int ci = 0; ci < kCh; ++ci) acc[ci] = 0.0f;
+            for (int a = 0; a < nh; ++a) {
+                for (int e = 0; e < nw; ++e) {
+                    const float *dr = db + (static_cast<int64_t>(hk[a]) * q.k + wk[e]) * q.P +
+                                      static_cast<int64_t>(hi[a]) * q.Wo + wj[e];
+                    float v[kCh];
+#pragma unroll
+                    for (int ci = 0; ci < kCh; ++ci) v[ci] = ci < nc ? __ldg(dr + ci * tstride) : 0.0f;
+#pragma unroll
+                    for (int ci = 0; ci < kCh; ++ci) acc[ci] = __fadd_rn(acc[ci], v[ci]);
+                }
+            }
+            const int64_t base = (b * q.C + c0) * hwin + pix;
+            float xv[kCh];
+#pragma unroll
+            for (int ci = 0; ci < kCh; ++ci) xv[ci] = ci < nc ? ld_f32<T>(x, base + ci * static_cast<int64_t>(hwin)) : 0.0f;
+#pragma unroll
+            for (int ci = 0; ci < kCh; ++ci) {
+                if (ci >= nc) break;
+                const float y = __bfloat162float(__float2bfloat16_rn(acc[ci]));
+                float qv = __fdiv_rn(xv[ci], scale_a);
+                if constexpr (sizeof(T) == 2) qv = __bfloat162float(__float2bfloat16_rn(qv));
+                const float ym = __fmul_rn(y, (qv < -1.0f || qv > 1.0f) ? 0.0f : 1.0f);
+                const float sg = (xv[ci] > 0.0f ? 1.0f : 0.0f) - (xv[ci] < 0.0f ? 1.0f : 0.0f);
+                tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(ym, sg), norm));
+                gx[base + ci * static_cast<int64_t>(hwin)] = __float2bfloat16_rn(ym);   // ym is bf16-exact
             }
         }
-        const float y = __bfloat162float(__float2bfloat16_rn(acc));
-        const float xv = ld_f32<T>(x, e);
-        float qv = __fdiv_rn(xv, scale_a);
-        if constexpr (sizeof(T) == 2) qv = __bfloat162float(__float2bfloat16_rn(qv));
-        const float ym = __fmul_rn(y, (qv < -1.0f || qv > 1.0f) ? 0.0f : 1.0f);
-        const float sg = (xv > 0.0f ? 1.0f : 0.0f) - (xv < 0.0f ? 1.0f : 0.0f);
-        tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(ym, sg), norm));
-        gx[e] = __float2bfloat16_rn(ym);                      // ym is bf16-exact
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xFFFFFFFFu, tsum, o);
     if ((threadIdx.x & 31) == 0) atomicAdd(sum, tsum);
 }
+
+template <typename T>
+cudaError_t launch_col2im(const float *dt, const T *x, const ConvBwdGeom &q, float scale_a, float norm,
+                          __nv_bfloat16 *gx, float *sum, cudaStream_t s);
 
 // grad_w[i] = out_t(alpha * sum over the K splits of part[s][i]), fp32 sums in
 // split order.
@@ -150,6 +212,21 @@ __global__ void __launch_bounds__(kThreads) split_sum_kernel(const float *__rest
     }
 }
 
+// Grid (columns / 256, rows) for the row-mapped kernels above (rows capped
+// at 65535; the kernels loop over the rest).
+template <typename K, typename... Args>
+cudaError_t launch_rows(K kern, int64_t cols, int64_t rows, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute pdl = pdl_attribute();
+    cfg.gridDim = dim3(static_cast<unsigned>((cols + kThreads - 1) / kThreads),
+                       static_cast<unsigned>(rows < 65535 ? (rows > 0 ? rows : 1) : 65535));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename K, typename... Args>
 cudaError_t launch_flat(K kern, int64_t work, cudaStream_t s, Args... args) {
     int64_t blocks = (work + kThreads - 1) / kThreads;
@@ -164,6 +241,15 @@ cudaError_t launch_flat(K kern, int64_t work, cudaStream_t s, Args... args) {
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename T>
+cudaError_t launch_col2im(const float *dt, const T *x, const ConvBwdGeom &q, float scale_a, float norm,
+                          __nv_bfloat16 *gx, float *sum, cudaStream_t s) {
+    const int64_t cols = q.H * q.W, rows = q.B * ((q.C + kCh - 1) / kCh);
+    if (q.s == 1) return launch_rows(col2im_mask_kernel<T, 1>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
+    if (q.s == 2) return launch_rows(col2im_mask_kernel<T, 2>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
+    return launch_rows(col2im_mask_kernel<T, 0>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
 }
 
 float bf16_round_h(float v) {
@@ -255,8 +341,10 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
     ConvBwdPlan pl;
     if (!make_plan(B, C, H, W, O, kernel_size, stride, padding, dilation, pl)) return BT_ERR_INVALID_ARG;
     const ConvBwdGeom &q = pl.q;
-    if (O % 8 != 0 || B > 65535) return BT_ERR_UNSUPPORTED;
-    if (q.P > (int64_t(1) << 31) - 512 || q.T > (int64_t(1) << 24)) return BT_ERR_UNSUPPORTED;
+    if (O % 8 != 0 || B > 65535 || kernel_size > 8) return BT_ERR_UNSUPPORTED;
+    if (q.P > (int64_t(1) << 31) - 512 || q.T > (int64_t(1) << 24) || H * W > (int64_t(1) << 31) - 512 ||
+        pl.ldp > (int64_t(1) << 31) - 512)
+        return BT_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (B == 0) {
         if (grad_scale_a != nullptr && cudaMemsetAsync(grad_scale_a, 0, sizeof(float), s) != cudaSuccess) return BT_ERR_CUDA;
@@ -299,24 +387,24 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
                            nullptr, err, s) != cudaSuccess)
             return BT_ERR_CUDA;
         const float norm = static_cast<float>(1.0 / std::sqrt(static_cast<double>(B) * C * H * W));
-        const int64_t n = B * C * H * W;
         const cudaError_t e =
             x_dtype == BT_F32
-                ? launch_flat(col2im_mask_kernel<float>, n, s, dt, static_cast<const float *>(x), q, scale_a, norm,
-                              static_cast<__nv_bfloat16 *>(grad_x), sum)
-                : launch_flat(col2im_mask_kernel<__nv_bfloat16>, n, s, dt, static_cast<const __nv_bfloat16 *>(x), q,
-                              scale_a, norm, static_cast<__nv_bfloat16 *>(grad_x), sum);
+                ? launch_col2im(dt, static_cast<const float *>(x), q, scale_a, norm, static_cast<__nv_bfloat16 *>(grad_x),
+                                sum, s)
+                : launch_col2im(dt, static_cast<const __nv_bfloat16 *>(x), q, scale_a, norm,
+                                static_cast<__nv_bfloat16 *>(grad_x), sum, s);
         if (e != cudaSuccess) return BT_ERR_CUDA;
     }
     if (grad_w != nullptr) {
         uint16_t *go = reinterpret_cast<uint16_t *>(ws + pl.go_off);
         uint16_t *u = reinterpret_cast<uint16_t *>(ws + pl.u_off);
         float *part = reinterpret_cast<float *>(ws + pl.part_off);
-        cudaError_t e = launch_flat(g_rows_kernel, q.O * pl.ldp, s, g16, q, pl.ldp, go);
+        cudaError_t e = launch_rows(g_rows_kernel, pl.ldp, q.O, s, g16, q, pl.ldp, go);
         if (e == cudaSuccess)
             e = x_dtype == BT_F32
-                    ? launch_flat(sign_im2col_t_kernel<float>, q.T * pl.ldp, s, static_cast<const float *>(x), q, pl.ldp, u)
-                    : launch_flat(sign_im2col_t_kernel<__nv_bfloat16>, q.T * pl.ldp, s,
+                    ? launch_rows(sign_im2col_t_kernel<float>, pl.ldp, (q.T + kTapRows - 1) / kTapRows, s,
+                                  static_cast<const float *>(x), q, pl.ldp, u)
+                    : launch_rows(sign_im2col_t_kernel<__nv_bfloat16>, pl.ldp, (q.T + kTapRows - 1) / kTapRows, s,
                                   static_cast<const __nv_bfloat16 *>(x), q, pl.ldp, u);
         if (e == cudaSuccess) e = launch_tc_bf16_splitk(go, pl.ldp, u, pl.ldp, O, q.T, pl.ldp, pl.splits, 1.0f, part, err, s);
         if (e == cudaSuccess)
