@@ -294,6 +294,45 @@ size_t bt_binary_linear_noalloc_max_bytes(void);
 bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo);
 
 /* ------------------------------------------------------------------------
+ * Device-side scales (no host synchronisation). The page's forward reads the
+ * scales with .item() (BinaryConv2dForward.forward: scale_a.item() *
+ * scale_w.item()), a host round trip per call; these variants take them from
+ * device memory, where BinaryConv2dCutlass.set_activation's first-call
+ * initialisation can be computed by bt_scale_init.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * bt_scale_init -- scale_out = (factor * x.abs().mean()).to(scale_dtype), the
+ * activation scale BinaryConv2dCutlass.set_activation sets on the first
+ * forward (factor 2 for a symmetric layer, 4 otherwise). x: n elements of
+ * x_dtype (F32, BF16, F16) in device memory; the mean is the exact sum of
+ * |x| (double) divided by n, rounded once to x_dtype; factor * mean is
+ * rounded to x_dtype, then to scale_dtype (F32, BF16, F16); the result is
+ * written as one device float. Uses one device-global accumulator per GPU:
+ * calls on one GPU must not overlap. Errors: INVALID_ARG (dtypes, n < 1,
+ * factor not finite > 0, null), ALIGNMENT, CUDA.
+ */
+bt_status bt_scale_init(const void *x, bt_dtype x_dtype, int64_t n, float factor, bt_dtype scale_dtype,
+                        float *scale_out, bt_stream stream);
+
+/*
+ * bt_binary_linear_dscale / bt_binary_conv2d_dscale -- bt_binary_linear /
+ * bt_binary_conv2d with the scales read on the device: `scales` points to two
+ * device floats {scale_a, scale_w}, 8-byte aligned; alpha = fp32(scale_a *
+ * scale_w) as for the host floats. The scales are used as they are (the host
+ * cannot check them). Same results, layouts and errors otherwise.
+ */
+bt_status bt_binary_linear_dscale(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t M,
+                                  int64_t N, int64_t K, const float *scales, const float *bias_a, int64_t bias_len,
+                                  void *out, bt_dtype out_dtype, bt_algo algo, void *workspace,
+                                  size_t workspace_bytes, bt_stream stream);
+bt_status bt_binary_conv2d_dscale(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t B,
+                                  int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
+                                  int padding, int dilation, const float *scales, const float *bias_a,
+                                  int64_t bias_len, void *out, bt_dtype out_dtype, bt_algo algo, void *workspace,
+                                  size_t workspace_bytes, bt_stream stream);
+
+/* ------------------------------------------------------------------------
  * Backward of the binary linear layer (straight-through estimator).
  * bitorch-engine BinaryLinearForward.backward states the steps for the linear
  * layer; BinaryConv2dForward.backward writes them out (for the convolution):

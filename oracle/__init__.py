@@ -439,3 +439,21 @@ def conv2d_backward(x, w, g, scale_a: float, scale_w: float, stride: int, paddin
             "grad_scale_a_abs": float(np.abs(terms.astype(np.float64)).sum()),
             "grad_weight": bf16_round(gw_exact), "grad_weight_exact": gw_exact}
 
+
+def scale_init(x, factor: float, x_dtype: str, scale_dtype: str) -> float:
+    """BinaryConv2dCutlass.set_activation's first-call scale:
+    (factor * x.abs().mean()).to(layer dtype). Reading: the mean is the exact
+    sum of |x| (float64) divided by n (one double division), rounded once to
+    x's dtype (x.abs().mean() is a tensor of x's dtype); factor * mean is
+    rounded to x's dtype, then to the layer's dtype."""
+    def to(v, dt):
+        v = np.asarray(v, dtype=np.float64)
+        if dt == "bf16":
+            return float(bf16_round(v))
+        if dt == "f16":
+            return float(torch.tensor(float(v), dtype=torch.float64).to(torch.float16).item())
+        return float(np.float32(v))
+    a = np.abs(_as_f32(x).astype(np.float64))
+    mean = to(a.sum() / a.size, x_dtype)
+    return to(to(np.float64(factor) * mean, x_dtype), scale_dtype)
+

@@ -264,3 +264,19 @@ def test_conv_backward_abi_validation():
     assert call(O=12) == bt.BT_ERR_UNSUPPORTED                                  # O not a multiple of 8
     assert call(gx=None) == bt.BT_ERR_INVALID_ARG                               # grad_scale_a without grad_x
     assert call(ldw=8) == bt.BT_ERR_INVALID_ARG                                 # ldw < O
+
+
+def test_device_scale_abi_validation():
+    si = bt._c_scale_init
+    assert si(256, bt.BT_I32, 10, 2.0, bt.BT_BF16, 512, None) == bt.BT_ERR_INVALID_ARG
+    assert si(256, bt.BT_BF16, 10, 2.0, bt.BT_I32, 512, None) == bt.BT_ERR_INVALID_ARG
+    assert si(256, bt.BT_BF16, 0, 2.0, bt.BT_BF16, 512, None) == bt.BT_ERR_INVALID_ARG
+    assert si(256, bt.BT_BF16, 10, 0.0, bt.BT_BF16, 512, None) == bt.BT_ERR_INVALID_ARG
+    assert si(None, bt.BT_BF16, 10, 2.0, bt.BT_BF16, 512, None) == bt.BT_ERR_INVALID_ARG
+    assert si(257, bt.BT_BF16, 10, 2.0, bt.BT_BF16, 512, None) == bt.BT_ERR_ALIGNMENT
+    ld = bt._c_lin_ds
+    assert ld(256, bt.BT_BF16, 512, bt.BT_CODE_E2M1, 4, 4, 64, None, None, 0, 768, bt.BT_BF16, 0, 1024, 4096,
+              None) == bt.BT_ERR_INVALID_ARG                                     # no scales
+    cd = bt._c_conv_ds
+    assert cd(256, bt.BT_BF16, 512, bt.BT_CODE_E2M1, 1, 8, 4, 4, 8, 3, 1, 1, 1, None, None, 0, 768, bt.BT_BF16,
+              0, 1024, 1 << 20, None) == bt.BT_ERR_INVALID_ARG

@@ -621,3 +621,28 @@ def test_planted_conv_backward_mistakes_are_caught(mistake):
     o = oracle.conv2d_backward(x, w, g, 0.7, 0.4, 1, 0, 2, "bf16")
     gi, gw = _conv_backward_scatter(x, w, g, 0.7, 0.4, 1, 0, 2, mistake)
     assert not (np.allclose(o["grad_input_exact"], gi) and np.allclose(o["grad_weight_exact"], gw))
+
+
+# ---------------------------------------------------------------------------
+# Activation scale initialisation (set_activation)
+# ---------------------------------------------------------------------------
+
+def test_scale_init_hand_example():
+    # |x| = [1, 3, 2, 2]: mean 2, symmetric factor 2 -> 4; asymmetric factor 4 -> 8
+    x = np.array([1.0, -3.0, 2.0, -2.0], np.float32)
+    assert oracle.scale_init(x, 2.0, "bf16", "bf16") == 4.0
+    assert oracle.scale_init(x, 4.0, "f32", "f32") == 8.0
+    # mean 1/3 in bf16: 0.333984375 (1.0101011b * 2^-2 rounded up), times 2 -> 0.66796875
+    y = np.array([1.0, 0.0, 0.0], np.float32)
+    assert oracle.scale_init(y, 2.0, "bf16", "bf16") == 0.66796875
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_scale_init_matches_torch_expression(dt):
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32}[dt]
+    for seed in range(5):
+        x = torch.randn(1000 + 37 * seed, generator=torch.Generator().manual_seed(seed)).to(tdt)
+        want = float((2 * x.abs().mean()).to(tdt))
+        got = oracle.scale_init(x.float().numpy(), 2.0, dt, dt)
+        step = abs(want) * (2.0 ** -7 if dt == "bf16" else 2.0 ** -23)
+        assert abs(got - want) <= step          # torch accumulates in fp32; at most one rounding step apart

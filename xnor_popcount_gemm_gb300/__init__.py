@@ -75,6 +75,11 @@ _c_bwd = _sig("bt_binary_linear_backward", _i, [_p, _i, _p, _i64, _p, _i64, _i64
 _c_cbwd_ws = _sig("bt_binary_conv2d_backward_workspace", _sz, [_i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _i])
 _c_cbwd = _sig("bt_binary_conv2d_backward", _i, [_p, _i, _p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
                                                  _f, _f, _p, _p, _p, _i, _p, _sz, _p])
+_c_scale_init = _sig("bt_scale_init", _i, [_p, _i, _i64, _f, _i, _p, _p])
+_c_lin_ds = _sig("bt_binary_linear_dscale", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _p, _p, _i64, _p, _i, _i,
+                                                _p, _sz, _p])
+_c_conv_ds = _sig("bt_binary_conv2d_dscale", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
+                                                 _p, _p, _i64, _p, _i, _i, _p, _sz, _p])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
 _c_status = _sig("bt_device_status", _i, [_p])
 
@@ -84,7 +89,8 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
             "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
-            "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_binary_conv2d_backward"]
+            "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_binary_conv2d_backward",
+            "bt_scale_init", "bt_binary_linear_dscale", "bt_binary_conv2d_dscale"]
 
 
 class BtError(RuntimeError):
@@ -307,7 +313,9 @@ def bt_binary_linear(x: torch.Tensor, weight: torch.Tensor, w_code: int, K: int,
                      x_packed: bool = False, out: torch.Tensor | None = None,
                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y = cast(fp32(dot * fp32(scale_a*scale_w))) for x [M, K] (or packed rows)
-    and a packed weight [N, row_bytes(K)]."""
+    and a packed weight [N, row_bytes(K)]. Passing a device float tensor
+    {scale_a, scale_w} as scale_a (scale_w ignored) reads the scales on the
+    device (bt_binary_linear_dscale)."""
     _contig(x, "x")
     _contig(weight, "weight")
     M, N = x.shape[0], weight.shape[0]
@@ -319,6 +327,12 @@ def bt_binary_linear(x: torch.Tensor, weight: torch.Tensor, w_code: int, K: int,
         out = torch.empty((M, N), dtype=_TORCH[ot], device=x.device)
     ws = _workspace(bt_binary_linear_workspace(M, K, xt, w_code), x.device, workspace)
     blen = 0 if bias_a is None else bias_a.numel()
+    if isinstance(scale_a, torch.Tensor):
+        # device scales: scale_a is a device float tensor holding {scale_a, scale_w}
+        _contig(scale_a, "scales")
+        _check(_c_lin_ds(_ptr(x), xt, _ptr(weight), w_code, M, N, K, _ptr(scale_a), _ptr(bias_a), blen,
+                         _ptr(out), ot, algo, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+        return out
     _check(_c_lin(_ptr(x), xt, _ptr(weight), w_code, M, N, K, scale_a, scale_w, _ptr(bias_a), blen,
                   _ptr(out), ot, algo, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
     return out
@@ -357,9 +371,28 @@ def bt_binary_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int,
     ws = _workspace(bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, xt, w_code),
                     x.device, workspace)
     blen = 0 if bias_a is None else bias_a.numel()
+    if isinstance(scale_a, torch.Tensor):
+        # device scales: scale_a is a device float tensor holding {scale_a, scale_w}
+        _contig(scale_a, "scales")
+        _check(_c_conv_ds(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding,
+                          dilation, _ptr(scale_a), _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),
+                          0 if ws is None else ws.numel(), _stream(stream)))
+        return out
     _check(_c_conv(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding,
                    dilation, scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),
                    0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def bt_scale_init(x: torch.Tensor, factor: float = 2.0, scale_dtype=None, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """(factor * x.abs().mean()).to(scale_dtype) computed on the device into a
+    one-element float tensor (scale_dtype defaults to x's dtype)."""
+    _contig(x, "x")
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    st = _DT[x.dtype if scale_dtype is None else scale_dtype]
+    _check(_c_scale_init(_ptr(x), _DT[x.dtype], x.numel(), factor, st, _ptr(out), _stream(stream)))
     return out
 
 

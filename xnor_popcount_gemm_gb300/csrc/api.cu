@@ -124,14 +124,16 @@ size_t bt_binary_linear_workspace(int64_t M, int64_t K, bt_dtype x_dtype, bt_cod
     return round_up(static_cast<size_t>(M) * static_cast<size_t>(row_bytes(K, code)), 256);
 }
 
-bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
-                           int64_t M, int64_t N, int64_t K, float scale_a, float scale_w,
-                           const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
-                           bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+namespace {
+// The forward with host scales (scales == nullptr) or device scales.
+bt_status linear_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t M, int64_t N,
+                      int64_t K, float scale_a, float scale_w, const float *scales, const float *bias_a,
+                      int64_t bias_len, void *out, bt_dtype out_dtype, bt_algo algo, void *workspace,
+                      size_t workspace_bytes, bt_stream stream) {
     if (!valid_code(w_code) || !valid_out(out_dtype)) return BT_ERR_INVALID_ARG;
     if (!(float_in(x_dtype) || x_dtype == BT_PACKED)) return BT_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 1) return BT_ERR_INVALID_ARG;
-    if (!valid_scale(scale_a) || !valid_scale(scale_w)) return BT_ERR_INVALID_ARG;
+    if (scales == nullptr && (!valid_scale(scale_a) || !valid_scale(scale_w))) return BT_ERR_INVALID_ARG;
     if (!(bias_len == 0 || bias_len == 1 || bias_len == K)) return BT_ERR_INVALID_ARG;
     if (bias_len > 0 && bias_a == nullptr && x_dtype != BT_PACKED) return BT_ERR_INVALID_ARG;
     if (algo != BT_ALGO_AUTO && algo != algo_for_code(w_code)) {
@@ -142,6 +144,7 @@ bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, 
     if (M == 0 || N == 0) return BT_OK;
     if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16)) return BT_ERR_ALIGNMENT;
+    if (scales != nullptr && !aligned(scales, 8)) return BT_ERR_ALIGNMENT;
     if ((M + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
     const bt_algo run = algo_for_code(w_code);
     if (run != BT_ALGO_POPC && K > kTcMaxK) return BT_ERR_UNSUPPORTED;
@@ -160,11 +163,29 @@ bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, 
     if (run == BT_ALGO_POPC)
         return from_cuda(launch_popc_linear(static_cast<const uint32_t *>(xp),
                                             static_cast<const uint32_t *>(weight), M, N, K, alpha, out,
-                                            out_dtype, s));
+                                            out_dtype, s, scales));
     unsigned int *err = device_error_word();
     if (err == nullptr) return BT_ERR_CUDA;
     return from_cuda(launch_tc_linear(static_cast<const uint8_t *>(xp), static_cast<const uint8_t *>(weight),
-                                      w_code, M, N, K, alpha, out, out_dtype, err, s));
+                                      w_code, M, N, K, alpha, out, out_dtype, err, s, scales));
+}
+}  // namespace
+
+bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                           int64_t M, int64_t N, int64_t K, float scale_a, float scale_w,
+                           const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
+                           bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+    return linear_impl(x, x_dtype, weight, w_code, M, N, K, scale_a, scale_w, nullptr, bias_a, bias_len, out,
+                       out_dtype, algo, workspace, workspace_bytes, stream);
+}
+
+bt_status bt_binary_linear_dscale(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t M,
+                                  int64_t N, int64_t K, const float *scales, const float *bias_a, int64_t bias_len,
+                                  void *out, bt_dtype out_dtype, bt_algo algo, void *workspace,
+                                  size_t workspace_bytes, bt_stream stream) {
+    if (scales == nullptr) return BT_ERR_INVALID_ARG;
+    return linear_impl(x, x_dtype, weight, w_code, M, N, K, 1.0f, 1.0f, scales, bias_a, bias_len, out, out_dtype,
+                       algo, workspace, workspace_bytes, stream);
 }
 
 size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride,
@@ -189,17 +210,18 @@ size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, in
     return n;
 }
 
-bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
-                           int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,
-                           int stride, int padding, int dilation, float scale_a, float scale_w,
-                           const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
-                           bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+namespace {
+bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t B, int64_t C,
+                    int64_t H, int64_t W, int64_t O, int kernel_size, int stride, int padding, int dilation,
+                    float scale_a, float scale_w, const float *scales, const float *bias_a, int64_t bias_len,
+                    void *out, bt_dtype out_dtype, bt_algo algo, void *workspace, size_t workspace_bytes,
+                    bt_stream stream) {
     if (!valid_code(w_code) || !valid_out(out_dtype)) return BT_ERR_INVALID_ARG;
     if (!(float_in(x_dtype) || x_dtype == BT_PACKED || x_dtype == BT_PACKED_IM2COL)) return BT_ERR_INVALID_ARG;
     if (x_dtype == BT_PACKED_IM2COL && w_code == BT_CODE_BITS) return BT_ERR_INVALID_ARG;
     if (B < 0 || C < 1 || H < 1 || W < 1 || O < 0) return BT_ERR_INVALID_ARG;
     if (kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return BT_ERR_INVALID_ARG;
-    if (!valid_scale(scale_a) || !valid_scale(scale_w)) return BT_ERR_INVALID_ARG;
+    if (scales == nullptr && (!valid_scale(scale_a) || !valid_scale(scale_w))) return BT_ERR_INVALID_ARG;
     if (!(bias_len == 0 || bias_len == 1 || bias_len == C)) return BT_ERR_INVALID_ARG;
     if (bias_len > 0 && bias_a == nullptr && float_in(x_dtype)) return BT_ERR_INVALID_ARG;
     if (algo != BT_ALGO_AUTO && algo != algo_for_code(w_code)) {
@@ -217,6 +239,7 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
     if (B == 0 || O == 0) return BT_OK;
     if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16)) return BT_ERR_ALIGNMENT;
+    if (scales != nullptr && !aligned(scales, 8)) return BT_ERR_ALIGNMENT;
     const int64_t M = B * g.Ho * g.Wo;
     if ((M + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
     const bt_algo run = algo_for_code(w_code);
@@ -236,14 +259,14 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
     if (err == nullptr) return BT_ERR_CUDA;
     if (x_dtype == BT_PACKED_IM2COL)
         return from_cuda(launch_tc_conv(static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(weight), w_code,
-                                        g, alpha, out, out_dtype, err, s));
+                                        g, alpha, out, out_dtype, err, s, scales));
     uint8_t *rows = ws + (x_dtype == BT_PACKED ? 0 : round_up(static_cast<size_t>(B * H * W * rbc), 256));
     if (run != BT_ALGO_POPC && x_dtype != BT_PACKED) {
         // one pass from x to the im2col rows, where the staged unfold applies
         const cudaError_t e = launch_pack_im2col(x, x_dtype, g, bias_a, bias_len, w_code, rows, false, s);
         if (e == cudaSuccess)
             return from_cuda(launch_tc_conv(rows, static_cast<const uint8_t *>(weight), w_code, g, alpha, out,
-                                            out_dtype, err, s));
+                                            out_dtype, err, s, scales));
         if (e != cudaErrorNotSupported) return BT_ERR_CUDA;
     }
     const void *xp = x;
@@ -254,11 +277,31 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
     }
     if (run == BT_ALGO_POPC)
         return from_cuda(launch_popc_conv(static_cast<const uint32_t *>(xp), static_cast<const uint32_t *>(weight),
-                                          g, alpha, out, out_dtype, s));
+                                          g, alpha, out, out_dtype, s, scales));
     cudaError_t e = launch_im2col_rows(static_cast<const uint8_t *>(xp), g, rbc, rows, s);
     if (e != cudaSuccess) return BT_ERR_CUDA;
     return from_cuda(launch_tc_conv(rows, static_cast<const uint8_t *>(weight), w_code, g, alpha, out, out_dtype, err,
-                                    s));
+                                    s, scales));
+}
+}  // namespace
+
+bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                           int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,
+                           int stride, int padding, int dilation, float scale_a, float scale_w,
+                           const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
+                           bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+    return conv_impl(x, x_dtype, weight, w_code, B, C, H, W, O, kernel_size, stride, padding, dilation, scale_a,
+                     scale_w, nullptr, bias_a, bias_len, out, out_dtype, algo, workspace, workspace_bytes, stream);
+}
+
+bt_status bt_binary_conv2d_dscale(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t B,
+                                  int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
+                                  int padding, int dilation, const float *scales, const float *bias_a,
+                                  int64_t bias_len, void *out, bt_dtype out_dtype, bt_algo algo, void *workspace,
+                                  size_t workspace_bytes, bt_stream stream) {
+    if (scales == nullptr) return BT_ERR_INVALID_ARG;
+    return conv_impl(x, x_dtype, weight, w_code, B, C, H, W, O, kernel_size, stride, padding, dilation, 1.0f, 1.0f,
+                     scales, bias_a, bias_len, out, out_dtype, algo, workspace, workspace_bytes, stream);
 }
 
 int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride, int padding,

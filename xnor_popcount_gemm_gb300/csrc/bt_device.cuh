@@ -174,4 +174,10 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// alpha = fp32(scale_a * scale_w) from two device floats: the product of two
+// floats is exact in double, rounded once to float.
+__device__ __forceinline__ float alpha_from(const float *scales) {
+    return __double2float_rn(__dmul_rn(static_cast<double>(scales[0]), static_cast<double>(scales[1])));
+}
+
 }  // namespace bt

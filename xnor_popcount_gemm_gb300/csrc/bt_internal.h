@@ -61,18 +61,22 @@ cudaError_t launch_im2col_rows(const uint8_t *xp, const ConvGeom &g, int64_t rbc
 // Bytes of that matrix.
 inline int64_t im2col_bytes(const ConvGeom &g, int64_t rbc) { return g.B * g.Ho * g.Wo * g.k * g.k * rbc; }
 
+// The contraction launchers scale by alpha, or, when `scales` is not null, by
+// fp32(scales[0] * scales[1]) read on the device (two device floats: scale_a,
+// scale_w), so that device-side scales need no host synchronisation.
 cudaError_t launch_popc_linear(const uint32_t *xp, const uint32_t *wp, int64_t M, int64_t N,
-                               int64_t K, float alpha, void *out, bt_dtype out_t, cudaStream_t s);
+                               int64_t K, float alpha, void *out, bt_dtype out_t, cudaStream_t s,
+                               const float *scales = nullptr);
 cudaError_t launch_popc_conv(const uint32_t *xp, const uint32_t *wp, const ConvGeom &g, float alpha,
-                             void *out, bt_dtype out_t, cudaStream_t s);
+                             void *out, bt_dtype out_t, cudaStream_t s, const float *scales = nullptr);
 
 cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M,
                              int64_t N, int64_t K, float alpha, void *out, bt_dtype out_t,
-                             unsigned int *err, cudaStream_t s);
+                             unsigned int *err, cudaStream_t s, const float *scales = nullptr);
 // rows: the im2col rows of the packed input (launch_im2col_rows); output NCHW.
 cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code, const ConvGeom &g,
                            float alpha, void *out, bt_dtype out_t, unsigned int *err,
-                           cudaStream_t s);
+                           cudaStream_t s, const float *scales = nullptr);
 
 // bf16 x bf16 contraction on the tensor cores (tcgen05 kind::f16, fp32
 // accumulators), for the backward's products: a code value beside bt_code's.

@@ -34,6 +34,7 @@ struct PopcArgs {
     int Kdot;                 // K (linear) or C (conv)
     int nslots;               // 4-word slots along the reduction
     float alpha;
+    const float *scales;      // not null: alpha = fp32(scales[0] * scales[1]) read here
     void *out;
     // conv geometry
     int H, W, Ho, Wo, k, s, p, d;
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(kThreads) popc_kernel(const PopcArgs a) {
 
     using OT = typename OutT<OUT>::type;
     OT *out = static_cast<OT *>(a.out);
+    const float alpha = a.scales != nullptr ? alpha_from(a.scales) : a.alpha;
     if (!CONV) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) popc_kernel(const PopcArgs a) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int64_t n = n0 + rbw[j];
-                if (n < a.N) out[m * a.N + n] = OutT<OUT>::cvt(a.Kdot - 2 * acc[i][j], a.alpha);
+                if (n < a.N) out[m * a.N + n] = OutT<OUT>::cvt(a.Kdot - 2 * acc[i][j], alpha);
             }
         }
     } else {
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) popc_kernel(const PopcArgs a) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int64_t o = n0 + rbw[j];
-                if (o < a.N) out[(b * a.N + o) * hw + pix] = OutT<OUT>::cvt(base - 2 * acc[i][j], a.alpha);
+                if (o < a.N) out[(b * a.N + o) * hw + pix] = OutT<OUT>::cvt(base - 2 * acc[i][j], alpha);
             }
         }
     }
@@ -206,25 +208,25 @@ cudaError_t launch(const PopcArgs &a, bt_dtype out_t, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_popc_linear(const uint32_t *xp, const uint32_t *wp, int64_t M, int64_t N, int64_t K,
-                               float alpha, void *out, bt_dtype out_t, cudaStream_t s) {
+                               float alpha, void *out, bt_dtype out_t, cudaStream_t s, const float *scales) {
     PopcArgs a{};
     a.A = xp; a.Bw = wp; a.M = M; a.N = N;
     a.Pw = static_cast<int>(row_bytes(K, BT_CODE_BITS) / 4);
     a.Kdot = static_cast<int>(K);
     a.nslots = a.Pw / 4;
-    a.alpha = alpha; a.out = out;
+    a.alpha = alpha; a.scales = scales; a.out = out;
     return launch<false>(a, out_t, s);
 }
 
 cudaError_t launch_popc_conv(const uint32_t *xp, const uint32_t *wp, const ConvGeom &g, float alpha,
-                             void *out, bt_dtype out_t, cudaStream_t s) {
+                             void *out, bt_dtype out_t, cudaStream_t s, const float *scales) {
     PopcArgs a{};
     a.A = xp; a.Bw = wp;
     a.M = g.B * g.Ho * g.Wo; a.N = g.O;
     a.Pw = static_cast<int>(row_bytes(g.C, BT_CODE_BITS) / 4);
     a.Kdot = static_cast<int>(g.C);
     a.nslots = g.k * g.k * (a.Pw / 4);
-    a.alpha = alpha; a.out = out;
+    a.alpha = alpha; a.scales = scales; a.out = out;
     a.H = static_cast<int>(g.H); a.W = static_cast<int>(g.W);
     a.Ho = static_cast<int>(g.Ho); a.Wo = static_cast<int>(g.Wo);
     a.k = g.k; a.s = g.s; a.p = g.p; a.d = g.d;

@@ -93,6 +93,7 @@ struct TcArgs {
     int64_t split_out;         // split-K: output elements between the splits' partial results
     uint32_t idesc;            // instruction descriptor
     float alpha;
+    const float *scales;       // not null: alpha = fp32(scales[0] * scales[1]), read by the epilogue
     void *out;
     unsigned int *err;
     int vec;                   // rows: 1 when output rows are 16-byte aligned (16-byte stores)
@@ -495,6 +496,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
         T *const out_base = static_cast<T *>(a.out);
         const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // this warp's staging box
         constexpr bool kMask = LAYOUT == kRowsMaskBf16 || LAYOUT == kRowsMaskF32;
+        const float alpha = a.scales != nullptr ? alpha_from(a.scales) : a.alpha;
         float tsum = 0.0f;                                // masked layouts: this lane's grad_scale_a terms
         int local = 0;
         for (int st = unit; st < a.num_super; st += nunits, ++local) {
@@ -549,7 +551,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
 #pragma unroll
                 for (int q = 0; q < kChunks; ++q) {
                     const uint32_t addr = sbox + static_cast<uint32_t>(lane * kBoxInner) + (box_chunk<kElem>(q, lane) << 4);
-                    const uint4 w = chunk16<OUT, kElem>(r, q * (16 / kElem), a.alpha);
+                    const uint4 w = chunk16<OUT, kElem>(r, q * (16 / kElem), alpha);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w.x), "r"(w.y), "r"(w.z),
                                  "r"(w.w)
                                  : "memory");
@@ -882,13 +884,15 @@ bool tc_available() { return encode_tiled() != nullptr; }
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encode_tiled(); }
 
 cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code, int64_t M, int64_t N, int64_t K,
-                             float alpha, void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
+                             float alpha, void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s,
+                             const float *scales) {
     TcArgs a{};
     Maps mp;
     TileCfg c;
     const int64_t rb = row_bytes(K, code);
     if (!plan(a, mp, c, code, xp, wp, M, N, rb, rb, rb)) return cudaErrorInvalidValue;
     a.alpha = alpha;
+    a.scales = scales;
     a.out = out;
     a.err = err;
     const int64_t ob = out_elem_bytes(out_t);
@@ -897,7 +901,7 @@ cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code,
 }
 
 cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
-                           void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s) {
+                           void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s, const float *scales) {
     // D = W x rows^T: rows of the tile are output channels, columns output pixels.
     const int64_t krow = static_cast<int64_t>(g.k) * g.k * row_bytes(g.C, code);
     TcArgs a{};
@@ -905,6 +909,7 @@ cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code,
     TileCfg c;
     if (!plan(a, mp, c, code, wp, rows, g.O, g.B * g.Ho * g.Wo, krow, krow, krow)) return cudaErrorInvalidValue;
     a.alpha = alpha;
+    a.scales = scales;
     a.out = out;
     a.err = err;
     a.hw = g.Ho * g.Wo;
