@@ -20,6 +20,9 @@ plain numpy / PyTorch CPU ops. Every function cites the passage it follows:
   formula and the unfold + mm lowering of a convolution.
 * torch/ao/quantization/experimental/linear.py, ``LinearAPoT.matmul``: the
   plain i-j-k triple loop of a matrix product.
+* banghao.live/blog/9, sections 3 and 4 (``MyQuantConv2d.forward``): the
+  W8A8 im2col + gemm convolution, with and without the SmoothQuant per-column
+  scale migration ``scale = sqrt(act_max / weight_max)``.
 * bitorch-engine ``BinaryConv2dForward.backward`` (the straight-through
   backward written out in code) and ``BinaryLinearForward.backward`` (the
   same steps in prose for the linear layer): ``grad_input`` from the upstream
@@ -62,6 +65,7 @@ import threading
 
 import numpy as np
 import torch
+import torch.nn.functional as F
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "bt_oracle.c")
@@ -456,4 +460,58 @@ def scale_init(x, factor: float, x_dtype: str, scale_dtype: str) -> float:
     a = np.abs(_as_f32(x).astype(np.float64))
     mean = to(a.sum() / a.size, x_dtype)
     return to(to(np.float64(factor) * mean, x_dtype), scale_dtype)
+
+
+# ----------------------------------------------------------------------------
+# W8A8 im2col + gemm convolution (banghao.live/blog/9 sections 3 and 4)
+# ----------------------------------------------------------------------------
+
+def fake_quant_int8(v: np.ndarray):
+    """The quantizers the page applies to the im2col rows and the flattened
+    weights, read as per-tensor symmetric int8 on [-127, 127] with a dynamic
+    max: amax = max|v|, scale = fp32(amax / 127), q = clamp(round-half-even(
+    v * fp32(1 / scale)), -127, 127) (torch's fake-quant rounding); returns q
+    (int64) and scale. An all-zero tensor gives q = 0, scale = 0."""
+    v = np.asarray(v, dtype=np.float32)
+    amax = np.float32(np.abs(v).max()) if v.size else np.float32(0)
+    if amax == 0:
+        return np.zeros(v.shape, np.int64), np.float32(0)
+    scale = np.float32(amax / np.float32(127))
+    inv = np.float32(np.float32(1) / scale)
+    q = np.clip(np.rint((v * inv).astype(np.float32)), -127, 127).astype(np.int64)
+    return q, scale
+
+
+def w8a8_conv2d(x, w, stride: int, padding: int, dilation: int, smooth: bool = False) -> dict:
+    """MyQuantConv2d.forward: unfold x into im2col rows [P, C*k*k] (zero
+    padding), flatten w to [O, C*k*k]; with SmoothQuant, per column
+    act = max|rows|, wmax = max|w|, scale = sqrt(act / wmax) (fp32), rows /=
+    scale, w *= scale; quantize both (fake_quant_int8); the product of the
+    dequantized values is sum(q_x * q_w) * s_x * s_w, taken exactly and
+    rounded as y = fp32(double(dot) * double(fp32(s_x * s_w))); NCHW out."""
+    x32 = torch.from_numpy(_as_f32(x))
+    w32 = _as_f32(w)
+    B, C, H, W = x32.shape
+    O, _, k, _ = w32.shape
+    ho = conv2d_out_size(H, k, stride, padding, dilation)
+    wo = conv2d_out_size(W, k, stride, padding, dilation)
+    rows = F.unfold(x32, k, dilation=dilation, padding=padding, stride=stride)     # [B, C*k*k, L]
+    rows = rows.transpose(1, 2).reshape(-1, C * k * k).numpy().astype(np.float32)
+    wf = w32.reshape(O, C * k * k).astype(np.float32)
+    scale_col = None
+    if smooth:
+        act = np.abs(rows).max(axis=0).astype(np.float32)
+        wmax = np.abs(wf).max(axis=0).astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            scale_col = np.sqrt((act / wmax).astype(np.float32)).astype(np.float32)
+            rows = (rows / scale_col).astype(np.float32)
+            wf = (wf * scale_col).astype(np.float32)
+    qx, sx = fake_quant_int8(rows)
+    qw, sw = fake_quant_int8(wf)
+    dot = qx @ qw.T                                                                # exact int64 [P, O]
+    alpha = np.float32(np.float64(sx) * np.float64(sw))
+    y = (dot.astype(np.float64) * np.float64(alpha)).astype(np.float32)
+    y = y.reshape(B, ho * wo, O).transpose(0, 2, 1).reshape(B, O, ho, wo)
+    return {"y": np.ascontiguousarray(y), "dot": dot, "qx": qx, "qw": qw, "sx": sx, "sw": sw, "alpha": alpha,
+            "scale": scale_col, "rows": rows, "wf": wf}
 

@@ -646,3 +646,60 @@ def test_scale_init_matches_torch_expression(dt):
         got = oracle.scale_init(x.float().numpy(), 2.0, dt, dt)
         step = abs(want) * (2.0 ** -7 if dt == "bf16" else 2.0 ** -23)
         assert abs(got - want) <= step          # torch accumulates in fp32; at most one rounding step apart
+
+
+# ---------------------------------------------------------------------------
+# W8A8 im2col + gemm convolution, with and without SmoothQuant
+# ---------------------------------------------------------------------------
+
+def test_golden_w8a8():
+    for ex in json.load(open(GOLDEN))["w8a8_conv"]:
+        o = oracle.w8a8_conv2d(np.array(ex["x"], np.float32), np.array(ex["w"], np.float32), ex["stride"],
+                               ex["padding"], ex["dilation"], ex["smooth"])
+        if "qx" in ex:
+            np.testing.assert_array_equal(o["qx"], ex["qx"], ex["why"])
+            np.testing.assert_array_equal(o["qw"], ex["qw"], ex["why"])
+            np.testing.assert_array_equal(o["dot"], ex["dot"], ex["why"])
+        if "balanced_max" in ex:
+            np.testing.assert_allclose(np.abs(o["rows"]).max(0), ex["balanced_max"], rtol=3e-7)
+            np.testing.assert_allclose(np.abs(o["wf"]).max(0), ex["balanced_max"], rtol=3e-7)
+
+
+def test_fake_quant_matches_torch_fake_quantize():
+    v = (torch.randn(5000, generator=torch.Generator().manual_seed(3)) * 3).numpy()
+    v[:4] = [0.0, -0.0, 1e-6, -2.5]
+    q, scale = oracle.fake_quant_int8(v)
+    want = torch.fake_quantize_per_tensor_affine(torch.from_numpy(v), float(scale), 0, -127, 127).numpy()
+    np.testing.assert_array_equal((q * np.float32(scale)).astype(np.float32), want)
+
+
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", [(2, 3, 7, 6, 4, 3, 1, 1, 1), (1, 4, 9, 9, 3, 3, 2, 1, 1),
+                                               (2, 2, 8, 8, 5, 3, 2, 2, 2), (1, 5, 5, 5, 2, 1, 1, 0, 1)])
+def test_w8a8_integer_inputs_reduce_to_conv2d(B, C, H, W, O, k, s, p, d):
+    # integer values with max |x| = max |w| = 127 quantize to themselves, so
+    # the dot is the plain convolution of x and w
+    rng = np.random.default_rng(B * 100 + C * 10 + k)
+    x = rng.integers(-127, 128, (B, C, H, W)).astype(np.float32)
+    w = rng.integers(-127, 128, (O, C, k, k)).astype(np.float32)
+    x.flat[0], w.flat[0] = 127.0, -127.0
+    o = oracle.w8a8_conv2d(x, w, s, p, d, smooth=False)
+    ho, wo = oracle.conv2d_out_size(H, k, s, p, d), oracle.conv2d_out_size(W, k, s, p, d)
+    want = F.conv2d(torch.from_numpy(x).double(), torch.from_numpy(w).double(), stride=s, padding=p,
+                    dilation=d).numpy()
+    dot = o["dot"].reshape(B, ho * wo, O).transpose(0, 2, 1).reshape(B, O, ho, wo)
+    np.testing.assert_array_equal(dot, want)
+    assert o["sx"] == np.float32(1.0) and o["sw"] == np.float32(1.0)
+    np.testing.assert_array_equal(o["y"], want.astype(np.float32))
+
+
+def test_w8a8_smooth_balances_column_maxima():
+    x = (torch.randn(2, 6, 8, 8, generator=torch.Generator().manual_seed(8)) *
+         torch.linspace(0.1, 20, 6).view(1, 6, 1, 1)).numpy()
+    w = torch.randn(5, 6, 3, 3, generator=torch.Generator().manual_seed(9)).numpy()
+    o = oracle.w8a8_conv2d(x, w, 1, 1, 1, smooth=True)
+    np.testing.assert_allclose(np.abs(o["rows"]).max(0), np.abs(o["wf"]).max(0), rtol=5e-7)
+    # migrating the scale leaves the unquantized product unchanged
+    plain = oracle.w8a8_conv2d(x, w, 1, 1, 1, smooth=False)
+    np.testing.assert_allclose(o["rows"].astype(np.float64) @ o["wf"].T.astype(np.float64),
+                               plain["rows"].astype(np.float64) @ plain["wf"].T.astype(np.float64), rtol=1e-5,
+                               atol=1e-4)
