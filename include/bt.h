@@ -333,6 +333,34 @@ bt_status bt_binary_conv2d_dscale(const void *x, bt_dtype x_dtype, const void *w
                                   size_t workspace_bytes, bt_stream stream);
 
 /* ------------------------------------------------------------------------
+ * W8A8 im2col + gemm convolution (banghao.live/blog/9 sections 3 and 4,
+ * MyQuantConv2d.forward), with optional SmoothQuant.
+ * ------------------------------------------------------------------------ */
+
+/* Workspace bytes bt_w8a8_conv2d needs (0 for invalid sizes). */
+size_t bt_w8a8_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
+                                int padding, int dilation);
+
+/*
+ * bt_w8a8_conv2d -- y = (unfold(x) quantized) @ (w.view(O, -1) quantized)^T
+ * reshaped to NCHW [B, O, Ho, Wo]. x NCHW and w OIHW are F32 or BF16; with
+ * smooth != 0 the per-column scale s = sqrt(max|rows[:, t]| / max|w[:, t]|)
+ * (fp32) divides the im2col rows and multiplies the weight first. Each side
+ * is quantized per tensor: scale = fp32(max|v| / 127), q = clamp(rint(v *
+ * fp32(1 / scale)), -127, 127) (torch's fake-quant rounding; q = 0 when the
+ * tensor is all zeros). The integer dot products are exact (tensor cores on
+ * bf16 copies of q, K split in parts of at most 1024 taps, parts added in
+ * double) and y = fp32(double(dot) * double(fp32(scale_x * scale_w))); out
+ * F32 or BF16 (rounded from that fp32). k <= 8; pointers 16-byte aligned,
+ * workspace 256-byte aligned (bt_w8a8_conv2d_workspace bytes); asynchronous
+ * on `stream`. Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+bt_status bt_w8a8_conv2d(const void *x, bt_dtype x_dtype, const void *w, bt_dtype w_dtype, int64_t B, int64_t C,
+                         int64_t H, int64_t W, int64_t O, int kernel_size, int stride, int padding, int dilation,
+                         int smooth, void *out, bt_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                         bt_stream stream);
+
+/* ------------------------------------------------------------------------
  * Backward of the binary linear layer (straight-through estimator).
  * bitorch-engine BinaryLinearForward.backward states the steps for the linear
  * layer; BinaryConv2dForward.backward writes them out (for the convolution):

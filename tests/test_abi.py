@@ -280,3 +280,22 @@ def test_device_scale_abi_validation():
     cd = bt._c_conv_ds
     assert cd(256, bt.BT_BF16, 512, bt.BT_CODE_E2M1, 1, 8, 4, 4, 8, 3, 1, 1, 1, None, None, 0, 768, bt.BT_BF16,
               0, 1024, 1 << 20, None) == bt.BT_ERR_INVALID_ARG
+
+
+def test_w8a8_abi_validation():
+    assert bt.bt_w8a8_conv2d_workspace(2, 8, 6, 6, 16, 3, 1, 1, 1) > 0
+    assert bt.bt_w8a8_conv2d_workspace(2, 8, 1, 1, 16, 3, 1, 0, 1) == 0
+    f = bt._c_w8
+
+    def call(**kw):
+        a = dict(x=256, xt=bt.BT_F32, w=512, wt=bt.BT_F32, B=2, C=8, H=6, W=6, O=16, k=3, s=1, p=1, d=1, sm=0,
+                 out=1024, ot=bt.BT_F32, ws=4096, wsb=1 << 24, st=None)
+        a.update(kw)
+        return f(*a.values())
+    assert call(xt=bt.BT_F16) == bt.BT_ERR_INVALID_ARG
+    assert call(ot=bt.BT_I32) == bt.BT_ERR_INVALID_ARG
+    assert call(k=0) == bt.BT_ERR_INVALID_ARG
+    assert call(H=1, p=0) == bt.BT_ERR_INVALID_ARG
+    assert call(k=9, H=20, W=20) == bt.BT_ERR_UNSUPPORTED
+    assert call(B=0) == bt.BT_OK
+    assert call(x=None) == bt.BT_ERR_INVALID_ARG

@@ -80,6 +80,9 @@ _c_lin_ds = _sig("bt_binary_linear_dscale", _i, [_p, _i, _p, _i, _i64, _i64, _i6
                                                 _p, _sz, _p])
 _c_conv_ds = _sig("bt_binary_conv2d_dscale", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
                                                  _p, _p, _i64, _p, _i, _i, _p, _sz, _p])
+_c_w8_ws = _sig("bt_w8a8_conv2d_workspace", _sz, [_i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i])
+_c_w8 = _sig("bt_w8a8_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _p, _i, _p,
+                                    _sz, _p])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
 _c_status = _sig("bt_device_status", _i, [_p])
 
@@ -90,7 +93,8 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
             "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_binary_conv2d_backward",
-            "bt_scale_init", "bt_binary_linear_dscale", "bt_binary_conv2d_dscale"]
+            "bt_scale_init", "bt_binary_linear_dscale", "bt_binary_conv2d_dscale", "bt_w8a8_conv2d_workspace",
+            "bt_w8a8_conv2d"]
 
 
 class BtError(RuntimeError):
@@ -381,6 +385,30 @@ def bt_binary_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int,
     _check(_c_conv(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding,
                    dilation, scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),
                    0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def bt_w8a8_conv2d_workspace(B: int, C: int, H: int, W: int, O: int, kernel_size: int, stride: int, padding: int,
+                             dilation: int) -> int:
+    return int(_c_w8_ws(B, C, H, W, O, kernel_size, stride, padding, dilation))
+
+
+def bt_w8a8_conv2d(x: torch.Tensor, w: torch.Tensor, stride: int, padding: int, dilation: int, smooth: bool = False,
+                   out_dtype=torch.float32, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """W8A8 im2col + gemm convolution of NCHW x with OIHW w (f32 or bf16),
+    optionally with SmoothQuant; NCHW out in out_dtype (f32 or bf16)."""
+    _contig(x, "x")
+    _contig(w, "w")
+    B, C, H, W = x.shape
+    O, _, k, _ = w.shape
+    Ho, Wo = conv2d_out_size(H, k, stride, padding, dilation), conv2d_out_size(W, k, stride, padding, dilation)
+    if out is None:
+        out = torch.empty((B, O, max(Ho, 0), max(Wo, 0)), dtype=out_dtype, device=x.device)
+    ws = _workspace(bt_w8a8_conv2d_workspace(B, C, H, W, O, k, stride, padding, dilation), x.device, workspace)
+    _check(_c_w8(_ptr(x), _DT[x.dtype], _ptr(w), _DT[w.dtype], B, C, H, W, O, k, stride, padding, dilation,
+                 1 if smooth else 0, _ptr(out), _DT[out.dtype], _ptr(ws), 0 if ws is None else ws.numel(),
+                 _stream(stream)))
     return out
 
 

@@ -180,4 +180,31 @@ __device__ __forceinline__ float alpha_from(const float *scales) {
     return __double2float_rn(__dmul_rn(static_cast<double>(scales[0]), static_cast<double>(scales[1])));
 }
 
+// The filter taps of a convolution that read input position `pos` along one
+// axis: kk with pos + pad - kk*d = i*s for an output index 0 <= i < nout,
+// listed as (tk[n], ti[n]); returns their number (at most k <= kMaxTapList).
+// S = the stride when it is 1 or 2 (the divisions become shifts), 0 for any.
+constexpr int kMaxTapList = 8;
+template <int S>
+__device__ __forceinline__ int tap_list(int pos, int pad, int k, int d, int s, int nout, int (&tk)[kMaxTapList],
+                                        int (&ti)[kMaxTapList]) {
+    int n = 0;
+    for (int kk = 0; kk < k; ++kk) {
+        const int r = pos + pad - kk * d;
+        if (r < 0) break;                                     // r falls as kk grows
+        int i;
+        if constexpr (S == 1) {
+            i = r;
+        } else if constexpr (S == 2) {
+            if (r & 1) continue;
+            i = r >> 1;
+        } else {
+            if (r % s != 0) continue;
+            i = r / s;
+        }
+        if (i < nout) { tk[n] = kk; ti[n] = i; ++n; }
+    }
+    return n;
+}
+
 }  // namespace bt

@@ -110,29 +110,6 @@ __global__ void __launch_bounds__(kThreads) sign_im2col_t_kernel(const T *__rest
 // the same for w -- are listed once per thread (S = the stride when it is 1
 // or 2, so the divisions become shifts; 0 for any stride); taps are summed
 // in (kh, kw) order.
-constexpr int kMaxTapList = 8;
-template <int S>
-__device__ __forceinline__ int tap_list(int pos, int pad, int k, int d, int s, int nout, int (&tk)[kMaxTapList],
-                                        int (&ti)[kMaxTapList]) {
-    int n = 0;
-    for (int kk = 0; kk < k; ++kk) {
-        const int r = pos + pad - kk * d;
-        if (r < 0) break;                                     // r falls as kk grows
-        int i;
-        if constexpr (S == 1) {
-            i = r;
-        } else if constexpr (S == 2) {
-            if (r & 1) continue;
-            i = r >> 1;
-        } else {
-            if (r % s != 0) continue;
-            i = r / s;
-        }
-        if (i < nout) { tk[n] = kk; ti[n] = i; ++n; }
-    }
-    return n;
-}
-
 constexpr int kCh = 8;                                        // channels per col2im thread
 template <typename T, int S>
 __global__ void __launch_bounds__(kThreads) col2im_mask_kernel(const float *__restrict__ dt, const T *__restrict__ x,
