@@ -45,8 +45,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the headline steps one call at a time instead of replaying them as a CUDA graph")
-    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
-                    help="backward: the straight-through backward of a linear workload (all three gradients)")
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward", "w8a8", "w8a8-smooth"],
+                    help="backward: the straight-through backward (all three gradients); w8a8[-smooth]: the W8A8 "
+                         "im2col + gemm convolution of a conv workload (with SmoothQuant)")
     return ap.parse_args()
 
 
@@ -665,6 +666,72 @@ def run_backward(args, rank, world):
     return line
 
 
+def run_w8a8(args, rank, world):
+    """K steps of the W8A8 im2col + gemm convolution on the workload's x and W
+    (quantization of both sides inside every step)."""
+    import xnor_popcount_gemm_gb300 as bt
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    wl = workloads.NAMED[args.workload]()
+    if wl.kind != "conv":
+        raise SystemExit("--pass w8a8 covers the conv workloads")
+    smooth = args.pass_ == "w8a8-smooth"
+    M, N, K = wl.gemm_shape()
+    B, C, H, W = wl.x.shape
+    O, k = wl.w.shape[0], wl.w.shape[2]
+    stream = torch.cuda.current_stream()
+    x_host = wl.x if wl.x.dtype in (torch.bfloat16, torch.float32) else wl.x.float()
+    w = wl.w.to(x_host.dtype).to(dev)
+    Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
+    Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
+    out_t = torch.float32
+    per = x_host.numel() * x_host.element_size() + B * O * Ho * Wo * 4
+    nbuf = max(1, -(-2 * L2_BYTES // per))
+    xs = [x_host.to(dev) for _ in range(nbuf)]
+    outs = [torch.empty(B, O, Ho, Wo, dtype=out_t, device=dev) for _ in range(nbuf)]
+    ws = torch.empty(bt.bt_w8a8_conv2d_workspace(B, C, H, W, O, k, wl.stride, wl.padding, wl.dilation),
+                     dtype=torch.uint8, device=dev)
+
+    def step(i):
+        j = i % nbuf
+        bt.bt_w8a8_conv2d(xs[j], w, wl.stride, wl.padding, wl.dilation, smooth=smooth, out=outs[j], workspace=ws)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert bt.bt_device_status() == 0
+    with ClockSampler(dev.index) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        a1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(a0.elapsed_time(a1), world) / args.steps
+    if bt.bt_device_status() != 0:
+        raise RuntimeError("device status")
+    peaks, peak_src = measured_peaks()
+    ops = 2.0 * M * N * K
+    return {
+        "metric": "W8A8 conv GOPS (2*M*N*K/s, quantization included)",
+        "value": round(ops * world / (ms / 1e3) / 1e9, 1),
+        "unit": "GOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 x int8 as bf16 on the tensor cores (exact fp32 K splits, double sum)",
+        "data": "synthetic (the workload's x and W)",
+        "config": {"workload": wl.name, "pass": args.pass_, "M": M, "N": N, "K": K,
+                   "l2": f"inputs+outputs rotate over {nbuf} buffers", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(ops / (ms / 1e3) / 1e12, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(ops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                     "traffic": None, "peak_source": f"{peak_src}: cuBLAS bf16 burst", "kernel": "whole call"},
+        "gpu_launches": 9 * args.steps,
+        "clocks": clk.summary(),
+    }
+
+
 # ---------------------------------------------------------------------------
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -730,7 +797,12 @@ def main():
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return
     rank, world = dist_init(args)
-    line = run_backward(args, rank, world) if args.pass_ == "backward" else run_ours(args, rank, world)
+    if args.pass_ == "backward":
+        line = run_backward(args, rank, world)
+    elif args.pass_.startswith("w8a8"):
+        line = run_w8a8(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

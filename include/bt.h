@@ -349,9 +349,10 @@ size_t bt_w8a8_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, int6
  * is quantized per tensor: scale = fp32(max|v| / 127), q = clamp(rint(v *
  * fp32(1 / scale)), -127, 127) (torch's fake-quant rounding; q = 0 when the
  * tensor is all zeros). The integer dot products are exact (tensor cores on
- * bf16 copies of q, K split in parts of at most 1024 taps, parts added in
- * double) and y = fp32(double(dot) * double(fp32(scale_x * scale_w))); out
- * F32 or BF16 (rounded from that fp32). k <= 8; pointers 16-byte aligned,
+ * bf16 copies of q, K split in parts of at most 1024 taps, parts added as
+ * integers) and y = fp32(double(dot) * double(fp32(scale_x * scale_w))); out
+ * F32 or BF16 (rounded from that fp32). k <= 8, C*k*k <= 131072 (UNSUPPORTED
+ * beyond); pointers 16-byte aligned,
  * workspace 256-byte aligned (bt_w8a8_conv2d_workspace bytes); asynchronous
  * on `stream`. Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA.
  */

@@ -104,10 +104,12 @@ cudaError_t launch_tc_bf16(const uint16_t *a, int64_t lda, const uint16_t *b, in
 
 // The same contraction split along K into `splits` equal parts (klen a
 // multiple of 64 * splits), each part's fp32 partial sums (times alpha) in
-// out [splits, M, N]; the caller adds them up.
+// out [splits, M, N] (or, with nchw_hw > 0, each part laid out NCHW as a
+// convolution's [N / nchw_hw images, M channels, nchw_hw pixels]); the caller
+// adds them up.
 cudaError_t launch_tc_bf16_splitk(const uint16_t *a, int64_t lda, const uint16_t *b, int64_t ldb, int64_t M,
                                   int64_t N, int64_t klen, int splits, float alpha, float *out, unsigned int *err,
-                                  cudaStream_t s);
+                                  cudaStream_t s, int64_t nchw_hw = 0);
 
 // out[c * ldo + r] = f(in[r * C + c]) as bf16 for r < R, c < C, and 0 for
 // R <= r < ldo: f = torch.sign (sign = true; in of type in_t) or the value

@@ -961,7 +961,7 @@ cudaError_t launch_tc_bf16(const uint16_t *a_ptr, int64_t lda, const uint16_t *b
 // applied); klen a multiple of 64 * splits.
 cudaError_t launch_tc_bf16_splitk(const uint16_t *a_ptr, int64_t lda, const uint16_t *b_ptr, int64_t ldb, int64_t M,
                                   int64_t N, int64_t klen, int splits, float alpha, float *out, unsigned int *err,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, int64_t nchw_hw) {
     if (splits < 1 || klen % (64 * splits) != 0) return cudaErrorInvalidValue;
     TcArgs a{};
     Maps mp;
@@ -975,6 +975,15 @@ cudaError_t launch_tc_bf16_splitk(const uint16_t *a_ptr, int64_t lda, const uint
     a.alpha = alpha;
     a.out = out;
     a.err = err;
+    if (nchw_hw > 0) {
+        // columns are pixels of images of nchw_hw pixels: each split's part NCHW
+        a.hw = nchw_hw;
+        a.vec = 4;
+        for (int v = 16; v > 4; v /= 2) {
+            if ((nchw_hw * 4) % v == 0 && aligned(out, static_cast<size_t>(v))) { a.vec = v; break; }
+        }
+        return launch_bf16_t<kNchwOut, BT_F32>(c.pair, mp, a, s);
+    }
     a.vec = (N % 4 == 0) && aligned(out, 16) ? 1 : 0;
     return launch_bf16_t<kRowsOut, BT_F32>(c.pair, mp, a, s);
 }

@@ -10,14 +10,14 @@
 // The int8 products run on the tensor cores as bf16 x bf16 (every int8 value
 // is a bf16 value, every product exact in fp32) in K splits of at most 1024
 // taps, so that each split's fp32 sum (|sum| <= 1024 * 127^2 < 2^24) is exact;
-// the splits are added in double (exact) and scaled once:
-// y = fp32(double(dot) * double(fp32(s_x * s_w))).
+// the splits are added as 32-bit integers (T <= 131072 taps keeps the total
+// below 2^31) and scaled once: y = fp32(double(dot) * double(fp32(s_x * s_w))).
 //
 // Steps: column maxima of |rows| straight from x (each input element raises
 // the maxima of the taps that read it) and of |w|; the smoothing scales and
 // the quantization constants; the quantized weight [O, T'] and im2col rows
 // [P, T'] (bf16, T' = T padded with zeros to the split size); the split
-// products (tc_gemm.cu); the NCHW sum.
+// products (tc_gemm.cu), each split's part stored NCHW; their sum.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -54,25 +54,42 @@ template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(const __nv_bflo
 }
 
 // act[t] = max over the im2col rows of |rows[:, t]| (as float bits; all >= 0):
-// each input element raises the taps that read it.
+// each input element raises the taps that read it. A block takes a run of
+// pixel positions of one channel (blockIdx.y) over every image; each thread
+// keeps the maxima of its position's taps in registers, then the block
+// reduces them per tap and issues one global atomic per tap.
 template <typename T, int S>
 __global__ void __launch_bounds__(kThreads) colmax_x_kernel(const T *__restrict__ x, Geo g, unsigned int *__restrict__ act) {
     pdl_launch_dependents();
     pdl_wait();
-    const uint32_t pix = blockIdx.x * kThreads + threadIdx.x;
+    __shared__ unsigned int tmax[kMaxTapList * kMaxTapList];
+    const int kk = g.k * g.k;
     const uint32_t W = static_cast<uint32_t>(g.W), hw = static_cast<uint32_t>(g.H * g.W);
-    if (pix >= hw) return;
-    const int h = static_cast<int>(pix / W), w = static_cast<int>(pix - (pix / W) * W);
+    const uint32_t pix = blockIdx.x * kThreads + threadIdx.x;
     int hk[kMaxTapList], hi[kMaxTapList], wk[kMaxTapList], wj[kMaxTapList];
-    const int nh = tap_list<S>(h, g.p, g.k, g.d, g.s, static_cast<int>(g.Ho), hk, hi);
-    const int nw = tap_list<S>(w, g.p, g.k, g.d, g.s, static_cast<int>(g.Wo), wk, wj);
-    if (nh == 0 || nw == 0) return;
-    for (int64_t plane = blockIdx.y; plane < g.B * g.C; plane += gridDim.y) {
-        const int64_t c = plane % g.C;
-        const unsigned int v = __float_as_uint(fabsf(to_f<T>(x, plane * hw + pix)));
-        if (v == 0u) continue;
-        for (int a = 0; a < nh; ++a)
-            for (int e = 0; e < nw; ++e) atomicMax(act + (c * g.k + hk[a]) * g.k + wk[e], v);
+    int nh = 0, nw = 0;
+    if (pix < hw) {
+        const int h = static_cast<int>(pix / W), w = static_cast<int>(pix - (pix / W) * W);
+        nh = tap_list<S>(h, g.p, g.k, g.d, g.s, static_cast<int>(g.Ho), hk, hi);
+        nw = tap_list<S>(w, g.p, g.k, g.d, g.s, static_cast<int>(g.Wo), wk, wj);
+    }
+    for (int i = threadIdx.x; i < kk; i += kThreads) tmax[i] = 0u;
+    __syncthreads();
+    for (int64_t c = blockIdx.y; c < g.C; c += gridDim.y) {
+        // the position's maximum over the images; every tap that reads the
+        // position sees the same values
+        unsigned int m = 0u;
+        if (nh > 0 && nw > 0)
+            for (int64_t b = 0; b < g.B; ++b) m = max(m, __float_as_uint(fabsf(to_f<T>(x, (b * g.C + c) * hw + pix))));
+        if (m != 0u)
+            for (int a = 0; a < nh; ++a)
+                for (int e = 0; e < nw; ++e) atomicMax(&tmax[hk[a] * g.k + wk[e]], m);
+        __syncthreads();
+        for (int i = threadIdx.x; i < kk; i += kThreads) {
+            if (tmax[i] != 0u) atomicMax(act + c * kk + i, tmax[i]);
+            tmax[i] = 0u;
+        }
+        __syncthreads();
     }
 }
 
@@ -166,51 +183,103 @@ __global__ void __launch_bounds__(kThreads) quant_w_kernel(const T *__restrict__
     }
 }
 
-// the im2col rows quantized: qx[p, t] (pitch Tp); a thread keeps its output
-// pixel p and walks the taps.
-template <typename T>
+// the im2col rows quantized: qx[p, t] (pitch Tp). A block takes 64 output
+// pixels and the taps of 4 channels: x is gathered tap by tap with the pixels
+// along the threads (reads along image rows), quantized into shared memory,
+// and written pixel by pixel as runs of 4*k*k taps (a warp per pixel). The
+// block's taps are tabulated once (channel, offsets, scale), so the loops
+// divide nothing; without SmoothQuant the scale is 1 and v / 1 = v is not
+// computed. The block of the last channel group also zeroes the padding taps
+// [T, Tp).
+constexpr int kQP = 64, kQC = 4, kQT = kQC * kMaxTapList * kMaxTapList;
+template <typename T, bool SMOOTH>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const T *__restrict__ x, Geo g, const float *__restrict__ scale,
                                                               const QParams *__restrict__ qp, uint16_t *__restrict__ qx) {
     pdl_launch_dependents();
     pdl_wait();
+    __shared__ uint16_t tile[kQP][kQT + 2];
+    __shared__ int pb[kQP], ph[kQP], pw[kQP];
+    __shared__ int toff[kQT], th[kQT], tw[kQT];
+    __shared__ float ts[kQT];
     const float inv = qp->inv_x;
-    const uint32_t hwo = static_cast<uint32_t>(g.Ho * g.Wo), wo = static_cast<uint32_t>(g.Wo);
-    const int64_t kk = static_cast<int64_t>(g.k) * g.k;
-    for (int64_t p = blockIdx.y; p < g.P; p += gridDim.y) {
-        const uint32_t b = static_cast<uint32_t>(p / hwo), pix = static_cast<uint32_t>(p - static_cast<int64_t>(b) * hwo);
-        const uint32_t oi = pix / wo, oj = pix - oi * wo;
-        for (int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; t < g.Tp;
-             t += static_cast<int64_t>(gridDim.x) * kThreads) {
-            uint16_t v = 0;
-            if (t < g.T) {
-                const int64_t c = t / kk, tap = t - c * kk;
-                const int kh = static_cast<int>(tap / g.k), kw = static_cast<int>(tap - kh * g.k);
-                const int ih = static_cast<int>(oi) * g.s - g.p + kh * g.d, iw = static_cast<int>(oj) * g.s - g.p + kw * g.d;
-                float xv = 0.0f;
-                if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W)
-                    xv = to_f<T>(x, ((static_cast<int64_t>(b) * g.C + c) * g.H + ih) * g.W + iw);
-                v = quant_bf16(__fdiv_rn(xv, scale[t]), inv);
-            }
-            qx[p * g.Tp + t] = v;
+    const int64_t p0 = static_cast<int64_t>(blockIdx.x) * kQP;
+    const int c0 = static_cast<int>(blockIdx.y) * kQC;
+    const int kk = g.k * g.k;
+    const int nc = g.C - c0 < kQC ? static_cast<int>(g.C - c0) : kQC;
+    const int ntaps = nc * kk;
+    if (threadIdx.x < kQP) {
+        const int64_t p = p0 + threadIdx.x;
+        int b = -1, h0 = 0, w0 = 0;
+        if (p < g.P) {
+            const uint32_t hwo = static_cast<uint32_t>(g.Ho * g.Wo), wo = static_cast<uint32_t>(g.Wo);
+            const uint32_t bb = static_cast<uint32_t>(p / hwo), pix = static_cast<uint32_t>(p - static_cast<int64_t>(bb) * hwo);
+            const uint32_t oi = pix / wo, oj = pix - oi * wo;
+            b = static_cast<int>(bb);
+            h0 = static_cast<int>(oi) * g.s - g.p;
+            w0 = static_cast<int>(oj) * g.s - g.p;
         }
+        pb[threadIdx.x] = b;
+        ph[threadIdx.x] = h0;
+        pw[threadIdx.x] = w0;
+    }
+    for (int tt = threadIdx.x; tt < ntaps; tt += kThreads) {
+        const int ci = tt / kk, tap = tt - ci * kk, kh = tap / g.k, kw = tap - kh * g.k;
+        toff[tt] = (c0 + ci) * static_cast<int>(g.H * g.W) + kh * g.d * static_cast<int>(g.W) + kw * g.d;
+        th[tt] = kh * g.d;
+        tw[tt] = kw * g.d;
+        ts[tt] = SMOOTH ? scale[(c0 + ci) * kk + tap] : 1.0f;
+    }
+    __syncthreads();
+    const int pp = threadIdx.x & (kQP - 1);
+    const int b = pb[pp], h0 = ph[pp], w0 = pw[pp];
+    // the pixel's image and window corner; per tap only the offset within the image
+    const T *xi = x + (b >= 0 ? static_cast<int64_t>(b) * g.C * g.H * g.W : 0);
+    const int corner = h0 * static_cast<int>(g.W) + w0;
+    const int H = static_cast<int>(g.H), W = static_cast<int>(g.W);
+    for (int tt = threadIdx.x / kQP; tt < ntaps; tt += kThreads / kQP) {
+        uint16_t v = 0;
+        if (b >= 0) {
+            const int ih = h0 + th[tt], iw = w0 + tw[tt];
+            float xv = 0.0f;
+            if (static_cast<unsigned>(ih) < static_cast<unsigned>(H) && static_cast<unsigned>(iw) < static_cast<unsigned>(W))
+                xv = to_f<T>(xi, corner + toff[tt]);
+            v = quant_bf16(SMOOTH ? __fdiv_rn(xv, ts[tt]) : xv, inv);
+        }
+        tile[pp][tt] = v;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int q = warp; q < kQP; q += kThreads / 32) {
+        const int64_t p = p0 + q;
+        if (p >= g.P) break;
+        uint16_t *row = qx + p * g.Tp + static_cast<int64_t>(c0) * kk;
+        for (int tt = lane; tt < ntaps; tt += 32) row[tt] = tile[q][tt];
+        if (c0 + kQC >= g.C)
+            for (int64_t t = g.T + lane; t < g.Tp; t += 32) qx[p * g.Tp + t] = 0;
     }
 }
 
-// out[b, o, pix] = fp32(double(sum over splits of part[s][o][b*Ho*Wo + pix]) * alpha)
+// out[i] = fp32(double(sum over splits of part[s][i]) * alpha), the parts laid
+// out NCHW like the output: the partial sums are integers below 2^24, added
+// exactly as 32-bit integers; while |sum| <= 2^24 the sum is exact in fp32 and
+// sum * alpha (48 bits) exact in double, so one fp32 multiply gives the same
+// result, and only larger sums take the double product.
+__device__ __forceinline__ float scale_dot(int acc, float alphaf) {
+    if (acc <= (1 << 24) && acc >= -(1 << 24)) return __fmul_rn(static_cast<float>(acc), alphaf);
+    return __double2float_rn(__dmul_rn(static_cast<double>(acc), static_cast<double>(alphaf)));
+}
+
 template <typename O>
-__global__ void __launch_bounds__(kThreads) combine_kernel(const float *__restrict__ part, int splits, Geo g,
+__global__ void __launch_bounds__(kThreads) combine_kernel(const float *__restrict__ part, int splits, int64_t n,
                                                            const QParams *__restrict__ qp, O *__restrict__ out) {
     pdl_launch_dependents();
     pdl_wait();
-    const double alpha = static_cast<double>(qp->alpha);
-    const int64_t hw = g.Ho * g.Wo, n = g.B * g.O * hw, plane = g.O * g.P;
+    const float alphaf = qp->alpha;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t pix = i % hw, r = i / hw, o = r % g.O, b = r / g.O;
-        const int64_t col = o * g.P + b * hw + pix;
-        double acc = 0.0;
-        for (int s = 0; s < splits; ++s) acc += static_cast<double>(__ldg(part + s * plane + col));
-        const float y = __double2float_rn(__dmul_rn(acc, alpha));
+        int acc = 0;
+        for (int s = 0; s < splits; ++s) acc += __float2int_rn(__ldg(part + s * n + i));
+        const float y = scale_dot(acc, alphaf);
         if constexpr (sizeof(O) == 4) out[i] = y;
         else out[i] = __float2bfloat16_rn(y);
     }
@@ -284,7 +353,7 @@ cudaError_t run(const TX *x, const TW *w, const Geo &g, int splits, int smooth, 
     uint16_t *qx = reinterpret_cast<uint16_t *>(ws + l.qx);
     float *part = reinterpret_cast<float *>(ws + l.part);
     cudaError_t e = cudaMemsetAsync(ws, 0, l.scale, s);            // act, wmax, amax_w, qp
-    const dim3 pix_grid(static_cast<unsigned>((g.H * g.W + kThreads - 1) / kThreads), rows_cap(g.B * g.C));
+    const dim3 pix_grid(static_cast<unsigned>((g.H * g.W + kThreads - 1) / kThreads), rows_cap(g.C));
     if (e == cudaSuccess) {
         if (g.s == 1) e = launch(colmax_x_kernel<TX, 1>, pix_grid, s, x, g, act);
         else if (g.s == 2) e = launch(colmax_x_kernel<TX, 2>, pix_grid, s, x, g, act);
@@ -299,15 +368,21 @@ cudaError_t run(const TX *x, const TW *w, const Geo &g, int splits, int smooth, 
     if (e == cudaSuccess)
         e = launch(quant_w_kernel<TW>, dim3(flat_blocks(g.O * g.Tp)), s, w, g, static_cast<const float *>(scale),
                    static_cast<const unsigned int *>(amax_w), qp, qw);
-    if (e == cudaSuccess)
-        e = launch(quant_rows_kernel<TX>, dim3(static_cast<unsigned>((g.Tp + kThreads - 1) / kThreads), rows_cap(g.P)), s, x,
-                   g, static_cast<const float *>(scale), static_cast<const QParams *>(qp), qx);
-    if (e == cudaSuccess) e = launch_tc_bf16_splitk(qw, g.Tp, qx, g.Tp, g.O, g.P, g.Tp, splits, 1.0f, part, err, s);
     if (e == cudaSuccess) {
-        const dim3 grid(flat_blocks(g.B * g.O * g.Ho * g.Wo));
-        e = out_t == BT_F32 ? launch(combine_kernel<float>, grid, s, static_cast<const float *>(part), splits, g,
+        const dim3 qgrid(static_cast<unsigned>((g.P + kQP - 1) / kQP), static_cast<unsigned>((g.C + kQC - 1) / kQC));
+        e = smooth ? launch(quant_rows_kernel<TX, true>, qgrid, s, x, g, static_cast<const float *>(scale),
+                            static_cast<const QParams *>(qp), qx)
+                   : launch(quant_rows_kernel<TX, false>, qgrid, s, x, g, static_cast<const float *>(scale),
+                            static_cast<const QParams *>(qp), qx);
+    }
+    if (e == cudaSuccess)
+        e = launch_tc_bf16_splitk(qw, g.Tp, qx, g.Tp, g.O, g.P, g.Tp, splits, 1.0f, part, err, s, g.Ho * g.Wo);
+    if (e == cudaSuccess) {
+        const int64_t n = g.B * g.O * g.Ho * g.Wo;
+        const dim3 grid(flat_blocks(n));
+        e = out_t == BT_F32 ? launch(combine_kernel<float>, grid, s, static_cast<const float *>(part), splits, n,
                                      static_cast<const QParams *>(qp), static_cast<float *>(out))
-                            : launch(combine_kernel<__nv_bfloat16>, grid, s, static_cast<const float *>(part), splits, g,
+                            : launch(combine_kernel<__nv_bfloat16>, grid, s, static_cast<const float *>(part), splits, n,
                                      static_cast<const QParams *>(qp), static_cast<__nv_bfloat16 *>(out));
     }
     return e;
@@ -342,7 +417,8 @@ bt_status bt_w8a8_conv2d(const void *x, bt_dtype x_dtype, const void *w, bt_dtyp
     int splits = 1;
     if (!make_geo(B, C, H, W, O, kernel_size, stride, padding, dilation, g, splits)) return BT_ERR_INVALID_ARG;
     if (kernel_size > kMaxTapList || H * W > (int64_t(1) << 31) - 512 || g.Ho * g.Wo > (int64_t(1) << 31) - 512 ||
-        g.P > (int64_t(1) << 31) - 512 || g.T > (int64_t(1) << 24) || O > (int64_t(1) << 24))
+        g.P > (int64_t(1) << 31) - 512 || g.T > 131072 || O > (int64_t(1) << 24) ||
+        C * H * W > (int64_t(1) << 31) - 1)
         return BT_ERR_UNSUPPORTED;
     if (B == 0) return BT_OK;
     if (x == nullptr || w == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
