@@ -18,7 +18,6 @@
 // operand times a bf16 scale is the page's bf16(sign * scale): the scale is
 // rounded to bf16 once on the host and applied to the fp32 sums.
 #include <cmath>
-#include <cstring>
 #include <type_traits>
 
 #include <cuda_bf16.h>
@@ -216,19 +215,7 @@ cudaError_t transpose_t(const void *in, int64_t R, int64_t C, int64_t ldo, uint1
     return cudaLaunchKernelEx(&cfg, transpose_kernel<T, SIGN>, static_cast<const T *>(in), R, C, ldo, out);
 }
 
-// Round a float to the nearest bf16 value (ties to even) on the host.
-float bf16_round_host(float v) {
-    uint32_t u;
-    std::memcpy(&u, &v, 4);
-    if ((u & 0x7F800000u) == 0x7F800000u) return v;                  // inf / NaN unchanged
-    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
-    float r;
-    std::memcpy(&r, &u, 4);
-    return r;
-}
-
 int64_t round_up64(int64_t v) { return (v + 63) / 64 * 64; }
-size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
 

@@ -149,6 +149,33 @@ inline cudaLaunchAttribute pdl_attribute() {
     return a;
 }
 
+// Round a float to the nearest bf16 value (ties to even), as a float; inf and
+// NaN unchanged.
+inline float bf16_round_host(float v) {
+    uint32_t u;
+    __builtin_memcpy(&u, &v, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u) return v;
+    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    float r;
+    __builtin_memcpy(&r, &u, 4);
+    return r;
+}
+
+inline size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Launch `kern` on `s` with programmatic dependent launch allowed.
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute pdl = pdl_attribute();
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = s;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Largest K (elements) for which the tensor-core kernels are used: a bound on
 // the magnitude of the fp32 partial sums they accumulate.
 constexpr int64_t kTcMaxK = 16384;

@@ -20,7 +20,6 @@
 //                    transposed [t, P], zeros for taps in the padding); the
 //                    long sum over P is split in K, the parts added in fp32.
 #include <cmath>
-#include <cstring>
 
 #include <cuda_bf16.h>
 
@@ -190,18 +189,13 @@ __global__ void __launch_bounds__(kThreads) split_sum_kernel(const float *__rest
 }
 
 // Grid (columns / 256, rows) for the row-mapped kernels above (rows capped
-// at 65535; the kernels loop over the rest).
+// at 65535; the kernels loop over the rest), and a flat grid of up to 16
+// blocks per SM.
 template <typename K, typename... Args>
 cudaError_t launch_rows(K kern, int64_t cols, int64_t rows, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute pdl = pdl_attribute();
-    cfg.gridDim = dim3(static_cast<unsigned>((cols + kThreads - 1) / kThreads),
-                       static_cast<unsigned>(rows < 65535 ? (rows > 0 ? rows : 1) : 65535));
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = s;
-    cfg.attrs = &pdl;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
+    return launch_pdl(kern, dim3(static_cast<unsigned>((cols + kThreads - 1) / kThreads),
+                                 static_cast<unsigned>(rows < 65535 ? (rows > 0 ? rows : 1) : 65535)),
+                      dim3(kThreads), s, args...);
 }
 
 template <typename K, typename... Args>
@@ -210,14 +204,7 @@ cudaError_t launch_flat(K kern, int64_t work, cudaStream_t s, Args... args) {
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute pdl = pdl_attribute();
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = s;
-    cfg.attrs = &pdl;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), s, args...);
 }
 
 template <typename T>
@@ -228,18 +215,6 @@ cudaError_t launch_col2im(const float *dt, const T *x, const ConvBwdGeom &q, flo
     if (q.s == 2) return launch_rows(col2im_mask_kernel<T, 2>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
     return launch_rows(col2im_mask_kernel<T, 0>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
 }
-
-float bf16_round_h(float v) {
-    uint32_t u;
-    std::memcpy(&u, &v, 4);
-    if ((u & 0x7F800000u) == 0x7F800000u) return v;
-    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
-    float r;
-    std::memcpy(&r, &u, 4);
-    return r;
-}
-
-size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 // Pieces of the workspace. The input gradient's (g per pixel, D) and the
 // weight gradient's (g rows, sign(x) im2col, partial sums) run one after the
@@ -271,12 +246,12 @@ bool make_plan(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int k, int
     pl.splits = static_cast<int>(sp);
     pl.ldp = (q.P + 64 * sp - 1) / (64 * sp) * (64 * sp);
     pl.gp_off = 0;
-    pl.dt_off = up256(static_cast<size_t>(q.P * O * 2));
-    pl.dgrad_bytes = pl.dt_off + up256(static_cast<size_t>(q.T * q.P * 4));
+    pl.dt_off = round_up256(static_cast<size_t>(q.P * O * 2));
+    pl.dgrad_bytes = pl.dt_off + round_up256(static_cast<size_t>(q.T * q.P * 4));
     pl.go_off = 0;
-    pl.u_off = up256(static_cast<size_t>(O * pl.ldp * 2));
-    pl.part_off = pl.u_off + up256(static_cast<size_t>(q.T * pl.ldp * 2));
-    pl.wgrad_bytes = pl.part_off + up256(static_cast<size_t>(sp * O * q.T * 4));
+    pl.u_off = round_up256(static_cast<size_t>(O * pl.ldp * 2));
+    pl.part_off = pl.u_off + round_up256(static_cast<size_t>(q.T * pl.ldp * 2));
+    pl.wgrad_bytes = pl.part_off + round_up256(static_cast<size_t>(sp * O * q.T * 4));
     return true;
 }
 
@@ -360,7 +335,7 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
             launch_transpose_bf16_batched(g16, BT_BF16, O, q.Ho * q.Wo, O, false, gp, static_cast<int>(B), s) !=
                 cudaSuccess)
             return BT_ERR_CUDA;
-        if (launch_tc_bf16(static_cast<const uint16_t *>(wst), ldw, gp, O, q.T, q.P, O, bf16_round_h(scale_w), dt, BT_F32,
+        if (launch_tc_bf16(static_cast<const uint16_t *>(wst), ldw, gp, O, q.T, q.P, O, bf16_round_host(scale_w), dt, BT_F32,
                            nullptr, err, s) != cudaSuccess)
             return BT_ERR_CUDA;
         const float norm = static_cast<float>(1.0 / std::sqrt(static_cast<double>(B) * C * H * W));
@@ -387,9 +362,9 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
         if (e == cudaSuccess)
             e = grad_w_dtype == BT_F32
                     ? launch_flat(split_sum_kernel<float>, O * q.T, s, static_cast<const float *>(part), pl.splits, O * q.T,
-                                  bf16_round_h(scale_a), static_cast<float *>(grad_w))
+                                  bf16_round_host(scale_a), static_cast<float *>(grad_w))
                     : launch_flat(split_sum_kernel<__nv_bfloat16>, O * q.T, s, static_cast<const float *>(part), pl.splits,
-                                  O * q.T, bf16_round_h(scale_a), static_cast<__nv_bfloat16 *>(grad_w));
+                                  O * q.T, bf16_round_host(scale_a), static_cast<__nv_bfloat16 *>(grad_w));
         if (e != cudaSuccess) return BT_ERR_CUDA;
     }
     return BT_OK;

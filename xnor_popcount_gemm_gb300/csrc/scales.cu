@@ -82,18 +82,6 @@ __global__ void finish_kernel(const double *__restrict__ acc, int64_t n, float f
 
 __device__ double g_abs_sum[128];
 
-template <typename K, typename... Args>
-cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute pdl = pdl_attribute();
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.stream = s;
-    cfg.attrs = &pdl;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 }  // namespace
 }  // namespace bt
 

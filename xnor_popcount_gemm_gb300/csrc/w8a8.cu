@@ -287,14 +287,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float *__restri
 
 template <typename K, typename... Args>
 cudaError_t launch(K kern, dim3 grid, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute pdl = pdl_attribute();
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = s;
-    cfg.attrs = &pdl;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
+    return launch_pdl(kern, grid, dim3(kThreads), s, args...);
 }
 
 unsigned flat_blocks(int64_t n) {
@@ -303,7 +296,6 @@ unsigned flat_blocks(int64_t n) {
     return static_cast<unsigned>(b < 1 ? 1 : (b > cap ? cap : b));
 }
 unsigned rows_cap(int64_t rows) { return static_cast<unsigned>(rows < 1 ? 1 : (rows > 65535 ? 65535 : rows)); }
-size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 bool make_geo(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int k, int s, int p, int d, Geo &g, int &splits) {
     g.B = B; g.C = C; g.H = H; g.W = W; g.O = O; g.k = k; g.s = s; g.p = p; g.d = d;
@@ -328,14 +320,14 @@ struct Layout {
 Layout layout(const Geo &g, int splits) {
     Layout l{};
     size_t o = 0;
-    l.act = o; o += up256(static_cast<size_t>(g.T) * 4);
-    l.wmax = o; o += up256(static_cast<size_t>(g.T) * 4);
+    l.act = o; o += round_up256(static_cast<size_t>(g.T) * 4);
+    l.wmax = o; o += round_up256(static_cast<size_t>(g.T) * 4);
     l.amax_w = o; o += 256;
     l.qp = o; o += 256;
-    l.scale = o; o += up256(static_cast<size_t>(g.T) * 4);
-    l.qw = o; o += up256(static_cast<size_t>(g.O * g.Tp) * 2);
-    l.qx = o; o += up256(static_cast<size_t>(g.P * g.Tp) * 2);
-    l.part = o; o += up256(static_cast<size_t>(splits) * g.O * g.P * 4);
+    l.scale = o; o += round_up256(static_cast<size_t>(g.T) * 4);
+    l.qw = o; o += round_up256(static_cast<size_t>(g.O * g.Tp) * 2);
+    l.qx = o; o += round_up256(static_cast<size_t>(g.P * g.Tp) * 2);
+    l.part = o; o += round_up256(static_cast<size_t>(splits) * g.O * g.P * 4);
     l.total = o;
     return l;
 }
