@@ -39,6 +39,35 @@ def test_w8a8_matches_oracle(B, C, H, W, O, k, s, p, d, smooth, dt):
     np.testing.assert_array_equal(got, want)
 
 
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", SHAPES[:4] + [(1, 7, 40, 40, 8, 3, 1, 0, 12)])
+@pytest.mark.parametrize("smooth", [False, True], ids=["plain", "smoothquant"])
+def test_w8a8_direct_gather_matches_oracle(B, C, H, W, O, k, s, p, d, smooth, monkeypatch):
+    # the direct gather (forced here; the last shape's dilated window fits no
+    # staged plan, so it takes the gather on its own) gives the same rows
+    monkeypatch.setenv("BT_W8A8_UNFOLD", "gather")
+    gen = torch.Generator().manual_seed(B * 1000 + C + k + 1)
+    x = (torch.randn(B, C, H, W, generator=gen) * torch.logspace(-1, 1.5, C).view(1, C, 1, 1)).to(torch.bfloat16)
+    w = (torch.randn(O, C, k, k, generator=gen) * 0.1).to(torch.bfloat16)
+    got = bt.bt_w8a8_conv2d(x.to(DEV), w.to(DEV), s, p, d, smooth=smooth).cpu().numpy()
+    want = oracle.w8a8_conv2d(x.float().numpy(), w.float().numpy(), s, p, d, smooth)["y"]
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", [(1, 7, 40, 40, 8, 3, 1, 0, 12), (1, 3, 33, 33, 8, 8, 1, 3, 1),
+                                               (1, 5, 30, 30, 8, 7, 1, 3, 1), (1, 33, 5, 150, 8, 3, 2, 1, 1),
+                                               (1, 300, 4, 4, 8, 1, 1, 0, 1), (2, 40, 9, 9, 8, 2, 1, 0, 1)])
+def test_w8a8_unusual_windows_match_oracle(B, C, H, W, O, k, s, p, d):
+    # dilated windows too wide to stage, 7x7 and 8x8 kernels (fewer pixel
+    # slots per unit), wide rows split in column ranges, 1x1 and 2x2 kernels
+    # (more channels per unit)
+    gen = torch.Generator().manual_seed(C * 7 + k)
+    x = torch.randn(B, C, H, W, generator=gen)
+    w = torch.randn(O, C, k, k, generator=gen)
+    got = bt.bt_w8a8_conv2d(x.to(DEV), w.to(DEV), s, p, d, smooth=True).cpu().numpy()
+    want = oracle.w8a8_conv2d(x.numpy(), w.numpy(), s, p, d, True)["y"]
+    np.testing.assert_array_equal(got, want)
+
+
 def test_w8a8_bf16_output_and_large_k():
     # C*k*k = 2304 taps: three K splits, each exact in fp32
     gen = torch.Generator().manual_seed(5)

@@ -128,6 +128,20 @@ template <> __device__ __forceinline__ uint32_t pack2_from_acc<BT_F16>(float a0,
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Division by a divisor fixed per launch, for n < 2^31: q = (hi32(m*n) + n) >> l
+// with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994).
+struct FastDiv {
+    uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) { return (__umulhi(f.m, n) + n) >> f.l; }
+
 // ---------------------------------------------------------------------------
 // Bounded waiting. Every spin in these kernels gives up after kWaitNs of
 // %globaltimer time, records kErrTimeout and lets the kernel return.

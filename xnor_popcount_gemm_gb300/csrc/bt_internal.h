@@ -163,17 +163,24 @@ inline float bf16_round_host(float v) {
 
 inline size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Launch `kern` on `s` with programmatic dependent launch allowed.
+// Launch `kern` on `s` with programmatic dependent launch allowed (and
+// `smem` bytes of dynamic shared memory).
 template <typename K, typename... Args>
-cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+cudaError_t launch_pdl_smem(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute pdl = pdl_attribute();
     cfg.gridDim = grid;
     cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+    return launch_pdl_smem(kern, grid, block, 0, s, args...);
 }
 
 // Largest K (elements) for which the tensor-core kernels are used: a bound on

@@ -189,20 +189,6 @@ __device__ __forceinline__ void store_masks(uint8_t *dst, uint32_t P0, uint32_t 
     }
 }
 
-// Division by a divisor fixed per launch, for n < 2^31: q = (hi32(m*n) + n) >> l
-// with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1 (Granlund and
-// Montgomery, "Division by invariant integers using multiplication", 1994).
-struct FastDiv {
-    uint32_t d, m, l;
-};
-FastDiv make_fastdiv(uint32_t d) {
-    uint32_t l = 0;
-    while ((uint64_t(1) << l) < d) ++l;
-    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
-    return FastDiv{d, static_cast<uint32_t>(m), l};
-}
-__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) { return (__umulhi(f.m, n) + n) >> f.l; }
-
 // rows, flat: every output group of every row, numbered g = row * G + j over
 // the whole [R, G] output, kFlatUnroll per thread in flight. Group j < Gf
 // holds elements 8j..8j+7 of the row and is read with VB-byte vectors (rows
