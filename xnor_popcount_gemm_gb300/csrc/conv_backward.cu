@@ -51,7 +51,9 @@ template <> __device__ __forceinline__ float ld_f32<__nv_bfloat16>(const __nv_bf
 // index is a 32-bit quotient of a row position; sizes are validated to fit.
 
 // g [B, O, Ho*Wo] -> go [O, ldp]: row o holds g[b, o, :] for b = 0, 1, ...
-// one after the other; columns P .. ldp-1 are 0.
+// one after the other; columns P .. ldp-1 are 0. A thread copies its column
+// of kGRows rows, all the loads issued before the stores.
+constexpr int kGRows = 8;
 __global__ void __launch_bounds__(kThreads) g_rows_kernel(const uint16_t *__restrict__ g, ConvBwdGeom q, int64_t ldp,
                                                           uint16_t *__restrict__ go) {
     pdl_launch_dependents();
@@ -59,11 +61,16 @@ __global__ void __launch_bounds__(kThreads) g_rows_kernel(const uint16_t *__rest
     const uint32_t hw = static_cast<uint32_t>(q.Ho * q.Wo);
     const uint32_t col = blockIdx.x * kThreads + threadIdx.x;
     if (col >= ldp) return;
-    const uint32_t b = col / hw, pix = col - b * hw;
-    for (int64_t o = blockIdx.y; o < q.O; o += gridDim.y) {
-        uint16_t v = 0;
-        if (col < q.P) v = g[(static_cast<int64_t>(b) * q.O + o) * hw + pix];
-        go[o * ldp + col] = v;
+    const bool live = col < q.P;
+    const uint32_t b = live ? col / hw : 0u, pix = col - b * hw;
+    const uint16_t *src = g + static_cast<int64_t>(b) * q.O * hw + pix;
+    for (int64_t o0 = static_cast<int64_t>(blockIdx.y) * kGRows; o0 < q.O; o0 += static_cast<int64_t>(gridDim.y) * kGRows) {
+        uint16_t v[kGRows];
+#pragma unroll
+        for (int r = 0; r < kGRows; ++r) v[r] = (live && o0 + r < q.O) ? src[(o0 + r) * hw] : uint16_t(0);
+#pragma unroll
+        for (int r = 0; r < kGRows; ++r)
+            if (o0 + r < q.O) go[(o0 + r) * ldp + col] = v[r];
     }
 }
 
@@ -351,7 +358,7 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
         uint16_t *go = reinterpret_cast<uint16_t *>(ws + pl.go_off);
         uint16_t *u = reinterpret_cast<uint16_t *>(ws + pl.u_off);
         float *part = reinterpret_cast<float *>(ws + pl.part_off);
-        cudaError_t e = launch_rows(g_rows_kernel, pl.ldp, q.O, s, g16, q, pl.ldp, go);
+        cudaError_t e = launch_rows(g_rows_kernel, pl.ldp, (q.O + kGRows - 1) / kGRows, s, g16, q, pl.ldp, go);
         if (e == cudaSuccess)
             e = x_dtype == BT_F32
                     ? launch_rows(sign_im2col_t_kernel<float>, pl.ldp, (q.T + kTapRows - 1) / kTapRows, s,
