@@ -77,8 +77,9 @@ __global__ void __launch_bounds__(kThreads) g_rows_kernel(const uint16_t *__rest
 // im2col of sign(x), transposed: u[t, p] (row pitch ldp) = sign(x[b, c, ih, iw])
 // as bf16 for tap t = (c, kh, kw) of output pixel p = (b, i, j), ih = i*s - p
 // + kh*d, iw = j*s - p + kw*d; 0 in the padding and for p >= P. A thread
-// keeps its pixel p and walks kTapRows consecutive taps, stepping (c, kh, kw)
-// without divisions.
+// keeps its pixel p and walks kTapRows consecutive taps, stepping (c, kh, kw),
+// (ih, iw), its channel plane and its output row without divisions or 64-bit
+// products (offsets within a plane are below H*W < 2^31).
 constexpr int kTapRows = 16;
 template <typename T>
 __global__ void __launch_bounds__(kThreads) sign_im2col_t_kernel(const T *__restrict__ x, ConvBwdGeom q, int64_t ldp,
@@ -91,20 +92,34 @@ __global__ void __launch_bounds__(kThreads) sign_im2col_t_kernel(const T *__rest
     const bool live = col < q.P;
     const uint32_t b = live ? col / hw : 0u, pix = col - b * hw, oi = pix / wo, oj = pix - oi * wo;
     const int h0 = static_cast<int>(oi) * q.s - q.p, w0 = static_cast<int>(oj) * q.s - q.p;
-    const int64_t xb = static_cast<int64_t>(b) * q.C * q.H * q.W;
+    const int H = static_cast<int>(q.H), W = static_cast<int>(q.W), k = q.k, d = q.d;
+    const int64_t HW = q.H * q.W;
+    const T *xb = x + static_cast<int64_t>(b) * q.C * HW;
+    const uint32_t kk = static_cast<uint32_t>(k * k);
     for (int64_t t0 = static_cast<int64_t>(blockIdx.y) * kTapRows; t0 < q.T;
          t0 += static_cast<int64_t>(gridDim.y) * kTapRows) {
-        const uint32_t kk = static_cast<uint32_t>(q.k * q.k);
-        uint32_t c = static_cast<uint32_t>(t0) / kk, tap = static_cast<uint32_t>(t0) - c * kk;
-        int kh = static_cast<int>(tap) / q.k, kw = static_cast<int>(tap) - kh * q.k;
-        const int64_t tend = t0 + kTapRows < q.T ? t0 + kTapRows : q.T;
-        for (int64_t t = t0; t < tend; ++t) {
+        const uint32_t c = static_cast<uint32_t>(t0) / kk, tap = static_cast<uint32_t>(t0) - c * kk;
+        int kh = static_cast<int>(tap) / k, kw = static_cast<int>(tap) - kh * k;
+        int ih = h0 + kh * d, iw = w0 + kw * d;
+        const T *xc = xb + static_cast<int64_t>(c) * HW;
+        uint16_t *ur = u + t0 * ldp + col;
+        const int n = static_cast<int>(t0 + kTapRows < q.T ? kTapRows : q.T - t0);
+        for (int i = 0; i < n; ++i, ur += ldp) {
             uint16_t v = 0;
-            const int ih = h0 + kh * q.d, iw = w0 + kw * q.d;
-            if (live && ih >= 0 && ih < q.H && iw >= 0 && iw < q.W)
-                v = sign_bf16_f(ld_f32<T>(x, xb + (static_cast<int64_t>(c) * q.H + ih) * q.W + iw));
-            u[t * ldp + col] = v;
-            if (++kw == q.k) { kw = 0; if (++kh == q.k) { kh = 0; ++c; } }
+            if (live && static_cast<unsigned>(ih) < static_cast<unsigned>(H) && static_cast<unsigned>(iw) < static_cast<unsigned>(W))
+                v = sign_bf16_f(ld_f32<T>(xc, ih * W + iw));
+            *ur = v;
+            iw += d;
+            if (++kw == k) {
+                kw = 0;
+                iw = w0;
+                ih += d;
+                if (++kh == k) {
+                    kh = 0;
+                    ih = h0;
+                    xc += HW;
+                }
+            }
         }
     }
 }
