@@ -130,11 +130,13 @@ __global__ void __launch_bounds__(kThreads) sign_im2col_t_kernel(const T *__rest
 // The taps that read (h, w) -- kh with h + p - kh*d = i*s, 0 <= i < Ho, and
 // the same for w -- are listed once per thread (S = the stride when it is 1
 // or 2, so the divisions become shifts; 0 for any stride); taps are summed
-// in (kh, kw) order.
+// in (kh, kw) order. The mask !(q < -1 || q > 1), q = x / scale_a rounded to
+// x's dtype, is !(x < -bound || x > bound) with the bound of mask_bound (NaN
+// keeps its gradient either way).
 constexpr int kCh = 8;                                        // channels per col2im thread
 template <typename T, int S>
 __global__ void __launch_bounds__(kThreads) col2im_mask_kernel(const float *__restrict__ dt, const T *__restrict__ x,
-                                                               ConvBwdGeom q, float scale_a, float norm,
+                                                               ConvBwdGeom q, float bound, float norm,
                                                                __nv_bfloat16 *__restrict__ gx, float *__restrict__ sum) {
     pdl_launch_dependents();
     pdl_wait();
@@ -175,9 +177,7 @@ __global__ void __launch_bounds__(kThreads) col2im_mask_kernel(const float *__re
             for (int ci = 0; ci < kCh; ++ci) {
                 if (ci >= nc) break;
                 const float y = __bfloat162float(__float2bfloat16_rn(acc[ci]));
-                float qv = __fdiv_rn(xv[ci], scale_a);
-                if constexpr (sizeof(T) == 2) qv = __bfloat162float(__float2bfloat16_rn(qv));
-                const float ym = __fmul_rn(y, (qv < -1.0f || qv > 1.0f) ? 0.0f : 1.0f);
+                const float ym = __fmul_rn(y, (xv[ci] < -bound || xv[ci] > bound) ? 0.0f : 1.0f);
                 const float sg = (xv[ci] > 0.0f ? 1.0f : 0.0f) - (xv[ci] < 0.0f ? 1.0f : 0.0f);
                 tsum = __fadd_rn(tsum, __fmul_rn(__fmul_rn(ym, sg), norm));
                 gx[base + ci * static_cast<int64_t>(hwin)] = __float2bfloat16_rn(ym);   // ym is bf16-exact
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads) col2im_mask_kernel(const float *__re
 }
 
 template <typename T>
-cudaError_t launch_col2im(const float *dt, const T *x, const ConvBwdGeom &q, float scale_a, float norm,
+cudaError_t launch_col2im(const float *dt, const T *x, const ConvBwdGeom &q, float bound, float norm,
                           __nv_bfloat16 *gx, float *sum, cudaStream_t s);
 
 // grad_w[i] = out_t(alpha * sum over the K splits of part[s][i]), fp32 sums in
@@ -230,12 +230,40 @@ cudaError_t launch_flat(K kern, int64_t work, cudaStream_t s, Args... args) {
 }
 
 template <typename T>
-cudaError_t launch_col2im(const float *dt, const T *x, const ConvBwdGeom &q, float scale_a, float norm,
+cudaError_t launch_col2im(const float *dt, const T *x, const ConvBwdGeom &q, float bound, float norm,
                           __nv_bfloat16 *gx, float *sum, cudaStream_t s) {
     const int64_t cols = q.H * q.W, rows = q.B * ((q.C + kCh - 1) / kCh);
-    if (q.s == 1) return launch_rows(col2im_mask_kernel<T, 1>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
-    if (q.s == 2) return launch_rows(col2im_mask_kernel<T, 2>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
-    return launch_rows(col2im_mask_kernel<T, 0>, cols, rows, s, dt, x, q, scale_a, norm, gx, sum);
+    if (q.s == 1) return launch_rows(col2im_mask_kernel<T, 1>, cols, rows, s, dt, x, q, bound, norm, gx, sum);
+    if (q.s == 2) return launch_rows(col2im_mask_kernel<T, 2>, cols, rows, s, dt, x, q, bound, norm, gx, sum);
+    return launch_rows(col2im_mask_kernel<T, 0>, cols, rows, s, dt, x, q, bound, norm, gx, sum);
+}
+
+// The straight-through mask keeps x where q = x / scale_a (fp32, then rounded
+// to x's dtype when that is bf16) lies in [-1, 1]. q is non-decreasing in x
+// and odd, so the kept x are [-bound, bound] (and NaN), bound = the largest
+// finite value v of x's dtype with q(v) <= 1: found here by bisection over
+// the bit patterns of the non-negative finite values, with the same IEEE
+// fp32 division and round-to-nearest-even as the definition.
+float mask_bound(float scale_a, bool bf16) {
+    auto value = [&](uint32_t u) {
+        const uint32_t bits = bf16 ? (u << 16) : u;
+        float f;
+        __builtin_memcpy(&f, &bits, 4);
+        return f;
+    };
+    auto kept = [&](uint32_t u) {
+        float qv = value(u) / scale_a;
+        if (bf16) qv = bf16_round_host(qv);
+        return qv <= 1.0f;
+    };
+    uint32_t lo = 0, hi = bf16 ? 0x7F7Fu : 0x7F7FFFFFu;   // kept(0); the largest finite pattern
+    if (kept(hi)) return value(hi);
+    while (hi - lo > 1) {
+        const uint32_t mid = lo + (hi - lo) / 2;
+        if (kept(mid)) lo = mid;
+        else hi = mid;
+    }
+    return value(lo);
 }
 
 // Pieces of the workspace. The input gradient's (g per pixel, D) and the
@@ -361,11 +389,12 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
                            nullptr, err, s) != cudaSuccess)
             return BT_ERR_CUDA;
         const float norm = static_cast<float>(1.0 / std::sqrt(static_cast<double>(B) * C * H * W));
+        const float bound = mask_bound(scale_a, x_dtype == BT_BF16);
         const cudaError_t e =
             x_dtype == BT_F32
-                ? launch_col2im(dt, static_cast<const float *>(x), q, scale_a, norm, static_cast<__nv_bfloat16 *>(grad_x),
+                ? launch_col2im(dt, static_cast<const float *>(x), q, bound, norm, static_cast<__nv_bfloat16 *>(grad_x),
                                 sum, s)
-                : launch_col2im(dt, static_cast<const __nv_bfloat16 *>(x), q, scale_a, norm,
+                : launch_col2im(dt, static_cast<const __nv_bfloat16 *>(x), q, bound, norm,
                                 static_cast<__nv_bfloat16 *>(grad_x), sum, s);
         if (e != cudaSuccess) return BT_ERR_CUDA;
     }
