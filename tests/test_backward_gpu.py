@@ -264,6 +264,33 @@ def test_conv_backward_grad_weight_f32():
     _conv_run_and_compare(2, 16, 12, 12, 32, 3, 2, 1, 1, torch.bfloat16, torch.float32, seed=9)
 
 
+@pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float32], ids=["x_bf16", "x_f32"])
+def test_conv_backward_mask_at_the_bound(x_dtype):
+    # every x on or next to +-scale_a in x's dtype (the consecutive values of
+    # the type around it, both signs): the kept set, decided from
+    # fp32(x / scale_a) rounded to x's dtype, must be the oracle's exactly.
+    # All-positive weights and gradients make every kept gradient nonzero.
+    sa = float(np.float32(0.7137))
+    if x_dtype == torch.bfloat16:
+        base = int(torch.tensor([sa]).to(torch.bfloat16).view(torch.int16).item())
+        vals = torch.tensor([base + j for j in range(-12, 13)], dtype=torch.int16).view(torch.bfloat16).float()
+    else:
+        base = int(np.float32(sa).view(np.int32))
+        vals = torch.from_numpy(np.array([base + j for j in range(-12, 13)], dtype=np.int32).view(np.float32))
+    vals = torch.cat([vals, -vals])
+    B, C, H, W, O = 1, 4, 5, 5, 8
+    x = vals.repeat((B * C * H * W + vals.numel() - 1) // vals.numel())[: B * C * H * W].view(B, C, H, W).to(x_dtype)
+    w = torch.ones(O, C, 3, 3, dtype=torch.bfloat16)
+    g = torch.ones(B, O, H, W, dtype=torch.bfloat16)
+    wst = bt.bt_sign_transpose(w.view(O, -1).to(DEV))
+    gx, _, _ = bt.bt_binary_conv2d_backward(x.to(DEV), wst, g.to(DEV), O, 3, 1, 1, 1, sa, 1.0, grad_weight_dtype=None)
+    o = oracle.conv2d_backward(x.float().numpy(), w.float().numpy(), g.float().numpy(), sa, 1.0, 1, 1, 1,
+                               "bf16" if x_dtype == torch.bfloat16 else "f32")
+    kept = gx.cpu().float().numpy() != 0
+    assert 0 < int(o["middle"].sum()) < o["middle"].size
+    np.testing.assert_array_equal(kept, o["middle"] != 0)
+
+
 def test_conv_backward_partial_and_empty():
     x, w, g, sa, sw = _conv_inputs(2, 8, 9, 9, 16, 3, 1, 1, 1, torch.bfloat16, 4)
     wst = bt.bt_sign_transpose(w.view(16, -1).to(DEV))

@@ -89,6 +89,22 @@ def test_w8a8_extreme_integer_sums_are_exact():
     np.testing.assert_array_equal(got, o["y"])
 
 
+@pytest.mark.parametrize("unfold", ["staged", "gather"])
+def test_w8a8_rounding_ties_to_even(unfold, monkeypatch):
+    # max|x| = 127, so the input scale is 1 and x * (1 / scale) = x: every
+    # other value is an exact tie k + 1/2, which rounds to even on both sides
+    if unfold == "gather":
+        monkeypatch.setenv("BT_W8A8_UNFOLD", "gather")
+    ties = torch.tensor([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5, -126.5, 63.5, -64.5, 127.0])
+    x = ties.repeat(2 * 3 * 6 * 6 // ties.numel()).view(2, 3, 6, 6)
+    gen = torch.Generator().manual_seed(11)
+    w = torch.randn(8, 3, 3, 3, generator=gen)
+    got = bt.bt_w8a8_conv2d(x.to(DEV), w.to(DEV), 1, 1, 1).cpu().numpy()
+    o = oracle.w8a8_conv2d(x.numpy(), w.numpy(), 1, 1, 1, False)
+    assert float(o["sx"]) == 1.0
+    np.testing.assert_array_equal(got, o["y"])
+
+
 def test_w8a8_zero_input_and_empty_batch():
     x = torch.zeros(2, 8, 6, 6, device=DEV)
     w = torch.randn(16, 8, 3, 3, device=DEV)
