@@ -482,13 +482,9 @@ def fake_quant_int8(v: np.ndarray):
     return q, scale
 
 
-def w8a8_conv2d(x, w, stride: int, padding: int, dilation: int, smooth: bool = False) -> dict:
-    """MyQuantConv2d.forward: unfold x into im2col rows [P, C*k*k] (zero
-    padding), flatten w to [O, C*k*k]; with SmoothQuant, per column
-    act = max|rows|, wmax = max|w|, scale = sqrt(act / wmax) (fp32), rows /=
-    scale, w *= scale; quantize both (fake_quant_int8); the product of the
-    dequantized values is sum(q_x * q_w) * s_x * s_w, taken exactly and
-    rounded as y = fp32(double(dot) * double(fp32(s_x * s_w))); NCHW out."""
+def _w8a8_quantized(x, w, stride: int, padding: int, dilation: int, smooth: bool):
+    """The quantized operands of MyQuantConv2d.forward (see w8a8_conv2d):
+    returns (rows, wf, scale_col, qx, sx, qw, sw, alpha, (B, O, ho, wo))."""
     x32 = torch.from_numpy(_as_f32(x))
     w32 = _as_f32(w)
     B, C, H, W = x32.shape
@@ -508,10 +504,36 @@ def w8a8_conv2d(x, w, stride: int, padding: int, dilation: int, smooth: bool = F
             wf = (wf * scale_col).astype(np.float32)
     qx, sx = fake_quant_int8(rows)
     qw, sw = fake_quant_int8(wf)
-    dot = qx @ qw.T                                                                # exact int64 [P, O]
     alpha = np.float32(np.float64(sx) * np.float64(sw))
+    return rows, wf, scale_col, qx, sx, qw, sw, alpha, (B, O, ho, wo)
+
+
+def w8a8_conv2d(x, w, stride: int, padding: int, dilation: int, smooth: bool = False) -> dict:
+    """MyQuantConv2d.forward: unfold x into im2col rows [P, C*k*k] (zero
+    padding), flatten w to [O, C*k*k]; with SmoothQuant, per column
+    act = max|rows|, wmax = max|w|, scale = sqrt(act / wmax) (fp32), rows /=
+    scale, w *= scale; quantize both (fake_quant_int8); the product of the
+    dequantized values is sum(q_x * q_w) * s_x * s_w, taken exactly and
+    rounded as y = fp32(double(dot) * double(fp32(s_x * s_w))); NCHW out."""
+    rows, wf, scale_col, qx, sx, qw, sw, alpha, (B, O, ho, wo) = _w8a8_quantized(x, w, stride, padding, dilation,
+                                                                                 smooth)
+    dot = qx @ qw.T                                                                # exact int64 [P, O]
     y = (dot.astype(np.float64) * np.float64(alpha)).astype(np.float32)
     y = y.reshape(B, ho * wo, O).transpose(0, 2, 1).reshape(B, O, ho, wo)
     return {"y": np.ascontiguousarray(y), "dot": dot, "qx": qx, "qw": qw, "sx": sx, "sw": sw, "alpha": alpha,
             "scale": scale_col, "rows": rows, "wf": wf}
 
+
+def w8a8_conv2d_at(x, w, stride: int, padding: int, dilation: int, smooth: bool, flat) -> np.ndarray:
+    """w8a8_conv2d's output at the flat NCHW indices `flat` only: the maxima
+    and the quantization over every row as there, the dot products of the
+    requested outputs alone (for workloads whose full product is too slow)."""
+    _, _, _, qx, _, qw, _, alpha, (B, O, ho, wo) = _w8a8_quantized(x, w, stride, padding, dilation, smooth)
+    flat = np.asarray(flat, dtype=np.int64)
+    j = flat % wo
+    i = (flat // wo) % ho
+    o = (flat // (wo * ho)) % O
+    b = flat // (wo * ho * O)
+    p = (b * ho + i) * wo + j
+    dot = np.einsum("ij,ij->i", qx[p], qw[o])
+    return (dot.astype(np.float64) * np.float64(alpha)).astype(np.float32)

@@ -703,3 +703,13 @@ def test_w8a8_smooth_balances_column_maxima():
     np.testing.assert_allclose(o["rows"].astype(np.float64) @ o["wf"].T.astype(np.float64),
                                plain["rows"].astype(np.float64) @ plain["wf"].T.astype(np.float64), rtol=1e-5,
                                atol=1e-4)
+
+
+@pytest.mark.parametrize("smooth", [False, True])
+def test_w8a8_at_agrees_with_full(smooth):
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((2, 5, 9, 8)) * np.logspace(-1, 1, 5)[None, :, None, None]).astype(np.float32)
+    w = rng.standard_normal((6, 5, 3, 3)).astype(np.float32)
+    full = oracle.w8a8_conv2d(x, w, 2, 1, 1, smooth)["y"]
+    flat = np.arange(full.size)
+    np.testing.assert_array_equal(oracle.w8a8_conv2d_at(x, w, 2, 1, 1, smooth, flat), full.reshape(-1))

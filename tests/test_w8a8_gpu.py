@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import oracle
+import workloads
 import xnor_popcount_gemm_gb300 as bt
 
 pytestmark = pytest.mark.gpu
@@ -111,3 +112,21 @@ def test_w8a8_zero_input_and_empty_batch():
     assert torch.all(bt.bt_w8a8_conv2d(x, w, 1, 1, 1).cpu() == 0)
     e = bt.bt_w8a8_conv2d(torch.empty(0, 8, 6, 6, device=DEV), w, 1, 1, 1)
     assert e.shape == (0, 16, 6, 6)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("smooth", [False, True], ids=["plain", "smoothquant"])
+@pytest.mark.parametrize("name", ["downsample_conv", "resnet_conv"])
+def test_w8a8_full_workloads_sampled(name, smooth):
+    # the benchmark's workloads at full size, as the benchmark calls them (f32
+    # out): sampled outputs and the four corners of every axis against the oracle
+    wl = workloads.NAMED[name]()
+    y = bt.bt_w8a8_conv2d(wl.x.to(DEV), wl.w.to(DEV), wl.stride, wl.padding, wl.dilation, smooth=smooth).cpu().numpy()
+    rng = np.random.default_rng(3)
+    idx = [rng.integers(0, n, 1500) for n in y.shape]
+    corners = np.array(np.meshgrid(*[[0, n - 1] for n in y.shape], indexing="ij")).reshape(4, -1)
+    b, o, i, j = [np.concatenate([a, c]) for a, c in zip(idx, corners)]
+    flat = ((b * y.shape[1] + o) * y.shape[2] + i) * y.shape[3] + j
+    want = oracle.w8a8_conv2d_at(wl.x.float().numpy(), wl.w.float().numpy(), wl.stride, wl.padding, wl.dilation,
+                                 smooth, flat)
+    np.testing.assert_array_equal(y.reshape(-1)[flat], want)
