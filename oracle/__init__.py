@@ -444,6 +444,26 @@ def conv2d_backward(x, w, g, scale_a: float, scale_w: float, stride: int, paddin
             "grad_weight": bf16_round(gw_exact), "grad_weight_exact": gw_exact}
 
 
+def conv2d_grad_weight_at(x, g, scale_a: float, stride: int, padding: int, dilation: int, k: int, o_idx,
+                          t_idx) -> np.ndarray:
+    """Entries (o, t) of conv2d_backward's exact weight gradient, t = (c, kh,
+    kw) flattened in OIHW order: the sum over images b and output pixels
+    (i, j) of g[b, o, i, j] * bf16(sign(x) * scale_a)[b, c, i*s - p + kh*d,
+    j*s - p + kw*d] (0 in the padding), in float64, from the unfold of the
+    scaled signs. For layers whose whole gradient is too slow here."""
+    x32 = _as_f32(x)
+    g64 = _as_f32(g).astype(np.float64)
+    xs = torch.from_numpy(bf16_round(sign(x32) * np.float32(scale_a)).astype(np.float64))
+    u = F.unfold(xs, k, dilation=dilation, padding=padding, stride=stride).numpy()     # [B, C*k*k, L]
+    gl = g64.reshape(g64.shape[0], g64.shape[1], -1)                                 # [B, O, L]
+    o_idx, t_idx = np.asarray(o_idx), np.asarray(t_idx)
+    out = np.empty(o_idx.size, np.float64)
+    for s0 in range(0, o_idx.size, 64):
+        o, t = o_idx[s0:s0 + 64], t_idx[s0:s0 + 64]
+        out[s0:s0 + 64] = (gl[:, o, :] * u[:, t, :]).sum(axis=(0, 2))
+    return out
+
+
 def scale_init(x, factor: float, x_dtype: str, scale_dtype: str) -> float:
     """BinaryConv2dCutlass.set_activation's first-call scale:
     (factor * x.abs().mean()).to(layer dtype). Reading: the mean is the exact

@@ -19,6 +19,7 @@ import pytest
 import torch
 
 import oracle
+import workloads
 import xnor_popcount_gemm_gb300 as bt
 
 pytestmark = pytest.mark.gpu
@@ -302,6 +303,48 @@ def test_conv_backward_partial_and_empty():
     ge = torch.empty(0, 16, 9, 9, dtype=torch.bfloat16, device=DEV)
     gxe, gsae, gwe = bt.bt_binary_conv2d_backward(e, wst, ge, 16, 3, 1, 1, 1, sa, sw)
     assert gxe.numel() == 0 and float(gsae.cpu()) == 0.0 and torch.all(gwe.cpu() == 0)
+
+
+@pytest.mark.slow
+def test_conv_backward_full_size_sampled():
+    # the stride-2 layer at full size as the benchmark runs it (its x and W,
+    # an N(0, 0.01) bf16 upstream gradient): grad_input of four whole images
+    # (each depends on its own g alone), sampled grad_weight entries, and
+    # grad_scale_a recomputed from the GPU's own grad_input
+    wl = workloads.NAMED["downsample_conv"]()
+    x, w = wl.x, wl.w
+    B, C, H, W = x.shape
+    O, _, k, _ = w.shape
+    s, p, d = wl.stride, wl.padding, wl.dilation
+    ho, wo = oracle.conv2d_out_size(H, k, s, p, d), oracle.conv2d_out_size(W, k, s, p, d)
+    gen = torch.Generator().manual_seed(31)
+    g = (torch.randn(B, O, ho, wo, generator=gen) * 0.01).to(torch.bfloat16)
+    sa, sw = wl.scale_a, wl.scale_w
+    wst = bt.bt_sign_transpose(w.reshape(O, -1).to(DEV))
+    gx, gsa, gw = bt.bt_binary_conv2d_backward(x.to(DEV), wst, g.to(DEV), O, k, s, p, d, sa, sw)
+    torch.cuda.synchronize()
+    gx, gsa, gw = gx.cpu(), float(gsa.cpu()), gw.cpu()
+    imgs = np.array([0, 1, 127, B - 1])
+    o = oracle.conv2d_backward(x[imgs].float().numpy(), w.float().numpy(), g[imgs].float().numpy(), sa, sw, s, p, d,
+                               "bf16")
+    bw = float(oracle.bf16_round(np.float32(sw)))
+    abs_in = torch.nn.grad.conv2d_input((len(imgs), C, H, W), torch.full(w.shape, bw, dtype=torch.float64),
+                                        g[imgs].double().abs(), stride=s, padding=p, dilation=d).numpy()
+    gxs = gx[imgs].float().numpy()
+    assert np.all(gxs[o["middle"] == 0] == 0), "mask disagrees"
+    _check_sum(gxs, o["grad_input"], abs_in, O * k * k, "conv grad_input images")
+    rng = np.random.default_rng(5)
+    oi = np.concatenate([rng.integers(0, O, 600), [0, 0, O - 1, O - 1]])
+    ti = np.concatenate([rng.integers(0, C * k * k, 600), [0, C * k * k - 1, 0, C * k * k - 1]])
+    want = oracle.conv2d_grad_weight_at(x.float().numpy(), g.float().numpy(), sa, s, p, d, k, oi, ti)
+    ba = float(oracle.bf16_round(np.float32(sa)))
+    bound = g.double().abs().sum(dim=(0, 2, 3)).numpy()[oi] * ba
+    _check_sum(gw.reshape(O, -1).float().numpy()[oi, ti], oracle.bf16_round(want), bound, B * ho * wo,
+               "conv grad_weight entries")
+    xf = x.float().numpy()
+    terms = ((gx.float().numpy() * oracle.sign(xf)).astype(np.float32) * np.float32(1.0 / np.sqrt(x.numel())))
+    terms = terms.astype(np.float64)
+    assert abs(gsa - terms.sum()) <= 1e-5 * np.abs(terms).sum()
 
 
 @pytest.mark.slow

@@ -713,3 +713,16 @@ def test_w8a8_at_agrees_with_full(smooth):
     full = oracle.w8a8_conv2d(x, w, 2, 1, 1, smooth)["y"]
     flat = np.arange(full.size)
     np.testing.assert_array_equal(oracle.w8a8_conv2d_at(x, w, 2, 1, 1, smooth, flat), full.reshape(-1))
+
+
+@pytest.mark.parametrize("s,p,d", [(1, 1, 1), (2, 1, 1), (2, 2, 2)])
+def test_conv2d_grad_weight_at_agrees_with_full(s, p, d):
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((2, 3, 9, 8)).astype(np.float32)
+    w = rng.standard_normal((4, 3, 3, 3)).astype(np.float32)
+    ho, wo = oracle.conv2d_out_size(9, 3, s, p, d), oracle.conv2d_out_size(8, 3, s, p, d)
+    g = oracle.bf16_round(rng.standard_normal((2, 4, ho, wo)).astype(np.float32))
+    full = oracle.conv2d_backward(x, w, g, 0.7, 0.3, s, p, d, "f32")["grad_weight_exact"].reshape(4, -1)
+    o_idx, t_idx = np.meshgrid(np.arange(4), np.arange(27), indexing="ij")
+    got = oracle.conv2d_grad_weight_at(x, g, 0.7, s, p, d, 3, o_idx.ravel(), t_idx.ravel())
+    np.testing.assert_array_equal(got, full.ravel())
