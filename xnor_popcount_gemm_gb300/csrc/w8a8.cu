@@ -249,10 +249,10 @@ __device__ __forceinline__ uint32_t quant_pair(float v0, float v1, float inv) {
 // gathers 8 taps of one pixel per thread, the pixels along the lanes (the
 // window read at a stride of s elements, the tile written with 16-byte
 // stores at an odd 16-byte pitch); stage 3 writes the runs of taps with
-// 16-byte stores, consecutive threads on consecutive chunks. Shared memory: tile [1 << qbits]
-// [pitch] u16, tap byte offsets [TB] int, pixel corner (bytes) and row
-// [1 << qbits] int each, scales [TB] f32 (SmoothQuant), window [CC][NR][NW]
-// (u16 codes, or T with SmoothQuant).
+// 16-byte stores, consecutive threads on consecutive chunks. Shared memory:
+// tile [1 << qbits][pitch] u16, tap byte offsets [TB] int, pixel corner
+// (bytes) and row [1 << qbits] int each, scales [TB] f32 (SmoothQuant),
+// window [CC][NR][NW] (u16 codes, or T with SmoothQuant).
 template <typename T, bool SMOOTH>
 __global__ void __launch_bounds__(kThreads, 5) quant_tile_kernel(const T *__restrict__ x, Geo g, QTile u,
                                                               const float *__restrict__ scale,
@@ -405,11 +405,11 @@ size_t qtile_smem(const QTile &u, int es, bool smooth) {
 }
 
 // The staged unfold's plan: 16 channels (more for small kernels, up to ~144
-// taps a row, at most the channel count rounded up to 16) and 64 pixel slots (fewer while the tile passes 28 KB), a band
-// of whole output rows where Wo fits, else a range of columns; the window
-// shrinks (rows, then columns) until it fits 16 KB, 16-bit offsets and
-// kStageItems items per thread. False:
-// no plan fits (very large dilation), the direct gather takes the call.
+// taps a row, at most the channel count rounded up to 16) and 64 pixel slots
+// (fewer while the tile passes 28 KB); a band of whole output rows where Wo
+// fits, else a range of columns; the window shrinks (rows, then columns)
+// until it fits 16 KB and kStageItems items per thread. False: no plan fits
+// (very large dilation), and the direct gather takes the call.
 bool plan_qtile(const Geo &g, int es, QTile &u) {
     const int kk = g.k * g.k;
     // 32-bit window coordinates and offsets within an image
@@ -434,7 +434,7 @@ bool plan_qtile(const Geo &g, int es, QTile &u) {
     for (;;) {
         const int64_t NR = (R - 1) * g.s + reach, NW = (Wc - 1) * g.s + reach;
         const int64_t E = NR * NW;
-        if (E * u.CC <= 65535 && E * u.CC * es <= 16 * 1024 && E * (u.CC / 8) <= kStageItems * kThreads) {
+        if (E * u.CC * es <= 16 * 1024 && E * (u.CC / 8) <= kStageItems * kThreads) {
             u.R = static_cast<int>(R);
             u.Wc = static_cast<int>(Wc);
             u.nb = static_cast<int>((g.Ho + R - 1) / R);
