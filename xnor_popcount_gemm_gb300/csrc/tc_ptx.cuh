@@ -76,16 +76,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
-// The same, delivered to every CTA of the cluster in `mask` (at the same
-// shared-memory offsets, signalling each one's mbarrier at `bar`'s offset).
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *m, int c0, int c1, uint32_t bar,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-        : "memory");
-}
 // 3-D tiled copies: coordinates {c0, c1, c2} of the box's first element.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, int c0, int c1, int c2, uint32_t bar) {
     asm volatile(
@@ -273,14 +263,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// The same arrival on the mbarrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(bar), "h"(mask)
-        : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
