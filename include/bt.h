@@ -267,8 +267,15 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype,
  * process exits. Calls allocate nothing (no cudaMalloc / cudaFree).
  *   - A problem whose bt_binary_linear_workspace(M, K, x_dtype, w_code)
  *     exceeds that size returns BT_ERR_WORKSPACE and launches nothing.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - The array's device address belongs to the CUDA context current on the
+ *     calling thread: each context that loads the library (the device's
+ *     primary context, a framework's own driver context) has its own copy.
+ *     The first call that packs activations in a context looks that address
+ *     up (cudaGetSymbolAddress, with the context current) and caches it per
+ *     context; make that first call before any stream capture.
+ *   - Packed activations (x_dtype BT_PACKED) and M == 0 need no scratch: such
+ *     a call goes straight to bt_binary_linear with no workspace and looks
+ *     nothing up.
  *   - Every call shares the one array: calls whose kernels overlap on the
  *     GPU race on it. Each call rewrites all of the scratch it reads, so
  *     nothing carries over from the previous call.

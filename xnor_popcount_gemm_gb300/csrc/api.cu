@@ -24,18 +24,32 @@ int device_sm_count() {
     return n[dev];
 }
 
-unsigned int *device_error_word() {
-    static std::mutex mu;
-    static unsigned int *ptrs[128] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (ptrs[dev] == nullptr) {
+bool current_context_id(unsigned long long *id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<unsigned int *>(p);
-    }
-    return ptrs[dev];
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (get_current == nullptr || get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+unsigned int *device_error_word() {
+    static SymbolAddressCache cache;
+    cudaError_t err = cudaSuccess;
+    return static_cast<unsigned int *>(
+        cache.get([](void **p) { return cudaGetSymbolAddress(p, g_error_word); }, &err));
 }
 
 namespace {

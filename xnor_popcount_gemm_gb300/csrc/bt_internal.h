@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -36,9 +37,53 @@ inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 // Streaming multiprocessors of the current device (looked up once per device).
 int device_sm_count();
 
-// Device error word of the current device (a static __device__ variable,
-// address looked up once per device). Returns nullptr on a CUDA error.
+// Device error word (a __device__ variable) as seen from the calling
+// thread's current CUDA context. Returns nullptr on a CUDA error.
 unsigned int *device_error_word();
+
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, never
+// reused within the process). False when no context is current or the driver
+// lacks the query.
+bool current_context_id(unsigned long long *id);
+
+// The device address of a __device__ variable belongs to one CUDA context:
+// another context on the same device (a framework's own driver context, or
+// the primary context again after cudaDeviceReset) holds its own copy of the
+// module at another address. This cache keys the address by the current
+// context's id. `lookup(void **)` runs cudaGetSymbolAddress in the translation
+// unit that defines the variable (the host-side name of a __device__
+// variable is a stand-in registered per translation unit) with the context
+// current; it runs once per context, or on every call when no context id can
+// be read.
+struct SymbolAddressCache {
+    static constexpr int kSlots = 16;
+    std::mutex mu;
+    unsigned long long ids[kSlots] = {};
+    void *ptrs[kSlots] = {};
+    int next = 0;
+
+    template <typename Lookup> void *get(Lookup lookup, cudaError_t *err) {
+        unsigned long long id = 0;
+        bool keyed = current_context_id(&id);
+        if (keyed) {
+            std::lock_guard<std::mutex> lock(mu);
+            for (int i = 0; i < kSlots; ++i)
+                if (ptrs[i] != nullptr && ids[i] == id) return ptrs[i];
+        }
+        void *p = nullptr;
+        *err = lookup(&p);
+        if (*err != cudaSuccess) return nullptr;
+        // the lookup may have made the device's primary context current
+        if (!keyed) keyed = current_context_id(&id);
+        if (keyed) {
+            std::lock_guard<std::mutex> lock(mu);
+            ids[next] = id;
+            ptrs[next] = p;
+            next = (next + 1) % kSlots;
+        }
+        return p;
+    }
+};
 
 // Launchers (enqueue only; the caller has validated every argument) ---------
 cudaError_t launch_pack_rows(const void *x, bt_dtype xt, int64_t R, int64_t K, const float *bias,

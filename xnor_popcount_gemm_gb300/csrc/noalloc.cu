@@ -15,8 +15,6 @@
 // sharing nothing but a host thread) race on it. Each call's pack kernel
 // rewrites every byte it later reads (rows and their zero padding), so
 // nothing left by an earlier call needs clearing.
-#include <mutex>
-
 #include "bt_internal.h"
 
 namespace bt {
@@ -27,26 +25,12 @@ constexpr size_t kNoallocScratchBytes = size_t(16) << 20;   // 16 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
 // In host code `g_noalloc_scratch` names a host-side stand-in, not device
-// memory, so its device address is looked up once per device (with that device
-// current) and cached.
+// memory. Its device address is looked up with the caller's device (and
+// context) current, once per CUDA context: each context that loads the library
+// holds its own copy of the array.
 void *scratch_address(cudaError_t *err) {
-    static std::mutex mu;
-    static void *ptrs[128] = {};
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= 128) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(mu);
-    if (ptrs[dev] == nullptr) {
-        void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        ptrs[dev] = p;
-    }
-    return ptrs[dev];
+    static SymbolAddressCache cache;
+    return cache.get([](void **p) { return cudaGetSymbolAddress(p, g_noalloc_scratch); }, err);
 }
 
 }  // namespace
@@ -60,6 +44,12 @@ extern "C" bt_status bt_binary_linear_noalloc(const void *x, bt_dtype x_dtype, c
                                               bt_algo algo, bt_stream stream) {
     const size_t need = bt_binary_linear_workspace(M, K, x_dtype, w_code);
     if (need > bt::kNoallocScratchBytes) return BT_ERR_WORKSPACE;
+    if (need == 0) {
+        // nothing to pack (packed x, M == 0, or arguments bt_binary_linear
+        // rejects): no scratch, so no address lookup either
+        return bt_binary_linear(x, x_dtype, weight, w_code, M, N, K, scale_a, scale_w, bias_a, bias_len, out,
+                                out_dtype, algo, nullptr, 0, stream);
+    }
     cudaError_t err = cudaSuccess;
     void *scratch = bt::scratch_address(&err);
     if (scratch == nullptr) return BT_ERR_CUDA;
