@@ -3,8 +3,9 @@
 One step = one forward over one batch of synthetic input: shift + sign +
 pack of the activations, the packed contraction and the fused scale + cast
 epilogue. Weights are packed once, before timing (bitorch-engine packs
-weights offline, in generate_quantized_weight / w_pack). Default workload: the 4096 x 4096 x 4096 bf16
-linear layer with a scalar activation bias.
+weights offline, in generate_quantized_weight / w_pack). Default workload: the
+largest configuration, the 8192 x 4096 x 11008 bf16 linear layer; after it,
+`all_configs` records every configuration with each code the library has.
 
 Prints ONE JSON line on rank 0. Under torchrun every rank runs its own
 replica of the workload (its shard of a batch N times larger; no collective
@@ -39,10 +40,13 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="llm_linear", choices=sorted(workloads.NAMED))
+    ap.add_argument("--workload", default="large_linear", choices=sorted(workloads.NAMED))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", default="auto", choices=["auto", "popc", "e4m3", "e2m1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the record of every configuration (all_configs) after the headline")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps per configuration and code")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the headline steps one call at a time instead of replaying them as a CUDA graph")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward", "w8a8", "w8a8-smooth"],
@@ -215,6 +219,243 @@ def roofline_peak(algo: str, peaks: dict, sms: int):
 ALGO_NAME = {0: "popc", 1: "e4m3", 2: "e2m1"}
 
 
+CODE_OF = {"popc": 0, "e4m3": 1, "e2m1": 2}
+
+
+class ForwardSetup:
+    """One forward step of a workload as a user's stream runs it: the pack call
+    (shift + sign + pack of x), then the contraction call (packed contraction
+    + fused scale and cast), over input and output buffers that rotate so that
+    one pass over them exceeds L2. Weights are packed once, here, outside any
+    timing (bitorch-engine packs them offline)."""
+
+    def __init__(self, bt, wl, code: int, algo: int, dev):
+        self.bt, self.wl, self.code, self.algo = bt, wl, code, algo
+        M, N, K = wl.gemm_shape()
+        self.M, self.N, self.K = M, N, K
+        self.out_t = {"f32": torch.float32, "bf16": torch.bfloat16}[wl.out_dtype]
+        if wl.kind == "linear":
+            self.wp = bt.bt_pack_sign(wl.w.to(dev), code)
+        else:
+            self.wp = bt.bt_pack_sign(wl.w.to(dev), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+        self.bias = None if wl.bias is None else wl.bias.to(dev)
+        self.x_bytes = wl.x.numel() * wl.x.element_size()
+        self.out_bytes = M * N * torch.tensor([], dtype=self.out_t).element_size()
+        self.nbuf = max(1, -(-2 * L2_BYTES // (self.x_bytes + self.out_bytes)))
+        self.xs = [wl.x.to(dev) for _ in range(self.nbuf)]
+        self.single_pass = False
+        self.ws_rows = None
+        if wl.kind == "linear":
+            self.outs = [torch.empty((M, N), dtype=self.out_t, device=dev) for _ in range(self.nbuf)]
+            self.ws = torch.empty(bt.bt_binary_linear_workspace(M, K, bt.BT_BF16, code), dtype=torch.uint8,
+                                  device=dev)
+            xp_shape = (M, bt.bt_packed_row_bytes(K, code))
+        else:
+            B, C, H, W = wl.x.shape
+            k = wl.w.shape[2]
+            self.C, self.k = C, k
+            Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
+            Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
+            self.im2col_hw = (B, H, W)
+            self.outs = [torch.empty((B, N, Ho, Wo), dtype=self.out_t, device=dev) for _ in range(self.nbuf)]
+            geom = (B, C, H, W, k, wl.stride, wl.padding, wl.dilation)
+            self.ws = torch.empty(max(1, bt.bt_binary_conv2d_workspace(*geom, bt.BT_BF16, code)), dtype=torch.uint8,
+                                  device=dev)
+            # the two public calls that split the library's own path for this shape
+            self.single_pass = bool(bt.bt_conv2d_single_pass(
+                *geom, {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16, torch.float16: bt.BT_F16}[wl.x.dtype],
+                code))
+            if not self.single_pass:
+                # packed NHWC pixels; the contraction call unfolds them (where it
+                # needs rows) or contracts them in place
+                xp_shape = (B, H, W, bt.bt_packed_row_bytes(C, code))
+                ws_rows_bytes = bt.bt_binary_conv2d_workspace(*geom, bt.BT_PACKED, code)
+                self.ws_rows = torch.empty(ws_rows_bytes, dtype=torch.uint8, device=dev) if ws_rows_bytes else None
+            else:
+                # im2col rows of packed codes (one pass from x), contracted with the weights
+                xp_shape = (B * Ho * Wo, k * k * bt.bt_packed_row_bytes(C, code))
+        self.xp = torch.empty(xp_shape, dtype=torch.uint8, device=dev)
+        # kernels per step: the pack, then the contraction; a contraction call
+        # that unfolds packed pixels into rows first adds one
+        unfolds = wl.kind == "conv" and not self.single_pass and self.ws_rows is not None
+        self.launches_per_step = 3 if unfolds else 2
+
+    def step(self, i, ev=None):
+        bt, wl = self.bt, self.wl
+        x, out = self.xs[i % self.nbuf], self.outs[i % self.nbuf]
+        if ev is not None:
+            ev[0].record(torch.cuda.current_stream())
+        if wl.kind == "linear":
+            bt.bt_pack_sign(x, self.code, bt.BT_LAYOUT_ROWS, self.bias, out=self.xp)
+        elif not self.single_pass:
+            bt.bt_pack_sign(x, self.code, bt.BT_LAYOUT_NCHW_TO_NHWC, self.bias, out=self.xp)
+        else:
+            bt.bt_pack_im2col(x, self.code, self.k, wl.stride, wl.padding, wl.dilation, self.bias, out=self.xp)
+        if ev is not None:
+            ev[1].record(torch.cuda.current_stream())
+        if wl.kind == "linear":
+            bt.bt_binary_linear(self.xp, self.wp, self.code, self.K, wl.scale_a, wl.scale_w, out=out,
+                                out_dtype=self.out_t, algo=self.algo, x_packed=True)
+        elif not self.single_pass:
+            bt.bt_binary_conv2d(self.xp, self.wp, self.code, self.C, self.k, wl.stride, wl.padding, wl.dilation,
+                                wl.scale_a, wl.scale_w, out=out, out_dtype=self.out_t, algo=self.algo,
+                                x_packed=True, workspace=self.ws_rows)
+        else:
+            bt.bt_binary_conv2d(self.xp, self.wp, self.code, self.C, self.k, wl.stride, wl.padding, wl.dilation,
+                                wl.scale_a, wl.scale_w, out=out, out_dtype=self.out_t, algo=self.algo,
+                                x_im2col_hw=self.im2col_hw)
+        if ev is not None:
+            ev[2].record(torch.cuda.current_stream())
+
+    def capture(self, steps: int, use_graph: bool):
+        """The K steps captured once into a CUDA graph (each public call's
+        kernels as nodes, nothing between the two calls of a step), or None
+        when capture is off or unsupported; and a note saying which."""
+        if not use_graph:
+            return None, "off (--no-graph)"
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(steps):
+                    self.step(i)
+            graph.replay()
+            torch.cuda.synchronize()
+            return graph, f"one CUDA graph of the {steps} steps, replayed"
+        except RuntimeError as e:                       # capture unsupported: launch eagerly
+            torch.cuda.synchronize()
+            return None, f"off (capture failed: {str(e).splitlines()[0][:80]})"
+
+    def run_steps(self, graph, steps: int, world: int = 1) -> float:
+        """Milliseconds of `steps` back-to-back steps (device events on the
+        launching stream, barrier and synchronize on both sides)."""
+        stream = torch.cuda.current_stream()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(steps):
+                self.step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return t0.elapsed_time(t1)
+
+    def split(self, steps: int):
+        """Mean milliseconds of the pack call and of the contraction call, from
+        events around each on the launching stream (they serialise the two and
+        add each launch's latency to its kernel)."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            self.step(i, evs[i])
+        torch.cuda.synchronize()
+        return (statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+                statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
+
+
+def step_bytes(wl) -> float:
+    """Algorithmic bytes of one forward step: x read once, the weights packed
+    to one bit per element, the output written once."""
+    M, N, K = wl.gemm_shape()
+    out_b = 4 if wl.out_dtype == "f32" else 2
+    return wl.x.numel() * wl.x.element_size() + N * K / 8 + M * N * out_b
+
+
+def contraction_bytes(wl, code, bt) -> float:
+    """Least bytes the contraction call moves: the packed activations (rows of
+    a linear layer; the packed pixels of a convolution, each read once by an
+    implicit im2col), the packed weights, the output."""
+    out_b = 4 if wl.out_dtype == "f32" else 2
+    if wl.kind == "linear":
+        M, K = wl.x.shape
+        N = wl.w.shape[0]
+        rb = bt.bt_packed_row_bytes(K, code)
+        return (M + N) * rb + M * N * out_b
+    B, C, H, W = wl.x.shape
+    O, k = wl.w.shape[0], wl.w.shape[2]
+    Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
+    Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
+    rbc = bt.bt_packed_row_bytes(C, code)
+    return B * H * W * rbc + O * k * k * rbc + B * O * Ho * Wo * out_b
+
+
+def roofline_of(ops: float, nbytes: float, ms: float, algo_name: str, peaks: dict, sms: int) -> dict:
+    """Roofline of `ops` binary ops moving `nbytes` in `ms`: bound by the pipe
+    of the code used (tensor fp4 / fp8, or the POPC ALU) when the ops per byte
+    exceed that pipe's ridge point (peak ops / measured HBM bandwidth), by HBM
+    otherwise; frac = achieved / peak of that bound."""
+    bound, peak, unit, how = roofline_peak(algo_name, peaks, sms)
+    intensity = ops / nbytes
+    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity < ridge:
+        bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
+        how = f"measured copy bandwidth; {intensity:.0f} ops/B < ridge {ridge:.0f}"
+        achieved = nbytes / (ms / 1e3) / 1e9
+    else:
+        achieved = ops / (ms / 1e3) / 1e12
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "algorithmic_bytes": int(nbytes), "ops_per_byte": round(intensity, 1),
+            "peak_how": how}
+
+
+# every configuration the workloads module names, in the order of the table
+CONFIG_ORDER = ["tiny_linear", "llm_linear", "resnet_conv", "downsample_conv", "downsample_conv_d2",
+                "large_linear", "ragged_linear"]
+
+
+def sweep_configs(bt, dev, peaks, peak_src, sms, args) -> dict:
+    """Every configuration, each code the library has (the planner's choice
+    first): graph-replayed step time, the pack / contraction split, and the
+    rooflines of the step (its algorithmic bytes) and of the contraction call.
+    The per-code step times show whether the planner ("ADAPTIVE") picks the
+    fastest code for each shape."""
+    steps, warm = args.config_steps, 3
+    out = {}
+    for name in CONFIG_ORDER:
+        wl = workloads.NAMED[name]()
+        M, N, K = wl.gemm_shape()
+        ops = wl.binary_ops()
+        op = bt.BT_OP_LINEAR if wl.kind == "linear" else bt.BT_OP_CONV2D
+        plan_code, _ = bt.bt_plan(op, M, N, K)
+        codes = [plan_code] + [c for c in (2, 1, 0) if c != plan_code]
+        per_code, rec = {}, None
+        for code in codes:
+            if code != 0 and K > 16384:
+                continue
+            su = ForwardSetup(bt, wl, code, bt.BT_ALGO_AUTO, dev)
+            n = steps if code != 0 else max(3, steps // 4)         # the popcount path is the slow one
+            for i in range(warm):
+                su.step(i)
+            torch.cuda.synchronize()
+            graph, _ = su.capture(n, not args.no_graph)
+            ms = su.run_steps(graph, n) / n
+            pack_ms, gemm_ms = su.split(n)
+            del graph
+            per_code[ALGO_NAME[code]] = round(ms * 1e3, 2)
+            if code == plan_code:
+                an = ALGO_NAME[code]
+                rec = {"M": M, "N": N, "K": K, "x_dtype": wl.x_dtype, "out_dtype": wl.out_dtype, "code": an,
+                       "step_us": round(ms * 1e3, 2), "pack_us": round(pack_ms * 1e3, 2),
+                       "contraction_us": round(gemm_ms * 1e3, 2), "gops": round(ops / (ms / 1e3) / 1e9, 1),
+                       "step_roofline": roofline_of(ops, step_bytes(wl), ms, an, peaks, sms),
+                       "contraction_roofline": roofline_of(ops, contraction_bytes(wl, code, bt), gemm_ms, an, peaks,
+                                                           sms),
+                       "steps": n}
+            del su
+            torch.cuda.empty_cache()
+        if bt.bt_device_status() != 0:
+            raise RuntimeError(f"device status after {name}")
+        rec["step_us_per_code"] = per_code
+        rec["fastest_code"] = min(per_code, key=per_code.get)
+        rec["planner_picks_fastest"] = rec["fastest_code"] == rec["code"]
+        out[wl.name] = rec
+    return {"peak_source": peak_src, "how": "graph-replayed steps per code (planner's code for the rooflines); "
+            "step roofline on x + 1-bit W + out bytes, contraction roofline on packed activations + packed W + out",
+            "configs": out}
+
+
 def run_ours(args, rank, world):
     import xnor_popcount_gemm_gb300 as bt
 
@@ -227,132 +468,29 @@ def run_ours(args, rank, world):
     if args.algo == "auto":
         code, algo = bt.bt_plan(op, M, N, K)
     else:
-        code = {"popc": bt.BT_CODE_BITS, "e4m3": bt.BT_CODE_E4M3, "e2m1": bt.BT_CODE_E2M1}[args.algo]
+        code = CODE_OF[args.algo]
         algo = bt.BT_ALGO_AUTO
     algo_name = ALGO_NAME[code]
-    out_t = {"f32": torch.float32, "bf16": torch.bfloat16}[wl.out_dtype]
-    stream = torch.cuda.current_stream()
-
-    # weights: packed once, outside timing
-    if wl.kind == "linear":
-        wp = bt.bt_pack_sign(wl.w.to(dev), code)
-    else:
-        wp = bt.bt_pack_sign(wl.w.to(dev), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
-    bias = None if wl.bias is None else wl.bias.to(dev)
-
-    # rotate over enough input/output buffers that one pass exceeds L2
-    x_bytes = wl.x.numel() * wl.x.element_size()
-    out_elems = M * N
-    out_bytes = out_elems * torch.tensor([], dtype=out_t).element_size()
-    nbuf = max(1, -(-2 * L2_BYTES // (x_bytes + out_bytes)))
-    xs = [wl.x.to(dev) for _ in range(nbuf)]
-    if wl.kind == "linear":
-        outs = [torch.empty((M, N), dtype=out_t, device=dev) for _ in range(nbuf)]
-        ws = torch.empty(bt.bt_binary_linear_workspace(M, K, bt.BT_BF16, code), dtype=torch.uint8, device=dev)
-        xp_shape = (M, bt.bt_packed_row_bytes(K, code))
-    else:
-        B, C, H, W = wl.x.shape
-        k = wl.w.shape[2]
-        Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
-        Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
-        outs = [torch.empty((B, N, Ho, Wo), dtype=out_t, device=dev) for _ in range(nbuf)]
-        geom = (B, C, H, W, k, wl.stride, wl.padding, wl.dilation)
-        ws = torch.empty(bt.bt_binary_conv2d_workspace(*geom, bt.BT_BF16, code), dtype=torch.uint8, device=dev)
-        # the two public calls that split the library's own path for this shape
-        single_pass = bt.bt_conv2d_single_pass(*geom, {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16,
-                                                       torch.float16: bt.BT_F16}[wl.x.dtype], code)
-        if not single_pass:
-            # packed NHWC pixels; the contraction call unfolds them (tensor cores) or
-            # contracts them in place (popcount)
-            xp_shape = (B, H, W, bt.bt_packed_row_bytes(C, code))
-            ws_rows_bytes = bt.bt_binary_conv2d_workspace(*geom, bt.BT_PACKED, code)
-            ws_rows = torch.empty(ws_rows_bytes, dtype=torch.uint8, device=dev) if ws_rows_bytes else None
-        else:
-            # im2col rows of packed codes (one pass from x), contracted with the weights
-            xp_shape = (B * Ho * Wo, k * k * bt.bt_packed_row_bytes(C, code))
-    xp = torch.empty(xp_shape, dtype=torch.uint8, device=dev)
-
-    # kernels per step: the pack, then the contraction; a tensor-core convolution
-    # that packs NHWC pixels unfolds them in one more kernel
-    launches_per_step = 3 if (wl.kind == "conv" and code != bt.BT_CODE_BITS and not single_pass) else 2
-
-    def step(i, ev=None):
-        x, out = xs[i % nbuf], outs[i % nbuf]
-        # pack (a1/a3) then contraction + epilogue (a5/a6 + a7): two public calls
-        if ev is not None:
-            ev[0].record(stream)
-        if wl.kind == "linear":
-            bt.bt_pack_sign(x, code, bt.BT_LAYOUT_ROWS, bias, out=xp)
-        elif not single_pass:
-            bt.bt_pack_sign(x, code, bt.BT_LAYOUT_NCHW_TO_NHWC, bias, out=xp)
-        else:
-            bt.bt_pack_im2col(x, code, k, wl.stride, wl.padding, wl.dilation, bias, out=xp)
-        if ev is not None:
-            ev[1].record(stream)
-        if wl.kind == "linear":
-            bt.bt_binary_linear(xp, wp, code, K, wl.scale_a, wl.scale_w, out=out, out_dtype=out_t,
-                                algo=algo, x_packed=True)
-        elif not single_pass:
-            bt.bt_binary_conv2d(xp, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
-                                wl.scale_w, out=out, out_dtype=out_t, algo=algo, x_packed=True,
-                                workspace=ws_rows)
-        else:
-            bt.bt_binary_conv2d(xp, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a,
-                                wl.scale_w, out=out, out_dtype=out_t, algo=algo, x_im2col_hw=(B, H, W))
-        if ev is not None:
-            ev[2].record(stream)
+    su = ForwardSetup(bt, wl, code, algo, dev)
 
     for i in range(args.warmup):
-        step(i)
+        su.step(i)
     torch.cuda.synchronize()
     assert bt.bt_device_status() == 0
 
     # headline: K steps back to back, nothing between the two calls of a step
     # (so a step's contraction may start as its pack drains, as in a user's
-    # stream); then the same K steps again with events around each kernel for
-    # the split and the roofline (those events serialise the two kernels and
-    # add each launch's latency to its kernel's time)
-    # The K headline steps are captured once into a CUDA graph (the same public
-    # calls, each kernel a node) and replayed, so the host's per-call overhead
-    # does not set the pace of small steps; --no-graph launches them one by one.
-    graph, graph_note = None, "off (--no-graph)"
-    if not args.no_graph:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                for i in range(args.steps):
-                    step(i)
-            graph.replay()
-            torch.cuda.synchronize()
-            graph_note = f"one CUDA graph of the {args.steps} steps, replayed"
-        except RuntimeError as e:                       # capture unsupported: launch eagerly
-            graph, graph_note = None, f"off (capture failed: {str(e).splitlines()[0][:80]})"
-            torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # stream), replayed from one CUDA graph so that the host's per-call overhead
+    # does not set the pace of small steps; then the same K steps again with
+    # events around each call for the split and the roofline
+    graph, graph_note = su.capture(args.steps, not args.no_graph)
     with ClockSampler(dev.index) as clk:
-        barrier(world)
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            for i in range(args.steps):
-                step(i)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        for i in range(args.steps):
-            step(i, evs[i])
-        torch.cuda.synchronize()
+        ms_total = max_over_ranks(su.run_steps(graph, args.steps, world), world)
+        pack_ms, gemm_ms = su.split(args.steps)
     status = bt.bt_device_status()
     if status != 0:
         raise RuntimeError(f"device status {bt.bt_status_string(status)}")
-    ms_total = max_over_ranks(t0.elapsed_time(t1), world)
     ms_step = ms_total / args.steps
-    pack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    gemm_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     value = ops * world * args.steps / (ms_total / 1e3) / 1e9
 
     # end to end through the public API from pinned host buffers: every step
@@ -360,22 +498,16 @@ def run_ours(args, rank, world):
     # are independent batches, so the copies of neighbouring steps overlap the
     # forward (three streams, two device slots); host buffers rotate over more
     # than the host's last-level cache so each copy reads and writes memory.
-    e2e_ms, nh = e2e_pipelined(wl, bt, code, algo, wp, bias, out_t, ws, xs, outs, stream, args, world)
+    e2e_ms, nh = e2e_pipelined(wl, bt, code, algo, su.wp, su.bias, su.out_t, su.ws, su.xs, su.outs,
+                               torch.cuda.current_stream(), args, world)
 
     peaks, peak_src = measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    bound, peak, unit, peak_how = roofline_peak(algo_name, peaks, sms)
-    achieved = ops / (gemm_ms / 1e3) / 1e12
-    # the contraction call's least traffic; below the ridge point (peak ops per
-    # byte of HBM) it is bounded by HBM, not by its pipe
-    call_bytes = contraction_bytes(wl, code, bt, single_pass if wl.kind == "conv" else False)
-    intensity = ops / call_bytes
-    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if intensity < ridge:
-        bound, unit = "hbm", "GB/s"
-        peak, peak_how = peaks["hbm_gbs"], f"measured copy bandwidth; {intensity:.0f} ops/B < ridge {ridge:.0f}"
-        achieved = call_bytes / (gemm_ms / 1e3) / 1e9
-    traffic = load_traffic(wl.name, algo_name)
+    roof = roofline_of(ops, contraction_bytes(wl, code, bt), gemm_ms, algo_name, peaks, sms)
+    roof.update({"traffic": load_traffic(wl.name, algo_name),
+                 "traffic_unit": "DRAM bytes per tc_kernel launch (ncu, this kernel source)",
+                 "peak_source": f"{peak_src}: {roof.pop('peak_how')}", "kernel": "contraction"})
+    pack_b = pack_bytes(wl, code, bt)
     line = {
         "metric": "binary GOPS (2*M*N*K/s)",
         "value": round(value, 1),
@@ -392,49 +524,31 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded; shapes of binarized LLM linear and ResNet conv layers)",
         "config": {"workload": wl.name, "M": M, "N": N, "K": K, "x_dtype": wl.x_dtype,
                    "out_dtype": wl.out_dtype, "code": algo_name, "weights": "pre-packed outside timing",
-                   "l2": f"inputs+outputs rotate over {nbuf} buffers ({nbuf * (x_bytes + out_bytes) / 1e6:.0f} MB > L2)",
+                   "l2": f"inputs+outputs rotate over {su.nbuf} buffers "
+                         f"({su.nbuf * (su.x_bytes + su.out_bytes) / 1e6:.0f} MB > L2)",
                    "parallelism": f"replicas x{world}", "launch": graph_note},
         "kernel_ms": {"pack": round(pack_ms, 5), "contraction": round(gemm_ms, 5),
-                      "how": "second pass of the same steps, CUDA events around each kernel on its stream"},
-        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": int(call_bytes), "ops_per_byte": round(intensity, 1),
-                     "traffic_unit": "DRAM bytes per tc_kernel launch (ncu, this kernel source)",
-                     "peak_source": f"{peak_src}: {peak_how}",
-                     "kernel": "contraction"},
-        "pack_roofline": {"bound": "hbm", "achieved": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9, 1),
+                      "how": "second pass of the same steps, CUDA events around each call on its stream"},
+        "roofline": roof,
+        "step_roofline": roofline_of(ops, step_bytes(wl), ms_step, algo_name, peaks, sms),
+        "pack_roofline": {"bound": "hbm", "achieved": round(pack_b / (pack_ms / 1e3) / 1e9, 1),
                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": round(pack_bytes(wl, code, bt) / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+                          "frac": round(pack_b / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
         "e2e": {"value": round(ops * world / (e2e_ms / 1e3) / 1e9, 1), "unit": "GOPS",
-                "h2d_bytes_per_step": int(x_bytes), "d2h_bytes_per_step": int(out_bytes),
+                "h2d_bytes_per_step": int(su.x_bytes), "d2h_bytes_per_step": int(su.out_bytes),
                 "ms_per_step": round(e2e_ms, 4),
                 "how": f"pinned host buffers (x{nh} rotating); copy-in, forward, copy-out on three streams, "
                        "neighbouring steps overlapped"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": su.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    del graph, su
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_configs:
+        line["all_configs"] = sweep_configs(bt, dev, peaks, peak_src, sms, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     return line
-
-
-def contraction_bytes(wl, code, bt, single_pass: bool) -> float:
-    """Least bytes the contraction call moves: its packed activations (packed
-    rows of a linear layer; im2col rows when the convolution was unfolded in
-    one pass; packed NHWC pixels otherwise), the packed weights, the output."""
-    out_b = 4 if wl.out_dtype == "f32" else 2
-    if wl.kind == "linear":
-        M, K = wl.x.shape
-        N = wl.w.shape[0]
-        rb = bt.bt_packed_row_bytes(K, code)
-        return (M + N) * rb + M * N * out_b
-    B, C, H, W = wl.x.shape
-    O, k = wl.w.shape[0], wl.w.shape[2]
-    Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
-    Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
-    rbc = bt.bt_packed_row_bytes(C, code)
-    x_b = B * Ho * Wo * k * k * rbc if single_pass else B * H * W * rbc
-    return x_b + O * k * k * rbc + B * O * Ho * Wo * out_b
 
 
 HOST_LLC_BYTES = 256 << 20     # rotate host buffers over more than this
