@@ -50,7 +50,7 @@ def test_packed_row_bytes_rejects_bad_input():
     assert bt.bt_packed_row_bytes(5, 7) == -1
 
 
-def test_workspace_queries():
+def test_workspace_queries(monkeypatch):
     assert bt.bt_binary_linear_workspace(4096, 4096, bt.BT_BF16, bt.BT_CODE_BITS) == 4096 * 512
     assert bt.bt_binary_linear_workspace(3, 33, bt.BT_F32, bt.BT_CODE_BITS) == 256
     assert bt.bt_binary_linear_workspace(10, 10, bt.BT_PACKED, bt.BT_CODE_BITS) == 0
@@ -59,7 +59,22 @@ def test_workspace_queries():
     assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_BITS) == 2 * 14 * 14 * 32
     assert ws(1, 1, 1, 1, 1, 1, 0, 1, bt.BT_F32, bt.BT_CODE_BITS) == 256
     assert ws(1, 1, 1, 1, 1, 1, 0, 1, bt.BT_PACKED, bt.BT_CODE_BITS) == 0
-    # E2M1: packed pixels, then the im2col rows [B*Ho*Wo, k*k*row_bytes(C)]
+    # E2M1 / E4M3 with the implicit-im2col contraction: the packed pixels only,
+    # nothing for packed input
+    assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 2 * 14 * 14 * 128
+    assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_PACKED, bt.BT_CODE_E2M1) == 0
+    assert ws(2, 128, 28, 28, 3, 2, 1, 1, bt.BT_BF16, bt.BT_CODE_E2M1) == 2 * 28 * 28 * 64
+    assert ws(1, 3, 5, 5, 3, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E4M3) == 1792
+    # rows wider than one tile (Wo = 298 > 240 columns): packed pixels, then
+    # the im2col rows [B*Ho*Wo, k*k*row_bytes(C)] of the explicit unfold
+    # (each part rounded up to 256 bytes: 298 x 9 x 64 = 171648 -> 171776)
+    assert ws(1, 16, 3, 300, 3, 1, 0, 1, bt.BT_BF16, bt.BT_CODE_E2M1) == 3 * 300 * 64 + 171776
+    # invalid geometry or arguments
+    assert ws(1, 8, 4, 4, 0, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
+    assert ws(1, 8, 4, 4, 3, 0, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
+    assert ws(1, 8, 4, 4, 3, 1, 0, 1, bt.BT_F32, 7) == 0
+    # the explicit unfold (BT_CONV_IMPLICIT=0): pixels, then the rows
+    monkeypatch.setenv("BT_CONV_IMPLICIT", "0")
     assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) == \
         2 * 14 * 14 * 128 + 2 * 14 * 14 * 9 * 128
     assert ws(2, 256, 14, 14, 3, 1, 1, 1, bt.BT_PACKED, bt.BT_CODE_E2M1) == 2 * 14 * 14 * 9 * 128
@@ -69,10 +84,6 @@ def test_workspace_queries():
     # E4M3: one byte per channel; each part rounded up to 256 bytes
     # (25 pixels x 64 B = 1600 -> 1792; 3 x 3 outputs x 9 taps x 64 B = 5184 -> 5376)
     assert ws(1, 3, 5, 5, 3, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E4M3) == 1792 + 5376
-    # invalid geometry or arguments
-    assert ws(1, 8, 4, 4, 0, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
-    assert ws(1, 8, 4, 4, 3, 0, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
-    assert ws(1, 8, 4, 4, 3, 1, 0, 1, bt.BT_F32, 7) == 0
 
 
 # Host validation. Pointers below are never dereferenced: every call fails
@@ -122,7 +133,7 @@ def conv(**kw):
     return C(*a.values())
 
 
-def test_conv_validation():
+def test_conv_validation(monkeypatch):
     assert conv(k=0) == bt.BT_ERR_INVALID_ARG
     assert conv(s=0) == bt.BT_ERR_INVALID_ARG
     assert conv(p=-1) == bt.BT_ERR_INVALID_ARG
@@ -133,7 +144,9 @@ def test_conv_validation():
     assert conv(sa=0.0) == bt.BT_ERR_INVALID_ARG
     assert conv(x=264 + 1) == bt.BT_ERR_ALIGNMENT
     assert conv(ws=None) == bt.BT_ERR_WORKSPACE
-    # the tensor-core codes need the im2col rows even for packed pixels
+    # with the explicit unfold (BT_CONV_IMPLICIT=0) the tensor-core codes need
+    # the im2col rows even for packed pixels
+    monkeypatch.setenv("BT_CONV_IMPLICIT", "0")
     assert conv(xt=bt.BT_PACKED, code=bt.BT_CODE_E2M1, ws=None) == bt.BT_ERR_WORKSPACE
     assert conv(xt=bt.BT_PACKED, code=bt.BT_CODE_E4M3, ws=4096, wsb=1024) == bt.BT_ERR_WORKSPACE
     assert conv(xt=bt.BT_PACKED, code=bt.BT_CODE_E2M1, ws=4096 + 16, wsb=1 << 20) == bt.BT_ERR_ALIGNMENT
@@ -299,3 +312,8 @@ def test_w8a8_abi_validation():
     assert call(k=9, H=20, W=20) == bt.BT_ERR_UNSUPPORTED
     assert call(B=0) == bt.BT_OK
     assert call(x=None) == bt.BT_ERR_INVALID_ARG
+
+
+def test_wait_timeout_setter_validates():
+    assert bt._c_wait(61 * 10**9) == bt.BT_ERR_INVALID_ARG
+    assert bt._c_wait(0) == bt.BT_OK          # the default (2 s)

@@ -314,16 +314,20 @@ def test_conv_f32_scalar_bias(code):
     assert_close_rel(got, oracle.binary_conv2d(x, w, 0.5, 2.0, 1, 1, 1, bias, "f32"))
 
 
+@pytest.mark.parametrize("implicit", ["1", "0"])
 @pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
-def test_conv_prepacked_input(code):
-    # packed NHWC pixels in, through a caller workspace sized by the query
+def test_conv_prepacked_input(code, implicit, monkeypatch):
+    # packed NHWC pixels in, through a caller workspace sized by the query:
+    # none for the popcount path and the implicit-im2col contraction, the
+    # im2col rows for the explicit unfold (BT_CONV_IMPLICIT=0)
+    monkeypatch.setenv("BT_CONV_IMPLICIT", implicit)
     B, C, H, W, O, k, s, p, d = 2, 96, 9, 11, 50, 3, 2, 1, 1
     x = _gen(11, (B, C, H, W), torch.bfloat16)
     w = _gen(12, (O, C, k, k), torch.bfloat16)
     xp = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
     wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
     nbytes = bt.bt_binary_conv2d_workspace(B, C, H, W, k, s, p, d, bt.BT_PACKED, code)
-    assert (nbytes == 0) == (code == bt.BT_CODE_BITS)
+    assert (nbytes == 0) == (code == bt.BT_CODE_BITS or implicit == "1")
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=DEV) if nbytes else None
     got = bt.bt_binary_conv2d(xp, wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32, x_packed=True,
                               workspace=ws).cpu()

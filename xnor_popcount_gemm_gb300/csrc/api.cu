@@ -1,5 +1,6 @@
 // The C ABI of libbt (declared in include/bt.h): argument validation, the
 // pack -> contract dispatch, the "ADAPTIVE" planner and the device error word.
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -23,6 +24,12 @@ int device_sm_count() {
     }
     return n[dev];
 }
+
+namespace {
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitNs};
+}  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 bool current_context_id(unsigned long long *id) {
     static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
@@ -215,11 +222,14 @@ size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, in
     if (approx > 4.0e18) return 0;
     size_t n = 0;
     if (x_dtype != BT_PACKED) n += round_up(static_cast<size_t>(B * H * W * rbc), 256);   // packed NHWC pixels
-    if (code != BT_CODE_BITS) {                                                            // im2col rows
+    if (code != BT_CODE_BITS) {
         ConvGeom g{B, C, H, W, 0, 0, 0, kernel_size, stride, padding, dilation};
         g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
         g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
-        n += round_up(static_cast<size_t>(im2col_bytes(g, rbc)), 256);
+        // the implicit-im2col contraction reads the packed pixels as they are;
+        // otherwise the im2col rows follow them
+        if (g.Ho >= 1 && g.Wo >= 1 && !conv_implicit_applies(g, code))
+            n += round_up(static_cast<size_t>(im2col_bytes(g, rbc)), 256);
     }
     return n;
 }
@@ -262,7 +272,8 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype,
                                                    w_code);
-    const bool needs_ws = float_in(x_dtype) || (x_dtype == BT_PACKED && run != BT_ALGO_POPC);
+    const bool implicit = run != BT_ALGO_POPC && x_dtype != BT_PACKED_IM2COL && conv_implicit_applies(g, w_code);
+    const bool needs_ws = float_in(x_dtype) || (x_dtype == BT_PACKED && run != BT_ALGO_POPC && !implicit);
     if (needs_ws && need == 0) return BT_ERR_UNSUPPORTED;      // beyond the sizes the query serves
     if (needs_ws && (workspace == nullptr || workspace_bytes < need)) return BT_ERR_WORKSPACE;
     if (needs_ws && !aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
@@ -274,6 +285,21 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
     if (x_dtype == BT_PACKED_IM2COL)
         return from_cuda(launch_tc_conv(static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(weight), w_code,
                                         g, alpha, out, out_dtype, err, s, scales));
+    if (implicit) {
+        // pack to channel-packed NHWC pixels (unless given), then the
+        // implicit-im2col contraction reads them in place
+        const void *xp = x;
+        if (x_dtype != BT_PACKED) {
+            if (launch_pack_nhwc(x, x_dtype, B, C, H * W, bias_a, bias_len, w_code, ws, s) != cudaSuccess)
+                return BT_ERR_CUDA;
+            xp = ws;
+        }
+        const cudaError_t e = launch_tc_conv_implicit(static_cast<const uint8_t *>(xp),
+                                                      static_cast<const uint8_t *>(weight), w_code, g, alpha, out,
+                                                      out_dtype, err, s, scales);
+        if (e == cudaErrorNotSupported) return BT_ERR_UNSUPPORTED;
+        return from_cuda(e);
+    }
     uint8_t *rows = ws + (x_dtype == BT_PACKED ? 0 : round_up(static_cast<size_t>(B * H * W * rbc), 256));
     if (run != BT_ALGO_POPC && x_dtype != BT_PACKED) {
         // one pass from x to the im2col rows, where the staged unfold applies
@@ -329,6 +355,7 @@ int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel
     g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
     g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
     if (g.Ho < 1 || g.Wo < 1) return 0;
+    if (conv_implicit_applies(g, code)) return 0;      // packed pixels, contracted in place
     return unfold_single_pass(g, x_dtype, code) ? 1 : 0;
 }
 
@@ -367,6 +394,12 @@ bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_a
     else c = (K <= kTcMaxK && tc_available()) ? BT_CODE_E2M1 : BT_CODE_BITS;
     *code = c;
     *algo = algo_for_code(c);
+    return BT_OK;
+}
+
+bt_status bt_set_wait_timeout(uint64_t ns) {
+    if (ns > 60ull * 1000000000ull) return BT_ERR_INVALID_ARG;
+    g_wait_limit_ns.store(ns == 0 ? kWaitNs : ns, std::memory_order_relaxed);
     return BT_OK;
 }
 

@@ -41,6 +41,10 @@ int device_sm_count();
 // thread's current CUDA context. Returns nullptr on a CUDA error.
 unsigned int *device_error_word();
 
+// Limit of the tensor-core kernels' bounded waits, in ns (bt_set_wait_timeout;
+// 2 s unless set).
+unsigned long long wait_limit_ns();
+
 // Unique id of the calling thread's current CUDA context (cuCtxGetId, never
 // reused within the process). False when no context is current or the driver
 // lacks the query.
@@ -184,6 +188,17 @@ cudaError_t launch_pack_im2col(const void *x, bt_dtype xt, const ConvGeom &g, co
 // Whether the convolution builds its im2col rows in one pass from x (for a
 // 16-byte aligned x of type xt): the staged plan exists and pays.
 bool unfold_single_pass(const ConvGeom &g, bt_dtype xt, bt_code code);
+
+// Implicit-im2col tensor-core convolution straight from channel-packed NHWC
+// pixels xp [B, H, W, row_bytes(C)] (codes E4M3 / E2M1), NCHW output. Whether
+// its plan applies to a geometry does not depend on O (g.O is ignored);
+// BT_CONV_IMPLICIT=0 in the environment turns it off (the explicit unfold
+// then runs). The launch returns cudaErrorNotSupported where the plan does
+// not apply.
+bool conv_implicit_applies(const ConvGeom &g, bt_code code);
+cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
+                                    void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s,
+                                    const float *scales = nullptr);
 
 // Launch attribute list allowing programmatic dependent launch (the kernel
 // overlaps its prologue with the previous kernel in the stream).
