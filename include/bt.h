@@ -475,6 +475,20 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
  */
 bt_status bt_device_status(bt_stream stream);
 
+/*
+ * bt_set_wait_timeout -- how long each bounded wait in the main loops of the
+ * tensor-core contraction kernels (producer, MMA issuer, epilogue) waits
+ * before giving up, in nanoseconds, for launches made after the call; 0
+ * restores the default of 2 s. Process-wide. The pages have no counterpart:
+ * it exists so that the timeout path can be exercised without breaking
+ * anything -- a limit shorter than a copy's or an MMA's latency makes the
+ * first real wait give up: the kernel records BT_ERR_TIMEOUT (read by
+ * bt_device_status), lets its copies and MMAs in flight finish (those drains
+ * always allow 2 s), frees its tensor memory and returns, and its output is
+ * incomplete. Errors: INVALID_ARG for a limit above 60 s.
+ */
+bt_status bt_set_wait_timeout(uint64_t ns);
+
 #ifdef __cplusplus
 }
 #endif

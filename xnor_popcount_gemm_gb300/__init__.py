@@ -23,7 +23,7 @@ __all__ = [
     "BT_OP_CONV2D", "bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
     "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
-    "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
+    "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_set_wait_timeout",
 ]
 
 BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_ALIGNMENT = 0, -1, -2, -3
@@ -85,6 +85,7 @@ _c_w8 = _sig("bt_w8a8_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64
                                     _sz, _p])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
 _c_status = _sig("bt_device_status", _i, [_p])
+_c_wait = _sig("bt_set_wait_timeout", _i, [ctypes.c_uint64])
 
 #: every symbol include/bt.h declares
 EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
@@ -94,7 +95,7 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
             "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_binary_conv2d_backward",
             "bt_scale_init", "bt_binary_linear_dscale", "bt_binary_conv2d_dscale", "bt_w8a8_conv2d_workspace",
-            "bt_w8a8_conv2d"]
+            "bt_w8a8_conv2d", "bt_set_wait_timeout"]
 
 
 class BtError(RuntimeError):
@@ -455,6 +456,12 @@ def bt_plan(op: int, M: int, N: int, K: int) -> tuple[int, int]:
     code, algo = _i(0), _i(0)
     _check(_c_plan(op, M, N, K, ctypes.byref(code), ctypes.byref(algo)))
     return code.value, algo.value
+
+
+def bt_set_wait_timeout(ns: int) -> None:
+    """Limit (ns) of the tensor-core kernels' bounded waits for later launches;
+    0 restores the default (2 s)."""
+    _check(_c_wait(ns))
 
 
 def bt_device_status(stream=None) -> int:

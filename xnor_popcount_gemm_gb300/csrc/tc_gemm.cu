@@ -48,8 +48,10 @@
 //                   row segments leave in 16-byte stores (or, for NCHW, runs
 //                   of pixels in the widest aligned stores). Once both CTAs'
 //                   warps have drained it, the buffer goes back to the MMA warp.
-// Every wait is bounded (kWaitNs): a wait that runs out records BT_ERR_TIMEOUT
-// in the device error word and the kernel winds down without trapping.
+// Every wait is bounded (bt_set_wait_timeout, 2 s by default; the teardown's
+// drains of copies and MMAs in flight always 2 s): a wait that runs out
+// records BT_ERR_TIMEOUT in the device error word and the kernel winds down
+// without trapping.
 #include <cudaTypedefs.h>
 
 #include <cstdio>
@@ -96,6 +98,7 @@ struct TcArgs {
     const float *scales;       // not null: alpha = fp32(scales[0] * scales[1]), read by the epilogue
     void *out;
     unsigned int *err;
+    unsigned long long wait_ns;  // limit of each bounded wait of the main loops (teardown drains: kWaitNs)
     int vec;                   // rows: 1 when output rows are 16-byte aligned (16-byte stores)
                                // NCHW: bytes each lane stores at once (a run of one channel's pixels)
     int64_t hw;                // NCHW: output pixels per image (Ho * Wo)
@@ -391,7 +394,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                 const int am0 = mt * kTileRows + a_first;
                 const int bn0 = nt * bn + b_first;
                 for (int kb = 0; kb < a.nk; ++kb) {
-                    if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err)) { ok = false; break; }
+                    if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                     const uint32_t adst = sA + s * kAStage, bdst = sB + s * kBStage;
                     const uint32_t fbar = PAIR ? tc::mapa(full(s), 0u) : full(s);
                     const int k0 = sp * a.slices + kb * D;
@@ -448,13 +451,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                 const int buf = local & 1;
                 if (local >= 2) {
                     // the epilogue (of both CTAs of a pair) has drained this buffer
-                    if (!tc::wait_bounded(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err))
+                    if (!tc::wait_bounded(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err, a.wait_ns))
                         break;
                     tc::fence_after_sync();
                 }
                 const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * acc_stride<CODE>();
                 for (int kb = 0; kb < a.nk; ++kb) {
-                    if (!tc::wait_bounded(full(s), ph, abort_flag, a.err)) { ok = false; break; }
+                    if (!tc::wait_bounded(full(s), ph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                     tc::fence_after_sync();
                     const int cnt = slice_count(kb);
                     for (int i = 0; i < cnt; ++i) {
@@ -506,7 +509,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
             const int64_t m0 = static_cast<int64_t>(mt) * kTileRows + (PAIR ? static_cast<int64_t>(crank) * kBM : 0);
             const int n0 = nt * bn;
             const int buf = local & 1;
-            if (!tc::wait_bounded(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err)) break;
+            if (!tc::wait_bounded(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err, a.wait_ns)) break;
             tc::fence_after_sync();
             bool released = false;
             auto release = [&]() {
@@ -771,6 +774,7 @@ template <int CODE, int LAYOUT, int OUT, bool PAIR>
 cudaError_t launch_t(const Maps &mp, TcArgs a, cudaStream_t s) {
     auto kern = tc_kernel<CODE, LAYOUT, OUT, PAIR>;
     a.stages = num_stages(a.bn, PAIR, a.d);
+    a.wait_ns = wait_limit_ns();
     const int smem = smem_bytes(a.bn, PAIR, a.d);
     if (a.stages < 2 || smem > kSmemMax) return cudaErrorInvalidValue;
     static std::once_flag once;

@@ -42,18 +42,49 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete. Gives up after
-// kWaitNs (or as soon as another thread has given up): records kErrTimeout
-// in the device error word, raises the CTA's abort flag and returns false.
+// limit_ns of %globaltimer time (or as soon as another thread has given up):
+// records kErrTimeout in the device error word, raises the CTA's abort flag
+// and returns false. At the default limit it waits with try_wait (which may
+// suspend the thread in hardware for a while) and reads the clock every 64
+// tries; a shorter limit polls with test_wait and reads the clock after every
+// try, so that a wait longer than the limit always gives up.
 static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                          unsigned int *err) {
+                                          unsigned int *err, unsigned long long limit_ns = kWaitNs) {
+    if (limit_ns < kWaitNs) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_test_wait(bar, parity)) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                atomicOr(err, kErrTimeout);
+                *abort_flag = 1u;
+                return false;
+            }
+        }
+        return true;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 63u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 atomicOr(err, kErrTimeout);
                 *abort_flag = 1u;
                 return false;
