@@ -10,6 +10,8 @@
 //          planes x one 16-byte run of pixels and writes each pixel's group.
 // Both are HBM streams: the input is read once and written 1/32 (bits),
 // 1/8 (E2M1) or 1/4 (E4M3) of its fp32 size.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "bt_device.cuh"
@@ -510,6 +512,132 @@ __device__ __forceinline__ uint64_t transpose8x8(uint64_t v) {
     return v ^ t ^ (t << 28);
 }
 
+// nhwc, warp-level. A unit is (image b, 32 consecutive pixels, 32 channels)
+// and belongs to one warp: lane l loads the 32 pixels of channel 32g + l
+// (16-byte loads along its channel plane) and keeps their signs as one 32-bit
+// word (bit p = pixel p binarizes to +1); a 32 x 32 bit-matrix transpose
+// across the warp (five rounds of shuffles, each swapping the off-diagonal
+// blocks of half the size between lanes l and l ^ s) leaves lane p with the
+// word of pixel p over the 32 channels, which it turns into codes and stores
+// (4 bytes of bits, 16 of E2M1, 32 of E4M3) at its place in the pixel's
+// packed row. No shared memory, no block barrier; consecutive warps take the
+// channel groups of the same pixels, so each pixel row is completed by
+// neighbouring warps. Channels past C are code 0 (the row's zero padding).
+// A lane's four 16-byte loads of its channel's 32 pixels go through the
+// L1-allocating read-only path, so that they share their 32-byte sectors.
+// Needs every channel plane 16-byte aligned and HW a multiple of 4 (f32) or
+// 8 (2-byte types); pixels past HW are neither loaded nor stored.
+template <int CODE> struct Group32;
+template <> struct Group32<BT_CODE_BITS> { static constexpr int kBytes = 4; };
+template <> struct Group32<BT_CODE_E2M1> { static constexpr int kBytes = 16; };
+template <> struct Group32<BT_CODE_E4M3> { static constexpr int kBytes = 32; };
+
+// Transpose of the 32 x 32 bit matrix whose row l is lane l's word: after it,
+// bit j of lane p's word is bit p of lane j's word before.
+__device__ __forceinline__ uint32_t transpose32_warp(uint32_t w, int lane) {
+    const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const int sft = 16 >> i;
+        const uint32_t m = masks[i];
+        const uint32_t t = __shfl_xor_sync(0xFFFFFFFFu, w, sft);
+        w = (lane & sft) ? ((w & ~m) | ((t >> sft) & m)) : ((w & m) | ((t & m) << sft));
+    }
+    return w;
+}
+
+template <typename T, int CODE>
+__global__ void __launch_bounds__(kPackThreads)
+pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, int npb, int ncg, int64_t units,
+                      const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out, int rb) {
+    constexpr int OB = Group32<CODE>::kBytes;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    pdl_launch_dependents();
+    pdl_wait();
+    const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
+    for (int64_t u = warp0; u < units; u += nwarps) {
+        const int cg = static_cast<int>(u % ncg);
+        const int64_t rest = u / ncg;
+        const int pb = static_cast<int>(rest % npb);
+        const int64_t b = rest / npb;
+        const int p0 = pb * 32;
+        const int c = cg * 32 + lane;
+        uint32_t pos = 0;                                 // bit p: pixel p0 + p binarizes to +1
+        if (c < C) {
+            const float bc = bias_len > 1 ? __ldg(bias + c) : bs;
+            const T *src = x + (b * C + c) * static_cast<int64_t>(HW) + p0;
+            const int npx = HW - p0 < 32 ? HW - p0 : 32;
+            Group<T> g[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (8 * k + 8 <= npx) {
+#pragma unroll
+                    for (int i = 0; i < Group<T>::kWords / 4; ++i) {
+                        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src + 8 * k) + i);
+                        g[k].w[4 * i] = q.x; g[k].w[4 * i + 1] = q.y; g[k].w[4 * i + 2] = q.z; g[k].w[4 * i + 3] = q.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < Group<T>::kWords; ++i) g[k].w[i] = 0u;
+                    if constexpr (sizeof(T) == 4) {               // HW a multiple of 4: half a group
+                        if (8 * k + 4 <= npx) {
+                            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src + 8 * k));
+                            g[k].w[0] = q.x; g[k].w[1] = q.y; g[k].w[2] = q.z; g[k].w[3] = q.w;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t P0, P1;
+                if (isfinite(bc)) {
+                    masks_ge<T>(g[k], -bc, P0, P1);
+                } else {
+                    float f[8], bb[8];
+                    g[k].unpack(f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) bb[e] = bc;
+                    masks_add(f, bb, P0, P1);
+                }
+                pos |= mask_byte(P0, P1) << (8 * k);
+            }
+        }
+        // lane p: bit j = channel 32 cg + j at pixel p0 + p
+        const uint32_t w = transpose32_warp(pos, lane);
+        if (p0 + lane >= HW) continue;
+        const int nvalid = C - cg * 32 >= 32 ? 32 : (C - cg * 32 > 0 ? C - cg * 32 : 0);
+        const uint32_t valid = nvalid == 32 ? 0xFFFFFFFFu : (1u << nvalid) - 1u;
+        uint8_t *dst = out + (b * HW + p0 + lane) * static_cast<int64_t>(rb) + cg * OB;
+        const uint32_t neg = ~w & valid;
+        if constexpr (CODE == BT_CODE_BITS) {
+            *reinterpret_cast<uint32_t *>(dst) = w & valid;
+        } else if constexpr (CODE == BT_CODE_E2M1) {
+            uint32_t q[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t nb = (neg >> (8 * i)) & 0xFFu, vb = (valid >> (8 * i)) & 0xFFu;
+                q[i] = 0x22222222u | (spread_nibbles(nb) << 3);
+                if (vb != 0xFFu) q[i] &= spread_nibbles(vb) * 0xFu;
+            }
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
+        } else {
+            uint32_t q[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t nb = (neg >> (8 * i)) & 0xFFu, vb = (valid >> (8 * i)) & 0xFFu;
+                uint64_t v = 0x3838383838383838ull | (spread_bytes(nb) << 7);
+                if (vb != 0xFFu) v &= spread_bytes(vb) * 0xFFull;
+                q[2 * i] = static_cast<uint32_t>(v);
+                q[2 * i + 1] = static_cast<uint32_t>(v >> 32);
+            }
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
+            *reinterpret_cast<uint4 *>(dst + 16) = make_uint4(q[4], q[5], q[6], q[7]);
+        }
+    }
+}
+
 // nhwc, transposed through shared memory. A unit is (image b, a run of
 // kNhwcPixels pixels, every channel). Phase 1 reads each channel plane's run
 // with 16-byte loads (consecutive threads, consecutive 8-pixel groups of a
@@ -875,6 +1003,16 @@ pack_im2col_direct_kernel(const T *__restrict__ x, int C, int H, int W, int Ho, 
     }
 }
 
+// The shared-memory transpose kernel is the default for channel-packed
+// pixels; BT_PACK_NHWC=warp selects the warp-level one (both stay under
+// test). Inside a convolution step the shared-memory kernel measured faster
+// on GB300: the warp-level kernel's loads of 16 bytes from 32 channel planes
+// per instruction pulled about 1.8 times the input through L2.
+bool nhwc_warp_disabled() {
+    const char *env = std::getenv("BT_PACK_NHWC");
+    return env == nullptr || std::strcmp(env, "warp") != 0;
+}
+
 int grid_for(int64_t threads) {
     int64_t blocks = (threads + kPackThreads - 1) / kPackThreads;
     const int64_t cap = int64_t(1) << 30;
@@ -957,6 +1095,20 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
                    uint8_t *out, int64_t rb, cudaStream_t s) {
     constexpr int E = Elem<T>::kPerVec;
     const bool vec = ((HW * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned(x, 16);
+    if (vec && HW < (int64_t(1) << 30) && C < (int64_t(1) << 30) && !nhwc_warp_disabled()) {
+        // warp-level units of 32 pixels x 32 channels
+        const int64_t npb = (HW + 31) / 32, ncg = rb / Group32<CODE>::kBytes;
+        const int64_t units = B * npb * ncg;
+        const int sms = device_sm_count();
+        const int64_t per_block = kPackThreads / 32;
+        const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * (2048 / kPackThreads);
+        int64_t blocks = (units + per_block - 1) / per_block;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        return launch_pdl(pack_nhwc_warp_kernel<T, CODE>, dim3(static_cast<unsigned>(blocks)), dim3(kPackThreads), s, x,
+                          static_cast<int>(C), static_cast<int>(HW), static_cast<int>(npb), static_cast<int>(ncg), units,
+                          bias, static_cast<int>(bias_len), out, static_cast<int>(rb));
+    }
     const int smem = kNhwcGroups * nhwc_cstride(static_cast<int>(C));
     const int64_t upi = (HW + kNhwcPixels - 1) / kNhwcPixels;
     const int64_t G = padded_elems<CODE>(rb) / 8;

@@ -67,8 +67,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 480;                  // E2M1: 32 columns of unit block scales
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;     // UE8M0 127 = 2^0 in every byte
 constexpr int kSmemMax = 232448;                  // 227 KB opt-in per CTA
-constexpr int kBoxBytes = 32 * 32 * 4;            // one epilogue staging box (f32 worst case)
-constexpr int kStagingBytes = kEpiWarps * kBoxBytes;
+// One epilogue staging box per epilogue warp: 32 x 32 outputs (4 KB for
+// 4-byte outputs, 2 KB for 2-byte ones).
+__host__ __device__ constexpr int staging_bytes(int out_elem) { return kEpiWarps * 32 * 32 * out_elem; }
 constexpr int kReserve = 1024 /*alignment*/ + 512 /*barriers*/;
 constexpr int kMaxTaps = 64;
 constexpr int kMaxPhases = 4;
@@ -89,6 +90,7 @@ struct ConvArgs {
     uint32_t stage_bytes;     // nph * nsl * img_bytes
     uint32_t img_tx;          // bytes one image's copy delivers: rv * wv * sw
     int b_stages;             // pixel stages (2, or 1 where two do not fit)
+    int pairs;                // 2-byte outputs read back two pixels per lane (wv, Wo, Ho*Wo even)
     int a_resident;           // 1: every weight slice loaded once, kept for the launch
     int a_d;                  // slices per weight box
     int a_boxes;              // resident: boxes covering all slices
@@ -195,7 +197,41 @@ __device__ __forceinline__ void box_to_planes(uint32_t sbox, int lane, bool vali
     }
 }
 
-template <int CODE, int OUT, int SW>
+// The same for 2-byte outputs, two virtual pixels per lane: lanes 0..15 take
+// the 16 pixel pairs of even rows, lanes 16..31 of odd rows, so each shared
+// load instruction reads two whole 64-byte rows and each store writes 4 bytes
+// per lane. Needs wv, Wo and Ho * Wo even, so that a pair is either two valid
+// pixels of one output row at an even offset or two dropped columns; p is
+// this lane's pair in the plane of channel o0 + (lane >> 4).
+__device__ __forceinline__ void box_to_planes_pairs(uint32_t sbox, int lane, bool valid, uint8_t *p, int64_t plane,
+                                                    int nrows) {
+    const int m = lane & 15, odd = lane >> 4;
+    const uint32_t lane_off = sbox + static_cast<uint32_t>(odd * 64 + (m & 3) * 4);
+    const int q = m >> 2;
+    uint32_t v[16];
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+        const uint32_t addr = lane_off + static_cast<uint32_t>(it * 128) + (static_cast<uint32_t>(q ^ (it & 3)) << 4);
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[it]) : "r"(addr));
+    }
+    if (!valid) return;
+    const int64_t step = 2 * plane;
+    if (nrows >= 32) {
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+            *reinterpret_cast<uint32_t *>(p) = v[it];
+            p += step;
+        }
+    } else {
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+            if (2 * it + odd < nrows) *reinterpret_cast<uint32_t *>(p) = v[it];
+            p += step;
+        }
+    }
+}
+
+template <int CODE, int OUT, int SW, bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
 conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const ConvArgs a) {
     using T = typename OutT<OUT>::type;
@@ -214,7 +250,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const uint32_t sA = base;
     const uint32_t sB = sA + a_bytes;
     const uint32_t sStage = sB + static_cast<uint32_t>(a.b_stages) * a.stage_bytes;
-    const uint32_t bars = sStage + kStagingBytes;
+    const uint32_t bars = sStage + staging_bytes(kElem);
     // barriers: afull[8], aempty[8], bfull[2], bempty[2], tfull[2], tempty[2], drain
     auto afull = [&](int i) { return bars + 8u * i; };
     auto aempty = [&](int i) { return bars + 8u * (kMaxAStages + i); };
@@ -392,7 +428,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // ---------------- epilogue (warps 2..9) ----------------
         pdl_wait();                                       // the previous kernel may still use `out`
         T *const out = static_cast<T *>(a.out);
-        const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);
+        const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * 32 * 32 * kElem);
         const float alpha = a.scales != nullptr ? alpha_from(a.scales) : a.alpha;
         const int half = (warp - 2) / 4;
         int local = 0;
@@ -426,12 +462,21 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                      : "memory");
                     }
                     __syncwarp();
-                    // read back with lanes along the pixels: lane = virtual pixel
-                    const int v = 32 * bx + lane;
-                    const int i = v / a.wv, j = v - i * a.wv;
-                    const bool valid = v < ncols && j < a.Wo;
-                    uint8_t *p = reinterpret_cast<uint8_t *>(plane0 + static_cast<int64_t>(i) * a.Wo + j);
-                    box_to_planes<kElem>(sbox, lane, valid, p, static_cast<int64_t>(hw) * kElem, nrows);
+                    // read back with lanes along the pixels
+                    if constexpr (PAIRS) {
+                        const int v = 32 * bx + 2 * (lane & 15);
+                        const int i = v / a.wv, j = v - i * a.wv;
+                        const bool valid = v < ncols && j < a.Wo;
+                        uint8_t *p = reinterpret_cast<uint8_t *>(plane0 + static_cast<int64_t>(lane >> 4) * hw +
+                                                                 static_cast<int64_t>(i) * a.Wo + j);
+                        box_to_planes_pairs(sbox, lane, valid, p, static_cast<int64_t>(hw) * kElem, nrows);
+                    } else {
+                        const int v = 32 * bx + lane;          // lane = virtual pixel
+                        const int i = v / a.wv, j = v - i * a.wv;
+                        const bool valid = v < ncols && j < a.Wo;
+                        uint8_t *p = reinterpret_cast<uint8_t *>(plane0 + static_cast<int64_t>(i) * a.Wo + j);
+                        box_to_planes<kElem>(sbox, lane, valid, p, static_cast<int64_t>(hw) * kElem, nrows);
+                    }
                 }
             }
             // every TMEM read of this tile is complete: hand the accumulator back
@@ -472,7 +517,7 @@ struct ConvPlan {
 // 64 taps, a virtual row that fits one tile, copies within TMA's box limits,
 // and shared memory for the weights (resident or a ring of at least two
 // stages) beside two pixel stages and the epilogue's staging.
-bool plan_conv(const ConvGeom &g, bt_code code, int sms, ConvPlan &p) {
+bool plan_conv(const ConvGeom &g, bt_code code, int sms, int out_elem, ConvPlan &p) {
     if (code != BT_CODE_E2M1 && code != BT_CODE_E4M3) return false;
     if (g.s < 1 || g.s > 2 || g.k < 1 || g.k * g.k > kMaxTaps) return false;
     if (g.B < 1 || g.B > (int64_t(1) << 24) || g.O < 1 || g.O > (int64_t(1) << 24)) return false;
@@ -527,6 +572,8 @@ bool plan_conv(const ConvGeom &g, bt_code code, int sms, ConvPlan &p) {
     qx_span = qx_off_max;
     a.wv = a.Wo + qx_span;
     const int bn_max = code == BT_CODE_E2M1 ? 240 : 256;
+    // an even row width keeps pixel pairs of an even Wo aligned in the output
+    if (a.Wo % 2 == 0 && a.wv % 2 == 1 && a.wv + 1 <= bn_max) a.wv += 1;
     if (a.wv > bn_max || a.wv * s > 256) return false;
     int ht = bn_max / a.wv;
     if (ht > a.Ho) ht = a.Ho;
@@ -554,51 +601,71 @@ bool plan_conv(const ConvGeom &g, bt_code code, int sms, ConvPlan &p) {
     const int64_t tiles = static_cast<int64_t>(a.num_ot) * a.B * a.bands;
     if (tiles > (int64_t(1) << 30)) return false;
     a.num_tiles = static_cast<int>(tiles);
-    // weights: resident if they fit beside the pixel stages and the staging;
-    // two pixel stages where they fit with a ring of two weight slices, else one
+    // weights resident (loaded once per CTA, each CTA keeping one channel
+    // tile) or streamed through a ring of slices re-read per tile; one or two
+    // pixel stages. Preference: resident + two stages; resident + one stage
+    // when a CTA gets at most two tiles (only the second tile's copy is then
+    // exposed); streamed + two stages; resident + one; streamed + one.
+    // BT_CONV_PLAN=r2|r1|s2|s1 picks one where it fits.
     const int nslices = a.ntap * a.nsl;
     const int64_t slice_a = static_cast<int64_t>(kBM) * sw;
-    a.b_stages = kMaxBStages;
-    if (kReserve + kStagingBytes + static_cast<int64_t>(kMaxBStages) * a.stage_bytes + 2 * slice_a > kSmemMax)
-        a.b_stages = 1;
-    const int64_t fixed = kReserve + kStagingBytes + static_cast<int64_t>(a.b_stages) * a.stage_bytes;
-    if (fixed > kSmemMax) return false;
-    const int64_t room = kSmemMax - fixed;
     int units = sms;
     if (units > a.num_tiles) units = a.num_tiles;
-    // resident weights: each CTA keeps one channel tile, so the grid is a
-    // multiple of the channel tiles
-    int a_d = 1;
+    int a_d_res = 1;
     for (int d = 8; d >= 1; --d)
-        if (nslices % d == 0) { a_d = d; break; }
-    const int a_boxes = nslices / a_d;
-    if (static_cast<int64_t>(a_boxes) * a_d * slice_a <= room && units >= a.num_ot) {
+        if (nslices % d == 0) { a_d_res = d; break; }
+    const int64_t a_res_bytes = static_cast<int64_t>(nslices) * slice_a;
+    auto fixed_of = [&](int bst) {
+        return kReserve + staging_bytes(out_elem) + static_cast<int64_t>(bst) * a.stage_bytes;
+    };
+    auto fits_res = [&](int bst) { return units >= a.num_ot && fixed_of(bst) + a_res_bytes <= kSmemMax; };
+    auto stream_d = [&](int bst, int *stages) {
+        for (int d = 4; d >= 1; --d) {
+            if (nslices % d != 0) continue;
+            const int64_t room = kSmemMax - fixed_of(bst);
+            const int64_t st = room > 0 ? room / (d * slice_a) : 0;
+            if (st >= 2) { *stages = static_cast<int>(st > kMaxAStages ? kMaxAStages : st); return d; }
+        }
+        return 0;
+    };
+    int st2 = 0, st1 = 0;
+    const int sd2 = stream_d(2, &st2), sd1 = stream_d(1, &st1);
+    const bool few = a.num_tiles <= 2 * ((units / a.num_ot) * a.num_ot > 0 ? (units / a.num_ot) * a.num_ot : units);
+    char plan = 0;                                   // 'R' resident, 'S' streamed
+    int bst = 2;
+    if (const char *env = std::getenv("BT_CONV_PLAN")) {
+        if (std::strcmp(env, "r2") == 0 && fits_res(2)) { plan = 'R'; bst = 2; }
+        else if (std::strcmp(env, "r1") == 0 && fits_res(1)) { plan = 'R'; bst = 1; }
+        else if (std::strcmp(env, "s2") == 0 && sd2) { plan = 'S'; bst = 2; }
+        else if (std::strcmp(env, "s1") == 0 && sd1) { plan = 'S'; bst = 1; }
+    }
+    if (plan == 0) {
+        if (fits_res(2)) { plan = 'R'; bst = 2; }
+        else if (few && fits_res(1)) { plan = 'R'; bst = 1; }
+        else if (sd2) { plan = 'S'; bst = 2; }
+        else if (fits_res(1)) { plan = 'R'; bst = 1; }
+        else if (sd1) { plan = 'S'; bst = 1; }
+        else return false;
+    }
+    a.b_stages = bst;
+    if (plan == 'R') {
         a.a_resident = 1;
-        a.a_d = a_d;
-        a.a_boxes = a_boxes;
+        a.a_d = a_d_res;
+        a.a_boxes = nslices / a_d_res;
         a.a_stages = 0;
         units = units / a.num_ot * a.num_ot;
-        p.smem = static_cast<int>(fixed + static_cast<int64_t>(a_boxes) * a_d * slice_a);
+        p.smem = static_cast<int>(fixed_of(bst) + a_res_bytes);
     } else {
         a.a_resident = 0;
         a.a_boxes = 0;
-        a_d = 0;
-        for (int d = 4; d >= 1; --d) {
-            if (nslices % d != 0) continue;
-            const int64_t st = room / (d * slice_a);
-            if (st >= 2) {
-                a_d = d;
-                a.a_stages = static_cast<int>(st > kMaxAStages ? kMaxAStages : st);
-                break;
-            }
-        }
-        if (a_d == 0) return false;
-        a.a_d = a_d;
-        p.smem = static_cast<int>(fixed + static_cast<int64_t>(a.a_stages) * a_d * slice_a);
+        a.a_d = bst == 2 ? sd2 : sd1;
+        a.a_stages = bst == 2 ? st2 : st1;
+        p.smem = static_cast<int>(fixed_of(bst) + static_cast<int64_t>(a.a_stages) * a.a_d * slice_a);
     }
     if (p.smem > kSmemMax) return false;
     p.grid = units < 1 ? 1 : units;
     a.idesc = make_idesc(code, kBM, a.bn);
+    a.pairs = (a.wv % 2 == 0 && a.Wo % 2 == 0 && (static_cast<int64_t>(a.Ho) * a.Wo) % 2 == 0) ? 1 : 0;
     return true;
 }
 
@@ -638,9 +705,9 @@ bool encode_maps(const ConvGeom &g, bt_code code, const ConvArgs &a, const uint8
     return true;
 }
 
-template <int CODE, int OUT, int SW>
+template <int CODE, int OUT, int SW, bool PAIRS>
 cudaError_t launch_t(const CUtensorMap &ma, const CUtensorMap &mb, const ConvPlan &p, cudaStream_t s) {
-    auto kern = conv_kernel<CODE, OUT, SW>;
+    auto kern = conv_kernel<CODE, OUT, SW, PAIRS>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] { attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax); });
@@ -662,10 +729,14 @@ template <int CODE, int SW>
 cudaError_t launch_out(const CUtensorMap &ma, const CUtensorMap &mb, const ConvPlan &p, bt_dtype out_t,
                        cudaStream_t s) {
     switch (out_t) {
-        case BT_F32: return launch_t<CODE, BT_F32, SW>(ma, mb, p, s);
-        case BT_BF16: return launch_t<CODE, BT_BF16, SW>(ma, mb, p, s);
-        case BT_F16: return launch_t<CODE, BT_F16, SW>(ma, mb, p, s);
-        default: return launch_t<CODE, BT_I32, SW>(ma, mb, p, s);
+        case BT_F32: return launch_t<CODE, BT_F32, SW, false>(ma, mb, p, s);
+        case BT_BF16:
+            return p.a.pairs ? launch_t<CODE, BT_BF16, SW, true>(ma, mb, p, s)
+                             : launch_t<CODE, BT_BF16, SW, false>(ma, mb, p, s);
+        case BT_F16:
+            return p.a.pairs ? launch_t<CODE, BT_F16, SW, true>(ma, mb, p, s)
+                             : launch_t<CODE, BT_F16, SW, false>(ma, mb, p, s);
+        default: return launch_t<CODE, BT_I32, SW, false>(ma, mb, p, s);
     }
 }
 
@@ -678,7 +749,7 @@ bool conv_implicit_applies(const ConvGeom &g, bt_code code) {
     ConvGeom q = g;
     q.O = kBM;                      // the plan's feasibility does not depend on O
     ConvPlan p;
-    return plan_conv(q, code, 148, p);
+    return plan_conv(q, code, 148, 4, p);   // 4-byte outputs need the most staging
 }
 
 cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
@@ -686,7 +757,8 @@ cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_cod
                                     const float *scales) {
     if (!conv_implicit_applies(g, code)) return cudaErrorNotSupported;
     ConvPlan p;
-    if (!plan_conv(g, code, device_sm_count(), p)) return cudaErrorNotSupported;
+    if (!plan_conv(g, code, device_sm_count(), out_t == BT_BF16 || out_t == BT_F16 ? 2 : 4, p))
+        return cudaErrorNotSupported;
     p.a.alpha = alpha;
     p.a.scales = scales;
     p.a.out = out;

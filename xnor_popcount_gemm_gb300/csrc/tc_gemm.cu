@@ -706,7 +706,9 @@ bool map_3d(CUtensorMap *m, const void *ptr, uint64_t pitch, uint64_t rows, uint
 // Tile configuration: the shape (single CTAs or CTA pairs), BN (a multiple of
 // 16 up to 240 for E2M1 / 256 for E4M3; the epilogue masks the part of its
 // last 32-column box past the tile) and D, the K slices per stage.
-// The cost model, from measurements on GB300 (2070 MHz): a problem takes
+// The cost model, whose constants are estimates fitted to measurements on
+// GB300 (2070 MHz; standalone probes and timing-only copies of this kernel
+// that are not part of this repository): a problem takes
 // `rounds` waves of tiles over the SMs (pairs: SMs / 2 at a time). A K slice
 // costs the largest of
 //   - its MMA time: an M=128 MMA of 32 bytes of K per row takes N / 2 clocks
