@@ -507,8 +507,8 @@ def run_ours(args, rank, world):
     peaks, peak_src = measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     roof = roofline_of(ops, contraction_bytes(wl, code, bt), gemm_ms, algo_name, peaks, sms)
-    roof.update({"traffic": load_traffic(wl.name, algo_name),
-                 "traffic_unit": "DRAM bytes per tc_kernel launch (ncu, this kernel source)",
+    roof.update({"traffic": load_traffic(wl.name, algo_name, wl.kind),
+                 "traffic_unit": "DRAM bytes per launch of the contraction kernel (ncu, this kernel source)",
                  "peak_source": f"{peak_src}: {roof.pop('peak_how')}", "kernel": "contraction"})
     pack_b = pack_bytes(wl, code, bt)
     line = {
@@ -645,23 +645,25 @@ def pack_bytes(wl, code, bt):
     return wl.x.numel() * wl.x.element_size() + B * Ho * Wo * k * k * bt.bt_packed_row_bytes(C, code)
 
 
-def kernel_source_hash() -> str:
-    """First 16 hex digits of the sha256 of the contraction kernel's sources."""
+def kernel_source_hash(kind: str = "linear") -> str:
+    """First 16 hex digits of the sha256 of the contraction kernel's sources:
+    tc_gemm.cu (linear) or tc_conv.cu (implicit-im2col convolution), then
+    tc_ptx.cuh."""
     h = hashlib.sha256()
-    for f in ("tc_gemm.cu", "tc_ptx.cuh"):
+    for f in ("tc_gemm.cu" if kind == "linear" else "tc_conv.cu", "tc_ptx.cuh"):
         with open(os.path.join(ROOT, "xnor_popcount_gemm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic(workload: str, algo: str):
+def load_traffic(workload: str, algo: str, kind: str = "linear"):
     """DRAM bytes per contraction launch from the committed ncu summary, if one
     exists for this workload and for the kernel source as it is now."""
     p = os.path.join(ROOT, "profiles", "contraction_dram_traffic.txt")
     if not os.path.exists(p):
         return None
     try:
-        src = kernel_source_hash()
+        src = kernel_source_hash(kind)
         for line in open(p):
             parts = line.split()
             if len(parts) == 3 and not line.startswith("#") and parts[0] == f"{workload}/{algo}" and parts[2] == src:

@@ -133,9 +133,9 @@ def test_pack_nhwc_sign_decision_edges(code, dtype):
                                    (4, 256, 3, 3), (2, 128, 28, 28), (1, 700, 10, 10), (1, 6200, 3, 3),
                                    (2, 33, 2, 2), (3, 96, 8, 12)])
 def test_pack_nchw_to_nhwc(code, dtype, shape, impl, monkeypatch):
-    # the shared-memory transpose by default; with BT_PACK_NHWC=warp, planes
-    # whose bytes are a multiple of 16 take the warp-level kernel (32 pixels x
-    # 32 channels per warp)
+    # planes whose bytes are a multiple of 16 take the warp-level kernel (32
+    # pixels x 32 channels per warp) unless BT_PACK_NHWC=smem; the others take
+    # the shared-memory transpose
     monkeypatch.setenv("BT_PACK_NHWC", impl)
     x = _gen(sum(shape), shape, dtype)
     for bias in (None, torch.tensor([-0.1]), torch.linspace(-0.3, 0.3, shape[1])):
@@ -430,8 +430,9 @@ def test_full_conv_workloads_bench_calls(name, code):
 # last slice, and rows shorter than one slice.
 # ---------------------------------------------------------------------------
 
-TC_CONFIGS = ["240,1", "224,2", "128,4", "64,2", "32,1", "208,2", "96,4",
-              "pair,240,2", "pair,224,1", "pair,160,4", "pair,128,2", "pair,64,4", "pair,32,1", "pair,208,2"]
+TC_CONFIGS = ["240,1", "224,2", "128,4", "64,2", "32,1", "208,2", "96,4", "224,3",
+              "pair,240,2", "pair,224,1", "pair,160,4", "pair,128,2", "pair,64,4", "pair,32,1", "pair,208,2",
+              "pair,224,3", "pair,240,3"]
 
 
 @pytest.mark.parametrize("cfg", TC_CONFIGS)

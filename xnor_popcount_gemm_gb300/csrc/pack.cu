@@ -513,84 +513,85 @@ __device__ __forceinline__ uint64_t transpose8x8(uint64_t v) {
 }
 
 // nhwc, warp-level. A unit is (image b, 32 consecutive pixels, 32 channels)
-// and belongs to one warp: lane l loads the 32 pixels of channel 32g + l
-// (16-byte loads along its channel plane) and keeps their signs as one 32-bit
-// word (bit p = pixel p binarizes to +1); a 32 x 32 bit-matrix transpose
-// across the warp (five rounds of shuffles, each swapping the off-diagonal
-// blocks of half the size between lanes l and l ^ s) leaves lane p with the
-// word of pixel p over the 32 channels, which it turns into codes and stores
-// (4 bytes of bits, 16 of E2M1, 32 of E4M3) at its place in the pixel's
-// packed row. No shared memory, no block barrier; consecutive warps take the
-// channel groups of the same pixels, so each pixel row is completed by
-// neighbouring warps. Channels past C are code 0 (the row's zero padding).
-// A lane's four 16-byte loads of its channel's 32 pixels go through the
-// L1-allocating read-only path, so that they share their 32-byte sectors.
-// Needs every channel plane 16-byte aligned and HW a multiple of 4 (f32) or
-// 8 (2-byte types); pixels past HW are neither loaded nor stored.
+// and belongs to one warp. Loads: in round k (0..3) lane l reads 8 pixels
+// (one 16-byte load for a 2-byte type, two for f32) of channel 8k + l / 4,
+// pixels 8 (l % 4) .. + 7, so each load instruction covers 8 channel planes
+// with 64 (128) contiguous bytes each, and turns them into one byte of sign
+// bits (bit = +1). Lane l's word then holds bit (c, p) for channel c = 8k +
+// (l >> 2) and pixel p = 8 (l & 3) + b at register bit 8k + b: lane bits
+// (c2 c1 c0 p4 p3), register bits (c4 c3 p2 p1 p0). Three rounds of shuffles
+// exchange lane bits 4, 3, 2 with register bits 2, 1, 0 (the off-diagonal
+// blocks of a bit-matrix transpose), and one shuffle permutes the lanes to
+// (p4 p3 p2 p1 p0): lane p ends with the word of pixel p, bit c for channel c.
+// It turns that into codes and stores them (4 bytes of bits, 16 of E2M1, 32
+// of E4M3) at its place in the pixel's packed row. No shared memory, no block
+// barrier. Consecutive warps take consecutive pixel blocks of the same
+// channels. Channels past C are code 0 (the row's zero padding). Needs every
+// channel plane 16-byte aligned and HW a multiple of 4 (f32) or 8 (2-byte
+// types); pixels past HW are neither loaded nor stored. (Measured on GB300
+// inside a convolution step, this layout beat both the shared-memory
+// transpose and a variant with one 512-byte plane run per load instruction.)
 template <int CODE> struct Group32;
 template <> struct Group32<BT_CODE_BITS> { static constexpr int kBytes = 4; };
 template <> struct Group32<BT_CODE_E2M1> { static constexpr int kBytes = 16; };
 template <> struct Group32<BT_CODE_E4M3> { static constexpr int kBytes = 32; };
+constexpr int kWarpPackPixels = 32;
 
-// Transpose of the 32 x 32 bit matrix whose row l is lane l's word: after it,
-// bit j of lane p's word is bit p of lane j's word before.
-__device__ __forceinline__ uint32_t transpose32_warp(uint32_t w, int lane) {
-    const uint32_t masks[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
-#pragma unroll
-    for (int i = 0; i < 5; ++i) {
-        const int sft = 16 >> i;
-        const uint32_t m = masks[i];
-        const uint32_t t = __shfl_xor_sync(0xFFFFFFFFu, w, sft);
-        w = (lane & sft) ? ((w & ~m) | ((t >> sft) & m)) : ((w & m) | ((t & m) << sft));
-    }
-    return w;
+// One exchange round: swaps, between lanes l and l ^ L, the bits whose lane bit
+// (weight L) differs from their register bit (weight R): afterwards bit (lane,
+// reg) holds what bit (lane with its L-bit set to reg's R-bit, reg with its
+// R-bit set to lane's L-bit) held. M: the register bits whose R-bit is 0.
+template <int L, int R, uint32_t M>
+__device__ __forceinline__ uint32_t exchange_bits(uint32_t w, int lane) {
+    const uint32_t t = __shfl_xor_sync(0xFFFFFFFFu, w, L);
+    return (lane & L) ? ((w & ~M) | ((t >> R) & M)) : ((w & M) | ((t & M) << R));
 }
 
 template <typename T, int CODE>
 __global__ void __launch_bounds__(kPackThreads)
-pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, int npb, int ncg, int64_t units,
+pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, FastDiv div_npb, FastDiv div_ncg,
                       const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out, int rb) {
     constexpr int OB = Group32<CODE>::kBytes;
     const int lane = threadIdx.x & 31;
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const uint32_t warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int ncg = static_cast<int>(div_ncg.d), npb = static_cast<int>(div_npb.d);
+    const int j = lane & 3;                                // this lane's 8-pixel chunk in the loads
     pdl_launch_dependents();
     pdl_wait();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
-    for (int64_t u = warp0; u < units; u += nwarps) {
-        const int cg = static_cast<int>(u % ncg);
-        const int64_t rest = u / ncg;
-        const int pb = static_cast<int>(rest % npb);
-        const int64_t b = rest / npb;
-        const int p0 = pb * 32;
-        const int c = cg * 32 + lane;
-        uint32_t pos = 0;                                 // bit p: pixel p0 + p binarizes to +1
-        if (c < C) {
-            const float bc = bias_len > 1 ? __ldg(bias + c) : bs;
-            const T *src = x + (b * C + c) * static_cast<int64_t>(HW) + p0;
-            const int npx = HW - p0 < 32 ? HW - p0 : 32;
-            Group<T> g[4];
+    for (uint32_t u = warp0; u < units; u += nwarps) {
+        const uint32_t rest = fdiv(u, div_npb);
+        const int p0 = static_cast<int>(u - rest * static_cast<uint32_t>(npb)) * kWarpPackPixels;
+        const uint32_t bimg = fdiv(rest, div_ncg);
+        const int cg = static_cast<int>(rest - bimg * static_cast<uint32_t>(ncg));
+        const int64_t b = bimg;
+        const int px = p0 + 8 * j;
+        const int nvalid_px = HW - px;                     // pixels of this lane's chunk inside the image
+        // all four rounds' loads go out before any of them is used
+        Group<T> g[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (8 * k + 8 <= npx) {
+        for (int k = 0; k < 4; ++k) {
+            const int c = cg * 32 + 8 * k + (lane >> 2);
 #pragma unroll
-                    for (int i = 0; i < Group<T>::kWords / 4; ++i) {
-                        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src + 8 * k) + i);
+            for (int i = 0; i < Group<T>::kWords; ++i) g[k].w[i] = 0u;
+            if (c < C && nvalid_px > 0) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(x + (b * C + c) * static_cast<int64_t>(HW) + px);
+#pragma unroll
+                for (int i = 0; i < Group<T>::kWords / 4; ++i) {
+                    if (i == 0 || nvalid_px >= 8) {           // f32: the second half only if inside
+                        const uint4 q = __ldg(src + i);
                         g[k].w[4 * i] = q.x; g[k].w[4 * i + 1] = q.y; g[k].w[4 * i + 2] = q.z; g[k].w[4 * i + 3] = q.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < Group<T>::kWords; ++i) g[k].w[i] = 0u;
-                    if constexpr (sizeof(T) == 4) {               // HW a multiple of 4: half a group
-                        if (8 * k + 4 <= npx) {
-                            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src + 8 * k));
-                            g[k].w[0] = q.x; g[k].w[1] = q.y; g[k].w[2] = q.z; g[k].w[3] = q.w;
-                        }
                     }
                 }
             }
+        }
+        uint32_t w = 0;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 4; ++k) {
+            const int c = cg * 32 + 8 * k + (lane >> 2);
+            if (c < C && nvalid_px > 0) {
+                const float bc = bias_len > 1 ? __ldg(bias + c) : bs;
                 uint32_t P0, P1;
                 if (isfinite(bc)) {
                     masks_ge<T>(g[k], -bc, P0, P1);
@@ -601,11 +602,14 @@ pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, int npb, int ncg, 
                     for (int e = 0; e < 8; ++e) bb[e] = bc;
                     masks_add(f, bb, P0, P1);
                 }
-                pos |= mask_byte(P0, P1) << (8 * k);
+                w |= mask_byte(P0, P1) << (8 * k);
             }
         }
-        // lane p: bit j = channel 32 cg + j at pixel p0 + p
-        const uint32_t w = transpose32_warp(pos, lane);
+        w = exchange_bits<16, 4, 0x0F0F0F0Fu>(w, lane);
+        w = exchange_bits<8, 2, 0x33333333u>(w, lane);
+        w = exchange_bits<4, 1, 0x55555555u>(w, lane);
+        w = __shfl_sync(0xFFFFFFFFu, w, ((lane & 7) << 2) | (lane >> 3));
+        // lane p: bit c = channel 32 cg + c at pixel p0 + p
         if (p0 + lane >= HW) continue;
         const int nvalid = C - cg * 32 >= 32 ? 32 : (C - cg * 32 > 0 ? C - cg * 32 : 0);
         const uint32_t valid = nvalid == 32 ? 0xFFFFFFFFu : (1u << nvalid) - 1u;
@@ -1003,14 +1007,12 @@ pack_im2col_direct_kernel(const T *__restrict__ x, int C, int H, int W, int Ho, 
     }
 }
 
-// The shared-memory transpose kernel is the default for channel-packed
-// pixels; BT_PACK_NHWC=warp selects the warp-level one (both stay under
-// test). Inside a convolution step the shared-memory kernel measured faster
-// on GB300: the warp-level kernel's loads of 16 bytes from 32 channel planes
-// per instruction pulled about 1.8 times the input through L2.
+// For channel-packed pixels the warp-level kernel (contiguous loads) is the
+// default where it applies; BT_PACK_NHWC=smem selects the shared-memory
+// transpose kernel instead (both stay under test).
 bool nhwc_warp_disabled() {
     const char *env = std::getenv("BT_PACK_NHWC");
-    return env == nullptr || std::strcmp(env, "warp") != 0;
+    return env != nullptr && std::strcmp(env, "smem") == 0;
 }
 
 int grid_for(int64_t threads) {
@@ -1096,18 +1098,21 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
     constexpr int E = Elem<T>::kPerVec;
     const bool vec = ((HW * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned(x, 16);
     if (vec && HW < (int64_t(1) << 30) && C < (int64_t(1) << 30) && !nhwc_warp_disabled()) {
-        // warp-level units of 32 pixels x 32 channels
-        const int64_t npb = (HW + 31) / 32, ncg = rb / Group32<CODE>::kBytes;
+        // warp-level units of 32 channels x 256 pixels
+        const int64_t npb = (HW + kWarpPackPixels - 1) / kWarpPackPixels, ncg = rb / Group32<CODE>::kBytes;
         const int64_t units = B * npb * ncg;
-        const int sms = device_sm_count();
-        const int64_t per_block = kPackThreads / 32;
-        const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * (2048 / kPackThreads);
-        int64_t blocks = (units + per_block - 1) / per_block;
-        if (blocks > cap) blocks = cap;
-        if (blocks < 1) blocks = 1;
-        return launch_pdl(pack_nhwc_warp_kernel<T, CODE>, dim3(static_cast<unsigned>(blocks)), dim3(kPackThreads), s, x,
-                          static_cast<int>(C), static_cast<int>(HW), static_cast<int>(npb), static_cast<int>(ncg), units,
-                          bias, static_cast<int>(bias_len), out, static_cast<int>(rb));
+        if (units < (int64_t(1) << 31)) {
+            const int sms = device_sm_count();
+            const int64_t per_block = kPackThreads / 32;
+            const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * (2048 / kPackThreads);
+            int64_t blocks = (units + per_block - 1) / per_block;
+            if (blocks > cap) blocks = cap;
+            if (blocks < 1) blocks = 1;
+            return launch_pdl(pack_nhwc_warp_kernel<T, CODE>, dim3(static_cast<unsigned>(blocks)), dim3(kPackThreads),
+                              s, x, static_cast<int>(C), static_cast<int>(HW), static_cast<uint32_t>(units),
+                              make_fastdiv(static_cast<uint32_t>(npb)), make_fastdiv(static_cast<uint32_t>(ncg)), bias,
+                              static_cast<int>(bias_len), out, static_cast<int>(rb));
+        }
     }
     const int smem = kNhwcGroups * nhwc_cstride(static_cast<int>(C));
     const int64_t upi = (HW + kNhwcPixels - 1) / kNhwcPixels;

@@ -74,8 +74,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 480;                 // 32 columns of unit block scales (E2M1)
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;    // UE8M0 127 = 2^0 in every byte
 constexpr int kSmemMax = 232448;                 // 227 KB opt-in per CTA
-constexpr int kBoxBytes = 32 * 128;              // one epilogue staging box: 32 rows x 128 B
-constexpr int kStagingBytes = kEpiWarps * kBoxBytes;   // one box per epilogue warp
+// One staging box per epilogue warp: 32 rows x 32 outputs (4 KB for 4-byte
+// outputs, 2 KB for 2-byte ones).
+__host__ __device__ constexpr int staging_bytes(int out_elem) { return kEpiWarps * 32 * 32 * out_elem; }
 constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
 constexpr int kMaxStages = 8;
 
@@ -115,11 +116,13 @@ __host__ __device__ __forceinline__ int b_slot_rows(int bn, bool pair) { return 
 // Shared memory: S stages of D slices of A (128 rows) and B, the epilogue
 // staging boxes, barriers. S is as many stages as fit (at most 8).
 int stage_bytes(int bn, bool pair, int d) { return (kBM + b_slot_rows(bn, pair)) * kRowB * d; }
-int num_stages(int bn, bool pair, int d) {
-    const int s = (kSmemMax - kReserve - kStagingBytes) / stage_bytes(bn, pair, d);
+int num_stages(int bn, bool pair, int d, int out_elem) {
+    const int s = (kSmemMax - kReserve - staging_bytes(out_elem)) / stage_bytes(bn, pair, d);
     return s > kMaxStages ? kMaxStages : s;
 }
-int smem_bytes(int bn, bool pair, int d) { return num_stages(bn, pair, d) * stage_bytes(bn, pair, d) + kStagingBytes + kReserve; }
+int smem_bytes(int bn, bool pair, int d, int out_elem) {
+    return num_stages(bn, pair, d, out_elem) * stage_bytes(bn, pair, d) + staging_bytes(out_elem) + kReserve;
+}
 
 // TMEM column of the second accumulator buffer; also the largest BN.
 template <int CODE> __host__ __device__ constexpr uint32_t acc_stride() { return CODE == BT_CODE_E2M1 ? 240u : 256u; }
@@ -305,7 +308,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base, sB = base + S * kAStage;
     const uint32_t sStage = sB + S * kBStage;                        // epilogue staging boxes
-    const uint32_t bars = sStage + kStagingBytes;                    // full[S], empty[S], tfull[2], tempty[2], drain
+    const uint32_t bars = sStage + staging_bytes(kElem);             // full[S], empty[S], tfull[2], tempty[2], drain
     uint8_t *gbars = smem_raw + (bars - raw);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbars + 8 * (2 * kMaxStages + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -497,7 +500,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
         // ---------------- epilogue (warps 2..9) ----------------
         pdl_wait();                                       // the previous kernel may still use `out`
         T *const out_base = static_cast<T *>(a.out);
-        const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * kBoxBytes);   // this warp's staging box
+        const uint32_t sbox = sStage + static_cast<uint32_t>((warp - 2) * 32 * kBoxInner);   // this warp's staging box
         constexpr bool kMask = LAYOUT == kRowsMaskBf16 || LAYOUT == kRowsMaskF32;
         const float alpha = a.scales != nullptr ? alpha_from(a.scales) : a.alpha;
         float tsum = 0.0f;                                // masked layouts: this lane's grad_scale_a terms
@@ -749,19 +752,19 @@ double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int
     return static_cast<double>(rounds) * tile + epi + 600.0;
 }
 
-TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn) {
+TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn, int out_elem) {
     if (const char *env = std::getenv("BT_TC_CONFIG")) {
         int bn = 0, d = 0;
         const bool pair = std::strncmp(env, "pair,", 5) == 0;
         if (std::sscanf(pair ? env + 5 : env, "%d,%d", &bn, &d) == 2 && bn >= 32 && bn <= max_bn && bn % 16 == 0 &&
-            (d == 1 || d == 2 || d == 4) && num_stages(bn, pair, d) >= 2)
+            d >= 1 && d <= 4 && num_stages(bn, pair, d, out_elem) >= 2)
             return TileCfg{pair, bn, d, 0.0};
     }
     TileCfg best{false, max_bn, 1, -1.0};
     for (int p = 1; p >= 0; --p)
         for (int d = 4; d >= 1; d /= 2)
             for (int bn = max_bn; bn >= 32; bn -= 16) {
-                if (num_stages(bn, p == 1, d) < 2) continue;
+                if (num_stages(bn, p == 1, d, out_elem) < 2) continue;
                 const double c = tile_cost(p == 1, bn, d, M, N, slices, sms);
                 if (best.cost < 0.0 || c < best.cost * 0.999) best = TileCfg{p == 1, bn, d, c};
             }
@@ -775,9 +778,9 @@ struct Maps {
 template <int CODE, int LAYOUT, int OUT, bool PAIR>
 cudaError_t launch_t(const Maps &mp, TcArgs a, cudaStream_t s) {
     auto kern = tc_kernel<CODE, LAYOUT, OUT, PAIR>;
-    a.stages = num_stages(a.bn, PAIR, a.d);
+    a.stages = num_stages(a.bn, PAIR, a.d, static_cast<int>(sizeof(typename OutT<OUT>::type)));
     a.wait_ns = wait_limit_ns();
-    const int smem = smem_bytes(a.bn, PAIR, a.d);
+    const int smem = smem_bytes(a.bn, PAIR, a.d, static_cast<int>(sizeof(typename OutT<OUT>::type)));
     if (a.stages < 2 || smem > kSmemMax) return cudaErrorInvalidValue;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -852,7 +855,7 @@ int out_elem_bytes(bt_dtype t) { return t == BT_BF16 || t == BT_F16 ? 2 : 4; }
 // rb_split > 0 the contraction is split along K into parts of rb_split bytes
 // (a multiple of 128) that the caller runs as K splits.
 bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const uint8_t *bp, int64_t M, int64_t N,
-          int64_t rb, int64_t pitch_a, int64_t pitch_b, int64_t rb_split = -1) {
+          int64_t rb, int64_t pitch_a, int64_t pitch_b, int out_elem, int64_t rb_split = -1) {
     if (rb % 16 != 0 || pitch_a % 16 != 0 || pitch_b % 16 != 0 || pitch_a < rb || pitch_b < rb ||
         M > (int64_t(1) << 31) - 512 || N > (int64_t(1) << 31) - 512)
         return false;
@@ -862,7 +865,7 @@ bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const ui
     a.slices = static_cast<int>(((rb_split > 0 ? rb_split : rb) + kRowB - 1) / kRowB);   // per K split
     a.full_slices = static_cast<int>(rb / kRowB);                                       // of the whole row
     const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;       // E2M1 keeps 32 TMEM columns for block scales
-    c = choose_cfg(M, N, a.slices, sm_count(), max_bn);
+    c = choose_cfg(M, N, a.slices, sm_count(), max_bn, out_elem);
     a.bn = c.bn;
     a.d = c.d;
     a.nk = (a.slices + a.d - 1) / a.d;
@@ -896,7 +899,7 @@ cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code,
     Maps mp;
     TileCfg c;
     const int64_t rb = row_bytes(K, code);
-    if (!plan(a, mp, c, code, xp, wp, M, N, rb, rb, rb)) return cudaErrorInvalidValue;
+    if (!plan(a, mp, c, code, xp, wp, M, N, rb, rb, rb, out_elem_bytes(out_t))) return cudaErrorInvalidValue;
     a.alpha = alpha;
     a.scales = scales;
     a.out = out;
@@ -913,7 +916,8 @@ cudaError_t launch_tc_conv(const uint8_t *rows, const uint8_t *wp, bt_code code,
     TcArgs a{};
     Maps mp;
     TileCfg c;
-    if (!plan(a, mp, c, code, wp, rows, g.O, g.B * g.Ho * g.Wo, krow, krow, krow)) return cudaErrorInvalidValue;
+    if (!plan(a, mp, c, code, wp, rows, g.O, g.B * g.Ho * g.Wo, krow, krow, krow, out_elem_bytes(out_t)))
+        return cudaErrorInvalidValue;
     a.alpha = alpha;
     a.scales = scales;
     a.out = out;
@@ -944,7 +948,7 @@ cudaError_t launch_tc_bf16(const uint16_t *a_ptr, int64_t lda, const uint16_t *b
     Maps mp;
     TileCfg c;
     if (!plan(a, mp, c, kCodeBF16, reinterpret_cast<const uint8_t *>(a_ptr), reinterpret_cast<const uint8_t *>(b_ptr),
-              M, N, klen * 2, lda * 2, ldb * 2))
+              M, N, klen * 2, lda * 2, ldb * 2, mask != nullptr ? 2 : out_elem_bytes(out_t)))
         return cudaErrorInvalidValue;
     a.alpha = alpha;
     a.out = out;
@@ -973,7 +977,7 @@ cudaError_t launch_tc_bf16_splitk(const uint16_t *a_ptr, int64_t lda, const uint
     Maps mp;
     TileCfg c;
     if (!plan(a, mp, c, kCodeBF16, reinterpret_cast<const uint8_t *>(a_ptr), reinterpret_cast<const uint8_t *>(b_ptr),
-              M, N, klen * 2, lda * 2, ldb * 2, klen * 2 / splits))
+              M, N, klen * 2, lda * 2, ldb * 2, 4, klen * 2 / splits))
         return cudaErrorInvalidValue;
     if (static_cast<int64_t>(a.num_tiles) * splits > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     a.num_super = a.num_tiles * splits;
