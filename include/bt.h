@@ -468,6 +468,47 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
                                     size_t workspace_bytes, bt_stream stream);
 
 /*
+ * bt_binary_linear_dscale_init / bt_binary_conv2d_dscale_init -- a layer's
+ * first forward, as BinaryConv2dCutlass.set_activation runs it: scale_a =
+ * (factor * x.abs().mean()), the mean rounded to x's dtype, times factor
+ * rounded to x's dtype, then to scale_dtype (F32, BF16, F16), is computed on
+ * the device and written to scales[0]; the forward then runs with alpha =
+ * fp32(scales[0] * scales[1]) (scales[1] = scale_w, read from device
+ * memory). The sum of |x| comes from the same read of x that packs it: the
+ * rows pack (16- or 8-byte aligned rows) and the channel-packed pixel pack
+ * (16-byte aligned planes) add each thread's compensated fp32 sum of |x| (its
+ * 8-element groups summed pairwise) in double, once per warp, to a
+ * per-context accumulator. Where those packs do not apply, a separate pass
+ * sums x in double. The sum's relative error is a few units of 2^-24; the
+ * rounded scale equals (factor * exact mean) rounded as above unless the exact
+ * mean lies within that error of a rounding boundary of x's dtype (for f32
+ * x: within a few fp32 ulps of it). Arguments otherwise as
+ * bt_binary_linear_dscale / bt_binary_conv2d_dscale with float x (the
+ * workspace of bt_binary_linear_workspace / bt_binary_conv2d_workspace for
+ * x's dtype); factor finite > 0. Calls on one GPU must not overlap (they
+ * share the accumulator). The pages have no separate entry point: this is
+ * set_activation's first call and the forward that follows, without the
+ * .item() host round trip.
+ */
+bt_status bt_binary_linear_dscale_init(const void *x, bt_dtype x_dtype,
+                                       const void *weight, bt_code w_code,
+                                       int64_t M, int64_t N, int64_t K,
+                                       float *scales, float factor, bt_dtype scale_dtype,
+                                       const float *bias_a, int64_t bias_len,
+                                       void *out, bt_dtype out_dtype, bt_algo algo,
+                                       void *workspace, size_t workspace_bytes,
+                                       bt_stream stream);
+bt_status bt_binary_conv2d_dscale_init(const void *x, bt_dtype x_dtype,
+                                       const void *weight, bt_code w_code,
+                                       int64_t B, int64_t C, int64_t H, int64_t W, int64_t O,
+                                       int kernel_size, int stride, int padding, int dilation,
+                                       float *scales, float factor, bt_dtype scale_dtype,
+                                       const float *bias_a, int64_t bias_len,
+                                       void *out, bt_dtype out_dtype, bt_algo algo,
+                                       void *workspace, size_t workspace_bytes,
+                                       bt_stream stream);
+
+/*
  * bt_device_status -- synchronizes `stream`, then reads and clears the
  * device error word of the current device: BT_ERR_TIMEOUT if a kernel's
  * bounded wait ran out since the last call, BT_ERR_CUDA if the stream holds a

@@ -317,3 +317,33 @@ def test_w8a8_abi_validation():
 def test_wait_timeout_setter_validates():
     assert bt._c_wait(61 * 10**9) == bt.BT_ERR_INVALID_ARG
     assert bt._c_wait(0) == bt.BT_OK          # the default (2 s)
+
+
+def test_first_forward_validation():
+    L = bt._c_lin_dsi
+    def lin(**kw):
+        a = dict(x=256, xt=bt.BT_BF16, w=512, code=bt.BT_CODE_E2M1, M=4, N=4, K=64, scales=1024, factor=2.0,
+                 sdt=bt.BT_BF16, bias=None, blen=0, out=2048, ot=bt.BT_F32, algo=0, ws=4096, wsb=1 << 20, s=None)
+        a.update(kw)
+        return L(*a.values())
+    assert lin(scales=None) == bt.BT_ERR_INVALID_ARG
+    assert lin(factor=0.0) == bt.BT_ERR_INVALID_ARG
+    assert lin(factor=float("inf")) == bt.BT_ERR_INVALID_ARG
+    assert lin(sdt=bt.BT_I32) == bt.BT_ERR_INVALID_ARG
+    assert lin(xt=bt.BT_PACKED) == bt.BT_ERR_INVALID_ARG          # x must be floats: the scale comes from it
+    assert lin(scales=1024 + 4) == bt.BT_ERR_ALIGNMENT
+    assert lin(ws=None) == bt.BT_ERR_WORKSPACE
+    assert lin(M=0) == bt.BT_OK
+    C = bt._c_conv_dsi
+    def conv(**kw):
+        a = dict(x=256, xt=bt.BT_BF16, w=512, code=bt.BT_CODE_E2M1, B=1, C=8, H=6, W=6, O=4, k=3, st=1, p=1, d=1,
+                 scales=1024, factor=2.0, sdt=bt.BT_BF16, bias=None, blen=0, out=2048, ot=bt.BT_F32, algo=0, ws=4096,
+                 wsb=1 << 20, s=None)
+        a.update(kw)
+        return C(*a.values())
+    assert conv(scales=None) == bt.BT_ERR_INVALID_ARG
+    assert conv(factor=-1.0) == bt.BT_ERR_INVALID_ARG
+    assert conv(k=0) == bt.BT_ERR_INVALID_ARG
+    assert conv(ws=None) == bt.BT_ERR_WORKSPACE
+    assert conv(B=0) == bt.BT_OK
+

@@ -79,3 +79,58 @@ def test_conv_device_scales_match_oracle(code, s, p, d):
     got = bt.bt_binary_conv2d(x.to(DEV), wp, code, 64, 3, s, p, d, scales, None, bias.to(DEV)).cpu()
     want = oracle.binary_conv2d(x, w, want_sa, 0.031, s, p, d, bias, "bf16")
     _close_rel(got, want)
+
+
+# ---------------------------------------------------------------------------
+# A layer's first forward: scale_a computed from the read of x that packs it
+# (bt_binary_*_dscale_init), then the forward with it.
+# ---------------------------------------------------------------------------
+
+NAMES = {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16"}
+
+
+def _check_scale(got, want, x_dtype):
+    # bf16 / f16 x: the rounded mean equals the oracle's for these inputs; f32
+    # x: within the sum's error (a few units of 2^-24 relative)
+    if x_dtype == torch.float32:
+        assert abs(got - want) <= abs(want) * 4 * 2.0 ** -24
+    else:
+        assert got == want
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32, torch.float16])
+@pytest.mark.parametrize("M,K", [(300, 520), (257, 1001), (64, 4096)])
+def test_linear_first_forward_scale_and_output(code, dt, M, K):
+    # K = 1001 (rows not 8-byte aligned) takes the two-pass fallback
+    x = torch.randn(M, K, generator=torch.Generator().manual_seed(M + K)).to(dt)
+    w = torch.randn(129, K, generator=torch.Generator().manual_seed(7))
+    bias = torch.tensor([0.05])
+    wp = bt.bt_pack_sign(w.to(DEV), code)
+    scales = torch.tensor([0.0, 0.021], dtype=torch.float32, device=DEV)
+    for factor, sdt in ((2.0, dt), (4.0, torch.float32)):
+        got = bt.bt_binary_linear_dscale_init(x.to(DEV), wp, code, K, scales, factor, sdt, bias.to(DEV),
+                                              out_dtype=torch.float32).cpu()
+        sa = float(scales[0].cpu())
+        want_sa = oracle.scale_init(x.float().numpy(), factor, NAMES[dt], NAMES[sdt])
+        _check_scale(sa, want_sa, dt)
+        _close_rel(got, oracle.binary_linear(x, w, sa, 0.021, bias, "f32"))
+
+
+@pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,C,H,W,s,p,d", [(4, 64, 16, 16, 1, 1, 1), (3, 128, 28, 28, 2, 1, 1),
+                                           (2, 40, 7, 9, 2, 2, 2), (1, 16, 3, 300, 1, 1, 1)])
+def test_conv_first_forward_scale_and_output(code, dt, B, C, H, W, s, p, d):
+    # 7 x 9 planes (not 16-byte aligned) take the two-pass fallback; 300-wide
+    # rows the explicit unfold
+    x = torch.randn(B, C, H, W, generator=torch.Generator().manual_seed(B * C + H)).to(dt)
+    w = torch.randn(33, C, 3, 3, generator=torch.Generator().manual_seed(9))
+    bias = torch.linspace(-0.1, 0.1, C)
+    wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    scales = torch.tensor([0.0, 0.031], dtype=torch.float32, device=DEV)
+    got = bt.bt_binary_conv2d_dscale_init(x.to(DEV), wp, code, 3, s, p, d, scales, 2.0, None, bias.to(DEV)).cpu()
+    sa = float(scales[0].cpu())
+    want_sa = oracle.scale_init(x.float().numpy(), 2.0, NAMES[dt], NAMES[dt])
+    _check_scale(sa, want_sa, dt)
+    _close_rel(got, oracle.binary_conv2d(x, w, sa, 0.031, s, p, d, bias, NAMES[dt]))

@@ -24,6 +24,7 @@ __all__ = [
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
     "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
     "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_set_wait_timeout",
+    "bt_binary_linear_dscale_init", "bt_binary_conv2d_dscale_init",
 ]
 
 BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_ALIGNMENT = 0, -1, -2, -3
@@ -80,6 +81,10 @@ _c_lin_ds = _sig("bt_binary_linear_dscale", _i, [_p, _i, _p, _i, _i64, _i64, _i6
                                                 _p, _sz, _p])
 _c_conv_ds = _sig("bt_binary_conv2d_dscale", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
                                                  _p, _p, _i64, _p, _i, _i, _p, _sz, _p])
+_c_lin_dsi = _sig("bt_binary_linear_dscale_init", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _p, _f, _i, _p, _i64, _p,
+                                                      _i, _i, _p, _sz, _p])
+_c_conv_dsi = _sig("bt_binary_conv2d_dscale_init", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i,
+                                                       _i, _p, _f, _i, _p, _i64, _p, _i, _i, _p, _sz, _p])
 _c_w8_ws = _sig("bt_w8a8_conv2d_workspace", _sz, [_i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i])
 _c_w8 = _sig("bt_w8a8_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _p, _i, _p,
                                     _sz, _p])
@@ -95,7 +100,7 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
             "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_binary_conv2d_backward",
             "bt_scale_init", "bt_binary_linear_dscale", "bt_binary_conv2d_dscale", "bt_w8a8_conv2d_workspace",
-            "bt_w8a8_conv2d", "bt_set_wait_timeout"]
+            "bt_w8a8_conv2d", "bt_set_wait_timeout", "bt_binary_linear_dscale_init", "bt_binary_conv2d_dscale_init"]
 
 
 class BtError(RuntimeError):
@@ -386,6 +391,57 @@ def bt_binary_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int,
     _check(_c_conv(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding,
                    dilation, scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),
                    0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def bt_binary_linear_dscale_init(x: torch.Tensor, weight: torch.Tensor, w_code: int, K: int, scales: torch.Tensor,
+                                 factor: float = 2.0, scale_dtype=None, bias_a=None, out_dtype=None,
+                                 algo: int = BT_ALGO_AUTO, out: torch.Tensor | None = None,
+                                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """A layer's first forward: scales[0] = (factor * mean|x|) in x's dtype,
+    then scale_dtype (x's dtype by default), computed from the read of x that
+    packs it; then the forward with alpha = fp32(scales[0] * scales[1])."""
+    _contig(x, "x")
+    _contig(weight, "weight")
+    _contig(scales, "scales")
+    M, N = x.shape[0], weight.shape[0]
+    xt = _DT[x.dtype]
+    st = _DT[scale_dtype if scale_dtype is not None else x.dtype]
+    ot = _DT[out_dtype if out_dtype is not None else x.dtype]
+    if out is None:
+        out = torch.empty((M, N), dtype=_TORCH[ot], device=x.device)
+    ws = _workspace(bt_binary_linear_workspace(M, K, xt, w_code), x.device, workspace)
+    blen = 0 if bias_a is None else bias_a.numel()
+    _check(_c_lin_dsi(_ptr(x), xt, _ptr(weight), w_code, M, N, K, _ptr(scales), factor, st, _ptr(bias_a), blen,
+                      _ptr(out), ot, algo, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def bt_binary_conv2d_dscale_init(x: torch.Tensor, weight: torch.Tensor, w_code: int, kernel_size: int, stride: int,
+                                 padding: int, dilation: int, scales: torch.Tensor, factor: float = 2.0,
+                                 scale_dtype=None, bias_a=None, out_dtype=None, algo: int = BT_ALGO_AUTO,
+                                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                 stream=None) -> torch.Tensor:
+    """The conv2d form of bt_binary_linear_dscale_init (NCHW x, packed weight
+    [O, k, k, row_bytes(C)], NCHW out)."""
+    _contig(x, "x")
+    _contig(weight, "weight")
+    _contig(scales, "scales")
+    B, C, H, W = x.shape
+    O = weight.shape[0]
+    xt = _DT[x.dtype]
+    st = _DT[scale_dtype if scale_dtype is not None else x.dtype]
+    ot = _DT[out_dtype if out_dtype is not None else x.dtype]
+    Ho = conv2d_out_size(H, kernel_size, stride, padding, dilation)
+    Wo = conv2d_out_size(W, kernel_size, stride, padding, dilation)
+    if out is None:
+        out = torch.empty((B, O, max(Ho, 0), max(Wo, 0)), dtype=_TORCH[ot], device=x.device)
+    ws = _workspace(bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, xt, w_code),
+                    x.device, workspace)
+    blen = 0 if bias_a is None else bias_a.numel()
+    _check(_c_conv_dsi(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding, dilation,
+                       _ptr(scales), factor, st, _ptr(bias_a), blen, _ptr(out), ot, algo, _ptr(ws),
+                       0 if ws is None else ws.numel(), _stream(stream)))
     return out
 
 

@@ -209,6 +209,40 @@ bt_status bt_binary_linear_dscale(const void *x, bt_dtype x_dtype, const void *w
                        algo, workspace, workspace_bytes, stream);
 }
 
+bt_status bt_binary_linear_dscale_init(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                                       int64_t M, int64_t N, int64_t K, float *scales, float factor,
+                                       bt_dtype scale_dtype, const float *bias_a, int64_t bias_len, void *out,
+                                       bt_dtype out_dtype, bt_algo algo, void *workspace, size_t workspace_bytes,
+                                       bt_stream stream) {
+    if (scales == nullptr || !float_in(x_dtype) || !float_in(scale_dtype)) return BT_ERR_INVALID_ARG;
+    if (!(std::isfinite(factor) && factor > 0.0f)) return BT_ERR_INVALID_ARG;
+    if (!valid_code(w_code) || !valid_out(out_dtype) || M < 0 || N < 0 || K < 1) return BT_ERR_INVALID_ARG;
+    if (!(bias_len == 0 || bias_len == 1 || bias_len == K) || (bias_len > 0 && bias_a == nullptr))
+        return BT_ERR_INVALID_ARG;
+    if (K > kMaxK) return BT_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return BT_OK;
+    if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16) || !aligned(scales, 8)) return BT_ERR_ALIGNMENT;
+    const size_t need = bt_binary_linear_workspace(M, K, x_dtype, w_code);
+    if (workspace == nullptr || workspace_bytes < need) return BT_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaSuccess;
+    double *acc = fused_abs_sum_accumulator(&err);
+    if (acc == nullptr || cudaMemsetAsync(acc, 0, sizeof(double), s) != cudaSuccess) return BT_ERR_CUDA;
+    // pack x and sum |x| in the same pass (or, where the fused pack does not
+    // apply, pack and sum in two)
+    cudaError_t e = launch_pack_rows_sum(x, x_dtype, M, K, bias_a, bias_len, w_code, workspace, acc, s);
+    if (e == cudaErrorNotSupported) {
+        e = launch_pack_rows(x, x_dtype, M, K, bias_a, bias_len, w_code, workspace, s);
+        if (e == cudaSuccess) e = launch_abs_sum(x, x_dtype, M * K, acc, s);
+    }
+    if (e != cudaSuccess) return BT_ERR_CUDA;
+    if (launch_scale_finish(acc, M * K, factor, x_dtype, scale_dtype, scales, s) != cudaSuccess) return BT_ERR_CUDA;
+    return linear_impl(workspace, BT_PACKED, weight, w_code, M, N, K, 1.0f, 1.0f, scales, nullptr, 0, out, out_dtype,
+                       algo, nullptr, 0, stream);
+}
+
 size_t bt_binary_conv2d_workspace(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride,
                                   int padding, int dilation, bt_dtype x_dtype, bt_code code) {
     if (B < 0 || C < 1 || H < 1 || W < 1 || !valid_code(code) || x_dtype == BT_PACKED_IM2COL) return 0;
@@ -342,6 +376,51 @@ bt_status bt_binary_conv2d_dscale(const void *x, bt_dtype x_dtype, const void *w
     if (scales == nullptr) return BT_ERR_INVALID_ARG;
     return conv_impl(x, x_dtype, weight, w_code, B, C, H, W, O, kernel_size, stride, padding, dilation, 1.0f, 1.0f,
                      scales, bias_a, bias_len, out, out_dtype, algo, workspace, workspace_bytes, stream);
+}
+
+bt_status bt_binary_conv2d_dscale_init(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                                       int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,
+                                       int stride, int padding, int dilation, float *scales, float factor,
+                                       bt_dtype scale_dtype, const float *bias_a, int64_t bias_len, void *out,
+                                       bt_dtype out_dtype, bt_algo algo, void *workspace, size_t workspace_bytes,
+                                       bt_stream stream) {
+    if (scales == nullptr || !float_in(x_dtype) || !float_in(scale_dtype)) return BT_ERR_INVALID_ARG;
+    if (!(std::isfinite(factor) && factor > 0.0f)) return BT_ERR_INVALID_ARG;
+    if (!valid_code(w_code) || !valid_out(out_dtype)) return BT_ERR_INVALID_ARG;
+    if (B < 0 || C < 1 || H < 1 || W < 1 || O < 0) return BT_ERR_INVALID_ARG;
+    if (kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return BT_ERR_INVALID_ARG;
+    if (!(bias_len == 0 || bias_len == 1 || bias_len == C) || (bias_len > 0 && bias_a == nullptr))
+        return BT_ERR_INVALID_ARG;
+    if (conv_out(H, kernel_size, stride, padding, dilation) < 1 || conv_out(W, kernel_size, stride, padding, dilation) < 1)
+        return BT_ERR_INVALID_ARG;
+    if (B == 0 || O == 0) return BT_OK;
+    if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16) || !aligned(scales, 8)) return BT_ERR_ALIGNMENT;
+    if (B > (int64_t(1) << 30) || C > kMaxK || H > (1 << 20) || W > (1 << 20)) return BT_ERR_UNSUPPORTED;
+    // workspace: the packed NHWC pixels, then what the contraction of packed
+    // pixels needs (the im2col rows of the explicit unfold, or nothing)
+    const size_t need = bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype,
+                                                   w_code);
+    if (need == 0) return BT_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < need) return BT_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
+    const size_t pix = round_up(static_cast<size_t>(B * H * W * row_bytes(C, w_code)), 256);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaSuccess;
+    double *acc = fused_abs_sum_accumulator(&err);
+    if (acc == nullptr || cudaMemsetAsync(acc, 0, sizeof(double), s) != cudaSuccess) return BT_ERR_CUDA;
+    cudaError_t e = launch_pack_nhwc_sum(x, x_dtype, B, C, H * W, bias_a, bias_len, w_code, workspace, acc, s);
+    if (e == cudaErrorNotSupported) {
+        e = launch_pack_nhwc(x, x_dtype, B, C, H * W, bias_a, bias_len, w_code, workspace, s);
+        if (e == cudaSuccess) e = launch_abs_sum(x, x_dtype, B * C * H * W, acc, s);
+    }
+    if (e != cudaSuccess) return BT_ERR_CUDA;
+    if (launch_scale_finish(acc, B * C * H * W, factor, x_dtype, scale_dtype, scales, s) != cudaSuccess)
+        return BT_ERR_CUDA;
+    uint8_t *rest = static_cast<uint8_t *>(workspace) + pix;
+    return conv_impl(workspace, BT_PACKED, weight, w_code, B, C, H, W, O, kernel_size, stride, padding, dilation, 1.0f,
+                     1.0f, scales, nullptr, 0, out, out_dtype, algo, need > pix ? rest : nullptr,
+                     need > pix ? workspace_bytes - pix : 0, stream);
 }
 
 int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride, int padding,

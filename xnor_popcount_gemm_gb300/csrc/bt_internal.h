@@ -200,6 +200,27 @@ cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_cod
                                     void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s,
                                     const float *scales = nullptr);
 
+// First-call activation scale (BinaryConv2dCutlass.set_activation): the sum
+// of |x| accumulates in a double per CUDA context (zero it before use; calls
+// that overlap on one GPU share it); launch_abs_sum adds the sum of |x| of n
+// elements to it in a separate pass; launch_scale_finish turns it into
+// (factor * mean) rounded to x's dtype, then to scale_dtype, written to
+// scale_out (one float).
+double *fused_abs_sum_accumulator(cudaError_t *err);
+cudaError_t launch_abs_sum(const void *x, bt_dtype x_dtype, int64_t n, double *acc, cudaStream_t s);
+cudaError_t launch_scale_finish(const double *acc, int64_t n, float factor, bt_dtype x_dtype, bt_dtype scale_dtype,
+                                float *scale_out, cudaStream_t s);
+
+// The activation packs with the sum of |x| of every element they read added to
+// *abs_sum (compensated fp32 per thread, double across warps): rows (the flat
+// kernel) and channel-packed pixels (the warp-level kernel). They return
+// cudaErrorNotSupported where those kernels do not apply; the caller then
+// packs as usual and sums in a separate pass.
+cudaError_t launch_pack_rows_sum(const void *x, bt_dtype xt, int64_t R, int64_t K, const float *bias,
+                                 int64_t bias_len, bt_code code, void *out, double *abs_sum, cudaStream_t s);
+cudaError_t launch_pack_nhwc_sum(const void *x, bt_dtype xt, int64_t B, int64_t C, int64_t HW, const float *bias,
+                                 int64_t bias_len, bt_code code, void *out, double *abs_sum, cudaStream_t s);
+
 // Launch attribute list allowing programmatic dependent launch (the kernel
 // overlaps its prologue with the previous kernel in the stream).
 inline cudaLaunchAttribute pdl_attribute() {

@@ -191,6 +191,32 @@ __device__ __forceinline__ void store_masks(uint8_t *dst, uint32_t P0, uint32_t 
     }
 }
 
+// Sum of |x| for the first-call activation scale, kept per thread as a
+// compensated fp32 pair (Neumaier: s + c), then added in double across the
+// warp and once per warp to the accumulator. An infinite term leaves the sum
+// infinite (no compensation of inf - inf).
+struct AbsSum {
+    float s = 0.0f, c = 0.0f;
+    __device__ __forceinline__ void add(float v) {
+        const float t = s + v;
+        if (isfinite(t)) c += fabsf(s) >= fabsf(v) ? (s - t) + v : (v - t) + s;
+        s = t;
+    }
+    template <typename T> __device__ __forceinline__ void add_group(const Group<T> &g) {
+        float f[8];
+        g.unpack(f);
+        add(((fabsf(f[0]) + fabsf(f[1])) + (fabsf(f[2]) + fabsf(f[3]))) +
+            ((fabsf(f[4]) + fabsf(f[5])) + (fabsf(f[6]) + fabsf(f[7]))));
+    }
+    // every lane of the warp calls it
+    __device__ __forceinline__ void flush(double *acc) {
+        double d = static_cast<double>(s) + static_cast<double>(c);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
+        if ((threadIdx.x & 31) == 0) atomicAdd(acc, d);
+    }
+};
+
 // rows, flat: every output group of every row, numbered g = row * G + j over
 // the whole [R, G] output, kFlatUnroll per thread in flight. Group j < Gf
 // holds elements 8j..8j+7 of the row and is read with VB-byte vectors (rows
@@ -199,11 +225,13 @@ __device__ __forceinline__ void store_masks(uint8_t *dst, uint32_t P0, uint32_t 
 // Consecutive threads take consecutive groups: contiguous loads and stores.
 constexpr int kFlatUnroll = 4;
 
-template <typename T, int CODE, bool COLBIAS, int VB>
+template <typename T, int CODE, bool COLBIAS, int VB, bool SUM = false>
 __global__ void __launch_bounds__(kPackThreads)
 pack_rows_flat_kernel(const T *__restrict__ x, uint32_t total, FastDiv divG, uint32_t Gf, int K,
-                      const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out) {
+                      const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out,
+                      double *__restrict__ abs_sum = nullptr) {
     constexpr int OB = GroupOut<CODE>::kBytes;
+    AbsSum asum;
     pdl_launch_dependents();
     pdl_wait();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
@@ -233,13 +261,16 @@ pack_rows_flat_kernel(const T *__restrict__ x, uint32_t total, FastDiv divG, uin
                     const T *xr = x + static_cast<int64_t>(row[u]) * K;
                     for (int e = 0; e < K - k0; ++e) {
                         const float b = COLBIAS ? __ldg(bias + k0 + e) : bs;
-                        neg |= is_negative(Elem<T>::to_f32(xr[k0 + e]), b) << e;
+                        const float v = Elem<T>::to_f32(xr[k0 + e]);
+                        neg |= is_negative(v, b) << e;
                         valid |= 1u << e;
+                        if constexpr (SUM) asum.add(fabsf(v));
                     }
                 }
                 store_group<CODE>(dst, neg, valid);             // (or row padding: code 0)
                 continue;
             }
+            if constexpr (SUM) asum.add_group(grp[u]);
             uint32_t P0, P1;
             if (!COLBIAS && finite) {
                 masks_ge<T>(grp[u], -bs, P0, P1);
@@ -260,6 +291,7 @@ pack_rows_flat_kernel(const T *__restrict__ x, uint32_t total, FastDiv divG, uin
             store_masks<CODE>(dst, P0, P1);
         }
     }
+    if constexpr (SUM) asum.flush(abs_sum);
 }
 
 // rows: one thread per group of 8 consecutive elements of a row, kGroupsPerThread
@@ -547,11 +579,13 @@ __device__ __forceinline__ uint32_t exchange_bits(uint32_t w, int lane) {
     return (lane & L) ? ((w & ~M) | ((t >> R) & M)) : ((w & M) | ((t & M) << R));
 }
 
-template <typename T, int CODE>
+template <typename T, int CODE, bool SUM = false>
 __global__ void __launch_bounds__(kPackThreads)
 pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, FastDiv div_npb, FastDiv div_ncg,
-                      const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out, int rb) {
+                      const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out, int rb,
+                      double *__restrict__ abs_sum = nullptr) {
     constexpr int OB = Group32<CODE>::kBytes;
+    AbsSum asum;
     const int lane = threadIdx.x & 31;
     const uint32_t warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -591,6 +625,7 @@ pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
         for (int k = 0; k < 4; ++k) {
             const int c = cg * 32 + 8 * k + (lane >> 2);
             if (c < C && nvalid_px > 0) {
+                if constexpr (SUM) asum.add_group(g[k]);         // zeros past HW add nothing
                 const float bc = bias_len > 1 ? __ldg(bias + c) : bs;
                 uint32_t P0, P1;
                 if (isfinite(bc)) {
@@ -640,6 +675,7 @@ pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
             *reinterpret_cast<uint4 *>(dst + 16) = make_uint4(q[4], q[5], q[6], q[7]);
         }
     }
+    if constexpr (SUM) asum.flush(abs_sum);
 }
 
 // nhwc, transposed through shared memory. A unit is (image b, a run of
@@ -1025,7 +1061,7 @@ int grid_for(int64_t threads) {
 
 template <typename T, int CODE>
 cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t bias_len, uint8_t *out,
-                   int64_t rb, cudaStream_t s) {
+                   int64_t rb, cudaStream_t s, double *abs_sum = nullptr) {
     const int64_t G = padded_elems<CODE>(rb) / 8;
     const int64_t per_block = kRowThreads * kGroupsPerThread;
     dim3 grid(static_cast<unsigned>((G + per_block - 1) / per_block), static_cast<unsigned>(R < 65535 ? R : 65535));
@@ -1049,12 +1085,29 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
         const uint32_t Gf = static_cast<uint32_t>(K / 8);
         const uint32_t tot = static_cast<uint32_t>(total);
         const int k = static_cast<int>(K), bl = static_cast<int>(bias_len);
+        if (abs_sum != nullptr) {
+            // the same, adding the sum of |x| to *abs_sum
+            if (vec)
+                return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 16, true>, x, tot, divG, Gf,
+                                                    k, bias, bl, out, abs_sum)
+                               : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 16, true>, x, tot, divG, Gf,
+                                                    k, bias, bl, out, abs_sum);
+            return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 8, true>, x, tot, divG, Gf, k,
+                                                bias, bl, out, abs_sum)
+                           : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 8, true>, x, tot, divG, Gf,
+                                                k, bias, bl, out, abs_sum);
+        }
         if (vec)
-            return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 16>, x, tot, divG, Gf, k, bias, bl, out)
-                           : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 16>, x, tot, divG, Gf, k, bias, bl, out);
-        return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 8>, x, tot, divG, Gf, k, bias, bl, out)
-                       : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 8>, x, tot, divG, Gf, k, bias, bl, out);
+            return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 16>, x, tot, divG, Gf, k, bias, bl, out,
+                                                static_cast<double *>(nullptr))
+                           : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 16>, x, tot, divG, Gf, k, bias, bl, out,
+                                                static_cast<double *>(nullptr));
+        return colbias ? cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, true, 8>, x, tot, divG, Gf, k, bias, bl, out,
+                                                static_cast<double *>(nullptr))
+                       : cudaLaunchKernelEx(&cfg, pack_rows_flat_kernel<T, CODE, false, 8>, x, tot, divG, Gf, k, bias, bl, out,
+                                                static_cast<double *>(nullptr));
     }
+    if (abs_sum != nullptr) return cudaErrorNotSupported;
     unsigned int *err = device_error_word();
     if (vec && err != nullptr) {
         auto kern = pack_rows_staged_kernel<T, CODE>;
@@ -1094,10 +1147,10 @@ cudaError_t rows_t(const T *x, int64_t R, int64_t K, const float *bias, int64_t 
 
 template <typename T, int CODE>
 cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bias, int64_t bias_len,
-                   uint8_t *out, int64_t rb, cudaStream_t s) {
+                   uint8_t *out, int64_t rb, cudaStream_t s, double *abs_sum = nullptr) {
     constexpr int E = Elem<T>::kPerVec;
     const bool vec = ((HW * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned(x, 16);
-    if (vec && HW < (int64_t(1) << 30) && C < (int64_t(1) << 30) && !nhwc_warp_disabled()) {
+    if (vec && HW < (int64_t(1) << 30) && C < (int64_t(1) << 30) && (abs_sum != nullptr || !nhwc_warp_disabled())) {
         // warp-level units of 32 channels x 256 pixels
         const int64_t npb = (HW + kWarpPackPixels - 1) / kWarpPackPixels, ncg = rb / Group32<CODE>::kBytes;
         const int64_t units = B * npb * ncg;
@@ -1108,12 +1161,19 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
             int64_t blocks = (units + per_block - 1) / per_block;
             if (blocks > cap) blocks = cap;
             if (blocks < 1) blocks = 1;
+            if (abs_sum != nullptr)
+                return launch_pdl(pack_nhwc_warp_kernel<T, CODE, true>, dim3(static_cast<unsigned>(blocks)),
+                                  dim3(kPackThreads), s, x, static_cast<int>(C), static_cast<int>(HW),
+                                  static_cast<uint32_t>(units), make_fastdiv(static_cast<uint32_t>(npb)),
+                                  make_fastdiv(static_cast<uint32_t>(ncg)), bias, static_cast<int>(bias_len), out,
+                                  static_cast<int>(rb), abs_sum);
             return launch_pdl(pack_nhwc_warp_kernel<T, CODE>, dim3(static_cast<unsigned>(blocks)), dim3(kPackThreads),
                               s, x, static_cast<int>(C), static_cast<int>(HW), static_cast<uint32_t>(units),
                               make_fastdiv(static_cast<uint32_t>(npb)), make_fastdiv(static_cast<uint32_t>(ncg)), bias,
-                              static_cast<int>(bias_len), out, static_cast<int>(rb));
+                              static_cast<int>(bias_len), out, static_cast<int>(rb), static_cast<double *>(nullptr));
         }
     }
+    if (abs_sum != nullptr) return cudaErrorNotSupported;
     const int smem = kNhwcGroups * nhwc_cstride(static_cast<int>(C));
     const int64_t upi = (HW + kNhwcPixels - 1) / kNhwcPixels;
     const int64_t G = padded_elems<CODE>(rb) / 8;
@@ -1155,25 +1215,25 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
 
 template <typename T>
 cudaError_t rows_code(const T *x, int64_t R, int64_t K, const float *bias, int64_t bias_len, bt_code code,
-                      void *out, cudaStream_t s) {
+                      void *out, cudaStream_t s, double *abs_sum = nullptr) {
     uint8_t *o = static_cast<uint8_t *>(out);
     const int64_t rb = row_bytes(K, code);
     switch (code) {
-        case BT_CODE_BITS: return rows_t<T, BT_CODE_BITS>(x, R, K, bias, bias_len, o, rb, s);
-        case BT_CODE_E4M3: return rows_t<T, BT_CODE_E4M3>(x, R, K, bias, bias_len, o, rb, s);
-        default: return rows_t<T, BT_CODE_E2M1>(x, R, K, bias, bias_len, o, rb, s);
+        case BT_CODE_BITS: return rows_t<T, BT_CODE_BITS>(x, R, K, bias, bias_len, o, rb, s, abs_sum);
+        case BT_CODE_E4M3: return rows_t<T, BT_CODE_E4M3>(x, R, K, bias, bias_len, o, rb, s, abs_sum);
+        default: return rows_t<T, BT_CODE_E2M1>(x, R, K, bias, bias_len, o, rb, s, abs_sum);
     }
 }
 
 template <typename T>
 cudaError_t nhwc_code(const T *x, int64_t B, int64_t C, int64_t HW, const float *bias, int64_t bias_len,
-                      bt_code code, void *out, cudaStream_t s) {
+                      bt_code code, void *out, cudaStream_t s, double *abs_sum = nullptr) {
     uint8_t *o = static_cast<uint8_t *>(out);
     const int64_t rb = row_bytes(C, code);
     switch (code) {
-        case BT_CODE_BITS: return nhwc_t<T, BT_CODE_BITS>(x, B, C, HW, bias, bias_len, o, rb, s);
-        case BT_CODE_E4M3: return nhwc_t<T, BT_CODE_E4M3>(x, B, C, HW, bias, bias_len, o, rb, s);
-        default: return nhwc_t<T, BT_CODE_E2M1>(x, B, C, HW, bias, bias_len, o, rb, s);
+        case BT_CODE_BITS: return nhwc_t<T, BT_CODE_BITS>(x, B, C, HW, bias, bias_len, o, rb, s, abs_sum);
+        case BT_CODE_E4M3: return nhwc_t<T, BT_CODE_E4M3>(x, B, C, HW, bias, bias_len, o, rb, s, abs_sum);
+        default: return nhwc_t<T, BT_CODE_E2M1>(x, B, C, HW, bias, bias_len, o, rb, s, abs_sum);
     }
 }
 
@@ -1186,6 +1246,17 @@ cudaError_t launch_pack_rows(const void *x, bt_dtype xt, int64_t R, int64_t K, c
         case BT_F32: return rows_code(static_cast<const float *>(x), R, K, bias, bias_len, code, out, s);
         case BT_BF16: return rows_code(static_cast<const __nv_bfloat16 *>(x), R, K, bias, bias_len, code, out, s);
         default: return rows_code(static_cast<const __half *>(x), R, K, bias, bias_len, code, out, s);
+    }
+}
+
+cudaError_t launch_pack_rows_sum(const void *x, bt_dtype xt, int64_t R, int64_t K, const float *bias,
+                                 int64_t bias_len, bt_code code, void *out, double *abs_sum, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    switch (xt) {
+        case BT_F32: return rows_code(static_cast<const float *>(x), R, K, bias, bias_len, code, out, s, abs_sum);
+        case BT_BF16:
+            return rows_code(static_cast<const __nv_bfloat16 *>(x), R, K, bias, bias_len, code, out, s, abs_sum);
+        default: return rows_code(static_cast<const __half *>(x), R, K, bias, bias_len, code, out, s, abs_sum);
     }
 }
 
@@ -1402,6 +1473,17 @@ cudaError_t launch_pack_nhwc(const void *x, bt_dtype xt, int64_t B, int64_t C, i
         case BT_F32: return nhwc_code(static_cast<const float *>(x), B, C, HW, bias, bias_len, code, out, s);
         case BT_BF16: return nhwc_code(static_cast<const __nv_bfloat16 *>(x), B, C, HW, bias, bias_len, code, out, s);
         default: return nhwc_code(static_cast<const __half *>(x), B, C, HW, bias, bias_len, code, out, s);
+    }
+}
+
+cudaError_t launch_pack_nhwc_sum(const void *x, bt_dtype xt, int64_t B, int64_t C, int64_t HW, const float *bias,
+                                 int64_t bias_len, bt_code code, void *out, double *abs_sum, cudaStream_t s) {
+    if (B == 0) return cudaSuccess;
+    switch (xt) {
+        case BT_F32: return nhwc_code(static_cast<const float *>(x), B, C, HW, bias, bias_len, code, out, s, abs_sum);
+        case BT_BF16:
+            return nhwc_code(static_cast<const __nv_bfloat16 *>(x), B, C, HW, bias, bias_len, code, out, s, abs_sum);
+        default: return nhwc_code(static_cast<const __half *>(x), B, C, HW, bias, bias_len, code, out, s, abs_sum);
     }
 }
 

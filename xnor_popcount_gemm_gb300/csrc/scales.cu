@@ -81,8 +81,41 @@ __global__ void finish_kernel(const double *__restrict__ acc, int64_t n, float f
 }
 
 __device__ double g_abs_sum[128];
+__device__ double g_abs_sum_fused;
 
 }  // namespace
+
+// Accumulator of the forwards that initialise scale_a while they pack x (one
+// per CUDA context), as seen from the current context.
+double *fused_abs_sum_accumulator(cudaError_t *err) {
+    static SymbolAddressCache cache;
+    return static_cast<double *>(cache.get([](void **p) { return cudaGetSymbolAddress(p, g_abs_sum_fused); }, err));
+}
+
+cudaError_t launch_abs_sum(const void *x, bt_dtype x_dtype, int64_t n, double *acc, cudaStream_t s) {
+    int64_t blocks = (n + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    switch (x_dtype) {
+        case BT_F32:
+            return launch_pdl(abs_sum_kernel<float>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), s,
+                              static_cast<const float *>(x), n, acc);
+        case BT_F16:
+            return launch_pdl(abs_sum_kernel<__half>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), s,
+                              static_cast<const __half *>(x), n, acc);
+        default:
+            return launch_pdl(abs_sum_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), s,
+                              static_cast<const __nv_bfloat16 *>(x), n, acc);
+    }
+}
+
+cudaError_t launch_scale_finish(const double *acc, int64_t n, float factor, bt_dtype x_dtype, bt_dtype scale_dtype,
+                                float *scale_out, cudaStream_t s) {
+    return launch_pdl(finish_kernel, dim3(1), dim3(1), s, acc, n, factor, static_cast<int>(x_dtype),
+                      static_cast<int>(scale_dtype), scale_out);
+}
+
 }  // namespace bt
 
 using namespace bt;

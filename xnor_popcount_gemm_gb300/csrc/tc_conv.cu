@@ -318,17 +318,6 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const int ot = t % a.num_ot, rest = t / a.num_ot;
                 const int b = rest / a.bands, band = rest - b * a.bands;
                 const int r0 = band * a.ht;
-                // the weights: once (resident), or the tile's slices through the ring
-                if (a.a_resident) {
-                    if (!a_loaded) {
-                        tc::mbar_arrive_expect_tx(afull(0), static_cast<uint32_t>(a.a_boxes * a.a_d) * kASlice);
-                        for (int i = 0; i < a.a_boxes; ++i)
-                            tc::tma_load_3d(sA + static_cast<uint32_t>(i * a.a_d) * kASlice, &tmA, 0, ot * kBM,
-                                            i * a.a_d, afull(0));
-                        a_last[0] = 0u;
-                        a_loaded = true;
-                    }
-                }
                 // the tile's phase images
                 if (!tc::wait_bounded(bempty(bs), bph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                 tc::mbar_arrive_expect_tx(bfull(bs), static_cast<uint32_t>(a.nph * a.nsl) * a.img_tx);
@@ -339,6 +328,24 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                     a.ph_x0[ph], a.stride * r0 + a.ph_y0[ph], b, bfull(bs));
                 b_last[bs] = bph;
                 if (++bs == a.b_stages) { bs = 0; bph ^= 1u; }
+                // resident weights: after the first tile's pixels, one barrier per
+                // box (up to kMaxAStages boxes; more share the first barrier), so
+                // that the first MMAs start once their taps have landed
+                if (a.a_resident && !a_loaded) {
+                    const bool per_box = a.a_boxes <= kMaxAStages;
+                    if (!per_box)
+                        tc::mbar_arrive_expect_tx(afull(0), static_cast<uint32_t>(a.a_boxes * a.a_d) * kASlice);
+                    for (int i = 0; i < a.a_boxes; ++i) {
+                        if (per_box) {
+                            tc::mbar_arrive_expect_tx(afull(i), static_cast<uint32_t>(a.a_d) * kASlice);
+                            a_last[i] = 0u;
+                        }
+                        tc::tma_load_3d(sA + static_cast<uint32_t>(i * a.a_d) * kASlice, &tmA, 0, ot * kBM,
+                                        i * a.a_d, afull(per_box ? i : 0));
+                    }
+                    if (!per_box) a_last[0] = 0u;
+                    a_loaded = true;
+                }
                 if (!a.a_resident) {
                     for (int i0 = 0; i0 < nslices; i0 += a.a_d) {
                         if (!tc::wait_bounded(aempty(as), aph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
@@ -375,42 +382,55 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         break;
                     tc::fence_after_sync();
                 }
-                if (a.a_resident && local == 0) {
-                    if (!tc::wait_bounded(afull(0), 0u, abort_flag, a.err, a.wait_ns)) break;
-                }
                 if (!tc::wait_bounded(bfull(bs), bph, abort_flag, a.err, a.wait_ns)) break;
                 tc::fence_after_sync();
                 const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * kAccStride;
-                const uint32_t bstage = sB + static_cast<uint32_t>(bs) * a.stage_bytes;
-                uint32_t abase = sA;
-                for (int idx = 0; idx < nslices; ++idx) {
-                    const int tp = idx / a.nsl, sl = idx - tp * a.nsl;
-                    uint32_t aaddr;
-                    if (a.a_resident) {
-                        aaddr = sA + static_cast<uint32_t>(idx) * kASlice;
-                    } else {
-                        const int within = idx % a.a_d;
-                        if (within == 0) {
-                            if (!tc::wait_bounded(afull(as), aph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
-                            tc::fence_after_sync();
-                            abase = sA + static_cast<uint32_t>(as * a.a_d) * kASlice;
-                        }
-                        aaddr = abase + static_cast<uint32_t>(within) * kASlice;
-                    }
+                // descriptors are built once and moved by adding (byte offset >> 4)
+                // to their start-address field (shared-memory addresses stay below
+                // 256 KB, so the 14-bit field never carries): the issuing thread
+                // spends a few integer adds per MMA, not a descriptor build
+                const uint64_t bdesc_stage = kmajor_desc(sB + static_cast<uint32_t>(bs) * a.stage_bytes, SW);
+                const uint64_t adesc_base = kmajor_desc(sA, SW);
+                const uint32_t img16 = a.img_bytes >> 4;
+                constexpr uint32_t kSlice16 = kASlice >> 4;
+                uint64_t adesc = adesc_base;
+                int idx = 0, within = 0, box = 0;
+                for (int tp = 0; tp < a.ntap && ok; ++tp) {
                     const uint32_t tapw = a.tap[tp];
-                    const uint32_t baddr = bstage + ((tapw >> 24) * static_cast<uint32_t>(a.nsl) + sl) * a.img_bytes +
-                                           (tapw & 0xFFFFFFu) * SW;
+                    uint64_t bd = bdesc_stage + (tapw >> 24) * static_cast<uint32_t>(a.nsl) * img16 +
+                                  (tapw & 0xFFFFFFu) * (SW >> 4);
+                    for (int sl = 0; sl < a.nsl; ++sl, ++idx) {
+                        if (within == 0) {
+                            if (a.a_resident) {
+                                // first tile: each box of weights on its own barrier (or all on the first)
+                                if (local == 0 && (a.a_boxes <= kMaxAStages || idx == 0)) {
+                                    if (!tc::wait_bounded(afull(a.a_boxes <= kMaxAStages ? box : 0), 0u, abort_flag, a.err,
+                                                          a.wait_ns)) { ok = false; break; }
+                                    tc::fence_after_sync();
+                                }
+                                adesc = adesc_base + static_cast<uint64_t>(idx) * kSlice16;
+                            } else {
+                                if (!tc::wait_bounded(afull(as), aph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                                tc::fence_after_sync();
+                                adesc = adesc_base + static_cast<uint64_t>(as * a.a_d) * kSlice16;
+                            }
+                        }
 #pragma unroll
-                    for (int kk = 0; kk < kMmaPerSlice; ++kk) {
-                        const uint64_t ad = kmajor_desc(aaddr + kk * 32, SW);
-                        const uint64_t bd = kmajor_desc(baddr + kk * 32, SW);
-                        const uint32_t acc = (idx | kk) != 0 ? 1u : 0u;
-                        if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, ad, bd, a.idesc, acc);
-                        else tc::mma_mxf4(dacc, ad, bd, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
-                    }
-                    if (!a.a_resident && (idx % a.a_d == a.a_d - 1 || idx == nslices - 1)) {
-                        tc::mma_commit(aempty(as));
-                        if (++as == a.a_stages) { as = 0; aph ^= 1u; }
+                        for (int kk = 0; kk < kMmaPerSlice; ++kk) {
+                            const uint32_t acc = (idx | kk) != 0 ? 1u : 0u;
+                            if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, adesc + 2 * kk, bd + 2 * kk, a.idesc, acc);
+                            else tc::mma_mxf4(dacc, adesc + 2 * kk, bd + 2 * kk, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+                        }
+                        adesc += kSlice16;
+                        bd += img16;
+                        if (++within == a.a_d) {
+                            within = 0;
+                            ++box;
+                            if (!a.a_resident) {
+                                tc::mma_commit(aempty(as));
+                                if (++as == a.a_stages) { as = 0; aph ^= 1u; }
+                            }
+                        }
                     }
                 }
                 if (!ok) break;
