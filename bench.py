@@ -247,6 +247,7 @@ class ForwardSetup:
         self.nbuf = max(1, -(-2 * L2_BYTES // (self.x_bytes + self.out_bytes)))
         self.xs = [wl.x.to(dev) for _ in range(self.nbuf)]
         self.single_pass = False
+        self.fused = False
         self.ws_rows = None
         if wl.kind == "linear":
             self.outs = [torch.empty((M, N), dtype=self.out_t, device=dev) for _ in range(self.nbuf)]
@@ -264,11 +265,16 @@ class ForwardSetup:
             geom = (B, C, H, W, k, wl.stride, wl.padding, wl.dilation)
             self.ws = torch.empty(max(1, bt.bt_binary_conv2d_workspace(*geom, bt.BT_BF16, code)), dtype=torch.uint8,
                                   device=dev)
-            # the two public calls that split the library's own path for this shape
-            self.single_pass = bool(bt.bt_conv2d_single_pass(
+            # the public calls that split the library's own path for this shape:
+            # one call on x (the convolution packs x itself), or pack + contraction
+            mode = bt.bt_conv2d_single_pass(
                 *geom, {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16, torch.float16: bt.BT_F16}[wl.x.dtype],
-                code))
-            if not self.single_pass:
+                code)
+            self.fused = mode == 2
+            self.single_pass = mode == 1
+            if self.fused:
+                xp_shape = (1,)
+            elif not self.single_pass:
                 # packed NHWC pixels; the contraction call unfolds them (where it
                 # needs rows) or contracts them in place
                 xp_shape = (B, H, W, bt.bt_packed_row_bytes(C, code))
@@ -281,7 +287,7 @@ class ForwardSetup:
         # kernels per step: the pack, then the contraction; a contraction call
         # that unfolds packed pixels into rows first adds one
         unfolds = wl.kind == "conv" and not self.single_pass and self.ws_rows is not None
-        self.launches_per_step = 3 if unfolds else 2
+        self.launches_per_step = 1 if self.fused else (3 if unfolds else 2)
 
     def step(self, i, ev=None):
         bt, wl = self.bt, self.wl
@@ -290,6 +296,8 @@ class ForwardSetup:
             ev[0].record(torch.cuda.current_stream())
         if wl.kind == "linear":
             bt.bt_pack_sign(x, self.code, bt.BT_LAYOUT_ROWS, self.bias, out=self.xp)
+        elif self.fused:
+            pass                                  # the convolution call packs x itself
         elif not self.single_pass:
             bt.bt_pack_sign(x, self.code, bt.BT_LAYOUT_NCHW_TO_NHWC, self.bias, out=self.xp)
         else:
@@ -299,6 +307,9 @@ class ForwardSetup:
         if wl.kind == "linear":
             bt.bt_binary_linear(self.xp, self.wp, self.code, self.K, wl.scale_a, wl.scale_w, out=out,
                                 out_dtype=self.out_t, algo=self.algo, x_packed=True)
+        elif self.fused:
+            bt.bt_binary_conv2d(x, self.wp, self.code, self.C, self.k, wl.stride, wl.padding, wl.dilation,
+                                wl.scale_a, wl.scale_w, self.bias, out=out, out_dtype=self.out_t, algo=self.algo)
         elif not self.single_pass:
             bt.bt_binary_conv2d(self.xp, self.wp, self.code, self.C, self.k, wl.stride, wl.padding, wl.dilation,
                                 wl.scale_a, wl.scale_w, out=out, out_dtype=self.out_t, algo=self.algo,
@@ -369,7 +380,8 @@ def step_bytes(wl) -> float:
 def contraction_bytes(wl, code, bt) -> float:
     """Least bytes the contraction call moves: the packed activations (rows of
     a linear layer; the packed pixels of a convolution, each read once by an
-    implicit im2col), the packed weights, the output."""
+    implicit im2col; x itself where the convolution packs it), the packed
+    weights, the output."""
     out_b = 4 if wl.out_dtype == "f32" else 2
     if wl.kind == "linear":
         M, K = wl.x.shape
@@ -381,7 +393,18 @@ def contraction_bytes(wl, code, bt) -> float:
     Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
     Wo = bt.conv2d_out_size(W, k, wl.stride, wl.padding, wl.dilation)
     rbc = bt.bt_packed_row_bytes(C, code)
+    if conv_mode(wl, code, bt) == 2:
+        return wl.x.numel() * wl.x.element_size() + O * k * k * rbc + B * O * Ho * Wo * out_b
     return B * H * W * rbc + O * k * k * rbc + B * O * Ho * Wo * out_b
+
+
+def conv_mode(wl, code, bt) -> int:
+    """bt_conv2d_single_pass for the workload's convolution: 2 one kernel from
+    x, 1 one-pass im2col rows + contraction, 0 NHWC pack + contraction."""
+    B, C, H, W = wl.x.shape
+    k = wl.w.shape[2]
+    dt = {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16, torch.float16: bt.BT_F16}[wl.x.dtype]
+    return bt.bt_conv2d_single_pass(B, C, H, W, k, wl.stride, wl.padding, wl.dilation, dt, code)
 
 
 def roofline_of(ops: float, nbytes: float, ms: float, algo_name: str, peaks: dict, sms: int) -> dict:
@@ -534,9 +557,10 @@ def run_ours(args, rank, world):
                       "how": "second pass of the same steps, CUDA events around each call on its stream"},
         "roofline": roof,
         "step_roofline": roofline_of(ops, step_bytes(wl), ms_step, algo_name, peaks, sms),
-        "pack_roofline": {"bound": "hbm", "achieved": round(pack_b / (pack_ms / 1e3) / 1e9, 1),
-                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": round(pack_b / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "pack_roofline": ({"bound": "hbm", "achieved": round(pack_b / (pack_ms / 1e3) / 1e9, 1),
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(pack_b / (pack_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
+                          if pack_b > 0 else "none: the convolution kernel packs x itself"),
         "e2e": {"value": round(ops * world / (e2e_ms / 1e3) / 1e9, 1), "unit": "GOPS",
                 "h2d_bytes_per_step": int(su.x_bytes), "d2h_bytes_per_step": int(su.out_bytes),
                 "ms_per_step": round(e2e_ms, 4),
@@ -636,8 +660,10 @@ def pack_bytes(wl, code, bt):
         return wl.x.numel() * wl.x.element_size() + M * bt.bt_packed_row_bytes(K, code)
     B, C, H, W = wl.x.shape
     k = wl.w.shape[2]
-    dt = {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16, torch.float16: bt.BT_F16}[wl.x.dtype]
-    if not bt.bt_conv2d_single_pass(B, C, H, W, k, wl.stride, wl.padding, wl.dilation, dt, code):
+    mode = conv_mode(wl, code, bt)
+    if mode == 2:
+        return 0.0                              # no pack call: the convolution packs x itself
+    if mode == 0:
         return wl.x.numel() * wl.x.element_size() + B * H * W * bt.bt_packed_row_bytes(C, code)
     # one pass: x read once, the im2col rows written
     Ho = bt.conv2d_out_size(H, k, wl.stride, wl.padding, wl.dilation)
@@ -647,10 +673,10 @@ def pack_bytes(wl, code, bt):
 
 def kernel_source_hash(kind: str = "linear") -> str:
     """First 16 hex digits of the sha256 of the contraction kernel's sources:
-    tc_gemm.cu (linear) or tc_conv.cu (implicit-im2col convolution), then
-    tc_ptx.cuh."""
+    tc_gemm.cu then tc_ptx.cuh (linear); tc_conv.cu, tc_ptx.cuh, then
+    sign_pack.cuh (implicit-im2col convolution)."""
     h = hashlib.sha256()
-    for f in ("tc_gemm.cu" if kind == "linear" else "tc_conv.cu", "tc_ptx.cuh"):
+    for f in ("tc_gemm.cu", "tc_ptx.cuh") if kind == "linear" else ("tc_conv.cu", "tc_ptx.cuh", "sign_pack.cuh"):
         with open(os.path.join(ROOT, "xnor_popcount_gemm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

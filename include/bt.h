@@ -162,13 +162,24 @@ bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, 
                          const float *bias, int64_t bias_len, bt_code code, void *out, bt_stream stream);
 
 /*
- * bt_conv2d_single_pass -- 1 when bt_binary_conv2d, given a 16-byte aligned
- * float x of this geometry and a tensor-core code, builds the im2col rows in
- * one pass from x (the staged form of bt_pack_im2col); 0 when it packs the
- * pixels to NHWC and unfolds them in a second kernel (or for BITS, or invalid
- * arguments). Either way the result is the same; this tells a caller which two
- * public calls split the same work (bt_pack_im2col + BT_PACKED_IM2COL, or
- * bt_pack_sign NCHW_TO_NHWC + BT_PACKED).
+ * bt_conv2d_single_pass -- how bt_binary_conv2d, given a 16-byte aligned float
+ * x of this geometry and a tensor-core code, splits its own work:
+ *   2  one kernel from x: the tensor-core convolution packs x itself (shift,
+ *      sign, channel packing into its shared-memory pixel stages) and needs
+ *      no workspace -- where the implicit-im2col plan applies, every channel
+ *      plane (H * W values of x_dtype) is a multiple of 16 bytes and the
+ *      environment sets BT_CONV_FUSED=1 (slower than route 0 on the ResNet
+ *      layers measured, so not the default);
+ *   1  the im2col rows built in one pass from x (the staged form of
+ *      bt_pack_im2col), then the contraction of those rows;
+ *   0  the pixels packed to NHWC (bt_pack_sign NCHW_TO_NHWC), then the
+ *      contraction of the packed pixels (in place, or after an unfold); also
+ *      for BITS and for invalid arguments.
+ * The result is the same on every route; this tells a caller which public
+ * calls reproduce the library's own launches (the one call on float x; or
+ * bt_pack_im2col + BT_PACKED_IM2COL; or bt_pack_sign + BT_PACKED).
+ * (BinaryConv2dForward.forward of bitorch-engine's layer module is one native
+ * call from x to the scaled output.)
  */
 int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel_size, int stride,
                           int padding, int dilation, bt_dtype x_dtype, bt_code code);

@@ -182,14 +182,23 @@ def test_conv_im2col_input_validation():
     assert bt.bt_binary_conv2d_workspace(2, 64, 8, 8, 3, 1, 1, 1, bt.BT_PACKED_IM2COL, bt.BT_CODE_E2M1) == 0
 
 
-def test_conv2d_single_pass_query():
+def test_conv2d_single_pass_query(monkeypatch):
     q = bt.bt_conv2d_single_pass
     geom = (2, 64, 16, 16, 3, 1, 1, 1)
-    assert q(*geom, bt.BT_F32, bt.BT_CODE_BITS) is False            # popcount convs contract NHWC pixels
-    assert q(*geom, bt.BT_PACKED, bt.BT_CODE_E2M1) is False         # already packed
-    assert q(0, 64, 16, 16, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) is False
-    assert q(2, 64, 1, 1, 3, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) is False   # window larger than the image
-    assert q(2, 2000, 16, 16, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) is False  # K beyond the tensor-core limit
+    assert q(*geom, bt.BT_F32, bt.BT_CODE_BITS) == 0                # popcount convs contract NHWC pixels
+    assert q(*geom, bt.BT_PACKED, bt.BT_CODE_E2M1) == 0             # already packed
+    assert q(0, 64, 16, 16, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
+    assert q(2, 64, 1, 1, 3, 1, 0, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0   # window larger than the image
+    assert q(2, 2000, 16, 16, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0  # K beyond the tensor-core limit
+    # one kernel from x (opt-in) where the implicit plan applies and the
+    # channel planes are whole 16-byte units; else the NHWC pack runs first
+    assert q(*geom, bt.BT_BF16, bt.BT_CODE_E2M1) == 0
+    monkeypatch.setenv("BT_CONV_FUSED", "1")
+    for code in (bt.BT_CODE_E2M1, bt.BT_CODE_E4M3):
+        assert q(*geom, bt.BT_F32, code) == 2
+        assert q(*geom, bt.BT_BF16, code) == 2
+        assert q(2, 64, 14, 14, 3, 1, 1, 1, bt.BT_BF16, code) == 0     # 392-byte planes
+        assert q(2, 64, 14, 14, 3, 1, 1, 1, bt.BT_F32, code) == 2      # 784-byte planes
 
 
 def test_pack_validation():

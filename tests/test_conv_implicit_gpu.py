@@ -9,7 +9,9 @@ strides 1 and 2 with every padding/dilation phase pattern, one and many
 bands of output rows per image, channel counts that are not a multiple of the
 128-channel tile, weights kept resident and weights streamed per tile, and
 inputs smaller than one staged image. The explicit unfold
-(BT_CONV_IMPLICIT=0) stays under test beside it.
+(BT_CONV_IMPLICIT=0) stays under test beside it. Float inputs take the route
+through the NHWC pack kernel here (BT_CONV_FUSED=0); the convolution that
+packs x itself has its own tests.
 """
 import numpy as np
 import pytest
@@ -74,9 +76,14 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["pair", "single"])
 @pytest.mark.parametrize("code", TC_CODES, ids=TC_IDS)
 @pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", SHAPES)
-def test_implicit_conv_matches_oracle(code, B, C, H, W, O, k, s, p, d):
+def test_implicit_conv_matches_oracle(code, B, C, H, W, O, k, s, p, d, pair, monkeypatch):
+    # pair: clusters of two CTAs, 256-channel tiles, half of a band's rows per
+    # CTA (where that plan fits); single: one CTA per 128-channel tile
+    monkeypatch.setenv("BT_CONV_FUSED", "0")
+    monkeypatch.setenv("BT_CONV_PAIR", pair)
     assert _implicit(B, C, H, W, k, s, p, d, code)
     x = _gen(B * 7 + C + H, (B, C, H, W), torch.bfloat16)
     w = _gen(O + k + C, (O, C, k, k), torch.bfloat16)
@@ -124,13 +131,18 @@ def test_implicit_conv_extreme_sums(code):
     assert int(got.abs().max()) == C * k * k
 
 
-def test_single_pass_query_follows_the_implicit_path():
+def test_single_pass_query_follows_the_implicit_path(monkeypatch):
     # where the contraction reads packed pixels in place, the library's own
-    # split is pack (NHWC) + contraction, never the one-pass unfold
+    # split is pack (NHWC) + contraction (or, opted in, one kernel from x with
+    # 16-byte channel planes), never the one-pass unfold
     for (B, C, H, W, k, s, p, d) in ((256, 128, 28, 28, 3, 2, 1, 1), (128, 256, 14, 14, 3, 1, 1, 1)):
         for code in TC_CODES:
             assert _implicit(B, C, H, W, k, s, p, d, code)
-            assert not bt.bt_conv2d_single_pass(B, C, H, W, k, s, p, d, bt.BT_BF16, code)
+            assert bt.bt_conv2d_single_pass(B, C, H, W, k, s, p, d, bt.BT_BF16, code) == 0
+            fused = (H * W * 2) % 16 == 0
+            monkeypatch.setenv("BT_CONV_FUSED", "1")
+            assert bt.bt_conv2d_single_pass(B, C, H, W, k, s, p, d, bt.BT_BF16, code) == (2 if fused else 0)
+            monkeypatch.delenv("BT_CONV_FUSED")
 
 
 @pytest.mark.parametrize("code", TC_CODES, ids=TC_IDS)

@@ -382,9 +382,15 @@ def test_full_linear_workloads(name, code):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("fused", ["1", "0"], ids=["fused", "two_kernels"])
 @pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
 @pytest.mark.parametrize("name", ["resnet_conv", "downsample_conv", "downsample_conv_d2"])
-def test_full_conv_workloads(name, code):
+def test_full_conv_workloads(name, code, fused, monkeypatch):
+    # float x: one kernel that packs x itself, or (BT_CONV_FUSED=0) the NHWC
+    # pack kernel, then the contraction of the packed pixels
+    if code == bt.BT_CODE_BITS and fused == "0":
+        pytest.skip("the popcount route has one form")
+    monkeypatch.setenv("BT_CONV_FUSED", fused)
     wl = workloads.NAMED[name]()
     B, C, H, W = wl.x.shape
     O, _, k, _ = wl.w.shape
@@ -402,8 +408,9 @@ def test_full_conv_workloads(name, code):
 @pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
 @pytest.mark.parametrize("name", ["resnet_conv", "downsample_conv", "downsample_conv_d2"])
 def test_full_conv_workloads_bench_calls(name, code):
-    """The two public calls the benchmark times (pack, then the contraction of
-    the packed activations), every output against the oracle."""
+    """The public calls the benchmark times (one call on x where the
+    convolution packs x itself; else the pack, then the contraction of the
+    packed activations), every output against the oracle."""
     wl = workloads.NAMED[name]()
     B, C, H, W = wl.x.shape
     O, _, k, _ = wl.w.shape
@@ -412,7 +419,10 @@ def test_full_conv_workloads_bench_calls(name, code):
     geom = (B, C, H, W, k, wl.stride, wl.padding, wl.dilation)
     xt = {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16}[wl.x.dtype]
     args = (code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a, wl.scale_w)
-    if bt.bt_conv2d_single_pass(*geom, xt, code):
+    mode = bt.bt_conv2d_single_pass(*geom, xt, code)
+    if mode == 2:
+        y = bt.bt_binary_conv2d(xd, wp, *args, out_dtype=OUT_T[wl.out_dtype])
+    elif mode == 1:
         rows = bt.bt_pack_im2col(xd, code, k, wl.stride, wl.padding, wl.dilation)
         y = bt.bt_binary_conv2d(rows, wp, *args, out_dtype=OUT_T[wl.out_dtype], x_im2col_hw=(B, H, W))
     else:

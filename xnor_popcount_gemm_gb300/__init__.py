@@ -187,9 +187,10 @@ def bt_pack_im2col(x: torch.Tensor, code: int, kernel_size: int, stride: int, pa
 
 
 def bt_conv2d_single_pass(B: int, C: int, H: int, W: int, kernel_size: int, stride: int, padding: int,
-                          dilation: int, x_dtype: int, code: int) -> bool:
-    """Whether bt_binary_conv2d unfolds x in one pass (as bt_pack_im2col)."""
-    return bool(_c_single_pass(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype, code))
+                          dilation: int, x_dtype: int, code: int) -> int:
+    """How bt_binary_conv2d splits its work on float x: 2 one kernel from x,
+    1 one-pass im2col rows + contraction, 0 NHWC pack + contraction."""
+    return int(_c_single_pass(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype, code))
 
 
 def bt_backward_weight_ld(N: int) -> int:

@@ -307,7 +307,10 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
     const size_t need = bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype,
                                                    w_code);
     const bool implicit = run != BT_ALGO_POPC && x_dtype != BT_PACKED_IM2COL && conv_implicit_applies(g, w_code);
-    const bool needs_ws = float_in(x_dtype) || (x_dtype == BT_PACKED && run != BT_ALGO_POPC && !implicit);
+    // one kernel from x where the contraction can pack its own input
+    const bool fused = implicit && float_in(x_dtype) && conv_fused_applies(g, w_code, x_dtype) &&
+                       (bias_len == 0 || aligned(bias_a, 4));
+    const bool needs_ws = (float_in(x_dtype) && !fused) || (x_dtype == BT_PACKED && run != BT_ALGO_POPC && !implicit);
     if (needs_ws && need == 0) return BT_ERR_UNSUPPORTED;      // beyond the sizes the query serves
     if (needs_ws && (workspace == nullptr || workspace_bytes < need)) return BT_ERR_WORKSPACE;
     if (needs_ws && !aligned(workspace, 256)) return BT_ERR_ALIGNMENT;
@@ -319,6 +322,13 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
     if (x_dtype == BT_PACKED_IM2COL)
         return from_cuda(launch_tc_conv(static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(weight), w_code,
                                         g, alpha, out, out_dtype, err, s, scales));
+    if (fused) {
+        const cudaError_t e = launch_tc_conv_fused(x, x_dtype, bias_len > 0 ? bias_a : nullptr, bias_len,
+                                                   static_cast<const uint8_t *>(weight), w_code, g, alpha, out,
+                                                   out_dtype, err, s, scales);
+        if (e == cudaErrorNotSupported) return BT_ERR_UNSUPPORTED;
+        return from_cuda(e);
+    }
     if (implicit) {
         // pack to channel-packed NHWC pixels (unless given), then the
         // implicit-im2col contraction reads them in place
@@ -434,6 +444,7 @@ int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel
     g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
     g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
     if (g.Ho < 1 || g.Wo < 1) return 0;
+    if (conv_fused_applies(g, code, x_dtype)) return 2;   // one kernel from x
     if (conv_implicit_applies(g, code)) return 0;      // packed pixels, contracted in place
     return unfold_single_pass(g, x_dtype, code) ? 1 : 0;
 }

@@ -199,6 +199,15 @@ bool conv_implicit_applies(const ConvGeom &g, bt_code code);
 cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
                                     void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s,
                                     const float *scales = nullptr);
+// The same convolution reading x itself (NCHW floats of type x_dtype, shifted
+// by bias (bias_len 1 or C; 0: none) and signed by its own packing warps): one
+// kernel, no workspace. It applies where the implicit plan does, every
+// channel plane (H * W values) is a multiple of 16 bytes and BT_CONV_FUSED=1
+// is set in the environment (otherwise the pack kernel runs first).
+bool conv_fused_applies(const ConvGeom &g, bt_code code, bt_dtype x_dtype);
+cudaError_t launch_tc_conv_fused(const void *x, bt_dtype x_dtype, const float *bias, int64_t bias_len,
+                                 const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha, void *out,
+                                 bt_dtype out_t, unsigned int *err, cudaStream_t s, const float *scales = nullptr);
 
 // First-call activation scale (BinaryConv2dCutlass.set_activation): the sum
 // of |x| accumulates in a double per CUDA context (zero it before use; calls
