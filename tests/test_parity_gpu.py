@@ -126,17 +126,22 @@ def test_pack_nhwc_sign_decision_edges(code, dtype):
         np.testing.assert_array_equal(got, want, err_msg=f"shift {bias.tolist()}")
 
 
-@pytest.mark.parametrize("impl", ["warp", "smem"])
+@pytest.mark.parametrize("impl", ["default", "warp", "smem"])
 @pytest.mark.parametrize("code", CODES, ids=CODE_IDS)
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("shape", [(2, 3, 5, 5), (3, 37, 4, 4), (2, 64, 14, 14), (1, 130, 7, 9),
                                    (4, 256, 3, 3), (2, 128, 28, 28), (1, 700, 10, 10), (1, 6200, 3, 3),
-                                   (2, 33, 2, 2), (3, 96, 8, 12)])
+                                   (2, 33, 2, 2), (3, 96, 8, 12), (2, 96, 40, 40)])
 def test_pack_nchw_to_nhwc(code, dtype, shape, impl, monkeypatch):
-    # planes whose bytes are a multiple of 16 take the warp-level kernel (32
-    # pixels x 32 channels per warp) unless BT_PACK_NHWC=smem; the others take
-    # the shared-memory transpose
-    monkeypatch.setenv("BT_PACK_NHWC", impl)
+    # planes whose bytes are a multiple of 16 take a warp-level kernel (32
+    # pixels x 32 channels per warp: for E2M1 the one shared with the
+    # convolution's packing warps, else, and with BT_PACK_NHWC=warp, the
+    # byte-mask one) unless BT_PACK_NHWC=smem; the others take the
+    # shared-memory transpose
+    if impl == "default":
+        monkeypatch.delenv("BT_PACK_NHWC", raising=False)
+    else:
+        monkeypatch.setenv("BT_PACK_NHWC", impl)
     x = _gen(sum(shape), shape, dtype)
     for bias in (None, torch.tensor([-0.1]), torch.linspace(-0.3, 0.3, shape[1])):
         got = bt.bt_pack_sign(x.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC,

@@ -547,6 +547,105 @@ pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
     if constexpr (SUM) asum.flush(abs_sum);
 }
 
+// nhwc, warp-level, E2M1 codes: the same units (32 channels x 32 pixels of
+// one image per warp), converted the way the convolution's packing warps
+// convert them. Lane l loads 8 pixels (16 bytes of a 2-byte type, 32 of f32)
+// of channel 32 cg + 8 k + l / 4 as predicated loads (zeros past C or HW); the
+// sign test x >= t is one comparison per pair of values (t the shift's
+// threshold, per channel or one for all), its bits land at lane bits (c2 c1
+// c0 p4 p3) and register bits (p0 p2 p1 c4 c3); three exchange rounds and one
+// shuffle leave lane p with channel c at bit 4 (c % 8) + c / 8, so the codes
+// of channels 8i..8i+7 are one shift and one logic op. Units are numbered with
+// the channel group fastest, so the warps that run at the same time fill
+// whole packed rows; each warp loads its next unit before it converts the
+// current one.
+template <typename T, bool CHAN>
+__global__ void __launch_bounds__(kPackThreads)
+pack_nhwc_e2m1_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, FastDiv div_ncg, FastDiv div_npb,
+                      const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out, int rb) {
+    constexpr int NV = sizeof(T) == 2 ? 1 : 2;                  // 16-byte loads per 8 pixels
+    const int lane = threadIdx.x & 31;
+    const uint32_t warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int ncg = static_cast<int>(div_ncg.d), npb = static_cast<int>(div_npb.d);
+    const int lc = lane >> 2, lp = 8 * (lane & 3);
+    const int64_t hw8 = static_cast<int64_t>(8) * HW;
+    const uint32_t keep16 = (lane & 16) ? 0xFFFF0000u : 0x0000FFFFu;
+    const uint32_t keep8 = (lane & 8) ? 0xFF00FF00u : 0x00FF00FFu, rot8 = (lane & 8) ? 8u : 24u;
+    const uint32_t keep4 = (lane & 4) ? 0xF0F0F0F0u : 0x0F0F0F0Fu, rot4 = (lane & 4) ? 4u : 28u;
+    const int src_lane = ((lane & 1) << 4) | (((lane >> 2) & 1) << 3) | (((lane >> 1) & 1) << 2) |
+                         (((lane >> 4) & 1) << 1) | ((lane >> 3) & 1);
+    pdl_launch_dependents();
+    pdl_wait();
+    const uint32_t t_all = shift_threshold<T>(bias_len == 1 ? __ldg(bias) : 0.0f);
+    // unit u: channel group cg (fastest), then pixel block blk of image b
+    auto decode = [&](uint32_t u, int &cg, int &b, int &blk) {
+        const uint32_t q = fdiv(u, div_ncg);
+        cg = static_cast<int>(u - q * static_cast<uint32_t>(ncg));
+        const uint32_t bi = fdiv(q, div_npb);
+        blk = static_cast<int>(q - bi * static_cast<uint32_t>(npb));
+        b = static_cast<int>(bi);
+    };
+    auto load = [&](uint4 (&g)[4][NV], uint32_t u) {
+        int cg, b, blk;
+        decode(u, cg, b, blk);
+        const int px = 32 * blk + lp;
+        const int lim = C - cg * 32 - lc;
+        const T *base = x + (static_cast<int64_t>(b) * C + cg * 32 + lc) * HW + px;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                g[k][v] = ld_nc_v4_if(base + k * hw8 + 4 * v, 8 * k < lim && px + 4 * v < HW);
+    };
+    auto convert = [&](const uint4 (&g)[4][NV], uint32_t u) {
+        int cg, b, blk;
+        decode(u, cg, b, blk);
+        uint32_t w = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t tk = t_all;
+            if constexpr (CHAN) {
+                const int c = cg * 32 + 8 * k + lc;
+                tk = shift_threshold<T>(c < C ? __ldg(bias + c) : 0.0f);
+            }
+            w |= sign_bits<T>(g[k][0], g[k][NV - 1], tk, k);
+        }
+        w = exchange_rot(w, 16, keep16, 16u);
+        w = exchange_rot(w, 8, keep8, rot8);
+        w = exchange_rot(w, 4, keep4, rot4);
+        w = __shfl_sync(0xFFFFFFFFu, w, src_lane);
+        const int p = 32 * blk + lane;
+        if (p >= HW) return;
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = ((~w << (3 - i)) & 0x88888888u) | 0x22222222u;
+        const int nvalid = C - cg * 32;
+        if (nvalid < 32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int nv = nvalid - 8 * i;            // channels of this word inside C
+                if (nv < 8) q[i] &= nv <= 0 ? 0u : (1u << (4 * nv)) - 1u;
+            }
+        }
+        *reinterpret_cast<uint4 *>(out + (static_cast<int64_t>(b) * HW + p) * rb + cg * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+    };
+    uint4 g0[4][NV], g1[4][NV];
+    uint32_t u = warp0;
+    if (u < units) load(g0, u);
+    while (u < units) {
+        const uint32_t u1 = u + nwarps;
+        if (u1 < units) load(g1, u1);
+        convert(g0, u);
+        u = u1;
+        if (u >= units) break;
+        const uint32_t u2 = u + nwarps;
+        if (u2 < units) load(g0, u2);
+        convert(g1, u);
+        u = u2;
+    }
+}
+
 // nhwc, transposed through shared memory. A unit is (image b, a run of
 // kNhwcPixels pixels, every channel). Phase 1 reads each channel plane's run
 // with 16-byte loads (consecutive threads, consecutive 8-pixel groups of a
@@ -912,12 +1011,18 @@ pack_im2col_direct_kernel(const T *__restrict__ x, int C, int H, int W, int Ho, 
     }
 }
 
-// For channel-packed pixels the warp-level kernel (contiguous loads) is the
-// default where it applies; BT_PACK_NHWC=smem selects the shared-memory
-// transpose kernel instead (both stay under test).
+// For channel-packed pixels the warp-level kernels (contiguous loads) are the
+// default where they apply (E2M1 from a 2-byte type: the conversion shared
+// with the convolution's packing warps); BT_PACK_NHWC=smem selects the
+// shared-memory transpose kernel and BT_PACK_NHWC=warp the byte-mask warp
+// kernel for every code (all stay under test).
 bool nhwc_warp_disabled() {
     const char *env = std::getenv("BT_PACK_NHWC");
     return env != nullptr && std::strcmp(env, "smem") == 0;
+}
+bool nhwc_e2m1_fast() {
+    const char *env = std::getenv("BT_PACK_NHWC");
+    return env == nullptr || (std::strcmp(env, "smem") != 0 && std::strcmp(env, "warp") != 0);
 }
 
 int grid_for(int64_t threads) {
@@ -1030,6 +1135,22 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
             int64_t blocks = (units + per_block - 1) / per_block;
             if (blocks > cap) blocks = cap;
             if (blocks < 1) blocks = 1;
+            // 2-byte inputs only: for f32 (two loads per 8 pixels) the byte-mask
+            // kernel measured faster on GB300
+            if (CODE == BT_CODE_E2M1 && sizeof(T) == 2 && abs_sum == nullptr && nhwc_e2m1_fast() &&
+                (bias_len <= 1 || aligned(bias, 4))) {
+                // channel group fastest: unit u = (b * npb + blk) * ncg + cg
+                const FastDiv dncg = make_fastdiv(static_cast<uint32_t>(ncg)), dnpb = make_fastdiv(static_cast<uint32_t>(npb));
+                if (bias_len > 1)
+                    return launch_pdl(pack_nhwc_e2m1_kernel<T, true>, dim3(static_cast<unsigned>(blocks)),
+                                      dim3(kPackThreads), s, x, static_cast<int>(C), static_cast<int>(HW),
+                                      static_cast<uint32_t>(units), dncg, dnpb, bias, static_cast<int>(bias_len), out,
+                                      static_cast<int>(rb));
+                return launch_pdl(pack_nhwc_e2m1_kernel<T, false>, dim3(static_cast<unsigned>(blocks)),
+                                  dim3(kPackThreads), s, x, static_cast<int>(C), static_cast<int>(HW),
+                                  static_cast<uint32_t>(units), dncg, dnpb, bias, static_cast<int>(bias_len), out,
+                                  static_cast<int>(rb));
+            }
             if (abs_sum != nullptr)
                 return launch_pdl(pack_nhwc_warp_kernel<T, CODE, true>, dim3(static_cast<unsigned>(blocks)),
                                   dim3(kPackThreads), s, x, static_cast<int>(C), static_cast<int>(HW),

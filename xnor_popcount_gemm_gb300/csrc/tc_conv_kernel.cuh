@@ -280,17 +280,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// A 16-byte load through the non-coherent path, issued where it stands in
-// the program (volatile: the pack loop relies on its loads going out ahead of
-// the conversion of earlier units).
-__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 // Bring `bytes` (a multiple of 16, from a 16-byte-aligned address) into L2.
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -305,83 +294,6 @@ template <int SW> __device__ __forceinline__ uint32_t swizzled(uint32_t addr) {
 
 __device__ __forceinline__ int sel4(const int (&v)[4], int i) {
     return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
-}
-
-// One bit-matrix exchange round across a warp, rotate form: swaps between
-// lanes l and l ^ L the bits whose lane bit L differs from their register bit
-// of weight R (R = L here). `keep` (the positions this lane keeps: R-bit equal
-// to its L-bit) and `rot` (R, or 32 - R where the L-bit is clear) are fixed per
-// lane. A shuffle, a funnel shift and one three-input logic op.
-__device__ __forceinline__ uint32_t exchange_rot(uint32_t w, int L, uint32_t keep, uint32_t rot) {
-    const uint32_t t = __shfl_xor_sync(0xFFFFFFFFu, w, L);
-    const uint32_t r = __funnelshift_r(t, t, rot);
-    return (w & keep) | (r & ~keep);
-}
-
-// A load of 16 bytes that only goes out where `ok` holds (zeros otherwise):
-// predicated in place, no branch.
-__device__ __forceinline__ uint4 ld_nc_v4_if(const void *p, bool ok) {
-    uint4 v;
-    asm volatile(
-        "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n"
-        " mov.b32 %0, 0;\n mov.b32 %1, 0;\n mov.b32 %2, 0;\n mov.b32 %3, 0;\n"
-        " @q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n}"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p), "r"(static_cast<int>(ok)));
-    return v;
-}
-
-// The sign test of the shift as one comparison x >= t (the activation shift
-// of BinaryConv2dCutlass.set_activation: +1 where x + b >= 0, the fp32 sum).
-// A finite b: t = -b, rounded up to a 2-byte input type (x + b >= 0 exactly
-// when x >= -b; for a 2-byte x exactly when x >= that rounding). b = +inf:
-// x + b >= 0 for every x but -inf and NaN, i.e. x >= the lowest finite value.
-// b = -inf or NaN: never, i.e. x >= NaN. Returned as the comparison operand's
-// bits: the value in both halves for a 2-byte type, the float for f32.
-template <typename XT> __device__ __forceinline__ uint32_t shift_threshold(float b);
-template <> __device__ __forceinline__ uint32_t shift_threshold<float>(float b) {
-    if (isfinite(b)) return __float_as_uint(-b);
-    return b > 0.0f ? 0xFF7FFFFFu : 0x7FC00000u;
-}
-template <> __device__ __forceinline__ uint32_t shift_threshold<__nv_bfloat16>(float b) {
-    if (isfinite(b)) {
-        const __nv_bfloat16 t = __float2bfloat16_ru(-b);
-        const uint32_t h = *reinterpret_cast<const uint16_t *>(&t);
-        return h | (h << 16);
-    }
-    return b > 0.0f ? 0xFF7FFF7Fu : 0x7FC07FC0u;
-}
-template <> __device__ __forceinline__ uint32_t shift_threshold<__half>(float b) {
-    if (isfinite(b)) {
-        const __half t = __float2half_ru(-b);
-        const uint32_t h = *reinterpret_cast<const uint16_t *>(&t);
-        return h | (h << 16);
-    }
-    return b > 0.0f ? 0xFBFFFBFFu : 0x7E007E00u;
-}
-
-// Sign bits of one load group (8 consecutive pixels of one channel, k = the
-// channel's bits 4..3) at register bit 16*p0 + 8*p2 + 4*p1 + k, p the pixel
-// within the group: with a 2-byte type each pair of values is one comparison
-// whose two 16-bit halves land on the pair's two bits.
-template <typename XT>
-__device__ __forceinline__ uint32_t sign_bits(const uint4 &lo, const uint4 &hi, uint32_t t, int k) {
-    uint32_t w = 0;
-    if constexpr (sizeof(XT) == 2) {
-        using T2 = typename Thresh<XT>::type;
-        const T2 tt = *reinterpret_cast<const T2 *>(&t);
-        w |= Thresh<XT>::ge(lo.x, tt) & (0x00010001u << k);
-        w |= Thresh<XT>::ge(lo.y, tt) & (0x00010001u << (4 + k));
-        w |= Thresh<XT>::ge(lo.z, tt) & (0x00010001u << (8 + k));
-        w |= Thresh<XT>::ge(lo.w, tt) & (0x00010001u << (12 + k));
-    } else {
-        const float tf = __uint_as_float(t);
-        const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            w |= (__uint_as_float(v[e]) >= tf ? 1u : 0u) << (16 * (e & 1) + 4 * (e >> 1) + k);
-    }
-    return w;
 }
 
 // The units of one tile that one packing warp converts: a contiguous run
@@ -678,7 +590,7 @@ __device__ __forceinline__ void pack_tiles(const ConvArgs &a, uint32_t sB, uint3
 // reach both CTAs.
 template <int CODE, int OUT, int SW, bool PAIRS, typename XT, bool CP>
 __global__ void __launch_bounds__(conv_threads<!std::is_void<XT>::value>(), 1)
-conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const ConvArgs a) {
+conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const __grid_constant__ ConvArgs a) {
     constexpr bool kFused = !std::is_void<XT>::value;
     using T = typename OutT<OUT>::type;
     constexpr int kElem = sizeof(T);
