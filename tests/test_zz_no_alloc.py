@@ -13,6 +13,8 @@ scratch holds, the refusal one row past it, and that a call changes neither
 torch's allocation count nor the device's free memory. This file is collected
 last on purpose.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -107,12 +109,20 @@ def test_noalloc_allocates_nothing():
     # the first call may load the library's module (and with it the array)
     bt.bt_binary_linear_noalloc(x, wp, code, K, 1.0, 1.0, out=out)
     torch.cuda.synchronize()
-    used0 = torch.cuda.memory_allocated()
-    free0, _ = torch.cuda.mem_get_info()
-    for _ in range(3):
-        bt.bt_binary_linear_noalloc(x, wp, code, K, 1.0, 1.0, out=out)
-    torch.cuda.synchronize()
-    free1, _ = torch.cuda.mem_get_info()
-    assert torch.cuda.memory_allocated() == used0
+    # tensors that earlier tests left in reference cycles are freed now, and no
+    # collection runs inside the window (it would lower the count, not raise it)
+    gc.collect()
+    gc.disable()
+    try:
+        used0 = torch.cuda.memory_allocated()
+        free0, _ = torch.cuda.mem_get_info()
+        for _ in range(3):
+            bt.bt_binary_linear_noalloc(x, wp, code, K, 1.0, 1.0, out=out)
+        torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        used1 = torch.cuda.memory_allocated()
+    finally:
+        gc.enable()
+    assert used1 == used0
     assert free1 == free0
     assert bt.bt_device_status() == 0

@@ -113,7 +113,8 @@ bool plan_conv(const ConvGeom &g, bt_code code, int sms, int out_elem, ConvPlan 
             const int qy = floor_div(ey, s), qx = floor_div(ex, s);
             const int id = phase_id[(ey - s * qy) * 2 + (ex - s * qx)];
             const int off = (qy - qy_min[id]) * a.wv + (qx - qx_min[id]);
-            a.tap[kh * g.k + kw] = (static_cast<uint32_t>(id) << 24) | static_cast<uint32_t>(off);
+            a.tap[kh * g.k + kw] = (static_cast<uint32_t>(kh * g.k + kw) << 24) | (static_cast<uint32_t>(id) << 20) |
+                                   static_cast<uint32_t>(off);
             if (off > max_off) max_off = off;
         }
     a.rv = (a.nb + max_off + a.wv - 1) / a.wv;       // rows staged per CTA

@@ -116,7 +116,7 @@ struct ConvArgs {
     int a_stages;             // streamed: ring depth
     int ph_x0[kMaxPhases];    // TMA start column of each phase image: s * qx_min + px
     int ph_y0[kMaxPhases];    // TMA start row relative to s * (first output row): s * qy_min + py
-    uint32_t tap[kMaxTaps];   // (phase << 24) | first staged row the tap reads
+    uint32_t tap[kMaxTaps];   // (tap index kh*k+kw << 24) | (phase << 20) | first staged row it reads
     uint32_t idesc;
     float alpha;
     const float *scales;      // not null: alpha = fp32(scales[0] * scales[1])
@@ -599,6 +599,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     constexpr int kMmaPerSlice = SW / 32;            // 32 bytes of K per MMA
     constexpr uint32_t kAccStride = CODE == BT_CODE_E2M1 ? 240u : 256u;
     constexpr uint32_t kPeers = CP ? 2u : 1u;
+    constexpr int kEpiBatch = kFused ? 1 : 2;         // TMEM boxes loaded per wait (registers: 32 per box)
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -756,6 +757,21 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int as = 0, bs = 0, local = 0;
             uint32_t aph = 0, bph = 0;
             bool ok = true;
+            // Up to kRegTaps taps of one K slice each with resident weights: every
+            // tap's A descriptor and B offset is built once, in registers, so a
+            // tile's MMAs go out back to back (building a tap's descriptors at issue
+            // time measured ~50 % slower per MMA on GB300 for 64-byte slices).
+            constexpr int kRegTaps = 9;
+            const bool reg_taps = a.a_resident && a.nsl == 1 && a.ntap <= kRegTaps;
+            const uint64_t adesc_base0 = kmajor_desc(sA, SW);
+            uint64_t adesc_t[kRegTaps];
+            uint32_t boff_t[kRegTaps];
+#pragma unroll
+            for (int t = 0; t < kRegTaps; ++t) {
+                const uint32_t tapw = t < a.ntap ? a.tap[t] : 0u;
+                adesc_t[t] = adesc_base0 + static_cast<uint64_t>(tapw >> 24) * ((kBM * SW) >> 4);
+                boff_t[t] = ((tapw >> 20) & 0xFu) * (a.img_bytes >> 4) + (tapw & 0xFFFFFu) * (SW >> 4);
+            }
             for (int t = unit; t < a.num_tiles && ok; t += nunits, ++local) {
                 const int buf = local & 1;
                 if (local >= 2) {
@@ -767,6 +783,37 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (!tc::wait_bounded(bfull(bs), bph, abort_flag, a.err, a.wait_ns)) break;
                 tc::fence_after_sync();
                 const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * kAccStride;
+                if (reg_taps) {
+                    const uint64_t bbase = kmajor_desc(sB + static_cast<uint32_t>(bs) * a.stage_bytes, SW);
+                    uint64_t bdt[kRegTaps];
+#pragma unroll
+                    for (int t = 0; t < kRegTaps; ++t) bdt[t] = bbase + boff_t[t];
+                    uint32_t waited = 0;                  // first tile: weight boxes already waited for
+#pragma unroll
+                    for (int t = 0; t < kRegTaps; ++t) {
+                        if (t < a.ntap) {
+                            if (local == 0) {
+                                const int bx = a.a_boxes <= kMaxAStages ? static_cast<int>(a.tap[t] >> 24) / a.a_d : 0;
+                                if (!((waited >> bx) & 1u)) {
+                                    if (!tc::wait_bounded(afull(bx), 0u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                                    tc::fence_after_sync();
+                                    waited |= 1u << bx;
+                                }
+                            }
+#pragma unroll
+                            for (int kk = 0; kk < kMmaPerSlice; ++kk) {
+                                const uint32_t acc = (t | kk) != 0 ? 1u : 0u;
+                                if (CP) {
+                                    if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4_pair(dacc, adesc_t[t] + 2 * kk, bdt[t] + 2 * kk, a.idesc, acc);
+                                    else tc::mma_mxf4_pair(dacc, adesc_t[t] + 2 * kk, bdt[t] + 2 * kk, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+                                } else {
+                                    if (CODE == BT_CODE_E4M3) tc::mma_f8f6f4(dacc, adesc_t[t] + 2 * kk, bdt[t] + 2 * kk, a.idesc, acc);
+                                    else tc::mma_mxf4(dacc, adesc_t[t] + 2 * kk, bdt[t] + 2 * kk, a.idesc, tmem + kSfCol, tmem + kSfCol + 16, acc);
+                                }
+                            }
+                        }
+                    }
+                } else {
                 // descriptors are built once and moved by adding (byte offset >> 4)
                 // to their start-address field (shared-memory addresses stay below
                 // 256 KB, so the 14-bit field never carries): the issuing thread
@@ -776,26 +823,32 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const uint32_t img16 = a.img_bytes >> 4;
                 constexpr uint32_t kSlice16 = kASlice >> 4;
                 uint64_t adesc = adesc_base;
-                int idx = 0, within = 0, box = 0;
+                int idx = 0, within = 0;
+                uint32_t waited = 0;                      // first tile: weight boxes already waited for
                 for (int tp = 0; tp < a.ntap && ok; ++tp) {
+                    // each tap: its phase image, its first staged row, its own weight slices
                     const uint32_t tapw = a.tap[tp];
-                    uint64_t bd = bdesc_stage + (tapw >> 24) * static_cast<uint32_t>(a.nsl) * img16 +
-                                  (tapw & 0xFFFFFFu) * (SW >> 4);
+                    const int tap_id = static_cast<int>(tapw >> 24);
+                    uint64_t bd = bdesc_stage + ((tapw >> 20) & 0xFu) * static_cast<uint32_t>(a.nsl) * img16 +
+                                  (tapw & 0xFFFFFu) * (SW >> 4);
                     for (int sl = 0; sl < a.nsl; ++sl, ++idx) {
-                        if (within == 0) {
-                            if (a.a_resident) {
-                                // first tile: each box of weights on its own barrier (or all on the first)
-                                if (local == 0 && (a.a_boxes <= kMaxAStages || idx == 0)) {
-                                    if (!tc::wait_bounded(afull(a.a_boxes <= kMaxAStages ? box : 0), 0u, abort_flag, a.err,
-                                                          a.wait_ns)) { ok = false; break; }
+                        if (a.a_resident) {
+                            const int sidx = tap_id * a.nsl + sl;           // the slice's place in the resident weights
+                            if (local == 0) {
+                                // first tile: the box of weights holding this slice (each box on its own
+                                // barrier, or all on the first)
+                                const int bx = a.a_boxes <= kMaxAStages ? sidx / a.a_d : 0;
+                                if (!((waited >> bx) & 1u)) {
+                                    if (!tc::wait_bounded(afull(bx), 0u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                                     tc::fence_after_sync();
+                                    waited |= 1u << bx;
                                 }
-                                adesc = adesc_base + static_cast<uint64_t>(idx) * kSlice16;
-                            } else {
-                                if (!tc::wait_bounded(afull(as), aph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
-                                tc::fence_after_sync();
-                                adesc = adesc_base + static_cast<uint64_t>(as * a.a_d) * kSlice16;
                             }
+                            adesc = adesc_base + static_cast<uint64_t>(sidx) * kSlice16;
+                        } else if (within == 0) {
+                            if (!tc::wait_bounded(afull(as), aph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                            tc::fence_after_sync();
+                            adesc = adesc_base + static_cast<uint64_t>(as * a.a_d) * kSlice16;
                         }
 #pragma unroll
                         for (int kk = 0; kk < kMmaPerSlice; ++kk) {
@@ -812,7 +865,6 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         bd += img16;
                         if (++within == a.a_d) {
                             within = 0;
-                            ++box;
                             if (!a.a_resident) {
                                 if (CP) tc::mma_commit_pair(aempty(as), 0x3);
                                 else tc::mma_commit(aempty(as));
@@ -820,6 +872,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             }
                         }
                     }
+                }
                 }
                 if (!ok) break;
                 if (CP) {
@@ -867,49 +920,66 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const int nbox = CP ? (a.bn + 31) / 32 : (ncols + 31) / 32;
             const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(buf) * kAccStride;
             T *const plane0 = out + (static_cast<int64_t>(b) * a.O + o0) * hw + static_cast<int64_t>(r0) * a.Wo;
-            if (nrows > 0) {
-                for (int bx = half; bx < nbox; bx += 2) {
-                    uint32_t r[32];
-                    tc::tmem_ld32(tbase + static_cast<uint32_t>(32 * bx), r);
-                    tc::tmem_ld_wait();
-                    // stage: row = this lane's channel, 32 virtual pixels, swizzled
-                    __syncwarp();
+            // hand the accumulator back once every TMEM read of this tile is complete
+            auto release = [&]() {
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if (CP && !leader) tc::mbar_arrive_cluster(tc::mapa(tempty(buf), 0u));
+                    else tc::mbar_arrive(tempty(buf));
+                }
+            };
+            if (nrows <= 0) {
+                release();
+            } else {
+                // this warp's boxes bx = half, half + 2, ... in batches of kEpiBatch: the
+                // TMEM loads of a batch go out together and are waited for once (a
+                // load waits long while MMAs of the other buffer run, most under CTA
+                // pairs); the accumulator goes back after the last batch's loads
+                const int nmine = (nbox - half + 1) / 2;
+                for (int j0 = 0; j0 < nmine; j0 += kEpiBatch) {
+                    uint32_t r[kEpiBatch][32];
 #pragma unroll
-                    for (int q = 0; q < kBoxRow / 16; ++q) {
-                        const uint32_t addr = sbox + static_cast<uint32_t>(lane * kBoxRow) + (box_chunk<kElem>(q, lane) << 4);
-                        const uint4 w = chunk16<OUT, kElem>(r, q * (16 / kElem), alpha);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w.x), "r"(w.y),
-                                     "r"(w.z), "r"(w.w)
-                                     : "memory");
-                    }
-                    __syncwarp();
-                    // read back with lanes along the pixels
-                    if constexpr (PAIRS) {
-                        const int col = 32 * bx + 2 * (lane & 15);
-                        const int sec = col >= a.nb ? 1 : 0;
-                        const int v = col + sec * vshift;
-                        const int i = v / a.wv, j = v - i * a.wv;
-                        const bool valid = col < a.bn && col - sec * a.nb < hcols && v < ncols && j < a.Wo;
-                        uint8_t *p = reinterpret_cast<uint8_t *>(plane0 + static_cast<int64_t>(lane >> 4) * hw +
-                                                                 static_cast<int64_t>(i) * a.Wo + j);
-                        box_to_planes_pairs(sbox, lane, valid, p, static_cast<int64_t>(hw) * kElem, nrows);
-                    } else {
-                        const int col = 32 * bx + lane;            // lane = accumulator column
-                        const int sec = col >= a.nb ? 1 : 0;
-                        const int v = col + sec * vshift;
-                        const int i = v / a.wv, j = v - i * a.wv;
-                        const bool valid = col < a.bn && col - sec * a.nb < hcols && v < ncols && j < a.Wo;
-                        uint8_t *p = reinterpret_cast<uint8_t *>(plane0 + static_cast<int64_t>(i) * a.Wo + j);
-                        box_to_planes<kElem>(sbox, lane, valid, p, static_cast<int64_t>(hw) * kElem, nrows);
+                    for (int j = 0; j < kEpiBatch; ++j)
+                        if (j0 + j < nmine) tc::tmem_ld32(tbase + static_cast<uint32_t>(32 * (half + 2 * (j0 + j))), r[j]);
+                    tc::tmem_ld_wait();
+                    if (j0 + kEpiBatch >= nmine) release();
+#pragma unroll
+                    for (int j = 0; j < kEpiBatch; ++j) {
+                        if (j0 + j >= nmine) break;
+                        const int bx = half + 2 * (j0 + j);
+                        // stage: row = this lane's channel, 32 virtual pixels, swizzled
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < kBoxRow / 16; ++q) {
+                            const uint32_t addr = sbox + static_cast<uint32_t>(lane * kBoxRow) + (box_chunk<kElem>(q, lane) << 4);
+                            const uint4 w = chunk16<OUT, kElem>(r[j], q * (16 / kElem), alpha);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w.x), "r"(w.y),
+                                         "r"(w.z), "r"(w.w)
+                                         : "memory");
+                        }
+                        __syncwarp();
+                        // read back with lanes along the pixels
+                        if constexpr (PAIRS) {
+                            const int col = 32 * bx + 2 * (lane & 15);
+                            const int sec = col >= a.nb ? 1 : 0;
+                            const int v = col + sec * vshift;
+                            const int i = v / a.wv, jx = v - i * a.wv;
+                            const bool valid = col < a.bn && col - sec * a.nb < hcols && v < ncols && jx < a.Wo;
+                            uint8_t *p = reinterpret_cast<uint8_t *>(plane0 + static_cast<int64_t>(lane >> 4) * hw +
+                                                                     static_cast<int64_t>(i) * a.Wo + jx);
+                            box_to_planes_pairs(sbox, lane, valid, p, static_cast<int64_t>(hw) * kElem, nrows);
+                        } else {
+                            const int col = 32 * bx + lane;            // lane = accumulator column
+                            const int sec = col >= a.nb ? 1 : 0;
+                            const int v = col + sec * vshift;
+                            const int i = v / a.wv, jx = v - i * a.wv;
+                            const bool valid = col < a.bn && col - sec * a.nb < hcols && v < ncols && jx < a.Wo;
+                            uint8_t *p = reinterpret_cast<uint8_t *>(plane0 + static_cast<int64_t>(i) * a.Wo + jx);
+                            box_to_planes<kElem>(sbox, lane, valid, p, static_cast<int64_t>(hw) * kElem, nrows);
+                        }
                     }
                 }
-            }
-            // every TMEM read of this tile is complete: hand the accumulator back
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                if (CP && !leader) tc::mbar_arrive_cluster(tc::mapa(tempty(buf), 0u));
-                else tc::mbar_arrive(tempty(buf));
             }
         }
     }
