@@ -155,3 +155,28 @@ def test_rows_too_wide_for_one_tile_take_the_explicit_unfold(code):
     wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
     got = bt.bt_binary_conv2d(x.to(DEV), wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32).cpu()
     assert torch.equal(got, torch.from_numpy(want))
+
+
+@pytest.mark.parametrize("code", TC_CODES, ids=TC_IDS)
+def test_weights_packed_just_before_each_call(code):
+    # After the library's own pack of x, the convolution may start its weight
+    # copies before it waits on that pack; the pack of x lets it start only once
+    # its own wait is over, so weights written by the kernel before (here a
+    # weight pack into the same buffer, right before every call) are complete
+    # by then. Every call must see the weights packed for it.
+    B, C, H, W, O, k, s, p, d = 4, 128, 28, 28, 256, 3, 2, 1, 1
+    x = _gen(51, (B, C, H, W), torch.bfloat16)
+    ws = [_gen(52 + i, (O, C, k, k), torch.bfloat16) for i in range(3)]
+    xd = x.to(DEV)
+    wbuf = bt.bt_pack_sign(ws[0].to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    wds = [w.to(DEV) for w in ws]
+    torch.cuda.synchronize()
+    outs = []
+    for i in range(6):
+        bt.bt_pack_sign(wds[i % 3], code, bt.BT_LAYOUT_NCHW_TO_NHWC, out=wbuf)
+        outs.append(bt.bt_binary_conv2d(xd, wbuf, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32))
+    torch.cuda.synchronize()
+    sx = oracle.binarize(x)
+    wants = [oracle.conv2d_dot(sx, oracle.binarize_weight(w), s, p, d) for w in ws]
+    for i, got in enumerate(outs):
+        assert torch.equal(got.cpu(), torch.from_numpy(wants[i % 3]))

@@ -340,7 +340,7 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
         }
         const cudaError_t e = launch_tc_conv_implicit(static_cast<const uint8_t *>(xp),
                                                       static_cast<const uint8_t *>(weight), w_code, g, alpha, out,
-                                                      out_dtype, err, s, scales);
+                                                      out_dtype, err, s, scales, x_dtype != BT_PACKED);
         if (e == cudaErrorNotSupported) return BT_ERR_UNSUPPORTED;
         return from_cuda(e);
     }

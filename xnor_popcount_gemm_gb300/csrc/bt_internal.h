@@ -196,9 +196,12 @@ bool unfold_single_pass(const ConvGeom &g, bt_dtype xt, bt_code code);
 // then runs). The launch returns cudaErrorNotSupported where the plan does
 // not apply.
 bool conv_implicit_applies(const ConvGeom &g, bt_code code);
+// after_own_pack: the kernel launched just before on the stream is the
+// library's pack of x (it writes the pixels only), so the weights may be read
+// before the wait on that kernel.
 cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
                                     void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s,
-                                    const float *scales = nullptr);
+                                    const float *scales = nullptr, bool after_own_pack = false);
 // The same convolution reading x itself (NCHW floats of type x_dtype, shifted
 // by bias (bias_len 1 or C; 0: none) and signed by its own packing warps): one
 // kernel, no workspace. It applies where the implicit plan does, every

@@ -362,8 +362,10 @@ pack_nhwc_kernel(const T *__restrict__ x, int B, int C, int HW, const float *__r
     const uint32_t npg = static_cast<uint32_t>((HW + E - 1) / E);
     const uint32_t ncg = static_cast<uint32_t>(padded_elems<CODE>(rb) / 8);
     const uint64_t total = static_cast<uint64_t>(B) * ncg * npg;
-    pdl_launch_dependents();
     pdl_wait();
+    // dependents start only after this wait: a convolution that follows may read its
+    // weights before its own wait, and those may come from the kernel before this one
+    pdl_launch_dependents();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
 
     for (uint64_t t = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
@@ -460,8 +462,10 @@ pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const int ncg = static_cast<int>(div_ncg.d), npb = static_cast<int>(div_npb.d);
     const int j = lane & 3;                                // this lane's 8-pixel chunk in the loads
-    pdl_launch_dependents();
     pdl_wait();
+    // dependents start only after this wait: a convolution that follows may read its
+    // weights before its own wait, and those may come from the kernel before this one
+    pdl_launch_dependents();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
     for (uint32_t u = warp0; u < units; u += nwarps) {
         const uint32_t rest = fdiv(u, div_npb);
@@ -575,8 +579,10 @@ pack_nhwc_e2m1_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
     const uint32_t keep4 = (lane & 4) ? 0xF0F0F0F0u : 0x0F0F0F0Fu, rot4 = (lane & 4) ? 4u : 28u;
     const int src_lane = ((lane & 1) << 4) | (((lane >> 2) & 1) << 3) | (((lane >> 1) & 1) << 2) |
                          (((lane >> 4) & 1) << 1) | ((lane >> 3) & 1);
-    pdl_launch_dependents();
     pdl_wait();
+    // dependents start only after this wait: a convolution that follows may read its
+    // weights before its own wait, and those may come from the kernel before this one
+    pdl_launch_dependents();
     const uint32_t t_all = shift_threshold<T>(bias_len == 1 ? __ldg(bias) : 0.0f);
     // unit u: channel group cg (fastest), then pixel block blk of image b
     auto decode = [&](uint32_t u, int &cg, int &b, int &blk) {
@@ -672,8 +678,10 @@ pack_nhwc_tr_kernel(const T *__restrict__ x, int C, int HW, int upi, uint32_t un
     const int cstride = nhwc_cstride(C);
     const int G = static_cast<int>(divG.d);
     const int tid = threadIdx.x;
-    pdl_launch_dependents();
     pdl_wait();
+    // dependents start only after this wait: a convolution that follows may read its
+    // weights before its own wait, and those may come from the kernel before this one
+    pdl_launch_dependents();
     const float bs = bias_len == 1 ? __ldg(bias) : 0.0f;
     const int items1 = C * kNhwcGroups;
 

@@ -293,7 +293,7 @@ bool conv_implicit_applies(const ConvGeom &g, bt_code code) {
 
 cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha,
                                     void *out, bt_dtype out_t, unsigned int *err, cudaStream_t s,
-                                    const float *scales) {
+                                    const float *scales, bool after_own_pack) {
     if (!conv_implicit_applies(g, code)) return cudaErrorNotSupported;
     ConvPlan p;
     if (!choose_plan(g, code, device_sm_count(), out_t == BT_BF16 || out_t == BT_F16 ? 2 : 4, p))
@@ -303,6 +303,7 @@ cudaError_t launch_tc_conv_implicit(const uint8_t *xp, const uint8_t *wp, bt_cod
     p.a.out = out;
     p.a.err = err;
     p.a.wait_ns = wait_limit_ns();
+    p.a.a_early = after_own_pack ? 1 : 0;
     CUtensorMap ma, mb;
     if (!encode_maps(g, code, p.a, xp, wp, &ma, &mb)) return cudaErrorInvalidValue;
     return launch_code<void>(ma, mb, p, code, out_t, s);

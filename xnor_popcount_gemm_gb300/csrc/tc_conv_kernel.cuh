@@ -135,6 +135,8 @@ struct ConvArgs {
     int ph_ymin, ph_ymax;     // least and greatest ph_y0
     int zero_rows;            // more than one band per image: staged rows past the image are cleared per tile
     int prefetch;             // bring the next tile's image into L2 ahead (one band per image only)
+    int a_early;              // resident weights may be copied before the wait for the previous kernel
+                              // (set only when that kernel is the library's own pack of x)
     int ht2;                  // rows of a band per CTA (a pair: ht / 2 each; one CTA: ht)
     int nb;                   // accumulator columns per CTA's rows (a pair: bn / 2; one CTA: bn)
 };
@@ -681,13 +683,35 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
-            pdl_wait();                                   // pixels (and weights) come from earlier kernels
             int as = 0, bs = 0;
             uint32_t aph = 0, bph = 0;
             uint32_t a_last[kMaxAStages], b_last[2];      // phase of each slot's last copy; 2 = none
             for (int i = 0; i < kMaxAStages; ++i) a_last[i] = 2u;
             b_last[0] = b_last[1] = 2u;
             bool ok = true, a_loaded = false;
+            // resident weights: one barrier per box (up to kMaxAStages boxes; more
+            // share the first barrier), so that the first MMAs start once their
+            // taps have landed
+            auto load_weights = [&](int ot) {
+                const int am0 = ot * static_cast<int>(kPeers) * kBM + ch_first;
+                const bool per_box = a.a_boxes <= kMaxAStages;
+                if (!per_box && leader)
+                    tc::mbar_arrive_expect_tx(afull(0), kPeers * static_cast<uint32_t>(a.a_boxes * a.a_d) * kASlice);
+                for (int i = 0; i < a.a_boxes; ++i) {
+                    const int bi = per_box ? i : 0;
+                    if (per_box && leader) tc::mbar_arrive_expect_tx(afull(i), kPeers * static_cast<uint32_t>(a.a_d) * kASlice);
+                    if (per_box) a_last[i] = 0u;
+                    const uint32_t dst = sA + static_cast<uint32_t>(i * a.a_d) * kASlice;
+                    if (CP) tc::tma_load_3d_pair(dst, &tmA, 0, am0, i * a.a_d, lead(afull(bi)));
+                    else tc::tma_load_3d(dst, &tmA, 0, am0, i * a.a_d, afull(bi));
+                }
+                if (!per_box) a_last[0] = 0u;
+                a_loaded = true;
+            };
+            // the weights are not written by the library's own pack of x, which is
+            // the kernel this one may overlap: they can be in flight before the wait
+            if (a.a_resident && a.a_early && unit < a.num_tiles) load_weights(unit % a.num_ot);
+            pdl_wait();                                   // pixels (and otherwise weights) come from earlier kernels
             for (int t = unit; t < a.num_tiles && ok; t += nunits) {
                 const int ot = t % a.num_ot, rest = t / a.num_ot;
                 const int b = rest / a.bands, band = rest - b * a.bands;
@@ -708,24 +732,8 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     b_last[bs] = bph;
                     if (++bs == a.b_stages) { bs = 0; bph ^= 1u; }
                 }
-                // resident weights: after the first tile's pixels, one barrier per
-                // box (up to kMaxAStages boxes; more share the first barrier), so
-                // that the first MMAs start once their taps have landed
-                if (a.a_resident && !a_loaded) {
-                    const bool per_box = a.a_boxes <= kMaxAStages;
-                    if (!per_box && leader)
-                        tc::mbar_arrive_expect_tx(afull(0), kPeers * static_cast<uint32_t>(a.a_boxes * a.a_d) * kASlice);
-                    for (int i = 0; i < a.a_boxes; ++i) {
-                        const int bi = per_box ? i : 0;
-                        if (per_box && leader) tc::mbar_arrive_expect_tx(afull(i), kPeers * static_cast<uint32_t>(a.a_d) * kASlice);
-                        if (per_box) a_last[i] = 0u;
-                        const uint32_t dst = sA + static_cast<uint32_t>(i * a.a_d) * kASlice;
-                        if (CP) tc::tma_load_3d_pair(dst, &tmA, 0, am0, i * a.a_d, lead(afull(bi)));
-                        else tc::tma_load_3d(dst, &tmA, 0, am0, i * a.a_d, afull(bi));
-                    }
-                    if (!per_box) a_last[0] = 0u;
-                    a_loaded = true;
-                }
+                // resident weights (unless already in flight): after the first tile's pixels
+                if (a.a_resident && !a_loaded) load_weights(ot);
                 if (!a.a_resident) {
                     for (int i0 = 0; i0 < nslices; i0 += a.a_d) {
                         if (!tc::wait_bounded(aempty(as), aph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
