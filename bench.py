@@ -673,10 +673,12 @@ def pack_bytes(wl, code, bt):
 
 def kernel_source_hash(kind: str = "linear") -> str:
     """First 16 hex digits of the sha256 of the contraction kernel's sources:
-    tc_gemm.cu then tc_ptx.cuh (linear); tc_conv.cu, tc_ptx.cuh, then
-    sign_pack.cuh (implicit-im2col convolution)."""
+    tc_gemm.cu then tc_ptx.cuh (linear); tc_conv_kernel.cuh, tc_conv.cu,
+    tc_ptx.cuh, then sign_pack.cuh (implicit-im2col convolution)."""
     h = hashlib.sha256()
-    for f in ("tc_gemm.cu", "tc_ptx.cuh") if kind == "linear" else ("tc_conv.cu", "tc_ptx.cuh", "sign_pack.cuh"):
+    files = ("tc_gemm.cu", "tc_ptx.cuh") if kind == "linear" else \
+        ("tc_conv_kernel.cuh", "tc_conv.cu", "tc_ptx.cuh", "sign_pack.cuh")
+    for f in files:
         with open(os.path.join(ROOT, "xnor_popcount_gemm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
