@@ -1147,17 +1147,25 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
             // kernel measured faster on GB300
             if (CODE == BT_CODE_E2M1 && sizeof(T) == 2 && abs_sum == nullptr && nhwc_e2m1_fast() &&
                 (bias_len <= 1 || aligned(bias, 4))) {
-                // channel group fastest: unit u = (b * npb + blk) * ncg + cg
+                // channel group fastest: unit u = (b * npb + blk) * ncg + cg; as many
+                // blocks as are resident at once (the warps loop over the units), so
+                // that no block waits for a second wave
                 const FastDiv dncg = make_fastdiv(static_cast<uint32_t>(ncg)), dnpb = make_fastdiv(static_cast<uint32_t>(npb));
-                if (bias_len > 1)
-                    return launch_pdl(pack_nhwc_e2m1_kernel<T, true>, dim3(static_cast<unsigned>(blocks)),
-                                      dim3(kPackThreads), s, x, static_cast<int>(C), static_cast<int>(HW),
-                                      static_cast<uint32_t>(units), dncg, dnpb, bias, static_cast<int>(bias_len), out,
-                                      static_cast<int>(rb));
-                return launch_pdl(pack_nhwc_e2m1_kernel<T, false>, dim3(static_cast<unsigned>(blocks)),
-                                  dim3(kPackThreads), s, x, static_cast<int>(C), static_cast<int>(HW),
-                                  static_cast<uint32_t>(units), dncg, dnpb, bias, static_cast<int>(bias_len), out,
-                                  static_cast<int>(rb));
+                auto kern = bias_len > 1 ? pack_nhwc_e2m1_kernel<T, true> : pack_nhwc_e2m1_kernel<T, false>;
+                static int per_sm[2] = {0, 0};
+                const int slot = bias_len > 1 ? 1 : 0;
+                if (per_sm[slot] == 0) {
+                    int n = 0;
+                    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kPackThreads, 0) != cudaSuccess || n < 1) n = 1;
+                    per_sm[slot] = n;
+                }
+                int64_t eb = static_cast<int64_t>(sms > 0 ? sms : 148) * per_sm[slot];
+                const int64_t need = (units + per_block - 1) / per_block;
+                if (eb > need) eb = need;
+                if (eb < 1) eb = 1;
+                return launch_pdl(kern, dim3(static_cast<unsigned>(eb)), dim3(kPackThreads), s, x, static_cast<int>(C),
+                                  static_cast<int>(HW), static_cast<uint32_t>(units), dncg, dnpb, bias,
+                                  static_cast<int>(bias_len), out, static_cast<int>(rb));
             }
             if (abs_sum != nullptr)
                 return launch_pdl(pack_nhwc_warp_kernel<T, CODE, true>, dim3(static_cast<unsigned>(blocks)),
