@@ -265,8 +265,38 @@ def test_conv_backward_grad_weight_f32():
     _conv_run_and_compare(2, 16, 12, 12, 32, 3, 2, 1, 1, torch.bfloat16, torch.float32, seed=9)
 
 
+# The input gradient as one implicit GEMM on the tensor cores (O a multiple of
+# 64; conv_dgrad.cu): sub-pixel phases of strides 1 to 4 (and phases no tap
+# reaches), dilation, 1x1 to 7x7 kernels, several bands of rows and channel
+# tiles, wide rows, channel counts that are not a multiple of 16, O in copies
+# of several 64-channel slices or one slice per copy ("slices"), and the route
+# it replaces ("gather": the tap matrix D, then the gather).
+CONV_BWD_IMPLICIT = [(2, 8, 9, 9, 64, 3, 1, 1, 1), (3, 5, 11, 10, 64, 3, 2, 1, 1), (2, 16, 12, 12, 128, 3, 2, 2, 2),
+                     (1, 3, 7, 7, 64, 1, 1, 0, 1), (2, 4, 6, 6, 64, 5, 1, 2, 1), (2, 20, 15, 13, 64, 3, 3, 1, 1),
+                     (1, 200, 9, 9, 192, 3, 1, 1, 1), (1, 40, 40, 40, 64, 3, 1, 1, 1), (1, 16, 33, 70, 64, 3, 2, 1, 1),
+                     (1, 16, 5, 200, 64, 3, 1, 1, 1), (1, 8, 17, 17, 64, 7, 2, 3, 1), (1, 8, 16, 16, 64, 4, 4, 0, 1),
+                     (1, 8, 3, 3, 64, 3, 4, 1, 1), (1, 8, 12, 12, 320, 3, 2, 0, 2), (1, 130, 6, 6, 512, 3, 1, 1, 1),
+                     (2, 128, 28, 28, 256, 3, 2, 1, 1), (2, 256, 14, 14, 256, 3, 1, 1, 1)]
+
+
+@pytest.mark.parametrize("route", ["implicit", "slices", "gather"])
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", CONV_BWD_IMPLICIT)
+def test_conv_backward_input_gradient_routes(B, C, H, W, O, k, s, p, d, route, monkeypatch):
+    monkeypatch.setenv("BT_CONV_DGRAD", route)
+    ho, wo = oracle.conv2d_out_size(H, k, s, p, d), oracle.conv2d_out_size(W, k, s, p, d)
+    # g per pixel, then the gather route's D or the implicit route's codes of x (16 bytes per 32 channels)
+    g_bytes = -(-B * ho * wo * O * 2 // 256) * 256
+    codes = -(-B * H * W * -(-C // 32) * 16 // 256) * 256
+    ws = bt.bt_binary_conv2d_backward_workspace(B, C, H, W, O, k, s, p, d, True, False)
+    assert ws == (g_bytes + -(-C * k * k * B * ho * wo * 4 // 256) * 256 if route == "gather" else g_bytes + codes)
+    x_dtype = torch.float32 if (B + C + k) % 2 else torch.bfloat16
+    differ = _conv_run_and_compare(B, C, H, W, O, k, s, p, d, x_dtype, torch.bfloat16, seed=B * C + H + s)
+    assert differ.mean() < 0.01
+
+
+@pytest.mark.parametrize("O", [8, 64], ids=["gather", "implicit"])
 @pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float32], ids=["x_bf16", "x_f32"])
-def test_conv_backward_mask_at_the_bound(x_dtype):
+def test_conv_backward_mask_at_the_bound(x_dtype, O):
     # every x on or next to +-scale_a in x's dtype (the consecutive values of
     # the type around it, both signs): the kept set, decided from
     # fp32(x / scale_a) rounded to x's dtype, must be the oracle's exactly.
@@ -279,7 +309,7 @@ def test_conv_backward_mask_at_the_bound(x_dtype):
         base = int(np.float32(sa).view(np.int32))
         vals = torch.from_numpy(np.array([base + j for j in range(-12, 13)], dtype=np.int32).view(np.float32))
     vals = torch.cat([vals, -vals])
-    B, C, H, W, O = 1, 4, 5, 5, 8
+    B, C, H, W = 1, 4, 5, 5
     x = vals.repeat((B * C * H * W + vals.numel() - 1) // vals.numel())[: B * C * H * W].view(B, C, H, W).to(x_dtype)
     w = torch.ones(O, C, 3, 3, dtype=torch.bfloat16)
     g = torch.ones(B, O, H, W, dtype=torch.bfloat16)

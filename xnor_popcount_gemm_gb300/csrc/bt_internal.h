@@ -171,6 +171,21 @@ cudaError_t launch_transpose_bf16(const void *in, bt_dtype in_t, int64_t R, int6
 cudaError_t launch_transpose_bf16_batched(const void *in, bt_dtype in_t, int64_t R, int64_t C, int64_t ldo, bool sign,
                                           uint16_t *out, int batch, cudaStream_t s);
 
+// Input gradient of the conv2d backward as one implicit GEMM (conv_dgrad.cu):
+// g_nhwc = g per pixel [B, Ho, Wo, O] bf16, wst = the signs [C*k*k rows (c,
+// kh, kw), ldw] bf16; writes gx [B, C, H, W] bf16 (bf16(alpha * sum), masked
+// to 0 where x lies outside [-bound, bound]) and adds the grad_scale_a terms
+// (times norm) to *sum. codes: dgrad_codes_bytes() of scratch (16-byte
+// aligned) for x's mask and sign codes. applies: O a multiple of 64, stride
+// <= 4, k*k <= 64, the layer's tiles fit (BT_CONV_DGRAD=gather turns the
+// route off).
+bool dgrad_implicit_applies(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int k, int s, int p, int d);
+size_t dgrad_codes_bytes(int64_t B, int64_t C, int64_t H, int64_t W);
+cudaError_t launch_dgrad_implicit(const uint16_t *g_nhwc, const uint16_t *wst, int64_t ldw, int64_t B, int64_t C,
+                                  int64_t H, int64_t W, int64_t O, int k, int s, int p, int d, const void *x,
+                                  bt_dtype x_dtype, float alpha, float bound, float norm, void *gx,
+                                  float *sum, void *codes, unsigned int *err, cudaStream_t stream);
+
 // True when this build carries the tensor-core kernels.
 bool tc_available();
 

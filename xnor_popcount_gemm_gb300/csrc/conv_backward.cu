@@ -271,6 +271,7 @@ float mask_bound(float scale_a, bool bf16) {
 // other on the stream, so they share the space.
 struct ConvBwdPlan {
     ConvBwdGeom q;
+    bool implicit;        // input gradient as one implicit GEMM (conv_dgrad.cu): no D
     int splits;
     int64_t ldp;          // padded P of the weight gradient's rows
     size_t gp_off, dt_off, dgrad_bytes;
@@ -287,17 +288,21 @@ bool make_plan(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int k, int
     q.Wo = wn / s + 1;
     q.P = B * q.Ho * q.Wo;
     q.T = C * k * k;
-    // K splits for the weight gradient: about two units of work per CTA pair
+    // K splits for the weight gradient: at most one unit of work per CTA pair (76
+    // pairs), so that no pair takes a second round
     const int64_t tiles = ((O + 255) / 256) * ((q.T + 223) / 224);
-    int64_t sp = (76 + tiles - 1) / tiles;
+    int64_t sp = 76 / tiles;
     if (sp > 64) sp = 64;
     if (sp < 1) sp = 1;
     while (sp > 1 && q.P / sp < 512) --sp;                   // keep >= 8 slices per split
     pl.splits = static_cast<int>(sp);
     pl.ldp = (q.P + 64 * sp - 1) / (64 * sp) * (64 * sp);
+    pl.implicit = dgrad_implicit_applies(B, C, H, W, O, k, s, p, d);
     pl.gp_off = 0;
     pl.dt_off = round_up256(static_cast<size_t>(q.P * O * 2));
-    pl.dgrad_bytes = pl.dt_off + round_up256(static_cast<size_t>(q.T * q.P * 4));
+    // the implicit route keeps x's codes where the gather route keeps D
+    pl.dgrad_bytes = pl.dt_off + (pl.implicit ? round_up256(dgrad_codes_bytes(B, C, H, W))
+                                              : round_up256(static_cast<size_t>(q.T * q.P * 4)));
     pl.go_off = 0;
     pl.u_off = round_up256(static_cast<size_t>(O * pl.ldp * 2));
     pl.part_off = pl.u_off + round_up256(static_cast<size_t>(q.T * pl.ldp * 2));
@@ -385,12 +390,19 @@ bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void 
             launch_transpose_bf16_batched(g16, BT_BF16, O, q.Ho * q.Wo, O, false, gp, static_cast<int>(B), s) !=
                 cudaSuccess)
             return BT_ERR_CUDA;
-        if (launch_tc_bf16(static_cast<const uint16_t *>(wst), ldw, gp, O, q.T, q.P, O, bf16_round_host(scale_w), dt, BT_F32,
-                           nullptr, err, s) != cudaSuccess)
-            return BT_ERR_CUDA;
         const float norm = static_cast<float>(1.0 / std::sqrt(static_cast<double>(B) * C * H * W));
         const float bound = mask_bound(scale_a, x_dtype == BT_BF16);
-        const cudaError_t e =
+        if (pl.implicit) {
+            // one kernel: the taps reduced inside the tile, mask and grad_scale_a in its epilogue
+            if (launch_dgrad_implicit(gp, static_cast<const uint16_t *>(wst), ldw, B, C, H, W, O, kernel_size, stride,
+                                      padding, dilation, x, x_dtype, bf16_round_host(scale_w), bound, norm, grad_x,
+                                      sum, dt, err, s) != cudaSuccess)
+                return BT_ERR_CUDA;
+        } else if (launch_tc_bf16(static_cast<const uint16_t *>(wst), ldw, gp, O, q.T, q.P, O, bf16_round_host(scale_w), dt,
+                                  BT_F32, nullptr, err, s) != cudaSuccess) {
+            return BT_ERR_CUDA;
+        }
+        const cudaError_t e = pl.implicit ? cudaSuccess :
             x_dtype == BT_F32
                 ? launch_col2im(dt, static_cast<const float *>(x), q, bound, norm, static_cast<__nv_bfloat16 *>(grad_x),
                                 sum, s)
