@@ -742,11 +742,11 @@ struct TileCfg {
     double cost;     // modelled clocks of the whole launch
 };
 
-double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int sms) {
+double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int sms, int splits) {
     const int rows = pair ? 2 * kBM : kBM;
     const int64_t num_m = (M + rows - 1) / rows, num_n = (N + bn - 1) / bn;
     const int64_t units = pair ? sms / 2 : sms;
-    const int64_t tiles = num_m * num_n;
+    const int64_t tiles = num_m * num_n * splits;          // every K split of every tile is a unit of work
     const int64_t rounds = (tiles + units - 1) / units;
     const double mma = (kRowB / 32) * (bn / 2.0);
     const double written = static_cast<double>(kBM + b_slot_rows(bn, pair)) * kRowB;
@@ -761,7 +761,7 @@ double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int
     return static_cast<double>(rounds) * tile + epi + 600.0;
 }
 
-TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn, int out_elem) {
+TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn, int out_elem, int splits) {
     if (const char *env = std::getenv("BT_TC_CONFIG")) {
         int bn = 0, d = 0;
         const bool pair = std::strncmp(env, "pair,", 5) == 0;
@@ -774,7 +774,7 @@ TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn, int ou
         for (int d = 4; d >= 1; d /= 2)
             for (int bn = max_bn; bn >= 32; bn -= 16) {
                 if (num_stages(bn, p == 1, d, out_elem) < 2) continue;
-                const double c = tile_cost(p == 1, bn, d, M, N, slices, sms);
+                const double c = tile_cost(p == 1, bn, d, M, N, slices, sms, splits);
                 if (best.cost < 0.0 || c < best.cost * 0.999) best = TileCfg{p == 1, bn, d, c};
             }
     return best;
@@ -865,6 +865,7 @@ int out_elem_bytes(bt_dtype t) { return t == BT_BF16 || t == BT_F16 ? 2 : 4; }
 // (a multiple of 128) that the caller runs as K splits.
 bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const uint8_t *bp, int64_t M, int64_t N,
           int64_t rb, int64_t pitch_a, int64_t pitch_b, int out_elem, int64_t rb_split = -1) {
+    const int splits = rb_split > 0 ? static_cast<int>(rb / rb_split) : 1;
     if (rb % 16 != 0 || pitch_a % 16 != 0 || pitch_b % 16 != 0 || pitch_a < rb || pitch_b < rb ||
         M > (int64_t(1) << 31) - 512 || N > (int64_t(1) << 31) - 512)
         return false;
@@ -874,7 +875,7 @@ bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const ui
     a.slices = static_cast<int>(((rb_split > 0 ? rb_split : rb) + kRowB - 1) / kRowB);   // per K split
     a.full_slices = static_cast<int>(rb / kRowB);                                       // of the whole row
     const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;       // E2M1 keeps 32 TMEM columns for block scales
-    c = choose_cfg(M, N, a.slices, sm_count(), max_bn, out_elem);
+    c = choose_cfg(M, N, a.slices, sm_count(), max_bn, out_elem, splits);
     a.bn = c.bn;
     a.d = c.d;
     a.nk = (a.slices + a.d - 1) / a.d;
