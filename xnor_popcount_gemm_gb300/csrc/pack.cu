@@ -560,8 +560,8 @@ pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
 // c0 p4 p3) and register bits (p0 p2 p1 c4 c3); three exchange rounds and one
 // shuffle leave lane p with channel c at bit 4 (c % 8) + c / 8, so the codes
 // of channels 8i..8i+7 are one shift and one logic op. Units are numbered with
-// the channel group fastest, so the warps that run at the same time fill
-// whole packed rows; each warp loads its next unit before it converts the
+// the pixel block fastest (the input, 8 to 16 times the output's bytes, is
+// read in runs); each warp loads its next unit before it converts the
 // current one.
 template <typename T, bool CHAN>
 __global__ void __launch_bounds__(kPackThreads)
@@ -584,12 +584,13 @@ pack_nhwc_e2m1_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
     // weights before its own wait, and those may come from the kernel before this one
     pdl_launch_dependents();
     const uint32_t t_all = shift_threshold<T>(bias_len == 1 ? __ldg(bias) : 0.0f);
-    // unit u: channel group cg (fastest), then pixel block blk of image b
+    // unit u: pixel block blk (fastest), then channel group cg of image b, so the
+    // warps that run at the same time read long runs of the same channel planes
     auto decode = [&](uint32_t u, int &cg, int &b, int &blk) {
-        const uint32_t q = fdiv(u, div_ncg);
-        cg = static_cast<int>(u - q * static_cast<uint32_t>(ncg));
-        const uint32_t bi = fdiv(q, div_npb);
-        blk = static_cast<int>(q - bi * static_cast<uint32_t>(npb));
+        const uint32_t q = fdiv(u, div_npb);
+        blk = static_cast<int>(u - q * static_cast<uint32_t>(npb));
+        const uint32_t bi = fdiv(q, div_ncg);
+        cg = static_cast<int>(q - bi * static_cast<uint32_t>(ncg));
         b = static_cast<int>(bi);
     };
     auto load = [&](uint4 (&g)[4][NV], uint32_t u) {
@@ -1147,7 +1148,7 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
             // kernel measured faster on GB300
             if (CODE == BT_CODE_E2M1 && sizeof(T) == 2 && abs_sum == nullptr && nhwc_e2m1_fast() &&
                 (bias_len <= 1 || aligned(bias, 4))) {
-                // channel group fastest: unit u = (b * npb + blk) * ncg + cg; as many
+                // pixel block fastest: unit u = (b * ncg + cg) * npb + blk; as many
                 // blocks as are resident at once (the warps loop over the units), so
                 // that no block waits for a second wave
                 const FastDiv dncg = make_fastdiv(static_cast<uint32_t>(ncg)), dnpb = make_fastdiv(static_cast<uint32_t>(npb));
