@@ -121,10 +121,11 @@ __device__ __forceinline__ uint4 load8_bf16(const T *p) {
 // chunk), pairs rows 2i and 2i+1 column by column with byte permutes, and
 // writes output row 2w + p as the words (w, rows 0..7 in pairs) -- 16 bytes
 // per output row; 16 threads cover a 256-byte output row segment.
-// Needs ldo a multiple of 8; rows whose length C is not a multiple of 8 are
-// read element by element (ALIGNED false). blockIdx.z walks a batch of
-// matrices stored one after the other.
-template <typename T, bool SIGN, bool ALIGNED>
+// Needs ldo a multiple of 8. VEC = 16: rows 16-byte aligned (C a multiple of
+// 8); VEC = 8: a 2-byte copy whose rows are 8-byte aligned (C a multiple of
+// 4), each chunk two 8-byte loads; VEC = 0: element by element. blockIdx.z
+// walks a batch of matrices stored one after the other.
+template <typename T, bool SIGN, int VEC>
 __global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restrict__ in, int64_t R, int64_t C,
                                                                int64_t ldo, uint16_t *__restrict__ out) {
     __shared__ uint4 tile[128 * 16];
@@ -139,8 +140,13 @@ __global__ void __launch_bounds__(kTThreads) transpose8_kernel(const T *__restri
     for (int i = 0; i < 8; ++i) {
         const int k = i * kTThreads + t, rr = k >> 4, q = k & 15;
         const int64_t r = r0 + rr, c = c0 + 8 * q;
-        if constexpr (ALIGNED) {
+        if constexpr (VEC == 16) {
             v[i] = (r < R && c < C) ? load8_bf16<T, SIGN>(in + r * C + c) : make_uint4(0u, 0u, 0u, 0u);
+        } else if constexpr (VEC == 8) {
+            static_assert(sizeof(T) == 2 && !SIGN, "8-byte chunks copy 2-byte elements");
+            const uint2 lo = (r < R && c < C) ? __ldg(reinterpret_cast<const uint2 *>(in + r * C + c)) : make_uint2(0u, 0u);
+            const uint2 hi = (r < R && c + 4 < C) ? __ldg(reinterpret_cast<const uint2 *>(in + r * C + c + 4)) : make_uint2(0u, 0u);
+            v[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
         } else {
             uint32_t w[4] = {0u, 0u, 0u, 0u};
             if (r < R) {
@@ -207,8 +213,12 @@ cudaError_t transpose_t(const void *in, int64_t R, int64_t C, int64_t ldo, uint1
         cfg.gridDim = dim3(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>((ldo + 127) / 128),
                            static_cast<unsigned>(batch));
         if (C % 8 == 0 && aligned(in, 16))
-            return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN, true>, static_cast<const T *>(in), R, C, ldo, out);
-        return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN, false>, static_cast<const T *>(in), R, C, ldo, out);
+            return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN, 16>, static_cast<const T *>(in), R, C, ldo, out);
+        if constexpr (sizeof(T) == 2 && !SIGN) {
+            if (C % 4 == 0 && aligned(in, 8))
+                return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN, 8>, static_cast<const T *>(in), R, C, ldo, out);
+        }
+        return cudaLaunchKernelEx(&cfg, transpose8_kernel<T, SIGN, 0>, static_cast<const T *>(in), R, C, ldo, out);
     }
     cfg.gridDim = dim3(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((ldo + kTile - 1) / kTile),
                        static_cast<unsigned>(batch));
