@@ -729,6 +729,12 @@ def run_backward(args, rank, world):
         g_shape = (M, N)
         if N % 8 or K % 8:
             raise SystemExit("--pass backward needs N and K multiples of 8")
+    if conv and bt.bt_conv2d_backward_implicit(B, C, H, W, O, k, wl.stride, wl.padding, wl.dilation):
+        dgrad_label = "the input-gradient call (g per pixel, codes of x, one implicit GEMM with the mask in its epilogue)"
+    elif conv:
+        dgrad_label = "the input-gradient call (g per pixel, product over the unfolded taps, gather with the mask)"
+    else:
+        dgrad_label = "the input-gradient call (product with the mask fused in its epilogue)"
     stream = torch.cuda.current_stream()
     gen = torch.Generator().manual_seed(1000)
     g_host = (torch.randn(*g_shape, generator=gen) * 0.01).to(torch.bfloat16)
@@ -806,7 +812,7 @@ def run_backward(args, rank, world):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
                      "peak_source": f"{peak_src}: cuBLAS bf16 burst",
-                     "kernel": "the input-gradient call (contraction + fused mask" + (", col2im" if conv else "") + ")"},
+                     "kernel": dgrad_label},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }

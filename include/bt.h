@@ -448,6 +448,15 @@ size_t bt_binary_conv2d_backward_workspace(int64_t B, int64_t C, int64_t H, int6
                                            int stride, int padding, int dilation, int want_grad_input,
                                            int want_grad_weight);
 
+/* bt_conv2d_backward_implicit -- 1 when bt_binary_conv2d_backward computes
+ * grad_x of this geometry as one implicit GEMM over the stride's sub-pixel
+ * phases (O a multiple of 64, stride <= 4, kernel_size <= 8, the phases'
+ * staged bands fit; BT_CONV_DGRAD=gather in the environment turns it off),
+ * 0 when it takes the tap matrix and gather route. Host-side planning only:
+ * touches no device. */
+int bt_conv2d_backward_implicit(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
+                                int padding, int dilation);
+
 /*
  * bt_binary_conv2d_backward -- the straight-through backward of the binary
  * conv2d layer, BinaryConv2dForward.backward step by step:
@@ -464,9 +473,13 @@ size_t bt_binary_conv2d_backward_workspace(int64_t B, int64_t C, int64_t H, int6
  *          (overwritten) or NULL, needs grad_x; grad_w [O, C, k, k] BF16 or
  *          F32 (the fp32 sums before the rounding) out, or NULL;
  *   workspace  bt_binary_conv2d_backward_workspace(...) bytes, 256-byte aligned.
- * The two convolution gradients run as tensor-core products (bf16 operands,
- * fp32 accumulators) over the unfolded taps; the input gradient gathers its
- * taps in fp32 and rounds once. O a multiple of 8, B <= 65535; scales finite
+ * Both gradients run on the tensor cores (bf16 operands, fp32 accumulators).
+ * grad_x: where bt_conv2d_backward_implicit says so, one implicit GEMM whose
+ * tiles reduce over the taps of each sub-pixel phase (the bf16 rounding, mask
+ * and grad_scale_a terms in its epilogue); else a product over the unfolded
+ * taps, then a gather that sums each element's taps in fp32 and rounds once.
+ * grad_w: a product over the unfolded signs of x, split along the pixels and
+ * summed in fp32. O a multiple of 8, B <= 65535; scales finite
  * > 0; pointers 16-byte aligned device memory owned by the caller;
  * asynchronous on `stream`. Errors: INVALID_ARG, ALIGNMENT, WORKSPACE,
  * UNSUPPORTED (O not a multiple of 8, sizes beyond the limits, no tensor

@@ -356,3 +356,23 @@ def test_first_forward_validation():
     assert conv(ws=None) == bt.BT_ERR_WORKSPACE
     assert conv(B=0) == bt.BT_OK
 
+
+
+def test_conv2d_backward_implicit_query(monkeypatch):
+    # host-side planning only: which route computes grad_x of a geometry
+    q = bt.bt_conv2d_backward_implicit
+    assert q(256, 128, 28, 28, 256, 3, 2, 1, 1)          # the stride-2 layer: four sub-pixel phases
+    assert q(128, 256, 14, 14, 256, 3, 1, 1, 1)          # the stride-1 layer
+    assert q(256, 128, 28, 28, 256, 3, 2, 2, 2)          # one phase with all nine taps, three with none
+    assert not q(2, 8, 9, 9, 16, 3, 1, 1, 1)             # O not a multiple of 64: tap matrix + gather
+    assert not q(2, 8, 9, 9, 64, 3, 5, 1, 1)             # stride above 4
+    assert not q(1, 8, 4, 600, 64, 3, 1, 1, 1)           # rows wider than a staged band
+    assert not q(0, 8, 9, 9, 64, 3, 1, 1, 1) and not q(2, 8, 9, 9, 64, 3, 1, 1, 0)
+    # the workspace follows the route: g per pixel plus the codes of x, or plus the tap matrix
+    ws = bt.bt_binary_conv2d_backward_workspace(2, 8, 9, 9, 64, 3, 1, 1, 1, True, False)
+    g_bytes, codes = -(-2 * 81 * 64 * 2 // 256) * 256, -(-2 * 81 * 16 // 256) * 256
+    assert ws == g_bytes + codes
+    monkeypatch.setenv("BT_CONV_DGRAD", "gather")
+    assert not q(256, 128, 28, 28, 256, 3, 2, 1, 1)
+    assert bt.bt_binary_conv2d_backward_workspace(2, 8, 9, 9, 64, 3, 1, 1, 1, True, False) == \
+        g_bytes + -(-8 * 9 * 2 * 81 * 4 // 256) * 256

@@ -289,6 +289,7 @@ def test_conv_backward_input_gradient_routes(B, C, H, W, O, k, s, p, d, route, m
     codes = -(-B * H * W * -(-C // 32) * 16 // 256) * 256
     ws = bt.bt_binary_conv2d_backward_workspace(B, C, H, W, O, k, s, p, d, True, False)
     assert ws == (g_bytes + -(-C * k * k * B * ho * wo * 4 // 256) * 256 if route == "gather" else g_bytes + codes)
+    assert bt.bt_conv2d_backward_implicit(B, C, H, W, O, k, s, p, d) == (route != "gather")
     x_dtype = torch.float32 if (B + C + k) % 2 else torch.bfloat16
     differ = _conv_run_and_compare(B, C, H, W, O, k, s, p, d, x_dtype, torch.bfloat16, seed=B * C + H + s)
     assert differ.mean() < 0.01

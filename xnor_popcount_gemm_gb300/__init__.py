@@ -74,6 +74,7 @@ _c_bwd_ws = _sig("bt_binary_linear_backward_workspace", _sz, [_i64, _i64, _i64, 
 _c_bwd = _sig("bt_binary_linear_backward", _i, [_p, _i, _p, _i64, _p, _i64, _i64, _i64, _f, _f, _p, _p, _p, _i,
                                                 _p, _sz, _p])
 _c_cbwd_ws = _sig("bt_binary_conv2d_backward_workspace", _sz, [_i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _i])
+_c_cbwd_impl = _sig("bt_conv2d_backward_implicit", _i, [_i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i])
 _c_cbwd = _sig("bt_binary_conv2d_backward", _i, [_p, _i, _p, _i64, _p, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i,
                                                  _f, _f, _p, _p, _p, _i, _p, _sz, _p])
 _c_scale_init = _sig("bt_scale_init", _i, [_p, _i, _i64, _f, _i, _p, _p])
@@ -98,7 +99,8 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
             "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
-            "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_binary_conv2d_backward",
+            "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_conv2d_backward_implicit",
+            "bt_binary_conv2d_backward",
             "bt_scale_init", "bt_binary_linear_dscale", "bt_binary_conv2d_dscale", "bt_w8a8_conv2d_workspace",
             "bt_w8a8_conv2d", "bt_set_wait_timeout", "bt_binary_linear_dscale_init", "bt_binary_conv2d_dscale_init"]
 
@@ -262,6 +264,13 @@ def bt_binary_conv2d_backward_workspace(B: int, C: int, H: int, W: int, O: int, 
                                         want_grad_weight: bool = True) -> int:
     return int(_c_cbwd_ws(B, C, H, W, O, kernel_size, stride, padding, dilation, 1 if want_grad_input else 0,
                           1 if want_grad_weight else 0))
+
+
+def bt_conv2d_backward_implicit(B: int, C: int, H: int, W: int, O: int, kernel_size: int, stride: int, padding: int,
+                                dilation: int) -> bool:
+    """Whether bt_binary_conv2d_backward computes grad_x of this geometry as
+    one implicit GEMM (else the tap matrix and gather route)."""
+    return bool(_c_cbwd_impl(B, C, H, W, O, kernel_size, stride, padding, dilation))
 
 
 def bt_binary_conv2d_backward(x: torch.Tensor, wst: torch.Tensor | None, g: torch.Tensor, O: int, kernel_size: int,

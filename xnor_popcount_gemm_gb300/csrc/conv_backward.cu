@@ -356,6 +356,15 @@ size_t bt_binary_conv2d_backward_workspace(int64_t B, int64_t C, int64_t H, int6
     return need;
 }
 
+int bt_conv2d_backward_implicit(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
+                                int padding, int dilation) {
+    ConvBwdPlan pl;
+    if (B < 1 || C < 1 || H < 1 || W < 1 || O < 1 || kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1 ||
+        !make_plan(B, C, H, W, O, kernel_size, stride, padding, dilation, pl))
+        return 0;
+    return pl.implicit ? 1 : 0;
+}
+
 bt_status bt_binary_conv2d_backward(const void *x, bt_dtype x_dtype, const void *wst, int64_t ldw, const void *g,
                                     int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
                                     int padding, int dilation, float scale_a, float scale_w, void *grad_x,
