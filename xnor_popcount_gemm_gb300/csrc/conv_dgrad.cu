@@ -272,7 +272,7 @@ dgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CU
             // chunk q of the band into slot gs: once per unit where the chunks stay
             // resident (slot q), else once per phase through the two-slot ring
             auto load_g = [&](const Unit &t, int q, int slot, uint32_t parity) {
-                if (!tc::wait_bounded(gempty(slot), parity ^ 1u, abort_flag, a.err, a.wait_ns)) return false;
+                if (!tc::wait_fast(gempty(slot), parity ^ 1u, abort_flag, a.err, a.wait_ns)) return false;
                 const uint32_t gdst = sG + static_cast<uint32_t>(slot) * a.gslot;
                 tc::mbar_arrive_expect_tx(gfull(slot), a.gbytes);
                 if (a.multi) {
@@ -300,7 +300,7 @@ dgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CU
                             if (++gs == 2) { gs = 0; gph ^= 1u; }
                         }
                         for (int i = 0; i < nt; ++i) {
-                            if (!tc::wait_bounded(wempty(ws), wph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                            if (!tc::wait_fast(wempty(ws), wph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                             const uint32_t wdst = sW + static_cast<uint32_t>(ws) * a.wslot;
                             const int tw = a.tap_w[a.ph_tap0[p] + i];
                             tc::mbar_arrive_expect_tx(wfull(ws), a.wbytes);
@@ -349,7 +349,7 @@ dgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CU
                 if (nt == 0) continue;
                 const int buf = local & 1;
                 if (local >= 2) {
-                    if (!tc::wait_bounded(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag,
+                    if (!tc::wait_fast(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag,
                                           a.err, a.wait_ns)) { ok = false; break; }
                     tc::fence_after_sync();
                 }
@@ -358,12 +358,12 @@ dgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CU
                 for (int q = 0; q < a.nchunks && ok; ++q) {
                     const int slot = a.resident ? q : gs;
                     if (!a.resident || p == a.ph_first) {
-                        if (!tc::wait_bounded(gfull(slot), gph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                        if (!tc::wait_fast(gfull(slot), gph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                         tc::fence_after_sync();
                     }
                     const uint32_t gA = sG + static_cast<uint32_t>(slot) * a.gslot;
                     for (int i = 0; i < nt; ++i) {
-                        if (!tc::wait_bounded(wfull(ws), wph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                        if (!tc::wait_fast(wfull(ws), wph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                         tc::fence_after_sync();
                         const uint32_t wB = sW + static_cast<uint32_t>(ws) * a.wslot;
                         const uint32_t shift = static_cast<uint32_t>(a.tap_shift[a.ph_tap0[p] + i]);
@@ -433,7 +433,7 @@ dgrad_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CU
                 const bool has = a.ph_ntap[p] > 0;
                 const int buf = local & 1;
                 if (has) {
-                    if (!tc::wait_bounded(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err,
+                    if (!tc::wait_fast(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err,
                                           a.wait_ns)) { ok = false; break; }
                     tc::fence_after_sync();
                 }

@@ -539,7 +539,7 @@ __device__ __forceinline__ void pack_tiles(const ConvArgs &a, uint32_t sB, uint3
         const int b = rest / bands, band = rest - b * bands;
         const int r0 = band * ht + row_first;             // this CTA's first row of the band
         if (prefetch && pw == 0 && t + nunits < num_tiles) prefetch_tile(t + nunits);
-        if (!tc::wait_bounded(bempty(bs), bph ^ 1u, abort_flag, a.err, a.wait_ns)) break;
+        if (!tc::wait_fast(bempty(bs), bph ^ 1u, abort_flag, a.err, a.wait_ns)) break;
         const uint32_t stage = sB + static_cast<uint32_t>(bs) * stage_bytes;
         if (a.zero_rows) {
             // staged rows above or below the image: a tile of another band may have filled them
@@ -719,7 +719,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const int am0 = ot * static_cast<int>(kPeers) * kBM + ch_first;
                 // the tile's phase images (the packing warps fill them from x instead)
                 if (!kFused) {
-                    if (!tc::wait_bounded(bempty(bs), bph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                    if (!tc::wait_fast(bempty(bs), bph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                     if (leader) tc::mbar_arrive_expect_tx(bfull(bs), kPeers * static_cast<uint32_t>(a.nph * a.nsl) * a.img_tx);
                     const uint32_t dst0 = sB + static_cast<uint32_t>(bs) * a.stage_bytes;
                     const uint32_t fbar = lead(bfull(bs));
@@ -736,7 +736,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (a.a_resident && !a_loaded) load_weights(ot);
                 if (!a.a_resident) {
                     for (int i0 = 0; i0 < nslices; i0 += a.a_d) {
-                        if (!tc::wait_bounded(aempty(as), aph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                        if (!tc::wait_fast(aempty(as), aph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                         if (leader) tc::mbar_arrive_expect_tx(afull(as), kPeers * static_cast<uint32_t>(a.a_d) * kASlice);
                         const uint32_t dst = sA + static_cast<uint32_t>(as * a.a_d) * kASlice;
                         if (CP) tc::tma_load_3d_pair(dst, &tmA, 0, am0, i0, lead(afull(as)));
@@ -784,11 +784,11 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 const int buf = local & 1;
                 if (local >= 2) {
                     // the epilogue (of both CTAs of a pair) has drained this buffer
-                    if (!tc::wait_bounded(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err, a.wait_ns))
+                    if (!tc::wait_fast(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err, a.wait_ns))
                         break;
                     tc::fence_after_sync();
                 }
-                if (!tc::wait_bounded(bfull(bs), bph, abort_flag, a.err, a.wait_ns)) break;
+                if (!tc::wait_fast(bfull(bs), bph, abort_flag, a.err, a.wait_ns)) break;
                 tc::fence_after_sync();
                 const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * kAccStride;
                 if (reg_taps) {
@@ -803,7 +803,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             if (local == 0) {
                                 const int bx = a.a_boxes <= kMaxAStages ? static_cast<int>(a.tap[t] >> 24) / a.a_d : 0;
                                 if (!((waited >> bx) & 1u)) {
-                                    if (!tc::wait_bounded(afull(bx), 0u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                                    if (!tc::wait_fast(afull(bx), 0u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                                     tc::fence_after_sync();
                                     waited |= 1u << bx;
                                 }
@@ -847,14 +847,14 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                 // barrier, or all on the first)
                                 const int bx = a.a_boxes <= kMaxAStages ? sidx / a.a_d : 0;
                                 if (!((waited >> bx) & 1u)) {
-                                    if (!tc::wait_bounded(afull(bx), 0u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                                    if (!tc::wait_fast(afull(bx), 0u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                                     tc::fence_after_sync();
                                     waited |= 1u << bx;
                                 }
                             }
                             adesc = adesc_base + static_cast<uint64_t>(sidx) * kSlice16;
                         } else if (within == 0) {
-                            if (!tc::wait_bounded(afull(as), aph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                            if (!tc::wait_fast(afull(as), aph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                             tc::fence_after_sync();
                             adesc = adesc_base + static_cast<uint64_t>(as * a.a_d) * kSlice16;
                         }
@@ -920,7 +920,7 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const int r0 = band * a.ht;
             const int hte = a.Ho - r0 < a.ht ? a.Ho - r0 : a.ht;       // output rows of this band
             const int buf = local & 1;
-            if (!tc::wait_bounded(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err, a.wait_ns)) break;
+            if (!tc::wait_fast(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err, a.wait_ns)) break;
             tc::fence_after_sync();
             const int o0 = ot * static_cast<int>(kPeers) * kBM + ch_first + quarter * 32;   // this warp's first channel
             const int nrows = a.O - o0 < 32 ? a.O - o0 : 32;

@@ -397,7 +397,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                 const int am0 = mt * kTileRows + a_first;
                 const int bn0 = nt * bn + b_first;
                 for (int kb = 0; kb < a.nk; ++kb) {
-                    if (!tc::wait_bounded(empty(s), ph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                    if (!tc::wait_fast(empty(s), ph ^ 1u, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                     const uint32_t adst = sA + s * kAStage, bdst = sB + s * kBStage;
                     const uint32_t fbar = PAIR ? tc::mapa(full(s), 0u) : full(s);
                     const int k0 = sp * a.slices + kb * D;
@@ -454,13 +454,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
                 const int buf = local & 1;
                 if (local >= 2) {
                     // the epilogue (of both CTAs of a pair) has drained this buffer
-                    if (!tc::wait_bounded(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err, a.wait_ns))
+                    if (!tc::wait_fast(tempty(buf), static_cast<uint32_t>((local - 2) >> 1) & 1u, abort_flag, a.err, a.wait_ns))
                         break;
                     tc::fence_after_sync();
                 }
                 const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * acc_stride<CODE>();
                 for (int kb = 0; kb < a.nk; ++kb) {
-                    if (!tc::wait_bounded(full(s), ph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
+                    if (!tc::wait_fast(full(s), ph, abort_flag, a.err, a.wait_ns)) { ok = false; break; }
                     tc::fence_after_sync();
                     const int cnt = slice_count(kb);
                     // descriptors built per MMA from 32-bit addresses (measured on GB300:
@@ -515,7 +515,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
             const int64_t m0 = static_cast<int64_t>(mt) * kTileRows + (PAIR ? static_cast<int64_t>(crank) * kBM : 0);
             const int n0 = nt * bn;
             const int buf = local & 1;
-            if (!tc::wait_bounded(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err, a.wait_ns)) break;
+            if (!tc::wait_fast(tfull(buf), static_cast<uint32_t>(local >> 1) & 1u, abort_flag, a.err, a.wait_ns)) break;
             tc::fence_after_sync();
             bool released = false;
             auto release = [&]() {
