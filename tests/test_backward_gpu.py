@@ -166,9 +166,13 @@ def test_linear_backward_partial_requests_and_empty():
     assert gxe.numel() == 0 and float(gsae.cpu()) == 0.0 and torch.all(gwe.cpu() == 0)
 
 
+@pytest.mark.parametrize("epi", ["4", "8"], ids=["epi4", "epi8"])
 @pytest.mark.parametrize("cfg", ["pair,224,2", "pair,128,2", "224,2", "128,4", "64,1", "pair,256,1"])
-def test_linear_backward_tile_configs(cfg, monkeypatch):
+def test_linear_backward_tile_configs(cfg, epi, monkeypatch):
+    # epi: one or two epilogue warps per TMEM lane quarter (the masked layouts
+    # run two unless forced)
     monkeypatch.setenv("BT_TC_CONFIG", cfg)
+    monkeypatch.setenv("BT_TC_EPI", epi)
     x, w, g, sa, sw, gx, gsa, gw = _run(300, 264, 520, torch.bfloat16, torch.bfloat16, seed=11)
     _compare(x, w, g, sa, sw, gx, gsa, gw, "bf16")
 

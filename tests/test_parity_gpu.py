@@ -450,10 +450,15 @@ TC_CONFIGS = ["240,1", "224,2", "128,4", "64,2", "32,1", "208,2", "96,4", "224,3
               "pair,224,3", "pair,240,3"]
 
 
+@pytest.mark.parametrize("epi", ["4", "8"], ids=["epi4", "epi8"])
 @pytest.mark.parametrize("cfg", TC_CONFIGS)
 @pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
-def test_linear_tc_configs(cfg, code, monkeypatch):
+def test_linear_tc_configs(cfg, code, epi, monkeypatch):
+    # epi: epilogue warps, one or two per TMEM lane quarter (BT_TC_EPI forces
+    # either; the planner takes one for aligned rows and long K), on aligned
+    # (N = 600, 200, 520) and ragged (N = 330) rows
     monkeypatch.setenv("BT_TC_CONFIG", cfg)
+    monkeypatch.setenv("BT_TC_EPI", epi)
     for (M, N, K) in ((700, 600, 1000), (1100, 330, 4100), (300, 200, 100), (260, 520, 700)):
         x = _gen(M + K, (M, K), torch.bfloat16)
         w = _gen(N + K, (N, K), torch.bfloat16)

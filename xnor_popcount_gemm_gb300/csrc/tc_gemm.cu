@@ -68,15 +68,18 @@ namespace {
 
 constexpr int kBM = 128;                         // rows of A per CTA (= MMA M per CTA)
 constexpr int kRowB = 128;                       // bytes of a K slice
-constexpr int kEpiWarps = 8;                     // two per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer, MMA, epilogue warps
+constexpr int kEpiWarps = 8;                     // at most two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer, MMA, epilogue warps (the most a launch takes)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 480;                 // 32 columns of unit block scales (E2M1)
 constexpr uint32_t kUnitScales = 0x7F7F7F7Fu;    // UE8M0 127 = 2^0 in every byte
 constexpr int kSmemMax = 232448;                 // 227 KB opt-in per CTA
 // One staging box per epilogue warp: 32 rows x 32 outputs (4 KB for 4-byte
 // outputs, 2 KB for 2-byte ones).
-__host__ __device__ constexpr int staging_bytes(int out_elem) { return kEpiWarps * 32 * 32 * out_elem; }
+// Epilogue staging: one 32 x 32 box of outputs per epilogue warp.
+__host__ __device__ constexpr int staging_bytes(int out_elem, int epi_warps = kEpiWarps) {
+    return epi_warps * 32 * 32 * out_elem;
+}
 constexpr int kReserve = 1024 /*alignment*/ + 256 /*barriers*/;
 constexpr int kMaxStages = 8;
 
@@ -104,6 +107,7 @@ struct TcArgs {
                                // NCHW: bytes each lane stores at once (a run of one channel's pixels)
     int64_t hw;                // NCHW: output pixels per image (Ho * Wo)
     int stages;                // smem ring depth
+    int epi_warps;             // epilogue warps of this launch: 4 (one per TMEM lane quarter) or 8 (two)
     const void *aux;           // masked layouts: x [M, N]
     float aux_scale;           // masked layouts: scale_a
     float aux_norm;            // masked layouts: 1 / sqrt(numel(x)), fp32
@@ -116,12 +120,13 @@ __host__ __device__ __forceinline__ int b_slot_rows(int bn, bool pair) { return 
 // Shared memory: S stages of D slices of A (128 rows) and B, the epilogue
 // staging boxes, barriers. S is as many stages as fit (at most 8).
 int stage_bytes(int bn, bool pair, int d) { return (kBM + b_slot_rows(bn, pair)) * kRowB * d; }
-int num_stages(int bn, bool pair, int d, int out_elem) {
-    const int s = (kSmemMax - kReserve - staging_bytes(out_elem)) / stage_bytes(bn, pair, d);
+int num_stages(int bn, bool pair, int d, int out_elem, int epi_warps = kEpiWarps) {
+    const int s = (kSmemMax - kReserve - staging_bytes(out_elem, epi_warps)) / stage_bytes(bn, pair, d);
     return s > kMaxStages ? kMaxStages : s;
 }
-int smem_bytes(int bn, bool pair, int d, int out_elem) {
-    return num_stages(bn, pair, d, out_elem) * stage_bytes(bn, pair, d) + staging_bytes(out_elem) + kReserve;
+int smem_bytes(int bn, bool pair, int d, int out_elem, int epi_warps = kEpiWarps) {
+    return num_stages(bn, pair, d, out_elem, epi_warps) * stage_bytes(bn, pair, d) + staging_bytes(out_elem, epi_warps) +
+           kReserve;
 }
 
 // TMEM column of the second accumulator buffer; also the largest BN.
@@ -308,7 +313,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sA = base, sB = base + S * kAStage;
     const uint32_t sStage = sB + S * kBStage;                        // epilogue staging boxes
-    const uint32_t bars = sStage + staging_bytes(kElem);             // full[S], empty[S], tfull[2], tempty[2], drain
+    const uint32_t bars = sStage + staging_bytes(kElem, a.epi_warps);   // full[S], empty[S], tfull[2], tempty[2], drain
     uint8_t *gbars = smem_raw + (bars - raw);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbars + 8 * (2 * kMaxStages + 5));
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -331,7 +336,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(tfull(b), 1);
             // one arrival per epilogue warp (of both CTAs of a pair)
-            tc::mbar_init(tempty(b), static_cast<uint32_t>(PAIR ? 2 * kEpiWarps : kEpiWarps));
+            tc::mbar_init(tempty(b), static_cast<uint32_t>(PAIR ? 2 * a.epi_warps : a.epi_warps));
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0u;
@@ -533,12 +538,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmA3, const __grid_constant__ CUte
             const int nbox = ncols > 0 ? static_cast<int>((ncols + 31) / 32) : 0;
             const int64_t mrow0 = m0 + quarter * 32;                         // this warp's first row
             // the two warps of a lane quarter take alternate 32-column boxes
-            const int half = (warp - 2) / 4;
-            const int total = mrow0 < a.M && nbox > half ? (nbox - half + 1) / 2 : 0;   // this warp's boxes
+            // the warps of a lane quarter take its 32-column boxes in turn
+            const int wpq = a.epi_warps / 4, half = (warp - 2) / 4;
+            const int total = mrow0 < a.M && nbox > half ? (nbox - half + wpq - 1) / wpq : 0;   // this warp's boxes
             const uint32_t tbase = tmem + lane_base + static_cast<uint32_t>(buf) * acc_stride<CODE>();
-            auto tcol_of = [&](int j) { return tbase + static_cast<uint32_t>(32 * (2 * j + half)); };
+            auto tcol_of = [&](int j) { return tbase + static_cast<uint32_t>(32 * (wpq * j + half)); };
             auto emit = [&](const uint32_t (&r)[32], int j) {
-                const int c0 = 32 * (2 * j + half);
+                const int c0 = 32 * (wpq * j + half);
                 // masked layouts: this lane's x chunks (the rows and columns of the
                 // 16-byte chunks it stores below) go in flight before the staging
                 XChunk<LAYOUT == kRowsMaskF32 ? kRowsMaskF32 : kRowsMaskBf16> xc[4];
@@ -778,12 +784,32 @@ struct Maps {
     CUtensorMap a3, b3, a2, b2;
 };
 
+// Epilogue warps of a launch, and with them the staging (one 32 x 32 box per
+// warp). The forward linears take one per TMEM lane quarter where each tile's
+// output rows are 16-byte aligned (whole-chunk stores) and its main loop (>= 8
+// K slices) hides the slower epilogue: the smaller staging keeps the CTA's
+// shared memory under the next carveout step (measured on GB300, same box: the
+// 8192x4096x11008 step 149 -> 141 us and the 4096^3 one 33.3 -> 31.5 us with
+// four-warp staging, whether or not the launch bound changed; eight warps with
+// eight-warp staging 148.8 / 32.9). Ragged rows (element stores) and the other
+// layouts keep two per quarter (the ragged linear measured 90 us with two,
+// 118 with one). BT_TC_EPI=4 or 8 in the environment forces either.
+int epilogue_warps(int code, int layout, const TcArgs &a) {
+    if (const char *env = std::getenv("BT_TC_EPI")) {
+        if (std::strcmp(env, "4") == 0) return 4;
+        if (std::strcmp(env, "8") == 0) return 8;
+    }
+    const bool forward = code == BT_CODE_E2M1 || code == BT_CODE_E4M3;
+    return forward && layout == kRowsOut && a.vec && a.slices >= 8 ? 4 : 8;
+}
+
 template <int CODE, int LAYOUT, int OUT, bool PAIR>
 cudaError_t launch_t(const Maps &mp, TcArgs a, cudaStream_t s) {
     auto kern = tc_kernel<CODE, LAYOUT, OUT, PAIR>;
-    a.stages = num_stages(a.bn, PAIR, a.d, static_cast<int>(sizeof(typename OutT<OUT>::type)));
+    a.epi_warps = epilogue_warps(CODE, LAYOUT, a);
+    a.stages = num_stages(a.bn, PAIR, a.d, static_cast<int>(sizeof(typename OutT<OUT>::type)), a.epi_warps);
     a.wait_ns = wait_limit_ns();
-    const int smem = smem_bytes(a.bn, PAIR, a.d, static_cast<int>(sizeof(typename OutT<OUT>::type)));
+    const int smem = smem_bytes(a.bn, PAIR, a.d, static_cast<int>(sizeof(typename OutT<OUT>::type)), a.epi_warps);
     if (a.stages < 2 || smem > kSmemMax) return cudaErrorInvalidValue;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -792,7 +818,7 @@ cudaError_t launch_t(const Maps &mp, TcArgs a, cudaStream_t s) {
     const int csize = PAIR ? 2 : 1;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(64 + 32 * a.epi_warps), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     attr[0] = pdl_attribute();
@@ -805,20 +831,21 @@ cudaError_t launch_t(const Maps &mp, TcArgs a, cudaStream_t s) {
     // as many units (CTAs, or pairs) as fit at once on the device, at most one per tile
     int units = sm_count() / csize;
     if (PAIR) {
-        // how many pairs fit at once: one query per device and shared-memory size
+        // how many pairs fit at once: one query per device, shared-memory size and block size
         static std::mutex mu;
         static int cached_smem[128] = {}, cached_fit[128] = {};
+        const int key = smem * 16 + a.epi_warps;
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) dev = 0;
         int fit = 0;
         {
             std::lock_guard<std::mutex> lock(mu);
-            if (cached_smem[dev] == smem) {
+            if (cached_smem[dev] == key) {
                 fit = cached_fit[dev];
             } else {
                 cfg.gridDim = dim3(static_cast<unsigned>(units * csize), 1, 1);
                 if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess) fit = 0;
-                cached_smem[dev] = smem;
+                cached_smem[dev] = key;
                 cached_fit[dev] = fit;
             }
         }
