@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", default="auto", choices=["auto", "popc", "e4m3", "e2m1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-tune", action="store_true",
+                    help="linear layers: skip the measured selection (bt_tune_linear) and take the cost model's shape")
+    ap.add_argument("--tune-reps", type=int, default=10, help="timed calls per candidate launch shape")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the record of every configuration (all_configs) after the headline")
     ap.add_argument("--config-steps", type=int, default=20, help="timed steps per configuration and code")
@@ -431,6 +434,37 @@ CONFIG_ORDER = ["tiny_linear", "llm_linear", "resnet_conv", "downsample_conv", "
                 "large_linear", "ragged_linear"]
 
 
+def tune_linear(bt, wl, dev, reps: int) -> dict:
+    """The measured "ADAPTIVE" selection of a linear workload, before any
+    warm-up or timing: bt_tune_linear times the contraction call as a step
+    makes it (packed x) in every candidate launch shape of each tensor-core
+    code, and the popcount kernel, keeping the fastest shape per code; bt_plan
+    then names the fastest code for the size."""
+    M, N, K = wl.gemm_shape()
+    out_t = {"f32": torch.float32, "bf16": torch.bfloat16}[wl.out_dtype]
+    xd = wl.x.to(dev)
+    bias = None if wl.bias is None else wl.bias.to(dev)
+    per = {}
+    for code in (2, 1, 0):
+        if code != 0 and K > 16384:
+            continue
+        wp = bt.bt_pack_sign(wl.w.to(dev), code)
+        xp = bt.bt_pack_sign(xd, code, bt.BT_LAYOUT_ROWS, bias)
+        r = bt.bt_tune_linear(xp, wp, code, K, wl.scale_a, wl.scale_w, out_dtype=out_t, x_packed=True,
+                              reps=reps if code != 0 else max(1, reps // 5))
+        shape = (f"{'pair' if r['pair'] else 'single'} bn{r['bn']} d{r['slices_per_stage']} "
+                 f"epi{r['epilogue_warps']}" if code != 0 else "popcount kernel")
+        per[ALGO_NAME[code]] = {"us": round(r["us"], 2), "us_cost_model_shape": round(r["us_model"], 2),
+                                "kept": shape, "candidates": r["candidates"]}
+        del wp, xp
+    del xd
+    torch.cuda.empty_cache()
+    code, _ = bt.bt_plan(bt.BT_OP_LINEAR, M, N, K)
+    return {"code": ALGO_NAME[code], "per_code": per,
+            "how": "bt_tune_linear: mean of the timed contraction calls per launch shape (CUDA events); "
+                   "bt_plan names the code with the shortest"}
+
+
 def sweep_configs(bt, dev, peaks, peak_src, sms, args) -> dict:
     """Every configuration, each code the library has (the planner's choice
     first): graph-replayed step time, the pack / contraction split, and the
@@ -444,6 +478,7 @@ def sweep_configs(bt, dev, peaks, peak_src, sms, args) -> dict:
         M, N, K = wl.gemm_shape()
         ops = wl.binary_ops()
         op = bt.BT_OP_LINEAR if wl.kind == "linear" else bt.BT_OP_CONV2D
+        sel = tune_linear(bt, wl, dev, args.tune_reps) if wl.kind == "linear" and not args.no_tune else None
         plan_code, _ = bt.bt_plan(op, M, N, K)
         codes = [plan_code] + [c for c in (2, 1, 0) if c != plan_code]
         per_code, rec = {}, None
@@ -473,6 +508,8 @@ def sweep_configs(bt, dev, peaks, peak_src, sms, args) -> dict:
             torch.cuda.empty_cache()
         if bt.bt_device_status() != 0:
             raise RuntimeError(f"device status after {name}")
+        if sel is not None:
+            rec["selection"] = sel
         rec["step_us_per_code"] = per_code
         rec["fastest_code"] = min(per_code, key=per_code.get)
         rec["planner_picks_fastest"] = rec["fastest_code"] == rec["code"]
@@ -491,6 +528,9 @@ def run_ours(args, rank, world):
     M, N, K = wl.gemm_shape()
     ops = wl.binary_ops()
     op = bt.BT_OP_LINEAR if wl.kind == "linear" else bt.BT_OP_CONV2D
+    selection = None
+    if wl.kind == "linear" and not args.no_tune:
+        selection = tune_linear(bt, wl, dev, args.tune_reps)
     if args.algo == "auto":
         code, algo = bt.bt_plan(op, M, N, K)
     else:
@@ -566,6 +606,7 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(e2e_ms, 4),
                 "how": f"pinned host buffers (x{nh} rotating); copy-in, forward, copy-out on three streams, "
                        "neighbouring steps overlapped"},
+        "selection": selection if selection is not None else "the cost model's launch shape (not measured)",
         "gpu_launches": su.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }

@@ -304,12 +304,57 @@ size_t bt_binary_linear_noalloc_max_bytes(void);
 
 /*
  * bt_plan -- the "ADAPTIVE" choice: the code (weight format) and kernel this
- * build runs fastest for a problem of this size, from measurements on GB300.
- * For BT_OP_LINEAR pass (M, N, K); for BT_OP_CONV2D pass M = B*Ho*Wo, N = O,
- * K = C*k*k. Returns BT_ERR_INVALID_ARG for null outputs or sizes < 1.
+ * build runs fastest for a problem of this size. For BT_OP_LINEAR pass
+ * (M, N, K); for BT_OP_CONV2D pass M = B*Ho*Wo, N = O, K = C*k*k. A linear
+ * size that bt_tune_linear has timed in this process, on the current device,
+ * gets the code with the shortest measured call among those timed; any other
+ * size the fixed rule measured on GB300 (E2M1 up to K = 16384, else BITS).
+ * Returns BT_ERR_INVALID_ARG for null outputs or sizes < 1.
  * The environment variable BT_FORCE_ALGO=popc|e4m3|e2m1 overrides it.
  */
 bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo);
+
+/* What bt_tune_linear measured and kept. */
+typedef struct {
+    bt_code code;              /* the weight's code that was timed */
+    int pair;                  /* tensor-core codes: 1 = 256-row tiles on CTA pairs (cta_group::2) */
+    int bn;                    /* tensor-core codes: output columns per tile */
+    int slices_per_stage;      /* tensor-core codes: 128-byte K slices per pipeline stage */
+    int epilogue_warps;        /* tensor-core codes: 4 or 8 */
+    int candidates;            /* launch shapes timed (1 for BT_CODE_BITS) */
+    float us;                  /* mean microseconds of one call in the kept shape */
+    float us_model;            /* the same for the shape the cost model picks unmeasured */
+} bt_tune_result;
+
+/*
+ * bt_tune_linear -- the measured form of the "ADAPTIVE" choice
+ * (BinaryLinearCuda: bmm_type defaults to BMM.ADAPTIVE, which selects the
+ * binary matrix-multiply kernel for the caller). Arguments as
+ * bt_binary_linear (algo AUTO). For the tensor-core codes it runs the call
+ * once untimed and `reps` times timed per candidate launch shape (the cost
+ * model's own pick first, then the cheapest tile width by the model for every
+ * other pairing and stage depth, each with 4 and 8 epilogue warps), with CUDA
+ * events on `stream`, and keeps the fastest: later bt_binary_linear calls on
+ * this device with the same (M, N, K, w_code, out_dtype) take that shape
+ * (bt_binary_linear_dscale, the first-forward and allocation-free variants
+ * too). For BT_CODE_BITS it times the one kernel. Either way the time is
+ * recorded against (M, N, K) for bt_plan's choice of code, so timing the same
+ * size once per code (weights packed in each) lets bt_plan pick the fastest.
+ * `out` holds the result of the last call. Blocks the calling thread until
+ * the stream has run every timed call. reps 1..10000; result not NULL.
+ * Errors: those of bt_binary_linear; BT_ERR_UNSUPPORTED while `stream` is
+ * being captured into a graph. M or N zero: nothing is timed or kept.
+ * The table is per process; the environment's BT_TC_CONFIG / BT_TC_EPI still
+ * override it.
+ */
+bt_status bt_tune_linear(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                         int64_t M, int64_t N, int64_t K, float scale_a, float scale_w,
+                         const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
+                         void *workspace, size_t workspace_bytes, int reps, bt_stream stream,
+                         bt_tune_result *result);
+
+/* Drops every shape and code bt_tune_linear kept (all devices). */
+void bt_tune_reset(void);
 
 /* ------------------------------------------------------------------------
  * Device-side scales (no host synchronisation). The page's forward reads the

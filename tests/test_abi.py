@@ -231,6 +231,24 @@ def test_plan_override(monkeypatch):
     assert bt.bt_plan(bt.BT_OP_LINEAR, 64, 64, 64) == (bt.BT_CODE_E4M3, bt.BT_ALGO_TC_E4M3)
 
 
+def test_tune_abi_validation():
+    # host-side checks only: no result struct, reps out of range, bad code or
+    # dtype, and a zero-row call (a no-op that times and keeps nothing)
+    T = bt._c_tune
+    res = bt.TuneResult()
+    r = ctypes.byref(res)
+    args = (None, bt.BT_F32, None, bt.BT_CODE_E2M1, 0, 8, 8, 1.0, 1.0, None, 0, None, bt.BT_F32, None, 0)
+    assert T(*args, 5, None, None) == bt.BT_ERR_INVALID_ARG
+    assert T(*args, 0, None, r) == bt.BT_ERR_INVALID_ARG
+    assert T(*args, 10001, None, r) == bt.BT_ERR_INVALID_ARG
+    bad_code = args[:3] + (7,) + args[4:]
+    assert T(*bad_code, 5, None, r) == bt.BT_ERR_INVALID_ARG
+    assert T(*args, 5, None, r) == bt.BT_OK
+    assert res.candidates == 0 and res.us == 0.0 and res.code == bt.BT_CODE_E2M1
+    bt.bt_tune_reset()
+    assert bt.bt_plan(bt.BT_OP_LINEAR, 16, 16, 1 << 20) == (bt.BT_CODE_BITS, bt.BT_ALGO_POPC)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_device_status_without_device():
     assert bt._c_status(None) == bt.BT_ERR_CUDA

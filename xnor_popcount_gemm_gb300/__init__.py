@@ -23,7 +23,8 @@ __all__ = [
     "BT_OP_CONV2D", "bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
     "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
-    "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_set_wait_timeout",
+    "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_tune_linear",
+            "bt_tune_reset", "bt_set_wait_timeout",
     "bt_binary_linear_dscale_init", "bt_binary_conv2d_dscale_init",
 ]
 
@@ -90,6 +91,17 @@ _c_w8_ws = _sig("bt_w8a8_conv2d_workspace", _sz, [_i64, _i64, _i64, _i64, _i64, 
 _c_w8 = _sig("bt_w8a8_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _p, _i, _p,
                                     _sz, _p])
 _c_plan = _sig("bt_plan", _i, [_i, _i64, _i64, _i64, ctypes.POINTER(_i), ctypes.POINTER(_i)])
+
+
+class TuneResult(ctypes.Structure):
+    """bt_tune_result: what bt_tune_linear measured and kept."""
+    _fields_ = [("code", _i), ("pair", _i), ("bn", _i), ("slices_per_stage", _i), ("epilogue_warps", _i),
+                ("candidates", _i), ("us", _f), ("us_model", _f)]
+
+
+_c_tune = _sig("bt_tune_linear", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _i64, _p, _i, _p, _sz, _i, _p,
+                                      ctypes.POINTER(TuneResult)])
+_c_tune_reset = _sig("bt_tune_reset", None, [])
 _c_status = _sig("bt_device_status", _i, [_p])
 _c_wait = _sig("bt_set_wait_timeout", _i, [ctypes.c_uint64])
 
@@ -97,7 +109,8 @@ _c_wait = _sig("bt_set_wait_timeout", _i, [ctypes.c_uint64])
 EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
             "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
-            "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass",
+            "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_tune_linear",
+            "bt_tune_reset",
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
             "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_conv2d_backward_implicit",
             "bt_binary_conv2d_backward",
@@ -522,6 +535,34 @@ def bt_plan(op: int, M: int, N: int, K: int) -> tuple[int, int]:
     code, algo = _i(0), _i(0)
     _check(_c_plan(op, M, N, K, ctypes.byref(code), ctypes.byref(algo)))
     return code.value, algo.value
+
+
+def bt_tune_linear(x: torch.Tensor, weight: torch.Tensor, w_code: int, K: int, scale_a: float, scale_w: float,
+                   bias_a=None, out_dtype=None, x_packed: bool = False, reps: int = 10,
+                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Time this linear forward in every candidate launch shape and keep the
+    fastest for later bt_binary_linear calls of the same size; returns the
+    bt_tune_result fields as a dict."""
+    _contig(x, "x")
+    _contig(weight, "weight")
+    M, N = x.shape[0], weight.shape[0]
+    xt = BT_PACKED if x_packed else _DT[x.dtype]
+    if out_dtype is None:
+        out_dtype = x.dtype if not x_packed else torch.float32
+    ot = _DT[out_dtype]
+    if out is None:
+        out = torch.empty((M, N), dtype=_TORCH[ot], device=x.device)
+    ws = _workspace(bt_binary_linear_workspace(M, K, xt, w_code), x.device, workspace)
+    blen = 0 if bias_a is None else bias_a.numel()
+    res = TuneResult()
+    _check(_c_tune(_ptr(x), xt, _ptr(weight), w_code, M, N, K, scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot,
+                   _ptr(ws), 0 if ws is None else ws.numel(), reps, _stream(stream), ctypes.byref(res)))
+    return {f: getattr(res, f) for f, _ in TuneResult._fields_}
+
+
+def bt_tune_reset() -> None:
+    """Forget every launch shape and code bt_tune_linear kept."""
+    _c_tune_reset()
 
 
 def bt_set_wait_timeout(ns: int) -> None:

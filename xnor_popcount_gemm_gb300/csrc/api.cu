@@ -4,6 +4,8 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
+#include <map>
 #include <mutex>
 
 #include "bt_device.cuh"
@@ -473,6 +475,135 @@ bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, 
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// The fastest code bt_tune_linear has measured per device and linear problem
+// size (over every output dtype it was run with), and that call's time.
+struct CodeKey {
+    int dev;
+    int64_t M, N, K;
+    bool operator<(const CodeKey &o) const {
+        if (dev != o.dev) return dev < o.dev;
+        if (M != o.M) return M < o.M;
+        if (N != o.N) return N < o.N;
+        return K < o.K;
+    }
+};
+struct CodeTime {
+    float us[3];        // per code, < 0 when not measured
+};
+std::mutex g_code_mu;
+std::map<CodeKey, CodeTime> g_code_times;
+
+CodeKey code_key(int64_t M, int64_t N, int64_t K) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    return CodeKey{dev, M, N, K};
+}
+
+bool measured_code(int64_t M, int64_t N, int64_t K, bt_code &code) {
+    std::lock_guard<std::mutex> lock(g_code_mu);
+    if (g_code_times.empty()) return false;
+    auto it = g_code_times.find(code_key(M, N, K));
+    if (it == g_code_times.end()) return false;
+    int best = -1;
+    for (int c = 0; c < 3; ++c)
+        if (it->second.us[c] >= 0.0f && (best < 0 || it->second.us[c] < it->second.us[best])) best = c;
+    if (best < 0) return false;
+    code = static_cast<bt_code>(best);
+    return true;
+}
+
+// Mean time of `reps` calls of `run` on stream s (after one untimed call),
+// in microseconds; negative when a call fails.
+float time_calls(const std::function<bt_status()> &run, int reps, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1, bt_status &st) {
+    st = run();
+    if (st != BT_OK) return -1.0f;
+    if (cudaEventRecord(e0, s) != cudaSuccess) return st = BT_ERR_CUDA, -1.0f;
+    for (int i = 0; i < reps; ++i)
+        if ((st = run()) != BT_OK) return -1.0f;
+    if (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess) return st = BT_ERR_CUDA, -1.0f;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) return st = BT_ERR_CUDA, -1.0f;
+    return 1000.0f * ms / static_cast<float>(reps);
+}
+}  // namespace
+
+bt_status bt_tune_linear(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t M, int64_t N,
+                         int64_t K, float scale_a, float scale_w, const float *bias_a, int64_t bias_len, void *out,
+                         bt_dtype out_dtype, void *workspace, size_t workspace_bytes, int reps, bt_stream stream,
+                         bt_tune_result *result) {
+    if (result == nullptr || reps < 1 || reps > 10000) return BT_ERR_INVALID_ARG;
+    *result = bt_tune_result{};
+    result->code = w_code;
+    if (M < 1 || N < 1) {
+        // nothing to time: a zero-size call is a no-op (or its argument error)
+        return linear_impl(x, x_dtype, weight, w_code, M, N, K, scale_a, scale_w, nullptr, bias_a, bias_len, out,
+                           out_dtype, BT_ALGO_AUTO, workspace, workspace_bytes, stream);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return BT_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return BT_ERR_UNSUPPORTED;       // timing needs real launches
+    auto run = [&] {
+        return linear_impl(x, x_dtype, weight, w_code, M, N, K, scale_a, scale_w, nullptr, bias_a, bias_len, out,
+                           out_dtype, BT_ALGO_AUTO, workspace, workspace_bytes, stream);
+    };
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess) return BT_ERR_CUDA;
+    if (cudaEventCreate(&e1) != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return BT_ERR_CUDA;
+    }
+    bt_status st = BT_OK;
+    float best = -1.0f;
+    if (w_code == BT_CODE_BITS) {
+        // one kernel for this code: time it
+        best = time_calls(run, reps, s, e0, e1, st);
+        result->candidates = 1;
+        result->us_model = best;
+    } else {
+        TcTileChoice cand[16];
+        const int n = tc_linear_candidates(M, N, K, w_code, out_dtype, cand, 16);
+        TcTileChoice win{};
+        for (int i = 0; i < n; ++i) {
+            tc_linear_force(&cand[i]);
+            const float us = time_calls(run, reps, s, e0, e1, st);
+            tc_linear_force(nullptr);
+            if (us < 0.0f) break;
+            ++result->candidates;
+            if (i == 0) result->us_model = us;
+            if (best < 0.0f || us < best) {
+                best = us;
+                win = cand[i];
+            }
+        }
+        if (st == BT_OK && n == 0) st = run();          // argument errors of a call with no candidate
+        if (st == BT_OK && best >= 0.0f) {
+            tc_linear_remember(M, N, K, w_code, out_dtype, win);
+            result->pair = win.pair;
+            result->bn = win.bn;
+            result->slices_per_stage = win.d;
+            result->epilogue_warps = win.epi;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st != BT_OK) return st;
+    result->us = best;
+    if (best >= 0.0f) {
+        std::lock_guard<std::mutex> lock(g_code_mu);
+        auto ins = g_code_times.insert({code_key(M, N, K), CodeTime{{-1.0f, -1.0f, -1.0f}}});
+        ins.first->second.us[static_cast<int>(w_code)] = best;
+    }
+    return BT_OK;
+}
+
+void bt_tune_reset(void) {
+    tc_linear_forget();
+    std::lock_guard<std::mutex> lock(g_code_mu);
+    g_code_times.clear();
+}
+
 bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_algo *algo) {
     if (code == nullptr || algo == nullptr || M < 1 || N < 1 || K < 1) return BT_ERR_INVALID_ARG;
     if (op != BT_OP_LINEAR && op != BT_OP_CONV2D) return BT_ERR_INVALID_ARG;
@@ -481,7 +612,9 @@ bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_a
     if (force != nullptr && std::strcmp(force, "popc") == 0) c = BT_CODE_BITS;
     else if (force != nullptr && std::strcmp(force, "e4m3") == 0) c = BT_CODE_E4M3;
     else if (force != nullptr && std::strcmp(force, "e2m1") == 0) c = BT_CODE_E2M1;
-    else c = (K <= kTcMaxK && tc_available()) ? BT_CODE_E2M1 : BT_CODE_BITS;
+    else if (op == BT_OP_LINEAR && measured_code(M, N, K, c)) {
+        // the fastest code bt_tune_linear measured for this size
+    } else c = (K <= kTcMaxK && tc_available()) ? BT_CODE_E2M1 : BT_CODE_BITS;
     *code = c;
     *algo = algo_for_code(c);
     return BT_OK;

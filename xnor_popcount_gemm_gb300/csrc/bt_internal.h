@@ -189,6 +189,26 @@ cudaError_t launch_dgrad_implicit(const uint16_t *g_nhwc, const uint16_t *wst, i
 // True when this build carries the tensor-core kernels.
 bool tc_available();
 
+// A launch shape of the linear layer's tensor-core contraction: CTA pairs
+// (cta_group::2) or single CTAs, bn output columns per tile, d 128-byte K
+// slices per pipeline stage, epi epilogue warps (4 or 8).
+struct TcTileChoice {
+    int pair, bn, d, epi;
+};
+// The shapes the measured selection times for an M x N x K linear contraction
+// in `code` (E4M3 / E2M1) writing out_t: the cost model's own choice first,
+// then the cheapest tile width by the model for every other (pair, d), each
+// with both epilogue warp counts. Writes at most `max`; returns how many.
+int tc_linear_candidates(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t, TcTileChoice *out,
+                         int max);
+// The shape the calling thread's linear contractions take until cleared
+// (nullptr): for timing one candidate.
+void tc_linear_force(const TcTileChoice *c);
+// Measured winners: the linear contractions of this device and (M, N, K,
+// code, out_t) take `c` from now on. tc_linear_forget drops every entry.
+void tc_linear_remember(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t, const TcTileChoice &c);
+void tc_linear_forget();
+
 // The driver's cuTensorMapEncodeTiled (looked up once), or nullptr.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 

@@ -57,6 +57,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
+#include <map>
 #include <mutex>
 
 #include "bt_device.cuh"
@@ -761,14 +763,23 @@ double tile_cost(bool pair, int bn, int d, int64_t M, int64_t N, int slices, int
     return static_cast<double>(rounds) * tile + epi + 600.0;
 }
 
-TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn, int out_elem, int splits) {
+bool valid_shape(bool pair, int bn, int d, int max_bn, int out_elem, int epi) {
+    return bn >= 32 && bn <= max_bn && bn % 16 == 0 && d >= 1 && d <= 4 &&
+           num_stages(bn, pair, d, out_elem, epi) >= 2;
+}
+
+// `pick` (a measured or forced shape, or nullptr) is taken when it is valid
+// for this problem; the environment's BT_TC_CONFIG comes first.
+TileCfg choose_cfg(int64_t M, int64_t N, int slices, int sms, int max_bn, int out_elem, int splits,
+                   const TcTileChoice *pick = nullptr) {
     if (const char *env = std::getenv("BT_TC_CONFIG")) {
         int bn = 0, d = 0;
         const bool pair = std::strncmp(env, "pair,", 5) == 0;
-        if (std::sscanf(pair ? env + 5 : env, "%d,%d", &bn, &d) == 2 && bn >= 32 && bn <= max_bn && bn % 16 == 0 &&
-            d >= 1 && d <= 4 && num_stages(bn, pair, d, out_elem) >= 2)
+        if (std::sscanf(pair ? env + 5 : env, "%d,%d", &bn, &d) == 2 && valid_shape(pair, bn, d, max_bn, out_elem, kEpiWarps))
             return TileCfg{pair, bn, d, 0.0};
     }
+    if (pick != nullptr && valid_shape(pick->pair != 0, pick->bn, pick->d, max_bn, out_elem, pick->epi))
+        return TileCfg{pick->pair != 0, pick->bn, pick->d, 0.0};
     TileCfg best{false, max_bn, 1, -1.0};
     for (int p = 1; p >= 0; --p)
         for (int d = 4; d >= 1; d /= 2)
@@ -799,6 +810,7 @@ int epilogue_warps(int code, int layout, const TcArgs &a) {
         if (std::strcmp(env, "4") == 0) return 4;
         if (std::strcmp(env, "8") == 0) return 8;
     }
+    if (a.epi_warps == 4 || a.epi_warps == 8) return a.epi_warps;      // a measured or forced shape's count
     const bool forward = code == BT_CODE_E2M1 || code == BT_CODE_E4M3;
     return forward && layout == kRowsOut && a.vec && a.slices >= 8 ? 4 : 8;
 }
@@ -885,7 +897,8 @@ int out_elem_bytes(bt_dtype t) { return t == BT_BF16 || t == BT_F16 ? 2 : 4; }
 // rb_split > 0 the contraction is split along K into parts of rb_split bytes
 // (a multiple of 128) that the caller runs as K splits.
 bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const uint8_t *bp, int64_t M, int64_t N,
-          int64_t rb, int64_t pitch_a, int64_t pitch_b, int out_elem, int64_t rb_split = -1) {
+          int64_t rb, int64_t pitch_a, int64_t pitch_b, int out_elem, int64_t rb_split = -1,
+          const TcTileChoice *pick = nullptr) {
     const int splits = rb_split > 0 ? static_cast<int>(rb / rb_split) : 1;
     if (rb % 16 != 0 || pitch_a % 16 != 0 || pitch_b % 16 != 0 || pitch_a < rb || pitch_b < rb ||
         M > (int64_t(1) << 31) - 512 || N > (int64_t(1) << 31) - 512)
@@ -896,7 +909,9 @@ bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const ui
     a.slices = static_cast<int>(((rb_split > 0 ? rb_split : rb) + kRowB - 1) / kRowB);   // per K split
     a.full_slices = static_cast<int>(rb / kRowB);                                       // of the whole row
     const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;       // E2M1 keeps 32 TMEM columns for block scales
-    c = choose_cfg(M, N, a.slices, sm_count(), max_bn, out_elem, splits);
+    c = choose_cfg(M, N, a.slices, sm_count(), max_bn, out_elem, splits, pick);
+    // the shape's epilogue warp count when it is the one taken (0: the usual rule)
+    a.epi_warps = (pick != nullptr && c.pair == (pick->pair != 0) && c.bn == pick->bn && c.d == pick->d) ? pick->epi : 0;
     a.bn = c.bn;
     a.d = c.d;
     a.nk = (a.slices + a.d - 1) / a.d;
@@ -917,9 +932,109 @@ bool plan(TcArgs &a, Maps &mp, TileCfg &c, int code, const uint8_t *ap, const ui
            map_2d(&mp.b2, bp, static_cast<uint64_t>(rb), static_cast<uint64_t>(pitch_b), static_cast<uint64_t>(N), b_box);
 }
 
+// Measured shapes of the linear contraction (bt_tune_linear), keyed by the
+// device and the problem, and the calling thread's forced shape.
+struct TunedKey {
+    int dev;
+    int64_t M, N, K;
+    int code, out_t;
+    bool operator<(const TunedKey &o) const {
+        if (dev != o.dev) return dev < o.dev;
+        if (M != o.M) return M < o.M;
+        if (N != o.N) return N < o.N;
+        if (K != o.K) return K < o.K;
+        if (code != o.code) return code < o.code;
+        return out_t < o.out_t;
+    }
+};
+std::mutex g_tuned_mu;
+std::map<TunedKey, TcTileChoice> g_tuned;
+std::atomic<int> g_tuned_count{0};          // entries: the common case (none) takes no lock
+thread_local const TcTileChoice *t_forced = nullptr;
+
+TunedKey tuned_key(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    return TunedKey{dev, M, N, K, static_cast<int>(code), static_cast<int>(out_t)};
+}
+
+// The shape a linear contraction takes: the thread's forced one, else the
+// measured winner for its key, else none (the cost model decides).
+bool linear_pick(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t, TcTileChoice &pick) {
+    if (t_forced != nullptr) {
+        pick = *t_forced;
+        return true;
+    }
+    if (g_tuned_count.load(std::memory_order_acquire) == 0) return false;
+    const TunedKey key = tuned_key(M, N, K, code, out_t);
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    auto it = g_tuned.find(key);
+    if (it == g_tuned.end()) return false;
+    pick = it->second;
+    return true;
+}
+
 }  // namespace
 
 bool tc_available() { return encode_tiled() != nullptr; }
+
+int tc_linear_candidates(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t, TcTileChoice *out,
+                         int max) {
+    if (out == nullptr || max < 1 || M < 1 || N < 1 || K < 1 || (code != BT_CODE_E4M3 && code != BT_CODE_E2M1))
+        return 0;
+    const int max_bn = code == BT_CODE_E2M1 ? 240 : 256;
+    const int oe = out_elem_bytes(out_t);
+    const int slices = static_cast<int>((row_bytes(K, code) + kRowB - 1) / kRowB);
+    const int sms = sm_count();
+    // the model's own choice, with the epilogue warp count its launch takes
+    const TileCfg first = choose_cfg(M, N, slices, sms, max_bn, oe, 1);
+    TcArgs probe{};
+    probe.slices = slices;
+    probe.vec = (N * oe) % 16 == 0 ? 1 : 0;         // the output is 16-byte aligned
+    const int epi0 = epilogue_warps(code, kRowsOut, probe);
+    int n = 0;
+    auto add = [&](bool pair, int bn, int d, int epi) {
+        if (n >= max || !valid_shape(pair, bn, d, max_bn, oe, epi)) return;
+        for (int i = 0; i < n; ++i)
+            if (out[i].pair == (pair ? 1 : 0) && out[i].bn == bn && out[i].d == d && out[i].epi == epi) return;
+        out[n++] = TcTileChoice{pair ? 1 : 0, bn, d, epi};
+    };
+    add(first.pair, first.bn, first.d, epi0);
+    add(first.pair, first.bn, first.d, epi0 == 4 ? 8 : 4);
+    for (int p = 1; p >= 0; --p)
+        for (int d = 4; d >= 1; d /= 2) {
+            if ((p == 1) == first.pair && d == first.d) continue;
+            int best_bn = 0;
+            double best = -1.0;
+            for (int bn = max_bn; bn >= 32; bn -= 16) {
+                if (num_stages(bn, p == 1, d, oe) < 2) continue;
+                const double cost = tile_cost(p == 1, bn, d, M, N, slices, sms, 1);
+                if (best < 0.0 || cost < best * 0.999) {
+                    best = cost;
+                    best_bn = bn;
+                }
+            }
+            if (best_bn == 0) continue;
+            add(p == 1, best_bn, d, 4);
+            add(p == 1, best_bn, d, 8);
+        }
+    return n;
+}
+
+void tc_linear_force(const TcTileChoice *c) { t_forced = c; }
+
+void tc_linear_remember(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t, const TcTileChoice &c) {
+    const TunedKey key = tuned_key(M, N, K, code, out_t);
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    g_tuned[key] = c;
+    g_tuned_count.store(static_cast<int>(g_tuned.size()), std::memory_order_release);
+}
+
+void tc_linear_forget() {
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    g_tuned.clear();
+    g_tuned_count.store(0, std::memory_order_release);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encode_tiled(); }
 
@@ -930,7 +1045,10 @@ cudaError_t launch_tc_linear(const uint8_t *xp, const uint8_t *wp, bt_code code,
     Maps mp;
     TileCfg c;
     const int64_t rb = row_bytes(K, code);
-    if (!plan(a, mp, c, code, xp, wp, M, N, rb, rb, rb, out_elem_bytes(out_t))) return cudaErrorInvalidValue;
+    TcTileChoice pick{};
+    const bool picked = linear_pick(M, N, K, code, out_t, pick);
+    if (!plan(a, mp, c, code, xp, wp, M, N, rb, rb, rb, out_elem_bytes(out_t), -1, picked ? &pick : nullptr))
+        return cudaErrorInvalidValue;
     a.alpha = alpha;
     a.scales = scales;
     a.out = out;
