@@ -45,8 +45,8 @@ def parse():
     ap.add_argument("--algo", default="auto", choices=["auto", "popc", "e4m3", "e2m1"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-tune", action="store_true",
-                    help="linear layers: skip the measured selection (bt_tune_linear) and take the cost model's shape")
-    ap.add_argument("--tune-reps", type=int, default=10, help="timed calls per candidate launch shape")
+                    help="skip the measured selection (bt_tune_linear / bt_tune_conv2d) and take the planner's shape")
+    ap.add_argument("--tune-reps", type=int, default=10, help="timed calls per candidate launch shape or plan")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the record of every configuration (all_configs) after the headline")
     ap.add_argument("--config-steps", type=int, default=20, help="timed steps per configuration and code")
@@ -436,10 +436,11 @@ CONFIG_ORDER = ["tiny_linear", "llm_linear", "resnet_conv", "downsample_conv", "
 
 def tune_linear(bt, wl, dev, reps: int) -> dict:
     """The measured "ADAPTIVE" selection of a linear workload, before any
-    warm-up or timing: bt_tune_linear times the contraction call as a step
-    makes it (packed x) in every candidate launch shape of each tensor-core
-    code, and the popcount kernel, keeping the fastest shape per code; bt_plan
-    then names the fastest code for the size."""
+    warm-up or timing: bt_tune_linear times the whole forward call on x (the
+    pack, then the contraction: the kernels of a step, back to back) in every
+    candidate launch shape of each tensor-core code, and the popcount kernel,
+    keeping the fastest shape per code; bt_plan then names the fastest code
+    for the size."""
     M, N, K = wl.gemm_shape()
     out_t = {"f32": torch.float32, "bf16": torch.bfloat16}[wl.out_dtype]
     xd = wl.x.to(dev)
@@ -449,20 +450,57 @@ def tune_linear(bt, wl, dev, reps: int) -> dict:
         if code != 0 and K > 16384:
             continue
         wp = bt.bt_pack_sign(wl.w.to(dev), code)
-        xp = bt.bt_pack_sign(xd, code, bt.BT_LAYOUT_ROWS, bias)
-        r = bt.bt_tune_linear(xp, wp, code, K, wl.scale_a, wl.scale_w, out_dtype=out_t, x_packed=True,
+        r = bt.bt_tune_linear(xd, wp, code, K, wl.scale_a, wl.scale_w, bias, out_dtype=out_t,
                               reps=reps if code != 0 else max(1, reps // 5))
         shape = (f"{'pair' if r['pair'] else 'single'} bn{r['bn']} d{r['slices_per_stage']} "
                  f"epi{r['epilogue_warps']}" if code != 0 else "popcount kernel")
         per[ALGO_NAME[code]] = {"us": round(r["us"], 2), "us_cost_model_shape": round(r["us_model"], 2),
                                 "kept": shape, "candidates": r["candidates"]}
-        del wp, xp
+        del wp
     del xd
     torch.cuda.empty_cache()
     code, _ = bt.bt_plan(bt.BT_OP_LINEAR, M, N, K)
     return {"code": ALGO_NAME[code], "per_code": per,
-            "how": "bt_tune_linear: mean of the timed contraction calls per launch shape (CUDA events); "
-                   "bt_plan names the code with the shortest"}
+            "how": "bt_tune_linear on x: mean of the timed forward calls (pack + contraction) per launch shape "
+                   "(CUDA events), a shape replacing the cost model's only when > 1 % faster; bt_plan names the "
+                   "code with the shortest"}
+
+
+def tune_conv(bt, wl, dev, reps: int) -> dict:
+    """The same for a convolution: bt_tune_conv2d times the whole call on x
+    (the NHWC pack, then the implicit-im2col contraction; or the convolution
+    packing x itself) in every candidate plan of each tensor-core code, and
+    the popcount route, keeping the fastest plan per code; bt_plan then names
+    the fastest code."""
+    M, N, K = wl.gemm_shape()
+    out_t = {"f32": torch.float32, "bf16": torch.bfloat16}[wl.out_dtype]
+    B, C, H, W = wl.x.shape
+    k = wl.w.shape[2]
+    xd = wl.x.to(dev)
+    bias = None if wl.bias is None else wl.bias.to(dev)
+    per = {}
+    for code in (2, 1, 0):
+        wp = bt.bt_pack_sign(wl.w.to(dev), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+        r = bt.bt_tune_conv2d(xd, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a, wl.scale_w, bias,
+                              out_dtype=out_t, reps=reps if code != 0 else max(1, reps // 5))
+        plan = (f"{'pair' if r['pair'] else 'single'} {'resident' if r['weights_resident'] else 'streamed'} "
+                f"weights, {r['pixel_stages']} pixel stage(s), "
+                f"{'packs x itself' if r['fused'] else 'after the NHWC pack'}" if code != 0 else "popcount route")
+        per[ALGO_NAME[code]] = {"us": round(r["us"], 2), "us_planner_plan": round(r["us_model"], 2), "kept": plan,
+                                "candidates": r["candidates"]}
+        del wp
+    del xd
+    torch.cuda.empty_cache()
+    code, _ = bt.bt_plan(bt.BT_OP_CONV2D, M, N, K)
+    return {"code": ALGO_NAME[code], "per_code": per,
+            "how": "bt_tune_conv2d on x: mean of the timed calls per plan (CUDA events), a plan replacing the "
+                   "planner's only when > 1 % faster; bt_plan names the code with the shortest"}
+
+
+def tune(bt, wl, dev, args):
+    if args.no_tune:
+        return None
+    return (tune_linear if wl.kind == "linear" else tune_conv)(bt, wl, dev, args.tune_reps)
 
 
 def sweep_configs(bt, dev, peaks, peak_src, sms, args) -> dict:
@@ -478,7 +516,7 @@ def sweep_configs(bt, dev, peaks, peak_src, sms, args) -> dict:
         M, N, K = wl.gemm_shape()
         ops = wl.binary_ops()
         op = bt.BT_OP_LINEAR if wl.kind == "linear" else bt.BT_OP_CONV2D
-        sel = tune_linear(bt, wl, dev, args.tune_reps) if wl.kind == "linear" and not args.no_tune else None
+        sel = tune(bt, wl, dev, args)
         plan_code, _ = bt.bt_plan(op, M, N, K)
         codes = [plan_code] + [c for c in (2, 1, 0) if c != plan_code]
         per_code, rec = {}, None
@@ -528,9 +566,7 @@ def run_ours(args, rank, world):
     M, N, K = wl.gemm_shape()
     ops = wl.binary_ops()
     op = bt.BT_OP_LINEAR if wl.kind == "linear" else bt.BT_OP_CONV2D
-    selection = None
-    if wl.kind == "linear" and not args.no_tune:
-        selection = tune_linear(bt, wl, dev, args.tune_reps)
+    selection = tune(bt, wl, dev, args)
     if args.algo == "auto":
         code, algo = bt.bt_plan(op, M, N, K)
     else:
@@ -606,7 +642,7 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(e2e_ms, 4),
                 "how": f"pinned host buffers (x{nh} rotating); copy-in, forward, copy-out on three streams, "
                        "neighbouring steps overlapped"},
-        "selection": selection if selection is not None else "the cost model's launch shape (not measured)",
+        "selection": selection if selection is not None else "the planner's launch shape (not measured)",
         "gpu_launches": su.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }

@@ -307,8 +307,9 @@ size_t bt_binary_linear_noalloc_max_bytes(void);
  * build runs fastest for a problem of this size. For BT_OP_LINEAR pass
  * (M, N, K); for BT_OP_CONV2D pass M = B*Ho*Wo, N = O, K = C*k*k. A linear
  * size that bt_tune_linear has timed in this process, on the current device,
- * gets the code with the shortest measured call among those timed; any other
- * size the fixed rule measured on GB300 (E2M1 up to K = 16384, else BITS).
+ * gets the code with the shortest measured call among those timed, and a
+ * convolution size that bt_tune_conv2d has timed likewise; any other size the
+ * fixed rule measured on GB300 (E2M1 up to K = 16384, else BITS).
  * Returns BT_ERR_INVALID_ARG for null outputs or sizes < 1.
  * The environment variable BT_FORCE_ALGO=popc|e4m3|e2m1 overrides it.
  */
@@ -334,7 +335,9 @@ typedef struct {
  * once untimed and `reps` times timed per candidate launch shape (the cost
  * model's own pick first, then the cheapest tile width by the model for every
  * other pairing and stage depth, each with 4 and 8 epilogue warps), with CUDA
- * events on `stream`, and keeps the fastest: later bt_binary_linear calls on
+ * events on `stream`, and keeps the fastest (a shape replaces the one kept so
+ * far, the model's first, only when it measures more than 1 % faster, so
+ * that timing noise does not move the choice): later bt_binary_linear calls on
  * this device with the same (M, N, K, w_code, out_dtype) take that shape
  * (bt_binary_linear_dscale, the first-forward and allocation-free variants
  * too). For BT_CODE_BITS it times the one kernel. Either way the time is
@@ -353,7 +356,51 @@ bt_status bt_tune_linear(const void *x, bt_dtype x_dtype, const void *weight, bt
                          void *workspace, size_t workspace_bytes, int reps, bt_stream stream,
                          bt_tune_result *result);
 
-/* Drops every shape and code bt_tune_linear kept (all devices). */
+/* What bt_tune_conv2d measured and kept. */
+typedef struct {
+    bt_code code;              /* the weight's code that was timed */
+    int pair;                  /* implicit plan: 1 = 256-channel tiles on CTA pairs (cta_group::2) */
+    int weights_resident;      /* implicit plan: 1 = weights held in shared memory, 0 = streamed per tile */
+    int pixel_stages;          /* implicit plan: staged pixel images in flight (1 or 2) */
+    int fused;                 /* 1 = the convolution packs x itself (no NHWC pack kernel first) */
+    int candidates;            /* plans timed (1 where the geometry has one route) */
+    float us;                  /* mean microseconds of one call in the kept plan */
+    float us_model;            /* the same for the plan the planner picks unmeasured */
+} bt_tune_conv_result;
+
+/*
+ * bt_tune_conv2d -- the measured "ADAPTIVE" choice for the convolution
+ * (BinaryConv2dForward.forward runs the native convolution the layer picks).
+ * Arguments as bt_binary_conv2d (algo AUTO). Where the implicit-im2col plan
+ * applies (codes E4M3 / E2M1, x not BT_PACKED_IM2COL) it runs the call once
+ * untimed and `reps` times timed per candidate plan -- the planner's own
+ * first, then every other fitting combination of CTA pairs or single CTAs,
+ * resident or streamed weights and 1 or 2 pixel stages, then each of them
+ * with the convolution packing x itself where x is float and that route
+ * applies -- with CUDA events on `stream`, and keeps the fastest (a plan
+ * replaces the planner's only when more than 1 % faster). Later
+ * bt_binary_conv2d calls on this device with the same geometry (B, C, H, W,
+ * O, kernel_size, stride, padding, dilation), w_code and out_dtype take it,
+ * whatever x's form; bt_conv2d_single_pass reports the kept route for the
+ * geometry. Elsewhere it times the one route. Either way the time is recorded
+ * against bt_plan's (M = B*Ho*Wo, N = O, K = C*k*k) for its choice of code.
+ * `workspace` must hold bt_binary_conv2d_workspace(...) bytes for x's form
+ * (the fused route needs none, the others what the query says). `out` holds
+ * the last call's result. Blocks the calling thread until the stream has run
+ * every timed call. reps 1..10000; result not NULL. Errors: those of
+ * bt_binary_conv2d; BT_ERR_UNSUPPORTED while `stream` is being captured. B or
+ * O zero: nothing is timed or kept. The environment's BT_CONV_PAIR /
+ * BT_CONV_PLAN / BT_CONV_FUSED still override the kept plan.
+ */
+bt_status bt_tune_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
+                         int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,
+                         int stride, int padding, int dilation, float scale_a, float scale_w,
+                         const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
+                         void *workspace, size_t workspace_bytes, int reps, bt_stream stream,
+                         bt_tune_conv_result *result);
+
+/* Drops every launch shape, plan and code bt_tune_linear / bt_tune_conv2d
+ * kept (all devices). */
 void bt_tune_reset(void);
 
 /* ------------------------------------------------------------------------

@@ -247,6 +247,17 @@ def test_tune_abi_validation():
     assert res.candidates == 0 and res.us == 0.0 and res.code == bt.BT_CODE_E2M1
     bt.bt_tune_reset()
     assert bt.bt_plan(bt.BT_OP_LINEAR, 16, 16, 1 << 20) == (bt.BT_CODE_BITS, bt.BT_ALGO_POPC)
+    # the convolution's: no result struct, reps out of range, a bad code, zero images
+    TC = bt._c_tune_conv
+    cres = bt.TuneConvResult()
+    cr = ctypes.byref(cres)
+    cargs = (None, bt.BT_F32, None, bt.BT_CODE_E2M1, 0, 64, 14, 14, 64, 3, 1, 1, 1, 1.0, 1.0, None, 0, None,
+             bt.BT_F32, None, 0)
+    assert TC(*cargs, 5, None, None) == bt.BT_ERR_INVALID_ARG
+    assert TC(*cargs, 0, None, cr) == bt.BT_ERR_INVALID_ARG
+    assert TC(*(cargs[:3] + (7,) + cargs[4:]), 5, None, cr) == bt.BT_ERR_INVALID_ARG
+    assert TC(*cargs, 5, None, cr) == bt.BT_OK
+    assert cres.candidates == 0 and cres.us == 0.0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")

@@ -122,3 +122,68 @@ def test_tune_refuses_a_capturing_stream():
     got = bt.bt_binary_linear(xd, wp, code, K, 1.0, 1.0, out_dtype=torch.int32).cpu()
     want = oracle.linear_dot(oracle.binarize(x), oracle.binarize_weight(w))
     np.testing.assert_array_equal(got.numpy(), want)
+
+
+# ---------------------------------------------------------------------------
+# Convolution: the implicit plans (pairs or single CTAs, resident or streamed
+# weights, one or two pixel stages, with or without the convolution packing x
+# itself)
+# ---------------------------------------------------------------------------
+
+CONV_GEOMS = [  # B, C, H, W, O, k, s, p, d, x dtype
+    (2, 128, 28, 28, 256, 3, 2, 1, 1, torch.bfloat16),
+    (2, 128, 28, 28, 256, 3, 2, 2, 2, torch.bfloat16),
+    (2, 256, 14, 14, 256, 3, 1, 1, 1, torch.float32),
+    (3, 64, 17, 19, 96, 3, 1, 1, 1, torch.float32),
+]
+
+
+@pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
+@pytest.mark.parametrize("geom", CONV_GEOMS, ids=["s2p1", "s2p2d2", "s1p1", "ragged"])
+def test_tune_conv_keeps_fastest_and_exact_plan(code, geom):
+    B, C, H, W, O, k, s, p, d, dt = geom
+    x = _gen(B + C + H, (B, C, H, W), dt)
+    w = _gen(O + C, (O, C, k, k), dt)
+    want = torch.from_numpy(oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d))
+    xd, wp = x.to(DEV), bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    out = torch.empty(want.shape, dtype=torch.int32, device=DEV)
+    res = bt.bt_tune_conv2d(xd, wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32, reps=2, out=out)
+    assert torch.equal(out.cpu(), want)
+    assert res["code"] == code and res["candidates"] >= (2 if O > 128 else 1)
+    assert res["us"] > 0.0 and res["us"] <= res["us_model"]
+    assert res["pixel_stages"] in (1, 2) and res["pair"] in (0, 1) and res["fused"] in (0, 1)
+    # later calls of the geometry take the kept plan: on x, and on packed pixels
+    got = bt.bt_binary_conv2d(xd, wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32).cpu()
+    assert torch.equal(got, want)
+    xp = bt.bt_pack_sign(xd, code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    got = bt.bt_binary_conv2d(xp, wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32, x_packed=True).cpu()
+    assert torch.equal(got, want)
+    sa, sw = workloads.mean_abs(x), workloads.mean_abs(w)
+    ot = "bf16" if dt == torch.bfloat16 else "f32"
+    y = bt.bt_binary_conv2d(xd, wp, code, C, k, s, p, d, sa, sw).cpu()
+    assert torch.equal(y, oracle.epilogue(want.numpy(), sa, sw, ot))
+    # the split the library reports for the geometry follows the kept route
+    xt = {torch.float32: bt.BT_F32, torch.bfloat16: bt.BT_BF16}[dt]
+    mode = bt.bt_conv2d_single_pass(B, C, H, W, k, s, p, d, xt, code)
+    assert (mode == 2) == (res["fused"] == 1)
+
+
+def test_plan_names_fastest_measured_conv_code():
+    B, C, H, W, O, k, s, p, d = 2, 128, 28, 28, 256, 3, 2, 1, 1
+    x = _gen(5, (B, C, H, W), torch.bfloat16)
+    w = _gen(6, (O, C, k, k), torch.bfloat16)
+    want = torch.from_numpy(oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d))
+    Ho = bt.conv2d_out_size(H, k, s, p, d)
+    M, N, K = B * Ho * Ho, O, C * k * k
+    before = bt.bt_plan(bt.BT_OP_CONV2D, M, N, K)
+    times = {}
+    for code in (bt.BT_CODE_BITS, bt.BT_CODE_E4M3, bt.BT_CODE_E2M1):
+        wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+        out = torch.empty(want.shape, dtype=torch.int32, device=DEV)
+        res = bt.bt_tune_conv2d(x.to(DEV), wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32, reps=2,
+                                out=out)
+        assert torch.equal(out.cpu(), want)
+        times[code] = res["us"]
+    assert bt.bt_plan(bt.BT_OP_CONV2D, M, N, K)[0] == min(times, key=times.get)
+    bt.bt_tune_reset()
+    assert bt.bt_plan(bt.BT_OP_CONV2D, M, N, K) == before

@@ -24,7 +24,7 @@ __all__ = [
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
     "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
     "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_tune_linear",
-            "bt_tune_reset", "bt_set_wait_timeout",
+            "bt_tune_reset", "bt_tune_conv2d", "bt_set_wait_timeout",
     "bt_binary_linear_dscale_init", "bt_binary_conv2d_dscale_init",
 ]
 
@@ -102,6 +102,16 @@ class TuneResult(ctypes.Structure):
 _c_tune = _sig("bt_tune_linear", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _f, _f, _p, _i64, _p, _i, _p, _sz, _i, _p,
                                       ctypes.POINTER(TuneResult)])
 _c_tune_reset = _sig("bt_tune_reset", None, [])
+
+
+class TuneConvResult(ctypes.Structure):
+    """bt_tune_conv_result: what bt_tune_conv2d measured and kept."""
+    _fields_ = [("code", _i), ("pair", _i), ("weights_resident", _i), ("pixel_stages", _i), ("fused", _i),
+                ("candidates", _i), ("us", _f), ("us_model", _f)]
+
+
+_c_tune_conv = _sig("bt_tune_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _f, _f, _p,
+                                           _i64, _p, _i, _p, _sz, _i, _p, ctypes.POINTER(TuneConvResult)])
 _c_status = _sig("bt_device_status", _i, [_p])
 _c_wait = _sig("bt_set_wait_timeout", _i, [ctypes.c_uint64])
 
@@ -110,7 +120,7 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
             "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_tune_linear",
-            "bt_tune_reset",
+            "bt_tune_reset", "bt_tune_conv2d",
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
             "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_conv2d_backward_implicit",
             "bt_binary_conv2d_backward",
@@ -560,8 +570,43 @@ def bt_tune_linear(x: torch.Tensor, weight: torch.Tensor, w_code: int, K: int, s
     return {f: getattr(res, f) for f, _ in TuneResult._fields_}
 
 
+def bt_tune_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int, kernel_size: int, stride: int,
+                   padding: int, dilation: int, scale_a: float, scale_w: float, bias_a=None, out_dtype=None,
+                   x_packed: bool = False, reps: int = 10, out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Time this convolution in every candidate plan and keep the fastest for
+    later bt_binary_conv2d calls of the same geometry; returns the
+    bt_tune_conv_result fields as a dict."""
+    _contig(x, "x")
+    _contig(weight, "weight")
+    if x_packed:
+        B, H, W = x.shape[0], x.shape[1], x.shape[2]
+        xt = BT_PACKED
+    else:
+        B, C2, H, W = x.shape
+        if C2 != C:
+            raise ValueError("C does not match x")
+        xt = _DT[x.dtype]
+    O = weight.shape[0]
+    if out_dtype is None:
+        out_dtype = x.dtype if not x_packed else torch.float32
+    ot = _DT[out_dtype]
+    Ho = conv2d_out_size(H, kernel_size, stride, padding, dilation)
+    Wo = conv2d_out_size(W, kernel_size, stride, padding, dilation)
+    if out is None:
+        out = torch.empty((B, O, max(Ho, 0), max(Wo, 0)), dtype=_TORCH[ot], device=x.device)
+    ws = _workspace(bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, xt, w_code),
+                    x.device, workspace)
+    blen = 0 if bias_a is None else bias_a.numel()
+    res = TuneConvResult()
+    _check(_c_tune_conv(_ptr(x), xt, _ptr(weight), w_code, B, C, H, W, O, kernel_size, stride, padding, dilation,
+                        scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, _ptr(ws), 0 if ws is None else ws.numel(),
+                        reps, _stream(stream), ctypes.byref(res)))
+    return {f: getattr(res, f) for f, _ in TuneConvResult._fields_}
+
+
 def bt_tune_reset() -> None:
-    """Forget every launch shape and code bt_tune_linear kept."""
+    """Forget every launch shape, plan and code bt_tune_linear / bt_tune_conv2d kept."""
     _c_tune_reset()
 
 

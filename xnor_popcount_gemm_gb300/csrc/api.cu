@@ -304,6 +304,16 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
     if ((M + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
     const bt_algo run = algo_for_code(w_code);
     if (run != BT_ALGO_POPC && C * kk > kTcMaxK) return BT_ERR_UNSUPPORTED;
+    // the plan bt_tune_conv2d kept for this geometry, unless one is forced already
+    ConvChoice kept{};
+    const bool use_kept = conv_forced() == nullptr && conv_lookup(g, w_code, out_dtype, kept);
+    if (use_kept) conv_force(&kept);
+    struct Unforce {
+        bool on;
+        ~Unforce() {
+            if (on) conv_force(nullptr);
+        }
+    } unforce{use_kept};
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = bt_binary_conv2d_workspace(B, C, H, W, kernel_size, stride, padding, dilation, x_dtype,
@@ -446,7 +456,17 @@ int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel
     g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
     g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
     if (g.Ho < 1 || g.Wo < 1) return 0;
-    if (conv_fused_applies(g, code, x_dtype)) return 2;   // one kernel from x
+    bool kept_fused = false;
+    if (conv_forced() == nullptr && conv_kept_fused(g, code, kept_fused)) {
+        // the route bt_tune_conv2d kept for this geometry
+        const ConvChoice f{-1, 0, 0, kept_fused ? 1 : 0};
+        conv_force(&f);
+        const bool fused = conv_fused_applies(g, code, x_dtype);
+        conv_force(nullptr);
+        if (fused) return 2;
+    } else if (conv_fused_applies(g, code, x_dtype)) {
+        return 2;                                          // one kernel from x
+    }
     if (conv_implicit_applies(g, code)) return 0;      // packed pixels, contracted in place
     return unfold_single_pass(g, x_dtype, code) ? 1 : 0;
 }
@@ -479,10 +499,11 @@ namespace {
 // The fastest code bt_tune_linear has measured per device and linear problem
 // size (over every output dtype it was run with), and that call's time.
 struct CodeKey {
-    int dev;
+    int dev, op;
     int64_t M, N, K;
     bool operator<(const CodeKey &o) const {
         if (dev != o.dev) return dev < o.dev;
+        if (op != o.op) return op < o.op;
         if (M != o.M) return M < o.M;
         if (N != o.N) return N < o.N;
         return K < o.K;
@@ -494,16 +515,22 @@ struct CodeTime {
 std::mutex g_code_mu;
 std::map<CodeKey, CodeTime> g_code_times;
 
-CodeKey code_key(int64_t M, int64_t N, int64_t K) {
+CodeKey code_key(bt_op op, int64_t M, int64_t N, int64_t K) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-    return CodeKey{dev, M, N, K};
+    return CodeKey{dev, static_cast<int>(op), M, N, K};
 }
 
-bool measured_code(int64_t M, int64_t N, int64_t K, bt_code &code) {
+void record_code_time(bt_op op, int64_t M, int64_t N, int64_t K, bt_code code, float us) {
+    std::lock_guard<std::mutex> lock(g_code_mu);
+    auto ins = g_code_times.insert({code_key(op, M, N, K), CodeTime{{-1.0f, -1.0f, -1.0f}}});
+    ins.first->second.us[static_cast<int>(code)] = us;
+}
+
+bool measured_code(bt_op op, int64_t M, int64_t N, int64_t K, bt_code &code) {
     std::lock_guard<std::mutex> lock(g_code_mu);
     if (g_code_times.empty()) return false;
-    auto it = g_code_times.find(code_key(M, N, K));
+    auto it = g_code_times.find(code_key(op, M, N, K));
     if (it == g_code_times.end()) return false;
     int best = -1;
     for (int c = 0; c < 3; ++c)
@@ -572,7 +599,10 @@ bt_status bt_tune_linear(const void *x, bt_dtype x_dtype, const void *weight, bt
             if (us < 0.0f) break;
             ++result->candidates;
             if (i == 0) result->us_model = us;
-            if (best < 0.0f || us < best) {
+            // another shape replaces the one kept so far (the model's own
+            // first) only when it measures more than 1 % faster: timing noise
+            // does not move the choice
+            if (best < 0.0f || us < 0.99f * best) {
                 best = us;
                 win = cand[i];
             }
@@ -590,16 +620,84 @@ bt_status bt_tune_linear(const void *x, bt_dtype x_dtype, const void *weight, bt
     cudaEventDestroy(e1);
     if (st != BT_OK) return st;
     result->us = best;
-    if (best >= 0.0f) {
-        std::lock_guard<std::mutex> lock(g_code_mu);
-        auto ins = g_code_times.insert({code_key(M, N, K), CodeTime{{-1.0f, -1.0f, -1.0f}}});
-        ins.first->second.us[static_cast<int>(w_code)] = best;
+    if (best >= 0.0f) record_code_time(BT_OP_LINEAR, M, N, K, w_code, best);
+    return BT_OK;
+}
+
+bt_status bt_tune_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code, int64_t B, int64_t C,
+                         int64_t H, int64_t W, int64_t O, int kernel_size, int stride, int padding, int dilation,
+                         float scale_a, float scale_w, const float *bias_a, int64_t bias_len, void *out,
+                         bt_dtype out_dtype, void *workspace, size_t workspace_bytes, int reps, bt_stream stream,
+                         bt_tune_conv_result *result) {
+    if (result == nullptr || reps < 1 || reps > 10000) return BT_ERR_INVALID_ARG;
+    *result = bt_tune_conv_result{};
+    result->code = w_code;
+    auto run = [&] {
+        return conv_impl(x, x_dtype, weight, w_code, B, C, H, W, O, kernel_size, stride, padding, dilation, scale_a,
+                         scale_w, nullptr, bias_a, bias_len, out, out_dtype, BT_ALGO_AUTO, workspace,
+                         workspace_bytes, stream);
+    };
+    // argument errors and empty problems: what the call itself answers
+    const int64_t Ho = conv_out(H, kernel_size, stride, padding, dilation);
+    const int64_t Wo = conv_out(W, kernel_size, stride, padding, dilation);
+    if (!valid_code(w_code) || B < 1 || O < 1 || C < 1 || H < 1 || W < 1 || kernel_size < 1 || stride < 1 ||
+        padding < 0 || dilation < 1 || Ho < 1 || Wo < 1)
+        return run();
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return BT_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return BT_ERR_UNSUPPORTED;       // timing needs real launches
+    ConvGeom g{B, C, H, W, O, Ho, Wo, kernel_size, stride, padding, dilation};
+    ConvChoice cand[24];
+    const int n = (x_dtype == BT_PACKED_IM2COL || w_code == BT_CODE_BITS)
+                      ? 0 : conv_candidates(g, w_code, x_dtype, out_dtype, cand, 24);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess) return BT_ERR_CUDA;
+    if (cudaEventCreate(&e1) != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return BT_ERR_CUDA;
     }
+    bt_status st = BT_OK;
+    float best = -1.0f;
+    if (n == 0) {
+        // one route for this code and geometry: time it
+        best = time_calls(run, reps, s, e0, e1, st);
+        result->candidates = st == BT_OK ? 1 : 0;
+        result->us_model = best;
+    } else {
+        ConvChoice win{};
+        for (int i = 0; i < n; ++i) {
+            conv_force(&cand[i]);
+            const float us = time_calls(run, reps, s, e0, e1, st);
+            conv_force(nullptr);
+            if (us < 0.0f) break;
+            ++result->candidates;
+            if (i == 0) result->us_model = us;
+            // as for the linear layer: a plan replaces the planner's only when > 1 % faster
+            if (best < 0.0f || us < 0.99f * best) {
+                best = us;
+                win = cand[i];
+            }
+        }
+        if (st == BT_OK && best >= 0.0f) {
+            conv_remember(g, w_code, out_dtype, win);
+            result->pair = win.pair;
+            result->weights_resident = win.plan == 'R' ? 1 : 0;
+            result->pixel_stages = win.bst;
+            result->fused = win.fused;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st != BT_OK) return st;
+    result->us = best;
+    if (best >= 0.0f) record_code_time(BT_OP_CONV2D, B * Ho * Wo, O, C * kernel_size * kernel_size, w_code, best);
     return BT_OK;
 }
 
 void bt_tune_reset(void) {
     tc_linear_forget();
+    conv_forget();
     std::lock_guard<std::mutex> lock(g_code_mu);
     g_code_times.clear();
 }
@@ -612,8 +710,8 @@ bt_status bt_plan(bt_op op, int64_t M, int64_t N, int64_t K, bt_code *code, bt_a
     if (force != nullptr && std::strcmp(force, "popc") == 0) c = BT_CODE_BITS;
     else if (force != nullptr && std::strcmp(force, "e4m3") == 0) c = BT_CODE_E4M3;
     else if (force != nullptr && std::strcmp(force, "e2m1") == 0) c = BT_CODE_E2M1;
-    else if (op == BT_OP_LINEAR && measured_code(M, N, K, c)) {
-        // the fastest code bt_tune_linear measured for this size
+    else if (measured_code(op, M, N, K, c)) {
+        // the fastest code bt_tune_linear / bt_tune_conv2d measured for this size
     } else c = (K <= kTcMaxK && tc_available()) ? BT_CODE_E2M1 : BT_CODE_BITS;
     *code = c;
     *algo = algo_for_code(c);

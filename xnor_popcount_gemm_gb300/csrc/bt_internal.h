@@ -247,6 +247,31 @@ cudaError_t launch_tc_conv_fused(const void *x, bt_dtype x_dtype, const float *b
                                  const uint8_t *wp, bt_code code, const ConvGeom &g, float alpha, void *out,
                                  bt_dtype out_t, unsigned int *err, cudaStream_t s, const float *scales = nullptr);
 
+// A launch plan of the implicit-im2col convolution, for the measured
+// selection: CTA pairs or single CTAs, weights resident ('R') or streamed
+// ('S'), 1 or 2 pixel stages, and (fused = 1) the convolution packing x
+// itself instead of the NHWC pack kernel running first.
+struct ConvChoice {
+    int pair, plan, bst, fused;
+};
+// The plans the measured selection times for this geometry, code, input and
+// output dtype: the planner's own first, then every other (pair, plan,
+// stages) that fits, then each of them packing x itself where that route
+// applies (float x). Writes at most `max`; returns how many (0 where the
+// implicit plan does not apply).
+int conv_candidates(const ConvGeom &g, bt_code code, bt_dtype x_dtype, bt_dtype out_t, ConvChoice *out, int max);
+// The plan the calling thread's convolutions take until cleared (nullptr);
+// the environment's BT_CONV_PAIR / BT_CONV_PLAN / BT_CONV_FUSED come first.
+void conv_force(const ConvChoice *c);
+const ConvChoice *conv_forced();
+// Measured winners per device, geometry (g.O included), code and output
+// dtype; conv_kept_fused answers for any O and output dtype (the most
+// recent entry of the geometry and code).
+void conv_remember(const ConvGeom &g, bt_code code, bt_dtype out_t, const ConvChoice &c);
+bool conv_lookup(const ConvGeom &g, bt_code code, bt_dtype out_t, ConvChoice &c);
+bool conv_kept_fused(const ConvGeom &g, bt_code code, bool &fused);
+void conv_forget();
+
 // First-call activation scale (BinaryConv2dCutlass.set_activation): the sum
 // of |x| accumulates in a double per CUDA context (zero it before use; calls
 // that overlap on one GPU share it); launch_abs_sum adds the sum of |x| of n

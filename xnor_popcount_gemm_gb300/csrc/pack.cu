@@ -563,7 +563,7 @@ pack_nhwc_warp_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
 // the pixel block fastest (the input, 8 to 16 times the output's bytes, is
 // read in runs); each warp loads its next unit before it converts the
 // current one.
-template <typename T, bool CHAN, bool PF>
+template <typename T, bool CHAN>
 __global__ void __launch_bounds__(kPackThreads)
 pack_nhwc_e2m1_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, FastDiv div_ncg, FastDiv div_npb,
                       const float *__restrict__ bias, int bias_len, uint8_t *__restrict__ out, int rb) {
@@ -603,8 +603,7 @@ pack_nhwc_e2m1_kernel(const T *__restrict__ x, int C, int HW, uint32_t units, Fa
         for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int v = 0; v < NV; ++v)
-                g[k][v] = PF ? ld_nc_v4_if_l2pf(base + k * hw8 + 4 * v, 8 * k < lim && px + 4 * v < HW)
-                             : ld_nc_v4_if(base + k * hw8 + 4 * v, 8 * k < lim && px + 4 * v < HW);
+                g[k][v] = ld_nc_v4_if(base + k * hw8 + 4 * v, 8 * k < lim && px + 4 * v < HW);
     };
     auto convert = [&](const uint4 (&g)[4][NV], uint32_t u) {
         int cg, b, blk;
@@ -1030,12 +1029,6 @@ bool nhwc_warp_disabled() {
     const char *env = std::getenv("BT_PACK_NHWC");
     return env != nullptr && std::strcmp(env, "smem") == 0;
 }
-// BT_PACK_L2PF=1: the E2M1 NHWC pack's loads ask L2 for whole 256-byte blocks.
-bool nhwc_l2_prefetch() {
-    const char *env = std::getenv("BT_PACK_L2PF");
-    return env != nullptr && std::strcmp(env, "1") == 0;
-}
-
 bool nhwc_e2m1_fast() {
     const char *env = std::getenv("BT_PACK_NHWC");
     return env == nullptr || (std::strcmp(env, "smem") != 0 && std::strcmp(env, "warp") != 0);
@@ -1159,11 +1152,9 @@ cudaError_t nhwc_t(const T *x, int64_t B, int64_t C, int64_t HW, const float *bi
                 // blocks as are resident at once (the warps loop over the units), so
                 // that no block waits for a second wave
                 const FastDiv dncg = make_fastdiv(static_cast<uint32_t>(ncg)), dnpb = make_fastdiv(static_cast<uint32_t>(npb));
-                const bool pf = nhwc_l2_prefetch();
-                auto kern = bias_len > 1 ? (pf ? pack_nhwc_e2m1_kernel<T, true, true> : pack_nhwc_e2m1_kernel<T, true, false>)
-                                         : (pf ? pack_nhwc_e2m1_kernel<T, false, true> : pack_nhwc_e2m1_kernel<T, false, false>);
-                static int per_sm[4] = {0, 0, 0, 0};
-                const int slot = (bias_len > 1 ? 1 : 0) + (pf ? 2 : 0);
+                auto kern = bias_len > 1 ? pack_nhwc_e2m1_kernel<T, true> : pack_nhwc_e2m1_kernel<T, false>;
+                static int per_sm[2] = {0, 0};
+                const int slot = bias_len > 1 ? 1 : 0;
                 if (per_sm[slot] == 0) {
                     int n = 0;
                     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kPackThreads, 0) != cudaSuccess || n < 1) n = 1;

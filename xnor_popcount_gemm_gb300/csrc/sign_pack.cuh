@@ -177,19 +177,6 @@ __device__ __forceinline__ uint4 ld_nc_v4_if(const void *p, bool ok) {
     return v;
 }
 
-// The same load with the hint that L2 fetch the whole aligned 256-byte block
-// around it (neighbouring warps read the rest of the block).
-__device__ __forceinline__ uint4 ld_nc_v4_if_l2pf(const void *p, bool ok) {
-    uint4 v;
-    asm volatile(
-        "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n"
-        " mov.b32 %0, 0;\n mov.b32 %1, 0;\n mov.b32 %2, 0;\n mov.b32 %3, 0;\n"
-        " @q ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];\n}"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p), "r"(static_cast<int>(ok)));
-    return v;
-}
-
 // The sign test of the shift as one comparison x >= t (the activation shift
 // of BinaryConv2dCutlass.set_activation: +1 where x + b >= 0, the fp32 sum).
 // A finite b: t = -b, rounded up to a 2-byte input type (x + b >= 0 exactly

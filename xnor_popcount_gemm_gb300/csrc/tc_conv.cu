@@ -1,9 +1,18 @@
 // Host side of the implicit-im2col binary convolution (kernel in
 // tc_conv_kernel.cuh): the plan of a geometry (tiles, phase images, taps,
 // shared-memory layout), the tensor maps, and the launches.
+#include <atomic>
+#include <utility>
+#include <vector>
+
 #include "tc_conv_kernel.cuh"
 
 namespace bt {
+
+// The calling thread's forced plan (bt_tune_conv2d, or a kept winner for the
+// call in progress).
+thread_local const ConvChoice *t_conv_force = nullptr;
+
 namespace conv {
 
 // ---------------------------------------------------------------------------
@@ -163,6 +172,10 @@ bool plan_conv(const ConvGeom &g, bt_code code, int sms, int out_elem, ConvPlan 
         else if (std::strcmp(env, "r1") == 0 && fits_res(1)) { plan = 'R'; bst = 1; }
         else if (std::strcmp(env, "s2") == 0 && sd2) { plan = 'S'; bst = 2; }
         else if (std::strcmp(env, "s1") == 0 && sd1) { plan = 'S'; bst = 1; }
+    } else if (const ConvChoice *f = t_conv_force) {
+        if (f->plan == 'R' && (f->bst == 1 || f->bst == 2) && fits_res(f->bst)) { plan = 'R'; bst = f->bst; }
+        else if (f->plan == 'S' && f->bst == 2 && sd2) { plan = 'S'; bst = 2; }
+        else if (f->plan == 'S' && f->bst == 1 && sd1) { plan = 'S'; bst = 1; }
     }
     if (plan == 0) {
         if (fits_res(2)) { plan = 'R'; bst = 2; }
@@ -247,6 +260,7 @@ bool encode_maps(const ConvGeom &g, bt_code code, const ConvArgs &a, const uint8
 bool choose_plan(const ConvGeom &g, bt_code code, int sms, int out_elem, ConvPlan &p) {
     int want = -1;
     if (const char *env = std::getenv("BT_CONV_PAIR")) want = std::strcmp(env, "0") == 0 ? 0 : 1;
+    else if (t_conv_force != nullptr && (t_conv_force->pair == 0 || t_conv_force->pair == 1)) want = t_conv_force->pair;
     if (want != 0 && sms >= 2 && (want == 1 || g.O > kBM) && plan_conv(g, code, sms, out_elem, p, true)) return true;
     return plan_conv(g, code, sms, out_elem, p, false);
 }
@@ -280,6 +294,130 @@ void plan_fused(const ConvGeom &g, bt_code code, ConvPlan &p) {
 }  // namespace conv
 
 using namespace conv;
+
+// ---------------------------------------------------------------------------
+// measured selection: candidates, the forced plan, the kept winners
+// ---------------------------------------------------------------------------
+
+void conv_force(const ConvChoice *c) { t_conv_force = c; }
+const ConvChoice *conv_forced() { return t_conv_force; }
+
+int conv_candidates(const ConvGeom &g, bt_code code, bt_dtype x_dtype, bt_dtype out_t, ConvChoice *out, int max) {
+    const ConvChoice *saved = t_conv_force;
+    t_conv_force = nullptr;
+    int n = 0;
+    auto add = [&](const ConvChoice &c) {
+        if (n >= max) return;
+        for (int i = 0; i < n; ++i)
+            if (out[i].pair == c.pair && out[i].plan == c.plan && out[i].bst == c.bst && out[i].fused == c.fused)
+                return;
+        out[n++] = c;
+    };
+    if (max > 0 && out != nullptr && conv_implicit_applies(g, code)) {
+        const int oe = out_t == BT_BF16 || out_t == BT_F16 ? 2 : 4;
+        const int sms = device_sm_count();
+        // the plan a launch takes under forced choice f (nullptr: the planner's own)
+        auto effective = [&](const ConvChoice *f, ConvChoice &c) {
+            t_conv_force = f;
+            ConvPlan p;
+            const bool ok = choose_plan(g, code, sms, oe, p);
+            t_conv_force = nullptr;
+            if (!ok) return false;
+            c = ConvChoice{p.cp ? 1 : 0, p.a.a_resident ? 'R' : 'S', p.a.b_stages, 0};
+            return true;
+        };
+        ConvChoice c{};
+        if (effective(nullptr, c)) add(c);
+        const int plans[4][2] = {{'R', 2}, {'R', 1}, {'S', 2}, {'S', 1}};
+        for (int pair = 1; pair >= 0; --pair)
+            for (const auto &pl : plans) {
+                const ConvChoice f{pair, pl[0], pl[1], 0};
+                if (effective(&f, c) && c.pair == f.pair && c.plan == f.plan && c.bst == f.bst) add(c);
+            }
+        // each plan again with the convolution packing x itself, where it can
+        bool fused_ok = false;
+        if (x_dtype == BT_F32 || x_dtype == BT_BF16 || x_dtype == BT_F16) {
+            const ConvChoice f{-1, 0, 0, 1};
+            t_conv_force = &f;
+            fused_ok = conv_fused_applies(g, code, x_dtype);
+            t_conv_force = nullptr;
+        }
+        if (fused_ok) {
+            const int m = n;
+            for (int i = 0; i < m; ++i) {
+                ConvChoice f = out[i];
+                f.fused = 1;
+                add(f);
+            }
+        }
+    }
+    t_conv_force = saved;
+    return n;
+}
+
+namespace {
+struct ConvKey {
+    int dev;
+    int64_t B, C, H, W, O;
+    int k, s, p, d, code, out_t;
+    bool same_geometry(const ConvKey &o) const {
+        return dev == o.dev && B == o.B && C == o.C && H == o.H && W == o.W && k == o.k && s == o.s && p == o.p &&
+               d == o.d && code == o.code;
+    }
+    bool operator==(const ConvKey &o) const { return same_geometry(o) && O == o.O && out_t == o.out_t; }
+};
+std::mutex g_conv_mu;
+std::vector<std::pair<ConvKey, ConvChoice>> g_conv_kept;      // most recent last
+std::atomic<int> g_conv_count{0};
+
+ConvKey conv_key(const ConvGeom &g, bt_code code, bt_dtype out_t) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    return ConvKey{dev, g.B, g.C, g.H, g.W, g.O, g.k, g.s, g.p, g.d, static_cast<int>(code), static_cast<int>(out_t)};
+}
+}  // namespace
+
+void conv_remember(const ConvGeom &g, bt_code code, bt_dtype out_t, const ConvChoice &c) {
+    const ConvKey key = conv_key(g, code, out_t);
+    std::lock_guard<std::mutex> lock(g_conv_mu);
+    for (size_t i = 0; i < g_conv_kept.size(); ++i)
+        if (g_conv_kept[i].first == key) {
+            g_conv_kept.erase(g_conv_kept.begin() + static_cast<std::ptrdiff_t>(i));
+            break;
+        }
+    g_conv_kept.emplace_back(key, c);
+    g_conv_count.store(static_cast<int>(g_conv_kept.size()), std::memory_order_release);
+}
+
+bool conv_lookup(const ConvGeom &g, bt_code code, bt_dtype out_t, ConvChoice &c) {
+    if (g_conv_count.load(std::memory_order_acquire) == 0) return false;
+    const ConvKey key = conv_key(g, code, out_t);
+    std::lock_guard<std::mutex> lock(g_conv_mu);
+    for (const auto &e : g_conv_kept)
+        if (e.first == key) {
+            c = e.second;
+            return true;
+        }
+    return false;
+}
+
+bool conv_kept_fused(const ConvGeom &g, bt_code code, bool &fused) {
+    if (g_conv_count.load(std::memory_order_acquire) == 0) return false;
+    const ConvKey key = conv_key(g, code, BT_F32);
+    std::lock_guard<std::mutex> lock(g_conv_mu);
+    for (auto it = g_conv_kept.rbegin(); it != g_conv_kept.rend(); ++it)
+        if (it->first.same_geometry(key)) {
+            fused = it->second.fused == 1;
+            return true;
+        }
+    return false;
+}
+
+void conv_forget() {
+    std::lock_guard<std::mutex> lock(g_conv_mu);
+    g_conv_kept.clear();
+    g_conv_count.store(0, std::memory_order_release);
+}
 
 bool conv_implicit_applies(const ConvGeom &g, bt_code code) {
     if (const char *env = std::getenv("BT_CONV_IMPLICIT")) {
@@ -315,8 +453,10 @@ bool conv_fused_applies(const ConvGeom &g, bt_code code, bt_dtype x_dtype) {
     // CTA, beside its MMA and epilogue warps, convert x more slowly than the
     // standalone pack kernel does with the whole GPU, so the two-kernel route
     // is the default and BT_CONV_FUSED=1 turns this one on
+    // (or a forced plan that packs x itself, where the environment is silent)
     const char *env = std::getenv("BT_CONV_FUSED");
-    if (env == nullptr || std::strcmp(env, "1") != 0) return false;
+    if (env != nullptr ? std::strcmp(env, "1") != 0 : !(t_conv_force != nullptr && t_conv_force->fused == 1))
+        return false;
     if (x_dtype != BT_F32 && x_dtype != BT_BF16 && x_dtype != BT_F16) return false;
     // every channel plane 16-byte aligned; pixel indices of a plane in 31 bits
     const int64_t hw = g.H * g.W;
