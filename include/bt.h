@@ -334,7 +334,8 @@ typedef struct {
  * bt_binary_linear (algo AUTO). For the tensor-core codes it runs the call
  * once untimed and `reps` times timed per candidate launch shape (the cost
  * model's own pick first, then the cheapest tile width by the model for every
- * other pairing and stage depth, each with 4 and 8 epilogue warps), with CUDA
+ * other pairing and stage depth of 1 to 4 K slices, each with 4 and 8
+ * epilogue warps), with CUDA
  * events on `stream`, and keeps the fastest (a shape replaces the one kept so
  * far, the model's first, only when it measures more than 1 % faster, so
  * that timing noise does not move the choice): later bt_binary_linear calls on

@@ -589,8 +589,8 @@ bt_status bt_tune_linear(const void *x, bt_dtype x_dtype, const void *weight, bt
         result->candidates = 1;
         result->us_model = best;
     } else {
-        TcTileChoice cand[16];
-        const int n = tc_linear_candidates(M, N, K, w_code, out_dtype, cand, 16);
+        TcTileChoice cand[24];
+        const int n = tc_linear_candidates(M, N, K, w_code, out_dtype, cand, 24);
         TcTileChoice win{};
         for (int i = 0; i < n; ++i) {
             tc_linear_force(&cand[i]);

@@ -1002,7 +1002,7 @@ int tc_linear_candidates(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype
     add(first.pair, first.bn, first.d, epi0);
     add(first.pair, first.bn, first.d, epi0 == 4 ? 8 : 4);
     for (int p = 1; p >= 0; --p)
-        for (int d = 4; d >= 1; d /= 2) {
+        for (int d = 4; d >= 1; --d) {
             if ((p == 1) == first.pair && d == first.d) continue;
             int best_bn = 0;
             double best = -1.0;
