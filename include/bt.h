@@ -335,7 +335,7 @@ typedef struct {
  * once untimed and `reps` times timed per candidate launch shape (the cost
  * model's own pick first, then the cheapest tile width by the model for every
  * other pairing and stage depth of 1 to 4 K slices, each with 4 and 8
- * epilogue warps), with CUDA
+ * epilogue warps, then narrower tiles in the model's pairing), with CUDA
  * events on `stream`, and keeps the fastest (a shape replaces the one kept so
  * far, the model's first, only when it measures more than 1 % faster, so
  * that timing noise does not move the choice): later bt_binary_linear calls on

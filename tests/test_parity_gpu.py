@@ -447,7 +447,7 @@ def test_full_conv_workloads_bench_calls(name, code):
 
 TC_CONFIGS = ["240,1", "224,2", "128,4", "64,2", "32,1", "208,2", "96,4", "224,3",
               "pair,240,2", "pair,224,1", "pair,160,4", "pair,128,2", "pair,64,4", "pair,32,1", "pair,208,2",
-              "pair,224,3", "pair,240,3"]
+              "pair,224,3", "pair,240,3", "pair,192,2", "pair,112,2", "pair,96,2", "192,2"]
 
 
 @pytest.mark.parametrize("epi", ["4", "8"], ids=["epi4", "epi8"])

@@ -199,7 +199,8 @@ struct TcTileChoice {
 // in `code` (E4M3 / E2M1) writing out_t: the cost model's own choice first,
 // then the cheapest tile width by the model for every other (pair, d) with d
 // of 1 to 4 K slices (the model itself picks among 1, 2 and 4), each
-// with both epilogue warp counts. Writes at most `max`; returns how many.
+// with both epilogue warp counts, then narrower tiles (BN 192 down to 96) in
+// the model's pairing and depth. Writes at most `max`; returns how many.
 int tc_linear_candidates(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t, TcTileChoice *out,
                          int max);
 // The shape the calling thread's linear contractions take until cleared

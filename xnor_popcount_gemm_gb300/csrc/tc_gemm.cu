@@ -1018,6 +1018,10 @@ int tc_linear_candidates(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype
             add(p == 1, best_bn, d, 4);
             add(p == 1, best_bn, d, 8);
         }
+    // narrower tiles in the model's pairing and stage depth: more, shorter
+    // tiles per SM, so less of the last tile's epilogue is left exposed
+    for (int bn : {192, 160, 128, 112, 96})
+        if (bn < first.bn) add(first.pair, bn, first.d, epi0);
     return n;
 }
 
