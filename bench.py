@@ -202,9 +202,11 @@ def measured_peaks():
 
 # nominal dense tensor rates (PFLOP/s) for the ratio to the measured bf16 peak
 NOMINAL_PF = {"bf16": 2.25, "e4m3": 4.5, "e2m1": 13.5}
-# 32-bit population counts per clock per SM: an estimate, from a standalone
-# probe on a GB300 (a loop of XOR + POPC on every SM) that is not part of this
-# repository; the denominator of the popcount path's ALU roofline.
+# 32-bit population counts per clock per SM: the per-SM issue rate the CUDA
+# programming guide's arithmetic-throughput table gives for the popc
+# instruction on recent compute capabilities, and what a standalone probe on a
+# GB300 (a loop of XOR + POPC on every SM, not part of this repository) reached;
+# the denominator of the popcount path's ALU roofline.
 POPC_PER_CLK_PER_SM = 16
 SM_COUNT_GB300 = 152
 

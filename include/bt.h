@@ -168,8 +168,9 @@ bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, 
  *      sign, channel packing into its shared-memory pixel stages) and needs
  *      no workspace -- where the implicit-im2col plan applies, every channel
  *      plane (H * W values of x_dtype) is a multiple of 16 bytes and the
- *      environment sets BT_CONV_FUSED=1 (slower than route 0 on the ResNet
- *      layers measured, so not the default);
+ *      environment sets BT_CONV_FUSED=1, or bt_tune_conv2d kept that route
+ *      for the geometry (slower than route 0 on the ResNet layers measured,
+ *      so not the default);
  *   1  the im2col rows built in one pass from x (the staged form of
  *      bt_pack_im2col), then the contraction of those rows;
  *   0  the pixels packed to NHWC (bt_pack_sign NCHW_TO_NHWC), then the
