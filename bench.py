@@ -644,7 +644,8 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(e2e_ms, 4),
                 "how": f"pinned host buffers (x{nh} rotating); copy-in, forward, copy-out on three streams, "
                        "neighbouring steps overlapped"},
-        "selection": selection if selection is not None else "the planner's launch shape (not measured)",
+        "selection": selection if selection is not None else
+        "not measured (--no-tune): the planner's launch shape, or the one the environment forces",
         "gpu_launches": su.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
