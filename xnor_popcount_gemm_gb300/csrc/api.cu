@@ -496,8 +496,9 @@ bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, 
 }
 
 namespace {
-// The fastest code bt_tune_linear has measured per device and linear problem
-// size (over every output dtype it was run with), and that call's time.
+// The call times bt_tune_linear / bt_tune_conv2d measured per device, layer
+// kind and problem size (M, N, K), one per code (the last timing of each, over
+// whatever output dtype it was run with); bt_plan takes the shortest.
 struct CodeKey {
     int dev, op;
     int64_t M, N, K;
