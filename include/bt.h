@@ -98,13 +98,21 @@ typedef enum {
 
 /*
  * Contraction kernels (the BMM type of BinaryLinearCuda, whose default
- * BMM.ADAPTIVE picks one; here BT_ALGO_AUTO does).
+ * BMM.ADAPTIVE picks one; here BT_ALGO_AUTO does, and BT_ALGO_TUNE does by
+ * measurement).
  */
 typedef enum {
     BT_ALGO_AUTO = 0,        /* the kernel for the weight's code chosen by bt_plan() */
     BT_ALGO_POPC = 1,        /* CUDA cores: XOR + popcount, code BITS */
     BT_ALGO_TC_E4M3 = 2,     /* tcgen05 kind::f8f6f4 on +1/-1 E4M3, code E4M3 */
-    BT_ALGO_TC_E2M1 = 3      /* tcgen05 kind::mxf4 on +1/-1 E2M1 (unit block scales), code E2M1 */
+    BT_ALGO_TC_E2M1 = 3,     /* tcgen05 kind::mxf4 on +1/-1 E2M1 (unit block scales), code E2M1 */
+    BT_ALGO_TUNE = 4         /* AUTO, measured: bt_binary_linear / bt_binary_conv2d only. The first
+                                call of a size (on this device, with this code and output dtype)
+                                that has launch shapes or plans to choose from runs bt_tune_linear /
+                                bt_tune_conv2d (3 timed calls per candidate; it blocks the calling
+                                thread) and returns with that call's result in out; later calls take
+                                the kept shape or plan. Inside a stream capture, for BT_CODE_BITS and
+                                where the convolution has one route, it runs as AUTO. */
 } bt_algo;
 
 typedef enum { BT_OP_LINEAR = 0, BT_OP_CONV2D = 1 } bt_op;

@@ -258,6 +258,20 @@ def test_tune_abi_validation():
     assert TC(*(cargs[:3] + (7,) + cargs[4:]), 5, None, cr) == bt.BT_ERR_INVALID_ARG
     assert TC(*cargs, 5, None, cr) == bt.BT_OK
     assert cres.candidates == 0 and cres.us == 0.0
+    # BT_ALGO_TUNE on the forward entry points: the same host checks as AUTO;
+    # the variants that take no measured selection refuse it
+    L = bt._c_lin
+    lin = (None, bt.BT_F32, None, bt.BT_CODE_E2M1, 0, 8, 8, 1.0, 1.0, None, 0, None, bt.BT_F32)
+    assert L(*lin, bt.BT_ALGO_TUNE, None, 0, None) == bt.BT_OK                     # zero rows: a no-op
+    assert L(*lin[:7], -1.0, *lin[8:], bt.BT_ALGO_TUNE, None, 0, None) == bt.BT_ERR_INVALID_ARG
+    assert L(*lin, 5, None, 0, None) == bt.BT_ERR_INVALID_ARG
+    C = bt._c_conv
+    conv = (None, bt.BT_F32, None, bt.BT_CODE_E2M1, 0, 64, 14, 14, 64, 3, 1, 1, 1, 1.0, 1.0, None, 0, None,
+            bt.BT_F32)
+    assert C(*conv, bt.BT_ALGO_TUNE, None, 0, None) == bt.BT_OK                     # zero images: a no-op
+    LD = bt._c_lin_ds
+    assert LD(None, bt.BT_F32, None, bt.BT_CODE_E2M1, 0, 8, 8, 256, None, 0, None, bt.BT_F32, bt.BT_ALGO_TUNE,
+              None, 0, None) == bt.BT_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")

@@ -187,3 +187,55 @@ def test_plan_names_fastest_measured_conv_code():
     assert bt.bt_plan(bt.BT_OP_CONV2D, M, N, K)[0] == min(times, key=times.get)
     bt.bt_tune_reset()
     assert bt.bt_plan(bt.BT_OP_CONV2D, M, N, K) == before
+
+
+# ---------------------------------------------------------------------------
+# BT_ALGO_TUNE: the forward entry points tune a size on its first call
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
+def test_algo_tune_linear_first_call_tunes(code):
+    M, N, K = 900, 520, 1700
+    x, w, want = _problem(M, N, K, torch.bfloat16, seed=7)
+    xd, wp = x.to(DEV), bt.bt_pack_sign(w.to(DEV), code)
+    for _ in range(2):          # the first call tunes, the second takes the kept shape
+        got = bt.bt_binary_linear(xd, wp, code, K, 1.0, 1.0, out_dtype=torch.int32, algo=bt.BT_ALGO_TUNE).cpu()
+        assert torch.equal(got, want)
+    # the size was timed: bt_plan names the one code measured for it
+    assert bt.bt_plan(bt.BT_OP_LINEAR, M, N, K)[0] == code
+
+
+@pytest.mark.parametrize("code", TC_CODES, ids=["e4m3", "e2m1"])
+def test_algo_tune_conv_first_call_tunes(code):
+    B, C, H, W, O, k, s, p, d = 2, 128, 28, 28, 256, 3, 2, 1, 1
+    x = _gen(11, (B, C, H, W), torch.bfloat16)
+    w = _gen(12, (O, C, k, k), torch.bfloat16)
+    want = torch.from_numpy(oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d))
+    xd, wp = x.to(DEV), bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    for _ in range(2):
+        got = bt.bt_binary_conv2d(xd, wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32,
+                                  algo=bt.BT_ALGO_TUNE).cpu()
+        assert torch.equal(got, want)
+    Ho = bt.conv2d_out_size(H, k, s, p, d)
+    assert bt.bt_plan(bt.BT_OP_CONV2D, B * Ho * Ho, O, C * k * k)[0] == code
+
+
+def test_algo_tune_inside_a_capture_runs_as_auto():
+    M, N, K = 512, 384, 1000
+    code = bt.BT_CODE_E4M3
+    x, w, want = _problem(M, N, K, torch.bfloat16, seed=9)
+    xd, wp = x.to(DEV), bt.bt_pack_sign(w.to(DEV), code)
+    out = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    ws = torch.empty(bt.bt_binary_linear_workspace(M, K, bt.BT_BF16, code), dtype=torch.uint8, device=DEV)
+    before = bt.bt_plan(bt.BT_OP_LINEAR, M, N, K)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        bt.bt_binary_linear(xd, wp, code, K, 1.0, 1.0, out_dtype=torch.int32, algo=bt.BT_ALGO_TUNE, out=out,
+                            workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), want)
+    # nothing was timed or kept
+    assert bt.bt_plan(bt.BT_OP_LINEAR, M, N, K) == before

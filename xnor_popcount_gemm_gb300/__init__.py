@@ -19,13 +19,13 @@ from . import build as _build
 __all__ = [
     "BtError", "lib_path", "BT_F32", "BT_BF16", "BT_F16", "BT_I32", "BT_PACKED", "BT_PACKED_IM2COL",
     "BT_CODE_BITS", "BT_CODE_E4M3", "BT_CODE_E2M1", "BT_LAYOUT_ROWS", "BT_LAYOUT_NCHW_TO_NHWC",
-    "BT_ALGO_AUTO", "BT_ALGO_POPC", "BT_ALGO_TC_E4M3", "BT_ALGO_TC_E2M1", "BT_OP_LINEAR",
+    "BT_ALGO_AUTO", "BT_ALGO_POPC", "BT_ALGO_TC_E4M3", "BT_ALGO_TC_E2M1", "BT_ALGO_TUNE", "BT_OP_LINEAR",
     "BT_OP_CONV2D", "bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_sign",
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
     "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
     "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_tune_linear",
-            "bt_tune_reset", "bt_tune_conv2d", "bt_set_wait_timeout",
-    "bt_binary_linear_dscale_init", "bt_binary_conv2d_dscale_init",
+    "bt_tune_reset", "bt_tune_conv2d", "bt_set_wait_timeout", "bt_binary_linear_dscale_init",
+    "bt_binary_conv2d_dscale_init",
 ]
 
 BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_ALIGNMENT = 0, -1, -2, -3
@@ -33,7 +33,7 @@ BT_ERR_WORKSPACE, BT_ERR_CUDA, BT_ERR_TIMEOUT = -4, -5, -6
 BT_F32, BT_BF16, BT_F16, BT_I32, BT_PACKED, BT_PACKED_IM2COL = 0, 1, 2, 3, 4, 5
 BT_CODE_BITS, BT_CODE_E4M3, BT_CODE_E2M1 = 0, 1, 2
 BT_LAYOUT_ROWS, BT_LAYOUT_NCHW_TO_NHWC = 0, 1
-BT_ALGO_AUTO, BT_ALGO_POPC, BT_ALGO_TC_E4M3, BT_ALGO_TC_E2M1 = 0, 1, 2, 3
+BT_ALGO_AUTO, BT_ALGO_POPC, BT_ALGO_TC_E4M3, BT_ALGO_TC_E2M1, BT_ALGO_TUNE = 0, 1, 2, 3, 4
 BT_OP_LINEAR, BT_OP_CONV2D = 0, 1
 
 _DT = {torch.float32: BT_F32, torch.bfloat16: BT_BF16, torch.float16: BT_F16, torch.int32: BT_I32}

@@ -68,6 +68,16 @@ bool float_in(int t) { return t == BT_F32 || t == BT_BF16 || t == BT_F16; }
 bool valid_out(int t) { return t == BT_F32 || t == BT_BF16 || t == BT_F16 || t == BT_I32; }
 bool valid_scale(float v) { return std::isfinite(v) && v > 0.0f; }
 
+// Timed calls per candidate when a call with BT_ALGO_TUNE tunes its size.
+constexpr int kAutoTuneReps = 3;
+
+// True while `s` is being captured into a graph (or when the query fails).
+bool stream_capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return true;
+    return cap != cudaStreamCaptureStatusNone;
+}
+
 bt_algo algo_for_code(bt_code c) {
     switch (c) {
         case BT_CODE_BITS: return BT_ALGO_POPC;
@@ -198,6 +208,18 @@ bt_status bt_binary_linear(const void *x, bt_dtype x_dtype, const void *weight, 
                            int64_t M, int64_t N, int64_t K, float scale_a, float scale_w,
                            const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
                            bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+    if (algo == BT_ALGO_TUNE) {
+        algo = BT_ALGO_AUTO;
+        // a size with launch shapes to choose from and none kept yet: tune it
+        // (the last timed call leaves this call's result in out)
+        if ((w_code == BT_CODE_E4M3 || w_code == BT_CODE_E2M1) && M >= 1 && N >= 1 && K >= 1 && K <= kTcMaxK &&
+            valid_out(out_dtype) && !tc_linear_kept(M, N, K, w_code, out_dtype) &&
+            !stream_capturing(reinterpret_cast<cudaStream_t>(stream))) {
+            bt_tune_result r;
+            return bt_tune_linear(x, x_dtype, weight, w_code, M, N, K, scale_a, scale_w, bias_a, bias_len, out,
+                                  out_dtype, workspace, workspace_bytes, kAutoTuneReps, stream, &r);
+        }
+    }
     return linear_impl(x, x_dtype, weight, w_code, M, N, K, scale_a, scale_w, nullptr, bias_a, bias_len, out,
                        out_dtype, algo, workspace, workspace_bytes, stream);
 }
@@ -386,6 +408,27 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
                            int stride, int padding, int dilation, float scale_a, float scale_w,
                            const float *bias_a, int64_t bias_len, void *out, bt_dtype out_dtype,
                            bt_algo algo, void *workspace, size_t workspace_bytes, bt_stream stream) {
+    if (algo == BT_ALGO_TUNE) {
+        algo = BT_ALGO_AUTO;
+        // a geometry with implicit plans to choose from and none kept yet: tune it
+        // (the last timed call leaves this call's result in out)
+        if ((w_code == BT_CODE_E4M3 || w_code == BT_CODE_E2M1) && x_dtype != BT_PACKED_IM2COL && valid_out(out_dtype) &&
+            B >= 1 && C >= 1 && H >= 1 && W >= 1 && O >= 1 && kernel_size >= 1 && kernel_size <= 64 &&
+            stride >= 1 && padding >= 0 && dilation >= 1 && H <= (1 << 20) && W <= (1 << 20) &&
+            C * kernel_size * kernel_size <= kTcMaxK) {
+            ConvGeom g{B, C, H, W, O, 0, 0, kernel_size, stride, padding, dilation};
+            g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
+            g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
+            ConvChoice kept{};
+            if (g.Ho >= 1 && g.Wo >= 1 && conv_implicit_applies(g, w_code) &&
+                !conv_lookup(g, w_code, out_dtype, kept) && !stream_capturing(reinterpret_cast<cudaStream_t>(stream))) {
+                bt_tune_conv_result r;
+                return bt_tune_conv2d(x, x_dtype, weight, w_code, B, C, H, W, O, kernel_size, stride, padding,
+                                      dilation, scale_a, scale_w, bias_a, bias_len, out, out_dtype, workspace,
+                                      workspace_bytes, kAutoTuneReps, stream, &r);
+            }
+        }
+    }
     return conv_impl(x, x_dtype, weight, w_code, B, C, H, W, O, kernel_size, stride, padding, dilation, scale_a,
                      scale_w, nullptr, bias_a, bias_len, out, out_dtype, algo, workspace, workspace_bytes, stream);
 }

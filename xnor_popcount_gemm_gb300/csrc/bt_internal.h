@@ -210,6 +210,8 @@ void tc_linear_force(const TcTileChoice *c);
 // code, out_t) take `c` from now on. tc_linear_forget drops every entry.
 void tc_linear_remember(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t, const TcTileChoice &c);
 void tc_linear_forget();
+// True when a measured winner is kept for this device and key.
+bool tc_linear_kept(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t);
 
 // The driver's cuTensorMapEncodeTiled (looked up once), or nullptr.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

@@ -1034,6 +1034,13 @@ void tc_linear_remember(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype 
     g_tuned_count.store(static_cast<int>(g_tuned.size()), std::memory_order_release);
 }
 
+bool tc_linear_kept(int64_t M, int64_t N, int64_t K, bt_code code, bt_dtype out_t) {
+    if (g_tuned_count.load(std::memory_order_acquire) == 0) return false;
+    const TunedKey key = tuned_key(M, N, K, code, out_t);
+    std::lock_guard<std::mutex> lock(g_tuned_mu);
+    return g_tuned.find(key) != g_tuned.end();
+}
+
 void tc_linear_forget() {
     std::lock_guard<std::mutex> lock(g_tuned_mu);
     g_tuned.clear();
