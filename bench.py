@@ -486,7 +486,7 @@ def tune_conv(bt, wl, dev, reps: int) -> dict:
         r = bt.bt_tune_conv2d(xd, wp, code, C, k, wl.stride, wl.padding, wl.dilation, wl.scale_a, wl.scale_w, bias,
                               out_dtype=out_t, reps=reps if code != 0 else max(1, reps // 5))
         plan = (f"{'pair' if r['pair'] else 'single'} {'resident' if r['weights_resident'] else 'streamed'} "
-                f"weights, {r['pixel_stages']} pixel stage(s), "
+                f"weights, {r['pixel_stages']} pixel stage(s), {r['band_split']}x the planner's bands, "
                 f"{'packs x itself' if r['fused'] else 'after the NHWC pack'}" if code != 0 else "popcount route")
         per[ALGO_NAME[code]] = {"us": round(r["us"], 2), "us_planner_plan": round(r["us_model"], 2), "kept": plan,
                                 "candidates": r["candidates"]}

@@ -376,6 +376,7 @@ typedef struct {
     int candidates;            /* plans timed (1 where the geometry has one route) */
     float us;                  /* mean microseconds of one call in the kept plan */
     float us_model;            /* the same for the plan the planner picks unmeasured */
+    int band_split;            /* implicit plan: bands per image, as a multiple of the planner's (1, 2, 4) */
 } bt_tune_conv_result;
 
 /*
@@ -385,9 +386,11 @@ typedef struct {
  * applies (codes E4M3 / E2M1, x not BT_PACKED_IM2COL) it runs the call once
  * untimed and `reps` times timed per candidate plan -- the planner's own
  * first, then every other fitting combination of CTA pairs or single CTAs,
- * resident or streamed weights and 1 or 2 pixel stages, then each of them
- * with the convolution packing x itself where x is float and that route
- * applies -- with CUDA events on `stream`, and keeps the fastest (a plan
+ * resident or streamed weights and 1 or 2 pixel stages, each also with 2 and
+ * 4 times the planner's bands per image (more, narrower tiles) where that
+ * changes the tiling, then each of them with the convolution packing x
+ * itself where x is float and that route applies -- with CUDA events on
+ * `stream`, and keeps the fastest (a plan
  * replaces the planner's only when more than 1 % faster). Later
  * bt_binary_conv2d calls on this device with the same geometry (B, C, H, W,
  * O, kernel_size, stride, padding, dilation), w_code and out_dtype take it,
@@ -400,7 +403,7 @@ typedef struct {
  * every timed call. reps 1..10000; result not NULL. Errors: those of
  * bt_binary_conv2d; BT_ERR_UNSUPPORTED while `stream` is being captured. B or
  * O zero: nothing is timed or kept. The environment's BT_CONV_PAIR /
- * BT_CONV_PLAN / BT_CONV_FUSED still override the kept plan.
+ * BT_CONV_PLAN / BT_CONV_FUSED / BT_CONV_SPLIT still override the kept plan.
  */
 bt_status bt_tune_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt_code w_code,
                          int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,

@@ -187,3 +187,23 @@ def test_fused_conv_needs_no_workspace():
     assert st == bt.BT_OK
     want = oracle.conv2d_dot(oracle.binarize(x.cpu()), oracle.binarize_weight(w), 1, 1, 1)
     assert torch.equal(out.cpu(), torch.from_numpy(want))
+
+
+@pytest.mark.parametrize("split", ["2", "4"])
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["pair", "single"])
+@pytest.mark.parametrize("code", TC_CODES, ids=TC_IDS)
+def test_fused_conv_more_bands(code, pair, split, monkeypatch):
+    # the convolution that packs x itself over 2 or 4 times the bands: staged
+    # rows past the image are cleared per tile
+    monkeypatch.setenv("BT_CONV_FUSED", "1")
+    monkeypatch.setenv("BT_CONV_PAIR", pair)
+    monkeypatch.setenv("BT_CONV_SPLIT", split)
+    for (B, C, H, W, O, k, s, p, d) in ((3, 128, 16, 16, 256, 3, 1, 1, 1), (2, 128, 28, 28, 130, 3, 2, 1, 1)):
+        x = _gen(41 + H, (B, C, H, W), torch.bfloat16)
+        w = _gen(42 + O, (O, C, k, k))
+        bias = torch.linspace(-0.2, 0.2, C)
+        assert _mode(x, C, k, s, p, d, code) == 2
+        wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+        want = oracle.conv2d_dot(oracle.binarize(x, bias, channel_axis=1), oracle.binarize_weight(w), s, p, d)
+        got = bt.bt_binary_conv2d(x.to(DEV), wp, code, C, k, s, p, d, 1.0, 1.0, bias.to(DEV), out_dtype=torch.int32)
+        assert torch.equal(got.cpu(), torch.from_numpy(want))

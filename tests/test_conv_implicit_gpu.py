@@ -180,3 +180,25 @@ def test_weights_packed_just_before_each_call(code):
     wants = [oracle.conv2d_dot(sx, oracle.binarize_weight(w), s, p, d) for w in ws]
     for i, got in enumerate(outs):
         assert torch.equal(got.cpu(), torch.from_numpy(wants[i % 3]))
+
+
+@pytest.mark.parametrize("split", ["2", "4"])
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["pair", "single"])
+@pytest.mark.parametrize("code", TC_CODES, ids=TC_IDS)
+@pytest.mark.parametrize("B,C,H,W,O,k,s,p,d", [SHAPES[0], SHAPES[2], SHAPES[3], SHAPES[4], SHAPES[5], SHAPES[13]])
+def test_implicit_conv_more_bands_matches_oracle(code, B, C, H, W, O, k, s, p, d, pair, split, monkeypatch):
+    # BT_CONV_SPLIT: each image cut into 2 or 4 times the bands that fit a
+    # tile (narrower tiles, as the measured selection may keep), packed pixels
+    # read in place
+    monkeypatch.setenv("BT_CONV_FUSED", "0")
+    monkeypatch.setenv("BT_CONV_PAIR", pair)
+    monkeypatch.setenv("BT_CONV_SPLIT", split)
+    assert _implicit(B, C, H, W, k, s, p, d, code)
+    x = _gen(B * 5 + C + H, (B, C, H, W), torch.bfloat16)
+    w = _gen(O + k + 3 * C, (O, C, k, k), torch.bfloat16)
+    want = oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d)
+    wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    sa, sw = workloads.mean_abs(x), workloads.mean_abs(w)
+    for od in ("i32", "bf16"):
+        got = bt.bt_binary_conv2d(x.to(DEV), wp, code, C, k, s, p, d, sa, sw, out_dtype=OUT_T[od]).cpu()
+        _close(got, oracle.epilogue(want, sa, sw, od))

@@ -107,7 +107,7 @@ _c_tune_reset = _sig("bt_tune_reset", None, [])
 class TuneConvResult(ctypes.Structure):
     """bt_tune_conv_result: what bt_tune_conv2d measured and kept."""
     _fields_ = [("code", _i), ("pair", _i), ("weights_resident", _i), ("pixel_stages", _i), ("fused", _i),
-                ("candidates", _i), ("us", _f), ("us_model", _f)]
+                ("candidates", _i), ("us", _f), ("us_model", _f), ("band_split", _i)]
 
 
 _c_tune_conv = _sig("bt_tune_conv2d", _i, [_p, _i, _p, _i, _i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _f, _f, _p,

@@ -502,7 +502,7 @@ int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel
     bool kept_fused = false;
     if (conv_forced() == nullptr && conv_kept_fused(g, code, kept_fused)) {
         // the route bt_tune_conv2d kept for this geometry
-        const ConvChoice f{-1, 0, 0, kept_fused ? 1 : 0};
+        const ConvChoice f{-1, 0, 0, kept_fused ? 1 : 0, 0};
         conv_force(&f);
         const bool fused = conv_fused_applies(g, code, x_dtype);
         conv_force(nullptr);
@@ -692,9 +692,9 @@ bt_status bt_tune_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt
     if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return BT_ERR_CUDA;
     if (cap != cudaStreamCaptureStatusNone) return BT_ERR_UNSUPPORTED;       // timing needs real launches
     ConvGeom g{B, C, H, W, O, Ho, Wo, kernel_size, stride, padding, dilation};
-    ConvChoice cand[24];
+    ConvChoice cand[64];
     const int n = (x_dtype == BT_PACKED_IM2COL || w_code == BT_CODE_BITS)
-                      ? 0 : conv_candidates(g, w_code, x_dtype, out_dtype, cand, 24);
+                      ? 0 : conv_candidates(g, w_code, x_dtype, out_dtype, cand, 64);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (cudaEventCreate(&e0) != cudaSuccess) return BT_ERR_CUDA;
     if (cudaEventCreate(&e1) != cudaSuccess) {
@@ -729,6 +729,7 @@ bt_status bt_tune_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt
             result->weights_resident = win.plan == 'R' ? 1 : 0;
             result->pixel_stages = win.bst;
             result->fused = win.fused;
+            result->band_split = win.split > 1 ? win.split : 1;
         }
     }
     cudaEventDestroy(e0);

@@ -253,14 +253,16 @@ cudaError_t launch_tc_conv_fused(const void *x, bt_dtype x_dtype, const float *b
 
 // A launch plan of the implicit-im2col convolution, for the measured
 // selection: CTA pairs or single CTAs, weights resident ('R') or streamed
-// ('S'), 1 or 2 pixel stages, and (fused = 1) the convolution packing x
-// itself instead of the NHWC pack kernel running first.
+// ('S'), 1 or 2 pixel stages, (fused = 1) the convolution packing x itself
+// instead of the NHWC pack kernel running first, and (split > 1) each image
+// cut into that many times the planner's bands (more, narrower tiles).
 struct ConvChoice {
-    int pair, plan, bst, fused;
+    int pair, plan, bst, fused, split;
 };
 // The plans the measured selection times for this geometry, code, input and
 // output dtype: the planner's own first, then every other (pair, plan,
-// stages) that fits, then each of them packing x itself where that route
+// stages) that fits, each also with 2 and 4 times the bands where that
+// changes the tiling, then each of them packing x itself where that route
 // applies (float x). Writes at most `max`; returns how many (0 where the
 // implicit plan does not apply).
 int conv_candidates(const ConvGeom &g, bt_code code, bt_dtype x_dtype, bt_dtype out_t, ConvChoice *out, int max);

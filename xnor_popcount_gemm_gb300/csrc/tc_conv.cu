@@ -92,11 +92,20 @@ bool plan_conv(const ConvGeom &g, bt_code code, int sms, int out_elem, ConvPlan 
     if (a.Wo % 2 == 0 && a.wv % 2 == 1 && a.wv + 1 <= bn_max) a.wv += 1;
     if (a.wv > bn_max || a.wv * s > 256) return false;
     p.cp = cp;
+    // BT_CONV_SPLIT=n (or a forced plan's split) cuts each image into n times
+    // as many bands as fit a tile: more, narrower tiles
+    int split = 1;
+    if (const char *env = std::getenv("BT_CONV_SPLIT")) split = std::atoi(env);
+    else if (t_conv_force != nullptr && t_conv_force->split > 1) split = t_conv_force->split;
+    if (split < 1) split = 1;
+    if (split > 8) split = 8;
     if (!cp) {
         int ht = bn_max / a.wv;
         if (ht > a.Ho) ht = a.Ho;
         a.bands = (a.Ho + ht - 1) / ht;
+        if (split > 1) a.bands = a.bands * split < a.Ho ? a.bands * split : a.Ho;
         a.ht = (a.Ho + a.bands - 1) / a.bands;       // balance the bands
+        a.bands = (a.Ho + a.ht - 1) / a.ht;          // (a split leaves no band empty)
         a.bn = (a.ht * a.wv + 15) / 16 * 16;
         if (a.bn < 32) a.bn = 32;
         if (a.bn > bn_max) return false;
@@ -108,7 +117,9 @@ bool plan_conv(const ConvGeom &g, bt_code code, int sms, int out_elem, ConvPlan 
         if (ht2 > (a.Ho + 1) / 2) ht2 = (a.Ho + 1) / 2;
         if (ht2 < 1) return false;
         a.bands = (a.Ho + 2 * ht2 - 1) / (2 * ht2);
+        if (split > 1) a.bands = a.bands * split < (a.Ho + 1) / 2 ? a.bands * split : (a.Ho + 1) / 2;
         a.ht2 = (a.Ho + 2 * a.bands - 1) / (2 * a.bands);   // balance the bands
+        a.bands = (a.Ho + 2 * a.ht2 - 1) / (2 * a.ht2);      // (a split leaves no band empty)
         a.ht = 2 * a.ht2;
         a.nb = (a.ht2 * a.wv + 7) / 8 * 8;
         if (a.nb < 16) a.nb = 16;
@@ -309,35 +320,52 @@ int conv_candidates(const ConvGeom &g, bt_code code, bt_dtype x_dtype, bt_dtype 
     auto add = [&](const ConvChoice &c) {
         if (n >= max) return;
         for (int i = 0; i < n; ++i)
-            if (out[i].pair == c.pair && out[i].plan == c.plan && out[i].bst == c.bst && out[i].fused == c.fused)
+            if (out[i].pair == c.pair && out[i].plan == c.plan && out[i].bst == c.bst && out[i].fused == c.fused &&
+                (out[i].split > 1 ? out[i].split : 1) == (c.split > 1 ? c.split : 1))
                 return;
         out[n++] = c;
     };
     if (max > 0 && out != nullptr && conv_implicit_applies(g, code)) {
         const int oe = out_t == BT_BF16 || out_t == BT_F16 ? 2 : 4;
         const int sms = device_sm_count();
-        // the plan a launch takes under forced choice f (nullptr: the planner's own)
-        auto effective = [&](const ConvChoice *f, ConvChoice &c) {
+        // the plan a launch takes under forced choice f (nullptr: the planner's
+        // own), and its bands per image
+        auto effective = [&](const ConvChoice *f, ConvChoice &c, int &bands) {
             t_conv_force = f;
             ConvPlan p;
             const bool ok = choose_plan(g, code, sms, oe, p);
             t_conv_force = nullptr;
             if (!ok) return false;
-            c = ConvChoice{p.cp ? 1 : 0, p.a.a_resident ? 'R' : 'S', p.a.b_stages, 0};
+            c = ConvChoice{p.cp ? 1 : 0, p.a.a_resident ? 'R' : 'S', p.a.b_stages, 0, f != nullptr ? f->split : 0};
+            bands = p.a.bands;
             return true;
         };
         ConvChoice c{};
-        if (effective(nullptr, c)) add(c);
+        int bands = 0;
+        if (effective(nullptr, c, bands)) add(c);
         const int plans[4][2] = {{'R', 2}, {'R', 1}, {'S', 2}, {'S', 1}};
         for (int pair = 1; pair >= 0; --pair)
             for (const auto &pl : plans) {
-                const ConvChoice f{pair, pl[0], pl[1], 0};
-                if (effective(&f, c) && c.pair == f.pair && c.plan == f.plan && c.bst == f.bst) add(c);
+                const ConvChoice f{pair, pl[0], pl[1], 0, 0};
+                int b0 = 0;
+                if (!(effective(&f, c, b0) && c.pair == f.pair && c.plan == f.plan && c.bst == f.bst)) continue;
+                add(c);
+                // the same plan over more bands, where that changes the tiling
+                int last = b0;
+                for (int sp = 2; sp <= 4; sp *= 2) {
+                    const ConvChoice fs{pair, pl[0], pl[1], 0, sp};
+                    int bs = 0;
+                    if (effective(&fs, c, bs) && c.pair == fs.pair && c.plan == fs.plan && c.bst == fs.bst &&
+                        bs > last) {
+                        add(c);
+                        last = bs;
+                    }
+                }
             }
         // each plan again with the convolution packing x itself, where it can
         bool fused_ok = false;
         if (x_dtype == BT_F32 || x_dtype == BT_BF16 || x_dtype == BT_F16) {
-            const ConvChoice f{-1, 0, 0, 1};
+            const ConvChoice f{-1, 0, 0, 1, 0};
             t_conv_force = &f;
             fused_ok = conv_fused_applies(g, code, x_dtype);
             t_conv_force = nullptr;
