@@ -202,3 +202,26 @@ def test_implicit_conv_more_bands_matches_oracle(code, B, C, H, W, O, k, s, p, d
     for od in ("i32", "bf16"):
         got = bt.bt_binary_conv2d(x.to(DEV), wp, code, C, k, s, p, d, sa, sw, out_dtype=OUT_T[od]).cpu()
         _close(got, oracle.epilogue(want, sa, sw, od))
+
+
+@pytest.mark.parametrize("split", ["2", "4"])
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["pair", "single"])
+@pytest.mark.parametrize("fused", ["0", "1"], ids=["packed", "fused"])
+@pytest.mark.parametrize("code", TC_CODES, ids=TC_IDS)
+def test_more_bands_several_tiles_per_cta(code, fused, pair, split, monkeypatch):
+    # enough images that CTAs take three or more tiles each, so both
+    # accumulator buffers are reused after bands whose last rows leave some
+    # epilogue warps without a box (the 14-row image cut into 4 bands of 4,
+    # 4, 4 and 2 rows): every warp must still hand the buffer back
+    monkeypatch.setenv("BT_CONV_FUSED", fused)
+    monkeypatch.setenv("BT_CONV_PAIR", pair)
+    monkeypatch.setenv("BT_CONV_SPLIT", split)
+    # (f32 x: 784-byte channel planes, so the convolution that packs x itself applies)
+    B, C, H, W, O, k, s, p, d = 48, 128, 14, 14, 256, 3, 1, 1, 1
+    x = _gen(B + 77, (B, C, H, W), torch.float32)
+    w = _gen(O + 78, (O, C, k, k), torch.float32)
+    want = oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d)
+    wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    got = bt.bt_binary_conv2d(x.to(DEV), wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32).cpu()
+    assert bt.bt_device_status() == 0
+    assert torch.equal(got, torch.from_numpy(want))

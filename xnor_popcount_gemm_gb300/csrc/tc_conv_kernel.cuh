@@ -945,6 +945,9 @@ conv_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 // load waits long while MMAs of the other buffer run, most under CTA
                 // pairs); the accumulator goes back after the last batch's loads
                 const int nmine = (nbox - half + 1) / 2;
+                // a warp with no box of this tile (a band of at most 32 valid
+                // columns) still hands the accumulator back
+                if (nmine <= 0) release();
                 for (int j0 = 0; j0 < nmine; j0 += kEpiBatch) {
                     uint32_t r[kEpiBatch][32];
 #pragma unroll
