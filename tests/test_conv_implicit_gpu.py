@@ -225,3 +225,23 @@ def test_more_bands_several_tiles_per_cta(code, fused, pair, split, monkeypatch)
     got = bt.bt_binary_conv2d(x.to(DEV), wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32).cpu()
     assert bt.bt_device_status() == 0
     assert torch.equal(got, torch.from_numpy(want))
+
+
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["pair", "single"])
+@pytest.mark.parametrize("code", TC_CODES, ids=TC_IDS)
+@pytest.mark.parametrize("B,C,H,W,O", [(400, 40, 1, 1, 17), (360, 64, 3, 3, 96)])
+def test_tiny_images_several_tiles_per_cta(code, B, C, H, W, O, pair, monkeypatch):
+    # images whose whole band fits one 32-column epilogue box, many of them:
+    # CTAs take three tiles or more, and the epilogue warps without a box must
+    # still hand each accumulator buffer back
+    monkeypatch.setenv("BT_CONV_FUSED", "0")
+    monkeypatch.setenv("BT_CONV_PAIR", pair)
+    k, s, p, d = 3, 1, 1, 1
+    assert _implicit(B, C, H, W, k, s, p, d, code)
+    x = _gen(B + H, (B, C, H, W), torch.bfloat16)
+    w = _gen(O + C, (O, C, k, k), torch.bfloat16)
+    want = oracle.conv2d_dot(oracle.binarize(x), oracle.binarize_weight(w), s, p, d)
+    wp = bt.bt_pack_sign(w.to(DEV), code, bt.BT_LAYOUT_NCHW_TO_NHWC)
+    got = bt.bt_binary_conv2d(x.to(DEV), wp, code, C, k, s, p, d, 1.0, 1.0, out_dtype=torch.int32).cpu()
+    assert bt.bt_device_status() == 0
+    assert torch.equal(got, torch.from_numpy(want))
