@@ -52,9 +52,11 @@ def parse():
     ap.add_argument("--config-steps", type=int, default=20, help="timed steps per configuration and code")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the headline steps one call at a time instead of replaying them as a CUDA graph")
-    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward", "w8a8", "w8a8-smooth"],
+    ap.add_argument("--pass", dest="pass_", default="forward",
+                    choices=["forward", "backward", "w8a8", "w8a8-smooth", "tune-survey"],
                     help="backward: the straight-through backward (all three gradients); w8a8[-smooth]: the W8A8 "
-                         "im2col + gemm convolution of a conv workload (with SmoothQuant)")
+                         "im2col + gemm convolution of a conv workload (with SmoothQuant); tune-survey: the "
+                         "measured selection over ResNet conv layers and LLM projection shapes")
     return ap.parse_args()
 
 
@@ -899,6 +901,63 @@ def run_backward(args, rank, world):
     return line
 
 
+# layers of the measured-selection survey: ResNet convolutions (B, C, H = W, O,
+# k, s, p, d, x dtype) and LLM projections (M, N, K; bf16 x)
+SURVEY_CONVS = [
+    (64, 64, 56, 64, 3, 1, 1, 1, torch.bfloat16), (64, 64, 56, 128, 3, 2, 1, 1, torch.bfloat16),
+    (128, 128, 28, 128, 3, 1, 1, 1, torch.bfloat16), (128, 128, 28, 256, 3, 2, 1, 1, torch.bfloat16),
+    (128, 256, 14, 256, 3, 1, 1, 1, torch.bfloat16), (128, 256, 14, 512, 3, 2, 1, 1, torch.bfloat16),
+    (256, 512, 7, 512, 3, 1, 1, 1, torch.bfloat16), (128, 256, 14, 256, 3, 1, 1, 1, torch.float32),
+    (256, 128, 28, 256, 3, 2, 1, 1, torch.bfloat16), (32, 512, 7, 2048, 1, 1, 0, 1, torch.bfloat16),
+]
+SURVEY_LINEARS = [(256, 4096, 4096), (1024, 4096, 4096), (2048, 11008, 4096), (4096, 4096, 11008),
+                  (8192, 11008, 4096), (512, 14336, 4096), (16384, 4096, 4096), (4096, 1024, 4096)]
+
+
+def run_tune_survey(args, rank, world):
+    """bt_tune_conv2d / bt_tune_linear on each survey layer (seeded random
+    inputs on the device): per layer the kept plan or shape, its time per call
+    and the planner's, with --tune-reps timed calls per candidate."""
+    import xnor_popcount_gemm_gb300 as bt
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    rows = []
+    for (B, C, H, O, k, s, p, d, dt) in SURVEY_CONVS:
+        x = torch.randn(B, C, H, H, device=dev, generator=g).to(dt)
+        w = torch.randn(O, C, k, k, device=dev, generator=g).to(dt)
+        wp = bt.bt_pack_sign(w, bt.BT_CODE_E2M1, bt.BT_LAYOUT_NCHW_TO_NHWC)
+        bt.bt_tune_reset()
+        r = bt.bt_tune_conv2d(x, wp, bt.BT_CODE_E2M1, C, k, s, p, d, 1.0, 1.0, reps=args.tune_reps)
+        rows.append({"layer": f"conv [{B},{C},{H},{H}] -> {O}, {k}x{k} s{s} p{p} d{d}, {str(dt)[6:]} x",
+                     "kept": f"{'pairs' if r['pair'] else 'single'}, {'resident' if r['weights_resident'] else 'streamed'}"
+                             f", {r['pixel_stages']} stage(s), {r['band_split']}x bands"
+                             f"{', packs x itself' if r['fused'] else ''}",
+                     "candidates": r["candidates"], "us": round(r["us"], 2), "us_planner": round(r["us_model"], 2)})
+        del x, w, wp
+    for (M, N, K) in SURVEY_LINEARS:
+        x = torch.randn(M, K, device=dev, generator=g).to(torch.bfloat16)
+        w = torch.randn(N, K, device=dev, generator=g).to(torch.bfloat16)
+        for code in (bt.BT_CODE_E2M1, bt.BT_CODE_E4M3):
+            wp = bt.bt_pack_sign(w, code)
+            bt.bt_tune_reset()
+            r = bt.bt_tune_linear(x, wp, code, K, 1.0, 1.0, reps=args.tune_reps)
+            rows.append({"layer": f"linear {M}x{N}x{K} {ALGO_NAME[code]}",
+                         "kept": f"{'pairs' if r['pair'] else 'single'}, BN {r['bn']}, {r['slices_per_stage']} "
+                                 f"slice(s) per stage, {r['epilogue_warps']} epilogue warps",
+                         "candidates": r["candidates"], "us": round(r["us"], 2), "us_planner": round(r["us_model"], 2),
+                         "gops": round(2.0 * M * N * K / r["us"] / 1e3, 1)})
+            del wp
+        del x, w
+    bt.bt_tune_reset()
+    if bt.bt_device_status() != 0:
+        raise RuntimeError("device status after the survey")
+    return {"metric": "measured selection survey", "pass": "tune-survey", "n_gpus": 1, "reps": args.tune_reps,
+            "how": "whole public calls on x timed per candidate with CUDA events; a candidate replaces the "
+                   "planner's choice only when > 1 % faster", "layers": rows}
+
+
 def run_w8a8(args, rank, world):
     """K steps of the W8A8 im2col + gemm convolution on the workload's x and W
     (quantization of both sides inside every step)."""
@@ -1032,6 +1091,8 @@ def main():
     rank, world = dist_init(args)
     if args.pass_ == "backward":
         line = run_backward(args, rank, world)
+    elif args.pass_ == "tune-survey":
+        line = run_tune_survey(args, rank, world)
     elif args.pass_.startswith("w8a8"):
         line = run_w8a8(args, rank, world)
     else:
