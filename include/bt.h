@@ -416,6 +416,41 @@ bt_status bt_tune_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt
  * kept (all devices). */
 void bt_tune_reset(void);
 
+/* The tiling of the implicit-im2col convolution (what bt_conv2d_plan_info reports). */
+typedef struct {
+    int implicit;           /* 1: the implicit plan applies (else the call unfolds into im2col rows) */
+    int pair;               /* 1: CTA pairs, 256-channel tiles */
+    int weights_resident;   /* 1: weights held in shared memory for the launch */
+    int pixel_stages;       /* staged pixel images in flight (1 or 2) */
+    int bands;              /* bands (tiles along the output rows) per image */
+    int band_rows;          /* output rows per band */
+    int cta_rows;           /* rows of a band one CTA stages (half a band for pairs) */
+    int row_width;          /* virtual row width wv >= Wo: accumulator column = row * wv + column */
+    int tile_n;             /* accumulator columns per tile (the MMA's N) */
+    int cta_n;              /* accumulator columns per CTA (tile_n / 2 for pairs) */
+    int staged_rows;        /* rows of wv pixels staged per phase image */
+    int phases;             /* phase images per tile (stride 2: up to 4) */
+    int max_tap_shift;      /* largest start shift, in virtual pixels, of a tap's B operand */
+    int tiles;              /* tiles per launch */
+    int smem_bytes;         /* dynamic shared memory per CTA */
+} bt_conv_plan_info;
+
+/*
+ * bt_conv2d_plan_info -- the tiling bt_binary_conv2d's implicit-im2col
+ * convolution takes for this geometry (no page counterpart: an inspection
+ * call, host only, no CUDA call). code E4M3 / E2M1; out_dtype sizes the
+ * epilogue's staging; sms the SMs to plan for (> 0); pair -1 for the
+ * planner's choice, 0 or 1 to ask for single CTAs or pairs (pairs where they
+ * fit); split >= 1 cuts each image into that many times the planner's bands
+ * (BT_CONV_SPLIT). The environment's BT_CONV_* variables apply as for a
+ * call. info->implicit = 0 where the implicit plan does not apply.
+ * Errors: BT_ERR_INVALID_ARG (info NULL, bad sizes, code or dtype, sms < 1,
+ * pair outside -1..1, split < 1).
+ */
+bt_status bt_conv2d_plan_info(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size,
+                              int stride, int padding, int dilation, bt_code code, bt_dtype out_dtype,
+                              int sms, int pair, int split, bt_conv_plan_info *info);
+
 /* ------------------------------------------------------------------------
  * Device-side scales (no host synchronisation). The page's forward reads the
  * scales with .item() (BinaryConv2dForward.forward: scale_a.item() *

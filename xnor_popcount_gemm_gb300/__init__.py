@@ -24,7 +24,7 @@ __all__ = [
     "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
     "bt_binary_conv2d", "bt_plan", "bt_device_status", "conv2d_out_size", "bt_binary_linear_noalloc",
     "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_tune_linear",
-    "bt_tune_reset", "bt_tune_conv2d", "bt_set_wait_timeout", "bt_binary_linear_dscale_init",
+    "bt_tune_reset", "bt_tune_conv2d", "bt_conv2d_plan_info", "bt_set_wait_timeout", "bt_binary_linear_dscale_init",
     "bt_binary_conv2d_dscale_init",
 ]
 
@@ -120,7 +120,7 @@ EXPORTED = ["bt_version", "bt_status_string", "bt_packed_row_bytes", "bt_pack_si
             "bt_binary_linear_workspace", "bt_binary_linear", "bt_binary_conv2d_workspace",
             "bt_binary_conv2d", "bt_plan", "bt_device_status", "bt_binary_linear_noalloc",
             "bt_binary_linear_noalloc_max_bytes", "bt_pack_im2col", "bt_conv2d_single_pass", "bt_tune_linear",
-            "bt_tune_reset", "bt_tune_conv2d",
+            "bt_tune_reset", "bt_tune_conv2d", "bt_conv2d_plan_info",
             "bt_backward_weight_ld", "bt_sign_transpose", "bt_binary_linear_backward_workspace",
             "bt_binary_linear_backward", "bt_binary_conv2d_backward_workspace", "bt_conv2d_backward_implicit",
             "bt_binary_conv2d_backward",
@@ -603,6 +603,28 @@ def bt_tune_conv2d(x: torch.Tensor, weight: torch.Tensor, w_code: int, C: int, k
                         scale_a, scale_w, _ptr(bias_a), blen, _ptr(out), ot, _ptr(ws), 0 if ws is None else ws.numel(),
                         reps, _stream(stream), ctypes.byref(res)))
     return {f: getattr(res, f) for f, _ in TuneConvResult._fields_}
+
+
+class ConvPlanInfo(ctypes.Structure):
+    """bt_conv_plan_info: the tiling of the implicit-im2col convolution."""
+    _fields_ = [(n, _i) for n in ("implicit", "pair", "weights_resident", "pixel_stages", "bands", "band_rows",
+                                  "cta_rows", "row_width", "tile_n", "cta_n", "staged_rows", "phases",
+                                  "max_tap_shift", "tiles", "smem_bytes")]
+
+
+_c_plan_info = _sig("bt_conv2d_plan_info", _i, [_i64, _i64, _i64, _i64, _i64, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                               ctypes.POINTER(ConvPlanInfo)])
+
+
+def bt_conv2d_plan_info(B: int, C: int, H: int, W: int, O: int, kernel_size: int, stride: int, padding: int,
+                        dilation: int, code: int, out_dtype=torch.float32, sms: int = 152, pair: int = -1,
+                        split: int = 1) -> dict:
+    """The tiling the implicit-im2col convolution takes for this geometry
+    (host only): the bt_conv_plan_info fields as a dict."""
+    info = ConvPlanInfo()
+    _check(_c_plan_info(B, C, H, W, O, kernel_size, stride, padding, dilation, code, _DT[out_dtype], sms, pair,
+                        split, ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in ConvPlanInfo._fields_}
 
 
 def bt_tune_reset() -> None:

@@ -740,6 +740,26 @@ bt_status bt_tune_conv2d(const void *x, bt_dtype x_dtype, const void *weight, bt
     return BT_OK;
 }
 
+bt_status bt_conv2d_plan_info(int64_t B, int64_t C, int64_t H, int64_t W, int64_t O, int kernel_size, int stride,
+                              int padding, int dilation, bt_code code, bt_dtype out_dtype, int sms, int pair, int split,
+                              bt_conv_plan_info *info) {
+    if (info == nullptr) return BT_ERR_INVALID_ARG;
+    *info = bt_conv_plan_info{};
+    if ((code != BT_CODE_E4M3 && code != BT_CODE_E2M1) || !valid_out(out_dtype)) return BT_ERR_INVALID_ARG;
+    if (B < 1 || C < 1 || H < 1 || W < 1 || O < 1 || kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1)
+        return BT_ERR_INVALID_ARG;
+    if (sms < 1 || pair < -1 || pair > 1 || split < 1) return BT_ERR_INVALID_ARG;
+    if (B > (int64_t(1) << 30) || C > kMaxK || H > (1 << 20) || W > (1 << 20) || kernel_size > 64 ||
+        padding > (1 << 20) || stride > (1 << 20) || dilation > (1 << 10))
+        return BT_ERR_INVALID_ARG;
+    ConvGeom g{B, C, H, W, O, 0, 0, kernel_size, stride, padding, dilation};
+    g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
+    g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
+    if (g.Ho < 1 || g.Wo < 1) return BT_ERR_INVALID_ARG;
+    conv_plan_query(g, code, out_dtype == BT_BF16 || out_dtype == BT_F16 ? 2 : 4, sms, pair, split, *info);
+    return BT_OK;
+}
+
 void bt_tune_reset(void) {
     tc_linear_forget();
     conv_forget();

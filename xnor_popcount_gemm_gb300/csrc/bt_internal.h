@@ -277,6 +277,11 @@ void conv_remember(const ConvGeom &g, bt_code code, bt_dtype out_t, const ConvCh
 bool conv_lookup(const ConvGeom &g, bt_code code, bt_dtype out_t, ConvChoice &c);
 bool conv_kept_fused(const ConvGeom &g, bt_code code, bool &fused);
 void conv_forget();
+// The tiling a convolution launch would take (host only, no CUDA call): sms
+// SMs, pair -1 (the planner's choice), 0 or 1, split >= 1 times the bands.
+// False where the implicit plan does not apply.
+bool conv_plan_query(const ConvGeom &g, bt_code code, int out_elem, int sms, int pair, int split,
+                     bt_conv_plan_info &info);
 
 // First-call activation scale (BinaryConv2dCutlass.set_activation): the sum
 // of |x| accumulates in a double per CUDA context (zero it before use; calls
