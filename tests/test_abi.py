@@ -269,6 +269,12 @@ def test_tune_abi_validation():
     conv = (None, bt.BT_F32, None, bt.BT_CODE_E2M1, 0, 64, 14, 14, 64, 3, 1, 1, 1, 1.0, 1.0, None, 0, None,
             bt.BT_F32)
     assert C(*conv, bt.BT_ALGO_TUNE, None, 0, None) == bt.BT_OK                     # zero images: a no-op
+    # C far past any limit: refused before any size product is formed
+    huge = (None, bt.BT_F32, None, bt.BT_CODE_E2M1, 2, 1 << 62, 14, 14, 64, 3, 1, 1, 1, 1.0, 1.0, None, 0, None,
+            bt.BT_F32)
+    for algo in (bt.BT_ALGO_AUTO, bt.BT_ALGO_TUNE):
+        assert C(*huge, algo, None, 0, None) == bt.BT_ERR_UNSUPPORTED
+    assert bt.bt_conv2d_single_pass(2, 1 << 62, 14, 14, 3, 1, 1, 1, bt.BT_F32, bt.BT_CODE_E2M1) == 0
     LD = bt._c_lin_ds
     assert LD(None, bt.BT_F32, None, bt.BT_CODE_E2M1, 0, 8, 8, 256, None, 0, None, bt.BT_F32, bt.BT_ALGO_TUNE,
               None, 0, None) == bt.BT_ERR_INVALID_ARG

@@ -315,7 +315,7 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
     g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
     if (g.Ho < 1 || g.Wo < 1) return BT_ERR_INVALID_ARG;
     const int64_t kk = static_cast<int64_t>(kernel_size) * kernel_size;
-    if (C * kk > kMaxK || H > (1 << 20) || W > (1 << 20) || kernel_size > 64 || padding > (1 << 20) ||
+    if (C > kMaxK || kernel_size > 64 || C * kk > kMaxK || H > (1 << 20) || W > (1 << 20) || padding > (1 << 20) ||
         stride > (1 << 20) || dilation > (1 << 10))
         return BT_ERR_UNSUPPORTED;
     if (B == 0 || O == 0) return BT_OK;
@@ -414,7 +414,7 @@ bt_status bt_binary_conv2d(const void *x, bt_dtype x_dtype, const void *weight, 
         // (the last timed call leaves this call's result in out)
         if ((w_code == BT_CODE_E4M3 || w_code == BT_CODE_E2M1) && x_dtype != BT_PACKED_IM2COL && valid_out(out_dtype) &&
             B >= 1 && C >= 1 && H >= 1 && W >= 1 && O >= 1 && kernel_size >= 1 && kernel_size <= 64 &&
-            stride >= 1 && padding >= 0 && dilation >= 1 && H <= (1 << 20) && W <= (1 << 20) &&
+            stride >= 1 && padding >= 0 && dilation >= 1 && H <= (1 << 20) && W <= (1 << 20) && C <= kTcMaxK &&
             C * kernel_size * kernel_size <= kTcMaxK) {
             ConvGeom g{B, C, H, W, O, 0, 0, kernel_size, stride, padding, dilation};
             g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
@@ -493,7 +493,7 @@ int bt_conv2d_single_pass(int64_t B, int64_t C, int64_t H, int64_t W, int kernel
     if (!float_in(x_dtype) || (code != BT_CODE_E4M3 && code != BT_CODE_E2M1)) return 0;
     if (B < 1 || C < 1 || H < 1 || W < 1 || kernel_size < 1 || stride < 1 || padding < 0 || dilation < 1) return 0;
     if (H > (1 << 20) || W > (1 << 20) || kernel_size > 64 || padding > (1 << 20) || stride > (1 << 20) ||
-        dilation > (1 << 10) || C * kernel_size * kernel_size > kTcMaxK)
+        dilation > (1 << 10) || C > kTcMaxK || C * kernel_size * kernel_size > kTcMaxK)
         return 0;
     ConvGeom g{B, C, H, W, 0, 0, 0, kernel_size, stride, padding, dilation};
     g.Ho = conv_out(H, kernel_size, stride, padding, dilation);
@@ -527,7 +527,7 @@ bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, 
     g.Wo = conv_out(W, kernel_size, stride, padding, dilation);
     if (g.Ho < 1 || g.Wo < 1) return BT_ERR_INVALID_ARG;
     const int64_t kk = static_cast<int64_t>(kernel_size) * kernel_size;
-    if (C * kk > kTcMaxK || H > (1 << 20) || W > (1 << 20) || kernel_size > 64 || padding > (1 << 20) ||
+    if (C > kTcMaxK || kernel_size > 64 || C * kk > kTcMaxK || H > (1 << 20) || W > (1 << 20) || padding > (1 << 20) ||
         stride > (1 << 20) || dilation > (1 << 10))
         return BT_ERR_UNSUPPORTED;
     if (B == 0) return BT_OK;
