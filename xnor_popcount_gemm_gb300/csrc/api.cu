@@ -178,7 +178,7 @@ bt_status linear_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_co
     if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16)) return BT_ERR_ALIGNMENT;
     if (scales != nullptr && !aligned(scales, 8)) return BT_ERR_ALIGNMENT;
-    if ((M + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
+    if (M > int64_t(65535) * 128) return BT_ERR_UNSUPPORTED;              // at most 65535 row tiles of 128
     const bt_algo run = algo_for_code(w_code);
     if (run != BT_ALGO_POPC && K > kTcMaxK) return BT_ERR_UNSUPPORTED;
 
@@ -322,8 +322,10 @@ bt_status conv_impl(const void *x, bt_dtype x_dtype, const void *weight, bt_code
     if (x == nullptr || weight == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(out, 16)) return BT_ERR_ALIGNMENT;
     if (scales != nullptr && !aligned(scales, 8)) return BT_ERR_ALIGNMENT;
+    // at most 65535 pixel tiles of 128 (each factor bounded first, so the product stays in range)
+    if (B > int64_t(65535) * 128 || g.Ho * g.Wo > int64_t(65535) * 128) return BT_ERR_UNSUPPORTED;
     const int64_t M = B * g.Ho * g.Wo;
-    if ((M + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
+    if (M > int64_t(65535) * 128) return BT_ERR_UNSUPPORTED;
     const bt_algo run = algo_for_code(w_code);
     if (run != BT_ALGO_POPC && C * kk > kTcMaxK) return BT_ERR_UNSUPPORTED;
     // the plan bt_tune_conv2d kept for this geometry, unless one is forced already
@@ -531,7 +533,8 @@ bt_status bt_pack_im2col(const void *x, bt_dtype x_dtype, int64_t B, int64_t C, 
         stride > (1 << 20) || dilation > (1 << 10))
         return BT_ERR_UNSUPPORTED;
     if (B == 0) return BT_OK;
-    if ((B * g.Ho * g.Wo + 127) / 128 > 65535) return BT_ERR_UNSUPPORTED;
+    if (B > int64_t(65535) * 128 || g.Ho * g.Wo > int64_t(65535) * 128 || B * g.Ho * g.Wo > int64_t(65535) * 128)
+        return BT_ERR_UNSUPPORTED;
     if (x == nullptr || out == nullptr) return BT_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4))) return BT_ERR_ALIGNMENT;
     return from_cuda(launch_pack_im2col(x, x_dtype, g, bias, bias_len, code, static_cast<uint8_t *>(out), true,
